@@ -1,0 +1,220 @@
+/*
+ * verkv.h -- C ABI of libverkv.so: KVFetch verified attention over a
+ * PoissonComp-compressed KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow "Verify Before You Fetch: Reliable KV Cache
+ * Compression for LLM Inference":
+ *   verkv_compress  -- PoissonComp, Algorithm 1 (Sec. 4.1, eq. (3)), plus the
+ *                      token-level key sketch of Appendix A.1.
+ *   verkv_decode    -- KVFetch, Algorithm 2 (Sec. 4.2: Definition 2 / eq. (5),
+ *                      Lemma 1 / eq. (7), eqs. (9)-(10), Theorem 2), followed by
+ *                      the weighted attention named in the comment closing
+ *                      Algorithm 2.
+ *
+ * Conventions
+ *   - Every entry point returns a verkv_status; nothing is thrown across the
+ *     ABI.  On any status other than VERKV_OK, verkv_last_error(ctx) holds a
+ *     one-line message.  Asynchronous CUDA faults surface as VERKV_ECUDA at
+ *     the next call that synchronises.
+ *   - "device" pointers are CUDA device (or managed) memory of the GPU that was
+ *     current when the context was created; "host" pointers are CPU memory.
+ *     "pinned" means page-locked (cudaHostAlloc / cudaHostRegister) memory the
+ *     GPU can read over the host link.
+ *   - A verkv_stream is a cudaStream_t (NULL = the legacy default stream).
+ *     Work is enqueued on that stream; one context is driven from one host
+ *     thread at a time and has no internal threads.
+ *   - The context owns all device memory it allocates.  Caller buffers are
+ *     borrowed for the duration of a call, except `kv_host` of
+ *     verkv_compress, which is borrowed until verkv_release of that slot.
+ *   - Layouts are row-major.  K/V rows of one token and one KV head are stored
+ *     K then V: [n_kv_heads][n][2][head_dim] in the element type `kv_dtype`.
+ */
+#ifndef VERKV_H
+#define VERKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct verkv_ctx verkv_ctx;
+typedef void* verkv_stream;
+
+typedef enum {
+    VERKV_OK = 0,
+    VERKV_EINVAL = 1,        /* bad argument or shape */
+    VERKV_ENOMEM = 2,        /* device or pinned allocation failed */
+    VERKV_ECUDA = 3,         /* a CUDA call or kernel failed */
+    VERKV_ETIMEOUT = 4,      /* a bounded device-side wait gave up */
+    VERKV_EUNSUPPORTED = 5,  /* configuration not built (e.g. head_dim != 128) */
+    VERKV_ESTATE = 6         /* call out of order (e.g. decode before compress) */
+} verkv_status;
+
+typedef enum {
+    VERKV_SKETCH_EXACT = 0,  /* the "perfect sketch": sketch weights = exact weights */
+    VERKV_SKETCH_INT8 = 1,   /* per-token symmetric int8 keys with an fp32 scale */
+    VERKV_SKETCH_2BIT = 2    /* Appendix A.1: d/8 rotate-half channel pairs, 2-bit, fp16 zero/scale per group */
+} verkv_sketch;
+
+typedef enum {
+    VERKV_DTYPE_BF16 = 0,
+    VERKV_DTYPE_F32 = 1
+} verkv_dtype;
+
+typedef struct {
+    int32_t n_layers;      /* number of layer slots                                   */
+    int32_t n_seqs;        /* number of sequence slots per layer                      */
+    int32_t max_batch;     /* largest B passed to verkv_decode                         */
+    int32_t n_kv_heads;    /* KV heads                                                */
+    int32_t n_q_heads;     /* query heads, a multiple of n_kv_heads (GQA group <= 8)  */
+    int32_t head_dim;      /* 128 (the only head dimension built)                     */
+    int32_t max_tokens;    /* upper bound on n per slot                               */
+    int32_t n_sink;        /* first tokens always kept (forced into H)                */
+    int32_t n_local;       /* last tokens always kept (forced into H)                 */
+    int32_t sketch_group;  /* 2-bit sketch: tokens per min/max group (128)            */
+    int32_t topk_width;    /* per query row, gain candidates sorted on chip (4096)    */
+    int32_t pad0;
+    double eta;            /* kept fraction: expected |H u S| = eta * n (Alg. 1)      */
+    uint64_t seed;         /* Philox4x32-10 key of the Poisson sample                 */
+    verkv_sketch sketch;
+    verkv_dtype kv_dtype;  /* element type of K and V                                 */
+} verkv_config;
+
+/* Per KV head, filled by verkv_compress (host memory, valid on return). */
+typedef struct {
+    double c;              /* water-filling constant of eq. (3); +inf if every token is kept */
+    int32_t n_capped;      /* tokens outside the sink/local windows with r = 1                */
+    int32_t n_h;           /* |H| (r = 1, sink and local included)                           */
+    int32_t n_l;           /* |L| (0 < r < 1)                                                 */
+    int32_t n_s;           /* |S|, the sampled part of L                                      */
+    int32_t n_resident;    /* |H| + |S| rows kept on the GPU                                  */
+    int32_t pad;
+} verkv_head_stats;
+
+/* Per query row (sequence b, query head h) of the last verkv_decode. */
+typedef struct {
+    double m;              /* logit shift used for the weights                                */
+    double D;              /* certificate denominator: sum_H w_i + sum_L w^_i                  */
+    double beta;           /* fixed point of Definition 2 (in units of exp(-m))               */
+    double sum_a;          /* beta(L) of eq. (7) = sum_L w^_i (1 - lambda_i)                  */
+    double V;              /* V(L) of eq. (7)                                                 */
+    double b;              /* b(L) of eq. (7)                                                 */
+    double eps_hat;        /* eq. (7) on the whole of L                                       */
+    int32_t n_l;           /* |L|                                                             */
+    int32_t kstar;         /* eq. (10); 0 when no fetch is needed                              */
+    int32_t no_fetch;      /* eps_hat < eps (Algorithm 2, line 3)                              */
+    int32_t fallback;      /* k* was beyond the on-chip candidate width: full-row path used   */
+    int32_t n_fetch;       /* |L_g[:k*] \ S|, tokens of this row read from the host            */
+    int32_t pad;
+} verkv_row_trace;
+
+/* Create a context for one GPU (the current device).  All slots empty.
+ * EINVAL: bad sizes, n_q_heads not a multiple of n_kv_heads, eta outside
+ * (0, 1]; EUNSUPPORTED: head_dim != 128 or GQA group > 8. */
+verkv_status verkv_create(const verkv_config* cfg, verkv_ctx** out);
+
+/* Free all device memory of the context.  Pending work on the streams the
+ * context was used with must be finished by the caller. */
+verkv_status verkv_destroy(verkv_ctx* ctx);
+
+/*
+ * PoissonComp (Algorithm 1) for one (layer, sequence) slot.
+ *   n_tokens  context length n, n_sink + n_local <= n <= max_tokens.
+ *   kv_host   pinned host [n_kv_heads][n][2][head_dim] kv_dtype: the offloaded
+ *             full cache.  Borrowed until verkv_release(layer, seq); decode
+ *             reads fetched rows from it.
+ *   kv_dev    optional device copy with the same layout (what prefill leaves
+ *             on the GPU).  NULL: compression reads kv_host over the host link.
+ *   obs_q     device [n_q_heads][W][head_dim] fp32 observation queries for the
+ *             synthetic importance score (Algorithm 1, line 1: per token, the
+ *             largest softmax weight any observation query of the KV head's
+ *             group gives it, divided by its maximum over tokens); or NULL.
+ *   tau       device [n_kv_heads][n] fp32 importance scores supplied by the
+ *             caller (any scorer C), used when obs_q is NULL.  Scores are
+ *             clamped to [2^-38, 1]; sink and local tokens get 1.
+ *   stats     optional host [n_kv_heads] output.
+ * Computes tau, the water-filling constant c with sum_i min(1, c tau_i) =
+ * eta n (eq. (3)), r_i = min(1, c tau_i) (stored as fp32; H = {r = 1}), the
+ * Poisson sample Z_i = [u_i < r_i] with u_i the top 24 bits of word 0 of
+ * Philox4x32-10 at key `seed` and counter (token, kv_head, layer, seq),
+ * compacts K/V rows of H u S into device memory (ascending token order) and
+ * builds the key sketch.  Synchronises `stream` before returning (the
+ * resident sizes decide allocations).  Replaces any previous state of the slot.
+ * EINVAL: eta n <= n_sink + n_local, sizes out of range, both obs_q and tau NULL.
+ */
+verkv_status verkv_compress(verkv_ctx* ctx, int32_t layer, int32_t seq, int32_t n_tokens, const void* kv_host,
+                            const void* kv_dev, const float* obs_q, int32_t W, const float* tau,
+                            verkv_stream stream, verkv_head_stats* stats);
+
+/*
+ * KVFetch (Algorithm 2) and the final attention for B query rows sets.
+ *   layer     layer slot.
+ *   seq_ids   host [B] sequence slots (each compressed in this layer).
+ *   q         device [B][n_q_heads][head_dim] fp32 queries.
+ *   eps       tolerance eps >= 0 on the relative error of the denominator.
+ *   delta     failure probability, 0 < delta < 1.
+ *   out       device [B][n_q_heads][head_dim] fp32 attention outputs.
+ * Per query row: sketch weights w^_i = exp(<q, k^_i>/sqrt(d) - m) on L and
+ * exact weights on H; the fixed point beta of Definition 2; the certificate
+ * eps^(L) of eq. (7) with D = sum_H w_i + sum_L w^_i; if eps^(L) >= eps, the
+ * gains g_i = eps^(L) - eps^(L \ {i}) (eq. (9)), the order L_g (descending,
+ * ties by token index) and k* of eq. (10); the rows of L_g[:k*] \ S of every
+ * query head of a KV head are fetched once (their union) from kv_host; the
+ * output is o = N^/D^ with weight 1 on H and on L_g[:k*] and lambda_i / r_i
+ * on the rest of S.  Asynchronous on `stream`: no host synchronisation.
+ * EINVAL: bad eps/delta/B; ESTATE: a slot was not compressed.
+ */
+verkv_status verkv_decode(verkv_ctx* ctx, int32_t layer, const int32_t* seq_ids, int32_t B, const float* q,
+                          double eps, double delta, float* out, verkv_stream stream);
+
+/* Drop the compressed state of a slot and end the borrow of its kv_host. */
+verkv_status verkv_release(verkv_ctx* ctx, int32_t layer, int32_t seq);
+
+/*
+ * Inspection (copies to caller host buffers; synchronises `stream`).
+ * verkv_get_compress_state: for KV head `kv_head` of slot (layer, seq):
+ *   c (may be NULL), tau [n] fp32 (NULL to skip), r [n] fp32, flags [n]
+ *   (2 = H, 1 = S, 0 = L \ S).  Any array pointer may be NULL.
+ */
+verkv_status verkv_get_compress_state(verkv_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, double* c,
+                                      float* tau, float* r, uint8_t* flags, verkv_stream stream);
+
+/* Sketch of one KV head, in the layout the decode reads:
+ *   INT8:  codes [n][head_dim] int8, scale [n] fp32.
+ *   2BIT:  pairs [head_dim/8] int32, codes [n][head_dim/4] (one 2-bit code per
+ *          byte, unpacked for inspection), zero and scale
+ *          [ceil(n/group)][head_dim/4] fp16 bit patterns.
+ *   EXACT: nothing (returns EINVAL). */
+verkv_status verkv_get_sketch(verkv_ctx* ctx, int32_t layer, int32_t seq, int32_t kv_head, int8_t* codes_i8,
+                              float* scale_f32, int32_t* pairs, uint8_t* codes_2bit, uint16_t* zero_f16,
+                              uint16_t* scale_f16, verkv_stream stream);
+
+/* Traces of the last verkv_decode: rows [B * n_q_heads] (row = b * n_q_heads + h). */
+verkv_status verkv_get_decode_trace(verkv_ctx* ctx, verkv_row_trace* rows, int32_t n_rows, verkv_stream stream);
+
+/* Tokens made exact for query row (b, h) in the last decode, L_g[:k*] (as a
+ * set, ascending), and the union of fetched rows of KV head (b, kv_head).
+ * `count` receives the size; at most `cap` tokens are written. */
+verkv_status verkv_get_exact_set(verkv_ctx* ctx, int32_t b, int32_t h, int32_t* tokens, int32_t cap,
+                                 int32_t* count, verkv_stream stream);
+verkv_status verkv_get_fetch_set(verkv_ctx* ctx, int32_t b, int32_t kv_head, int32_t* tokens, int32_t cap,
+                                 int32_t* count, verkv_stream stream);
+
+/* Sketch weights w^_i (fp32, in units of exp(-m)) of row (b, h) over L in
+ * ascending token order, and those tokens. */
+verkv_status verkv_get_row_weights(verkv_ctx* ctx, int32_t b, int32_t h, float* w_hat, int32_t* tokens,
+                                   int32_t cap, int32_t* count, verkv_stream stream);
+
+/* Number of kernels the last verkv_decode / verkv_compress enqueued. */
+int32_t verkv_last_launch_count(const verkv_ctx* ctx);
+
+const char* verkv_status_str(verkv_status s);
+const char* verkv_last_error(const verkv_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERKV_H */

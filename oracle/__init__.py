@@ -76,7 +76,7 @@ def lib():
             L.vko_logits_2bit.argtypes = [i64, i32, P, P, P, P, P, i32, P]
             L.vko_beta_breakpoints.argtypes = [i64, P, P]
             L.vko_beta_breakpoints.restype = f64
-            L.vko_kvfetch_row.argtypes = [i64, P, P, P, P, f64, f64, i32, P, P, P, P, P]
+            L.vko_kvfetch_row.argtypes = [i64, P, P, P, P, f64, f64, i32, P, P, P, P, P, P]
             L.vko_kvfetch_row.restype = i32
             L.vko_attention_row.argtypes = [i64, i32, P, P, P, P, P, P, P]
             L.vko_kvfetch_rows.argtypes = [i64, i64, P, P, P, P, P, f64, f64, i32, P, P, i32]
@@ -224,10 +224,11 @@ def kvfetch_row(flags, r32, t_exact, t_sketch, eps: float, delta: float, mode: i
     n_l = int((flags != 2).sum())
     order = np.zeros(max(n_l, 1), np.int64)
     mask = np.zeros(n, np.uint8)
+    resid = np.full(n_l + 1, np.nan)
     lib().vko_kvfetch_row(n, _p(flags), _p(r32), _p(te), _p(ts), float(eps), float(delta), int(mode),
-                          ctypes.byref(cert), _p(lam), _p(gain), _p(order), _p(mask))
+                          ctypes.byref(cert), _p(lam), _p(gain), _p(order), _p(mask), _p(resid))
     out = cert.as_dict()
-    out.update(lam=lam, gain=gain, order=order[:n_l], exact_mask=mask.astype(bool))
+    out.update(lam=lam, gain=gain, order=order[:n_l], exact_mask=mask.astype(bool), resid=resid)
     return out
 
 

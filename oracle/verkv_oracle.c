@@ -496,11 +496,12 @@ static int cmp_gain(const void* a, const void* b)
  *   gain[n]               : g_i on L when the row fetches (0 elsewhere).
  *   order[|L|]            : L sorted by gain descending, ties by token index.
  *   exact_mask[n]         : 1 for the tokens of L_g[:k*] (made exact).
+ *   resid[|L| + 1]        : eps^(L_g[k:]) for k = 0..|L| (from tail sums; for diagnostics).
  * Returns 0.
  */
 int vko_kvfetch_row(int64_t n, const uint8_t* flags, const float* r32, const double* t_exact,
                     const double* t_sketch, double eps, double delta, int mode, vko_cert* cert,
-                    double* lambda, double* gain, int64_t* order, uint8_t* exact_mask)
+                    double* lambda, double* gain, int64_t* order, uint8_t* exact_mask, double* resid)
 {
     int64_t nl = 0;
     double m = -INFINITY;
@@ -617,6 +618,17 @@ int vko_kvfetch_row(int64_t n, const uint8_t* flags, const float* r32, const dou
                 if (cert_from_sums(ts[kstar], tv[kstar], tb[kstar], ldelta, D) < eps) break;
             free(ts); free(tv); free(tb);
         }
+        if (resid) {
+            double s1 = 0.0, s2 = 0.0, b1 = 0.0;
+            resid[nl] = 0.0;
+            for (int64_t p = nl - 1; p >= 0; --p) {
+                int64_t j = ord[p];
+                s1 += a[j];
+                s2 += v[j];
+                if (bb[j] > b1) b1 = bb[j];
+                resid[p] = cert_from_sums(s1, s2, b1, ldelta, D);
+            }
+        }
         if (gain) for (int64_t j = 0; j < nl; ++j) gain[lidx[j]] = g[j];
         if (exact_mask) for (int64_t p = 0; p < kstar; ++p) exact_mask[lidx[ord[p]]] = 1;
         free(g);
@@ -674,7 +686,7 @@ int vko_kvfetch_rows(int64_t rows, int64_t n, const uint8_t* flags, const float*
     for (int64_t u = 0; u < rows; ++u) {
         const int64_t kv = kv_of[u];
         vko_kvfetch_row(n, flags + kv * n, r32 + kv * n, t_exact + u * n, t_sketch + u * n, eps, delta, mode,
-                        certs + u, NULL, NULL, NULL, exact_masks ? exact_masks + u * n : NULL);
+                        certs + u, NULL, NULL, NULL, exact_masks ? exact_masks + u * n : NULL, NULL);
     }
     return 0;
 }

@@ -1,0 +1,179 @@
+"""Shared drivers for the parity tests: run one workload through the CUDA library (via the C ABI)
+and through the oracle, from the same seeded inputs.  Nothing computed by the CUDA path is ever fed
+to the oracle."""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+import oracle
+from verified_kv_cache_gb300 import workloads
+
+G_GAP = 1e-6      # fetched-set exemption: oracle gains closer than this (relative) at the k* boundary
+K_GAP = 1e-6      # k* exemption: residual certificate within this (relative) of eps
+REL_SCALAR = 1e-4 # c, beta, eps_hat
+REL_OUT = 2e-3    # attention output, relative L2
+
+
+# ----------------------------------------------------------------------------- oracle side
+@dataclass
+class OracleSlot:
+    tau: np.ndarray          # [Hkv, n] fp32
+    c: np.ndarray            # [Hkv]
+    r32: np.ndarray          # [Hkv, n]
+    r64: np.ndarray
+    flags: np.ndarray        # [Hkv, n]
+    sketch: dict = field(default_factory=dict)
+
+
+def oracle_tau(w: workloads.Workload, b: int) -> np.ndarray:
+    G, W = w.group, w.obs_q.shape[2]
+    out = np.zeros((w.n_kv, w.n), np.float32)
+    for h in range(w.n_kv):
+        Q = w.obs_q[b, h * G:(h + 1) * G].reshape(G * W, w.d)
+        out[h] = oracle.tau(w.K[b, h], Q, w.n_sink, w.n_local)
+    return out
+
+
+def oracle_compress(w: workloads.Workload, b: int, tau: np.ndarray, layer: int = 0, seq: int = 0,
+                    seed: int | None = None) -> OracleSlot:
+    seed = w.seed if seed is None else seed
+    Hkv, n = w.n_kv, w.n
+    c = np.zeros(Hkv)
+    r32 = np.zeros((Hkv, n), np.float32)
+    r64 = np.zeros((Hkv, n))
+    flags = np.zeros((Hkv, n), np.uint8)
+    sk = {}
+    for h in range(Hkv):
+        c[h], _, r64[h], r32[h] = oracle.waterfill(tau[h], w.n_sink, w.n_local, w.eta * n)
+        flags[h] = oracle.poisson_sample(r32[h], seed, h, layer, seq)
+        if w.sketch == "int8":
+            sk[h] = oracle.sketch_int8(w.K[b, h])
+        elif w.sketch == "2bit":
+            sk[h] = oracle.sketch_2bit(w.K[b, h])
+    return OracleSlot(tau, c, r32, r64, flags, sk)
+
+
+def oracle_sketch_logits(w, b, h, q, slot: OracleSlot):
+    if w.sketch == "exact":
+        return oracle.logits_exact(q, w.K[b, h])
+    if w.sketch == "int8":
+        codes, scale = slot.sketch[h]
+        return oracle.logits_int8(q, codes, scale)
+    pairs, codes, zero, scale = slot.sketch[h]
+    return oracle.logits_2bit(q, pairs, codes, zero, scale)
+
+
+def oracle_decode(w, b, slot: OracleSlot, q_bh: np.ndarray, eps, delta, mode=1):
+    """q_bh: [Hq, d] for sequence b.  Returns per row dicts and per KV head fetch unions and outputs."""
+    G = w.group
+    rows = []
+    for hq in range(w.n_q):
+        h = hq // G
+        q = q_bh[hq].astype(np.float64)
+        te = oracle.logits_exact(q, w.K[b, h])
+        ts = oracle_sketch_logits(w, b, h, q, slot)
+        res = oracle.kvfetch_row(slot.flags[h], slot.r32[h], te, ts, eps, delta, mode=mode)
+        res["out"] = oracle.attention_row(slot.flags[h], slot.r32[h], te, w.V[b, h], res["lam"], res["exact_mask"])
+        rows.append(res)
+    unions = []
+    for h in range(w.n_kv):
+        u = np.zeros(w.n, bool)
+        for g in range(G):
+            u |= rows[h * G + g]["exact_mask"] & (slot.flags[h] == 0)
+        unions.append(np.nonzero(u)[0])
+    return rows, unions
+
+
+# ----------------------------------------------------------------------------- CUDA side
+class GpuCase:
+    """Holds the device/pinned buffers of one workload for the library."""
+
+    def __init__(self, w: workloads.Workload, lib_ctx, layers=1):
+        import torch
+        self.w = w
+        self.ctx = lib_ctx
+        self.kv_host = []
+        self.kv_dev = []
+        self.obs = []
+        for b in range(w.batch):
+            arr = w.kv_host_layout(b)
+            t = torch.from_numpy(arr)
+            if w.kv_dtype == "bf16":
+                t = t.view(torch.bfloat16)
+            pinned = t.pin_memory()
+            self.kv_host.append(pinned)
+            self.kv_dev.append(pinned.to("cuda"))
+            self.obs.append(torch.from_numpy(np.ascontiguousarray(w.obs_q[b])).to("cuda"))
+
+    def compress(self, b, layer=0, seq=None, tau=None, use_dev=True):
+        import torch
+        seq = b if seq is None else seq
+        tau_t = None
+        if tau is not None:
+            tau_t = torch.from_numpy(np.ascontiguousarray(tau, np.float32)).to("cuda")
+        stats = self.ctx.compress(layer, seq, self.w.n, self.kv_host[b], self.kv_dev[b] if use_dev else None,
+                                  None if tau is not None else self.obs[b], self.w.obs_q.shape[2], tau_t)
+        torch.cuda.synchronize()
+        return stats
+
+    def decode(self, q_step: np.ndarray, eps, delta, layer=0, seq_ids=None):
+        import torch
+        B = q_step.shape[0]
+        seq_ids = list(range(B)) if seq_ids is None else seq_ids
+        q = torch.from_numpy(np.ascontiguousarray(q_step, np.float32)).to("cuda")
+        out = torch.empty_like(q)
+        self.ctx.decode(layer, seq_ids, q, eps, delta, out)
+        torch.cuda.synchronize()
+        return out.cpu().numpy()
+
+
+def make_lib_ctx(w, n_layers=1, n_seqs=None, max_batch=None, max_tokens=None):
+    from verified_kv_cache_gb300 import binding
+    return binding.VerKV(n_kv_heads=w.n_kv, n_q_heads=w.n_q, max_tokens=max_tokens or w.n, head_dim=w.d,
+                         n_layers=n_layers, n_seqs=n_seqs or w.batch, max_batch=max_batch or w.batch,
+                         n_sink=w.n_sink, n_local=w.n_local, eta=w.eta, seed=w.seed, sketch=w.sketch,
+                         kv_dtype=w.kv_dtype)
+
+
+# ----------------------------------------------------------------------------- comparisons
+def rel(a, b):
+    return abs(a - b) / max(abs(b), 1e-300)
+
+
+def check_row(gpu_trace, gpu_set, orow, eps, flags_h):
+    """Compare one query row.  Returns 'ok', 'exempt-k' or 'exempt-g'; raises on a real mismatch."""
+    assert rel(gpu_trace["eps_hat"], orow["eps_hat"]) <= REL_SCALAR, (gpu_trace["eps_hat"], orow["eps_hat"])
+    assert rel(gpu_trace["beta"] / gpu_trace["D"], orow["beta"] / orow["D"]) <= REL_SCALAR
+    nf_o = bool(orow["no_fetch"])
+    if bool(gpu_trace["no_fetch"]) != nf_o:
+        assert abs(orow["eps_hat"] - eps) <= K_GAP * eps, ("no-fetch decision differs", gpu_trace, orow["eps_hat"])
+        return "exempt-k"
+    if nf_o:
+        assert gpu_trace["kstar"] == 0 and len(gpu_set) == 0
+        return "ok"
+    o_set = np.nonzero(orow["exact_mask"])[0]
+    k_o, k_g = int(orow["kstar"]), int(gpu_trace["kstar"])
+    if k_o != k_g:
+        lo, hi = min(k_o, k_g), max(k_o, k_g)
+        resid = orow["resid"]
+        # every residual certificate between the two answers must sit within K_GAP of eps
+        band = resid[lo:hi]
+        assert np.all(np.abs(band - eps) <= K_GAP * eps), ("k* differs", k_o, k_g, band, eps)
+        return "exempt-k"
+    if np.array_equal(np.sort(gpu_set), o_set):
+        return "ok"
+    diff = np.setxor1d(gpu_set, o_set)
+    g = orow["gain"]
+    order = orow["order"]
+    g_in = g[order[k_o - 1]]
+    g_out = g[order[k_o]] if k_o < len(order) else 0.0
+    assert g_in - g_out <= G_GAP * g_in, ("fetched set differs beyond the gain-gap exemption", diff[:10], g_in, g_out)
+    assert np.all(np.abs(g[diff] - g_in) <= G_GAP * g_in), ("set difference outside the boundary band", diff[:10])
+    return "exempt-g"
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))

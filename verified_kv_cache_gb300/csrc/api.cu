@@ -1,0 +1,364 @@
+// C ABI of libverkv.so (declared in include/verkv.h): argument checks, slot bookkeeping, the
+// decode workspace and the inspection getters.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace verkv {
+int decode_max_batch();
+int decode_sel_width();
+}  // namespace verkv
+
+using namespace verkv;
+
+struct verkv_ctx {
+    Ctx c;
+};
+
+namespace {
+
+verkv_status fail(Ctx& ctx, verkv_status s, const char* msg)
+{
+    ctx.err = msg;
+    return s;
+}
+
+void free_ws(Ctx& c)
+{
+    void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ubits, c.ulist, c.ucount, c.staging, c.part,
+                    c.d_slot_n};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+}
+
+verkv_status alloc_ws(Ctx& ctx)
+{
+    const verkv_config& cfg = ctx.cfg;
+    const size_t rows = (size_t)cfg.max_batch * cfg.n_q_heads;
+    const size_t n = (size_t)cfg.max_tokens;
+    int p2 = 1;
+    while (p2 < cfg.max_tokens) p2 <<= 1;
+    ctx.ws_rows = (int)rows;
+    ctx.ws_n = cfg.max_tokens;
+    ctx.ws_npow2 = p2;
+    const size_t kvb = (size_t)cfg.max_batch * cfg.n_kv_heads;
+    VK_CUDA(cudaMalloc(&ctx.tl, sizeof(float2) * rows * n));
+    VK_CUDA(cudaMalloc(&ctx.th, sizeof(float2) * rows * n));
+    VK_CUDA(cudaMalloc(&ctx.wl, sizeof(float) * rows * n));
+    VK_CUDA(cudaMalloc(&ctx.rows, sizeof(RowState) * rows));
+    VK_CUDA(cudaMemset(ctx.rows, 0, sizeof(RowState) * rows));
+    VK_CUDA(cudaMalloc(&ctx.keys, sizeof(unsigned long long) * rows * (size_t)p2));
+    VK_CUDA(cudaMalloc(&ctx.mark, sizeof(int32_t) * rows * n));
+    VK_CUDA(cudaMemset(ctx.mark, 0, sizeof(int32_t) * rows * n));
+    VK_CUDA(cudaMalloc(&ctx.elist, sizeof(int32_t) * rows * n));
+    VK_CUDA(cudaMalloc(&ctx.ubits, sizeof(uint32_t) * kvb * (n / 32 + 1)));
+    VK_CUDA(cudaMemset(ctx.ubits, 0, sizeof(uint32_t) * kvb * (n / 32 + 1)));
+    VK_CUDA(cudaMalloc(&ctx.ulist, sizeof(int32_t) * kvb * n));
+    VK_CUDA(cudaMalloc(&ctx.ucount, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMemset(ctx.ucount, 0, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMalloc(&ctx.staging, kvb * n * 2 * kHeadDim * ctx.elt));
+    VK_CUDA(cudaMalloc(&ctx.part, sizeof(float) * rows * ctx.nsplit * (kHeadDim + 2)));
+    return VERKV_OK;
+}
+
+bool slot_ok(const Ctx& c, int layer, int seq)
+{
+    return layer >= 0 && layer < c.cfg.n_layers && seq >= 0 && seq < c.cfg.n_seqs;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* verkv_status_str(verkv_status s)
+{
+    switch (s) {
+        case VERKV_OK: return "ok";
+        case VERKV_EINVAL: return "invalid argument";
+        case VERKV_ENOMEM: return "out of memory";
+        case VERKV_ECUDA: return "CUDA error";
+        case VERKV_ETIMEOUT: return "device wait timed out";
+        case VERKV_EUNSUPPORTED: return "unsupported configuration";
+        case VERKV_ESTATE: return "call out of order";
+    }
+    return "unknown status";
+}
+
+const char* verkv_last_error(const verkv_ctx* ctx) { return ctx ? ctx->c.err.c_str() : "null context"; }
+
+int32_t verkv_last_launch_count(const verkv_ctx* ctx) { return ctx ? ctx->c.last_launches : 0; }
+
+verkv_status verkv_create(const verkv_config* cfg, verkv_ctx** out)
+{
+    if (!cfg || !out) return VERKV_EINVAL;
+    *out = nullptr;
+    verkv_ctx* h = new (std::nothrow) verkv_ctx();
+    if (!h) return VERKV_ENOMEM;
+    Ctx& ctx = h->c;
+    ctx.cfg = *cfg;
+    verkv_status st = VERKV_OK;
+    const verkv_config& c = ctx.cfg;
+    if (c.n_layers <= 0 || c.n_seqs <= 0 || c.max_batch <= 0 || c.n_kv_heads <= 0 || c.n_q_heads <= 0 ||
+        c.max_tokens <= 0 || c.n_sink < 0 || c.n_local < 0 || c.n_q_heads % c.n_kv_heads != 0 ||
+        !(c.eta > 0.0 && c.eta <= 1.0) || (c.kv_dtype != VERKV_DTYPE_BF16 && c.kv_dtype != VERKV_DTYPE_F32) ||
+        (c.sketch != VERKV_SKETCH_EXACT && c.sketch != VERKV_SKETCH_INT8 && c.sketch != VERKV_SKETCH_2BIT))
+        st = fail(ctx, VERKV_EINVAL, "invalid configuration");
+    else if (c.head_dim != kHeadDim)
+        st = fail(ctx, VERKV_EUNSUPPORTED, "only head_dim 128 is built");
+    else if (c.max_batch > decode_max_batch())
+        st = fail(ctx, VERKV_EUNSUPPORTED, "max_batch above the built maximum (32)");
+    else if (c.sketch == VERKV_SKETCH_2BIT && c.sketch_group != 128)
+        st = fail(ctx, VERKV_EUNSUPPORTED, "the 2-bit sketch is built for groups of 128 tokens");
+    else if ((long long)c.max_tokens > (1ll << 26))
+        st = fail(ctx, VERKV_EUNSUPPORTED, "max_tokens above 2^26");
+    if (st == VERKV_OK) {
+        ctx.G = c.n_q_heads / c.n_kv_heads;
+        if (ctx.G != 1 && ctx.G != 2 && ctx.G != 4 && ctx.G != 8)
+            st = fail(ctx, VERKV_EUNSUPPORTED, "GQA group must be 1, 2, 4 or 8");
+    }
+    if (st == VERKV_OK) {
+        ctx.elt = c.kv_dtype == VERKV_DTYPE_BF16 ? 2 : 4;
+        cudaGetDevice(&ctx.device);
+        ctx.slots.resize((size_t)c.n_layers * c.n_seqs);
+        st = alloc_ws(ctx);
+    }
+    if (st != VERKV_OK) {
+        free_ws(ctx);
+        delete h;
+        return st;
+    }
+    *out = h;
+    return VERKV_OK;
+}
+
+verkv_status verkv_destroy(verkv_ctx* h)
+{
+    if (!h) return VERKV_EINVAL;
+    for (Slot& s : h->c.slots) free_slot(s);
+    free_ws(h->c);
+    delete h;
+    return VERKV_OK;
+}
+
+verkv_status verkv_compress(verkv_ctx* h, int32_t layer, int32_t seq, int32_t n_tokens, const void* kv_host,
+                            const void* kv_dev, const float* obs_q, int32_t W, const float* tau, verkv_stream stream,
+                            verkv_head_stats* stats)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    const verkv_config& c = ctx.cfg;
+    if (!slot_ok(ctx, layer, seq)) return fail(ctx, VERKV_EINVAL, "layer/seq slot out of range");
+    if (n_tokens <= 0 || n_tokens > c.max_tokens || n_tokens < c.n_sink + c.n_local)
+        return fail(ctx, VERKV_EINVAL, "n_tokens out of range");
+    if (!(c.eta * (double)n_tokens > (double)(c.n_sink + c.n_local)))
+        return fail(ctx, VERKV_EINVAL, "eta * n does not cover the sink and local tokens");
+    if (!kv_host) return fail(ctx, VERKV_EINVAL, "kv_host is required (the offloaded cache)");
+    if (!obs_q && !tau) return fail(ctx, VERKV_EINVAL, "either obs_q or tau is required");
+    if (obs_q && W <= 0) return fail(ctx, VERKV_EINVAL, "W must be positive");
+    if ((reinterpret_cast<uintptr_t>(kv_host) & 15) || (reinterpret_cast<uintptr_t>(kv_dev) & 15))
+        return fail(ctx, VERKV_EINVAL, "K/V buffers must be 16-byte aligned");
+    ctx.last_launches = 0;
+    Slot& s = ctx.slot(layer, seq);
+    verkv_status rc = compress_slot(ctx, s, layer, seq, n_tokens, kv_host, kv_dev, obs_q, W, tau, (cudaStream_t)stream);
+    if (rc != VERKV_OK) {
+        cudaStreamSynchronize((cudaStream_t)stream);
+        free_slot(s);
+        return rc;
+    }
+    if (stats) std::copy(s.stats.begin(), s.stats.end(), stats);
+    return VERKV_OK;
+}
+
+verkv_status verkv_decode(verkv_ctx* h, int32_t layer, const int32_t* seq_ids, int32_t B, const float* q, double eps,
+                          double delta, float* out, verkv_stream stream)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    const verkv_config& c = ctx.cfg;
+    if (layer < 0 || layer >= c.n_layers) return fail(ctx, VERKV_EINVAL, "layer out of range");
+    if (!seq_ids || B <= 0 || B > c.max_batch) return fail(ctx, VERKV_EINVAL, "bad batch");
+    if (!q || !out) return fail(ctx, VERKV_EINVAL, "q and out are required");
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 3))
+        return fail(ctx, VERKV_EINVAL, "q must be 16-byte aligned");
+    if (!(eps >= 0.0) || !std::isfinite(eps)) return fail(ctx, VERKV_EINVAL, "eps must be finite and >= 0");
+    if (!(delta > 0.0 && delta < 1.0)) return fail(ctx, VERKV_EINVAL, "delta must lie in (0, 1)");
+    for (int b = 0; b < B; ++b) {
+        if (seq_ids[b] < 0 || seq_ids[b] >= c.n_seqs) return fail(ctx, VERKV_EINVAL, "seq id out of range");
+        if (!ctx.slot(layer, seq_ids[b]).live) return fail(ctx, VERKV_ESTATE, "slot was not compressed");
+        for (int b2 = 0; b2 < b; ++b2)
+            if (seq_ids[b2] == seq_ids[b]) return fail(ctx, VERKV_EINVAL, "duplicate seq id in a batch");
+    }
+    return decode_rows(ctx, layer, seq_ids, B, q, eps, delta, out, (cudaStream_t)stream);
+}
+
+verkv_status verkv_release(verkv_ctx* h, int32_t layer, int32_t seq)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (!slot_ok(ctx, layer, seq)) return fail(ctx, VERKV_EINVAL, "layer/seq slot out of range");
+    VK_CUDA(cudaDeviceSynchronize());
+    free_slot(ctx.slot(layer, seq));
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_compress_state(verkv_ctx* h, int32_t layer, int32_t seq, int32_t kv_head, double* cval,
+                                      float* tau, float* r, uint8_t* flags, verkv_stream stream)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (!slot_ok(ctx, layer, seq) || kv_head < 0 || kv_head >= ctx.cfg.n_kv_heads)
+        return fail(ctx, VERKV_EINVAL, "slot or head out of range");
+    Slot& s = ctx.slot(layer, seq);
+    if (!s.live) return fail(ctx, VERKV_ESTATE, "slot was not compressed");
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t off = (size_t)kv_head * s.n;
+    if (tau) VK_CUDA(cudaMemcpyAsync(tau, s.tau + off, sizeof(float) * s.n, cudaMemcpyDeviceToHost, st));
+    if (r) VK_CUDA(cudaMemcpyAsync(r, s.r + off, sizeof(float) * s.n, cudaMemcpyDeviceToHost, st));
+    if (flags) VK_CUDA(cudaMemcpyAsync(flags, s.flags + off, s.n, cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaStreamSynchronize(st));
+    if (cval) *cval = s.stats[kv_head].c;
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_sketch(verkv_ctx* h, int32_t layer, int32_t seq, int32_t kv_head, int8_t* codes_i8,
+                              float* scale_f32, int32_t* pairs, uint8_t* codes_2bit, uint16_t* zero_f16,
+                              uint16_t* scale_f16, verkv_stream stream)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (!slot_ok(ctx, layer, seq) || kv_head < 0 || kv_head >= ctx.cfg.n_kv_heads)
+        return fail(ctx, VERKV_EINVAL, "slot or head out of range");
+    Slot& s = ctx.slot(layer, seq);
+    if (!s.live) return fail(ctx, VERKV_ESTATE, "slot was not compressed");
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t n = s.n, off = (size_t)kv_head * n;
+    if (ctx.cfg.sketch == VERKV_SKETCH_INT8) {
+        if (codes_i8) VK_CUDA(cudaMemcpyAsync(codes_i8, s.codes8 + off * kHeadDim, n * kHeadDim, cudaMemcpyDeviceToHost, st));
+        if (scale_f32) VK_CUDA(cudaMemcpyAsync(scale_f32, s.scale8 + off, sizeof(float) * n, cudaMemcpyDeviceToHost, st));
+        VK_CUDA(cudaStreamSynchronize(st));
+        return VERKV_OK;
+    }
+    if (ctx.cfg.sketch == VERKV_SKETCH_2BIT) {
+        const size_t ng = (n + ctx.cfg.sketch_group - 1) / ctx.cfg.sketch_group, kept = kHeadDim / 4;
+        std::vector<uint64_t> packed(n);
+        VK_CUDA(cudaMemcpyAsync(packed.data(), s.codes2 + off, sizeof(uint64_t) * n, cudaMemcpyDeviceToHost, st));
+        if (pairs) VK_CUDA(cudaMemcpyAsync(pairs, s.pairs + (size_t)kv_head * (kHeadDim / 8), sizeof(int32_t) * (kHeadDim / 8),
+                                           cudaMemcpyDeviceToHost, st));
+        if (zero_f16) VK_CUDA(cudaMemcpyAsync(zero_f16, s.zero2 + (size_t)kv_head * ng * kept, 2 * ng * kept,
+                                              cudaMemcpyDeviceToHost, st));
+        if (scale_f16) VK_CUDA(cudaMemcpyAsync(scale_f16, s.scale2 + (size_t)kv_head * ng * kept, 2 * ng * kept,
+                                               cudaMemcpyDeviceToHost, st));
+        VK_CUDA(cudaStreamSynchronize(st));
+        if (codes_2bit)
+            for (size_t i = 0; i < n; ++i)
+                for (size_t j = 0; j < kept; ++j) codes_2bit[i * kept + j] = (uint8_t)((packed[i] >> (2 * j)) & 3u);
+        return VERKV_OK;
+    }
+    return fail(ctx, VERKV_EINVAL, "the exact sketch has no codes");
+}
+
+verkv_status verkv_get_decode_trace(verkv_ctx* h, verkv_row_trace* out, int32_t n_rows, verkv_stream stream)
+{
+    if (!h || !out) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    const int rows = ctx.last_B * ctx.cfg.n_q_heads;
+    if (n_rows < rows) return fail(ctx, VERKV_EINVAL, "n_rows smaller than B * n_q_heads of the last decode");
+    std::vector<RowState> rs(rows);
+    VK_CUDA(cudaMemcpyAsync(rs.data(), ctx.rows, sizeof(RowState) * rows, cudaMemcpyDeviceToHost, (cudaStream_t)stream));
+    VK_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    for (int i = 0; i < rows; ++i) {
+        verkv_row_trace& t = out[i];
+        const RowState& s = rs[i];
+        memset(&t, 0, sizeof(t));
+        int mi = s.m_ord;
+        float mf;
+        int bits = mi >= 0 ? mi : mi ^ 0x7fffffff;
+        memcpy(&mf, &bits, 4);
+        t.m = mf;
+        t.D = s.D;
+        t.beta = s.beta;
+        t.sum_a = s.sum_a;
+        t.V = s.V;
+        t.b = s.b1;
+        t.eps_hat = s.eps_hat;
+        t.n_l = s.n_l;
+        t.kstar = s.kstar;
+        t.no_fetch = s.no_fetch;
+        t.fallback = s.fallback;
+        t.n_fetch = s.n_fetch;
+    }
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_exact_set(verkv_ctx* h, int32_t b, int32_t hq, int32_t* tokens, int32_t cap, int32_t* count,
+                                 verkv_stream stream)
+{
+    if (!h || !count) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (b < 0 || b >= ctx.last_B || hq < 0 || hq >= ctx.cfg.n_q_heads) return fail(ctx, VERKV_EINVAL, "row out of range");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int row = b * ctx.cfg.n_q_heads + hq;
+    RowState rs;
+    VK_CUDA(cudaMemcpyAsync(&rs, ctx.rows + row, sizeof(RowState), cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaStreamSynchronize(st));
+    const int k = std::max(0, rs.kstar);
+    *count = k;
+    const int m = std::min(k, cap);
+    if (tokens && m > 0) {
+        std::vector<int32_t> all(k);
+        VK_CUDA(cudaMemcpyAsync(all.data(), ctx.elist + (size_t)row * ctx.ws_n, sizeof(int32_t) * k,
+                                cudaMemcpyDeviceToHost, st));
+        VK_CUDA(cudaStreamSynchronize(st));
+        std::sort(all.begin(), all.end());
+        std::copy(all.begin(), all.begin() + m, tokens);
+    }
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_fetch_set(verkv_ctx* h, int32_t b, int32_t kv, int32_t* tokens, int32_t cap, int32_t* count,
+                                 verkv_stream stream)
+{
+    if (!h || !count) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (b < 0 || b >= ctx.last_B || kv < 0 || kv >= ctx.cfg.n_kv_heads) return fail(ctx, VERKV_EINVAL, "row out of range");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int idx = b * ctx.cfg.n_kv_heads + kv;
+    int cnt = 0;
+    VK_CUDA(cudaMemcpyAsync(&cnt, ctx.ucount + idx, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaStreamSynchronize(st));
+    *count = cnt;
+    const int m = std::min(cnt, cap);
+    if (tokens && m > 0) {
+        VK_CUDA(cudaMemcpyAsync(tokens, ctx.ulist + (size_t)idx * ctx.ws_n, sizeof(int32_t) * m, cudaMemcpyDeviceToHost, st));
+        VK_CUDA(cudaStreamSynchronize(st));
+    }
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_row_weights(verkv_ctx* h, int32_t b, int32_t hq, float* w_hat, int32_t* tokens, int32_t cap,
+                                   int32_t* count, verkv_stream stream)
+{
+    if (!h || !count) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (b < 0 || b >= ctx.last_B || hq < 0 || hq >= ctx.cfg.n_q_heads) return fail(ctx, VERKV_EINVAL, "row out of range");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int row = b * ctx.cfg.n_q_heads + hq;
+    const int kv = hq / ctx.G;
+    Slot& s = ctx.slot(ctx.last_layer, ctx.last_seq[b]);
+    const int nl = s.stats[kv].n_l;
+    *count = nl;
+    const int m = std::min(nl, cap);
+    if (w_hat && m > 0)
+        VK_CUDA(cudaMemcpyAsync(w_hat, ctx.wl + (size_t)row * ctx.ws_n, sizeof(float) * m, cudaMemcpyDeviceToHost, st));
+    if (tokens && m > 0)
+        VK_CUDA(cudaMemcpyAsync(tokens, s.ltok + (size_t)kv * s.n, sizeof(int32_t) * m, cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaStreamSynchronize(st));
+    return VERKV_OK;
+}
+
+}  // extern "C"

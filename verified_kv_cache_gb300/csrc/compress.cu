@@ -1,0 +1,657 @@
+// PoissonComp on the GPU: importance scores, water-filling, the Philox Poisson sample, compaction
+// of H u S into device memory and the token-level key sketch.
+// Paper: "Verify Before You Fetch: Reliable KV Cache Compression for LLM Inference",
+// Algorithm 1 / Sec. 4.1 (eq. (3)) and Appendix A.1 (key sketch).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace verkv {
+
+namespace {
+
+constexpr int kTauTok = 64;   // tokens per score tile
+constexpr int kTauRows = 64;  // observation rows per chunk
+constexpr int kTauLd = kHeadDim + 1;
+
+// --------------------------------------------------------------------------------------------
+// Importance scores (Algorithm 1, line 1), synthetic scorer: for the observation rows of the KV
+// head's query-head group, p_j(i) = softmax_i(<Q_j, K_i>/sqrt(d)); tau_i = max_j p_j(i) / max.
+// Pass 0 computes per (row, tile) the max logit and the sum of exp(logit - max); pass 1 turns the
+// per-row totals into p and keeps the max over rows for each token.
+// --------------------------------------------------------------------------------------------
+template <typename T, int PASS>
+__global__ void __launch_bounds__(256) tau_tile_kernel(const T* __restrict__ kv, int n, int R, int G, int W,
+                                                       const float* __restrict__ obs_q, float scale,
+                                                       float2* __restrict__ part, const float2* __restrict__ rowstat,
+                                                       float* __restrict__ tau_raw, int* __restrict__ tau_max)
+{
+    extern __shared__ float smem[];
+    float* Ks = smem;                        // [kTauTok][kTauLd]
+    float* Qs = Ks + kTauTok * kTauLd;       // [kTauRows][kTauLd]
+    float* Ls = Qs + kTauRows * kTauLd;      // [kTauRows][kTauTok + 1]
+    float* best = Ls + kTauRows * (kTauTok + 1);  // [kTauTok]
+    const int h = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x;
+    const int t0 = tile * kTauTok;
+    const int ntiles = gridDim.x;
+    const int64_t head_base = (int64_t)h * n * 2 * kHeadDim;
+    for (int e = tid; e < kTauTok * kHeadDim; e += blockDim.x) {
+        int t = e / kHeadDim, c = e % kHeadDim;
+        float v = 0.f;
+        if (t0 + t < n) v = Elt<T>::load(kv, head_base + (int64_t)(t0 + t) * 2 * kHeadDim + c);
+        Ks[t * kTauLd + c] = v;
+    }
+    if (PASS == 1 && tid < kTauTok) best[tid] = 0.f;
+    const int tx = tid & 15, ty = tid >> 4;   // 16 x 16 threads, each a 4 x 4 block
+    for (int r0 = 0; r0 < R; r0 += kTauRows) {
+        __syncthreads();
+        for (int e = tid; e < kTauRows * kHeadDim; e += blockDim.x) {
+            int rr = e / kHeadDim, c = e % kHeadDim;
+            int row = r0 + rr;
+            float v = 0.f;
+            if (row < R) {
+                int g = row / W, w = row % W;
+                v = obs_q[((int64_t)(h * G + g) * W + w) * kHeadDim + c];
+            }
+            Qs[rr * kTauLd + c] = v;
+        }
+        __syncthreads();
+        float acc[4][4] = {};
+        for (int c = 0; c < kHeadDim; ++c) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = Qs[(ty + 16 * i) * kTauLd + c];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Ks[(tx + 16 * j) * kTauLd + c];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                int rr = ty + 16 * i, t = tx + 16 * j;
+                float l = acc[i][j] * scale;
+                if (PASS == 1) {
+                    int row = r0 + rr;
+                    float p = 0.f;
+                    if (row < R && t0 + t < n) {
+                        float2 ms = rowstat[(int64_t)h * R + row];
+                        p = __fdiv_rn(expf(l - ms.x), ms.y);
+                    }
+                    l = p;
+                }
+                Ls[rr * (kTauTok + 1) + t] = l;
+            }
+        __syncthreads();
+        if (PASS == 0) {
+            if (tid < kTauRows && r0 + tid < R) {
+                float mx = -INFINITY;
+                for (int t = 0; t < kTauTok && t0 + t < n; ++t) mx = fmaxf(mx, Ls[tid * (kTauTok + 1) + t]);
+                float s = 0.f;
+                for (int t = 0; t < kTauTok && t0 + t < n; ++t) s += expf(Ls[tid * (kTauTok + 1) + t] - mx);
+                part[((int64_t)h * R + r0 + tid) * ntiles + tile] = make_float2(mx, s);
+            }
+        } else {
+            if (tid < kTauTok) {
+                float mx = best[tid];
+                for (int rr = 0; rr < kTauRows; ++rr) mx = fmaxf(mx, Ls[rr * (kTauTok + 1) + tid]);
+                best[tid] = mx;
+            }
+        }
+    }
+    if (PASS == 1) {
+        __syncthreads();
+        if (tid < kTauTok && t0 + tid < n) {
+            tau_raw[(int64_t)h * n + t0 + tid] = best[tid];
+            atomicMax(&tau_max[h], float_to_ordered(best[tid]));
+        }
+    }
+}
+
+__global__ void tau_rowstat_kernel(const float2* __restrict__ part, int ntiles, float2* __restrict__ rowstat, int rows)
+{
+    const int row = blockIdx.x * blockDim.y + threadIdx.y;
+    if (row >= rows) return;
+    const float2* p = part + (int64_t)row * ntiles;
+    float mx = -INFINITY;
+    for (int t = threadIdx.x; t < ntiles; t += 32) mx = fmaxf(mx, p[t].x);
+    mx = warp_max(mx);
+    double s = 0.0;
+    for (int t = threadIdx.x; t < ntiles; t += 32) s += (double)p[t].y * exp((double)p[t].x - (double)mx);
+    s = warp_sum(s);
+    if (threadIdx.x == 0) rowstat[row] = make_float2(mx, (float)s);
+}
+
+// tau := tau_raw / max (or the caller's scores), clamped to [2^-38, 1]; sink and local := 1.
+__global__ void tau_finish_kernel(float* __restrict__ tau, const float* __restrict__ src, const int* __restrict__ tau_max,
+                                  int n, int n_sink, int n_local)
+{
+    const int h = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float v = src[(int64_t)h * n + i];
+    if (tau_max) v = __fdiv_rn(v, ordered_to_float(tau_max[h]));
+    v = tau_clamp(v);
+    if (i < n_sink || i >= n - n_local) v = 1.0f;
+    tau[(int64_t)h * n + i] = v;
+}
+
+// --------------------------------------------------------------------------------------------
+// Water-filling (Algorithm 1, lines 2-3; eq. (3)).  With U the tokens outside the sink/local
+// windows and B' = eta n - |I|, the constant is c = (B' - t) / S where t tokens of U are capped
+// (c tau >= 1) and S is the exact sum of the other scores.  For a threshold theta let
+// psi(theta) = (B' - #{tau > theta}) theta - sum_{tau <= theta} tau; the capped set is
+// {tau > theta*} for the largest data value theta* with psi(theta*) < 0, and {theta > 0 :
+// psi(theta) < 0} is an interval, so a bisection over the fp32 bit patterns finds it.  Sums are
+// exact: clamped scores are integers in units of 2^-61, accumulated in 2 x 64-bit words and
+// rounded to double once.
+// --------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t tau_fixed(float t)
+{
+    const uint32_t b = __float_as_uint(t);
+    const uint64_t m = (b & 0x7fffffu) | 0x800000u;
+    const int e = (int)((b >> 23) & 0xff) - 127;
+    return m << (e + 38);
+}
+
+struct WfPass {
+    int cnt_gt;
+    double s_le;
+    uint32_t max_le;  // largest bit pattern <= u (0 if none)
+    uint32_t min_gt;  // smallest bit pattern > u (0xffffffff if none)
+};
+
+__device__ WfPass wf_pass(const float* __restrict__ t, int n, int n_sink, int n_local, uint32_t u, void* sm_raw)
+{
+    struct Sm {
+        unsigned long long lo, hi;
+        int cnt;
+        unsigned int max_le, min_gt;
+    };
+    Sm* sm = reinterpret_cast<Sm*>(sm_raw);
+    __syncthreads();
+    if (threadIdx.x == 0) { sm->lo = 0; sm->hi = 0; sm->cnt = 0; sm->max_le = 0; sm->min_gt = 0xffffffffu; }
+    __syncthreads();
+    unsigned long long lo = 0, hi = 0;
+    int cnt = 0;
+    uint32_t mx = 0, mn = 0xffffffffu;
+    for (int i = n_sink + threadIdx.x; i < n - n_local; i += blockDim.x) {
+        const uint32_t b = __float_as_uint(t[i]);
+        if (b > u) { ++cnt; mn = min(mn, b); }
+        else {
+            const uint64_t f = tau_fixed(t[i]);
+            lo += f & 0xffffffffull;
+            hi += f >> 32;
+            mx = max(mx, b);
+        }
+    }
+    lo = warp_sum(lo);
+    hi = warp_sum(hi);
+    cnt = warp_sum(cnt);
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&sm->lo, lo);
+        atomicAdd(&sm->hi, hi);
+        atomicAdd(&sm->cnt, cnt);
+        atomicMax(&sm->max_le, mx);
+        atomicMin(&sm->min_gt, mn);
+    }
+    __syncthreads();
+    WfPass r;
+    r.cnt_gt = sm->cnt;
+    const unsigned long long L = sm->lo, Hh = sm->hi;
+    const uint64_t low64 = (Hh << 32) + L;
+    const uint64_t carry = low64 < L ? 1 : 0;
+    const uint64_t high64 = (Hh >> 32) + carry;
+    r.s_le = ldexp(u128_to_double_rn(high64, low64), -61);
+    r.max_le = sm->max_le;
+    r.min_gt = sm->min_gt;
+    return r;
+}
+
+__global__ void __launch_bounds__(1024) waterfill_kernel(const float* __restrict__ tau, int n, int n_sink,
+                                                         int n_local, double budget, double* __restrict__ c_out,
+                                                         int* __restrict__ capped_out, int* __restrict__ neartie)
+{
+    __shared__ __align__(16) unsigned char sm[64];
+    const int h = blockIdx.x;
+    const float* t = tau + (int64_t)h * n;
+    const int nf = n_sink + n_local;
+    const double bprime = budget - (double)nf;
+    const int nu = n - nf;
+    if (bprime >= (double)nu) {
+        if (threadIdx.x == 0) { c_out[h] = INFINITY; capped_out[h] = nu; }
+        return;
+    }
+    auto pred = [&](uint32_t u) -> bool {
+        WfPass p = wf_pass(t, n, n_sink, n_local, u, sm);
+        return (bprime - (double)p.cnt_gt) * (double)__uint_as_float(u) < p.s_le;
+    };
+    uint32_t lo = 1u, hi = 0x3f800000u;
+    uint32_t ustar;
+    if (pred(hi)) ustar = hi;
+    else {
+        while (hi - lo > 1u) {
+            const uint32_t mid = lo + (hi - lo) / 2u;
+            if (pred(mid)) lo = mid; else hi = mid;
+        }
+        ustar = lo;
+    }
+    WfPass p = wf_pass(t, n, n_sink, n_local, ustar, sm);
+    const double c = (bprime - (double)p.cnt_gt) / p.s_le;
+    // The same decision at the data values themselves (the form of the rule that walks the
+    // sorted scores): the capped/uncapped boundary must be accepted at max_le and rejected at min_gt.
+    int tie = 0;
+    if (p.max_le != 0 && !((bprime - (double)p.cnt_gt) * (double)__uint_as_float(p.max_le) < p.s_le)) tie = 1;
+    if (p.min_gt != 0xffffffffu) {
+        WfPass q = wf_pass(t, n, n_sink, n_local, p.min_gt, sm);
+        if ((bprime - (double)q.cnt_gt) * (double)__uint_as_float(p.min_gt) < q.s_le) tie = 1;
+    }
+    if (threadIdx.x == 0) {
+        c_out[h] = c;
+        capped_out[h] = p.cnt_gt;
+        if (tie) atomicAdd(neartie, 1);
+    }
+}
+
+// --------------------------------------------------------------------------------------------
+// r_i = min(1, c tau_i) rounded to fp32 (H = {r = 1}); Z_i = [u_i < r_i] (Algorithm 1, lines 3-4).
+// --------------------------------------------------------------------------------------------
+__global__ void sample_kernel(const float* __restrict__ tau, const double* __restrict__ c, int n, int n_sink,
+                              int n_local, uint64_t seed, int layer, int seq, float* __restrict__ r_out,
+                              uint8_t* __restrict__ flags)
+{
+    const int h = blockIdx.y;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int64_t k = (int64_t)h * n + i;
+    float r;
+    if (i < n_sink || i >= n - n_local) r = 1.0f;
+    else {
+        const double ct = c[h] * (double)tau[k];
+        r = ct < 1.0 ? __double2float_rn(ct) : 1.0f;
+    }
+    r_out[k] = r;
+    uint8_t f;
+    if (r == 1.0f) f = 2;
+    else f = poisson_uniform(seed, (uint32_t)i, (uint32_t)h, (uint32_t)layer, (uint32_t)seq) < r ? 1 : 0;
+    flags[k] = f;
+}
+
+// Ordered compaction of one KV head: L list (with r in L order), resident list (H u S), H list.
+// lpos[token] is the L index for tokens of L and -(H index) - 1 for tokens of H.
+__global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ flags, const float* __restrict__ r,
+                                                       int n, int32_t* __restrict__ lpos, int32_t* __restrict__ ltok,
+                                                       float* __restrict__ rl, int32_t* __restrict__ rtok,
+                                                       int32_t* __restrict__ hslot, int32_t* __restrict__ counts)
+{
+    __shared__ int scratch[32];
+    const int h = blockIdx.x;
+    const int64_t base = (int64_t)h * n;
+    int offL = 0, offR = 0, offH = 0, offS = 0;
+    for (int t0 = 0; t0 < n; t0 += blockDim.x) {
+        const int i = t0 + threadIdx.x;
+        const int f = i < n ? flags[base + i] : -1;
+        const int isL = (f == 0 || f == 1), isR = (f == 1 || f == 2), isH = (f == 2), isS = (f == 1);
+        int tot1, tot2;
+        const int ex1 = block_exclusive_scan(isL | (isR << 16), scratch, &tot1);
+        const int ex2 = block_exclusive_scan(isH | (isS << 16), scratch, &tot2);
+        const int pL = ex1 & 0xffff, pR = ex1 >> 16, pH = ex2 & 0xffff;
+        if (i < n) {
+            if (isL) {
+                ltok[base + offL + pL] = i;
+                rl[base + offL + pL] = r[base + i];
+                lpos[base + i] = offL + pL;
+            } else {
+                lpos[base + i] = -(offH + pH) - 1;
+            }
+            if (isR) rtok[base + offR + pR] = i;
+            if (isH) hslot[base + offH + pH] = offR + pR;
+        }
+        offL += tot1 & 0xffff;
+        offR += tot1 >> 16;
+        offH += tot2 & 0xffff;
+        offS += tot2 >> 16;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        counts[h * 4 + 0] = offH;
+        counts[h * 4 + 1] = offL;
+        counts[h * 4 + 2] = offS;
+        counts[h * 4 + 3] = offR;
+    }
+}
+
+// Copy the K/V rows of H u S (ascending tokens) into the resident cache; one warp per row.
+__global__ void gather_resident_kernel(const unsigned char* __restrict__ src, int n, size_t row_bytes,
+                                       const int32_t* __restrict__ rtok, const int32_t* __restrict__ counts,
+                                       const int64_t* __restrict__ res_off, unsigned char* __restrict__ dst)
+{
+    const int h = blockIdx.y;
+    const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
+    const int m = counts[h * 4 + 3];
+    for (int s = blockIdx.x * warps + (threadIdx.x >> 5); s < m; s += gridDim.x * warps) {
+        const int tok = rtok[(int64_t)h * n + s];
+        const uint4* from = reinterpret_cast<const uint4*>(src + ((int64_t)h * n + tok) * row_bytes);
+        uint4* to = reinterpret_cast<uint4*>(dst + (res_off[h] + s) * (int64_t)row_bytes);
+        for (size_t v = lane; v < row_bytes / 16; v += 32) to[v] = from[v];
+    }
+}
+
+// --------------------------------------------------------------------------------------------
+// Int8 sketch: per token s = max|k| / 127 (fp32), code = rint(k / s) clamped to [-127, 127].
+// One warp per token, 4 channels per lane.
+// --------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void sketch_int8_kernel(const T* __restrict__ kv, int n, int n_kv, int8_t* __restrict__ codes,
+                                   float* __restrict__ scale)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t tok = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (tok >= (int64_t)n * n_kv) return;
+    const T* k = kv + tok * 2 * kHeadDim;  // [h][i] flattened: tok = h * n + i
+    float v[4];
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[j] = Elt<T>::load(k, lane * 4 + j);
+        mx = fmaxf(mx, fabsf(v[j]));
+    }
+    mx = warp_max(mx);
+    const float s = __fdiv_rn(mx, 127.0f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int q = 0;
+        if (s > 0.f) {
+            float x = rintf(__fdiv_rn(v[j], s));
+            x = fminf(fmaxf(x, -127.f), 127.f);
+            q = (int)x;
+        }
+        packed |= ((uint32_t)(q & 0xff)) << (8 * j);
+    }
+    reinterpret_cast<uint32_t*>(codes + tok * kHeadDim)[lane] = packed;
+    if (lane == 0) scale[tok] = s;
+}
+
+// 2-bit sketch, step 1: energy of each rotate-half pair (p, p + d/2), summed in double.
+template <typename T>
+__global__ void pair_energy_kernel(const T* __restrict__ kv, int n, int tokens_per_block, double* __restrict__ energy)
+{
+    const int h = blockIdx.y, c = threadIdx.x;  // blockDim.x == kHeadDim
+    const int i0 = blockIdx.x * tokens_per_block;
+    const int i1 = min(n, i0 + tokens_per_block);
+    double e = 0.0;
+    for (int i = i0; i < i1; ++i) {
+        const double x = (double)Elt<T>::load(kv, ((int64_t)h * n + i) * 2 * kHeadDim + c);
+        e += x * x;
+    }
+    atomicAdd(&energy[h * (kHeadDim / 2) + (c % (kHeadDim / 2))], e);
+}
+
+// Step 2: the d/8 pairs of largest energy (ties: lower pair index), ascending.
+__global__ void select_pairs_kernel(const double* __restrict__ energy, int32_t* __restrict__ pairs)
+{
+    constexpr int P = kHeadDim / 2, K = kHeadDim / 8;
+    __shared__ double e[P];
+    __shared__ int chosen[P];
+    const int h = blockIdx.x, p = threadIdx.x;  // blockDim.x == P
+    e[p] = energy[h * P + p];
+    __syncthreads();
+    int rank = 0;
+    for (int q = 0; q < P; ++q) rank += (e[q] > e[p]) || (e[q] == e[p] && q < p);
+    chosen[p] = rank < K;
+    __syncthreads();
+    if (chosen[p]) {
+        int pos = 0;
+        for (int q = 0; q < p; ++q) pos += chosen[q];
+        pairs[h * K + pos] = p;
+    }
+}
+
+__device__ __forceinline__ uint64_t spread_bits(uint32_t x)
+{
+    uint64_t v = x;
+    v = (v | (v << 16)) & 0x0000FFFF0000FFFFull;
+    v = (v | (v << 8)) & 0x00FF00FF00FF00FFull;
+    v = (v | (v << 4)) & 0x0F0F0F0F0F0F0F0Full;
+    v = (v | (v << 2)) & 0x3333333333333333ull;
+    v = (v | (v << 1)) & 0x5555555555555555ull;
+    return v;
+}
+
+// Step 3: per (group of `group` tokens, kept channel) zero = fp16(min), scale = fp16((max-min)/3),
+// code = rint((k - zero) / scale) clamped to [0, 3].  One warp per group, lane = kept channel.
+template <typename T>
+__global__ void sketch_2bit_kernel(const T* __restrict__ kv, int n, int group, const int32_t* __restrict__ pairs,
+                                   uint64_t* __restrict__ codes, __half* __restrict__ zero, __half* __restrict__ scl)
+{
+    constexpr int NP = kHeadDim / 8, KEPT = kHeadDim / 4;
+    const int h = blockIdx.y, g = blockIdx.x, lane = threadIdx.x;  // blockDim.x == 32 == KEPT
+    const int ch = lane < NP ? pairs[h * NP + lane] : pairs[h * NP + lane - NP] + kHeadDim / 2;
+    const int i0 = g * group, i1 = min(n, i0 + group);
+    float mn = INFINITY, mx = -INFINITY;
+    for (int i = i0; i < i1; ++i) {
+        const float v = Elt<T>::load(kv, ((int64_t)h * n + i) * 2 * kHeadDim + ch);
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+    }
+    const __half zh = __float2half_rn(mn);
+    const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+    const int ngroups = (n + group - 1) / group;
+    zero[((int64_t)h * ngroups + g) * KEPT + lane] = zh;
+    scl[((int64_t)h * ngroups + g) * KEPT + lane] = sh;
+    const float zf = __half2float(zh), sf = __half2float(sh);
+    for (int i = i0; i < i1; ++i) {
+        const float v = Elt<T>::load(kv, ((int64_t)h * n + i) * 2 * kHeadDim + ch);
+        int code = 0;
+        if (sf > 0.f) {
+            float x = rintf(__fdiv_rn(__fsub_rn(v, zf), sf));
+            x = fminf(fmaxf(x, 0.f), 3.f);
+            code = (int)x;
+        }
+        const uint32_t b0 = __ballot_sync(0xffffffffu, code & 1);
+        const uint32_t b1 = __ballot_sync(0xffffffffu, code >> 1);
+        if (lane == 0) codes[(int64_t)h * n + i] = spread_bits(b0) | (spread_bits(b1) << 1);
+    }
+}
+
+// Exact sketch: keep the keys themselves ([h][n][d]).
+template <typename T>
+__global__ void copy_keys_kernel(const T* __restrict__ kv, int64_t rows, T* __restrict__ out)
+{
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= rows * kHeadDim) return;
+    const int64_t row = e / kHeadDim, c = e % kHeadDim;
+    out[e] = kv[row * 2 * kHeadDim + c];
+}
+
+template <typename T>
+verkv_status run_scores(Ctx& ctx, Slot& s, const T* kv, int n, const float* obs_q, int W, const float* tau_in,
+                        cudaStream_t st)
+{
+    const verkv_config& cfg = ctx.cfg;
+    const int Hkv = cfg.n_kv_heads;
+    dim3 g1((n + 255) / 256, Hkv);
+    if (!obs_q) {
+        tau_finish_kernel<<<g1, 256, 0, st>>>(s.tau, tau_in, nullptr, n, cfg.n_sink, cfg.n_local);
+        VK_LAUNCH_CHECK();
+        return VERKV_OK;
+    }
+    const int R = ctx.G * W;
+    const int ntiles = (n + kTauTok - 1) / kTauTok;
+    float2 *part = nullptr, *rowstat = nullptr;
+    float* tau_raw = nullptr;
+    int* tau_max = nullptr;
+    VK_CUDA(cudaMallocAsync(&part, sizeof(float2) * (size_t)Hkv * R * ntiles, st));
+    VK_CUDA(cudaMallocAsync(&rowstat, sizeof(float2) * (size_t)Hkv * R, st));
+    VK_CUDA(cudaMallocAsync(&tau_raw, sizeof(float) * (size_t)Hkv * n, st));
+    VK_CUDA(cudaMallocAsync(&tau_max, sizeof(int) * Hkv, st));
+    VK_CUDA(cudaMemsetAsync(tau_max, 0x80, sizeof(int) * Hkv, st));  // ordered(-huge)
+    const size_t smem = sizeof(float) * ((size_t)kTauTok * kTauLd + (size_t)kTauRows * kTauLd +
+                                         (size_t)kTauRows * (kTauTok + 1) + kTauTok);
+    static bool attr_done[2] = {false, false};
+    if (!attr_done[sizeof(T) == 4]) {
+        VK_CUDA(cudaFuncSetAttribute(tau_tile_kernel<T, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        VK_CUDA(cudaFuncSetAttribute(tau_tile_kernel<T, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        attr_done[sizeof(T) == 4] = true;
+    }
+    const float scale = (float)(1.0 / std::sqrt((double)kHeadDim));
+    dim3 gt(ntiles, Hkv);
+    tau_tile_kernel<T, 0><<<gt, 256, smem, st>>>(kv, n, R, ctx.G, W, obs_q, scale, part, nullptr, nullptr, nullptr);
+    VK_LAUNCH_CHECK();
+    dim3 br(32, 8);
+    tau_rowstat_kernel<<<(Hkv * R + 7) / 8, br, 0, st>>>(part, ntiles, rowstat, Hkv * R);
+    VK_LAUNCH_CHECK();
+    tau_tile_kernel<T, 1><<<gt, 256, smem, st>>>(kv, n, R, ctx.G, W, obs_q, scale, nullptr, rowstat, tau_raw, tau_max);
+    VK_LAUNCH_CHECK();
+    tau_finish_kernel<<<g1, 256, 0, st>>>(s.tau, tau_raw, tau_max, n, cfg.n_sink, cfg.n_local);
+    VK_LAUNCH_CHECK();
+    VK_CUDA(cudaFreeAsync(part, st));
+    VK_CUDA(cudaFreeAsync(rowstat, st));
+    VK_CUDA(cudaFreeAsync(tau_raw, st));
+    VK_CUDA(cudaFreeAsync(tau_max, st));
+    return VERKV_OK;
+}
+
+template <typename T>
+verkv_status run_sketch(Ctx& ctx, Slot& s, const T* kv, int n, cudaStream_t st)
+{
+    const verkv_config& cfg = ctx.cfg;
+    const int Hkv = cfg.n_kv_heads;
+    if (cfg.sketch == VERKV_SKETCH_INT8) {
+        const int64_t toks = (int64_t)Hkv * n;
+        sketch_int8_kernel<T><<<(unsigned)((toks + 7) / 8), 256, 0, st>>>(kv, n, Hkv, s.codes8, s.scale8);
+        VK_LAUNCH_CHECK();
+    } else if (cfg.sketch == VERKV_SKETCH_2BIT) {
+        VK_CUDA(cudaMemsetAsync(s.energy, 0, sizeof(double) * Hkv * (kHeadDim / 2), st));
+        const int tpb = 256;
+        pair_energy_kernel<T><<<dim3((n + tpb - 1) / tpb, Hkv), kHeadDim, 0, st>>>(kv, n, tpb, s.energy);
+        VK_LAUNCH_CHECK();
+        select_pairs_kernel<<<Hkv, kHeadDim / 2, 0, st>>>(s.energy, s.pairs);
+        VK_LAUNCH_CHECK();
+        const int ngroups = (n + cfg.sketch_group - 1) / cfg.sketch_group;
+        sketch_2bit_kernel<T><<<dim3(ngroups, Hkv), 32, 0, st>>>(kv, n, cfg.sketch_group, s.pairs, s.codes2, s.zero2,
+                                                                s.scale2);
+        VK_LAUNCH_CHECK();
+    } else {
+        const int64_t rows = (int64_t)Hkv * n;
+        copy_keys_kernel<T><<<(unsigned)((rows * kHeadDim + 255) / 256), 256, 0, st>>>(
+            kv, rows, reinterpret_cast<T*>(s.kexact));
+        VK_LAUNCH_CHECK();
+    }
+    return VERKV_OK;
+}
+
+}  // namespace
+
+void free_slot(Slot& s)
+{
+    void* ptrs[] = {s.tau, s.r, s.flags, s.lpos, s.ltok, s.rl, s.rtok, s.hslot, s.counts, s.c, s.capped, s.kvres,
+                    s.res_off, s.codes8, s.scale8, s.codes2, s.zero2, s.scale2, s.pairs, s.energy, s.kexact};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+    s = Slot();
+}
+
+verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const void* kv_host, const void* kv_dev,
+                           const float* obs_q, int W, const float* tau, cudaStream_t st)
+{
+    const verkv_config& cfg = ctx.cfg;
+    const int Hkv = cfg.n_kv_heads;
+    const size_t hn = (size_t)Hkv * n;
+    VK_CUDA(cudaStreamSynchronize(st));
+    free_slot(s);
+    s.n = n;
+    s.kv_host = kv_host;
+    VK_CUDA(cudaMalloc(&s.tau, sizeof(float) * hn));
+    VK_CUDA(cudaMalloc(&s.r, sizeof(float) * hn));
+    VK_CUDA(cudaMalloc(&s.flags, hn));
+    VK_CUDA(cudaMalloc(&s.lpos, sizeof(int32_t) * hn));
+    VK_CUDA(cudaMalloc(&s.ltok, sizeof(int32_t) * hn));
+    VK_CUDA(cudaMalloc(&s.rl, sizeof(float) * hn));
+    VK_CUDA(cudaMalloc(&s.rtok, sizeof(int32_t) * hn));
+    VK_CUDA(cudaMalloc(&s.hslot, sizeof(int32_t) * hn));
+    VK_CUDA(cudaMalloc(&s.counts, sizeof(int32_t) * Hkv * 4));
+    VK_CUDA(cudaMalloc(&s.c, sizeof(double) * Hkv));
+    VK_CUDA(cudaMalloc(&s.capped, sizeof(int32_t) * (Hkv + 1)));
+    VK_CUDA(cudaMalloc(&s.res_off, sizeof(int64_t) * (Hkv + 1)));
+    if (cfg.sketch == VERKV_SKETCH_INT8) {
+        VK_CUDA(cudaMalloc(&s.codes8, hn * kHeadDim));
+        VK_CUDA(cudaMalloc(&s.scale8, sizeof(float) * hn));
+    } else if (cfg.sketch == VERKV_SKETCH_2BIT) {
+        const size_t ng = (size_t)(n + cfg.sketch_group - 1) / cfg.sketch_group;
+        VK_CUDA(cudaMalloc(&s.codes2, sizeof(uint64_t) * hn));
+        VK_CUDA(cudaMalloc(&s.zero2, sizeof(__half) * Hkv * ng * (kHeadDim / 4)));
+        VK_CUDA(cudaMalloc(&s.scale2, sizeof(__half) * Hkv * ng * (kHeadDim / 4)));
+        VK_CUDA(cudaMalloc(&s.pairs, sizeof(int32_t) * Hkv * (kHeadDim / 8)));
+        VK_CUDA(cudaMalloc(&s.energy, sizeof(double) * Hkv * (kHeadDim / 2)));
+    } else {
+        VK_CUDA(cudaMalloc(&s.kexact, hn * kHeadDim * ctx.elt));
+    }
+    const void* kv = kv_dev ? kv_dev : kv_host;
+    verkv_status rc;
+    if (cfg.kv_dtype == VERKV_DTYPE_BF16)
+        rc = run_scores<__nv_bfloat16>(ctx, s, (const __nv_bfloat16*)kv, n, obs_q, W, tau, st);
+    else
+        rc = run_scores<float>(ctx, s, (const float*)kv, n, obs_q, W, tau, st);
+    if (rc != VERKV_OK) return rc;
+
+    VK_CUDA(cudaMemsetAsync(s.capped + Hkv, 0, sizeof(int32_t), st));
+    waterfill_kernel<<<Hkv, 1024, 0, st>>>(s.tau, n, cfg.n_sink, cfg.n_local, cfg.eta * (double)n, s.c, s.capped,
+                                          s.capped + Hkv);
+    VK_LAUNCH_CHECK();
+    sample_kernel<<<dim3((n + 255) / 256, Hkv), 256, 0, st>>>(s.tau, s.c, n, cfg.n_sink, cfg.n_local, cfg.seed, layer,
+                                                            seq, s.r, s.flags);
+    VK_LAUNCH_CHECK();
+    compact_kernel<<<Hkv, 1024, 0, st>>>(s.flags, s.r, n, s.lpos, s.ltok, s.rl, s.rtok, s.hslot, s.counts);
+    VK_LAUNCH_CHECK();
+
+    std::vector<int32_t> counts((size_t)Hkv * 4), capped((size_t)Hkv + 1);
+    std::vector<double> cval(Hkv);
+    VK_CUDA(cudaMemcpyAsync(counts.data(), s.counts, sizeof(int32_t) * Hkv * 4, cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaMemcpyAsync(capped.data(), s.capped, sizeof(int32_t) * (Hkv + 1), cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaMemcpyAsync(cval.data(), s.c, sizeof(double) * Hkv, cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaStreamSynchronize(st));
+    s.res_off_host.assign((size_t)Hkv + 1, 0);
+    s.stats.assign((size_t)Hkv, verkv_head_stats{});
+    int max_res = 0;
+    for (int h = 0; h < Hkv; ++h) {
+        verkv_head_stats& hs = s.stats[h];
+        hs.c = cval[h];
+        hs.n_capped = capped[h];
+        hs.n_h = counts[h * 4 + 0];
+        hs.n_l = counts[h * 4 + 1];
+        hs.n_s = counts[h * 4 + 2];
+        hs.n_resident = counts[h * 4 + 3];
+        s.res_off_host[h + 1] = s.res_off_host[h] + hs.n_resident;
+        max_res = std::max(max_res, hs.n_resident);
+    }
+    const size_t row_bytes = 2 * kHeadDim * ctx.elt;
+    VK_CUDA(cudaMalloc(&s.kvres, std::max<size_t>(1, (size_t)s.res_off_host[Hkv]) * row_bytes));
+    VK_CUDA(cudaMemcpyAsync(s.res_off, s.res_off_host.data(), sizeof(int64_t) * (Hkv + 1), cudaMemcpyHostToDevice, st));
+    if (max_res > 0) {
+        gather_resident_kernel<<<dim3((max_res + 7) / 8, Hkv), 256, 0, st>>>(
+            (const unsigned char*)kv, n, row_bytes, s.rtok, s.counts, s.res_off, (unsigned char*)s.kvres);
+        VK_LAUNCH_CHECK();
+    }
+    if (cfg.kv_dtype == VERKV_DTYPE_BF16)
+        rc = run_sketch<__nv_bfloat16>(ctx, s, (const __nv_bfloat16*)kv, n, st);
+    else
+        rc = run_sketch<float>(ctx, s, (const float*)kv, n, st);
+    if (rc != VERKV_OK) return rc;
+    VK_CUDA(cudaStreamSynchronize(st));
+    s.live = true;
+    return VERKV_OK;
+}
+
+}  // namespace verkv

@@ -1,0 +1,156 @@
+// Internal state of a libverkv context (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/verkv.h"
+
+namespace verkv {
+
+// Compressed state of one (layer, sequence) slot.  Per-KV-head arrays are laid out
+// [n_kv_heads][n] with head stride n (the slot's context length).
+struct Slot {
+    bool live = false;
+    int n = 0;
+    const void* kv_host = nullptr;  // borrowed pinned [Hkv][n][2][d]
+
+    float* tau = nullptr;       // [Hkv][n] importance scores after clamping / forcing
+    float* r = nullptr;         // [Hkv][n] inclusion probabilities (fp32)
+    uint8_t* flags = nullptr;   // [Hkv][n] 2 = H, 1 = S, 0 = L \ S
+    int32_t* lpos = nullptr;    // [Hkv][n] token -> index in L (ascending tokens); -(H index)-1 for H
+    int32_t* ltok = nullptr;    // [Hkv][n] L index -> token
+    float* rl = nullptr;        // [Hkv][n] r by L index
+    int32_t* rtok = nullptr;    // [Hkv][n] resident slot -> token (H u S ascending)
+    int32_t* hslot = nullptr;   // [Hkv][n] H index -> resident slot
+    int32_t* counts = nullptr;  // [Hkv][4] |H|, |L|, |S|, |H|+|S|
+    double* c = nullptr;        // [Hkv] water-filling constant
+    int32_t* capped = nullptr;  // [Hkv] tokens outside sink/local with r = 1
+    void* kvres = nullptr;      // [sum_h m_h][2][d] resident K/V rows, head h from res_off[h]
+    int64_t* res_off = nullptr; // device [Hkv + 1] row offsets into kvres
+
+    // sketches
+    int8_t* codes8 = nullptr;   // [Hkv][n][d]
+    float* scale8 = nullptr;    // [Hkv][n]
+    uint64_t* codes2 = nullptr; // [Hkv][n] 2-bit codes of the kept channels, channel j at bits 2j..2j+1
+    __half* zero2 = nullptr;    // [Hkv][ngroups][d/4]
+    __half* scale2 = nullptr;   // [Hkv][ngroups][d/4]
+    int32_t* pairs = nullptr;   // [Hkv][d/8] kept rotate-half pairs, ascending
+    double* energy = nullptr;   // [Hkv][d/2] pair energies (scratch of the 2-bit sketch)
+    void* kexact = nullptr;     // [Hkv][n][d] keys for the exact sketch
+
+    std::vector<verkv_head_stats> stats;     // host copy
+    std::vector<int64_t> res_off_host;       // host copy of res_off
+};
+
+// Per query row scalars of one decode (device).  Doubles are accumulated with atomics.
+struct RowState {
+    int m_ord;          // ordered-int of the logit shift m (max logit)
+    int no_fetch;
+    int kstar;
+    int fallback;
+    int n_l;
+    int n_h;
+    int n_fetch;        // |E \ S|
+    int b_arg;          // L index of the largest b_i
+    double D;           // sum_H w + sum_L w^
+    double alpha_sum;   // sum_L w^ (1 - r): upper end of the beta bracket
+    double beta;
+    double sum_a;
+    double V;
+    double b1, b2;      // largest and second-largest b_i
+    double eps_hat;
+    double pad;
+};
+
+struct Ctx {
+    verkv_config cfg{};
+    int device = 0;
+    int G = 1;                      // query heads per KV head
+    size_t elt = 2;                 // bytes per K/V element
+    std::vector<Slot> slots;        // [n_layers * n_seqs]
+    std::string err;
+    int last_launches = 0;
+    int gen = 0;                    // decode generation tag
+
+    // decode workspace, sized for max_batch rows sets
+    int ws_rows = 0;                // max_batch * n_q_heads
+    int ws_n = 0;                   // max_tokens
+    int ws_npow2 = 0;               // next power of two >= max_tokens
+    float2* tl = nullptr;           // [rows][n] sketch logits (hi, lo) by L index
+    float2* th = nullptr;           // [rows][n] exact logits by H index
+    float* wl = nullptr;            // [rows][n] sketch weights by L index
+    RowState* rows = nullptr;       // [rows]
+    unsigned long long* keys = nullptr;  // [rows][npow2] gain keys (full-row path)
+    int32_t* mark = nullptr;        // [rows][n] generation tag: L index made exact
+    int32_t* elist = nullptr;       // [rows][n] tokens made exact
+    uint32_t* ubits = nullptr;      // [max_batch][Hkv][n/32 + 1] union bitmap
+    int32_t* ulist = nullptr;       // [max_batch][Hkv][n] fetched union, ascending tokens
+    int32_t* ucount = nullptr;      // [max_batch][Hkv]
+    void* staging = nullptr;        // [max_batch][Hkv][n][2][d] fetched rows
+    float* part = nullptr;          // [rows][nsplit][d + 2] attention partials
+    int nsplit = 16;
+
+    // per-decode small arrays
+    int32_t* d_slot_n = nullptr;    // [max_batch] n of each row set's slot
+    int last_B = 0;
+    int last_layer = -1;
+    std::vector<int> last_seq;
+    std::vector<int> last_n;
+
+    Slot& slot(int layer, int seq) { return slots[(size_t)layer * cfg.n_seqs + seq]; }
+};
+
+// Slot pointers for the decode kernels (device-side copy, one entry per b).
+struct SlotView {
+    int n;
+    int pad;
+    const float* r;
+    const uint8_t* flags;
+    const int32_t* lpos;
+    const int32_t* ltok;
+    const float* rl;
+    const int32_t* rtok;
+    const int32_t* hslot;
+    const int32_t* counts;
+    const void* kvres;
+    const int64_t* res_off;
+    const void* kv_host;
+    const int8_t* codes8;
+    const float* scale8;
+    const uint64_t* codes2;
+    const __half* zero2;
+    const __half* scale2;
+    const int32_t* pairs;
+    const void* kexact;
+};
+
+verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const void* kv_host, const void* kv_dev,
+                           const float* obs_q, int W, const float* tau, cudaStream_t st);
+verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, const float* q, double eps,
+                         double delta, float* out, cudaStream_t st);
+void free_slot(Slot& s);
+
+}  // namespace verkv
+
+#define VK_CUDA(call)                                                                        \
+    do {                                                                                     \
+        cudaError_t e_ = (call);                                                             \
+        if (e_ != cudaSuccess) {                                                             \
+            ctx.err = std::string(#call) + ": " + cudaGetErrorString(e_);                    \
+            return e_ == cudaErrorMemoryAllocation ? VERKV_ENOMEM : VERKV_ECUDA;            \
+        }                                                                                    \
+    } while (0)
+
+#define VK_LAUNCH_CHECK()                                                                    \
+    do {                                                                                     \
+        cudaError_t e_ = cudaGetLastError();                                                 \
+        if (e_ != cudaSuccess) {                                                             \
+            ctx.err = std::string("kernel launch: ") + cudaGetErrorString(e_);               \
+            return VERKV_ECUDA;                                                              \
+        }                                                                                    \
+        ++ctx.last_launches;                                                                 \
+    } while (0)
