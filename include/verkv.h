@@ -210,6 +210,17 @@ verkv_status verkv_get_row_weights(verkv_ctx* ctx, int32_t b, int32_t h, float* 
 /* Number of kernels the last verkv_decode / verkv_compress enqueued. */
 int32_t verkv_last_launch_count(const verkv_ctx* ctx);
 
+/* Per-kernel timing (the per-phase breakdown of a decode step).  When enabled, every later
+ * verkv_decode / verkv_compress records a CUDA event on its stream before its first kernel and
+ * after each kernel it launches; no host synchronisation is added.  Records accumulate across calls
+ * (up to 4096 kernels) until verkv_get_kernel_times, which synchronises on the last event, returns
+ * the kernel names (static strings) and the device milliseconds of each launch (for compress these
+ * include host-side gaps between launches), and clears the record.  `count` receives the number of
+ * records; at most `cap` are written.  Enabling clears the record. */
+verkv_status verkv_set_kernel_timing(verkv_ctx* ctx, int32_t enable);
+verkv_status verkv_get_kernel_times(verkv_ctx* ctx, const char** names, float* ms, int32_t cap, int32_t* count,
+                                    verkv_stream stream);
+
 const char* verkv_status_str(verkv_status s);
 const char* verkv_last_error(const verkv_ctx* ctx);
 

@@ -100,6 +100,10 @@ def lib():
     L.verkv_get_row_weights.restype = st
     L.verkv_last_launch_count.argtypes = [P]
     L.verkv_last_launch_count.restype = i32
+    L.verkv_set_kernel_timing.argtypes = [P, i32]
+    L.verkv_set_kernel_timing.restype = st
+    L.verkv_get_kernel_times.argtypes = [P, P, P, i32, P, P]
+    L.verkv_get_kernel_times.restype = st
     L.verkv_status_str.argtypes = [st]
     L.verkv_status_str.restype = ctypes.c_char_p
     L.verkv_last_error.argtypes = [P]
@@ -179,6 +183,18 @@ class VerKV:
 
     def last_launch_count(self) -> int:
         return lib().verkv_last_launch_count(self.h)
+
+    def set_kernel_timing(self, enable: bool):
+        self._check(lib().verkv_set_kernel_timing(self.h, 1 if enable else 0))
+
+    def kernel_times(self, stream=None):
+        """[(kernel name, ms)] of every kernel launched by the timed calls since the last read."""
+        cap = 4096
+        names = (ctypes.c_char_p * cap)()
+        ms = (ctypes.c_float * cap)()
+        cnt = ctypes.c_int32()
+        self._check(lib().verkv_get_kernel_times(self.h, names, ms, cap, ctypes.byref(cnt), _stream(stream)))
+        return [(names[i].decode(), float(ms[i])) for i in range(min(cnt.value, cap))]
 
     # -- inspection
     def compress_state(self, layer, seq, kv_head, n, stream=None):

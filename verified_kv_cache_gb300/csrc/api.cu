@@ -139,6 +139,7 @@ verkv_status verkv_create(const verkv_config* cfg, verkv_ctx** out)
 verkv_status verkv_destroy(verkv_ctx* h)
 {
     if (!h) return VERKV_EINVAL;
+    for (cudaEvent_t e : h->c.ev) cudaEventDestroy(e);
     for (Slot& s : h->c.slots) free_slot(s);
     free_ws(h->c);
     delete h;
@@ -358,6 +359,43 @@ verkv_status verkv_get_row_weights(verkv_ctx* h, int32_t b, int32_t hq, float* w
     if (tokens && m > 0)
         VK_CUDA(cudaMemcpyAsync(tokens, s.ltok + (size_t)kv * s.n, sizeof(int32_t) * m, cudaMemcpyDeviceToHost, st));
     VK_CUDA(cudaStreamSynchronize(st));
+    return VERKV_OK;
+}
+
+verkv_status verkv_set_kernel_timing(verkv_ctx* h, int32_t enable)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (enable && ctx.ev.empty()) {
+        ctx.ev.resize(Ctx::kMaxTimed + 1);
+        for (cudaEvent_t& e : ctx.ev) VK_CUDA(cudaEventCreate(&e));
+    }
+    ctx.timing = enable != 0;
+    ctx.n_ev = 0;
+    ctx.ev_prev = -1;
+    ctx.ev_name.clear();
+    ctx.ev_from.clear();
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_kernel_times(verkv_ctx* h, const char** names, float* ms, int32_t cap, int32_t* count,
+                                    verkv_stream stream)
+{
+    if (!h || !count) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    const int n = (int)ctx.ev_name.size();
+    *count = n;
+    (void)stream;
+    if (n > 0) VK_CUDA(cudaEventSynchronize(ctx.ev[ctx.n_ev - 1]));
+    for (int i = 0; i < n && i < cap; ++i) {
+        if (names) names[i] = ctx.ev_name[i];
+        // entry i ends at the event recorded right after its launch: the i-th non-begin event
+        if (ms) VK_CUDA(cudaEventElapsedTime(&ms[i], ctx.ev[ctx.ev_from[i]], ctx.ev[ctx.ev_from[i] + 1]));
+    }
+    ctx.n_ev = 0;
+    ctx.ev_prev = -1;
+    ctx.ev_name.clear();
+    ctx.ev_from.clear();
     return VERKV_OK;
 }
 

@@ -484,7 +484,7 @@ verkv_status run_scores(Ctx& ctx, Slot& s, const T* kv, int n, const float* obs_
     dim3 g1((n + 255) / 256, Hkv);
     if (!obs_q) {
         tau_finish_kernel<<<g1, 256, 0, st>>>(s.tau, tau_in, nullptr, n, cfg.n_sink, cfg.n_local);
-        VK_LAUNCH_CHECK();
+        VK_LAUNCHED("tau_finish");
         return VERKV_OK;
     }
     const int R = ctx.G * W;
@@ -508,14 +508,14 @@ verkv_status run_scores(Ctx& ctx, Slot& s, const T* kv, int n, const float* obs_
     const float scale = (float)(1.0 / std::sqrt((double)kHeadDim));
     dim3 gt(ntiles, Hkv);
     tau_tile_kernel<T, 0><<<gt, 256, smem, st>>>(kv, n, R, ctx.G, W, obs_q, scale, part, nullptr, nullptr, nullptr);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("tau_tile");
     dim3 br(32, 8);
     tau_rowstat_kernel<<<(Hkv * R + 7) / 8, br, 0, st>>>(part, ntiles, rowstat, Hkv * R);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("tau_rowstat");
     tau_tile_kernel<T, 1><<<gt, 256, smem, st>>>(kv, n, R, ctx.G, W, obs_q, scale, nullptr, rowstat, tau_raw, tau_max);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("tau_tile");
     tau_finish_kernel<<<g1, 256, 0, st>>>(s.tau, tau_raw, tau_max, n, cfg.n_sink, cfg.n_local);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("tau_finish");
     VK_CUDA(cudaFreeAsync(part, st));
     VK_CUDA(cudaFreeAsync(rowstat, st));
     VK_CUDA(cudaFreeAsync(tau_raw, st));
@@ -531,23 +531,23 @@ verkv_status run_sketch(Ctx& ctx, Slot& s, const T* kv, int n, cudaStream_t st)
     if (cfg.sketch == VERKV_SKETCH_INT8) {
         const int64_t toks = (int64_t)Hkv * n;
         sketch_int8_kernel<T><<<(unsigned)((toks + 7) / 8), 256, 0, st>>>(kv, n, Hkv, s.codes8, s.scale8);
-        VK_LAUNCH_CHECK();
+        VK_LAUNCHED("sketch_int8");
     } else if (cfg.sketch == VERKV_SKETCH_2BIT) {
         VK_CUDA(cudaMemsetAsync(s.energy, 0, sizeof(double) * Hkv * (kHeadDim / 2), st));
         const int tpb = 256;
         pair_energy_kernel<T><<<dim3((n + tpb - 1) / tpb, Hkv), kHeadDim, 0, st>>>(kv, n, tpb, s.energy);
-        VK_LAUNCH_CHECK();
+        VK_LAUNCHED("pair_energy");
         select_pairs_kernel<<<Hkv, kHeadDim / 2, 0, st>>>(s.energy, s.pairs);
-        VK_LAUNCH_CHECK();
+        VK_LAUNCHED("select_pairs");
         const int ngroups = (n + cfg.sketch_group - 1) / cfg.sketch_group;
         sketch_2bit_kernel<T><<<dim3(ngroups, Hkv), 32, 0, st>>>(kv, n, cfg.sketch_group, s.pairs, s.codes2, s.zero2,
                                                                 s.scale2);
-        VK_LAUNCH_CHECK();
+        VK_LAUNCHED("sketch_2bit");
     } else {
         const int64_t rows = (int64_t)Hkv * n;
         copy_keys_kernel<T><<<(unsigned)((rows * kHeadDim + 255) / 256), 256, 0, st>>>(
             kv, rows, reinterpret_cast<T*>(s.kexact));
-        VK_LAUNCH_CHECK();
+        VK_LAUNCHED("copy_keys");
     }
     return VERKV_OK;
 }
@@ -599,6 +599,7 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
         VK_CUDA(cudaMalloc(&s.kexact, hn * kHeadDim * ctx.elt));
     }
     const void* kv = kv_dev ? kv_dev : kv_host;
+    VK_TIMING_BEGIN();
     verkv_status rc;
     if (cfg.kv_dtype == VERKV_DTYPE_BF16)
         rc = run_scores<__nv_bfloat16>(ctx, s, (const __nv_bfloat16*)kv, n, obs_q, W, tau, st);
@@ -609,12 +610,12 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
     VK_CUDA(cudaMemsetAsync(s.capped + Hkv, 0, sizeof(int32_t), st));
     waterfill_kernel<<<Hkv, 1024, 0, st>>>(s.tau, n, cfg.n_sink, cfg.n_local, cfg.eta * (double)n, s.c, s.capped,
                                           s.capped + Hkv);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("waterfill");
     sample_kernel<<<dim3((n + 255) / 256, Hkv), 256, 0, st>>>(s.tau, s.c, n, cfg.n_sink, cfg.n_local, cfg.seed, layer,
                                                             seq, s.r, s.flags);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("sample");
     compact_kernel<<<Hkv, 1024, 0, st>>>(s.flags, s.r, n, s.lpos, s.ltok, s.rl, s.rtok, s.hslot, s.counts);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("compact");
 
     std::vector<int32_t> counts((size_t)Hkv * 4), capped((size_t)Hkv + 1);
     std::vector<double> cval(Hkv);
@@ -642,7 +643,7 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
     if (max_res > 0) {
         gather_resident_kernel<<<dim3((max_res + 7) / 8, Hkv), 256, 0, st>>>(
             (const unsigned char*)kv, n, row_bytes, s.rtok, s.counts, s.res_off, (unsigned char*)s.kvres);
-        VK_LAUNCH_CHECK();
+        VK_LAUNCHED("gather_resident");
     }
     if (cfg.kv_dtype == VERKV_DTYPE_BF16)
         rc = run_sketch<__nv_bfloat16>(ctx, s, (const __nv_bfloat16*)kv, n, st);

@@ -1017,8 +1017,9 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
 {
     const verkv_config& cfg = ctx.cfg;
     const int rowsN = B * a.Hq;
+    VK_TIMING_BEGIN();
     init_rows_kernel<<<(rowsN + 127) / 128, 128, 0, st>>>(ctx.rows, views, a, B);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("init_rows");
     const dim3 gs((max_n + kTile - 1) / kTile, B * a.Hkv);
     if (cfg.sketch == VERKV_SKETCH_INT8)
         score_int8_kernel<G><<<gs, kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl);
@@ -1026,34 +1027,34 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         score_2bit_kernel<G><<<gs, kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl);
     else
         score_exact_kernel<T, G><<<gs, kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("score_sketch");
     if (max_nh > 0) {
         score_h_kernel<T, G><<<dim3((max_nh + kTile - 1) / kTile, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows,
                                                                                             ctx.th);
-        VK_LAUNCH_CHECK();
+        VK_LAUNCHED("score_h");
     }
     const int wmax = std::max(max_nl, max_nh);
     weights_kernel<<<dim3(std::max(1, (wmax + 255) / 256), rowsN), 256, 0, st>>>(views, a, ctx.rows, ctx.tl, ctx.th,
                                                                                 ctx.wl);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("weights");
     beta_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("beta");
     const size_t sel_smem = sizeof(unsigned long long) * kSelWidth;
     select_kernel<<<rowsN, 1024, sel_smem, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("select");
     fallback_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("fallback");
     union_kernel<<<B * a.Hkv, 1024, 0, st>>>(views, a, ctx.rows, ctx.elist, ctx.ubits, ctx.ulist, ctx.ucount);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("union");
     const int row_bytes = (int)(2 * kHeadDim * sizeof(T));
     gather_kernel<<<dim3(B * a.Hkv, 16), 256, 0, st>>>(views, a, ctx.ulist, ctx.ucount,
                                                        (unsigned char*)ctx.staging, row_bytes);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("gather");
     attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), 128, 0, st>>>(views, q, a, ctx.rows, ctx.wl, ctx.mark, ctx.ulist,
                                                                  ctx.ucount, (const T*)ctx.staging, ctx.part);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("attn");
     merge_kernel<<<rowsN, kHeadDim, 0, st>>>(a, ctx.part, out);
-    VK_LAUNCH_CHECK();
+    VK_LAUNCHED("merge");
     return VERKV_OK;
 }
 

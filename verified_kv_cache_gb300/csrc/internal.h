@@ -74,7 +74,17 @@ struct Ctx {
     std::vector<Slot> slots;        // [n_layers * n_seqs]
     std::string err;
     int last_launches = 0;
-    int gen = 0;                    // decode generation tag
+
+    // optional per-kernel timing: events recorded between launches on the call's stream, kept
+    // across calls until read (verkv_get_kernel_times)
+    static constexpr int kMaxTimed = 4096;
+    bool timing = false;
+    std::vector<cudaEvent_t> ev;          // pool of kMaxTimed + 1 events
+    std::vector<const char*> ev_name;     // entry i: kernel name
+    std::vector<int> ev_from;             // entry i: event index before the kernel
+    int n_ev = 0;                         // events used
+    int ev_prev = -1;                     // event recorded last
+    int gen = 0;                          // decode generation tag
 
     // decode workspace, sized for max_batch rows sets
     int ws_rows = 0;                // max_batch * n_q_heads
@@ -145,12 +155,29 @@ void free_slot(Slot& s);
         }                                                                                    \
     } while (0)
 
-#define VK_LAUNCH_CHECK()                                                                    \
+// After every kernel launch: check the launch, count it, and (when timing) record an event.
+#define VK_LAUNCHED(name)                                                                    \
     do {                                                                                     \
         cudaError_t e_ = cudaGetLastError();                                                 \
         if (e_ != cudaSuccess) {                                                             \
-            ctx.err = std::string("kernel launch: ") + cudaGetErrorString(e_);               \
+            ctx.err = std::string("kernel launch (") + (name) + "): " + cudaGetErrorString(e_); \
             return VERKV_ECUDA;                                                              \
         }                                                                                    \
         ++ctx.last_launches;                                                                 \
+        if (ctx.timing && ctx.ev_prev >= 0 && ctx.n_ev < verkv::Ctx::kMaxTimed) {            \
+            ctx.ev_name.push_back(name);                                                     \
+            ctx.ev_from.push_back(ctx.ev_prev);                                              \
+            cudaEventRecord(ctx.ev[ctx.n_ev], st);                                           \
+            ctx.ev_prev = ctx.n_ev++;                                                        \
+        }                                                                                    \
+    } while (0)
+
+// Start of a timed call.
+#define VK_TIMING_BEGIN()                                                                    \
+    do {                                                                                     \
+        ctx.ev_prev = -1;                                                                    \
+        if (ctx.timing && ctx.n_ev < verkv::Ctx::kMaxTimed) {                                \
+            cudaEventRecord(ctx.ev[ctx.n_ev], st);                                           \
+            ctx.ev_prev = ctx.n_ev++;                                                        \
+        }                                                                                    \
     } while (0)
