@@ -177,6 +177,7 @@ def run_verkv(args):
         one_step([])
     torch.cuda.synchronize()
     # fetch statistics of the workload (one untimed decode sweep with traces)
+    ctx.compress(0, 0, w.n, kv_host, kv_dev, obs, W, None, st)
     fetch_frac, no_fetch, union_rows, kstars = [], 0, [], []
     for s in range(S):
         ctx.decode(0, [0], q_dev[s], w.eps, w.delta, out[s], st)
