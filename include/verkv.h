@@ -221,6 +221,28 @@ verkv_status verkv_set_kernel_timing(verkv_ctx* ctx, int32_t enable);
 verkv_status verkv_get_kernel_times(verkv_ctx* ctx, const char** names, float* ms, int32_t cap, int32_t* count,
                                     verkv_stream stream);
 
+/*
+ * Allocation-free certificate for one query row (no counterpart in the paper: it is the decision
+ * of verkv_decode for a single row -- the beta fixed point, eq. (7), the gains, the full ranking and
+ * k* -- packaged for callers that cannot allocate device memory, e.g. code inside a stream capture
+ * whose graph must not own allocations, or under a fixed external memory budget).
+ *   w_hat   device [n_l] fp32 sketch weights of the row's L tokens (any common scale),
+ *   r       device [n_l] fp32 inclusion probabilities of those tokens (0 < r < 1),
+ *   D       the certificate denominator in the same scale (sum_H w + sum_L w_hat), > 0,
+ *   scalars device [4] output: beta, eps_hat, beta(L), V(L),
+ *   kstar   device [1] output: k* (0 when eps_hat < eps),
+ *   exact   device [n_l] output: the first k* entries are the indices (into w_hat) of L_g[:k*].
+ * Creates no context and calls no allocator.  Scratch is a library-wide static device array of
+ * VERKV_STATIC_MAX_L 64-bit keys (512 KiB, held by every GPU that loads the library until exit):
+ * n_l > VERKV_STATIC_MAX_L returns VERKV_EINVAL.  All calls share that array, so calls whose kernels
+ * overlap on a GPU (different streams, or several host threads) race and must be serialised by the
+ * caller.  The first call on each device looks up the array's device address (with that device
+ * current) and should be made before any stream capture.  Asynchronous on `stream`. */
+#define VERKV_STATIC_MAX_L 65536
+verkv_status verkv_certify_row_static(const float* w_hat, const float* r, int32_t n_l, double D, double eps,
+                                      double delta, double* scalars, int32_t* kstar, int32_t* exact,
+                                      verkv_stream stream);
+
 const char* verkv_status_str(verkv_status s);
 const char* verkv_last_error(const verkv_ctx* ctx);
 

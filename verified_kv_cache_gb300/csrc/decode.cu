@@ -1149,3 +1149,201 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
 }
 
 }  // namespace verkv
+
+// ================================================================================================
+// Allocation-free variant of the per-row decision (the beta solve, eq. (7), the gains, the full-row
+// ranking and k* of the full-row path above) for callers that cannot allocate device memory: code
+// running where cudaMalloc is unavailable or forbidden (inside a stream capture whose graph must not
+// own allocations, under an external memory pool or budget, in a real-time loop).  Its only scratch
+// is the file-scope array below, which every GPU that loads the library holds until the process
+// exits; all calls share it.
+// ================================================================================================
+#include <mutex>
+
+namespace verkv {
+namespace {
+
+constexpr int kStaticMaxL = 65536;  // largest |L| the allocation-free entry point accepts
+__device__ __align__(256) unsigned long long g_static_keys[kStaticMaxL];
+
+__global__ void __launch_bounds__(1024) certify_static_kernel(const float* __restrict__ w, const float* __restrict__ rr,
+                                                              int nl, double D, float eps_f, double eps, double ld,
+                                                              unsigned long long* __restrict__ key,
+                                                              double* __restrict__ out_scalars,
+                                                              int32_t* __restrict__ out_kstar,
+                                                              int32_t* __restrict__ out_exact)
+{
+    __shared__ ff red[32];
+    __shared__ float redf[32];
+    __shared__ int redi[32];
+    __shared__ ScanVal shs[32];
+    __shared__ ScanVal chunk_total;
+    __shared__ int found;
+    // top of the beta bracket: sum_L w (1 - r)
+    ff al = {0.f, 0.f};
+    for (int j = threadIdx.x; j < nl; j += blockDim.x) al = ff_add(al, two_prod(w[j], __fsub_rn(1.0f, rr[j])));
+    al = block_sum_ff(al, red);
+    double lo = 0.0, hi = ff_to_double(al), theta = hi;
+    // safeguarded Newton on G(beta) = beta (1 + R) - A - W (Definition 2's fixed point)
+    for (int it = 0; it < 200 && nl > 0; ++it) {
+        ff A = {0.f, 0.f}, Wf = {0.f, 0.f}, Rs = {0.f, 0.f};
+        for (int j = threadIdx.x; j < nl; j += blockDim.x) {
+            const float wj = w[j], rj = rr[j];
+            if (!(wj > 0.f)) continue;
+            const float a1 = __fmul_rn(wj, __fsub_rn(1.0f, rj));
+            const float ga = __fdiv_rn(a1, rj);
+            if (theta <= (double)a1) A = ff_add_f(A, a1);
+            else if (theta < (double)ga) {
+                Wf = ff_add_f(Wf, wj);
+                Rs = ff_add_f(Rs, __fdiv_rn(rj, __fsub_rn(1.0f, rj)));
+            }
+        }
+        A = block_sum_ff(A, red);
+        Wf = block_sum_ff(Wf, red);
+        Rs = block_sum_ff(Rs, red);
+        const double Ad = ff_to_double(A), Wd = ff_to_double(Wf), Rd = ff_to_double(Rs);
+        const double g = theta * (1.0 + Rd) - Ad - Wd;
+        if (g >= 0.0) hi = fmin(hi, theta); else lo = fmax(lo, theta);
+        double nt = (Ad + Wd) / (1.0 + Rd);
+        if (nt == theta) break;
+        if (!(nt > lo && nt < hi)) nt = 0.5 * (lo + hi);
+        if (nt == theta || hi - lo <= 1e-16 * hi) { theta = nt; break; }
+        theta = nt;
+    }
+    const double beta = nl > 0 ? theta : 0.0;
+    const float bf = (float)beta;
+    // eq. (7) sums and the two largest b_i
+    ff sa = {0.f, 0.f}, sv = {0.f, 0.f};
+    float b1 = 0.f, b2 = 0.f;
+    int arg = 0x7fffffff;
+    for (int j = threadIdx.x; j < nl; j += blockDim.x) {
+        const Coef c = coef_of(w[j], rr[j], bf);
+        sa = ff_add_f(sa, c.a);
+        sv = ff_add_f(sv, c.v);
+        if (c.b > b1 || (c.b == b1 && j < arg)) { b2 = b1; b1 = c.b; arg = j; }
+        else if (c.b > b2) b2 = c.b;
+    }
+    sa = block_sum_ff(sa, red);
+    sv = block_sum_ff(sv, red);
+    const float B1 = block_max(b1, redf);
+    int cand = (b1 == B1) ? arg : 0x7fffffff;
+    __syncthreads();
+    for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+    if ((threadIdx.x & 31) == 0) redi[threadIdx.x >> 5] = cand;
+    __syncthreads();
+    cand = (threadIdx.x & 31) < (blockDim.x >> 5) ? redi[threadIdx.x & 31] : 0x7fffffff;
+    for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+    const int ARG = cand;
+    const float B2 = block_max((arg == ARG) ? b2 : b1, redf);
+    const double SA = ff_to_double(sa), SV = ff_to_double(sv);
+    const double t = (double)B1 * ld / 3.0;
+    const double eh = nl > 0 ? (SA + t + sqrt(t * t + 2.0 * SV * ld)) / D : 0.0;
+    const bool no_fetch = eh < eps;
+    if (threadIdx.x == 0) {
+        out_scalars[0] = beta;
+        out_scalars[1] = eh;
+        out_scalars[2] = SA;
+        out_scalars[3] = SV;
+    }
+    if (no_fetch) {
+        if (threadIdx.x == 0) *out_kstar = 0;
+        return;
+    }
+    // gains (eq. (9)) as sort keys: (g descending, index ascending)
+    GainParams gp;
+    {
+        const double t2 = (nl > 1 ? (double)B2 : 0.0) * ld / 3.0;
+        const double Aq = t * t + 2.0 * SV * ld;
+        gp.t = (float)t;
+        gp.tm2 = (float)t2;
+        gp.A = (float)Aq;
+        gp.sqrtA = (float)sqrt(Aq);
+        gp.ld2 = (float)(2.0 * ld);
+    }
+    int P = 1;
+    while (P < nl) P <<= 1;
+    for (int j = threadIdx.x; j < P; j += blockDim.x) {
+        if (j < nl) {
+            const Coef c = coef_of(w[j], rr[j], bf);
+            key[j] = gain_key(gain_num(c, j, ARG, gp), j);
+        } else {
+            key[j] = ~0ull;  // padding: every call rewrites [0, P)
+        }
+    }
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
+                const int a0 = 2 * i - (i & (stride - 1));
+                const int a1 = a0 + stride;
+                const bool up = ((a0 & size) == 0);
+                const unsigned long long x = key[a0], y = key[a1];
+                if ((x > y) == up) { key[a0] = y; key[a1] = x; }
+            }
+            __syncthreads();
+        }
+    }
+    // eq. (10): residual certificates from the end of the order backwards
+    const float ldf = (float)ld, Df = (float)D;
+    ScanVal carry = {{0.f, 0.f}, {0.f, 0.f}, 0.f};
+    if (threadIdx.x == 0) found = -1;
+    __syncthreads();
+    int kstar = -1;
+    for (int c1 = nl; c1 > 0; c1 -= blockDim.x) {
+        const int c0 = max(0, c1 - (int)blockDim.x);
+        const int p = c0 + threadIdx.x;
+        ScanVal mine = {{0.f, 0.f}, {0.f, 0.f}, 0.f};
+        if (p < c1) {
+            const int j = (int)(key[p] & 0xffffffffu);
+            const Coef c = coef_of(w[j], rr[j], bf);
+            mine = ScanVal{{c.a, 0.f}, {c.v, 0.f}, c.b};
+        }
+        const ScanVal after = block_suffix_exclusive(mine, shs);
+        const ScanVal own = scan_combine(mine, after);
+        const ScanVal incl = scan_combine(own, carry);
+        if (p < c1 && p >= 1 && !(cert_f(incl.a.hi + incl.a.lo, incl.v.hi + incl.v.lo, incl.b, ldf, Df) < eps_f))
+            atomicMax(&found, p);
+        if (threadIdx.x == 0) chunk_total = own;
+        __syncthreads();
+        if (found >= 0) { kstar = found + 1; break; }
+        carry = scan_combine(carry, chunk_total);
+        __syncthreads();
+    }
+    if (kstar < 1) kstar = 1;
+    for (int p = threadIdx.x; p < kstar; p += blockDim.x) out_exact[p] = (int32_t)(key[p] & 0xffffffffu);
+    if (threadIdx.x == 0) *out_kstar = kstar;
+}
+
+std::mutex g_static_mu;
+void* g_static_ptr[256] = {};
+
+}  // namespace
+}  // namespace verkv
+
+extern "C" verkv_status verkv_certify_row_static(const float* w_hat, const float* r, int32_t n_l, double D, double eps,
+                                                 double delta, double* scalars, int32_t* kstar, int32_t* exact,
+                                                 verkv_stream stream)
+{
+    using namespace verkv;
+    if (n_l < 0 || n_l > kStaticMaxL) return VERKV_EINVAL;  // beyond the static scratch
+    if (!(eps >= 0.0) || !std::isfinite(eps) || !(delta > 0.0 && delta < 1.0) || !(D > 0.0)) return VERKV_EINVAL;
+    if (!scalars || !kstar || (n_l > 0 && (!w_hat || !r || !exact))) return VERKV_EINVAL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return VERKV_ECUDA;
+    void* ptr = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_static_mu);
+        if (!g_static_ptr[dev]) {
+            // the array's host-side name is only a stand-in: its device address comes from the runtime
+            if (cudaGetSymbolAddress(&g_static_ptr[dev], g_static_keys) != cudaSuccess) {
+                g_static_ptr[dev] = nullptr;
+                return VERKV_ECUDA;
+            }
+        }
+        ptr = g_static_ptr[dev];
+    }
+    certify_static_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(
+        w_hat, r, n_l, D, (float)eps, eps, std::log(2.0 / delta), reinterpret_cast<unsigned long long*>(ptr), scalars,
+        kstar, exact);
+    return cudaGetLastError() == cudaSuccess ? VERKV_OK : VERKV_ECUDA;
+}
