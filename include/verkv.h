@@ -107,6 +107,9 @@ typedef struct {
     int32_t no_fetch;      /* eps_hat < eps (Algorithm 2, line 3)                              */
     int32_t fallback;      /* k* was beyond the on-chip candidate width: full-row path used   */
     int32_t n_fetch;       /* |L_g[:k*] \ S|, tokens of this row read from the host            */
+    int32_t beta_iters;    /* passes the beta solve took                                       */
+    int32_t sel_passes;    /* radix-select passes of the on-chip ranking                       */
+    uint32_t phase_ns[6];  /* on-chip decision: ns in weights, beta, eq. (7), gain keys, k* search, exact set */
     int32_t pad;
 } verkv_row_trace;
 

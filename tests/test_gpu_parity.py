@@ -200,15 +200,32 @@ def test_batch_of_sequences_with_different_lengths():
     ctx.close()
 
 
-def test_full_row_path_when_kstar_exceeds_the_on_chip_width():
-    """Flat attention and a tight tolerance: k* is beyond the 4096 candidates ranked on chip, so the
-    full-row path runs, and it matches the oracle."""
+def test_large_kstar_on_the_cluster_path():
+    """Flat attention and a tight tolerance: k* runs into the thousands (well past any fixed candidate
+    width), decided by the cluster kernel's radix search, and matches the oracle."""
     w = small_case("int8", n=20000, steps=1, query_mode="random", eta=1 / 8)
     w.queries *= 0.3
     ctx = make_lib_ctx(w)
     gc = GpuCase(w, ctx)
     tau, stats, osl = _compress_both(w, gc)
     eps = 0.002
+    gc.decode(w.queries[0], eps, 0.05)
+    trace = ctx.decode_trace(w.n_q)
+    assert max(t["kstar"] for t in trace) > 8192, [t["kstar"] for t in trace]
+    _decode_parity(w, gc, osl, eps, 0.05, steps=[0])
+    ctx.close()
+
+
+def test_full_row_path_for_long_rows():
+    """|L| above the on-chip capacity of the cluster kernel (65536 per row) uses the multi-kernel path:
+    on-chip ranking of 4096 candidates and, when k* lies beyond them, the full-row sort."""
+    w = small_case("int8", n=72000, steps=1, query_mode="random", eta=1 / 16, n_kv=2, n_q=4)
+    w.queries *= 0.3
+    ctx = make_lib_ctx(w)
+    gc = GpuCase(w, ctx)
+    tau, stats, osl = _compress_both(w, gc)
+    assert max(s["n_l"] for s in stats) > 65536
+    eps = 0.005
     gc.decode(w.queries[0], eps, 0.05)
     trace = ctx.decode_trace(w.n_q)
     assert any(t["fallback"] for t in trace), [t["kstar"] for t in trace]

@@ -49,10 +49,13 @@ class RowTrace(ctypes.Structure):
                 ("sum_a", ctypes.c_double), ("V", ctypes.c_double), ("b", ctypes.c_double),
                 ("eps_hat", ctypes.c_double), ("n_l", ctypes.c_int32), ("kstar", ctypes.c_int32),
                 ("no_fetch", ctypes.c_int32), ("fallback", ctypes.c_int32), ("n_fetch", ctypes.c_int32),
+                ("beta_iters", ctypes.c_int32), ("sel_passes", ctypes.c_int32), ("phase_ns", ctypes.c_uint32 * 6),
                 ("pad", ctypes.c_int32)]
 
     def as_dict(self):
-        return {k: getattr(self, k) for k, _ in self._fields_ if k != "pad"}
+        d = {k: getattr(self, k) for k, _ in self._fields_ if k not in ("pad", "phase_ns")}
+        d["phase_ns"] = list(self.phase_ns)
+        return d
 
 
 _lib = None

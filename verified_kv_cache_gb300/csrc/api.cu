@@ -292,6 +292,9 @@ verkv_status verkv_get_decode_trace(verkv_ctx* h, verkv_row_trace* out, int32_t 
         t.no_fetch = s.no_fetch;
         t.fallback = s.fallback;
         t.n_fetch = s.n_fetch;
+        t.beta_iters = s.beta_iters;
+        t.sel_passes = s.sel_passes;
+        for (int k = 0; k < 6; ++k) t.phase_ns[k] = s.phase_ns[k];
     }
     return VERKV_OK;
 }

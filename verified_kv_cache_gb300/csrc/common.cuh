@@ -229,6 +229,13 @@ __device__ __forceinline__ double u128_to_double_rn(uint64_t hi, uint64_t lo)
     return ldexp(__ull2double_rn(top), bits_hi);
 }
 
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 __device__ __forceinline__ float tau_clamp(float t)
 {
     return t > kTauFloor ? (t < 1.0f ? t : 1.0f) : kTauFloor;

@@ -7,8 +7,12 @@
 #include <cmath>
 #include <cstring>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace verkv {
 
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const f
     }
 }
 
-// Exact logits of the tokens of H (resident keys), by H index.
+// Exact logits of the tokens of H (resident keys), by H index; one thread per (token, query head).
 template <typename T, int G>
 __global__ void __launch_bounds__(kTile) score_h_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
                                                         RowState* __restrict__ rows, float2* __restrict__ th)
@@ -286,30 +290,26 @@ __global__ void __launch_bounds__(kTile) score_h_kernel(Views views, const float
     const SlotView& V = views.v[b];
     const int n = V.n;
     const int nh = V.counts[kv * 4 + 0];
-    if (blockIdx.x * kTile >= nh) return;
+    if (blockIdx.x * (kTile / G) >= nh) return;
     for (int e = threadIdx.x; e < G * kHeadDim; e += blockDim.x)
         qs[e / kHeadDim][e % kHeadDim] = q[((int64_t)b * a.Hq + kv * G) * kHeadDim + e];
     __syncthreads();
-    const int k = blockIdx.x * kTile + threadIdx.x;
-    float mloc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
+    const int g = threadIdx.x % G;
+    const int k = blockIdx.x * (kTile / G) + threadIdx.x / G;
+    float mloc = -INFINITY;
     if (k < nh) {
         const int slot = V.hslot[(int64_t)kv * n + k];
         const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + slot) * 2 * kHeadDim;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const ff t = exact_logit<T>(qs[g], key, a.inv_sqrt_d);
-            const int row = row_of(b, kv * G + g, a.Hq);
-            th[(int64_t)row * a.ws_n + k] = make_float2(t.hi, t.lo);
-            mloc[g] = t.hi;
-        }
+        const ff t = exact_logit<T>(qs[g], key, a.inv_sqrt_d);
+        const int row = row_of(b, kv * G + g, a.Hq);
+        th[(int64_t)row * a.ws_n + k] = make_float2(t.hi, t.lo);
+        mloc = t.hi;
     }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float m = block_max(mloc[g], red);
-        if (threadIdx.x == 0 && m > -INFINITY) atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_ord, float_to_ordered(m));
-    }
+    // max per query head: lanes with the same g are G apart
+    for (int o = 16; o >= G; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if ((threadIdx.x & 31) < G && mloc > -INFINITY)
+        atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_ord, float_to_ordered(mloc));
+    (void)red;
 }
 
 // --------------------------------------------------------------------------------------------
@@ -756,7 +756,13 @@ __global__ void __launch_bounds__(1024) fallback_kernel(Views views, DecodeArgs 
     const float bf = (float)R.beta;
     int P = 1;
     while (P < nl) P <<= 1;
-    for (int p = nl + threadIdx.x; p < P; p += blockDim.x) key[p] = ~0ull;
+    {
+        const GainParams gp = gain_params(R, a.ldelta);
+        for (int j = threadIdx.x; j < P; j += blockDim.x) {
+            if (j < nl) key[j] = gain_key(gain_num(coef_of(w[j], rr[j], bf), j, R.b_arg, gp), j);
+            else key[j] = ~0ull;
+        }
+    }
     __syncthreads();
     for (int size = 2; size <= P; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -799,6 +805,568 @@ __global__ void __launch_bounds__(1024) fallback_kernel(Views views, DecodeArgs 
     if (kstar < 1) kstar = 1;
     if (threadIdx.x == 0) R.fallback = 1;
     emit_exact_set(key, kstar, row, V, kv, a, mark, elist, R, redi);
+}
+
+// --------------------------------------------------------------------------------------------
+// Fused decision for rows whose L fits on chip (|L| <= 8 x kDecideCap): one thread-block cluster
+// of C CTAs per query row.  CTA c keeps the L entries [c S, (c + 1) S) of the row (S = ceil(|L|/C))
+// in shared memory for every pass.  Sums are float-float per thread (or exact fixed point),
+// block-reduced, and combined in rank order across the cluster through distributed shared memory,
+// so all CTAs of a row take identical decisions.  Scalar double-precision work is done by one
+// thread per CTA and broadcast (FP64 throughput is low on this part).
+//   phase 0: w^ = exp(t^ - m) (also written to wl for the attention), r, gamma = w^(1-r)/r and
+//            rho = r/(1-r); D, sum w^, sum w^(1-r), sum rho.
+//   phase 1: Definition 2's fixed point by safeguarded Newton on G(beta) = beta (1 + R) - A - W,
+//            started above the root (four times the all-interior solution).
+//   phase 2: a_i, v_i, b_i; eq. (7); the no-fetch test (Algorithm 2, lines 2-5).
+//   phase 3: gain keys (eq. (9)) and k* (eq. (10)) by an MSD radix search over the keys: per
+//            8-bit digit, a cluster-wide histogram of counts, exact fixed-point sums of a_i and v_i
+//            and the max of b_i gives the residual certificate at every bin boundary, so the bin
+//            holding the k*-th key is found without sorting; the search stops once that bin holds
+//            one key.
+//   phase 4: E = L_g[:k*] = the keys up to the k*-th, written as marks and a token list.
+// --------------------------------------------------------------------------------------------
+constexpr int kDecideThreads = 1024;
+constexpr int kDecideCap = 8192;   // L entries per CTA
+constexpr int kDecideMaxCluster = 8;
+constexpr size_t kDecideSmem = (size_t)kDecideCap * (4 + 4 + 8 + 4);
+
+struct DecideSlot {
+    double v[8];
+    unsigned int cnt[256];
+    unsigned int pa[3][256], pv[3][256];  // 14-bit pieces of the fixed-point sums of a_i and v_i
+    unsigned int mb[256];
+};
+
+// Block-wide sums of N float-float values at once (two barriers); every thread gets the totals.
+template <int N>
+__device__ __forceinline__ void block_sum_ff_n(ff (&v)[N], ff* scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int k = 0; k < N; ++k) v[k] = ff_add(v[k], shfl_xor_ff(v[k], o));
+    __syncthreads();
+    if (lane == 0)
+#pragma unroll
+        for (int k = 0; k < N; ++k) scratch[warp * N + k] = v[k];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = lane < nw ? scratch[lane * N + k] : ff{0.f, 0.f};
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int k = 0; k < N; ++k) v[k] = ff_add(v[k], shfl_xor_ff(v[k], o));
+}
+
+__device__ __forceinline__ void cluster_combine(cg::cluster_group& cl, DecideSlot* slot, int parity, int nv,
+                                                double* out)
+{
+    // thread 0 of every CTA has written slot[parity].v[0..nv); sum them in rank order
+    cl.sync();
+    if (threadIdx.x < nv) {
+        double s = 0.0;
+        for (unsigned rk = 0; rk < cl.num_blocks(); ++rk) s += cl.map_shared_rank(slot, rk)[parity].v[threadIdx.x];
+        out[threadIdx.x] = s;
+    }
+    __syncthreads();
+}
+
+// Scalars of one row, computed by thread 0 of each CTA and broadcast through shared memory.
+struct DecideScalars {
+    double theta, lo, hi, D;
+    float th_up, th_dn;        // theta rounded up / down: alpha >= theta <=> alpha >= th_up, gamma > theta <=> gamma > th_dn
+    int done;
+    float bf;                  // beta in fp32
+    GainParams gp;
+    int arg, no_fetch;
+    float Df, ldf, sa_scale, sv_scale;  // fixed-point scales: a_i * sa_scale, v_i * sv_scale (totals ~2^40)
+    // radix search state
+    unsigned long long prefix, pmask;
+    int rem_cnt;                        // keys below the current prefix range (removed)
+    unsigned long long rest_a, rest_v;  // keys above the current prefix range (kept), fixed point
+    unsigned int rest_b;                // max b over them (ordered float bits)
+    int kstar, found;
+    unsigned long long kkey;            // the k*-th smallest key
+};
+
+__device__ __forceinline__ void set_theta(DecideScalars& sc, double th)
+{
+    sc.theta = th;
+    sc.th_up = __double2float_ru(th);
+    sc.th_dn = __double2float_rd(th);
+}
+
+__device__ __forceinline__ unsigned int fmax_bits(float x) { return __float_as_uint(fmaxf(x, 0.f)); }
+
+__global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, DecodeArgs a,
+                                                                   RowState* __restrict__ rows,
+                                                                   const float2* __restrict__ tl,
+                                                                   const float2* __restrict__ th,
+                                                                   float* __restrict__ wl,
+                                                                   int32_t* __restrict__ mark,
+                                                                   int32_t* __restrict__ elist)
+{
+    cg::cluster_group cl = cg::this_cluster();
+    const int C = (int)cl.num_blocks();
+    const int rank = (int)cl.block_rank();
+    const int row = blockIdx.x / C;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    // region A: w^, r (phases 0-2) -> a_i, v_i (phase 3); region B: gamma, rho -> keys; region C: b_i
+    float* sw = reinterpret_cast<float*>(dsm);
+    float* sr = sw + kDecideCap;
+    float* sg = sr + kDecideCap;
+    float* sp = sg + kDecideCap;
+    unsigned long long* skey = reinterpret_cast<unsigned long long*>(sg);
+    float* sb = sp + kDecideCap;
+    float* sa_ = sw;
+    float* sv_ = sr;
+    __shared__ DecideSlot slot[2];
+    __shared__ double bc[8];
+    __shared__ ff redff[32 * 4];
+    __shared__ float redf[32];
+    __shared__ int redi[32];
+    __shared__ DecideScalars sc;
+    __shared__ int wcnt[32];
+    __shared__ int tot_c[256];
+    __shared__ unsigned long long tot_a[256], tot_v[256];
+    __shared__ unsigned int tot_b[256];
+    const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int b = row / a.Hq, kv = (row % a.Hq) / a.G;
+    const SlotView& V = views.v[b];
+    RowState& R = rows[row];
+    const int nl = R.n_l, nh = R.n_h;
+    const int S = (nl + C - 1) / C;
+    const int j0 = min(nl, rank * S), j1 = min(nl, j0 + S), ns = j1 - j0;
+    const float m = ordered_to_float(R.m_ord);
+    const float* rl = V.rl + (int64_t)kv * V.n;
+    int parity = 0;
+    const bool timer = rank == 0 && tid == 0;
+    unsigned long long t_prev = timer ? global_ns() : 0ull;
+    auto stamp = [&](int k) {
+        if (timer) {
+            const unsigned long long t = global_ns();
+            R.phase_ns[k] = (unsigned)(t - t_prev);
+            t_prev = t;
+        }
+    };
+
+    // ---- phase 0: weights and the row totals
+    {
+        ff acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // D, sum w, sum alpha, sum rho
+        for (int i = tid; i < ns; i += T) {
+            const int j = j0 + i;
+            const float w = weight_of(tl[(int64_t)row * a.ws_n + j], m);
+            const float r = rl[j];
+            sw[i] = w;
+            sr[i] = r;
+            wl[(int64_t)row * a.ws_n + j] = w;
+            const float al = __fmul_rn(w, __fsub_rn(1.0f, r));
+            const float rho = __fdiv_rn(r, __fsub_rn(1.0f, r));
+            sg[i] = __fdiv_rn(al, r);
+            sp[i] = rho;
+            acc[0] = ff_add_f(acc[0], w);
+            acc[1] = ff_add_f(acc[1], w);
+            acc[2] = ff_add(acc[2], two_prod(w, __fsub_rn(1.0f, r)));
+            acc[3] = ff_add_f(acc[3], rho);
+        }
+        if (rank == 0)
+            for (int k = tid; k < nh; k += T) acc[0] = ff_add_f(acc[0], weight_of(th[(int64_t)row * a.ws_n + k], m));
+        block_sum_ff_n<4>(acc, redff);
+        if (tid == 0)
+            for (int k = 0; k < 4; ++k) slot[parity].v[k] = ff_to_double(acc[k]);
+    }
+    cluster_combine(cl, slot, parity, 4, bc);
+    parity ^= 1;
+    if (tid == 0) {
+        const double At = bc[2];
+        if (rank == 0) {
+            R.D = bc[0];
+            R.alpha_sum = At;
+        }
+        sc.D = bc[0];
+        sc.lo = 0.0;
+        sc.hi = At;
+        set_theta(sc, fmin(At, 4.0 * bc[1] / (1.0 + bc[3])));
+        sc.done = (nl == 0 || !(At > 0.0));
+    }
+    __syncthreads();
+    stamp(0);
+
+    // ---- phase 1: beta (Newton on the classes; thread 0 does the scalar update)
+    int iters = 0;
+    while (!sc.done) {
+        ++iters;
+        const float tu = sc.th_up, td = sc.th_dn;
+        ff acc[3] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // A, W, R
+        for (int i = tid; i < ns; i += T) {
+            const float wj = sw[i];
+            if (!(wj > 0.f)) continue;
+            const float al = __fmul_rn(wj, __fsub_rn(1.0f, sr[i]));
+            if (al >= tu) acc[0] = ff_add_f(acc[0], al);   // theta <= alpha: lambda = r
+            else if (sg[i] > td) {                           // theta < gamma: interior
+                acc[1] = ff_add_f(acc[1], wj);
+                acc[2] = ff_add_f(acc[2], sp[i]);
+            }
+        }
+        block_sum_ff_n<3>(acc, redff);
+        if (tid == 0)
+            for (int k = 0; k < 3; ++k) slot[parity].v[k] = ff_to_double(acc[k]);
+        cluster_combine(cl, slot, parity, 3, bc);
+        parity ^= 1;
+        if (tid == 0) {
+            const double theta = sc.theta;
+            const double Ad = bc[0], Wd = bc[1], Rd = bc[2];
+            const double g = theta * (1.0 + Rd) - Ad - Wd;
+            if (g >= 0.0) sc.hi = fmin(sc.hi, theta); else sc.lo = fmax(sc.lo, theta);
+            double nt = (Ad + Wd) / (1.0 + Rd);
+            if (nt == theta || iters >= 200) sc.done = 1;
+            else {
+                if (!(nt > sc.lo && nt < sc.hi)) nt = sc.lo > 0.0 ? sqrt(sc.lo * sc.hi) : 0.5 * (sc.lo + sc.hi);
+                if (nt == theta || sc.hi - sc.lo <= 1e-16 * sc.hi) sc.done = 1;
+                set_theta(sc, nt);
+            }
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const double beta = nl > 0 ? sc.theta : 0.0;
+        sc.theta = beta;
+        sc.bf = (float)beta;
+    }
+    __syncthreads();
+    const float bf = sc.bf;
+    stamp(1);
+
+    // ---- phase 2: eq. (7)
+    float b1 = 0.f, b2 = 0.f;
+    int arg = 0x7fffffff;
+    {
+        ff acc[2] = {{0.f, 0.f}, {0.f, 0.f}};
+        for (int i = tid; i < ns; i += T) {
+            const Coef c = coef_of(sw[i], sr[i], bf);
+            acc[0] = ff_add_f(acc[0], c.a);
+            acc[1] = ff_add_f(acc[1], c.v);
+            const int j = j0 + i;
+            if (c.b > b1 || (c.b == b1 && j < arg)) { b2 = b1; b1 = c.b; arg = j; }
+            else if (c.b > b2) b2 = c.b;
+        }
+        block_sum_ff_n<2>(acc, redff);
+        if (tid == 0) {
+            slot[parity].v[0] = ff_to_double(acc[0]);
+            slot[parity].v[1] = ff_to_double(acc[1]);
+        }
+    }
+    const float B1l = block_max(b1, redf);
+    int cnd = (b1 == B1l) ? arg : 0x7fffffff;
+    __syncthreads();
+    for (int o = 16; o > 0; o >>= 1) cnd = min(cnd, __shfl_xor_sync(0xffffffffu, cnd, o));
+    if (lane == 0) redi[warp] = cnd;
+    __syncthreads();
+    cnd = lane < (T >> 5) ? redi[lane] : 0x7fffffff;
+    for (int o = 16; o > 0; o >>= 1) cnd = min(cnd, __shfl_xor_sync(0xffffffffu, cnd, o));
+    const int ARGl = cnd;
+    const float B2l = block_max((arg == ARGl) ? b2 : b1, redf);
+    if (tid == 0) {
+        slot[parity].v[2] = (double)B1l;
+        slot[parity].v[3] = (double)B2l;
+        slot[parity].v[4] = (double)ARGl;
+    }
+    cluster_combine(cl, slot, parity, 2, bc);
+    if (tid == 0) {
+        // the two largest b across the cluster (lowest index among equal maxima)
+        float B1 = 0.f, B2 = 0.f;
+        int ARG = 0x7fffffff;
+        for (int rk = 0; rk < C; ++rk) {
+            const DecideSlot* rs = cl.map_shared_rank(slot, rk);
+            const float x1 = (float)rs[parity].v[2];
+            const int xa = (int)rs[parity].v[4];
+            if (x1 > B1 || (x1 == B1 && xa < ARG)) { B1 = x1; ARG = xa; }
+        }
+        for (int rk = 0; rk < C; ++rk) {
+            const DecideSlot* rs = cl.map_shared_rank(slot, rk);
+            B2 = fmaxf(B2, (int)rs[parity].v[4] == ARG ? (float)rs[parity].v[3] : (float)rs[parity].v[2]);
+        }
+        const double SA = bc[0], SV = bc[1], ld = a.ldelta;
+        const double t3 = (double)B1 * ld / 3.0;
+        const double eh = nl > 0 ? (SA + t3 + sqrt(t3 * t3 + 2.0 * SV * ld)) / sc.D : 0.0;
+        sc.no_fetch = (eh < a.eps) || nl == 0;
+        sc.arg = ARG;
+        const double t2 = (nl > 1 ? (double)B2 : 0.0) * ld / 3.0;
+        const double Aq = t3 * t3 + 2.0 * SV * ld;
+        sc.gp.t = (float)t3;
+        sc.gp.tm2 = (float)t2;
+        sc.gp.A = (float)Aq;
+        sc.gp.sqrtA = (float)sqrt(Aq);
+        sc.gp.ld2 = (float)(2.0 * ld);
+        sc.ldf = (float)ld;
+        sc.Df = (float)sc.D;
+        sc.sa_scale = SA > 0.0 ? (float)(0x1p40 / SA) : 0.f;
+        sc.sv_scale = SV > 0.0 ? (float)(0x1p40 / SV) : 0.f;
+        sc.prefix = 0;
+        sc.pmask = 0;
+        sc.rem_cnt = 0;
+        sc.rest_a = 0;
+        sc.rest_v = 0;
+        sc.rest_b = 0;
+        sc.found = 0;
+        sc.kstar = nl;
+        sc.kkey = ~0ull;
+        if (rank == 0) {
+            R.beta = sc.theta;
+            R.sum_a = SA;
+            R.V = SV;
+            R.b1 = nl > 0 ? B1 : 0.0;
+            R.b2 = nl > 1 ? B2 : 0.0;
+            R.b_arg = nl > 0 ? ARG : -1;
+            R.eps_hat = eh;
+            R.no_fetch = eh < a.eps;
+            R.kstar = 0;
+            R.fallback = 0;
+            R.n_fetch = 0;
+            R.beta_iters = iters;
+        }
+    }
+    parity ^= 1;
+    __syncthreads();
+    stamp(2);
+    if (sc.no_fetch) {
+        cl.sync();
+        return;
+    }
+
+    // ---- phase 3: gain keys, then k* by the radix search
+    {
+        const GainParams gp = sc.gp;
+        const int ARG = sc.arg;
+        const float fa = sc.sa_scale, fv = sc.sv_scale;
+        for (int i = tid; i < ns; i += T) {
+            const Coef c = coef_of(sw[i], sr[i], bf);
+            const unsigned long long k = gain_key(gain_num(c, j0 + i, ARG, gp), j0 + i);
+            sa_[i] = __fmul_rn(c.a, fa);   // fixed-point-scaled a_i, v_i (exactly converted below)
+            sv_[i] = __fmul_rn(c.v, fv);
+            sb[i] = c.b;
+            skey[i] = k;
+        }
+    }
+    __syncthreads();
+    stamp(3);
+    const float ldf = sc.ldf, Df = sc.Df, inv_fa = sc.sa_scale > 0.f ? 1.0f / sc.sa_scale : 0.f,
+                inv_fv = sc.sv_scale > 0.f ? 1.0f / sc.sv_scale : 0.f;
+    int passes = 0;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        ++passes;
+        DecideSlot& my = slot[parity];
+        for (int dd = tid; dd < 256; dd += T) {
+            my.cnt[dd] = 0;
+            my.pa[0][dd] = my.pa[1][dd] = my.pa[2][dd] = 0;
+            my.pv[0][dd] = my.pv[1][dd] = my.pv[2][dd] = 0;
+            my.mb[dd] = 0;
+        }
+        __syncthreads();
+        const unsigned long long prefix = sc.prefix, pmask = sc.pmask;
+        for (int i0 = 0; i0 < ns; i0 += T) {
+            // every lane of a warp runs the same iterations, so the warp can aggregate per digit
+            const int i = i0 + tid;
+            const unsigned long long k = i < ns ? skey[i] : ~0ull;
+            const bool act = i < ns && (k & pmask) == prefix;
+            if (!__any_sync(0xffffffffu, act)) continue;
+            const unsigned dig = act ? (unsigned)((k >> shift) & 255) : 256u + (unsigned)lane;
+            const unsigned peers = __match_any_sync(0xffffffffu, dig);
+            if (act) {
+                // one shared-memory update per digit group; the fixed-point values (< 2^42) are split
+                // in 14-bit pieces so that every sum stays within 32 bits (8192 x 2^14 < 2^32)
+                const unsigned long long fa = __float2ull_rn(sa_[i]), fv = __float2ull_rn(sv_[i]);
+                unsigned ra[3], rv[3];
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    ra[q] = __reduce_add_sync(peers, (unsigned)((fa >> (14 * q)) & 0x3fff));
+                    rv[q] = __reduce_add_sync(peers, (unsigned)((fv >> (14 * q)) & 0x3fff));
+                }
+                const unsigned bm = __reduce_max_sync(peers, fmax_bits(sb[i]));
+                if ((__ffs(peers) - 1) == lane) {
+                    atomicAdd(&my.cnt[dig], (unsigned)__popc(peers));
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) {
+                        atomicAdd(&my.pa[q][dig], ra[q]);
+                        atomicAdd(&my.pv[q][dig], rv[q]);
+                    }
+                    atomicMax(&my.mb[dig], bm);
+                }
+            }
+        }
+        cl.sync();
+        // cluster totals per bin: one bin per thread
+        if (tid < 256) {
+            int c = 0;
+            unsigned long long sa2 = 0, sv2 = 0;
+            unsigned int mb2 = 0;
+            for (int rk = 0; rk < C; ++rk) {
+                const DecideSlot& rs = cl.map_shared_rank(slot, rk)[parity];
+                c += (int)rs.cnt[tid];
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    sa2 += (unsigned long long)rs.pa[q][tid] << (14 * q);
+                    sv2 += (unsigned long long)rs.pv[q][tid] << (14 * q);
+                }
+                mb2 = max(mb2, rs.mb[tid]);
+            }
+            tot_c[tid] = c;
+            tot_a[tid] = sa2;
+            tot_v[tid] = sv2;
+            tot_b[tid] = mb2;
+        }
+        __syncthreads();
+        // warp 0: the first boundary whose residual certificate is below eps
+        if (warp == 0) {
+            int c8[8];
+            unsigned long long a8[8], v8[8];
+            unsigned int b8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int dd = lane * 8 + k;
+                c8[k] = tot_c[dd];
+                a8[k] = tot_a[dd];
+                v8[k] = tot_v[dd];
+                b8[k] = tot_b[dd];
+            }
+            // suffix (higher bins = smaller gains) sums over the lanes above, then within the lane
+            unsigned long long la = 0, lv = 0;
+            unsigned int lb = 0;
+            int lc = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) { la += a8[k]; lv += v8[k]; lb = max(lb, b8[k]); lc += c8[k]; }
+            unsigned long long xa = la, xv = lv;
+            unsigned int xb = lb;
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long ya = __shfl_down_sync(0xffffffffu, xa, o);
+                const unsigned long long yv = __shfl_down_sync(0xffffffffu, xv, o);
+                const unsigned int yb = __shfl_down_sync(0xffffffffu, xb, o);
+                if (lane + o < 32) { xa += ya; xv += yv; xb = max(xb, yb); }
+            }
+            // xa: sum over lanes >= lane; exclusive part above this lane:
+            unsigned long long above_a = xa - la, above_v = xv - lv;
+            unsigned int above_b = __shfl_down_sync(0xffffffffu, xb, 1);
+            if (lane == 31) above_b = 0;
+            // prefix count of bins below this lane (removed when this lane's bins are reached)
+            int cincl = lc;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, cincl, o);
+                if (lane >= o) cincl += y;
+            }
+            int cbelow = cincl - lc;
+            // boundary after bin d of this lane: rest = bins > d of the range + the kept part outside it
+            int first = 0x7fffffff, cnt_through = 0;
+            unsigned long long ra = sc.rest_a + above_a, rv = sc.rest_v + above_v;
+            unsigned int rb = max(sc.rest_b, above_b);
+            // walk this lane's bins from the top down to build the rest after each bin
+            unsigned long long suf_a[8], suf_v[8];
+            unsigned int suf_b[8];
+#pragma unroll
+            for (int k = 7; k >= 0; --k) {
+                suf_a[k] = ra;
+                suf_v[k] = rv;
+                suf_b[k] = rb;
+                ra += a8[k];
+                rv += v8[k];
+                rb = max(rb, b8[k]);
+            }
+            int cb = cbelow;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                cb += c8[k];
+                if (first == 0x7fffffff && c8[k] > 0) {
+                    const float A_ = (float)suf_a[k] * inv_fa, V_ = (float)suf_v[k] * inv_fv;
+                    const float B_ = __uint_as_float(suf_b[k]);
+                    const bool empty = (sc.rem_cnt + cb) == nl;
+                    if (!empty && cert_f(A_, V_, B_, ldf, Df) < a.eps_f) {
+                        first = lane * 8 + k;
+                        cnt_through = cb;
+                    }
+                }
+            }
+            const unsigned who = __ballot_sync(0xffffffffu, first != 0x7fffffff);
+            if (who == 0) {
+                // no boundary of this range works: every key of the range is removed (only possible
+                // at the top level, where it means k* = |L|: eps^(empty) = 0 is always accepted)
+                if (lane == 0) { sc.found = 1; sc.kstar = nl; sc.kkey = ~0ull; }
+            } else {
+                const int src = __ffs(who) - 1;
+                if (lane == src) {
+                    const int d = first;
+                    const int in_bin = c8[d - lane * 8];
+                    const int before = cnt_through - in_bin;     // bins below d, this range
+                    // rest after bin d (kept) for the next level = suf values of bin d
+                    sc.rest_a = suf_a[d - lane * 8];
+                    sc.rest_v = suf_v[d - lane * 8];
+                    sc.rest_b = suf_b[d - lane * 8];
+                    sc.rem_cnt += before;
+                    sc.prefix |= (unsigned long long)d << shift;
+                    sc.pmask |= 255ull << shift;
+                    if (in_bin == 1 || shift == 0) {
+                        sc.found = 1;
+                        sc.kstar = sc.rem_cnt + 1;
+                        sc.kkey = sc.prefix | ~sc.pmask;  // keys of this bin are <= this bound
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        parity ^= 1;
+        if (sc.found) break;
+    }
+    if (timer) R.sel_passes = passes;
+    stamp(4);
+
+    // ---- phase 4: E = keys up to the k*-th; each CTA writes its own members
+    {
+        const unsigned long long kk = sc.kkey;
+        int lcnt = 0;
+        for (int i = tid; i < ns; i += T) lcnt += skey[i] <= kk;
+        lcnt = block_sum(lcnt, redi);
+        if (tid == 0) slot[parity].v[0] = (double)lcnt;
+        cl.sync();
+        if (tid == 0) {
+            int off = 0;
+            for (int rk = 0; rk < rank; ++rk) off += (int)cl.map_shared_rank(slot, rk)[parity].v[0];
+            sc.rem_cnt = off;   // reuse: this CTA's offset in the exact list
+        }
+        __syncthreads();
+        int nf = 0;
+        int off = sc.rem_cnt;
+        for (int i0 = 0; i0 < ns; i0 += T) {
+            const int i = i0 + tid;
+            const bool in = i < ns && skey[i] <= kk;
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            if (lane == 0) wcnt[warp] = __popc(bal);
+            __syncthreads();
+            int wbase = 0, tot = 0;
+            for (int w2 = 0; w2 < (T >> 5); ++w2) {
+                if (w2 < warp) wbase += wcnt[w2];
+                tot += wcnt[w2];
+            }
+            if (in) {
+                const int j = j0 + i;
+                const int pos = off + wbase + __popc(bal & ((1u << lane) - 1));
+                const int tok = V.ltok[(int64_t)kv * V.n + j];
+                mark[(int64_t)row * a.ws_n + j] = a.gen;
+                elist[(int64_t)row * a.ws_n + pos] = tok;
+                nf += V.flags[(int64_t)kv * V.n + tok] == 0;
+            }
+            off += tot;
+            __syncthreads();
+        }
+        nf = block_sum(nf, redi);
+        if (tid == 0) slot[parity].v[1] = (double)nf;
+        cl.sync();
+        if (rank == 0 && tid == 0) {
+            int total_nf = 0;
+            for (int rk = 0; rk < C; ++rk) total_nf += (int)cl.map_shared_rank(slot, rk)[parity].v[1];
+            R.kstar = sc.kstar;
+            R.n_fetch = total_nf;
+        }
+        cl.sync();
+    }
+    stamp(5);
 }
 
 // --------------------------------------------------------------------------------------------
@@ -847,21 +1415,36 @@ __global__ void __launch_bounds__(1024) union_kernel(Views views, DecodeArgs a, 
     if (threadIdx.x == 0) ucount[b * a.Hkv + kv] = base;
 }
 
-__global__ void gather_kernel(Views views, DecodeArgs a, const int32_t* __restrict__ ulist,
-                              const int32_t* __restrict__ ucount, unsigned char* __restrict__ staging, int row_bytes)
+__global__ void __launch_bounds__(256) gather_kernel(Views views, DecodeArgs a, const int32_t* __restrict__ ulist,
+                                                     const int32_t* __restrict__ ucount,
+                                                     unsigned char* __restrict__ staging, int row_bytes)
 {
     const int b = blockIdx.x / a.Hkv, kv = blockIdx.x % a.Hkv;
     const SlotView& V = views.v[b];
     const int cnt = ucount[b * a.Hkv + kv];
     const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
     const int32_t* lst = ulist + (int64_t)(b * a.Hkv + kv) * a.ws_n;
-    const unsigned char* host = reinterpret_cast<const unsigned char*>(V.kv_host);
+    const unsigned char* host = reinterpret_cast<const unsigned char*>(V.kv_host) + (int64_t)kv * V.n * row_bytes;
     unsigned char* dst = staging + (int64_t)(b * a.Hkv + kv) * a.ws_n * row_bytes;
-    for (int u = blockIdx.y * warps + (threadIdx.x >> 5); u < cnt; u += gridDim.y * warps) {
-        const int tok = lst[u];
-        const uint4* src = reinterpret_cast<const uint4*>(host + ((int64_t)kv * V.n + tok) * row_bytes);
-        uint4* to = reinterpret_cast<uint4*>(dst + (int64_t)u * row_bytes);
-        for (int v = lane; v < row_bytes / 16; v += 32) to[v] = src[v];
+    const int vec = row_bytes / 16;  // 16-byte pieces per row (32 for bf16, 64 for fp32)
+    const int stride = gridDim.y * warps;
+    // four rows in flight per warp: their zero-copy host loads overlap
+    for (int u0 = blockIdx.y * warps + (threadIdx.x >> 5); u0 < cnt; u0 += 4 * stride) {
+        int tok[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int u = u0 + k * stride;
+            tok[k] = u < cnt ? lst[u] : -1;
+        }
+        for (int v = lane; v < vec; v += 32) {
+            uint4 x[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (tok[k] >= 0) x[k] = reinterpret_cast<const uint4*>(host + (int64_t)tok[k] * row_bytes)[v];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (tok[k] >= 0) reinterpret_cast<uint4*>(dst + (int64_t)(u0 + k * stride) * row_bytes)[v] = x[k];
+        }
     }
 }
 
@@ -887,15 +1470,47 @@ template <> struct Vec4<float> {
     static __device__ __forceinline__ float4 load(const float* p) { return *reinterpret_cast<const float4*>(p); }
 };
 
+// One warp handles a contiguous run of rows.  The per-row weight factors (which depend on the
+// row's token, its flags, whether it was made exact for each query head, and lambda_i / r_i for
+// sampled tokens) are resolved 32 rows at a time, one row per lane, so their dependent loads overlap;
+// then the K/V rows are streamed two at a time.
 template <typename T, int G>
-__global__ void __launch_bounds__(128) attn_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
+__device__ __forceinline__ void attn_weights_batch(const SlotView& V, int kv, int n, int m_res, const int32_t* ul,
+                                                   const int32_t* __restrict__ mark, const float* __restrict__ wl,
+                                                   const int* rowg, const float* beta, int gen, int ws_n, int rix,
+                                                   bool valid, float* om)
+{
+#pragma unroll
+    for (int g = 0; g < G; ++g) om[g] = 0.f;
+    if (!valid) return;
+    const bool staged = rix >= m_res;
+    const int tok = staged ? ul[rix - m_res] : V.rtok[(int64_t)kv * n + rix];
+    const int f = V.flags[(int64_t)kv * n + tok];
+    if (f == 2) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) om[g] = 1.f;
+        return;
+    }
+    const int li = V.lpos[(int64_t)kv * n + tok];
+    float r = 0.f;
+    if (f == 1 && !staged) r = V.rl[(int64_t)kv * n + li];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if (mark[(int64_t)rowg[g] * ws_n + li] == gen) om[g] = 1.f;
+        else if (f == 1 && !staged) om[g] = __fdiv_rn(lambda_of(wl[(int64_t)rowg[g] * ws_n + li], r, beta[g]), r);
+    }
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(256) attn_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
                                                    const RowState* __restrict__ rows, const float* __restrict__ wl,
                                                    const int32_t* __restrict__ mark,
                                                    const int32_t* __restrict__ ulist, const int32_t* __restrict__ ucount,
                                                    const T* __restrict__ staging, float* __restrict__ part)
 {
-    __shared__ float sm_m[4][G], sm_l[4][G];
-    __shared__ float sm_acc[4][G][kHeadDim];
+    constexpr int NW = 8;
+    __shared__ float sm_m[NW][G], sm_l[NW][G];
+    __shared__ float sm_acc[NW][G][kHeadDim];
     const int b = blockIdx.x / a.Hkv, kv = blockIdx.x % a.Hkv;
     const SlotView& V = views.v[b];
     const int n = V.n;
@@ -903,8 +1518,10 @@ __global__ void __launch_bounds__(128) attn_kernel(Views views, const float* __r
     const int m_res = V.counts[kv * 4 + 3];
     const int nu = ucount[b * a.Hkv + kv];
     const int total = m_res + nu;
-    const int per = (total + a.nsplit - 1) / a.nsplit;
+    const int per = (total + gridDim.y - 1) / gridDim.y;
     const int r0 = blockIdx.y * per, r1 = min(total, r0 + per);
+    const int perw = (r1 - r0 + NW - 1) / NW;
+    const int w0 = min(r1, r0 + warp * perw), w1 = min(r1, w0 + perw);
     float qv[G][4];
     float beta[G];
     int rowg[G];
@@ -912,7 +1529,10 @@ __global__ void __launch_bounds__(128) attn_kernel(Views views, const float* __r
     for (int g = 0; g < G; ++g) {
         rowg[g] = row_of(b, kv * G + g, a.Hq);
         const float4 t = *reinterpret_cast<const float4*>(q + (int64_t)rowg[g] * kHeadDim + lane * 4);
-        qv[g][0] = t.x; qv[g][1] = t.y; qv[g][2] = t.z; qv[g][3] = t.w;
+        qv[g][0] = t.x * a.inv_sqrt_d_f;
+        qv[g][1] = t.y * a.inv_sqrt_d_f;
+        qv[g][2] = t.z * a.inv_sqrt_d_f;
+        qv[g][3] = t.w * a.inv_sqrt_d_f;
         beta[g] = (float)rows[rowg[g]].beta;
     }
     float mrun[G], lrun[G], acc[G][4];
@@ -924,46 +1544,50 @@ __global__ void __launch_bounds__(128) attn_kernel(Views views, const float* __r
     }
     const T* res = reinterpret_cast<const T*>(V.kvres) + V.res_off[kv] * 2 * kHeadDim;
     const T* stg = staging + (int64_t)(b * a.Hkv + kv) * a.ws_n * 2 * kHeadDim;
-    for (int rix = r0 + warp; rix < r1; rix += 4) {
-        const T* rowp;
-        int tok;
-        bool staged = rix >= m_res;
-        if (!staged) {
-            rowp = res + (int64_t)rix * 2 * kHeadDim;
-            tok = V.rtok[(int64_t)kv * n + rix];
-        } else {
-            const int u = rix - m_res;
-            rowp = stg + (int64_t)u * 2 * kHeadDim;
-            tok = ulist[(int64_t)(b * a.Hkv + kv) * a.ws_n + u];
-        }
-        const int f = V.flags[(int64_t)kv * n + tok];
-        const int li = V.lpos[(int64_t)kv * n + tok];
-        const float4 k4 = Vec4<T>::load(rowp + lane * 4);
-        const float4 v4 = Vec4<T>::load(rowp + kHeadDim + lane * 4);
+    const int32_t* ul = ulist + (int64_t)(b * a.Hkv + kv) * a.ws_n;
+    for (int base = w0; base < w1; base += 32) {
+        float om_l[G];
+        attn_weights_batch<T, G>(V, kv, n, m_res, ul, mark, wl, rowg, beta, a.gen, a.ws_n, base + lane,
+                                 base + lane < w1, om_l);
+        const int cnt = min(32, w1 - base);
+        for (int k = 0; k < cnt; k += 2) {
+            const int rA = base + k, rB = base + k + 1;
+            const bool hasB = k + 1 < cnt;
+            const T* pA = rA < m_res ? res + (int64_t)rA * 2 * kHeadDim : stg + (int64_t)(rA - m_res) * 2 * kHeadDim;
+            const T* pB = hasB ? (rB < m_res ? res + (int64_t)rB * 2 * kHeadDim
+                                             : stg + (int64_t)(rB - m_res) * 2 * kHeadDim)
+                               : pA;
+            const float4 kA = Vec4<T>::load(pA + lane * 4), vA = Vec4<T>::load(pA + kHeadDim + lane * 4);
+            const float4 kB = Vec4<T>::load(pB + lane * 4), vB = Vec4<T>::load(pB + kHeadDim + lane * 4);
+            float sA[G], sB[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float s = qv[g][0] * k4.x + qv[g][1] * k4.y + qv[g][2] * k4.z + qv[g][3] * k4.w;
-            s = warp_sum(s);
-            float om;
-            if (f == 2) om = 1.f;
-            else {
-                const bool exact = mark[(int64_t)rowg[g] * a.ws_n + li] == a.gen;
-                if (exact) om = 1.f;
-                else if (f == 1 && !staged) {
-                    const float r = V.rl[(int64_t)kv * n + li];
-                    om = __fdiv_rn(lambda_of(wl[(int64_t)rowg[g] * a.ws_n + li], r, beta[g]), r);
-                } else om = 0.f;
+            for (int g = 0; g < G; ++g) {
+                sA[g] = qv[g][0] * kA.x + qv[g][1] * kA.y + qv[g][2] * kA.z + qv[g][3] * kA.w;
+                sB[g] = qv[g][0] * kB.x + qv[g][1] * kB.y + qv[g][2] * kB.z + qv[g][3] * kB.w;
             }
-            if (om > 0.f) {
-                const float x = s * a.inv_sqrt_d_f;
-                const float mn = fmaxf(mrun[g], x);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    sA[g] += __shfl_xor_sync(0xffffffffu, sA[g], o);
+                    sB[g] += __shfl_xor_sync(0xffffffffu, sB[g], o);
+                }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float oA = __shfl_sync(0xffffffffu, om_l[g], k);
+                const float oB = hasB ? __shfl_sync(0xffffffffu, om_l[g], k + 1) : 0.f;
+                const float xA = oA > 0.f ? sA[g] : -INFINITY;
+                const float xB = oB > 0.f ? sB[g] : -INFINITY;
+                const float mn = fmaxf(mrun[g], fmaxf(xA, xB));
+                if (mn == -INFINITY) continue;
                 const float corr = expf(mrun[g] - mn);
-                const float p = om * expf(x - mn);
-                lrun[g] = lrun[g] * corr + p;
-                acc[g][0] = acc[g][0] * corr + p * v4.x;
-                acc[g][1] = acc[g][1] * corr + p * v4.y;
-                acc[g][2] = acc[g][2] * corr + p * v4.z;
-                acc[g][3] = acc[g][3] * corr + p * v4.w;
+                const float pA_ = oA > 0.f ? oA * expf(xA - mn) : 0.f;
+                const float pB_ = oB > 0.f ? oB * expf(xB - mn) : 0.f;
+                lrun[g] = lrun[g] * corr + pA_ + pB_;
+                acc[g][0] = acc[g][0] * corr + pA_ * vA.x + pB_ * vB.x;
+                acc[g][1] = acc[g][1] * corr + pA_ * vA.y + pB_ * vB.y;
+                acc[g][2] = acc[g][2] * corr + pA_ * vA.z + pB_ * vB.z;
+                acc[g][3] = acc[g][3] * corr + pA_ * vA.w + pB_ * vB.w;
                 mrun[g] = mn;
             }
         }
@@ -980,13 +1604,13 @@ __global__ void __launch_bounds__(128) attn_kernel(Views views, const float* __r
     for (int e = threadIdx.x; e < G * kHeadDim; e += blockDim.x) {
         const int g = e / kHeadDim, c = e % kHeadDim;
         float M = -INFINITY;
-        for (int w2 = 0; w2 < 4; ++w2) M = fmaxf(M, sm_m[w2][g]);
+        for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, sm_m[w2][g]);
         float L = 0.f, A = 0.f;
         if (M > -INFINITY)
-            for (int w2 = 0; w2 < 4; ++w2) {
-                const float s = sm_m[w2][g] > -INFINITY ? expf(sm_m[w2][g] - M) : 0.f;
-                L += sm_l[w2][g] * s;
-                A += sm_acc[w2][g][c] * s;
+            for (int w2 = 0; w2 < NW; ++w2) {
+                const float sc = sm_m[w2][g] > -INFINITY ? expf(sm_m[w2][g] - M) : 0.f;
+                L += sm_l[w2][g] * sc;
+                A += sm_acc[w2][g][c] * sc;
             }
         float* pp = part + ((int64_t)rowg[g] * a.nsplit + blockIdx.y) * (kHeadDim + 2);
         pp[c] = A;
@@ -1029,28 +1653,48 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         score_exact_kernel<T, G><<<gs, kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl);
     VK_LAUNCHED("score_sketch");
     if (max_nh > 0) {
-        score_h_kernel<T, G><<<dim3((max_nh + kTile - 1) / kTile, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows,
+        score_h_kernel<T, G><<<dim3((max_nh * G + kTile - 1) / kTile, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows,
                                                                                             ctx.th);
         VK_LAUNCHED("score_h");
     }
-    const int wmax = std::max(max_nl, max_nh);
-    weights_kernel<<<dim3(std::max(1, (wmax + 255) / 256), rowsN), 256, 0, st>>>(views, a, ctx.rows, ctx.tl, ctx.th,
-                                                                                ctx.wl);
-    VK_LAUNCHED("weights");
-    beta_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl);
-    VK_LAUNCHED("beta");
-    const size_t sel_smem = sizeof(unsigned long long) * kSelWidth;
-    select_kernel<<<rowsN, 1024, sel_smem, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
-    VK_LAUNCHED("select");
+    if (max_nl <= kDecideMaxCluster * kDecideCap) {
+        int C = 1;
+        while (C * kDecideCap < max_nl) C <<= 1;
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(rowsN * C);
+        lc.blockDim = dim3(kDecideThreads);
+        lc.dynamicSmemBytes = kDecideSmem;
+        lc.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        VK_CUDA(cudaLaunchKernelEx(&lc, decide_kernel, views, a, ctx.rows, (const float2*)ctx.tl,
+                                   (const float2*)ctx.th, ctx.wl, ctx.mark, ctx.elist));
+        VK_LAUNCHED("decide");
+    } else {
+        const int wmax = std::max(max_nl, max_nh);
+        weights_kernel<<<dim3(std::max(1, (wmax + 255) / 256), rowsN), 256, 0, st>>>(views, a, ctx.rows, ctx.tl,
+                                                                                    ctx.th, ctx.wl);
+        VK_LAUNCHED("weights");
+        beta_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl);
+        VK_LAUNCHED("beta");
+        const size_t sel_smem = sizeof(unsigned long long) * kSelWidth;
+        select_kernel<<<rowsN, 1024, sel_smem, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
+        VK_LAUNCHED("select");
+    }
     fallback_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
     VK_LAUNCHED("fallback");
     union_kernel<<<B * a.Hkv, 1024, 0, st>>>(views, a, ctx.rows, ctx.elist, ctx.ubits, ctx.ulist, ctx.ucount);
     VK_LAUNCHED("union");
     const int row_bytes = (int)(2 * kHeadDim * sizeof(T));
-    gather_kernel<<<dim3(B * a.Hkv, 16), 256, 0, st>>>(views, a, ctx.ulist, ctx.ucount,
+    gather_kernel<<<dim3(B * a.Hkv, std::max(8, 1216 / (B * a.Hkv))), 256, 0, st>>>(views, a, ctx.ulist, ctx.ucount,
                                                        (unsigned char*)ctx.staging, row_bytes);
     VK_LAUNCHED("gather");
-    attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), 128, 0, st>>>(views, q, a, ctx.rows, ctx.wl, ctx.mark, ctx.ulist,
+    attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), 256, 0, st>>>(views, q, a, ctx.rows, ctx.wl, ctx.mark, ctx.ulist,
                                                                  ctx.ucount, (const T*)ctx.staging, ctx.part);
     VK_LAUNCHED("attn");
     merge_kernel<<<rowsN, kHeadDim, 0, st>>>(a, ctx.part, out);
@@ -1089,6 +1733,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     if (!g_attr_done) {
         VK_CUDA(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)(sizeof(unsigned long long) * kSelWidth)));
+        VK_CUDA(cudaFuncSetAttribute(decide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
         g_attr_done = true;
     }
     Views views;
@@ -1132,7 +1777,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     a.ws_n = ctx.ws_n;
     a.ws_npow2 = ctx.ws_npow2;
     a.gen = ++ctx.gen;
-    a.nsplit = ctx.nsplit;
+    a.nsplit = std::min(ctx.nsplit, std::max(8, (1216 + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
     a.eps = eps;
     a.eps_f = (float)eps;
     a.ldelta = std::log(2.0 / delta);

@@ -64,6 +64,9 @@ struct RowState {
     double b1, b2;      // largest and second-largest b_i
     double eps_hat;
     double pad;
+    int beta_iters;     // passes of the beta solve
+    int sel_passes;     // radix-select passes
+    unsigned int phase_ns[6];  // decide kernel: ns spent in phases 0..4 and in the ranking (rank 0)
 };
 
 struct Ctx {
@@ -102,7 +105,7 @@ struct Ctx {
     int32_t* ucount = nullptr;      // [max_batch][Hkv]
     void* staging = nullptr;        // [max_batch][Hkv][n][2][d] fetched rows
     float* part = nullptr;          // [rows][nsplit][d + 2] attention partials
-    int nsplit = 16;
+    int nsplit = 128;               // largest split of the attention over blocks per KV head
 
     // per-decode small arrays
     int32_t* d_slot_n = nullptr;    // [max_batch] n of each row set's slot
