@@ -259,9 +259,38 @@ def run_verkv(args):
                 "frac": ach / hbm_peak, "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
                 "algorithmic_bytes": by, "avg_us": avg_ms * 1e3}
 
-    roofline = roof(dom)
+    # host-link peak: a bulk pinned host -> device copy (the same link the fetch uses)
+    link_peak = None
+    if rank == 0:
+        src = torch.empty(256 * 1024 * 1024, dtype=torch.uint8).pin_memory()
+        dst = torch.empty_like(src, device=dev)
+        best = None
+        for _ in range(4):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(st)
+            dst.copy_(src, non_blocking=True)
+            b_.record(st)
+            b_.synchronize()
+            ms_ = a_.elapsed_time(b_)
+            best = ms_ if best is None else min(best, ms_)
+        link_peak = src.numel() / (best / 1e3) / 1e9
+        del src, dst
+
+    def roof_link(kname):
+        if kname not in agg or not link_peak:
+            return None
+        avg_ms = agg[kname][0] / agg[kname][1]
+        by = algorithmic_bytes(kname, stats0, traces, w, row_bytes)
+        ach = by / (avg_ms / 1e3) / 1e9
+        return {"kernel": kname, "bound": "host_link", "achieved": ach, "peak": link_peak, "unit": "GB/s",
+                "frac": ach / link_peak, "traffic": None,
+                "peak_source": "measured in this run: pinned host -> device copy of 256 MiB",
+                "algorithmic_bytes": by, "avg_us": avg_ms * 1e3}
+
+    roofline = roof_link(dom) if dom == "gather" else roof(dom)
     roof_score = roof("score_sketch")
     roof_attn = roof("attn")
+    roof_gather = roof_link("gather")
 
     # ---------------------------------------------------------------- end to end through the public API
     e2e = None
@@ -314,6 +343,7 @@ def run_verkv(args):
             "kernel_share": {k: round(v[0] / total_ms, 4) for k, v in sorted(agg.items(), key=lambda kv: -kv[1][0])},
             "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()},
             "roofline": roofline, "roofline_score_sketch": roof_score, "roofline_attn": roof_attn,
+            "roofline_gather": roof_gather, "host_link_peak_gbs": link_peak,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
         }
         print(json.dumps(line))

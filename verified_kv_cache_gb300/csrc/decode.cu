@@ -27,6 +27,7 @@ struct Views {
 };
 
 struct DecodeArgs {
+    uint32_t* ubits;  // [B][Hkv][ws_n/32 + 1] union bitmap of fetched tokens (set by the decision kernels)
     int Hkv, Hq, G, ws_n, ws_npow2, gen, nsplit;
     float eps_f;
     double eps, ldelta;
@@ -595,7 +596,11 @@ __device__ void emit_exact_set(const unsigned long long* sorted, int kstar, int 
         const int tok = V.ltok[(int64_t)kv * V.n + j];
         mark[(int64_t)row * a.ws_n + j] = a.gen;
         elist[(int64_t)row * a.ws_n + p] = tok;
-        nf += V.flags[(int64_t)kv * V.n + tok] == 0;
+        if (V.flags[(int64_t)kv * V.n + tok] == 0) {
+            ++nf;
+            const int b = row / a.Hq;
+            atomicOr(&a.ubits[(int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1) + (tok >> 5)], 1u << (tok & 31));
+        }
     }
     nf = block_sum(nf, redi);
     if (threadIdx.x == 0) {
@@ -1350,7 +1355,10 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                 const int tok = V.ltok[(int64_t)kv * V.n + j];
                 mark[(int64_t)row * a.ws_n + j] = a.gen;
                 elist[(int64_t)row * a.ws_n + pos] = tok;
-                nf += V.flags[(int64_t)kv * V.n + tok] == 0;
+                if (V.flags[(int64_t)kv * V.n + tok] == 0) {
+                    ++nf;
+                    atomicOr(&a.ubits[(int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1) + (tok >> 5)], 1u << (tok & 31));
+                }
             }
             off += tot;
             __syncthreads();
@@ -1370,9 +1378,9 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
 }
 
 // --------------------------------------------------------------------------------------------
-// D7: union of L_g[:k*] \ S over the query heads of a KV head (ascending tokens), and the copy of
-// those rows from the pinned host cache into the staging area (zero-copy loads, one warp per
-// row, 16 bytes per lane).
+// D7: union of L_g[:k*] \ S over the query heads of a KV head (the decision kernels set its bits),
+// compacted to ascending tokens, and the copy of those rows from the pinned host cache into the
+// staging area (zero-copy loads, one warp per row, 16 bytes per lane, several rows in flight).
 // --------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) union_kernel(Views views, DecodeArgs a, const RowState* __restrict__ rows,
                                                      const int32_t* __restrict__ elist, uint32_t* __restrict__ ubits,
@@ -1384,15 +1392,8 @@ __global__ void __launch_bounds__(1024) union_kernel(Views views, DecodeArgs a, 
     const int n = V.n;
     const int nwords = (n + 31) / 32;
     uint32_t* bits = ubits + (int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1);
-    for (int g = 0; g < a.G; ++g) {
-        const int row = row_of(b, kv * a.G + g, a.Hq);
-        const int ks = rows[row].kstar;
-        for (int p = threadIdx.x; p < ks; p += blockDim.x) {
-            const int tok = elist[(int64_t)row * a.ws_n + p];
-            if (V.flags[(int64_t)kv * n + tok] == 0) atomicOr(&bits[tok >> 5], 1u << (tok & 31));
-        }
-    }
-    __syncthreads();
+    (void)rows;
+    (void)elist;
     int base = 0;
     int32_t* out = ulist + (int64_t)(b * a.Hkv + kv) * a.ws_n;
     for (int w0 = 0; w0 < nwords; w0 += blockDim.x) {
@@ -1618,21 +1619,37 @@ __global__ void __launch_bounds__(256) attn_kernel(Views views, const float* __r
     }
 }
 
-__global__ void merge_kernel(DecodeArgs a, const float* __restrict__ part, float* __restrict__ out)
+// LSE merge of the split partials of one query row: per-split scale factors are computed once (one
+// split per thread), then each thread sums its channel over the splits.
+__global__ void __launch_bounds__(kHeadDim) merge_kernel(DecodeArgs a, const float* __restrict__ part,
+                                                         float* __restrict__ out)
 {
+    __shared__ float scl[128];
+    __shared__ float red[32];
     const int row = blockIdx.x, c = threadIdx.x;
-    const float* pp = part + (int64_t)row * a.nsplit * (kHeadDim + 2);
-    float M = -INFINITY;
-    for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, pp[s * (kHeadDim + 2) + kHeadDim]);
-    float L = 0.f, A = 0.f;
-    for (int s = 0; s < a.nsplit; ++s) {
+    const int ns = a.nsplit;
+    const float* pp = part + (int64_t)row * ns * (kHeadDim + 2);
+    float mx = -INFINITY;
+    for (int s = c; s < ns; s += blockDim.x) mx = fmaxf(mx, pp[s * (kHeadDim + 2) + kHeadDim]);
+    const float M = block_max(mx, red);
+    float l = 0.f;
+    for (int s = c; s < ns; s += blockDim.x) {
         const float m = pp[s * (kHeadDim + 2) + kHeadDim];
-        if (m == -INFINITY) continue;
-        const float sc = expf(m - M);
-        L += pp[s * (kHeadDim + 2) + kHeadDim + 1] * sc;
-        A += pp[s * (kHeadDim + 2) + c] * sc;
+        const float f = m == -INFINITY ? 0.f : expf(m - M);
+        scl[s] = f;
+        l += pp[s * (kHeadDim + 2) + kHeadDim + 1] * f;
     }
-    out[(int64_t)row * kHeadDim + c] = A / L;
+    const float L = block_sum(l, red);
+    float A0 = 0.f, A1 = 0.f, A2 = 0.f, A3 = 0.f;
+    int s = 0;
+    for (; s + 4 <= ns; s += 4) {
+        A0 += pp[(s + 0) * (kHeadDim + 2) + c] * scl[s + 0];
+        A1 += pp[(s + 1) * (kHeadDim + 2) + c] * scl[s + 1];
+        A2 += pp[(s + 2) * (kHeadDim + 2) + c] * scl[s + 2];
+        A3 += pp[(s + 3) * (kHeadDim + 2) + c] * scl[s + 3];
+    }
+    for (; s < ns; ++s) A0 += pp[s * (kHeadDim + 2) + c] * scl[s];
+    out[(int64_t)row * kHeadDim + c] = ((A0 + A1) + (A2 + A3)) / L;
 }
 
 template <typename T, int G>
@@ -1686,8 +1703,10 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         select_kernel<<<rowsN, 1024, sel_smem, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
         VK_LAUNCHED("select");
     }
-    fallback_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
-    VK_LAUNCHED("fallback");
+    if (max_nl > kDecideMaxCluster * kDecideCap) {
+        fallback_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
+        VK_LAUNCHED("fallback");
+    }
     union_kernel<<<B * a.Hkv, 1024, 0, st>>>(views, a, ctx.rows, ctx.elist, ctx.ubits, ctx.ulist, ctx.ucount);
     VK_LAUNCHED("union");
     const int row_bytes = (int)(2 * kHeadDim * sizeof(T));
@@ -1777,6 +1796,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     a.ws_n = ctx.ws_n;
     a.ws_npow2 = ctx.ws_npow2;
     a.gen = ++ctx.gen;
+    a.ubits = ctx.ubits;
     a.nsplit = std::min(ctx.nsplit, std::max(8, (1216 + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
     a.eps = eps;
     a.eps_f = (float)eps;
