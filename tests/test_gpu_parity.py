@@ -217,14 +217,15 @@ def test_large_kstar_on_the_cluster_path():
 
 
 def test_full_row_path_for_long_rows():
-    """|L| above the on-chip capacity of the cluster kernel (65536 per row) uses the multi-kernel path:
-    on-chip ranking of 4096 candidates and, when k* lies beyond them, the full-row sort."""
-    w = small_case("int8", n=72000, steps=1, query_mode="random", eta=1 / 16, n_kv=2, n_q=4)
+    """|L| above the on-chip capacity of the cluster kernel (131072 per row with 16-CTA clusters) uses
+    the multi-kernel path: on-chip ranking of 4096 candidates and, when k* lies beyond them, the
+    full-row sort."""
+    w = small_case("int8", n=150000, steps=1, query_mode="random", eta=1 / 16, n_kv=2, n_q=4)
     w.queries *= 0.3
     ctx = make_lib_ctx(w)
     gc = GpuCase(w, ctx)
-    tau, stats, osl = _compress_both(w, gc)
-    assert max(s["n_l"] for s in stats) > 65536
+    tau, stats, osl = _compress_both(w, gc, tau=workloads.synthetic_scores(w.n_kv, w.n, seed=9))
+    assert max(s["n_l"] for s in stats) > 131072
     eps = 0.005
     gc.decode(w.queries[0], eps, 0.05)
     trace = ctx.decode_trace(w.n_q)

@@ -833,7 +833,7 @@ __global__ void __launch_bounds__(1024) fallback_kernel(Views views, DecodeArgs 
 // --------------------------------------------------------------------------------------------
 constexpr int kDecideThreads = 1024;
 constexpr int kDecideCap = 8192;   // L entries per CTA
-constexpr int kDecideMaxCluster = 8;
+constexpr int kDecideMaxCluster = 16;  // 16 is a non-portable cluster size: used when the GPU can run it
 constexpr size_t kDecideSmem = (size_t)kDecideCap * (4 + 4 + 8 + 4);
 
 struct DecideSlot {
@@ -1652,6 +1652,8 @@ __global__ void __launch_bounds__(kHeadDim) merge_kernel(DecodeArgs a, const flo
     out[(int64_t)row * kHeadDim + c] = ((A0 + A1) + (A2 + A3)) / L;
 }
 
+int g_decide_max_cluster = 8;  // largest cluster the decide kernel is launched with (set once)
+
 template <typename T, int G>
 verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, int B, int max_n, int max_nl,
                            int max_nh, const float* q, float* out, cudaStream_t st)
@@ -1674,7 +1676,7 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
                                                                                             ctx.th);
         VK_LAUNCHED("score_h");
     }
-    if (max_nl <= kDecideMaxCluster * kDecideCap) {
+    if (max_nl <= g_decide_max_cluster * kDecideCap) {
         int C = 1;
         while (C * kDecideCap < max_nl) C <<= 1;
         cudaLaunchConfig_t lc = {};
@@ -1703,7 +1705,7 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         select_kernel<<<rowsN, 1024, sel_smem, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
         VK_LAUNCHED("select");
     }
-    if (max_nl > kDecideMaxCluster * kDecideCap) {
+    if (max_nl > g_decide_max_cluster * kDecideCap) {
         fallback_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
         VK_LAUNCHED("fallback");
     }
@@ -1753,6 +1755,24 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         VK_CUDA(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)(sizeof(unsigned long long) * kSelWidth)));
         VK_CUDA(cudaFuncSetAttribute(decide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
+        // a 16-CTA cluster (non-portable) lets rows of up to 16 x kDecideCap entries stay on chip
+        if (cudaFuncSetAttribute(decide_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = dim3(kDecideMaxCluster);
+            lc.blockDim = dim3(kDecideThreads);
+            lc.dynamicSmemBytes = kDecideSmem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = kDecideMaxCluster;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            lc.attrs = attr;
+            lc.numAttrs = 1;
+            int nclusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&nclusters, decide_kernel, &lc) == cudaSuccess && nclusters > 0)
+                g_decide_max_cluster = kDecideMaxCluster;
+        }
+        cudaGetLastError();  // a refused query leaves no error behind
         g_attr_done = true;
     }
     Views views;
