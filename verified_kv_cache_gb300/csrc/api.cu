@@ -276,10 +276,12 @@ verkv_status verkv_get_decode_trace(verkv_ctx* h, verkv_row_trace* out, int32_t 
         verkv_row_trace& t = out[i];
         const RowState& s = rs[i];
         memset(&t, 0, sizeof(t));
-        int mi = s.m_ord;
-        float mf;
-        int bits = mi >= 0 ? mi : mi ^ 0x7fffffff;
-        memcpy(&mf, &bits, 4);
+        float mf = -INFINITY;
+        if ((unsigned)(s.m_tag >> 32) == (unsigned)ctx.gen) {
+            const int mi = (int)((unsigned)s.m_tag ^ 0x80000000u);
+            const int bits = mi >= 0 ? mi : mi ^ 0x7fffffff;
+            memcpy(&mf, &bits, 4);
+        }
         t.m = mf;
         t.D = s.D;
         t.beta = s.beta;

@@ -192,6 +192,19 @@ __device__ __forceinline__ int float_to_ordered(float f)
 }
 __device__ __forceinline__ float ordered_to_float(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
 
+// A running maximum tagged with a generation: values of an older generation compare smaller, so the
+// slot needs no reset between calls.  atomicMax on the 64-bit word keeps the largest float of the
+// newest generation.
+__device__ __forceinline__ unsigned long long tag_max(unsigned gen, float f)
+{
+    return ((unsigned long long)gen << 32) | (unsigned)(float_to_ordered(f) ^ 0x80000000);
+}
+__device__ __forceinline__ float untag_max(unsigned long long t, unsigned gen)
+{
+    if ((unsigned)(t >> 32) != gen) return -INFINITY;
+    return ordered_to_float((int)((unsigned)t ^ 0x80000000u));
+}
+
 // ---------------------------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., SC'11): ten rounds of two 32x32 -> 64-bit products, key bumped by
 // the Weyl constants between rounds.  The Poisson draw of a token uses word 0 of the block at

@@ -47,7 +47,7 @@ __global__ void init_rows_kernel(RowState* __restrict__ rows, Views views, Decod
     const int b = row / a.Hq, kv = (row % a.Hq) / a.G;
     RowState s;
     memset(&s, 0, sizeof(s));
-    s.m_ord = float_to_ordered(-INFINITY);
+    s.m_tag = 0;
     s.n_h = views.v[b].counts[kv * 4 + 0];
     s.n_l = views.v[b].counts[kv * 4 + 1];
     s.b_arg = -1;
@@ -149,9 +149,11 @@ __global__ void __launch_bounds__(kTile) score_int8_kernel(Views views, const fl
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const float m = block_max(mloc[g], red);
-        if (threadIdx.x == 0 && m > -INFINITY) atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_ord, float_to_ordered(m));
+        const float m = warp_max(mloc[g]);
+        if ((threadIdx.x & 31) == 0 && m > -INFINITY)
+            atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
     }
+    (void)red;
 }
 
 template <int G>
@@ -221,9 +223,11 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const float m = block_max(mloc[g], red);
-        if (threadIdx.x == 0 && m > -INFINITY) atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_ord, float_to_ordered(m));
+        const float m = warp_max(mloc[g]);
+        if ((threadIdx.x & 31) == 0 && m > -INFINITY)
+            atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
     }
+    (void)red;
 }
 
 // Exact float-float dot product <q, k>/sqrt(d) of one key row (fp32 or bf16 elements).
@@ -275,9 +279,11 @@ __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const f
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const float m = block_max(mloc[g], red);
-        if (threadIdx.x == 0 && m > -INFINITY) atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_ord, float_to_ordered(m));
+        const float m = warp_max(mloc[g]);
+        if ((threadIdx.x & 31) == 0 && m > -INFINITY)
+            atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
     }
+    (void)red;
 }
 
 // Exact logits of the tokens of H (resident keys), by H index; one thread per (token, query head).
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(kTile) score_h_kernel(Views views, const float
     // max per query head: lanes with the same g are G apart
     for (int o = 16; o >= G; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
     if ((threadIdx.x & 31) < G && mloc > -INFINITY)
-        atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_ord, float_to_ordered(mloc));
+        atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, mloc));
     (void)red;
 }
 
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(256) weights_kernel(Views views, DecodeArgs a,
     RowState& R = rows[row];
     const int nl = R.n_l, nh = R.n_h;
     if (blockIdx.x * blockDim.x >= max(nl, nh)) return;
-    const float m = ordered_to_float(R.m_ord);
+    const float m = untag_max(R.m_tag, (unsigned)a.gen);
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     ff d = {0.f, 0.f}, al = {0.f, 0.f};
     if (j < nl) {
@@ -939,10 +945,10 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const int b = row / a.Hq, kv = (row % a.Hq) / a.G;
     const SlotView& V = views.v[b];
     RowState& R = rows[row];
-    const int nl = R.n_l, nh = R.n_h;
+    const int nl = V.counts[kv * 4 + 1], nh = V.counts[kv * 4 + 0];
     const int S = (nl + C - 1) / C;
     const int j0 = min(nl, rank * S), j1 = min(nl, j0 + S), ns = j1 - j0;
-    const float m = ordered_to_float(R.m_ord);
+    const float m = untag_max(R.m_tag, (unsigned)a.gen);
     const float* rl = V.rl + (int64_t)kv * V.n;
     int parity = 0;
     const bool timer = rank == 0 && tid == 0;
@@ -987,6 +993,10 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         if (rank == 0) {
             R.D = bc[0];
             R.alpha_sum = At;
+            R.n_l = nl;
+            R.n_h = nh;
+            R.sel_passes = 0;
+            for (int k = 0; k < 6; ++k) R.phase_ns[k] = 0;
         }
         sc.D = bc[0];
         sc.lo = 0.0;
@@ -1620,36 +1630,39 @@ __global__ void __launch_bounds__(256) attn_kernel(Views views, const float* __r
 }
 
 // LSE merge of the split partials of one query row: per-split scale factors are computed once (one
-// split per thread), then each thread sums its channel over the splits.
-__global__ void __launch_bounds__(kHeadDim) merge_kernel(DecodeArgs a, const float* __restrict__ part,
-                                                         float* __restrict__ out)
+// split per thread), then four groups of 128 threads each sum a quarter of the splits per channel.
+__global__ void __launch_bounds__(4 * kHeadDim) merge_kernel(DecodeArgs a, const float* __restrict__ part,
+                                                             float* __restrict__ out)
 {
     __shared__ float scl[128];
     __shared__ float red[32];
-    const int row = blockIdx.x, c = threadIdx.x;
+    __shared__ float accs[4][kHeadDim];
+    const int row = blockIdx.x, t = threadIdx.x, c = t % kHeadDim, grp = t / kHeadDim;
     const int ns = a.nsplit;
     const float* pp = part + (int64_t)row * ns * (kHeadDim + 2);
     float mx = -INFINITY;
-    for (int s = c; s < ns; s += blockDim.x) mx = fmaxf(mx, pp[s * (kHeadDim + 2) + kHeadDim]);
+    for (int s = t; s < ns; s += blockDim.x) mx = fmaxf(mx, pp[s * (kHeadDim + 2) + kHeadDim]);
     const float M = block_max(mx, red);
     float l = 0.f;
-    for (int s = c; s < ns; s += blockDim.x) {
+    for (int s = t; s < ns; s += blockDim.x) {
         const float m = pp[s * (kHeadDim + 2) + kHeadDim];
         const float f = m == -INFINITY ? 0.f : expf(m - M);
         scl[s] = f;
         l += pp[s * (kHeadDim + 2) + kHeadDim + 1] * f;
     }
     const float L = block_sum(l, red);
-    float A0 = 0.f, A1 = 0.f, A2 = 0.f, A3 = 0.f;
-    int s = 0;
-    for (; s + 4 <= ns; s += 4) {
+    const int q4 = (ns + 3) / 4;
+    const int s0 = min(ns, grp * q4), s1 = min(ns, s0 + q4);
+    float A0 = 0.f, A1 = 0.f;
+    int s = s0;
+    for (; s + 2 <= s1; s += 2) {
         A0 += pp[(s + 0) * (kHeadDim + 2) + c] * scl[s + 0];
         A1 += pp[(s + 1) * (kHeadDim + 2) + c] * scl[s + 1];
-        A2 += pp[(s + 2) * (kHeadDim + 2) + c] * scl[s + 2];
-        A3 += pp[(s + 3) * (kHeadDim + 2) + c] * scl[s + 3];
     }
-    for (; s < ns; ++s) A0 += pp[s * (kHeadDim + 2) + c] * scl[s];
-    out[(int64_t)row * kHeadDim + c] = ((A0 + A1) + (A2 + A3)) / L;
+    if (s < s1) A0 += pp[s * (kHeadDim + 2) + c] * scl[s];
+    accs[grp][c] = A0 + A1;
+    __syncthreads();
+    if (grp == 0) out[(int64_t)row * kHeadDim + c] = ((accs[0][c] + accs[1][c]) + (accs[2][c] + accs[3][c])) / L;
 }
 
 int g_decide_max_cluster = 8;  // largest cluster the decide kernel is launched with (set once)
@@ -1661,8 +1674,11 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
     const verkv_config& cfg = ctx.cfg;
     const int rowsN = B * a.Hq;
     VK_TIMING_BEGIN();
-    init_rows_kernel<<<(rowsN + 127) / 128, 128, 0, st>>>(ctx.rows, views, a, B);
-    VK_LAUNCHED("init_rows");
+    const bool on_chip = max_nl <= g_decide_max_cluster * kDecideCap;
+    if (!on_chip) {
+        init_rows_kernel<<<(rowsN + 127) / 128, 128, 0, st>>>(ctx.rows, views, a, B);
+        VK_LAUNCHED("init_rows");
+    }
     const dim3 gs((max_n + kTile - 1) / kTile, B * a.Hkv);
     if (cfg.sketch == VERKV_SKETCH_INT8)
         score_int8_kernel<G><<<gs, kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl);
@@ -1676,7 +1692,7 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
                                                                                             ctx.th);
         VK_LAUNCHED("score_h");
     }
-    if (max_nl <= g_decide_max_cluster * kDecideCap) {
+    if (on_chip) {
         int C = 1;
         while (C * kDecideCap < max_nl) C <<= 1;
         cudaLaunchConfig_t lc = {};
@@ -1718,7 +1734,7 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
     attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), 256, 0, st>>>(views, q, a, ctx.rows, ctx.wl, ctx.mark, ctx.ulist,
                                                                  ctx.ucount, (const T*)ctx.staging, ctx.part);
     VK_LAUNCHED("attn");
-    merge_kernel<<<rowsN, kHeadDim, 0, st>>>(a, ctx.part, out);
+    merge_kernel<<<rowsN, 4 * kHeadDim, 0, st>>>(a, ctx.part, out);
     VK_LAUNCHED("merge");
     return VERKV_OK;
 }

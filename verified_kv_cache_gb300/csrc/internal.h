@@ -48,7 +48,8 @@ struct Slot {
 
 // Per query row scalars of one decode (device).  Doubles are accumulated with atomics.
 struct RowState {
-    int m_ord;          // ordered-int of the logit shift m (max logit)
+    unsigned long long m_tag;  // (decode generation << 32) | order-preserving bits of the max logit m
+    int m_pad;
     int no_fetch;
     int kstar;
     int fallback;
