@@ -909,6 +909,23 @@ __device__ __forceinline__ void set_theta(DecideScalars& sc, double th)
 
 __device__ __forceinline__ unsigned int fmax_bits(float x) { return __float_as_uint(fmaxf(x, 0.f)); }
 
+// A non-negative fp32 value below 2^42, rounded to an integer and split into three 14-bit pieces with
+// fp32 arithmetic only (each step is exact: the value carries 24 significant bits).
+__device__ __forceinline__ void fixed_pieces(float x, unsigned* p)
+{
+    const float h2 = floorf(x * 0x1p-28f);
+    const float r2 = __fsub_rn(x, h2 * 0x1p28f);
+    const float h1 = floorf(r2 * 0x1p-14f);
+    const float r1 = rintf(__fsub_rn(r2, h1 * 0x1p14f));
+    // rounding can carry r1 to 2^14; fold the carry so every piece stays below 2^14
+    const float c1 = r1 >= 0x1p14f ? 1.f : 0.f;
+    const float h1c = h1 + c1, r1c = r1 - c1 * 0x1p14f;
+    const float c2 = h1c >= 0x1p14f ? 1.f : 0.f;
+    p[0] = (unsigned)r1c;
+    p[1] = (unsigned)(h1c - c2 * 0x1p14f);
+    p[2] = (unsigned)(h2 + c2);
+}
+
 __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, DecodeArgs a,
                                                                    RowState* __restrict__ rows,
                                                                    const float2* __restrict__ tl,
@@ -1190,12 +1207,13 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             if (act) {
                 // one shared-memory update per digit group; the fixed-point values (< 2^42) are split
                 // in 14-bit pieces so that every sum stays within 32 bits (8192 x 2^14 < 2^32)
-                const unsigned long long fa = __float2ull_rn(sa_[i]), fv = __float2ull_rn(sv_[i]);
-                unsigned ra[3], rv[3];
+                unsigned pa3[3], pv3[3], ra[3], rv[3];
+                fixed_pieces(sa_[i], pa3);
+                fixed_pieces(sv_[i], pv3);
 #pragma unroll
                 for (int q = 0; q < 3; ++q) {
-                    ra[q] = __reduce_add_sync(peers, (unsigned)((fa >> (14 * q)) & 0x3fff));
-                    rv[q] = __reduce_add_sync(peers, (unsigned)((fv >> (14 * q)) & 0x3fff));
+                    ra[q] = __reduce_add_sync(peers, pa3[q]);
+                    rv[q] = __reduce_add_sync(peers, pv3[q]);
                 }
                 const unsigned bm = __reduce_max_sync(peers, fmax_bits(sb[i]));
                 if ((__ffs(peers) - 1) == lane) {
@@ -1347,31 +1365,18 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         }
         __syncthreads();
         int nf = 0;
-        int off = sc.rem_cnt;
-        for (int i0 = 0; i0 < ns; i0 += T) {
-            const int i = i0 + tid;
-            const bool in = i < ns && skey[i] <= kk;
-            const unsigned bal = __ballot_sync(0xffffffffu, in);
-            if (lane == 0) wcnt[warp] = __popc(bal);
-            __syncthreads();
-            int wbase = 0, tot = 0;
-            for (int w2 = 0; w2 < (T >> 5); ++w2) {
-                if (w2 < warp) wbase += wcnt[w2];
-                tot += wcnt[w2];
+        if (tid == 0) wcnt[0] = sc.rem_cnt;  // running position in the exact list (order is irrelevant)
+        __syncthreads();
+        for (int i = tid; i < ns; i += T) {
+            if (skey[i] > kk) continue;
+            const int j = j0 + i;
+            const int tok = V.ltok[(int64_t)kv * V.n + j];
+            mark[(int64_t)row * a.ws_n + j] = a.gen;
+            elist[(int64_t)row * a.ws_n + atomicAdd(&wcnt[0], 1)] = tok;
+            if (V.flags[(int64_t)kv * V.n + tok] == 0) {
+                ++nf;
+                atomicOr(&a.ubits[(int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1) + (tok >> 5)], 1u << (tok & 31));
             }
-            if (in) {
-                const int j = j0 + i;
-                const int pos = off + wbase + __popc(bal & ((1u << lane) - 1));
-                const int tok = V.ltok[(int64_t)kv * V.n + j];
-                mark[(int64_t)row * a.ws_n + j] = a.gen;
-                elist[(int64_t)row * a.ws_n + pos] = tok;
-                if (V.flags[(int64_t)kv * V.n + tok] == 0) {
-                    ++nf;
-                    atomicOr(&a.ubits[(int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1) + (tok >> 5)], 1u << (tok & 31));
-                }
-            }
-            off += tot;
-            __syncthreads();
         }
         nf = block_sum(nf, redi);
         if (tid == 0) slot[parity].v[1] = (double)nf;
