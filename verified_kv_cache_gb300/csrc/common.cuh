@@ -81,6 +81,57 @@ __device__ __forceinline__ ff ff_mul(ff x, ff y)
 
 __device__ __forceinline__ ff ff_neg(ff x) { return {-x.hi, -x.lo}; }
 
+__device__ __forceinline__ ff ff_sub(ff x, ff y) { return ff_add(x, ff_neg(y)); }
+
+// x / y: the fp32 quotient corrected by one step on the float-float remainder (~2^-46 relative).
+__device__ __forceinline__ ff ff_div(ff x, ff y)
+{
+    const float q1 = __fdiv_rn(x.hi, y.hi);
+    const ff r = ff_sub(x, ff_mul_f(y, q1));
+    return fast_two_sum(q1, __fdiv_rn(r.hi, y.hi));
+}
+
+// sqrt(x) for x >= 0: the fp32 root corrected by one Newton step on the float-float residual.
+__device__ __forceinline__ ff ff_sqrt(ff x)
+{
+    if (!(x.hi > 0.f)) return {0.f, 0.f};
+    const float s = __fsqrt_rn(x.hi);
+    const ff e = ff_sub(x, two_prod(s, s));
+    return fast_two_sum(s, __fdiv_rn(e.hi, __fmul_rn(2.0f, s)));
+}
+
+// Comparisons of normalised float-float values (|lo| <= ulp(hi)/2).
+__device__ __forceinline__ bool ff_lt(ff x, ff y) { return x.hi < y.hi || (x.hi == y.hi && x.lo < y.lo); }
+__device__ __forceinline__ bool ff_eq(ff x, ff y) { return x.hi == y.hi && x.lo == y.lo; }
+__device__ __forceinline__ ff ff_min(ff x, ff y) { return ff_lt(y, x) ? y : x; }
+__device__ __forceinline__ ff ff_max(ff x, ff y) { return ff_lt(x, y) ? y : x; }
+
+// The binary64 value of a binary32 one, assembled from its bit fields (sign, exponent rebiased from
+// 127 to 1023, fraction widened by 29 bits; subnormals normalised): exact, and free of the
+// conversion instructions, which are slow on parts with few FP64 units.
+__device__ __forceinline__ double f32_to_f64_bits(float x)
+{
+    const unsigned u = __float_as_uint(x);
+    const unsigned long long sign = (unsigned long long)(u >> 31) << 63;
+    const unsigned e = (u >> 23) & 0xffu;
+    unsigned long long frac = u & 0x7fffffu;
+    unsigned long long bits;
+    if (e == 0xffu) {
+        bits = sign | (0x7ffull << 52) | (frac << 29);
+    } else if (e != 0u) {
+        bits = sign | ((unsigned long long)(e + 896u) << 52) | (frac << 29);
+    } else if (frac == 0ull) {
+        bits = sign;
+    } else {
+        // value = frac * 2^-149 with the top set bit at position p (0..22)
+        const int p = 31 - __clz((unsigned)frac);
+        bits = sign | ((unsigned long long)(p + 874) << 52) | ((frac << (52 - p)) & ((1ull << 52) - 1ull));
+    }
+    return __longlong_as_double((long long)bits);
+}
+
+__device__ __forceinline__ double ff_to_f64(ff x) { return f32_to_f64_bits(x.hi) + f32_to_f64_bits(x.lo); }
+
 __device__ __forceinline__ double ff_to_double(ff x) { return (double)x.hi + (double)x.lo; }
 
 __device__ __forceinline__ ff ff_from_double(double v)

@@ -31,6 +31,7 @@ struct DecodeArgs {
     int Hkv, Hq, G, ws_n, ws_npow2, gen, nsplit;
     float eps_f;
     double eps, ldelta;
+    ff eps_ff, ld_ff;   // eps and log(2/delta) as float-float
     float inv_sqrt_d_f;
     ff inv_sqrt_d;
 };
@@ -382,6 +383,9 @@ __device__ __forceinline__ float lambda_of(float w, float r, float beta)
 
 __device__ __forceinline__ Coef coef_of(float w, float r, float beta)
 {
+    // w = 0 (an underflowed weight) gives lambda = 1 and a = v = b = 0 exactly; returning early also
+    // keeps zero numerators away from the division's slow path
+    if (!(w > 0.f)) return {0.f, 0.f, 0.f};
     const float lam = lambda_of(w, r, beta);
     Coef c;
     c.a = __fmul_rn(w, __fsub_rn(1.0f, lam));
@@ -473,6 +477,7 @@ __global__ void __launch_bounds__(1024) beta_kernel(Views views, DecodeArgs a, R
         const double t = (double)B1 * ld / 3.0;
         const double eh = nl > 0 ? (SA + t + sqrt(t * t + 2.0 * SV * ld)) / R.D : 0.0;
         R.beta = beta;
+        R.beta_f = bf;
         R.sum_a = SA;
         R.V = SV;
         R.b1 = nl > 0 ? B1 : 0.0;
@@ -830,28 +835,113 @@ __global__ void __launch_bounds__(1024) fallback_kernel(Views views, DecodeArgs 
 //   phase 1: Definition 2's fixed point by safeguarded Newton on G(beta) = beta (1 + R) - A - W,
 //            started above the root (four times the all-interior solution).
 //   phase 2: a_i, v_i, b_i; eq. (7); the no-fetch test (Algorithm 2, lines 2-5).
-//   phase 3: gain keys (eq. (9)) and k* (eq. (10)) by an MSD radix search over the keys: per
-//            8-bit digit, a cluster-wide histogram of counts, exact fixed-point sums of a_i and v_i
-//            and the max of b_i gives the residual certificate at every bin boundary, so the bin
-//            holding the k*-th key is found without sorting; the search stops once that bin holds
-//            one key.
+//   phase 3: gain keys (eq. (9)) and k* (eq. (10)) by an MSD radix search over the 48-bit keys
+//            (gain descending, L index ascending): per 11-bit digit, a cluster-wide histogram of
+//            counts, exact fixed-point sums of a_i and v_i and the max of b_i (plain 32-bit shared
+//            atomics) gives the residual certificate at every bin boundary, so the bin holding the
+//            k*-th key is found without sorting; the search stops once that bin holds one key.
 //   phase 4: E = L_g[:k*] = the keys up to the k*-th, written as marks and a token list.
 // --------------------------------------------------------------------------------------------
 constexpr int kDecideThreads = 1024;
 constexpr int kDecideCap = 8192;   // L entries per CTA
 constexpr int kDecideMaxCluster = 16;  // 16 is a non-portable cluster size: used when the GPU can run it
-constexpr size_t kDecideSmem = (size_t)kDecideCap * (4 + 4 + 8 + 4);
+// k* search: keys of 31 gain bits and 17 index bits, digits of 11 bits (the last level takes 4)
+constexpr int kKeyBits = 48;
+constexpr int kSearchBits = 11;
+constexpr int kSearchLevels = 5;
+constexpr int kSearchBins = 1 << kSearchBits;
+// histogram fields per bin: count, max b, three 14-bit pieces of sum a, three of sum v
+constexpr int kSearchFields = 8;
+constexpr size_t kDecideSmem = (size_t)kDecideCap * 16 + (size_t)kSearchFields * kSearchBins * 4;
+static_assert(kDecideCap * kDecideMaxCluster <= (1 << (kKeyBits - 31)), "L index must fit the key's low bits");
 
 struct DecideSlot {
-    double v[8];
-    unsigned int cnt[256];
-    unsigned int pa[3][256], pv[3][256];  // 14-bit pieces of the fixed-point sums of a_i and v_i
-    unsigned int mb[256];
+    ff v[8];
+    float f[4];
+    int i[4];
 };
 
-// Block-wide sums of N float-float values at once (two barriers); every thread gets the totals.
+// The two largest b_i of a set and the (lowest) L index of the largest.
+struct Top2 {
+    float b1, b2;
+    int arg;
+};
+
+__device__ __forceinline__ Top2 top2_merge(const Top2& x, const Top2& y)
+{
+    if (y.b1 > x.b1 || (y.b1 == x.b1 && y.arg < x.arg)) return {y.b1, fmaxf(y.b2, x.b1), y.arg};
+    return {x.b1, fmaxf(x.b2, y.b1), x.arg};
+}
+
+__device__ __forceinline__ Top2 shfl_xor_top2(const Top2& x, int o)
+{
+    return {__shfl_xor_sync(0xffffffffu, x.b1, o), __shfl_xor_sync(0xffffffffu, x.b2, o),
+            __shfl_xor_sync(0xffffffffu, x.arg, o)};
+}
+
+// Sort key of an L entry: ~bits(D g_i) (gain descending; g_i >= 0 so the sign bit is dropped), then
+// the L index ascending.
+__device__ __forceinline__ unsigned long long search_key(unsigned key32, int j)
+{
+    return ((unsigned long long)(key32 & 0x7fffffffu) << (kKeyBits - 31)) | (unsigned)j;
+}
+
+struct SearchAcc {
+    unsigned long long a, v;  // fixed-point sums
+    unsigned b, c;            // max b (ordered bits), count
+};
+
+// A CTA's proposal for the level's boundary: the residual after its first acceptable bin.
+struct SearchProp {
+    unsigned long long a, v;
+    unsigned b, c, in_bin;
+    int cand;                 // the bin (0x7fffffff: none in this CTA's slice)
+};
+
+__device__ __forceinline__ SearchAcc search_add(const SearchAcc& x, const SearchAcc& y)
+{
+    return {x.a + y.a, x.v + y.v, max(x.b, y.b), x.c + y.c};
+}
+
+__device__ __forceinline__ SearchAcc shfl_down_acc(const SearchAcc& x, int o)
+{
+    return {__shfl_down_sync(0xffffffffu, x.a, o), __shfl_down_sync(0xffffffffu, x.v, o),
+            __shfl_down_sync(0xffffffffu, x.b, o), __shfl_down_sync(0xffffffffu, x.c, o)};
+}
+
+// Block-wide exclusive suffix (the combination over threads with a higher index).
+__device__ SearchAcc block_suffix_search(const SearchAcc& mine, SearchAcc* sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const SearchAcc zero = {0ull, 0ull, 0u, 0u};
+    SearchAcc x = mine;
+    for (int o = 1; o < 32; o <<= 1) {
+        const SearchAcc y = shfl_down_acc(x, o);
+        if (lane + o < 32) x = search_add(x, y);
+    }
+    if (lane == 0) sh[warp] = x;   // warp total
+    SearchAcc r = shfl_down_acc(x, 1);
+    if (lane == 31) r = zero;
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive suffix over the warp totals
+        SearchAcc t = lane < nw ? sh[lane] : zero;
+        for (int o = 1; o < 32; o <<= 1) {
+            const SearchAcc y = shfl_down_acc(t, o);
+            if (lane + o < 32) t = search_add(t, y);
+        }
+        SearchAcc e = shfl_down_acc(t, 1);
+        if (lane == 31) e = zero;
+        __syncwarp();
+        if (lane < nw) sh[32 + lane] = e;
+    }
+    __syncthreads();
+    return search_add(r, sh[32 + warp]);
+}
+
+// Block-wide sums of N float-float values at once (two barriers); the totals end in warp 0.
 template <int N>
-__device__ __forceinline__ void block_sum_ff_n(ff (&v)[N], ff* scratch)
+__device__ __forceinline__ void block_sum_ff_w0(ff (&v)[N], ff* scratch)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
     for (int o = 16; o > 0; o >>= 1)
@@ -862,21 +952,23 @@ __device__ __forceinline__ void block_sum_ff_n(ff (&v)[N], ff* scratch)
 #pragma unroll
         for (int k = 0; k < N; ++k) scratch[warp * N + k] = v[k];
     __syncthreads();
+    if (warp == 0) {
 #pragma unroll
-    for (int k = 0; k < N; ++k) v[k] = lane < nw ? scratch[lane * N + k] : ff{0.f, 0.f};
-    for (int o = 16; o > 0; o >>= 1)
+        for (int k = 0; k < N; ++k) v[k] = lane < nw ? scratch[lane * N + k] : ff{0.f, 0.f};
+        for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-        for (int k = 0; k < N; ++k) v[k] = ff_add(v[k], shfl_xor_ff(v[k], o));
+            for (int k = 0; k < N; ++k) v[k] = ff_add(v[k], shfl_xor_ff(v[k], o));
+    }
 }
 
 __device__ __forceinline__ void cluster_combine(cg::cluster_group& cl, DecideSlot* slot, int parity, int nv,
-                                                double* out)
+                                                ff* out)
 {
     // thread 0 of every CTA has written slot[parity].v[0..nv); sum them in rank order
     cl.sync();
     if (threadIdx.x < nv) {
-        double s = 0.0;
-        for (unsigned rk = 0; rk < cl.num_blocks(); ++rk) s += cl.map_shared_rank(slot, rk)[parity].v[threadIdx.x];
+        ff s = {0.f, 0.f};
+        for (unsigned rk = 0; rk < cl.num_blocks(); ++rk) s = ff_add(s, cl.map_shared_rank(slot, rk)[parity].v[threadIdx.x]);
         out[threadIdx.x] = s;
     }
     __syncthreads();
@@ -884,7 +976,7 @@ __device__ __forceinline__ void cluster_combine(cg::cluster_group& cl, DecideSlo
 
 // Scalars of one row, computed by thread 0 of each CTA and broadcast through shared memory.
 struct DecideScalars {
-    double theta, lo, hi, D;
+    ff theta, lo, hi, D;
     float th_up, th_dn;        // theta rounded up / down: alpha >= theta <=> alpha >= th_up, gamma > theta <=> gamma > th_dn
     int done;
     float bf;                  // beta in fp32
@@ -892,19 +984,21 @@ struct DecideScalars {
     int arg, no_fetch;
     float Df, ldf, sa_scale, sv_scale;  // fixed-point scales: a_i * sa_scale, v_i * sv_scale (totals ~2^40)
     // radix search state
-    unsigned long long prefix, pmask;
+    unsigned long long prefix;          // key bits fixed so far
     int rem_cnt;                        // keys below the current prefix range (removed)
     unsigned long long rest_a, rest_v;  // keys above the current prefix range (kept), fixed point
-    unsigned int rest_b;                // max b over them (ordered float bits)
+    unsigned int rest_b, rest_c;        // max b over them (ordered float bits), their count
     int kstar, found;
     unsigned long long kkey;            // the k*-th smallest key
 };
 
-__device__ __forceinline__ void set_theta(DecideScalars& sc, double th)
+// theta >= 0 is a normalised float-float (hi = RN(hi + lo)), so the smallest float >= theta is hi, or
+// the next float up when lo > 0; the largest float <= theta is hi, or the next float down when lo < 0.
+__device__ __forceinline__ void set_theta(DecideScalars& sc, ff th)
 {
     sc.theta = th;
-    sc.th_up = __double2float_ru(th);
-    sc.th_dn = __double2float_rd(th);
+    sc.th_up = th.lo > 0.f ? __uint_as_float(__float_as_uint(th.hi) + 1u) : th.hi;
+    sc.th_dn = th.lo < 0.f ? __uint_as_float(__float_as_uint(th.hi) - 1u) : th.hi;
 }
 
 __device__ __forceinline__ unsigned int fmax_bits(float x) { return __float_as_uint(fmaxf(x, 0.f)); }
@@ -939,25 +1033,27 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const int rank = (int)cl.block_rank();
     const int row = blockIdx.x / C;
     extern __shared__ __align__(16) unsigned char dsm[];
-    // region A: w^, r (phases 0-2) -> a_i, v_i (phase 3); region B: gamma, rho -> keys; region C: b_i
+    // w^, r (phases 0-2) -> scaled a_i, v_i (phase 3); gamma, rho -> gain keys, b_i; then the histogram
     float* sw = reinterpret_cast<float*>(dsm);
     float* sr = sw + kDecideCap;
     float* sg = sr + kDecideCap;
     float* sp = sg + kDecideCap;
-    unsigned long long* skey = reinterpret_cast<unsigned long long*>(sg);
-    float* sb = sp + kDecideCap;
+    unsigned* skey = reinterpret_cast<unsigned*>(sg);
+    float* sb = sp;
     float* sa_ = sw;
     float* sv_ = sr;
+    unsigned* hist = reinterpret_cast<unsigned*>(sp + kDecideCap);  // [kSearchFields][kSearchBins]
     __shared__ DecideSlot slot[2];
-    __shared__ double bc[8];
+    __shared__ ff bc[8];
     __shared__ ff redff[32 * 4];
+    __shared__ Top2 stop2[32];
     __shared__ float redf[32];
     __shared__ int redi[32];
     __shared__ DecideScalars sc;
     __shared__ int wcnt[32];
-    __shared__ int tot_c[256];
-    __shared__ unsigned long long tot_a[256], tot_v[256];
-    __shared__ unsigned int tot_b[256];
+    __shared__ SearchAcc sacc[64];
+    __shared__ SearchAcc ssum;   // this CTA's slice total at the current search level
+    __shared__ SearchProp sprop;
     const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31, warp = tid >> 5;
     const int b = row / a.Hq, kv = (row % a.Hq) / a.G;
     const SlotView& V = views.v[b];
@@ -981,45 +1077,68 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     // ---- phase 0: weights and the row totals
     {
         ff acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // D, sum w, sum alpha, sum rho
-        for (int i = tid; i < ns; i += T) {
-            const int j = j0 + i;
-            const float w = weight_of(tl[(int64_t)row * a.ws_n + j], m);
-            const float r = rl[j];
+        const float2* tlr = tl + (int64_t)row * a.ws_n + j0;
+        const float* rlr = rl + j0;
+        float* wlr = wl + (int64_t)row * a.ws_n + j0;
+        // all loads of a thread issued before any is used
+        float2 tv[8];
+        float rv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + k * T;
+            tv[k] = i < ns ? tlr[i] : make_float2(0.f, 0.f);
+            rv[k] = i < ns ? rlr[i] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + k * T;
+            if (i >= ns) break;
+            const float w = weight_of(tv[k], m);
+            const float r = rv[k];
             sw[i] = w;
             sr[i] = r;
-            wl[(int64_t)row * a.ws_n + j] = w;
+            wlr[i] = w;
             const float al = __fmul_rn(w, __fsub_rn(1.0f, r));
             const float rho = __fdiv_rn(r, __fsub_rn(1.0f, r));
-            sg[i] = __fdiv_rn(al, r);
+            sg[i] = w > 0.f ? __fdiv_rn(al, r) : 0.f;
             sp[i] = rho;
             acc[0] = ff_add_f(acc[0], w);
             acc[1] = ff_add_f(acc[1], w);
             acc[2] = ff_add(acc[2], two_prod(w, __fsub_rn(1.0f, r)));
             acc[3] = ff_add_f(acc[3], rho);
         }
-        if (rank == 0)
-            for (int k = tid; k < nh; k += T) acc[0] = ff_add_f(acc[0], weight_of(th[(int64_t)row * a.ws_n + k], m));
-        block_sum_ff_n<4>(acc, redff);
+        if (rank == 0) {
+            const float2* thr = th + (int64_t)row * a.ws_n;
+            for (int k0 = tid; k0 < nh; k0 += 4 * T) {
+                float2 hv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) hv[u] = k0 + u * T < nh ? thr[k0 + u * T] : make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (k0 + u * T < nh) acc[0] = ff_add_f(acc[0], weight_of(hv[u], m));
+            }
+        }
+        block_sum_ff_w0<4>(acc, redff);
         if (tid == 0)
-            for (int k = 0; k < 4; ++k) slot[parity].v[k] = ff_to_double(acc[k]);
+            for (int k = 0; k < 4; ++k) slot[parity].v[k] = acc[k];
     }
     cluster_combine(cl, slot, parity, 4, bc);
     parity ^= 1;
     if (tid == 0) {
-        const double At = bc[2];
+        const ff At = bc[2];
         if (rank == 0) {
-            R.D = bc[0];
-            R.alpha_sum = At;
+            R.D = ff_to_f64(bc[0]);
+            R.alpha_sum = ff_to_f64(At);
             R.n_l = nl;
             R.n_h = nh;
             R.sel_passes = 0;
             for (int k = 0; k < 6; ++k) R.phase_ns[k] = 0;
         }
         sc.D = bc[0];
-        sc.lo = 0.0;
+        sc.lo = ff{0.f, 0.f};
         sc.hi = At;
-        set_theta(sc, fmin(At, 4.0 * bc[1] / (1.0 + bc[3])));
-        sc.done = (nl == 0 || !(At > 0.0));
+        set_theta(sc, ff_min(At, ff_div(ff_mul_f(bc[1], 4.0f), ff_add_f(bc[3], 1.0f))));
+        sc.done = (nl == 0 || !(At.hi > 0.f));
     }
     __syncthreads();
     stamp(0);
@@ -1040,118 +1159,109 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                 acc[2] = ff_add_f(acc[2], sp[i]);
             }
         }
-        block_sum_ff_n<3>(acc, redff);
+        block_sum_ff_w0<3>(acc, redff);
         if (tid == 0)
-            for (int k = 0; k < 3; ++k) slot[parity].v[k] = ff_to_double(acc[k]);
+            for (int k = 0; k < 3; ++k) slot[parity].v[k] = acc[k];
         cluster_combine(cl, slot, parity, 3, bc);
         parity ^= 1;
         if (tid == 0) {
-            const double theta = sc.theta;
-            const double Ad = bc[0], Wd = bc[1], Rd = bc[2];
-            const double g = theta * (1.0 + Rd) - Ad - Wd;
-            if (g >= 0.0) sc.hi = fmin(sc.hi, theta); else sc.lo = fmax(sc.lo, theta);
-            double nt = (Ad + Wd) / (1.0 + Rd);
-            if (nt == theta || iters >= 200) sc.done = 1;
+            const ff theta = sc.theta;
+            const ff AW = ff_add(bc[0], bc[1]), oneR = ff_add_f(bc[2], 1.0f);
+            const ff g = ff_sub(ff_mul(theta, oneR), AW);
+            if (g.hi >= 0.f) sc.hi = ff_min(sc.hi, theta); else sc.lo = ff_max(sc.lo, theta);
+            ff nt = ff_div(AW, oneR);
+            if (ff_eq(nt, theta) || iters >= 200) sc.done = 1;
             else {
-                if (!(nt > sc.lo && nt < sc.hi)) nt = sc.lo > 0.0 ? sqrt(sc.lo * sc.hi) : 0.5 * (sc.lo + sc.hi);
-                if (nt == theta || sc.hi - sc.lo <= 1e-16 * sc.hi) sc.done = 1;
+                if (!(ff_lt(sc.lo, nt) && ff_lt(nt, sc.hi)))
+                    nt = sc.lo.hi > 0.f ? ff_sqrt(ff_mul(sc.lo, sc.hi)) : ff_mul_f(ff_add(sc.lo, sc.hi), 0.5f);
+                if (ff_eq(nt, theta) || ff_sub(sc.hi, sc.lo).hi <= 0x1p-44f * sc.hi.hi) sc.done = 1;
                 set_theta(sc, nt);
             }
         }
         __syncthreads();
     }
     if (tid == 0) {
-        const double beta = nl > 0 ? sc.theta : 0.0;
-        sc.theta = beta;
-        sc.bf = (float)beta;
+        if (nl == 0) sc.theta = ff{0.f, 0.f};
+        sc.bf = sc.theta.hi;
     }
     __syncthreads();
     const float bf = sc.bf;
     stamp(1);
 
     // ---- phase 2: eq. (7)
-    float b1 = 0.f, b2 = 0.f;
-    int arg = 0x7fffffff;
     {
         ff acc[2] = {{0.f, 0.f}, {0.f, 0.f}};
+        Top2 t2 = {0.f, 0.f, 0x7fffffff};
         for (int i = tid; i < ns; i += T) {
             const Coef c = coef_of(sw[i], sr[i], bf);
             acc[0] = ff_add_f(acc[0], c.a);
             acc[1] = ff_add_f(acc[1], c.v);
             const int j = j0 + i;
-            if (c.b > b1 || (c.b == b1 && j < arg)) { b2 = b1; b1 = c.b; arg = j; }
-            else if (c.b > b2) b2 = c.b;
+            if (c.b > t2.b1 || (c.b == t2.b1 && j < t2.arg)) { t2.b2 = t2.b1; t2.b1 = c.b; t2.arg = j; }
+            else if (c.b > t2.b2) t2.b2 = c.b;
         }
-        block_sum_ff_n<2>(acc, redff);
-        if (tid == 0) {
-            slot[parity].v[0] = ff_to_double(acc[0]);
-            slot[parity].v[1] = ff_to_double(acc[1]);
+        for (int o = 16; o > 0; o >>= 1) t2 = top2_merge(t2, shfl_xor_top2(t2, o));
+        if (lane == 0) stop2[warp] = t2;
+        block_sum_ff_w0<2>(acc, redff);   // its barriers also publish stop2
+        if (warp == 0) {
+            Top2 x = stop2[lane];
+            for (int o = 16; o > 0; o >>= 1) x = top2_merge(x, shfl_xor_top2(x, o));
+            if (tid == 0) {
+                slot[parity].v[0] = acc[0];
+                slot[parity].v[1] = acc[1];
+                slot[parity].f[0] = x.b1;
+                slot[parity].f[1] = x.b2;
+                slot[parity].i[0] = x.arg;
+            }
         }
-    }
-    const float B1l = block_max(b1, redf);
-    int cnd = (b1 == B1l) ? arg : 0x7fffffff;
-    __syncthreads();
-    for (int o = 16; o > 0; o >>= 1) cnd = min(cnd, __shfl_xor_sync(0xffffffffu, cnd, o));
-    if (lane == 0) redi[warp] = cnd;
-    __syncthreads();
-    cnd = lane < (T >> 5) ? redi[lane] : 0x7fffffff;
-    for (int o = 16; o > 0; o >>= 1) cnd = min(cnd, __shfl_xor_sync(0xffffffffu, cnd, o));
-    const int ARGl = cnd;
-    const float B2l = block_max((arg == ARGl) ? b2 : b1, redf);
-    if (tid == 0) {
-        slot[parity].v[2] = (double)B1l;
-        slot[parity].v[3] = (double)B2l;
-        slot[parity].v[4] = (double)ARGl;
     }
     cluster_combine(cl, slot, parity, 2, bc);
     if (tid == 0) {
-        // the two largest b across the cluster (lowest index among equal maxima)
-        float B1 = 0.f, B2 = 0.f;
-        int ARG = 0x7fffffff;
+        // the two largest b across the cluster (lowest index among equal maxima), merged in rank order
+        Top2 x = {0.f, 0.f, 0x7fffffff};
         for (int rk = 0; rk < C; ++rk) {
             const DecideSlot* rs = cl.map_shared_rank(slot, rk);
-            const float x1 = (float)rs[parity].v[2];
-            const int xa = (int)rs[parity].v[4];
-            if (x1 > B1 || (x1 == B1 && xa < ARG)) { B1 = x1; ARG = xa; }
+            x = top2_merge(x, Top2{rs[parity].f[0], rs[parity].f[1], rs[parity].i[0]});
         }
-        for (int rk = 0; rk < C; ++rk) {
-            const DecideSlot* rs = cl.map_shared_rank(slot, rk);
-            B2 = fmaxf(B2, (int)rs[parity].v[4] == ARG ? (float)rs[parity].v[3] : (float)rs[parity].v[2]);
-        }
-        const double SA = bc[0], SV = bc[1], ld = a.ldelta;
-        const double t3 = (double)B1 * ld / 3.0;
-        const double eh = nl > 0 ? (SA + t3 + sqrt(t3 * t3 + 2.0 * SV * ld)) / sc.D : 0.0;
-        sc.no_fetch = (eh < a.eps) || nl == 0;
-        sc.arg = ARG;
-        const double t2 = (nl > 1 ? (double)B2 : 0.0) * ld / 3.0;
-        const double Aq = t3 * t3 + 2.0 * SV * ld;
-        sc.gp.t = (float)t3;
-        sc.gp.tm2 = (float)t2;
-        sc.gp.A = (float)Aq;
-        sc.gp.sqrtA = (float)sqrt(Aq);
-        sc.gp.ld2 = (float)(2.0 * ld);
-        sc.ldf = (float)ld;
-        sc.Df = (float)sc.D;
-        sc.sa_scale = SA > 0.0 ? (float)(0x1p40 / SA) : 0.f;
-        sc.sv_scale = SV > 0.0 ? (float)(0x1p40 / SV) : 0.f;
+        const float B1 = x.b1, B2 = nl > 1 ? x.b2 : 0.f;
+        const ff SA = bc[0], SV = bc[1], ld = a.ld_ff;
+        const ff three = {3.0f, 0.f};
+        const ff t3 = ff_div(ff_mul_f(ld, B1), three);
+        const ff Aq = ff_add(ff_mul(t3, t3), ff_mul_f(ff_mul(SV, ld), 2.0f));
+        const ff sq = ff_sqrt(Aq);
+        const ff eh = nl > 0 ? ff_div(ff_add(ff_add(SA, t3), sq), sc.D) : ff{0.f, 0.f};
+        const bool nof = ff_lt(eh, a.eps_ff);
+        sc.no_fetch = nof || nl == 0;
+        sc.arg = x.arg;
+        const ff t2 = ff_div(ff_mul_f(ld, B2), three);
+        sc.gp.t = t3.hi;
+        sc.gp.tm2 = t2.hi;
+        sc.gp.A = Aq.hi;
+        sc.gp.sqrtA = sq.hi;
+        sc.gp.ld2 = __fmul_rn(2.0f, ld.hi);
+        sc.ldf = ld.hi;
+        sc.Df = sc.D.hi;
+        sc.sa_scale = SA.hi > 0.f ? __fdiv_rn(0x1p40f, SA.hi) : 0.f;
+        sc.sv_scale = SV.hi > 0.f ? __fdiv_rn(0x1p40f, SV.hi) : 0.f;
         sc.prefix = 0;
-        sc.pmask = 0;
         sc.rem_cnt = 0;
         sc.rest_a = 0;
         sc.rest_v = 0;
         sc.rest_b = 0;
+        sc.rest_c = 0;
         sc.found = 0;
         sc.kstar = nl;
         sc.kkey = ~0ull;
         if (rank == 0) {
-            R.beta = sc.theta;
-            R.sum_a = SA;
-            R.V = SV;
-            R.b1 = nl > 0 ? B1 : 0.0;
-            R.b2 = nl > 1 ? B2 : 0.0;
-            R.b_arg = nl > 0 ? ARG : -1;
-            R.eps_hat = eh;
-            R.no_fetch = eh < a.eps;
+            R.beta = ff_to_f64(sc.theta);
+            R.beta_f = bf;
+            R.sum_a = ff_to_f64(SA);
+            R.V = ff_to_f64(SV);
+            R.b1 = nl > 0 ? f32_to_f64_bits(B1) : 0.0;
+            R.b2 = f32_to_f64_bits(B2);
+            R.b_arg = nl > 0 ? x.arg : -1;
+            R.eps_hat = ff_to_f64(eh);
+            R.no_fetch = nof;
             R.kstar = 0;
             R.fallback = 0;
             R.n_fetch = 0;
@@ -1173,217 +1283,213 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         const float fa = sc.sa_scale, fv = sc.sv_scale;
         for (int i = tid; i < ns; i += T) {
             const Coef c = coef_of(sw[i], sr[i], bf);
-            const unsigned long long k = gain_key(gain_num(c, j0 + i, ARG, gp), j0 + i);
+            skey[i] = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
             sa_[i] = __fmul_rn(c.a, fa);   // fixed-point-scaled a_i, v_i (exactly converted below)
             sv_[i] = __fmul_rn(c.v, fv);
             sb[i] = c.b;
-            skey[i] = k;
         }
     }
-    __syncthreads();
     stamp(3);
-    const float ldf = sc.ldf, Df = sc.Df, inv_fa = sc.sa_scale > 0.f ? 1.0f / sc.sa_scale : 0.f,
-                inv_fv = sc.sv_scale > 0.f ? 1.0f / sc.sv_scale : 0.f;
-    int passes = 0;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-        ++passes;
-        DecideSlot& my = slot[parity];
-        for (int dd = tid; dd < 256; dd += T) {
-            my.cnt[dd] = 0;
-            my.pa[0][dd] = my.pa[1][dd] = my.pa[2][dd] = 0;
-            my.pv[0][dd] = my.pv[1][dd] = my.pv[2][dd] = 0;
-            my.mb[dd] = 0;
-        }
-        __syncthreads();
-        const unsigned long long prefix = sc.prefix, pmask = sc.pmask;
-        for (int i0 = 0; i0 < ns; i0 += T) {
-            // every lane of a warp runs the same iterations, so the warp can aggregate per digit
-            const int i = i0 + tid;
-            const unsigned long long k = i < ns ? skey[i] : ~0ull;
-            const bool act = i < ns && (k & pmask) == prefix;
-            if (!__any_sync(0xffffffffu, act)) continue;
-            const unsigned dig = act ? (unsigned)((k >> shift) & 255) : 256u + (unsigned)lane;
-            const unsigned peers = __match_any_sync(0xffffffffu, dig);
-            if (act) {
-                // one shared-memory update per digit group; the fixed-point values (< 2^42) are split
-                // in 14-bit pieces so that every sum stays within 32 bits (8192 x 2^14 < 2^32)
-                unsigned pa3[3], pv3[3], ra[3], rv[3];
-                fixed_pieces(sa_[i], pa3);
-                fixed_pieces(sv_[i], pv3);
+    {
+        const float ldf = sc.ldf, Df = sc.Df, inv_fa = sc.sa_scale > 0.f ? 1.0f / sc.sa_scale : 0.f,
+                    inv_fv = sc.sv_scale > 0.f ? 1.0f / sc.sv_scale : 0.f;
+        const SearchAcc zero = {0ull, 0ull, 0u, 0u};
+        int passes = 0;
+        uint4* hist4 = reinterpret_cast<uint4*>(hist);
+        for (int k = tid; k < kSearchFields * kSearchBins / 4; k += T) hist4[k] = make_uint4(0u, 0u, 0u, 0u);
+        cl.sync();   // every histogram of the cluster is zero before any CTA adds to a remote one
+        for (int lev = 0; lev < kSearchLevels; ++lev) {
+            ++passes;
+            const int width = lev < kSearchLevels - 1 ? kSearchBits : kKeyBits - kSearchBits * (kSearchLevels - 1);
+            const int shift = kKeyBits - kSearchBits * lev - width;
+            const int nb = 1 << width;
+            const int sl = nb / C;   // bins per slice: CTA r owns the cluster totals of bins [r sl, (r + 1) sl)
+            const unsigned long long hi = sc.prefix;
+            const int up = shift + width;
+            for (int i = tid; i < ns; i += T) {
+                const unsigned long long K = search_key(skey[i], j0 + i);
+                if ((K >> up) != hi) continue;
+                const unsigned d = (unsigned)(K >> shift) & (unsigned)(nb - 1);
+                unsigned pa[3], pv[3];
+                fixed_pieces(sa_[i], pa);
+                fixed_pieces(sv_[i], pv);
+                atomicAdd(&hist[d], 1u);
+                atomicMax(&hist[kSearchBins + d], fmax_bits(sb[i]));
 #pragma unroll
                 for (int q = 0; q < 3; ++q) {
-                    ra[q] = __reduce_add_sync(peers, pa3[q]);
-                    rv[q] = __reduce_add_sync(peers, pv3[q]);
-                }
-                const unsigned bm = __reduce_max_sync(peers, fmax_bits(sb[i]));
-                if ((__ffs(peers) - 1) == lane) {
-                    atomicAdd(&my.cnt[dig], (unsigned)__popc(peers));
-#pragma unroll
-                    for (int q = 0; q < 3; ++q) {
-                        atomicAdd(&my.pa[q][dig], ra[q]);
-                        atomicAdd(&my.pv[q][dig], rv[q]);
-                    }
-                    atomicMax(&my.mb[dig], bm);
+                    atomicAdd(&hist[(2 + q) * kSearchBins + d], pa[q]);
+                    atomicAdd(&hist[(5 + q) * kSearchBins + d], pv[q]);
                 }
             }
-        }
-        cl.sync();
-        // cluster totals per bin: one bin per thread
-        if (tid < 256) {
-            int c = 0;
-            unsigned long long sa2 = 0, sv2 = 0;
-            unsigned int mb2 = 0;
-            for (int rk = 0; rk < C; ++rk) {
-                const DecideSlot& rs = cl.map_shared_rank(slot, rk)[parity];
-                c += (int)rs.cnt[tid];
+            __syncthreads();
+            if (C > 1) {
+                // add the non-empty bins of the other slices into their owners' histograms
+                for (int d = tid; d < nb; d += T) {
+                    const int ow = d / sl;
+                    const unsigned cnt = hist[d];
+                    if (ow == rank || cnt == 0u) continue;
+                    unsigned* dst = cl.map_shared_rank(hist, ow);
+                    atomicAdd(dst + d, cnt);
+                    atomicMax(dst + kSearchBins + d, hist[kSearchBins + d]);
+#pragma unroll
+                    for (int f = 2; f < kSearchFields; ++f) atomicAdd(dst + f * kSearchBins + d, hist[f * kSearchBins + d]);
+                }
+                cl.sync();
+            }
+            // cluster totals of this CTA's bins d0 = rank sl + 2 tid and d0 + 1
+            const int d0 = rank * sl + 2 * tid;
+            unsigned c2[2] = {0u, 0u}, b2[2] = {0u, 0u};
+            unsigned long long a2[2] = {0ull, 0ull}, v2[2] = {0ull, 0ull};
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (2 * tid + k >= sl) break;   // a slice of one bin (16 CTAs at the last level)
+                const int d = d0 + k;
+                c2[k] = hist[d];
+                b2[k] = hist[kSearchBins + d];
 #pragma unroll
                 for (int q = 0; q < 3; ++q) {
-                    sa2 += (unsigned long long)rs.pa[q][tid] << (14 * q);
-                    sv2 += (unsigned long long)rs.pv[q][tid] << (14 * q);
-                }
-                mb2 = max(mb2, rs.mb[tid]);
-            }
-            tot_c[tid] = c;
-            tot_a[tid] = sa2;
-            tot_v[tid] = sv2;
-            tot_b[tid] = mb2;
-        }
-        __syncthreads();
-        // warp 0: the first boundary whose residual certificate is below eps
-        if (warp == 0) {
-            int c8[8];
-            unsigned long long a8[8], v8[8];
-            unsigned int b8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int dd = lane * 8 + k;
-                c8[k] = tot_c[dd];
-                a8[k] = tot_a[dd];
-                v8[k] = tot_v[dd];
-                b8[k] = tot_b[dd];
-            }
-            // suffix (higher bins = smaller gains) sums over the lanes above, then within the lane
-            unsigned long long la = 0, lv = 0;
-            unsigned int lb = 0;
-            int lc = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) { la += a8[k]; lv += v8[k]; lb = max(lb, b8[k]); lc += c8[k]; }
-            unsigned long long xa = la, xv = lv;
-            unsigned int xb = lb;
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long ya = __shfl_down_sync(0xffffffffu, xa, o);
-                const unsigned long long yv = __shfl_down_sync(0xffffffffu, xv, o);
-                const unsigned int yb = __shfl_down_sync(0xffffffffu, xb, o);
-                if (lane + o < 32) { xa += ya; xv += yv; xb = max(xb, yb); }
-            }
-            // xa: sum over lanes >= lane; exclusive part above this lane:
-            unsigned long long above_a = xa - la, above_v = xv - lv;
-            unsigned int above_b = __shfl_down_sync(0xffffffffu, xb, 1);
-            if (lane == 31) above_b = 0;
-            // prefix count of bins below this lane (removed when this lane's bins are reached)
-            int cincl = lc;
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, cincl, o);
-                if (lane >= o) cincl += y;
-            }
-            int cbelow = cincl - lc;
-            // boundary after bin d of this lane: rest = bins > d of the range + the kept part outside it
-            int first = 0x7fffffff, cnt_through = 0;
-            unsigned long long ra = sc.rest_a + above_a, rv = sc.rest_v + above_v;
-            unsigned int rb = max(sc.rest_b, above_b);
-            // walk this lane's bins from the top down to build the rest after each bin
-            unsigned long long suf_a[8], suf_v[8];
-            unsigned int suf_b[8];
-#pragma unroll
-            for (int k = 7; k >= 0; --k) {
-                suf_a[k] = ra;
-                suf_v[k] = rv;
-                suf_b[k] = rb;
-                ra += a8[k];
-                rv += v8[k];
-                rb = max(rb, b8[k]);
-            }
-            int cb = cbelow;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                cb += c8[k];
-                if (first == 0x7fffffff && c8[k] > 0) {
-                    const float A_ = (float)suf_a[k] * inv_fa, V_ = (float)suf_v[k] * inv_fv;
-                    const float B_ = __uint_as_float(suf_b[k]);
-                    const bool empty = (sc.rem_cnt + cb) == nl;
-                    if (!empty && cert_f(A_, V_, B_, ldf, Df) < a.eps_f) {
-                        first = lane * 8 + k;
-                        cnt_through = cb;
-                    }
+                    a2[k] += (unsigned long long)hist[(2 + q) * kSearchBins + d] << (14 * q);
+                    v2[k] += (unsigned long long)hist[(5 + q) * kSearchBins + d] << (14 * q);
                 }
             }
-            const unsigned who = __ballot_sync(0xffffffffu, first != 0x7fffffff);
-            if (who == 0) {
-                // no boundary of this range works: every key of the range is removed (only possible
-                // at the top level, where it means k* = |L|: eps^(empty) = 0 is always accepted)
-                if (lane == 0) { sc.found = 1; sc.kstar = nl; sc.kkey = ~0ull; }
-            } else {
-                const int src = __ffs(who) - 1;
-                if (lane == src) {
-                    const int d = first;
-                    const int in_bin = c8[d - lane * 8];
-                    const int before = cnt_through - in_bin;     // bins below d, this range
-                    // rest after bin d (kept) for the next level = suf values of bin d
-                    sc.rest_a = suf_a[d - lane * 8];
-                    sc.rest_v = suf_v[d - lane * 8];
-                    sc.rest_b = suf_b[d - lane * 8];
-                    sc.rem_cnt += before;
-                    sc.prefix |= (unsigned long long)d << shift;
-                    sc.pmask |= 255ull << shift;
-                    if (in_bin == 1 || shift == 0) {
+            // exclusive suffix within the slice (higher bins = smaller gains); the slice total goes out
+            const SearchAcc mine = {a2[0] + a2[1], v2[0] + v2[1], max(b2[0], b2[1]), c2[0] + c2[1]};
+            SearchAcc above = block_suffix_search(mine, sacc);
+            if (tid == 0) ssum = search_add(above, mine);
+            // the histogram is consumed: clear it for the next level
+            for (int k = tid; k < kSearchFields * kSearchBins / 4; k += T) hist4[k] = make_uint4(0u, 0u, 0u, 0u);
+            cl.sync();
+            // the slices above this one, then the keys above the level's range
+            if (warp == 0) {
+                SearchAcc x = (lane > rank && lane < C) ? *cl.map_shared_rank(&ssum, lane) : zero;
+                for (int o = 16; o > 0; o >>= 1) {
+                    const SearchAcc y = {__shfl_xor_sync(0xffffffffu, x.a, o), __shfl_xor_sync(0xffffffffu, x.v, o),
+                                         __shfl_xor_sync(0xffffffffu, x.b, o), __shfl_xor_sync(0xffffffffu, x.c, o)};
+                    x = search_add(x, y);
+                }
+                if (lane == 0) sacc[0] = x;
+            }
+            __syncthreads();
+            above = search_add(above, sacc[0]);
+            above.a += sc.rest_a;
+            above.v += sc.rest_v;
+            above.b = max(above.b, sc.rest_b);
+            above.c += sc.rest_c;
+            // residual after bin d0 + 1 = above; after bin d0 = above + bin d0 + 1
+            SearchAcc after[2];
+            after[1] = above;
+            after[0] = {above.a + a2[1], above.v + v2[1], max(above.b, b2[1]), above.c + c2[1]};
+            int cand = 0x7fffffff;
+#pragma unroll
+            for (int k = 1; k >= 0; --k) {
+                if (c2[k] > 0 && after[k].c > 0) {
+                    const float A_ = (float)after[k].a * inv_fa, V_ = (float)after[k].v * inv_fv;
+                    if (cert_f(A_, V_, __uint_as_float(after[k].b), ldf, Df) < a.eps_f) cand = d0 + k;
+                }
+            }
+            cand = __reduce_min_sync(0xffffffffu, cand);
+            if (lane == 0) redi[warp] = cand;
+            __syncthreads();
+            cand = __reduce_min_sync(0xffffffffu, redi[lane]);
+            if (cand != 0x7fffffff && (cand - rank * sl) >> 1 == tid) {
+                const bool first = cand == d0;
+                const SearchAcc rest = first ? after[0] : after[1];
+                sprop.a = rest.a;
+                sprop.v = rest.v;
+                sprop.b = rest.b;
+                sprop.c = rest.c;
+                sprop.in_bin = first ? c2[0] : c2[1];
+            }
+            if (tid == 0) sprop.cand = cand;
+            cl.sync();
+            // the first bin of the level (lowest CTA with a candidate) whose residual is acceptable
+            if (warp == 0) {
+                const int cr = lane < C ? cl.map_shared_rank(&sprop, lane)->cand : 0x7fffffff;
+                const unsigned who = __ballot_sync(0xffffffffu, cr != 0x7fffffff);
+                if (lane == 0) {
+                    if (who == 0u) {
+                        // no boundary of the range leaves an acceptable non-empty residual: every key is
+                        // taken (only possible at the top level: eps^(empty) = 0 is always accepted)
                         sc.found = 1;
-                        sc.kstar = sc.rem_cnt + 1;
-                        sc.kkey = sc.prefix | ~sc.pmask;  // keys of this bin are <= this bound
+                        sc.kstar = nl;
+                        sc.kkey = ~0ull;
+                    } else {
+                        const SearchProp p = *cl.map_shared_rank(&sprop, __ffs(who) - 1);
+                        sc.rest_a = p.a;
+                        sc.rest_v = p.v;
+                        sc.rest_b = p.b;
+                        sc.rest_c = p.c;
+                        sc.rem_cnt = nl - (int)p.in_bin - (int)p.c;
+                        sc.prefix = (hi << width) | (unsigned long long)p.cand;
+                        if (p.in_bin == 1u || shift == 0) {
+                            sc.found = 1;
+                            sc.kstar = sc.rem_cnt + (int)p.in_bin;
+                            sc.kkey = (sc.prefix << shift) | ((1ull << shift) - 1ull);
+                        }
                     }
                 }
             }
+            __syncthreads();
+            if (sc.found) break;
         }
-        __syncthreads();
-        parity ^= 1;
-        if (sc.found) break;
+        if (timer) R.sel_passes = passes;
     }
-    if (timer) R.sel_passes = passes;
     stamp(4);
 
     // ---- phase 4: E = keys up to the k*-th; each CTA writes its own members
     {
         const unsigned long long kk = sc.kkey;
+        static_assert(kDecideCap == 8 * kDecideThreads, "emit assumes eight entries per thread");
+        bool sel[8];
         int lcnt = 0;
-        for (int i = tid; i < ns; i += T) lcnt += skey[i] <= kk;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + k * T;
+            sel[k] = i < ns && search_key(skey[i], j0 + i) <= kk;
+            lcnt += sel[k];
+        }
+        // tokens and residency of the selected entries: all loads issued before any is used
+        int tok[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) tok[k] = sel[k] ? V.ltok[(int64_t)kv * V.n + j0 + tid + k * T] : 0;
+        unsigned char res[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) res[k] = sel[k] ? V.flags[(int64_t)kv * V.n + tok[k]] : 1;
         lcnt = block_sum(lcnt, redi);
-        if (tid == 0) slot[parity].v[0] = (double)lcnt;
+        if (tid == 0) slot[parity].i[0] = lcnt;
         cl.sync();
         if (tid == 0) {
             int off = 0;
-            for (int rk = 0; rk < rank; ++rk) off += (int)cl.map_shared_rank(slot, rk)[parity].v[0];
-            sc.rem_cnt = off;   // reuse: this CTA's offset in the exact list
+            for (int rk = 0; rk < rank; ++rk) off += cl.map_shared_rank(slot, rk)[parity].i[0];
+            wcnt[0] = off;   // running position in the exact list (order is irrelevant)
         }
         __syncthreads();
         int nf = 0;
-        if (tid == 0) wcnt[0] = sc.rem_cnt;  // running position in the exact list (order is irrelevant)
-        __syncthreads();
-        for (int i = tid; i < ns; i += T) {
-            if (skey[i] > kk) continue;
-            const int j = j0 + i;
-            const int tok = V.ltok[(int64_t)kv * V.n + j];
-            mark[(int64_t)row * a.ws_n + j] = a.gen;
-            elist[(int64_t)row * a.ws_n + atomicAdd(&wcnt[0], 1)] = tok;
-            if (V.flags[(int64_t)kv * V.n + tok] == 0) {
-                ++nf;
-                atomicOr(&a.ubits[(int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1) + (tok >> 5)], 1u << (tok & 31));
+        int32_t* el = elist + (int64_t)row * a.ws_n;
+        uint32_t* ub = a.ubits + (int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const unsigned m8 = __ballot_sync(0xffffffffu, sel[k]);
+            if (m8 == 0u) continue;
+            int base = 0;
+            if (lane == __ffs(m8) - 1) base = atomicAdd(&wcnt[0], __popc(m8));
+            base = __shfl_sync(0xffffffffu, base, __ffs(m8) - 1);
+            if (sel[k]) {
+                const int j = j0 + tid + k * T;
+                mark[(int64_t)row * a.ws_n + j] = a.gen;
+                el[base + __popc(m8 & ((1u << lane) - 1u))] = tok[k];
+                if (res[k] == 0) {
+                    ++nf;
+                    atomicOr(&ub[tok[k] >> 5], 1u << (tok[k] & 31));
+                }
             }
         }
         nf = block_sum(nf, redi);
-        if (tid == 0) slot[parity].v[1] = (double)nf;
+        if (tid == 0) slot[parity].i[1] = nf;
         cl.sync();
         if (rank == 0 && tid == 0) {
             int total_nf = 0;
-            for (int rk = 0; rk < C; ++rk) total_nf += (int)cl.map_shared_rank(slot, rk)[parity].v[1];
+            for (int rk = 0; rk < C; ++rk) total_nf += cl.map_shared_rank(slot, rk)[parity].i[1];
             R.kstar = sc.kstar;
             R.n_fetch = total_nf;
         }
@@ -1549,7 +1655,7 @@ __global__ void __launch_bounds__(256) attn_kernel(Views views, const float* __r
         qv[g][1] = t.y * a.inv_sqrt_d_f;
         qv[g][2] = t.z * a.inv_sqrt_d_f;
         qv[g][3] = t.w * a.inv_sqrt_d_f;
-        beta[g] = (float)rows[rowg[g]].beta;
+        beta[g] = rows[rowg[g]].beta_f;
     }
     float mrun[G], lrun[G], acc[G][4];
 #pragma unroll
@@ -1842,6 +1948,10 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     a.eps = eps;
     a.eps_f = (float)eps;
     a.ldelta = std::log(2.0 / delta);
+    a.eps_ff.hi = (float)eps;
+    a.eps_ff.lo = (float)(eps - (double)a.eps_ff.hi);
+    a.ld_ff.hi = (float)a.ldelta;
+    a.ld_ff.lo = (float)(a.ldelta - (double)a.ld_ff.hi);
     const double isd = 1.0 / std::sqrt((double)kHeadDim);
     a.inv_sqrt_d_f = (float)isd;
     a.inv_sqrt_d.hi = (float)isd;

@@ -64,7 +64,8 @@ struct RowState {
     double V;
     double b1, b2;      // largest and second-largest b_i
     double eps_hat;
-    double pad;
+    float beta_f;       // beta in fp32 (what the attention weights use)
+    float pad;
     int beta_iters;     // passes of the beta solve
     int sel_passes;     // radix-select passes
     unsigned int phase_ns[6];  // decide kernel: ns spent in phases 0..4 and in the ranking (rank 0)
