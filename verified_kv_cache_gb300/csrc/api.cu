@@ -30,10 +30,12 @@ verkv_status fail(Ctx& ctx, verkv_status s, const char* msg)
 
 void free_ws(Ctx& c)
 {
-    void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ubits, c.ulist, c.ucount, c.staging, c.part,
+    void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.ucount,
+                    c.staging, c.part,
                     c.d_slot_n};
     for (void* p : ptrs)
         if (p) cudaFree(p);
+    if (c.h_err) cudaFreeHost(c.h_err);
 }
 
 verkv_status alloc_ws(Ctx& ctx)
@@ -56,14 +58,27 @@ verkv_status alloc_ws(Ctx& ctx)
     VK_CUDA(cudaMalloc(&ctx.mark, sizeof(int32_t) * rows * n));
     VK_CUDA(cudaMemset(ctx.mark, 0, sizeof(int32_t) * rows * n));
     VK_CUDA(cudaMalloc(&ctx.elist, sizeof(int32_t) * rows * n));
-    VK_CUDA(cudaMalloc(&ctx.ubits, sizeof(uint32_t) * kvb * (n / 32 + 1)));
-    VK_CUDA(cudaMemset(ctx.ubits, 0, sizeof(uint32_t) * kvb * (n / 32 + 1)));
+    VK_CUDA(cudaMalloc(&ctx.ebits, sizeof(uint32_t) * rows * (n / 32 + 1)));
+    VK_CUDA(cudaMemset(ctx.ebits, 0, sizeof(uint32_t) * rows * (n / 32 + 1)));
+    VK_CUDA(cudaMalloc(&ctx.om, sizeof(float) * rows * n));
     VK_CUDA(cudaMalloc(&ctx.ulist, sizeof(int32_t) * kvb * n));
+    VK_CUDA(cudaMalloc(&ctx.umask, kvb * n));
     VK_CUDA(cudaMalloc(&ctx.ucount, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMemset(ctx.ucount, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.staging, kvb * n * 2 * kHeadDim * ctx.elt));
     VK_CUDA(cudaMalloc(&ctx.part, sizeof(float) * rows * ctx.nsplit * (kHeadDim + 2)));
+    VK_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&ctx.h_err), sizeof(int), cudaHostAllocMapped));
+    *ctx.h_err = 0;
+    VK_CUDA(cudaHostGetDevicePointer(reinterpret_cast<void**>(&ctx.d_err), ctx.h_err, 0));
     return VERKV_OK;
+}
+
+// The mapped error word is written by a kernel whose bounded wait gave up; reading it clears it.
+bool take_device_timeout(Ctx& ctx)
+{
+    if (!ctx.h_err || *reinterpret_cast<volatile int*>(ctx.h_err) == 0) return false;
+    *reinterpret_cast<volatile int*>(ctx.h_err) = 0;
+    return true;
 }
 
 bool slot_ok(const Ctx& c, int layer, int seq)
@@ -124,6 +139,9 @@ verkv_status verkv_create(const verkv_config* cfg, verkv_ctx** out)
     if (st == VERKV_OK) {
         ctx.elt = c.kv_dtype == VERKV_DTYPE_BF16 ? 2 : 4;
         cudaGetDevice(&ctx.device);
+        int nsm = 0;
+        if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, ctx.device) == cudaSuccess && nsm > 0)
+            ctx.num_sms = nsm;
         ctx.slots.resize((size_t)c.n_layers * c.n_seqs);
         st = alloc_ws(ctx);
     }
@@ -188,6 +206,7 @@ verkv_status verkv_decode(verkv_ctx* h, int32_t layer, const int32_t* seq_ids, i
         return fail(ctx, VERKV_EINVAL, "q must be 16-byte aligned");
     if (!(eps >= 0.0) || !std::isfinite(eps)) return fail(ctx, VERKV_EINVAL, "eps must be finite and >= 0");
     if (!(delta > 0.0 && delta < 1.0)) return fail(ctx, VERKV_EINVAL, "delta must lie in (0, 1)");
+    if (take_device_timeout(ctx)) return fail(ctx, VERKV_ETIMEOUT, "a bounded device-side wait gave up in an earlier call");
     for (int b = 0; b < B; ++b) {
         if (seq_ids[b] < 0 || seq_ids[b] >= c.n_seqs) return fail(ctx, VERKV_EINVAL, "seq id out of range");
         if (!ctx.slot(layer, seq_ids[b]).live) return fail(ctx, VERKV_ESTATE, "slot was not compressed");
@@ -272,6 +291,7 @@ verkv_status verkv_get_decode_trace(verkv_ctx* h, verkv_row_trace* out, int32_t 
     std::vector<RowState> rs(rows);
     VK_CUDA(cudaMemcpyAsync(rs.data(), ctx.rows, sizeof(RowState) * rows, cudaMemcpyDeviceToHost, (cudaStream_t)stream));
     VK_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    if (take_device_timeout(ctx)) return fail(ctx, VERKV_ETIMEOUT, "a bounded device-side wait gave up");
     for (int i = 0; i < rows; ++i) {
         verkv_row_trace& t = out[i];
         const RowState& s = rs[i];

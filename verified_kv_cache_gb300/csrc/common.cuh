@@ -86,6 +86,7 @@ __device__ __forceinline__ ff ff_sub(ff x, ff y) { return ff_add(x, ff_neg(y)); 
 // x / y: the fp32 quotient corrected by one step on the float-float remainder (~2^-46 relative).
 __device__ __forceinline__ ff ff_div(ff x, ff y)
 {
+    if (x.hi == 0.f) return {0.f, 0.f};   // also keeps zero numerators off the division's slow path
     const float q1 = __fdiv_rn(x.hi, y.hi);
     const ff r = ff_sub(x, ff_mul_f(y, q1));
     return fast_two_sum(q1, __fdiv_rn(r.hi, y.hi));

@@ -27,7 +27,9 @@ struct Views {
 };
 
 struct DecodeArgs {
-    uint32_t* ubits;  // [B][Hkv][ws_n/32 + 1] union bitmap of fetched tokens (set by the decision kernels)
+    uint32_t* ebits;  // [B Hq][ws_n/32 + 1] per query row: tokens of L_g[:k*] \ S (set by the decision kernels)
+    float* om;        // [B Hq][ws_n] weight factor of each resident slot (set by the scoring and decision kernels)
+    int* err;         // mapped host word, set when a bounded device-side wait gives up
     int Hkv, Hq, G, ws_n, ws_npow2, gen, nsplit;
     float eps_f;
     double eps, ldelta;
@@ -311,6 +313,7 @@ __global__ void __launch_bounds__(kTile) score_h_kernel(Views views, const float
         const ff t = exact_logit<T>(qs[g], key, a.inv_sqrt_d);
         const int row = row_of(b, kv * G + g, a.Hq);
         th[(int64_t)row * a.ws_n + k] = make_float2(t.hi, t.lo);
+        a.om[(int64_t)row * a.ws_n + slot] = 1.0f;   // H: weight factor 1
         mloc = t.hi;
     }
     // max per query head: lanes with the same g are G apart
@@ -609,8 +612,7 @@ __device__ void emit_exact_set(const unsigned long long* sorted, int kstar, int 
         elist[(int64_t)row * a.ws_n + p] = tok;
         if (V.flags[(int64_t)kv * V.n + tok] == 0) {
             ++nf;
-            const int b = row / a.Hq;
-            atomicOr(&a.ubits[(int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1) + (tok >> 5)], 1u << (tok & 31));
+            atomicOr(&a.ebits[(int64_t)row * (a.ws_n / 32 + 1) + (tok >> 5)], 1u << (tok & 31));
         }
     }
     nf = block_sum(nf, redi);
@@ -1047,7 +1049,6 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     __shared__ ff bc[8];
     __shared__ ff redff[32 * 4];
     __shared__ Top2 stop2[32];
-    __shared__ float redf[32];
     __shared__ int redi[32];
     __shared__ DecideScalars sc;
     __shared__ int wcnt[32];
@@ -1188,10 +1189,20 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const float bf = sc.bf;
     stamp(1);
 
-    // ---- phase 2: eq. (7)
+    // ---- phase 2: eq. (7); the weight factor lambda_i / r_i of the sampled entries
     {
         ff acc[2] = {{0.f, 0.f}, {0.f, 0.f}};
         Top2 t2 = {0.f, 0.f, 0x7fffffff};
+        int slv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) slv[k] = tid + k * T < ns ? V.lslot[(int64_t)kv * V.n + j0 + tid + k * T] : -1;
+        float* omr = a.om + (int64_t)row * a.ws_n;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (slv[k] >= 0) {
+                const int i = tid + k * T;
+                omr[slv[k]] = __fdiv_rn(lambda_of(sw[i], sr[i], bf), sr[i]);
+            }
         for (int i = tid; i < ns; i += T) {
             const Coef c = coef_of(sw[i], sr[i], bf);
             acc[0] = ff_add_f(acc[0], c.a);
@@ -1448,13 +1459,14 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             sel[k] = i < ns && search_key(skey[i], j0 + i) <= kk;
             lcnt += sel[k];
         }
-        // tokens and residency of the selected entries: all loads issued before any is used
-        int tok[8];
+        // tokens and resident slots of the selected entries: all loads issued before any is used
+        int tok[8], sl8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) tok[k] = sel[k] ? V.ltok[(int64_t)kv * V.n + j0 + tid + k * T] : 0;
-        unsigned char res[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) res[k] = sel[k] ? V.flags[(int64_t)kv * V.n + tok[k]] : 1;
+        for (int k = 0; k < 8; ++k) {
+            const int64_t e = (int64_t)kv * V.n + j0 + tid + k * T;
+            tok[k] = sel[k] ? V.ltok[e] : 0;
+            sl8[k] = sel[k] ? V.lslot[e] : -1;
+        }
         lcnt = block_sum(lcnt, redi);
         if (tid == 0) slot[parity].i[0] = lcnt;
         cl.sync();
@@ -1466,7 +1478,8 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         __syncthreads();
         int nf = 0;
         int32_t* el = elist + (int64_t)row * a.ws_n;
-        uint32_t* ub = a.ubits + (int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1);
+        uint32_t* eb = a.ebits + (int64_t)row * (a.ws_n / 32 + 1);
+        float* omr = a.om + (int64_t)row * a.ws_n;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const unsigned m8 = __ballot_sync(0xffffffffu, sel[k]);
@@ -1475,12 +1488,12 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             if (lane == __ffs(m8) - 1) base = atomicAdd(&wcnt[0], __popc(m8));
             base = __shfl_sync(0xffffffffu, base, __ffs(m8) - 1);
             if (sel[k]) {
-                const int j = j0 + tid + k * T;
-                mark[(int64_t)row * a.ws_n + j] = a.gen;
                 el[base + __popc(m8 & ((1u << lane) - 1u))] = tok[k];
-                if (res[k] == 0) {
+                if (sl8[k] >= 0) {
+                    omr[sl8[k]] = 1.0f;   // sampled and made exact: weight factor 1
+                } else {
                     ++nf;
-                    atomicOr(&ub[tok[k] >> 5], 1u << (tok[k] & 31));
+                    atomicOr(&eb[tok[k] >> 5], 1u << (tok[k] & 31));
                 }
             }
         }
@@ -1499,42 +1512,78 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
 }
 
 // --------------------------------------------------------------------------------------------
-// D7: union of L_g[:k*] \ S over the query heads of a KV head (the decision kernels set its bits),
-// compacted to ascending tokens, and the copy of those rows from the pinned host cache into the
-// staging area (zero-copy loads, one warp per row, 16 bytes per lane, several rows in flight).
+// D7: union over the query heads of a KV head of L_g[:k*] \ S (per-row bitmaps set by the decision
+// kernels), compacted to ascending tokens together with the mask of the query heads whose exact set
+// holds each token (bit g); the bitmaps are cleared for the next call.  Then the copy of those rows
+// from the pinned host cache into the staging area (zero-copy loads, one warp per row, 16 bytes per
+// lane, several rows in flight).
 // --------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) union_kernel(Views views, DecodeArgs a, const RowState* __restrict__ rows,
-                                                     const int32_t* __restrict__ elist, uint32_t* __restrict__ ubits,
-                                                     int32_t* __restrict__ ulist, int32_t* __restrict__ ucount)
+template <int G>
+__global__ void __launch_bounds__(1024) union_kernel(Views views, DecodeArgs a, int32_t* __restrict__ ulist,
+                                                     uint8_t* __restrict__ umask, int32_t* __restrict__ ucount)
 {
     __shared__ int scratch[32];
     const int b = blockIdx.x / a.Hkv, kv = blockIdx.x % a.Hkv;
-    const SlotView& V = views.v[b];
-    const int n = V.n;
+    const int n = views.v[b].n;
     const int nwords = (n + 31) / 32;
-    uint32_t* bits = ubits + (int64_t)(b * a.Hkv + kv) * (a.ws_n / 32 + 1);
-    (void)rows;
-    (void)elist;
+    const int64_t stride = a.ws_n / 32 + 1;
+    uint32_t* eb = a.ebits + (int64_t)row_of(b, kv * G, a.Hq) * stride;   // the G rows are consecutive
     int base = 0;
     int32_t* out = ulist + (int64_t)(b * a.Hkv + kv) * a.ws_n;
+    uint8_t* msk = umask + (int64_t)(b * a.Hkv + kv) * a.ws_n;
     for (int w0 = 0; w0 < nwords; w0 += blockDim.x) {
         const int wi = w0 + threadIdx.x;
-        uint32_t word = wi < nwords ? bits[wi] : 0u;
+        uint32_t wg[G];
+        uint32_t word = 0u;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            wg[g] = wi < nwords ? eb[g * stride + wi] : 0u;
+            word |= wg[g];
+        }
         int total;
         const int ex = block_exclusive_scan(__popc(word), scratch, &total);
         int pos = base + ex;
-        if (wi < nwords && word) {
-            bits[wi] = 0u;
+        if (word) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                if (wg[g]) eb[g * stride + wi] = 0u;
             while (word) {
                 const int bit = __ffs(word) - 1;
-                out[pos++] = wi * 32 + bit;
-                word &= word - 1;
+                unsigned m = 0u;
+#pragma unroll
+                for (int g = 0; g < G; ++g) m |= ((wg[g] >> bit) & 1u) << g;
+                out[pos] = wi * 32 + bit;
+                msk[pos] = (uint8_t)m;
+                ++pos;
+                word &= word - 1u;
             }
         }
         base += total;
         __syncthreads();
     }
     if (threadIdx.x == 0) ucount[b * a.Hkv + kv] = base;
+}
+
+// Weight factors of the sampled entries on the full-row path (the fused decision kernel writes
+// them itself): 1 when the entry was made exact, lambda_i / r_i otherwise.
+__global__ void __launch_bounds__(256) om_sampled_kernel(Views views, DecodeArgs a, const RowState* __restrict__ rows,
+                                                         const float* __restrict__ wl, const int32_t* __restrict__ mark)
+{
+    const int row = blockIdx.y;
+    const int b = row / a.Hq, kv = (row % a.Hq) / a.G;
+    const SlotView& V = views.v[b];
+    const int nl = rows[row].n_l;
+    const float beta = rows[row].beta_f;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < nl; j += gridDim.x * blockDim.x) {
+        const int sl = V.lslot[(int64_t)kv * V.n + j];
+        if (sl < 0) continue;
+        float w = 1.0f;
+        if (mark[(int64_t)row * a.ws_n + j] != a.gen) {
+            const float r = V.rl[(int64_t)kv * V.n + j];
+            w = __fdiv_rn(lambda_of(wl[(int64_t)row * a.ws_n + j], r, beta), r);
+        }
+        a.om[(int64_t)row * a.ws_n + sl] = w;
+    }
 }
 
 __global__ void __launch_bounds__(256) gather_kernel(Views views, DecodeArgs a, const int32_t* __restrict__ ulist,
@@ -1572,171 +1621,309 @@ __global__ void __launch_bounds__(256) gather_kernel(Views views, DecodeArgs a, 
 
 // --------------------------------------------------------------------------------------------
 // D8: weighted attention (comment closing Algorithm 2; estimator of Theorem 2).  Rows: the
-// resident H u S rows and the staged rows of the KV head; per query head the weight factor is 1 on
-// H and on L_g[:k*], lambda_i / r_i on S \ L_g[:k*], and 0 on staged rows fetched for another query
-// head.  Split over `nsplit` blocks per KV head; one warp per K/V row, 4 channels per lane, all G
-// query heads at once (each K/V byte is read once for the group).
+// resident H u S rows of the KV head, then its staged rows.  Per query head the weight factor is
+// the one the scoring and decision kernels wrote for each resident slot (1 on H and on L_g[:k*],
+// lambda_i / r_i on S \ L_g[:k*]) and, on a staged row, 1 if the head's exact set holds it, else 0.
+// Each block takes every gridDim.y-th chunk of 32 KB of rows (64 bf16 rows) of one KV head; chunks
+// arrive by bulk asynchronous copies (one or two per chunk: the rows are contiguous in the resident
+// cache and in the staging area) into a three-stage ring completed on mbarriers, while the block
+// computes on the previous chunk: q.k for all G query heads (a row's 128 channels split over 2G
+// threads), an online softmax per head, and p.v with two channels per thread.
 // --------------------------------------------------------------------------------------------
-template <typename T> struct Vec4;
-template <> struct Vec4<__nv_bfloat16> {
-    static __device__ __forceinline__ float4 load(const __nv_bfloat16* p)
-    {
-        const uint2 u = *reinterpret_cast<const uint2*>(p);
-        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
-        const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
-        const float2 fx = __bfloat1622float2(x), fy = __bfloat1622float2(y);
-        return make_float4(fx.x, fx.y, fy.x, fy.y);
-    }
-};
-template <> struct Vec4<float> {
-    static __device__ __forceinline__ float4 load(const float* p) { return *reinterpret_cast<const float4*>(p); }
-};
+constexpr int kAttnChunkBytes = 32768;
+constexpr int kAttnStages = 3;
+constexpr int kAttnThreads = 256;
+constexpr unsigned kWaitLimit = 1u << 22;   // try_wait polls before a wait is declared failed
 
-// One warp handles a contiguous run of rows.  The per-row weight factors (which depend on the
-// row's token, its flags, whether it was made exact for each query head, and lambda_i / r_i for
-// sampled tokens) are resolved 32 rows at a time, one row per lane, so their dependent loads overlap;
-// then the K/V rows are streamed two at a time.
-template <typename T, int G>
-__device__ __forceinline__ void attn_weights_batch(const SlotView& V, int kv, int n, int m_res, const int32_t* ul,
-                                                   const int32_t* __restrict__ mark, const float* __restrict__ wl,
-                                                   const int* rowg, const float* beta, int gen, int ws_n, int rix,
-                                                   bool valid, float* om)
+__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count)
 {
-#pragma unroll
-    for (int g = 0; g < G; ++g) om[g] = 0.f;
-    if (!valid) return;
-    const bool staged = rix >= m_res;
-    const int tok = staged ? ul[rix - m_res] : V.rtok[(int64_t)kv * n + rix];
-    const int f = V.flags[(int64_t)kv * n + tok];
-    if (f == 2) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) om[g] = 1.f;
-        return;
-    }
-    const int li = V.lpos[(int64_t)kv * n + tok];
-    float r = 0.f;
-    if (f == 1 && !staged) r = V.rl[(int64_t)kv * n + li];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if (mark[(int64_t)rowg[g] * ws_n + li] == gen) om[g] = 1.f;
-        else if (f == 1 && !staged) om[g] = __fdiv_rn(lambda_of(wl[(int64_t)rowg[g] * ws_n + li], r, beta[g]), r);
-    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
-template <typename T, int G>
-__global__ void __launch_bounds__(256) attn_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
-                                                   const RowState* __restrict__ rows, const float* __restrict__ wl,
-                                                   const int32_t* __restrict__ mark,
-                                                   const int32_t* __restrict__ ulist, const int32_t* __restrict__ ucount,
-                                                   const T* __restrict__ staging, float* __restrict__ part)
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned bytes)
 {
-    constexpr int NW = 8;
-    __shared__ float sm_m[NW][G], sm_l[NW][G];
-    __shared__ float sm_acc[NW][G][kHeadDim];
-    const int b = blockIdx.x / a.Hkv, kv = blockIdx.x % a.Hkv;
-    const SlotView& V = views.v[b];
-    const int n = V.n;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int m_res = V.counts[kv * 4 + 3];
-    const int nu = ucount[b * a.Hkv + kv];
-    const int total = m_res + nu;
-    const int per = (total + gridDim.y - 1) / gridDim.y;
-    const int r0 = blockIdx.y * per, r1 = min(total, r0 + per);
-    const int perw = (r1 - r0 + NW - 1) / NW;
-    const int w0 = min(r1, r0 + warp * perw), w1 = min(r1, w0 + perw);
-    float qv[G][4];
-    float beta[G];
-    int rowg[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        rowg[g] = row_of(b, kv * G + g, a.Hq);
-        const float4 t = *reinterpret_cast<const float4*>(q + (int64_t)rowg[g] * kHeadDim + lane * 4);
-        qv[g][0] = t.x * a.inv_sqrt_d_f;
-        qv[g][1] = t.y * a.inv_sqrt_d_f;
-        qv[g][2] = t.z * a.inv_sqrt_d_f;
-        qv[g][3] = t.w * a.inv_sqrt_d_f;
-        beta[g] = rows[rowg[g]].beta_f;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false if it did not complete within the limit.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, unsigned limit)
+{
+    const unsigned addr = smem_u32(bar);
+    for (unsigned it = 0; it < limit; ++it) {
+        unsigned done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
     }
-    float mrun[G], lrun[G], acc[G][4];
+    return false;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global memory into this
+// block's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+template <typename T> struct RowCvt;
+template <> struct RowCvt<__nv_bfloat16> {
+    // 8 channels from 16 bytes
+    static __device__ __forceinline__ void load8(const void* p, float* o)
+    {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        mrun[g] = -INFINITY;
-        lrun[g] = 0.f;
-        acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
-    }
-    const T* res = reinterpret_cast<const T*>(V.kvres) + V.res_off[kv] * 2 * kHeadDim;
-    const T* stg = staging + (int64_t)(b * a.Hkv + kv) * a.ws_n * 2 * kHeadDim;
-    const int32_t* ul = ulist + (int64_t)(b * a.Hkv + kv) * a.ws_n;
-    for (int base = w0; base < w1; base += 32) {
-        float om_l[G];
-        attn_weights_batch<T, G>(V, kv, n, m_res, ul, mark, wl, rowg, beta, a.gen, a.ws_n, base + lane,
-                                 base + lane < w1, om_l);
-        const int cnt = min(32, w1 - base);
-        for (int k = 0; k < cnt; k += 2) {
-            const int rA = base + k, rB = base + k + 1;
-            const bool hasB = k + 1 < cnt;
-            const T* pA = rA < m_res ? res + (int64_t)rA * 2 * kHeadDim : stg + (int64_t)(rA - m_res) * 2 * kHeadDim;
-            const T* pB = hasB ? (rB < m_res ? res + (int64_t)rB * 2 * kHeadDim
-                                             : stg + (int64_t)(rB - m_res) * 2 * kHeadDim)
-                               : pA;
-            const float4 kA = Vec4<T>::load(pA + lane * 4), vA = Vec4<T>::load(pA + kHeadDim + lane * 4);
-            const float4 kB = Vec4<T>::load(pB + lane * 4), vB = Vec4<T>::load(pB + kHeadDim + lane * 4);
-            float sA[G], sB[G];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                sA[g] = qv[g][0] * kA.x + qv[g][1] * kA.y + qv[g][2] * kA.z + qv[g][3] * kA.w;
-                sB[g] = qv[g][0] * kB.x + qv[g][1] * kB.y + qv[g][2] * kB.z + qv[g][3] * kB.w;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    sA[g] += __shfl_xor_sync(0xffffffffu, sA[g], o);
-                    sB[g] += __shfl_xor_sync(0xffffffffu, sB[g], o);
-                }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float oA = __shfl_sync(0xffffffffu, om_l[g], k);
-                const float oB = hasB ? __shfl_sync(0xffffffffu, om_l[g], k + 1) : 0.f;
-                const float xA = oA > 0.f ? sA[g] : -INFINITY;
-                const float xB = oB > 0.f ? sB[g] : -INFINITY;
-                const float mn = fmaxf(mrun[g], fmaxf(xA, xB));
-                if (mn == -INFINITY) continue;
-                const float corr = expf(mrun[g] - mn);
-                const float pA_ = oA > 0.f ? oA * expf(xA - mn) : 0.f;
-                const float pB_ = oB > 0.f ? oB * expf(xB - mn) : 0.f;
-                lrun[g] = lrun[g] * corr + pA_ + pB_;
-                acc[g][0] = acc[g][0] * corr + pA_ * vA.x + pB_ * vB.x;
-                acc[g][1] = acc[g][1] * corr + pA_ * vA.y + pB_ * vB.y;
-                acc[g][2] = acc[g][2] * corr + pA_ * vA.z + pB_ * vB.z;
-                acc[g][3] = acc[g][3] * corr + pA_ * vA.w + pB_ * vB.w;
-                mrun[g] = mn;
-            }
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+            o[2 * k] = f.x;
+            o[2 * k + 1] = f.y;
         }
     }
+    static __device__ __forceinline__ float2 load2(const void* p)
+    {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    }
+};
+template <> struct RowCvt<float> {
+    static __device__ __forceinline__ void load8(const void* p, float* o)
+    {
+        const float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
+        o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+        o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+    }
+    static __device__ __forceinline__ float2 load2(const void* p) { return *reinterpret_cast<const float2*>(p); }
+};
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
+                                                            const int32_t* __restrict__ ucount,
+                                                            const uint8_t* __restrict__ umask,
+                                                            const T* __restrict__ staging, float* __restrict__ part)
+{
+    constexpr int ROWB = 2 * kHeadDim * (int)sizeof(T);   // one K/V row
+    constexpr int CR = kAttnChunkBytes / ROWB;             // rows per chunk
+    constexpr int NS = kAttnStages;
+    constexpr int QS = 64 / G;                             // channels per q.k thread
+    constexpr int NSL = kHeadDim / QS;                     // threads per row in q.k (2G)
+    constexpr int RSTEP = kAttnThreads / NSL;              // rows per q.k pass
+    constexpr int EPT = (CR * G + kAttnThreads - 1) / kAttnThreads;  // weight factors per thread
+    constexpr int PVI = (G * (kHeadDim / 2) + kAttnThreads - 1) / kAttnThreads;  // p.v items per thread
+    static_assert(QS % 8 == 0 && CR <= 64 && CR >= 32, "attention tiling");
+    extern __shared__ __align__(128) unsigned char sbuf[];  // NS x kAttnChunkBytes
+    __shared__ __align__(8) unsigned long long full[NS];
+    __shared__ float s_om[2][CR][G];
+    __shared__ float s_p[CR][G];
+    __shared__ float s_corr[G], s_m[G], s_l[G];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
+    const SlotView& V = views.v[b];
+    const int m_res = V.counts[kv * 4 + 3];
+    const int nu = ucount[unit];
+    const int total = m_res + nu;
+    const int nch = (total + CR - 1) / CR;
+    const int y = blockIdx.y, ny = gridDim.y;
+    const int nmine = nch > y ? (nch - y + ny - 1) / ny : 0;
+    const unsigned char* res = reinterpret_cast<const unsigned char*>(V.kvres) + V.res_off[kv] * (int64_t)ROWB;
+    const unsigned char* stg = reinterpret_cast<const unsigned char*>(staging) + (int64_t)unit * a.ws_n * ROWB;
+    const uint8_t* um = umask + (int64_t)unit * a.ws_n;
+    const int row0 = row_of(b, kv * G, a.Hq);   // the G query rows of the KV head are consecutive
+
+    // q slice of this thread (pre-scaled by 1/sqrt(d)), all G heads
+    const int sl = tid % NSL;
+    float qr[G][QS];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if (lane == 0) { sm_m[warp][g] = mrun[g]; sm_l[warp][g] = lrun[g]; }
-        sm_acc[warp][g][lane * 4 + 0] = acc[g][0];
-        sm_acc[warp][g][lane * 4 + 1] = acc[g][1];
-        sm_acc[warp][g][lane * 4 + 2] = acc[g][2];
-        sm_acc[warp][g][lane * 4 + 3] = acc[g][3];
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < QS; ++c) qr[g][c] = q[(int64_t)(row0 + g) * kHeadDim + sl * QS + c] * a.inv_sqrt_d_f;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_bad = 0;
+    }
+    if (tid < G) {
+        s_m[tid] = -INFINITY;
+        s_l[tid] = 0.f;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < G * kHeadDim; e += blockDim.x) {
-        const int g = e / kHeadDim, c = e % kHeadDim;
-        float M = -INFINITY;
-        for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, sm_m[w2][g]);
-        float L = 0.f, A = 0.f;
-        if (M > -INFINITY)
-            for (int w2 = 0; w2 < NW; ++w2) {
-                const float sc = sm_m[w2][g] > -INFINITY ? expf(sm_m[w2][g] - M) : 0.f;
-                L += sm_l[w2][g] * sc;
-                A += sm_acc[w2][g][c] * sc;
+
+    auto issue = [&](int k) {
+        const int st = k % NS;
+        const int r0 = (y + k * ny) * CR, r1 = min(total, r0 + CR);
+        unsigned char* dst = sbuf + st * kAttnChunkBytes;
+        mbar_expect_tx(&full[st], (unsigned)((r1 - r0) * ROWB));
+        const int rm = min(r1, m_res);
+        if (rm > r0) bulk_g2s(dst, res + (int64_t)r0 * ROWB, (unsigned)((rm - r0) * ROWB), &full[st]);
+        const int s0 = max(r0, m_res);
+        if (r1 > s0)
+            bulk_g2s(dst + (s0 - r0) * ROWB, stg + (int64_t)(s0 - m_res) * ROWB, (unsigned)((r1 - s0) * ROWB),
+                     &full[st]);
+    };
+    // weight factors of chunk k, element e = r G + g of the chunk
+    auto load_om = [&](int k, float (&o)[EPT]) {
+        const int r0 = (y + k * ny) * CR, r1 = min(total, r0 + CR);
+#pragma unroll
+        for (int u = 0; u < EPT; ++u) {
+            const int e = tid + u * kAttnThreads;
+            const int r = e / G, g = e % G, R = r0 + r;
+            float w = 0.f;
+            if (e < CR * G && R < r1)
+                w = R < m_res ? a.om[(int64_t)(row0 + g) * a.ws_n + R] : (float)((um[R - m_res] >> g) & 1u);
+            o[u] = w;
+        }
+    };
+    auto store_om = [&](int buf, const float (&o)[EPT]) {
+#pragma unroll
+        for (int u = 0; u < EPT; ++u) {
+            const int e = tid + u * kAttnThreads;
+            if (e < CR * G) s_om[buf][e / G][e % G] = o[u];
+        }
+    };
+
+    if (tid == 0)
+        for (int k = 0; k < min(NS, nmine); ++k) issue(k);
+    float omv[EPT];
+    if (nmine > 0) {
+        load_om(0, omv);
+        store_om(0, omv);
+    }
+    float acc[PVI][2];
+#pragma unroll
+    for (int u = 0; u < PVI; ++u) acc[u][0] = acc[u][1] = 0.f;
+
+    int k = 0;
+    for (; k < nmine; ++k) {
+        const int st = k % NS;
+        const int r0 = (y + k * ny) * CR, cnt = min(total, r0 + CR) - r0;
+        if (k + 1 < nmine) load_om(k + 1, omv);   // stored at the end of this iteration
+        __syncthreads();
+        if (!mbar_wait(&full[st], (unsigned)((k / NS) & 1), kWaitLimit)) atomicOr(&s_bad, 1);
+        __syncthreads();
+        if (s_bad) break;
+        const unsigned char* buf = sbuf + st * kAttnChunkBytes;
+        // q.k: thread (row, slice); the 2G threads of a row are consecutive lanes
+        for (int r = tid / NSL; r < CR; r += RSTEP) {
+            float d[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) d[g] = 0.f;
+            if (r < cnt) {
+                const unsigned char* kr = buf + r * ROWB + sl * QS * (int)sizeof(T);
+#pragma unroll
+                for (int c8 = 0; c8 < QS; c8 += 8) {
+                    float kk[8];
+                    RowCvt<T>::load8(kr + c8 * (int)sizeof(T), kk);
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) d[g] = fmaf(qr[g][c8 + c], kk[c], d[g]);
+                }
             }
-        float* pp = part + ((int64_t)rowg[g] * a.nsplit + blockIdx.y) * (kHeadDim + 2);
-        pp[c] = A;
-        if (c == 0) { pp[kHeadDim] = M; pp[kHeadDim + 1] = L; }
+#pragma unroll
+            for (int o = 1; o < NSL; o <<= 1)
+#pragma unroll
+                for (int g = 0; g < G; ++g) d[g] += __shfl_xor_sync(0xffffffffu, d[g], o);
+            if (sl < G) {
+                float x = d[0];
+#pragma unroll
+                for (int g = 1; g < G; ++g)
+                    if (sl == g) x = d[g];
+                s_p[r][sl] = (r < cnt && s_om[k & 1][r][sl] > 0.f) ? x : -INFINITY;
+            }
+        }
+        __syncthreads();
+        // online softmax: warp g takes query head g
+        if (warp < G) {
+            const int g = warp;
+            float x[CR / 32], p[CR / 32];
+            float cmax = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < CR / 32; ++h) {
+                x[h] = s_p[lane + 32 * h][g];
+                cmax = fmaxf(cmax, x[h]);
+            }
+            cmax = warp_max(cmax);
+            const float Mold = s_m[g], Mnew = fmaxf(Mold, cmax);
+            float corr = 1.f, ls = 0.f;
+            if (Mnew > -INFINITY) {
+                corr = Mold > -INFINITY ? expf(Mold - Mnew) : 0.f;
+#pragma unroll
+                for (int h = 0; h < CR / 32; ++h) {
+                    p[h] = x[h] > -INFINITY ? s_om[k & 1][lane + 32 * h][g] * expf(x[h] - Mnew) : 0.f;
+                    ls += p[h];
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < CR / 32; ++h) p[h] = 0.f;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+#pragma unroll
+            for (int h = 0; h < CR / 32; ++h) s_p[lane + 32 * h][g] = p[h];
+            __syncwarp();
+            if (lane == 0) {
+                s_l[g] = s_l[g] * corr + ls;
+                s_m[g] = Mnew;
+                s_corr[g] = corr;
+            }
+        }
+        __syncthreads();
+        // p.v: item (g, channel pair)
+#pragma unroll
+        for (int u = 0; u < PVI; ++u) {
+            const int e = tid + u * kAttnThreads;
+            if (e < G * (kHeadDim / 2)) {
+                const int g = e / (kHeadDim / 2), c2 = 2 * (e % (kHeadDim / 2));
+                const float cr = s_corr[g];
+                float a0 = acc[u][0] * cr, a1 = acc[u][1] * cr;
+                const unsigned char* vb = buf + kHeadDim * (int)sizeof(T) + c2 * (int)sizeof(T);
+                for (int r = 0; r < cnt; ++r) {
+                    const float pr = s_p[r][g];
+                    const float2 v = RowCvt<T>::load2(vb + r * ROWB);
+                    a0 = fmaf(pr, v.x, a0);
+                    a1 = fmaf(pr, v.y, a1);
+                }
+                acc[u][0] = a0;
+                acc[u][1] = a1;
+            }
+        }
+        if (k + 1 < nmine) store_om((k + 1) & 1, omv);
+        __syncthreads();   // stage st and s_p are free
+        if (tid == 0 && k + NS < nmine) issue(k + NS);
+    }
+    if (s_bad) {
+        // a copy did not complete in time: report it, and before leaving wait (bounded) for the
+        // copies this block still has in flight
+        if (tid == 0) {
+            *(volatile int*)a.err = 1;
+            for (int kk = k; kk < min(nmine, k + NS); ++kk) mbar_wait(&full[kk % NS], (unsigned)((kk / NS) & 1), kWaitLimit);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int u = 0; u < PVI; ++u) {
+        const int e = tid + u * kAttnThreads;
+        if (e < G * (kHeadDim / 2)) {
+            const int g = e / (kHeadDim / 2), c2 = 2 * (e % (kHeadDim / 2));
+            float* pp = part + ((int64_t)(row0 + g) * a.nsplit + y) * (kHeadDim + 2);
+            pp[c2] = acc[u][0];
+            pp[c2 + 1] = acc[u][1];
+            if (c2 == 0) {
+                pp[kHeadDim] = s_m[g];
+                pp[kHeadDim + 1] = s_l[g];
+            }
+        }
     }
 }
 
@@ -1836,14 +2023,25 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         fallback_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
         VK_LAUNCHED("fallback");
     }
-    union_kernel<<<B * a.Hkv, 1024, 0, st>>>(views, a, ctx.rows, ctx.elist, ctx.ubits, ctx.ulist, ctx.ucount);
+    if (!on_chip) {
+        om_sampled_kernel<<<dim3(std::max(1, std::min(64, (max_nl + 255) / 256)), rowsN), 256, 0, st>>>(
+            views, a, ctx.rows, ctx.wl, ctx.mark);
+        VK_LAUNCHED("om_sampled");
+    }
+    union_kernel<G><<<B * a.Hkv, 1024, 0, st>>>(views, a, ctx.ulist, ctx.umask, ctx.ucount);
     VK_LAUNCHED("union");
     const int row_bytes = (int)(2 * kHeadDim * sizeof(T));
     gather_kernel<<<dim3(B * a.Hkv, std::max(8, 1216 / (B * a.Hkv))), 256, 0, st>>>(views, a, ctx.ulist, ctx.ucount,
                                                        (unsigned char*)ctx.staging, row_bytes);
     VK_LAUNCHED("gather");
-    attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), 256, 0, st>>>(views, q, a, ctx.rows, ctx.wl, ctx.mark, ctx.ulist,
-                                                                 ctx.ucount, (const T*)ctx.staging, ctx.part);
+    static bool attn_attr = false;   // one per (T, G) instantiation
+    if (!attn_attr) {
+        VK_CUDA(cudaFuncSetAttribute(attn_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kAttnStages * kAttnChunkBytes));
+        attn_attr = true;
+    }
+    attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), kAttnThreads, kAttnStages * kAttnChunkBytes, st>>>(
+        views, q, a, ctx.ucount, ctx.umask, (const T*)ctx.staging, ctx.part);
     VK_LAUNCHED("attn");
     merge_kernel<<<rowsN, 4 * kHeadDim, 0, st>>>(a, ctx.part, out);
     VK_LAUNCHED("merge");
@@ -1916,6 +2114,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         v.lpos = s.lpos;
         v.ltok = s.ltok;
         v.rl = s.rl;
+        v.lslot = s.lslot;
         v.rtok = s.rtok;
         v.hslot = s.hslot;
         v.counts = s.counts;
@@ -1943,8 +2142,11 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     a.ws_n = ctx.ws_n;
     a.ws_npow2 = ctx.ws_npow2;
     a.gen = ++ctx.gen;
-    a.ubits = ctx.ubits;
-    a.nsplit = std::min(ctx.nsplit, std::max(8, (1216 + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
+    a.ebits = ctx.ebits;
+    a.om = ctx.om;
+    a.err = ctx.d_err;
+    // attention splits per KV head: about two blocks per SM over the whole call
+    a.nsplit = std::min(ctx.nsplit, std::max(1, (2 * ctx.num_sms + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
     a.eps = eps;
     a.eps_f = (float)eps;
     a.ldelta = std::log(2.0 / delta);

@@ -24,6 +24,7 @@ struct Slot {
     int32_t* lpos = nullptr;    // [Hkv][n] token -> index in L (ascending tokens); -(H index)-1 for H
     int32_t* ltok = nullptr;    // [Hkv][n] L index -> token
     float* rl = nullptr;        // [Hkv][n] r by L index
+    int32_t* lslot = nullptr;   // [Hkv][n] L index -> resident slot when the token is in S, else -1
     int32_t* rtok = nullptr;    // [Hkv][n] resident slot -> token (H u S ascending)
     int32_t* hslot = nullptr;   // [Hkv][n] H index -> resident slot
     int32_t* counts = nullptr;  // [Hkv][4] |H|, |L|, |S|, |H|+|S|
@@ -100,14 +101,19 @@ struct Ctx {
     float* wl = nullptr;            // [rows][n] sketch weights by L index
     RowState* rows = nullptr;       // [rows]
     unsigned long long* keys = nullptr;  // [rows][npow2] gain keys (full-row path)
-    int32_t* mark = nullptr;        // [rows][n] generation tag: L index made exact
+    int32_t* mark = nullptr;        // [rows][n] generation tag: L index made exact (full-row path)
     int32_t* elist = nullptr;       // [rows][n] tokens made exact
-    uint32_t* ubits = nullptr;      // [max_batch][Hkv][n/32 + 1] union bitmap
+    uint32_t* ebits = nullptr;      // [rows][n/32 + 1] per query row: tokens of L_g[:k*] \ S (bitmap)
+    float* om = nullptr;            // [rows][n] per query row: weight factor of each resident slot
     int32_t* ulist = nullptr;       // [max_batch][Hkv][n] fetched union, ascending tokens
+    uint8_t* umask = nullptr;       // [max_batch][Hkv][n] query heads (bit g) whose exact set holds the row
     int32_t* ucount = nullptr;      // [max_batch][Hkv]
     void* staging = nullptr;        // [max_batch][Hkv][n][2][d] fetched rows
     float* part = nullptr;          // [rows][nsplit][d + 2] attention partials
     int nsplit = 128;               // largest split of the attention over blocks per KV head
+    int num_sms = 152;              // multiprocessors of the context's device
+    int* h_err = nullptr;           // mapped pinned host word: a device-side bounded wait gave up
+    int* d_err = nullptr;           // its device address
 
     // per-decode small arrays
     int32_t* d_slot_n = nullptr;    // [max_batch] n of each row set's slot
@@ -128,6 +134,7 @@ struct SlotView {
     const int32_t* lpos;
     const int32_t* ltok;
     const float* rl;
+    const int32_t* lslot;
     const int32_t* rtok;
     const int32_t* hslot;
     const int32_t* counts;
