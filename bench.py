@@ -101,10 +101,8 @@ def algorithmic_bytes(kernel, stats, traces, w, row_bytes):
     R = sum(s["n_resident"] for s in stats)
     sk = {"2bit": (d // 4) * 2 / 8 + (d // 4) * 4 / 128, "int8": d + 4, "exact": d * (2 if w.kv_dtype == "bf16" else 4)}
     s_sk = sk[w.sketch]
-    if kernel == "score_sketch":      # sketch of every L token, flags of every token, the queries
-        return L * s_sk + Hkv * n + Hq * d * 4
-    if kernel == "score_h":           # exact keys of H
-        return H * row_bytes / 2
+    if kernel == "score":             # sketch of every L token, the L/H position of every token,
+        return L * s_sk + Hkv * n * 4 + H * row_bytes / 2 + Hq * d * 4   # exact keys of H, the queries
     if kernel == "weights":           # r of L
         return L * 4 * (Hq // Hkv)
     if kernel == "attn":              # resident K/V rows and the fetched rows, once per KV head
@@ -288,7 +286,7 @@ def run_verkv(args):
                 "algorithmic_bytes": by, "avg_us": avg_ms * 1e3}
 
     roofline = roof_link(dom) if dom == "gather" else roof(dom)
-    roof_score = roof("score_sketch")
+    roof_score = roof("score")
     roof_attn = roof("attn")
     roof_gather = roof_link("gather")
 
@@ -342,7 +340,7 @@ def run_verkv(args):
             "mean_kstar": statistics.mean(kstars) if kstars else None,
             "kernel_share": {k: round(v[0] / total_ms, 4) for k, v in sorted(agg.items(), key=lambda kv: -kv[1][0])},
             "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()},
-            "roofline": roofline, "roofline_score_sketch": roof_score, "roofline_attn": roof_attn,
+            "roofline": roofline, "roofline_score": roof_score, "roofline_attn": roof_attn,
             "roofline_gather": roof_gather, "host_link_peak_gbs": link_peak,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
         }

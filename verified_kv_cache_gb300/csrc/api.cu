@@ -30,7 +30,7 @@ verkv_status fail(Ctx& ctx, verkv_status s, const char* msg)
 
 void free_ws(Ctx& c)
 {
-    void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.ucount,
+    void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.adone, c.ucount,
                     c.staging, c.part,
                     c.d_slot_n};
     for (void* p : ptrs)
@@ -63,6 +63,8 @@ verkv_status alloc_ws(Ctx& ctx)
     VK_CUDA(cudaMalloc(&ctx.om, sizeof(float) * rows * n));
     VK_CUDA(cudaMalloc(&ctx.ulist, sizeof(int32_t) * kvb * n));
     VK_CUDA(cudaMalloc(&ctx.umask, kvb * n));
+    VK_CUDA(cudaMalloc(&ctx.adone, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMemset(ctx.adone, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.ucount, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMemset(ctx.ucount, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.staging, kvb * n * 2 * kHeadDim * ctx.elt));

@@ -30,6 +30,7 @@ struct DecodeArgs {
     uint32_t* ebits;  // [B Hq][ws_n/32 + 1] per query row: tokens of L_g[:k*] \ S (set by the decision kernels)
     float* om;        // [B Hq][ws_n] weight factor of each resident slot (set by the scoring and decision kernels)
     int* err;         // mapped host word, set when a bounded device-side wait gives up
+    int* done;        // [B Hkv] attention blocks finished per KV head (the last one merges; left at 0)
     int Hkv, Hq, G, ws_n, ws_npow2, gen, nsplit;
     float eps_f;
     double eps, ldelta;
@@ -39,6 +40,37 @@ struct DecodeArgs {
 };
 
 __device__ __forceinline__ int row_of(int b, int hq, int Hq) { return b * Hq + hq; }
+
+// K/V row elements (bf16 or fp32) to fp32: eight channels from 16 (or 32) bytes, or a pair.
+template <typename T> struct RowCvt;
+template <> struct RowCvt<__nv_bfloat16> {
+    // 8 channels from 16 bytes
+    static __device__ __forceinline__ void load8(const void* p, float* o)
+    {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+            o[2 * k] = f.x;
+            o[2 * k + 1] = f.y;
+        }
+    }
+    static __device__ __forceinline__ float2 load2(const void* p)
+    {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    }
+};
+template <> struct RowCvt<float> {
+    static __device__ __forceinline__ void load8(const void* p, float* o)
+    {
+        const float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
+        o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+        o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
+    }
+    static __device__ __forceinline__ float2 load2(const void* p) { return *reinterpret_cast<const float2*>(p); }
+};
+
 
 // --------------------------------------------------------------------------------------------
 // Per-row state init.
@@ -99,84 +131,99 @@ __device__ __forceinline__ ff combine3(float s1, float s2, float s3)
 }
 
 template <int G>
-__global__ void __launch_bounds__(kTile) score_int8_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
-                                                           RowState* __restrict__ rows, float2* __restrict__ tl)
+constexpr int kInt8TokensPerThread = G <= 4 ? 4 : 2;
+
+// Exact logits of the tokens of H (resident keys), by H index, for the blocks of a scoring launch
+// past its L tiles: 8 threads per (token, query head), 16 channels each (float-float partial sums
+// combined over the 8 lanes), 128 / (8 G) tokens per block.  Also sets the weight factor of the
+// token's resident slot to 1 for every query head.
+template <typename T, int G>
+__device__ __forceinline__ void score_h_tile(const Views& views, const float* __restrict__ q, const DecodeArgs& a,
+                                             RowState* __restrict__ rows, float2* __restrict__ th, int tile)
 {
-    __shared__ QSplitInt8<G> qs;
-    __shared__ float red[32];
+    constexpr int TPB = kTile / (8 * G);
     const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
     const SlotView& V = views.v[b];
     const int n = V.n;
-    const int i = blockIdx.x * kTile + threadIdx.x;
-    split_q_int8<G>(q + ((int64_t)b * a.Hq + kv * G) * kHeadDim, qs, red);
-    __syncthreads();
-    const int64_t hi_ = (int64_t)kv * n + i;
-    const bool live = i < n && V.flags[hi_] != 2;
-    float mloc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
+    const int nh = V.counts[kv * 4 + 0];
+    const int t = threadIdx.x;
+    const int part = t & 7, g = (t >> 3) % G, tk = t / (8 * G);
+    const int hk = tile * TPB + tk;
+    const bool live = hk < nh;
+    const int row = row_of(b, kv * G + g, a.Hq);
+    ff s = {0.f, 0.f};
+    int slot = 0;
     if (live) {
-        float s1[G], s2[G], s3[G];
+        slot = V.hslot[(int64_t)kv * n + hk];
+        const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + slot) * 2 * kHeadDim + part * 16;
+        const float* qr = q + (int64_t)row * kHeadDim + part * 16;
+        float kk[16], qq[16];
+        RowCvt<T>::load8(key, kk);
+        RowCvt<T>::load8(key + 8, kk + 8);
 #pragma unroll
-        for (int g = 0; g < G; ++g) s1[g] = s2[g] = s3[g] = 0.f;
-        const uint4* crow = reinterpret_cast<const uint4*>(V.codes8 + hi_ * kHeadDim);
-#pragma unroll 1
-        for (int c16 = 0; c16 < kHeadDim / 16; ++c16) {
-            const uint4 w4 = crow[c16];
-            const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-#pragma unroll
-                for (int bte = 0; bte < 4; ++bte) {
-                    const int c = c16 * 16 + k * 4 + bte;
-                    const float cf = (float)(int8_t)((w[k] >> (8 * bte)) & 0xff);
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        s1[g] = __fmaf_rn(qs.h1[g][c], cf, s1[g]);
-                        s2[g] = __fmaf_rn(qs.h2[g][c], cf, s2[g]);
-                        s3[g] = __fmaf_rn(qs.l2[g][c], cf, s3[g]);
-                    }
-                }
-            }
+        for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 x = reinterpret_cast<const float4*>(qr)[c4];
+            qq[4 * c4] = x.x;
+            qq[4 * c4 + 1] = x.y;
+            qq[4 * c4 + 2] = x.z;
+            qq[4 * c4 + 3] = x.w;
         }
-        const float sc = V.scale8[hi_];
-        const int li = V.lpos[hi_];
+        float hi = 0.f, lo = 0.f;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            ff t = combine3(s1[g], s2[g], s3[g]);
-            t = ff_mul(ff_mul_f(t, sc), a.inv_sqrt_d);
-            const int row = row_of(b, kv * G + g, a.Hq);
-            tl[(int64_t)row * a.ws_n + li] = make_float2(t.hi, t.lo);
-            mloc[g] = t.hi;
+        for (int c = 0; c < 16; ++c) {
+            const ff p = two_prod(qq[c], kk[c]);
+            const ff u = two_sum(hi, p.hi);
+            hi = u.hi;
+            lo = __fadd_rn(lo, __fadd_rn(u.lo, p.lo));
         }
+        s = fast_two_sum(hi, lo);
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float m = warp_max(mloc[g]);
-        if ((threadIdx.x & 31) == 0 && m > -INFINITY)
-            atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
+    for (int o = 1; o < 8; o <<= 1) s = ff_add(s, shfl_xor_ff(s, o));
+    float mloc = -INFINITY;
+    if (live && part == 0) {
+        const ff x = ff_mul(s, a.inv_sqrt_d);
+        th[(int64_t)row * a.ws_n + hk] = make_float2(x.hi, x.lo);
+        a.om[(int64_t)row * a.ws_n + slot] = 1.0f;   // H: weight factor 1
+        mloc = x.hi;
     }
-    (void)red;
+    // max per query head: lanes of head g are the 8-lane groups with the same g in the warp
+    for (int o = 8 * G; o < 32; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if ((threadIdx.x & 31) < 8 * G && part == 0 && mloc > -INFINITY)
+        atomicMax(&rows[row].m_tag, tag_max((unsigned)a.gen, mloc));
 }
 
-template <int G>
+// 2-bit sketch tile: GPB sketch groups (of kTile tokens) per block; warp w scores group w, each
+// lane four tokens of it, so every shared-memory load of the query split (four channels at a
+// time) serves four tokens.
+constexpr int kGroupsPerBlock = kTile / 32;
+
+template <typename T, int G>
 __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
-                                                           RowState* __restrict__ rows, float2* __restrict__ tl)
+                                                           RowState* __restrict__ rows, float2* __restrict__ tl,
+                                                           float2* __restrict__ th, int n_ltiles)
 {
-    constexpr int NP = kHeadDim / 8, KEPT = kHeadDim / 4;
-    __shared__ float k1[G][KEPT], rho[G][KEPT];
-    __shared__ ff zsum[G];
-    __shared__ float red[32];
+    if ((int)blockIdx.x >= n_ltiles) {
+        score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
+        return;
+    }
+    constexpr int NP = kHeadDim / 8, KEPT = kHeadDim / 4, GPB = kGroupsPerBlock, TPT = kTile / 32;
+    __shared__ __align__(16) float k1[GPB][G][KEPT];
+    __shared__ __align__(16) float rho[GPB][G][KEPT];
+    __shared__ ff zsum[GPB][G];
     const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
     const SlotView& V = views.v[b];
     const int n = V.n;
-    const int grp = blockIdx.x;  // kTile == sketch group
     const int ngroups = (n + kTile - 1) / kTile;
-    if (grp >= ngroups) return;  // a shorter sequence of the batch
+    const int grp0 = blockIdx.x * GPB;
+    if (grp0 >= ngroups) return;  // a shorter sequence of the batch
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float* qb = q + ((int64_t)b * a.Hq + kv * G) * kHeadDim;
-    // per (head, group): kappa_j = q_ch * scale, Z = sum_j q_ch * zero, split of kappa
-    for (int gg = threadIdx.x >> 5; gg < G; gg += blockDim.x >> 5) {
-        const int j = threadIdx.x & 31;
+    // per (group, head): kappa_j = q_ch * scale, Z = sum_j q_ch * zero, grid split of kappa
+    for (int task = warp; task < GPB * G; task += kTile / 32) {
+        const int gi = task / G, gg = task % G, grp = grp0 + gi;
+        if (grp >= ngroups) continue;
+        const int j = lane;
         const int p = V.pairs[kv * NP + (j % NP)];
         const int ch = j < NP ? p : p + kHeadDim / 2;
         const float qc = qb[gg * kHeadDim + ch];
@@ -185,43 +232,157 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
         const ff kap = two_prod(qc, sc);
         ff zz = two_prod(qc, z);
         zz = warp_sum_ff(zz);
-        float mx = warp_max(fabsf(kap.hi));
+        const float mx = warp_max(fabsf(kap.hi));
         int E;
         frexpf(mx, &E);
         const float K1 = ldexpf(rintf(ldexpf(kap.hi, 17 - E)), E - 17);
-        k1[gg][j] = K1;
-        rho[gg][j] = __fadd_rn(__fsub_rn(kap.hi, K1), kap.lo);
-        if (j == 0) zsum[gg] = zz;
+        k1[gi][gg][j] = K1;
+        rho[gi][gg][j] = __fadd_rn(__fsub_rn(kap.hi, K1), kap.lo);
+        if (j == 0) zsum[gi][gg] = zz;
     }
     __syncthreads();
-    const int i = grp * kTile + threadIdx.x;
-    const int64_t hi_ = (int64_t)kv * n + i;
-    const bool live = i < n && V.flags[hi_] != 2;
+    const int gi = warp, grp = grp0 + gi;
     float mloc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
-    if (live) {
-        const uint64_t w = V.codes2[hi_];
-        float s1[G], s2[G];
+    if (grp < ngroups) {
+        int li[TPT];
+        uint64_t w[TPT];
 #pragma unroll
-        for (int g = 0; g < G; ++g) s1[g] = s2[g] = 0.f;
+        for (int t = 0; t < TPT; ++t) {
+            const int i = grp * kTile + lane + 32 * t;
+            li[t] = i < n ? V.lpos[(int64_t)kv * n + i] : -1;   // < 0: not in L
+            w[t] = li[t] >= 0 ? V.codes2[(int64_t)kv * n + i] : 0ull;
+        }
+        float s1[TPT][G], s2[TPT][G];
 #pragma unroll
-        for (int j = 0; j < KEPT; ++j) {
-            const float cf = (float)((w >> (2 * j)) & 3u);
+        for (int t = 0; t < TPT; ++t)
+#pragma unroll
+            for (int g = 0; g < G; ++g) s1[t][g] = s2[t][g] = 0.f;
+#pragma unroll
+        for (int j4 = 0; j4 < KEPT; j4 += 4) {
+            float cf[TPT][4];
+#pragma unroll
+            for (int t = 0; t < TPT; ++t)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) cf[t][jj] = (float)((unsigned)(w[t] >> (2 * (j4 + jj))) & 3u);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                s1[g] = __fmaf_rn(k1[g][j], cf, s1[g]);
-                s2[g] = __fmaf_rn(rho[g][j], cf, s2[g]);
+                const float4 K = *reinterpret_cast<const float4*>(&k1[gi][g][j4]);
+                const float4 R = *reinterpret_cast<const float4*>(&rho[gi][g][j4]);
+                const float kq[4] = {K.x, K.y, K.z, K.w}, rq[4] = {R.x, R.y, R.z, R.w};
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                    for (int t = 0; t < TPT; ++t) {
+                        s1[t][g] = __fmaf_rn(kq[jj], cf[t][jj], s1[t][g]);
+                        s2[t][g] = __fmaf_rn(rq[jj], cf[t][jj], s2[t][g]);
+                    }
             }
         }
-        const int li = V.lpos[hi_];
+#pragma unroll
+        for (int t = 0; t < TPT; ++t) {
+            if (li[t] < 0) continue;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                ff x = ff_add(zsum[gi][g], two_sum(s1[t][g], s2[t][g]));
+                x = ff_mul(x, a.inv_sqrt_d);
+                const int row = row_of(b, kv * G + g, a.Hq);
+                tl[(int64_t)row * a.ws_n + li[t]] = make_float2(x.hi, x.lo);
+                mloc[g] = fmaxf(mloc[g], x.hi);
+            }
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float m = warp_max(mloc[g]);
+        if (lane == 0 && m > -INFINITY) atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
+    }
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kTile) score_int8_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
+                                                           RowState* __restrict__ rows, float2* __restrict__ tl,
+                                                           float2* __restrict__ th, int n_ltiles)
+{
+    if ((int)blockIdx.x >= n_ltiles) {
+        score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
+        return;
+    }
+    constexpr int TPT = kInt8TokensPerThread<G>;   // tokens per thread: each query-split load serves them all
+    __shared__ __align__(16) QSplitInt8<G> qs;
+    __shared__ float red[32];
+    const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
+    const SlotView& V = views.v[b];
+    const int n = V.n;
+    const int i0 = blockIdx.x * kTile * TPT;
+    if (i0 >= n) return;  // a shorter sequence of the batch
+    split_q_int8<G>(q + ((int64_t)b * a.Hq + kv * G) * kHeadDim, qs, red);
+    __syncthreads();
+    int li[TPT];
+#pragma unroll
+    for (int t = 0; t < TPT; ++t) {
+        const int i = i0 + t * kTile + threadIdx.x;
+        li[t] = i < n ? V.lpos[(int64_t)kv * n + i] : -1;   // < 0: not in L
+    }
+    float s1[TPT][G], s2[TPT][G], s3[TPT][G];
+#pragma unroll
+    for (int t = 0; t < TPT; ++t)
+#pragma unroll
+        for (int g = 0; g < G; ++g) s1[t][g] = s2[t][g] = s3[t][g] = 0.f;
+#pragma unroll 1
+    for (int c16 = 0; c16 < kHeadDim / 16; ++c16) {
+        uint32_t w[TPT][4];
+#pragma unroll
+        for (int t = 0; t < TPT; ++t) {
+            uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+            if (li[t] >= 0)
+                w4 = reinterpret_cast<const uint4*>(V.codes8 + ((int64_t)kv * n + i0 + t * kTile + threadIdx.x) * kHeadDim)[c16];
+            w[t][0] = w4.x;
+            w[t][1] = w4.y;
+            w[t][2] = w4.z;
+            w[t][3] = w4.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int c = c16 * 16 + k * 4;
+            float cf[TPT][4];
+#pragma unroll
+            for (int t = 0; t < TPT; ++t)
+#pragma unroll
+                for (int bte = 0; bte < 4; ++bte) cf[t][bte] = (float)(int8_t)((w[t][k] >> (8 * bte)) & 0xffu);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float4 H1 = *reinterpret_cast<const float4*>(&qs.h1[g][c]);
+                const float4 H2 = *reinterpret_cast<const float4*>(&qs.h2[g][c]);
+                const float4 L2 = *reinterpret_cast<const float4*>(&qs.l2[g][c]);
+                const float h1[4] = {H1.x, H1.y, H1.z, H1.w}, h2[4] = {H2.x, H2.y, H2.z, H2.w},
+                            l2[4] = {L2.x, L2.y, L2.z, L2.w};
+#pragma unroll
+                for (int bte = 0; bte < 4; ++bte)
+#pragma unroll
+                    for (int t = 0; t < TPT; ++t) {
+                        s1[t][g] = __fmaf_rn(h1[bte], cf[t][bte], s1[t][g]);
+                        s2[t][g] = __fmaf_rn(h2[bte], cf[t][bte], s2[t][g]);
+                        s3[t][g] = __fmaf_rn(l2[bte], cf[t][bte], s3[t][g]);
+                    }
+            }
+        }
+    }
+    float mloc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < TPT; ++t) {
+        if (li[t] < 0) continue;
+        const float sc = V.scale8[(int64_t)kv * n + i0 + t * kTile + threadIdx.x];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            ff t = ff_add(zsum[g], two_sum(s1[g], s2[g]));
-            t = ff_mul(t, a.inv_sqrt_d);
+            ff x = combine3(s1[t][g], s2[t][g], s3[t][g]);
+            x = ff_mul(ff_mul_f(x, sc), a.inv_sqrt_d);
             const int row = row_of(b, kv * G + g, a.Hq);
-            tl[(int64_t)row * a.ws_n + li] = make_float2(t.hi, t.lo);
-            mloc[g] = t.hi;
+            tl[(int64_t)row * a.ws_n + li[t]] = make_float2(x.hi, x.lo);
+            mloc[g] = fmaxf(mloc[g], x.hi);
         }
     }
 #pragma unroll
@@ -230,7 +391,6 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
         if ((threadIdx.x & 31) == 0 && m > -INFINITY)
             atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
     }
-    (void)red;
 }
 
 // Exact float-float dot product <q, k>/sqrt(d) of one key row (fp32 or bf16 elements).
@@ -253,8 +413,13 @@ __device__ __forceinline__ ff exact_logit(const float* __restrict__ q, const T* 
 // Exact sketch: the L logits from the keys themselves.
 template <typename T, int G>
 __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
-                                                            RowState* __restrict__ rows, float2* __restrict__ tl)
+                                                            RowState* __restrict__ rows, float2* __restrict__ tl,
+                                                            float2* __restrict__ th, int n_ltiles)
 {
+    if ((int)blockIdx.x >= n_ltiles) {
+        score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
+        return;
+    }
     __shared__ float qs[G][kHeadDim];
     __shared__ float red[32];
     const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
@@ -286,40 +451,6 @@ __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const f
         if ((threadIdx.x & 31) == 0 && m > -INFINITY)
             atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
     }
-    (void)red;
-}
-
-// Exact logits of the tokens of H (resident keys), by H index; one thread per (token, query head).
-template <typename T, int G>
-__global__ void __launch_bounds__(kTile) score_h_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
-                                                        RowState* __restrict__ rows, float2* __restrict__ th)
-{
-    __shared__ float qs[G][kHeadDim];
-    __shared__ float red[32];
-    const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
-    const SlotView& V = views.v[b];
-    const int n = V.n;
-    const int nh = V.counts[kv * 4 + 0];
-    if (blockIdx.x * (kTile / G) >= nh) return;
-    for (int e = threadIdx.x; e < G * kHeadDim; e += blockDim.x)
-        qs[e / kHeadDim][e % kHeadDim] = q[((int64_t)b * a.Hq + kv * G) * kHeadDim + e];
-    __syncthreads();
-    const int g = threadIdx.x % G;
-    const int k = blockIdx.x * (kTile / G) + threadIdx.x / G;
-    float mloc = -INFINITY;
-    if (k < nh) {
-        const int slot = V.hslot[(int64_t)kv * n + k];
-        const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + slot) * 2 * kHeadDim;
-        const ff t = exact_logit<T>(qs[g], key, a.inv_sqrt_d);
-        const int row = row_of(b, kv * G + g, a.Hq);
-        th[(int64_t)row * a.ws_n + k] = make_float2(t.hi, t.lo);
-        a.om[(int64_t)row * a.ws_n + slot] = 1.0f;   // H: weight factor 1
-        mloc = t.hi;
-    }
-    // max per query head: lanes with the same g are G apart
-    for (int o = 16; o >= G; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-    if ((threadIdx.x & 31) < G && mloc > -INFINITY)
-        atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, mloc));
     (void)red;
 }
 
@@ -1522,17 +1653,19 @@ template <int G>
 __global__ void __launch_bounds__(1024) union_kernel(Views views, DecodeArgs a, int32_t* __restrict__ ulist,
                                                      uint8_t* __restrict__ umask, int32_t* __restrict__ ucount)
 {
-    __shared__ int scratch[32];
+    __shared__ int wsum[32], wbase[33];
     const int b = blockIdx.x / a.Hkv, kv = blockIdx.x % a.Hkv;
     const int n = views.v[b].n;
     const int nwords = (n + 31) / 32;
     const int64_t stride = a.ws_n / 32 + 1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t* eb = a.ebits + (int64_t)row_of(b, kv * G, a.Hq) * stride;   // the G rows are consecutive
-    int base = 0;
     int32_t* out = ulist + (int64_t)(b * a.Hkv + kv) * a.ws_n;
     uint8_t* msk = umask + (int64_t)(b * a.Hkv + kv) * a.ws_n;
-    for (int w0 = 0; w0 < nwords; w0 += blockDim.x) {
-        const int wi = w0 + threadIdx.x;
+    int base = 0;
+    for (int w0 = 0; w0 < nwords; w0 += 1024) {
+        // lane l of warp w holds word w0 + 32 w + l
+        const int wi = w0 + warp * 32 + lane;
         uint32_t wg[G];
         uint32_t word = 0u;
 #pragma unroll
@@ -1540,25 +1673,45 @@ __global__ void __launch_bounds__(1024) union_kernel(Views views, DecodeArgs a, 
             wg[g] = wi < nwords ? eb[g * stride + wi] : 0u;
             word |= wg[g];
         }
-        int total;
-        const int ex = block_exclusive_scan(__popc(word), scratch, &total);
-        int pos = base + ex;
-        if (word) {
 #pragma unroll
-            for (int g = 0; g < G; ++g)
-                if (wg[g]) eb[g * stride + wi] = 0u;
-            while (word) {
-                const int bit = __ffs(word) - 1;
-                unsigned m = 0u;
+        for (int g = 0; g < G; ++g)
+            if (wg[g]) eb[g * stride + wi] = 0u;
+        const int cnt = __popc(word);
+        int incl = cnt;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int v = wsum[lane];
+            int x = v;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            wbase[lane] = x - v;
+            if (lane == 31) wbase[32] = x;
+        }
+        __syncthreads();
+        const int pos = base + wbase[warp] + incl - cnt;   // first output position of this lane's word
+        // the warp's 32 words in turn, one bit per lane: coalesced writes
+        const unsigned any = __ballot_sync(0xffffffffu, word != 0u);
+        for (unsigned rest = any; rest; rest &= rest - 1u) {
+            const int k = __ffs(rest) - 1;
+            const uint32_t wk = __shfl_sync(0xffffffffu, word, k);
+            const int pk = __shfl_sync(0xffffffffu, pos, k);
+            unsigned m = 0u;
 #pragma unroll
-                for (int g = 0; g < G; ++g) m |= ((wg[g] >> bit) & 1u) << g;
-                out[pos] = wi * 32 + bit;
-                msk[pos] = (uint8_t)m;
-                ++pos;
-                word &= word - 1u;
+            for (int g = 0; g < G; ++g) m |= ((__shfl_sync(0xffffffffu, wg[g], k) >> lane) & 1u) << g;
+            if ((wk >> lane) & 1u) {
+                const int at = pk + __popc(wk & ((1u << lane) - 1u));
+                out[at] = (w0 + warp * 32 + k) * 32 + lane;
+                msk[at] = (uint8_t)m;
             }
         }
-        base += total;
+        base += wbase[32];
         __syncthreads();
     }
     if (threadIdx.x == 0) ucount[b * a.Hkv + kv] = base;
@@ -1633,6 +1786,7 @@ __global__ void __launch_bounds__(256) gather_kernel(Views views, DecodeArgs a, 
 constexpr int kAttnChunkBytes = 32768;
 constexpr int kAttnStages = 3;
 constexpr int kAttnThreads = 256;
+constexpr int kMaxSplit = 128;              // attention splits per KV head (partials merged per query row)
 constexpr unsigned kWaitLimit = 1u << 22;   // try_wait polls before a wait is declared failed
 
 __device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
@@ -1676,40 +1830,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
                  : "memory");
 }
 
-template <typename T> struct RowCvt;
-template <> struct RowCvt<__nv_bfloat16> {
-    // 8 channels from 16 bytes
-    static __device__ __forceinline__ void load8(const void* p, float* o)
-    {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-            o[2 * k] = f.x;
-            o[2 * k + 1] = f.y;
-        }
-    }
-    static __device__ __forceinline__ float2 load2(const void* p)
-    {
-        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-    }
-};
-template <> struct RowCvt<float> {
-    static __device__ __forceinline__ void load8(const void* p, float* o)
-    {
-        const float4 x = reinterpret_cast<const float4*>(p)[0], y = reinterpret_cast<const float4*>(p)[1];
-        o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
-        o[4] = y.x; o[5] = y.y; o[6] = y.z; o[7] = y.w;
-    }
-    static __device__ __forceinline__ float2 load2(const void* p) { return *reinterpret_cast<const float2*>(p); }
-};
-
 template <typename T, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
                                                             const int32_t* __restrict__ ucount,
                                                             const uint8_t* __restrict__ umask,
-                                                            const T* __restrict__ staging, float* __restrict__ part)
+                                                            const T* __restrict__ staging, float* __restrict__ part,
+                                                            int* __restrict__ done, float* __restrict__ out)
 {
     constexpr int ROWB = 2 * kHeadDim * (int)sizeof(T);   // one K/V row
     constexpr int CR = kAttnChunkBytes / ROWB;             // rows per chunk
@@ -1925,42 +2051,47 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
             }
         }
     }
-}
-
-// LSE merge of the split partials of one query row: per-split scale factors are computed once (one
-// split per thread), then four groups of 128 threads each sum a quarter of the splits per channel.
-__global__ void __launch_bounds__(4 * kHeadDim) merge_kernel(DecodeArgs a, const float* __restrict__ part,
-                                                             float* __restrict__ out)
-{
-    __shared__ float scl[128];
-    __shared__ float red[32];
-    __shared__ float accs[4][kHeadDim];
-    const int row = blockIdx.x, t = threadIdx.x, c = t % kHeadDim, grp = t / kHeadDim;
-    const int ns = a.nsplit;
-    const float* pp = part + (int64_t)row * ns * (kHeadDim + 2);
-    float mx = -INFINITY;
-    for (int s = t; s < ns; s += blockDim.x) mx = fmaxf(mx, pp[s * (kHeadDim + 2) + kHeadDim]);
-    const float M = block_max(mx, red);
-    float l = 0.f;
-    for (int s = t; s < ns; s += blockDim.x) {
-        const float m = pp[s * (kHeadDim + 2) + kHeadDim];
-        const float f = m == -INFINITY ? 0.f : expf(m - M);
-        scl[s] = f;
-        l += pp[s * (kHeadDim + 2) + kHeadDim + 1] * f;
-    }
-    const float L = block_sum(l, red);
-    const int q4 = (ns + 3) / 4;
-    const int s0 = min(ns, grp * q4), s1 = min(ns, s0 + q4);
-    float A0 = 0.f, A1 = 0.f;
-    int s = s0;
-    for (; s + 2 <= s1; s += 2) {
-        A0 += pp[(s + 0) * (kHeadDim + 2) + c] * scl[s + 0];
-        A1 += pp[(s + 1) * (kHeadDim + 2) + c] * scl[s + 1];
-    }
-    if (s < s1) A0 += pp[s * (kHeadDim + 2) + c] * scl[s];
-    accs[grp][c] = A0 + A1;
+    // the last block of the KV head to finish merges the gridDim.y partials of its G query rows
+    // (log-sum-exp over the splits); the counter is left at zero for the next call
+    __shared__ int s_last;
+    __shared__ float s_scl[G][kMaxSplit];
+    __shared__ float s_L[G];
+    __threadfence();
     __syncthreads();
-    if (grp == 0) out[(int64_t)row * kHeadDim + c] = ((accs[0][c] + accs[1][c]) + (accs[2][c] + accs[3][c])) / L;
+    if (tid == 0) s_last = atomicAdd(&done[unit], 1) == ny - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (warp < G) {
+        const int g = warp;
+        const float* pr = part + (int64_t)(row0 + g) * a.nsplit * (kHeadDim + 2);
+        float M = -INFINITY;
+        for (int sp = lane; sp < ny; sp += 32) M = fmaxf(M, pr[sp * (kHeadDim + 2) + kHeadDim]);
+        M = warp_max(M);
+        float L = 0.f;
+        for (int sp = lane; sp < ny; sp += 32) {
+            const float m = pr[sp * (kHeadDim + 2) + kHeadDim];
+            const float f = m == -INFINITY ? 0.f : expf(m - M);
+            s_scl[g][sp] = f;
+            L += pr[sp * (kHeadDim + 2) + kHeadDim + 1] * f;
+        }
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) s_L[g] = L;
+    }
+    __syncthreads();
+    for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
+        const int g = e / kHeadDim, c = e % kHeadDim;
+        const float* pr = part + (int64_t)(row0 + g) * a.nsplit * (kHeadDim + 2);
+        float A0 = 0.f, A1 = 0.f;
+        int sp = 0;
+        for (; sp + 2 <= ny; sp += 2) {
+            A0 = fmaf(pr[sp * (kHeadDim + 2) + c], s_scl[g][sp], A0);
+            A1 = fmaf(pr[(sp + 1) * (kHeadDim + 2) + c], s_scl[g][sp + 1], A1);
+        }
+        if (sp < ny) A0 = fmaf(pr[sp * (kHeadDim + 2) + c], s_scl[g][sp], A0);
+        out[(int64_t)(row0 + g) * kHeadDim + c] = (A0 + A1) / s_L[g];
+    }
+    if (tid == 0) done[unit] = 0;
 }
 
 int g_decide_max_cluster = 8;  // largest cluster the decide kernel is launched with (set once)
@@ -1977,19 +2108,19 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         init_rows_kernel<<<(rowsN + 127) / 128, 128, 0, st>>>(ctx.rows, views, a, B);
         VK_LAUNCHED("init_rows");
     }
-    const dim3 gs((max_n + kTile - 1) / kTile, B * a.Hkv);
-    if (cfg.sketch == VERKV_SKETCH_INT8)
-        score_int8_kernel<G><<<gs, kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl);
-    else if (cfg.sketch == VERKV_SKETCH_2BIT)
-        score_2bit_kernel<G><<<gs, kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl);
-    else
-        score_exact_kernel<T, G><<<gs, kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl);
-    VK_LAUNCHED("score_sketch");
-    if (max_nh > 0) {
-        score_h_kernel<T, G><<<dim3((max_nh * G + kTile - 1) / kTile, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows,
-                                                                                            ctx.th);
-        VK_LAUNCHED("score_h");
+    // one launch scores L (sketch tiles) and H (exact tiles past them)
+    const int h_tiles = (max_nh + kTile / (8 * G) - 1) / (kTile / (8 * G));
+    if (cfg.sketch == VERKV_SKETCH_INT8) {
+        const int lt = (max_n + kTile * kInt8TokensPerThread<G> - 1) / (kTile * kInt8TokensPerThread<G>);
+        score_int8_kernel<T, G><<<dim3(lt + h_tiles, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl, ctx.th, lt);
+    } else if (cfg.sketch == VERKV_SKETCH_2BIT) {
+        const int lt = ((max_n + kTile - 1) / kTile + kGroupsPerBlock - 1) / kGroupsPerBlock;
+        score_2bit_kernel<T, G><<<dim3(lt + h_tiles, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl, ctx.th, lt);
+    } else {
+        const int lt = (max_n + kTile - 1) / kTile;
+        score_exact_kernel<T, G><<<dim3(lt + h_tiles, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl, ctx.th, lt);
     }
+    VK_LAUNCHED("score");
     if (on_chip) {
         int C = 1;
         while (C * kDecideCap < max_nl) C <<= 1;
@@ -2041,10 +2172,8 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         attn_attr = true;
     }
     attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), kAttnThreads, kAttnStages * kAttnChunkBytes, st>>>(
-        views, q, a, ctx.ucount, ctx.umask, (const T*)ctx.staging, ctx.part);
+        views, q, a, ctx.ucount, ctx.umask, (const T*)ctx.staging, ctx.part, a.done, out);
     VK_LAUNCHED("attn");
-    merge_kernel<<<rowsN, 4 * kHeadDim, 0, st>>>(a, ctx.part, out);
-    VK_LAUNCHED("merge");
     return VERKV_OK;
 }
 
@@ -2145,8 +2274,9 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     a.ebits = ctx.ebits;
     a.om = ctx.om;
     a.err = ctx.d_err;
+    a.done = ctx.adone;
     // attention splits per KV head: about two blocks per SM over the whole call
-    a.nsplit = std::min(ctx.nsplit, std::max(1, (2 * ctx.num_sms + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
+    a.nsplit = std::min(std::min(ctx.nsplit, kMaxSplit), std::max(1, (2 * ctx.num_sms + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
     a.eps = eps;
     a.eps_f = (float)eps;
     a.ldelta = std::log(2.0 / delta);

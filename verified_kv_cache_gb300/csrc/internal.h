@@ -107,6 +107,7 @@ struct Ctx {
     float* om = nullptr;            // [rows][n] per query row: weight factor of each resident slot
     int32_t* ulist = nullptr;       // [max_batch][Hkv][n] fetched union, ascending tokens
     uint8_t* umask = nullptr;       // [max_batch][Hkv][n] query heads (bit g) whose exact set holds the row
+    int32_t* adone = nullptr;       // [max_batch][Hkv] attention blocks finished (zero between calls)
     int32_t* ucount = nullptr;      // [max_batch][Hkv]
     void* staging = nullptr;        // [max_batch][Hkv][n][2][d] fetched rows
     float* part = nullptr;          // [rows][nsplit][d + 2] attention partials
