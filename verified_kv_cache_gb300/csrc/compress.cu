@@ -292,6 +292,7 @@ __global__ void sample_kernel(const float* __restrict__ tau, const double* __res
 __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ flags, const float* __restrict__ r,
                                                        int n, int32_t* __restrict__ lpos, int32_t* __restrict__ ltok,
                                                        float* __restrict__ rl, int32_t* __restrict__ lslot,
+                                                       float2* __restrict__ lq,
                                                        int32_t* __restrict__ rtok,
                                                        int32_t* __restrict__ hslot, int32_t* __restrict__ counts)
 {
@@ -312,6 +313,10 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict
                 ltok[base + offL + pL] = i;
                 rl[base + offL + pL] = r[base + i];
                 lslot[base + offL + pL] = isS ? offR + pR : -1;
+                {
+                    const float rr = r[base + i], cr = __fsub_rn(1.0f, rr);
+                    lq[base + offL + pL] = make_float2(__fdiv_rn(cr, rr), __fdiv_rn(rr, cr));
+                }
                 lpos[base + i] = offL + pL;
             } else {
                 lpos[base + i] = -(offH + pH) - 1;
@@ -558,7 +563,7 @@ verkv_status run_sketch(Ctx& ctx, Slot& s, const T* kv, int n, cudaStream_t st)
 
 void free_slot(Slot& s)
 {
-    void* ptrs[] = {s.tau, s.r, s.flags, s.lpos, s.ltok, s.rl, s.lslot, s.rtok, s.hslot, s.counts, s.c, s.capped, s.kvres,
+    void* ptrs[] = {s.tau, s.r, s.flags, s.lpos, s.ltok, s.rl, s.lslot, s.lq, s.rtok, s.hslot, s.counts, s.c, s.capped, s.kvres,
                     s.res_off, s.codes8, s.scale8, s.codes2, s.zero2, s.scale2, s.pairs, s.energy, s.kexact};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -582,6 +587,7 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
     VK_CUDA(cudaMalloc(&s.ltok, sizeof(int32_t) * hn));
     VK_CUDA(cudaMalloc(&s.rl, sizeof(float) * hn));
     VK_CUDA(cudaMalloc(&s.lslot, sizeof(int32_t) * hn));
+    VK_CUDA(cudaMalloc(&s.lq, sizeof(float2) * hn));
     VK_CUDA(cudaMalloc(&s.rtok, sizeof(int32_t) * hn));
     VK_CUDA(cudaMalloc(&s.hslot, sizeof(int32_t) * hn));
     VK_CUDA(cudaMalloc(&s.counts, sizeof(int32_t) * Hkv * 4));
@@ -617,8 +623,8 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
     sample_kernel<<<dim3((n + 255) / 256, Hkv), 256, 0, st>>>(s.tau, s.c, n, cfg.n_sink, cfg.n_local, cfg.seed, layer,
                                                             seq, s.r, s.flags);
     VK_LAUNCHED("sample");
-    compact_kernel<<<Hkv, 1024, 0, st>>>(s.flags, s.r, n, s.lpos, s.ltok, s.rl, s.lslot, s.rtok, s.hslot,
-                                          s.counts);
+    compact_kernel<<<Hkv, 1024, 0, st>>>(s.flags, s.r, n, s.lpos, s.ltok, s.rl, s.lslot, s.lq, s.rtok,
+                                          s.hslot, s.counts);
     VK_LAUNCHED("compact");
 
     std::vector<int32_t> counts((size_t)Hkv * 4), capped((size_t)Hkv + 1);

@@ -1072,25 +1072,38 @@ __device__ SearchAcc block_suffix_search(const SearchAcc& mine, SearchAcc* sh)
     return search_add(r, sh[32 + warp]);
 }
 
-// Block-wide sums of N float-float values at once (two barriers); the totals end in warp 0.
+// Block-wide sums of N fp32 partials, returned as float-float in warp 0: a compensated warp
+// reduction (the rounding error of every addition is carried along), then float-float across the
+// warps (two barriers).
 template <int N>
-__device__ __forceinline__ void block_sum_ff_w0(ff (&v)[N], ff* scratch)
+__device__ __forceinline__ void block_sum_f_w0(const float (&v)[N], ff (&out)[N], ff* scratch)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    float s[N], e[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        s[k] = v[k];
+        e[k] = 0.f;
+    }
     for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-        for (int k = 0; k < N; ++k) v[k] = ff_add(v[k], shfl_xor_ff(v[k], o));
+        for (int k = 0; k < N; ++k) {
+            const float y = __shfl_xor_sync(0xffffffffu, s[k], o), ye = __shfl_xor_sync(0xffffffffu, e[k], o);
+            const ff t = two_sum(s[k], y);
+            s[k] = t.hi;
+            e[k] = __fadd_rn(__fadd_rn(e[k], ye), t.lo);
+        }
     __syncthreads();
     if (lane == 0)
 #pragma unroll
-        for (int k = 0; k < N; ++k) scratch[warp * N + k] = v[k];
+        for (int k = 0; k < N; ++k) scratch[warp * N + k] = fast_two_sum(s[k], e[k]);
     __syncthreads();
     if (warp == 0) {
 #pragma unroll
-        for (int k = 0; k < N; ++k) v[k] = lane < nw ? scratch[lane * N + k] : ff{0.f, 0.f};
+        for (int k = 0; k < N; ++k) out[k] = lane < nw ? scratch[lane * N + k] : ff{0.f, 0.f};
         for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-            for (int k = 0; k < N; ++k) v[k] = ff_add(v[k], shfl_xor_ff(v[k], o));
+            for (int k = 0; k < N; ++k) out[k] = ff_add(out[k], shfl_xor_ff(out[k], o));
     }
 }
 
@@ -1166,15 +1179,16 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const int rank = (int)cl.block_rank();
     const int row = blockIdx.x / C;
     extern __shared__ __align__(16) unsigned char dsm[];
-    // w^, r (phases 0-2) -> scaled a_i, v_i (phase 3); gamma, rho -> gain keys, b_i; then the histogram
+    // phases 0-1: w^, r, gamma, rho; phase 2 leaves b_i, r, a_i, v_i; phase 3: b_i, gain keys, scaled a_i,
+    // scaled v_i; then the histogram
     float* sw = reinterpret_cast<float*>(dsm);
     float* sr = sw + kDecideCap;
     float* sg = sr + kDecideCap;
     float* sp = sg + kDecideCap;
-    unsigned* skey = reinterpret_cast<unsigned*>(sg);
-    float* sb = sp;
-    float* sa_ = sw;
-    float* sv_ = sr;
+    unsigned* skey = reinterpret_cast<unsigned*>(sr);
+    float* sb = sw;
+    float* sa_ = sg;
+    float* sv_ = sp;
     unsigned* hist = reinterpret_cast<unsigned*>(sp + kDecideCap);  // [kSearchFields][kSearchBins]
     __shared__ DecideSlot slot[2];
     __shared__ ff bc[8];
@@ -1208,18 +1222,22 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
 
     // ---- phase 0: weights and the row totals
     {
-        ff acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // D, sum w, sum alpha, sum rho
+        // per-thread partial sums in fp32 (at most eight terms), combined across the block and the
+        // cluster in float-float: sum_L w^, sum_H w, sum alpha, sum rho
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
         const float2* tlr = tl + (int64_t)row * a.ws_n + j0;
         const float* rlr = rl + j0;
+        const float2* lqr = V.lq + (int64_t)kv * V.n + j0;
         float* wlr = wl + (int64_t)row * a.ws_n + j0;
         // all loads of a thread issued before any is used
-        float2 tv[8];
+        float2 tv[8], qv[8];
         float rv[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + k * T;
             tv[k] = i < ns ? tlr[i] : make_float2(0.f, 0.f);
             rv[k] = i < ns ? rlr[i] : 0.f;
+            qv[k] = i < ns ? lqr[i] : make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -1230,14 +1248,11 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             sw[i] = w;
             sr[i] = r;
             wlr[i] = w;
-            const float al = __fmul_rn(w, __fsub_rn(1.0f, r));
-            const float rho = __fdiv_rn(r, __fsub_rn(1.0f, r));
-            sg[i] = w > 0.f ? __fdiv_rn(al, r) : 0.f;
-            sp[i] = rho;
-            acc[0] = ff_add_f(acc[0], w);
-            acc[1] = ff_add_f(acc[1], w);
-            acc[2] = ff_add(acc[2], two_prod(w, __fsub_rn(1.0f, r)));
-            acc[3] = ff_add_f(acc[3], rho);
+            sg[i] = __fmul_rn(w, qv[k].x);   // gamma = w (1 - r) / r
+            sp[i] = qv[k].y;                 // rho = r / (1 - r)
+            acc[0] = __fadd_rn(acc[0], w);
+            acc[2] = __fadd_rn(acc[2], __fmul_rn(w, __fsub_rn(1.0f, r)));
+            acc[3] = __fadd_rn(acc[3], qv[k].y);
         }
         if (rank == 0) {
             const float2* thr = th + (int64_t)row * a.ws_n;
@@ -1247,29 +1262,33 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                 for (int u = 0; u < 4; ++u) hv[u] = k0 + u * T < nh ? thr[k0 + u * T] : make_float2(-INFINITY, 0.f);
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    if (k0 + u * T < nh) acc[0] = ff_add_f(acc[0], weight_of(hv[u], m));
+                    if (k0 + u * T < nh) acc[1] = __fadd_rn(acc[1], weight_of(hv[u], m));
             }
         }
-        block_sum_ff_w0<4>(acc, redff);
-        if (tid == 0)
-            for (int k = 0; k < 4; ++k) slot[parity].v[k] = acc[k];
+        ff tot[4];
+        block_sum_f_w0<4>(acc, tot, redff);
+        if (tid == 0) {
+            for (int k = 0; k < 4; ++k) slot[parity].v[k] = tot[k];
+            if (rank == 0) { wcnt[0] = 0; wcnt[1] = 0; }   // exact-list position and fetch count (phase 4)
+        }
     }
     cluster_combine(cl, slot, parity, 4, bc);
     parity ^= 1;
     if (tid == 0) {
         const ff At = bc[2];
+        const ff Dt = ff_add(bc[0], bc[1]);
         if (rank == 0) {
-            R.D = ff_to_f64(bc[0]);
+            R.D = ff_to_f64(Dt);
             R.alpha_sum = ff_to_f64(At);
             R.n_l = nl;
             R.n_h = nh;
             R.sel_passes = 0;
             for (int k = 0; k < 6; ++k) R.phase_ns[k] = 0;
         }
-        sc.D = bc[0];
+        sc.D = Dt;
         sc.lo = ff{0.f, 0.f};
         sc.hi = At;
-        set_theta(sc, ff_min(At, ff_div(ff_mul_f(bc[1], 4.0f), ff_add_f(bc[3], 1.0f))));
+        set_theta(sc, ff_min(At, ff_div(ff_mul_f(bc[0], 4.0f), ff_add_f(bc[3], 1.0f))));
         sc.done = (nl == 0 || !(At.hi > 0.f));
     }
     __syncthreads();
@@ -1280,20 +1299,21 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     while (!sc.done) {
         ++iters;
         const float tu = sc.th_up, td = sc.th_dn;
-        ff acc[3] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // A, W, R
+        float acc[3] = {0.f, 0.f, 0.f};  // A, W, R
         for (int i = tid; i < ns; i += T) {
             const float wj = sw[i];
             if (!(wj > 0.f)) continue;
             const float al = __fmul_rn(wj, __fsub_rn(1.0f, sr[i]));
-            if (al >= tu) acc[0] = ff_add_f(acc[0], al);   // theta <= alpha: lambda = r
-            else if (sg[i] > td) {                           // theta < gamma: interior
-                acc[1] = ff_add_f(acc[1], wj);
-                acc[2] = ff_add_f(acc[2], sp[i]);
+            if (al >= tu) acc[0] = __fadd_rn(acc[0], al);   // theta <= alpha: lambda = r
+            else if (sg[i] > td) {                            // theta < gamma: interior
+                acc[1] = __fadd_rn(acc[1], wj);
+                acc[2] = __fadd_rn(acc[2], sp[i]);
             }
         }
-        block_sum_ff_w0<3>(acc, redff);
+        ff tot[3];
+        block_sum_f_w0<3>(acc, tot, redff);
         if (tid == 0)
-            for (int k = 0; k < 3; ++k) slot[parity].v[k] = acc[k];
+            for (int k = 0; k < 3; ++k) slot[parity].v[k] = tot[k];
         cluster_combine(cl, slot, parity, 3, bc);
         parity ^= 1;
         if (tid == 0) {
@@ -1320,37 +1340,55 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const float bf = sc.bf;
     stamp(1);
 
-    // ---- phase 2: eq. (7); the weight factor lambda_i / r_i of the sampled entries
+    // ---- phase 2: lambda, a_i, v_i, b_i and eq. (7); the weight factor lambda_i / r_i of the
+    // sampled entries.  a, v, b replace gamma, rho, w^ in shared memory.
     {
-        ff acc[2] = {{0.f, 0.f}, {0.f, 0.f}};
+        float acc[2] = {0.f, 0.f};
         Top2 t2 = {0.f, 0.f, 0x7fffffff};
         int slv[8];
+        float rqv[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) slv[k] = tid + k * T < ns ? V.lslot[(int64_t)kv * V.n + j0 + tid + k * T] : -1;
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + k * T;
+            slv[k] = i < ns ? V.lslot[(int64_t)kv * V.n + j0 + i] : -1;
+            rqv[k] = i < ns ? V.lq[(int64_t)kv * V.n + j0 + i].x : 0.f;
+        }
         float* omr = a.om + (int64_t)row * a.ws_n;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (slv[k] >= 0) {
-                const int i = tid + k * T;
-                omr[slv[k]] = __fdiv_rn(lambda_of(sw[i], sr[i], bf), sr[i]);
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + k * T;
+            if (i >= ns) break;
+            const float w = sw[i], r = sr[i];
+            Coef c = {0.f, 0.f, 0.f};
+            float lam = 1.0f;
+            if (w > 0.f) {
+                // lambda = clip(beta r / (w (1 - r)), r, 1) = clip(beta / gamma, r, 1)
+                lam = fminf(fmaxf(__fdiv_rn(bf, sg[i]), r), 1.0f);
+                const float lw = __fmul_rn(lam, w);
+                c.a = __fmul_rn(w, __fsub_rn(1.0f, lam));
+                c.v = __fmul_rn(__fmul_rn(lw, lw), rqv[k]);          // (lambda w)^2 (1 - r) / r
+                c.b = __fmul_rn(lw, fmaxf(1.0f, rqv[k]));            // lambda w / r max(r, 1 - r)
             }
-        for (int i = tid; i < ns; i += T) {
-            const Coef c = coef_of(sw[i], sr[i], bf);
-            acc[0] = ff_add_f(acc[0], c.a);
-            acc[1] = ff_add_f(acc[1], c.v);
+            if (slv[k] >= 0) omr[slv[k]] = __fdiv_rn(lam, r);
+            sg[i] = c.a;
+            sp[i] = c.v;
+            sw[i] = c.b;
+            acc[0] = __fadd_rn(acc[0], c.a);
+            acc[1] = __fadd_rn(acc[1], c.v);
             const int j = j0 + i;
             if (c.b > t2.b1 || (c.b == t2.b1 && j < t2.arg)) { t2.b2 = t2.b1; t2.b1 = c.b; t2.arg = j; }
             else if (c.b > t2.b2) t2.b2 = c.b;
         }
         for (int o = 16; o > 0; o >>= 1) t2 = top2_merge(t2, shfl_xor_top2(t2, o));
         if (lane == 0) stop2[warp] = t2;
-        block_sum_ff_w0<2>(acc, redff);   // its barriers also publish stop2
+        ff tot[2];
+        block_sum_f_w0<2>(acc, tot, redff);   // its barriers also publish stop2
         if (warp == 0) {
             Top2 x = stop2[lane];
             for (int o = 16; o > 0; o >>= 1) x = top2_merge(x, shfl_xor_top2(x, o));
             if (tid == 0) {
-                slot[parity].v[0] = acc[0];
-                slot[parity].v[1] = acc[1];
+                slot[parity].v[0] = tot[0];
+                slot[parity].v[1] = tot[1];
                 slot[parity].f[0] = x.b1;
                 slot[parity].f[1] = x.b2;
                 slot[parity].i[0] = x.arg;
@@ -1424,11 +1462,12 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         const int ARG = sc.arg;
         const float fa = sc.sa_scale, fv = sc.sv_scale;
         for (int i = tid; i < ns; i += T) {
-            const Coef c = coef_of(sw[i], sr[i], bf);
+            Coef c;
+            c.a = sg[i];
+            c.v = sp[i];
             skey[i] = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
             sa_[i] = __fmul_rn(c.a, fa);   // fixed-point-scaled a_i, v_i (exactly converted below)
             sv_[i] = __fmul_rn(c.v, fv);
-            sb[i] = c.b;
         }
     }
     stamp(3);
@@ -1578,17 +1617,16 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     }
     stamp(4);
 
-    // ---- phase 4: E = keys up to the k*-th; each CTA writes its own members
+    // ---- phase 4: E = keys up to the k*-th; each CTA writes its own members, claiming positions of
+    // the exact list (whose order is irrelevant) and counting fetched tokens on rank 0's counters
     {
         const unsigned long long kk = sc.kkey;
         static_assert(kDecideCap == 8 * kDecideThreads, "emit assumes eight entries per thread");
         bool sel[8];
-        int lcnt = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + k * T;
             sel[k] = i < ns && search_key(skey[i], j0 + i) <= kk;
-            lcnt += sel[k];
         }
         // tokens and resident slots of the selected entries: all loads issued before any is used
         int tok[8], sl8[8];
@@ -1598,15 +1636,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             tok[k] = sel[k] ? V.ltok[e] : 0;
             sl8[k] = sel[k] ? V.lslot[e] : -1;
         }
-        lcnt = block_sum(lcnt, redi);
-        if (tid == 0) slot[parity].i[0] = lcnt;
-        cl.sync();
-        if (tid == 0) {
-            int off = 0;
-            for (int rk = 0; rk < rank; ++rk) off += cl.map_shared_rank(slot, rk)[parity].i[0];
-            wcnt[0] = off;   // running position in the exact list (order is irrelevant)
-        }
-        __syncthreads();
+        int* pos0 = cl.map_shared_rank(&wcnt[0], 0);
         int nf = 0;
         int32_t* el = elist + (int64_t)row * a.ws_n;
         uint32_t* eb = a.ebits + (int64_t)row * (a.ws_n / 32 + 1);
@@ -1616,7 +1646,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             const unsigned m8 = __ballot_sync(0xffffffffu, sel[k]);
             if (m8 == 0u) continue;
             int base = 0;
-            if (lane == __ffs(m8) - 1) base = atomicAdd(&wcnt[0], __popc(m8));
+            if (lane == __ffs(m8) - 1) base = atomicAdd(pos0, __popc(m8));
             base = __shfl_sync(0xffffffffu, base, __ffs(m8) - 1);
             if (sel[k]) {
                 el[base + __popc(m8 & ((1u << lane) - 1u))] = tok[k];
@@ -1628,16 +1658,13 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                 }
             }
         }
-        nf = block_sum(nf, redi);
-        if (tid == 0) slot[parity].i[1] = nf;
-        cl.sync();
+        nf = __reduce_add_sync(0xffffffffu, (unsigned)nf);
+        if (lane == 0 && nf > 0) atomicAdd(cl.map_shared_rank(&wcnt[1], 0), nf);
+        cl.sync();   // every CTA's additions to rank 0's counters are done (and no CTA leaves early)
         if (rank == 0 && tid == 0) {
-            int total_nf = 0;
-            for (int rk = 0; rk < C; ++rk) total_nf += cl.map_shared_rank(slot, rk)[parity].i[1];
             R.kstar = sc.kstar;
-            R.n_fetch = total_nf;
+            R.n_fetch = wcnt[1];
         }
-        cl.sync();
     }
     stamp(5);
 }
@@ -2244,6 +2271,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         v.ltok = s.ltok;
         v.rl = s.rl;
         v.lslot = s.lslot;
+        v.lq = s.lq;
         v.rtok = s.rtok;
         v.hslot = s.hslot;
         v.counts = s.counts;

@@ -25,6 +25,7 @@ struct Slot {
     int32_t* ltok = nullptr;    // [Hkv][n] L index -> token
     float* rl = nullptr;        // [Hkv][n] r by L index
     int32_t* lslot = nullptr;   // [Hkv][n] L index -> resident slot when the token is in S, else -1
+    float2* lq = nullptr;       // [Hkv][n] by L index: ((1 - r) / r, r / (1 - r))
     int32_t* rtok = nullptr;    // [Hkv][n] resident slot -> token (H u S ascending)
     int32_t* hslot = nullptr;   // [Hkv][n] H index -> resident slot
     int32_t* counts = nullptr;  // [Hkv][4] |H|, |L|, |S|, |H|+|S|
@@ -136,6 +137,7 @@ struct SlotView {
     const int32_t* ltok;
     const float* rl;
     const int32_t* lslot;
+    const float2* lq;
     const int32_t* rtok;
     const int32_t* hslot;
     const int32_t* counts;
