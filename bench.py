@@ -105,10 +105,9 @@ def algorithmic_bytes(kernel, stats, traces, w, row_bytes):
         return L * s_sk + Hkv * n * 4 + H * row_bytes / 2 + Hq * d * 4   # exact keys of H, the queries
     if kernel == "weights":           # r of L
         return L * 4 * (Hq // Hkv)
-    if kernel == "attn":              # resident K/V rows and the fetched rows, once per KV head
-        U = traces.get("union_rows", 0)
-        return (R + U) * row_bytes + Hq * d * 8
-    if kernel == "gather":            # fetched rows: read over the host link, written to HBM
+    if kernel == "attn":              # resident K/V rows from HBM, once per KV head, and the queries
+        return R * row_bytes + Hq * d * 8
+    if kernel == "attn_link":         # the fetched rows: over the host link, once per KV head
         return traces.get("union_rows", 0) * row_bytes
     return None
 
@@ -278,17 +277,18 @@ def run_verkv(args):
         if kname not in agg or not link_peak:
             return None
         avg_ms = agg[kname][0] / agg[kname][1]
-        by = algorithmic_bytes(kname, stats0, traces, w, row_bytes)
+        by = algorithmic_bytes(kname + "_link", stats0, traces, w, row_bytes)
         ach = by / (avg_ms / 1e3) / 1e9
         return {"kernel": kname, "bound": "host_link", "achieved": ach, "peak": link_peak, "unit": "GB/s",
                 "frac": ach / link_peak, "traffic": None,
                 "peak_source": "measured in this run: pinned host -> device copy of 256 MiB",
                 "algorithmic_bytes": by, "avg_us": avg_ms * 1e3}
 
-    roofline = roof_link(dom) if dom == "gather" else roof(dom)
+    # the attention kernel also carries the fetch: the host link bounds it whenever rows are fetched
+    roofline = roof_link(dom) if dom == "attn" else roof(dom)
     roof_score = roof("score")
     roof_attn = roof("attn")
-    roof_gather = roof_link("gather")
+    roof_link_attn = roof_link("attn")
 
     # ---------------------------------------------------------------- end to end through the public API
     e2e = None
@@ -341,7 +341,7 @@ def run_verkv(args):
             "kernel_share": {k: round(v[0] / total_ms, 4) for k, v in sorted(agg.items(), key=lambda kv: -kv[1][0])},
             "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()},
             "roofline": roofline, "roofline_score": roof_score, "roofline_attn": roof_attn,
-            "roofline_gather": roof_gather, "host_link_peak_gbs": link_peak,
+            "roofline_attn_link": roof_link_attn, "host_link_peak_gbs": link_peak,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
         }
         print(json.dumps(line))

@@ -31,7 +31,7 @@ verkv_status fail(Ctx& ctx, verkv_status s, const char* msg)
 void free_ws(Ctx& c)
 {
     void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.adone, c.ucount,
-                    c.staging, c.part,
+                    c.part,
                     c.d_slot_n};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -67,7 +67,6 @@ verkv_status alloc_ws(Ctx& ctx)
     VK_CUDA(cudaMemset(ctx.adone, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.ucount, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMemset(ctx.ucount, 0, sizeof(int32_t) * kvb));
-    VK_CUDA(cudaMalloc(&ctx.staging, kvb * n * 2 * kHeadDim * ctx.elt));
     VK_CUDA(cudaMalloc(&ctx.part, sizeof(float) * rows * ctx.nsplit * (kHeadDim + 2)));
     VK_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&ctx.h_err), sizeof(int), cudaHostAllocMapped));
     *ctx.h_err = 0;

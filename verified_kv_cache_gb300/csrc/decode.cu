@@ -42,6 +42,16 @@ struct DecodeArgs {
 __device__ __forceinline__ int row_of(int b, int hq, int Hq) { return b * Hq + hq; }
 
 // K/V row elements (bf16 or fp32) to fp32: eight channels from 16 (or 32) bytes, or a pair.
+// Asynchronous 16-byte copy global -> shared (L2 only), and its group commit / wait.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <typename T> struct RowCvt;
 template <> struct RowCvt<__nv_bfloat16> {
     // 8 channels from 16 bytes
@@ -219,26 +229,32 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
     if (grp0 >= ngroups) return;  // a shorter sequence of the batch
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float* qb = q + ((int64_t)b * a.Hq + kv * G) * kHeadDim;
-    // per (group, head): kappa_j = q_ch * scale, Z = sum_j q_ch * zero, grid split of kappa
-    for (int task = warp; task < GPB * G; task += kTile / 32) {
-        const int gi = task / G, gg = task % G, grp = grp0 + gi;
-        if (grp >= ngroups) continue;
-        const int j = lane;
-        const int p = V.pairs[kv * NP + (j % NP)];
-        const int ch = j < NP ? p : p + kHeadDim / 2;
-        const float qc = qb[gg * kHeadDim + ch];
-        const int64_t pi = ((int64_t)kv * ngroups + grp) * KEPT + j;
-        const float z = __half2float(V.zero2[pi]), sc = __half2float(V.scale2[pi]);
-        const ff kap = two_prod(qc, sc);
-        ff zz = two_prod(qc, z);
-        zz = warp_sum_ff(zz);
-        const float mx = warp_max(fabsf(kap.hi));
-        int E;
-        frexpf(mx, &E);
-        const float K1 = ldexpf(rintf(ldexpf(kap.hi, 17 - E)), E - 17);
-        k1[gi][gg][j] = K1;
-        rho[gi][gg][j] = __fadd_rn(__fsub_rn(kap.hi, K1), kap.lo);
-        if (j == 0) zsum[gi][gg] = zz;
+    // per (group, head): kappa_j = q_ch * scale, Z = sum_j q_ch * zero, grid split of kappa.  Warp w
+    // takes group w, lane j kept channel j; every load is issued before the arithmetic.
+    {
+        const int gi = warp, grp = grp0 + gi;
+        if (grp < ngroups) {
+            const int j = lane;
+            const int64_t pi = ((int64_t)kv * ngroups + grp) * KEPT + j;
+            const float z = __half2float(V.zero2[pi]), sc = __half2float(V.scale2[pi]);
+            const int p = V.pairs[kv * NP + (j % NP)];
+            const int ch = j < NP ? p : p + kHeadDim / 2;
+            float qc[G];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) qc[gg] = qb[gg * kHeadDim + ch];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                const ff kap = two_prod(qc[gg], sc);
+                const ff zz = warp_sum_ff(two_prod(qc[gg], z));
+                const float mx = warp_max(fabsf(kap.hi));
+                int E;
+                frexpf(mx, &E);
+                const float K1 = ldexpf(rintf(ldexpf(kap.hi, 17 - E)), E - 17);
+                k1[gi][gg][j] = K1;
+                rho[gi][gg][j] = __fadd_rn(__fsub_rn(kap.hi, K1), kap.lo);
+                if (j == 0) zsum[gi][gg] = zz;
+            }
+        }
     }
     __syncthreads();
     const int gi = warp, grp = grp0 + gi;
@@ -1107,15 +1123,34 @@ __device__ __forceinline__ void block_sum_f_w0(const float (&v)[N], ff (&out)[N]
     }
 }
 
-__device__ __forceinline__ void cluster_combine(cg::cluster_group& cl, DecideSlot* slot, int parity, int nv,
-                                                ff* out)
+// Thread 0 of every CTA has written slot[parity].v[0..nv) (and, for TOP2, its top-2 of b); warp 0
+// reads them, one rank per lane, and combines them with a butterfly of symmetric operations, so
+// every CTA of the cluster obtains bit-identical totals.
+template <bool TOP2>
+__device__ __forceinline__ void cluster_combine(cg::cluster_group& cl, DecideSlot* slot, int parity, int nv, ff* out,
+                                                Top2* top)
 {
-    // thread 0 of every CTA has written slot[parity].v[0..nv); sum them in rank order
     cl.sync();
-    if (threadIdx.x < nv) {
-        ff s = {0.f, 0.f};
-        for (unsigned rk = 0; rk < cl.num_blocks(); ++rk) s = ff_add(s, cl.map_shared_rank(slot, rk)[parity].v[threadIdx.x]);
-        out[threadIdx.x] = s;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        ff x[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        Top2 t = {0.f, 0.f, 0x7fffffff};
+        if (lane < (int)cl.num_blocks()) {
+            const DecideSlot* rs = cl.map_shared_rank(slot, lane) + parity;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (k < nv) x[k] = rs->v[k];
+            if (TOP2) t = Top2{rs->f[0], rs->f[1], rs->i[0]};
+        }
+        for (int o = 1; o < kDecideMaxCluster; o <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[k] = ff_add(x[k], shfl_xor_ff(x[k], o));
+            if (TOP2) t = top2_merge(t, shfl_xor_top2(t, o));
+        }
+        if (lane == 0) {
+            for (int k = 0; k < nv; ++k) out[k] = x[k];
+            if (TOP2) *top = t;
+        }
     }
     __syncthreads();
 }
@@ -1194,9 +1229,10 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     __shared__ ff bc[8];
     __shared__ ff redff[32 * 4];
     __shared__ Top2 stop2[32];
+    __shared__ Top2 ctop;
     __shared__ int redi[32];
     __shared__ DecideScalars sc;
-    __shared__ int wcnt[32];
+    __shared__ int wcnt[2];
     __shared__ SearchAcc sacc[64];
     __shared__ SearchAcc ssum;   // this CTA's slice total at the current search level
     __shared__ SearchProp sprop;
@@ -1220,8 +1256,15 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         }
     };
 
-    // ---- phase 0: weights and the row totals
+    // ---- phase 0: weights and the row totals; this row's exact-set bitmap (left by the previous
+    // call for its attention) is cleared for phase 4
     {
+        {
+            const int64_t stride = a.ws_n / 32 + 1;
+            uint32_t* eb = a.ebits + (int64_t)row * stride;
+            const int per = (int)((stride + C - 1) / C);
+            for (int wi = rank * per + tid; wi < min((int)stride, (rank + 1) * per); wi += T) eb[wi] = 0u;
+        }
         // per-thread partial sums in fp32 (at most eight terms), combined across the block and the
         // cluster in float-float: sum_L w^, sum_H w, sum alpha, sum rho
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1245,13 +1288,14 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             if (i >= ns) break;
             const float w = weight_of(tv[k], m);
             const float r = rv[k];
+            const float al = __fmul_rn(w, __fsub_rn(1.0f, r));
             sw[i] = w;
-            sr[i] = r;
+            sr[i] = al;                      // alpha = w (1 - r)
             wlr[i] = w;
             sg[i] = __fmul_rn(w, qv[k].x);   // gamma = w (1 - r) / r
             sp[i] = qv[k].y;                 // rho = r / (1 - r)
             acc[0] = __fadd_rn(acc[0], w);
-            acc[2] = __fadd_rn(acc[2], __fmul_rn(w, __fsub_rn(1.0f, r)));
+            acc[2] = __fadd_rn(acc[2], al);
             acc[3] = __fadd_rn(acc[3], qv[k].y);
         }
         if (rank == 0) {
@@ -1272,7 +1316,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             if (rank == 0) { wcnt[0] = 0; wcnt[1] = 0; }   // exact-list position and fetch count (phase 4)
         }
     }
-    cluster_combine(cl, slot, parity, 4, bc);
+    cluster_combine<false>(cl, slot, parity, 4, bc, nullptr);
     parity ^= 1;
     if (tid == 0) {
         const ff At = bc[2];
@@ -1303,7 +1347,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         for (int i = tid; i < ns; i += T) {
             const float wj = sw[i];
             if (!(wj > 0.f)) continue;
-            const float al = __fmul_rn(wj, __fsub_rn(1.0f, sr[i]));
+            const float al = sr[i];
             if (al >= tu) acc[0] = __fadd_rn(acc[0], al);   // theta <= alpha: lambda = r
             else if (sg[i] > td) {                            // theta < gamma: interior
                 acc[1] = __fadd_rn(acc[1], wj);
@@ -1314,7 +1358,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         block_sum_f_w0<3>(acc, tot, redff);
         if (tid == 0)
             for (int k = 0; k < 3; ++k) slot[parity].v[k] = tot[k];
-        cluster_combine(cl, slot, parity, 3, bc);
+        cluster_combine<false>(cl, slot, parity, 3, bc, nullptr);
         parity ^= 1;
         if (tid == 0) {
             const ff theta = sc.theta;
@@ -1346,30 +1390,40 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         float acc[2] = {0.f, 0.f};
         Top2 t2 = {0.f, 0.f, 0x7fffffff};
         int slv[8];
-        float rqv[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + k * T;
             slv[k] = i < ns ? V.lslot[(int64_t)kv * V.n + j0 + i] : -1;
-            rqv[k] = i < ns ? V.lq[(int64_t)kv * V.n + j0 + i].x : 0.f;
         }
         float* omr = a.om + (int64_t)row * a.ws_n;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + k * T;
             if (i >= ns) break;
-            const float w = sw[i], r = sr[i];
+            // with alpha = w (1 - r), gamma = alpha / r, rho = r / (1 - r):
+            //   beta <= alpha: lambda = r, a = alpha, lambda w = w - alpha, v = lambda w alpha,
+            //                  b = max(lambda w, alpha), weight factor 1;
+            //   otherwise:     lambda = min(beta / gamma, 1), a = w - lambda w, v = lambda (lambda w) gamma,
+            //                  b = max(lambda w, lambda gamma), weight factor lambda (1 + rho) / rho
+            const float w = sw[i], al = sr[i], gam = sg[i], rho = sp[i];
             Coef c = {0.f, 0.f, 0.f};
-            float lam = 1.0f;
-            if (w > 0.f) {
-                // lambda = clip(beta r / (w (1 - r)), r, 1) = clip(beta / gamma, r, 1)
-                lam = fminf(fmaxf(__fdiv_rn(bf, sg[i]), r), 1.0f);
+            float om_i = 1.0f;
+            if (!(w > 0.f)) {
+                om_i = __fdiv_rn(__fadd_rn(1.0f, rho), rho);   // lambda = 1: 1 / r
+            } else if (bf <= al) {
+                const float lw = __fsub_rn(w, al);
+                c.a = al;
+                c.v = __fmul_rn(lw, al);
+                c.b = fmaxf(lw, al);
+            } else {
+                const float lam = fminf(__fdiv_rn(bf, gam), 1.0f);
                 const float lw = __fmul_rn(lam, w);
-                c.a = __fmul_rn(w, __fsub_rn(1.0f, lam));
-                c.v = __fmul_rn(__fmul_rn(lw, lw), rqv[k]);          // (lambda w)^2 (1 - r) / r
-                c.b = __fmul_rn(lw, fmaxf(1.0f, rqv[k]));            // lambda w / r max(r, 1 - r)
+                c.a = __fsub_rn(w, lw);
+                c.v = __fmul_rn(__fmul_rn(lam, lw), gam);
+                c.b = fmaxf(lw, __fmul_rn(lam, gam));
+                if (slv[k] >= 0) om_i = __fdiv_rn(__fmul_rn(lam, __fadd_rn(1.0f, rho)), rho);
             }
-            if (slv[k] >= 0) omr[slv[k]] = __fdiv_rn(lam, r);
+            if (slv[k] >= 0) omr[slv[k]] = om_i;
             sg[i] = c.a;
             sp[i] = c.v;
             sw[i] = c.b;
@@ -1395,14 +1449,10 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             }
         }
     }
-    cluster_combine(cl, slot, parity, 2, bc);
+    cluster_combine<true>(cl, slot, parity, 2, bc, &ctop);
     if (tid == 0) {
-        // the two largest b across the cluster (lowest index among equal maxima), merged in rank order
-        Top2 x = {0.f, 0.f, 0x7fffffff};
-        for (int rk = 0; rk < C; ++rk) {
-            const DecideSlot* rs = cl.map_shared_rank(slot, rk);
-            x = top2_merge(x, Top2{rs[parity].f[0], rs[parity].f[1], rs[parity].i[0]});
-        }
+        // the two largest b across the cluster (lowest index among equal maxima)
+        const Top2 x = ctop;
         const float B1 = x.b1, B2 = nl > 1 ? x.b2 : 0.f;
         const ff SA = bc[0], SV = bc[1], ld = a.ld_ff;
         const ff three = {3.0f, 0.f};
@@ -1451,10 +1501,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     parity ^= 1;
     __syncthreads();
     stamp(2);
-    if (sc.no_fetch) {
-        cl.sync();
-        return;
-    }
+    if (!sc.no_fetch) {
 
     // ---- phase 3: gain keys, then k* by the radix search
     {
@@ -1666,84 +1713,18 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             R.n_fetch = wcnt[1];
         }
     }
+    }
     stamp(5);
+
+    cl.sync();   // no CTA leaves while its shared memory may still be read
 }
 
 // --------------------------------------------------------------------------------------------
 // D7: union over the query heads of a KV head of L_g[:k*] \ S (per-row bitmaps set by the decision
 // kernels), compacted to ascending tokens together with the mask of the query heads whose exact set
-// holds each token (bit g); the bitmaps are cleared for the next call.  Then the copy of those rows
-// from the pinned host cache into the staging area (zero-copy loads, one warp per row, 16 bytes per
-// lane, several rows in flight).
+// holds each token (bit g); the bitmaps are cleared for the next call.  The rows themselves cross the
+// host link inside the attention kernel, straight into its shared-memory ring.
 // --------------------------------------------------------------------------------------------
-template <int G>
-__global__ void __launch_bounds__(1024) union_kernel(Views views, DecodeArgs a, int32_t* __restrict__ ulist,
-                                                     uint8_t* __restrict__ umask, int32_t* __restrict__ ucount)
-{
-    __shared__ int wsum[32], wbase[33];
-    const int b = blockIdx.x / a.Hkv, kv = blockIdx.x % a.Hkv;
-    const int n = views.v[b].n;
-    const int nwords = (n + 31) / 32;
-    const int64_t stride = a.ws_n / 32 + 1;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t* eb = a.ebits + (int64_t)row_of(b, kv * G, a.Hq) * stride;   // the G rows are consecutive
-    int32_t* out = ulist + (int64_t)(b * a.Hkv + kv) * a.ws_n;
-    uint8_t* msk = umask + (int64_t)(b * a.Hkv + kv) * a.ws_n;
-    int base = 0;
-    for (int w0 = 0; w0 < nwords; w0 += 1024) {
-        // lane l of warp w holds word w0 + 32 w + l
-        const int wi = w0 + warp * 32 + lane;
-        uint32_t wg[G];
-        uint32_t word = 0u;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            wg[g] = wi < nwords ? eb[g * stride + wi] : 0u;
-            word |= wg[g];
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-            if (wg[g]) eb[g * stride + wi] = 0u;
-        const int cnt = __popc(word);
-        int incl = cnt;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) wsum[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            const int v = wsum[lane];
-            int x = v;
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            wbase[lane] = x - v;
-            if (lane == 31) wbase[32] = x;
-        }
-        __syncthreads();
-        const int pos = base + wbase[warp] + incl - cnt;   // first output position of this lane's word
-        // the warp's 32 words in turn, one bit per lane: coalesced writes
-        const unsigned any = __ballot_sync(0xffffffffu, word != 0u);
-        for (unsigned rest = any; rest; rest &= rest - 1u) {
-            const int k = __ffs(rest) - 1;
-            const uint32_t wk = __shfl_sync(0xffffffffu, word, k);
-            const int pk = __shfl_sync(0xffffffffu, pos, k);
-            unsigned m = 0u;
-#pragma unroll
-            for (int g = 0; g < G; ++g) m |= ((__shfl_sync(0xffffffffu, wg[g], k) >> lane) & 1u) << g;
-            if ((wk >> lane) & 1u) {
-                const int at = pk + __popc(wk & ((1u << lane) - 1u));
-                out[at] = (w0 + warp * 32 + k) * 32 + lane;
-                msk[at] = (uint8_t)m;
-            }
-        }
-        base += wbase[32];
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) ucount[b * a.Hkv + kv] = base;
-}
-
 // Weight factors of the sampled entries on the full-row path (the fused decision kernel writes
 // them itself): 1 when the entry was made exact, lambda_i / r_i otherwise.
 __global__ void __launch_bounds__(256) om_sampled_kernel(Views views, DecodeArgs a, const RowState* __restrict__ rows,
@@ -1766,49 +1747,18 @@ __global__ void __launch_bounds__(256) om_sampled_kernel(Views views, DecodeArgs
     }
 }
 
-__global__ void __launch_bounds__(256) gather_kernel(Views views, DecodeArgs a, const int32_t* __restrict__ ulist,
-                                                     const int32_t* __restrict__ ucount,
-                                                     unsigned char* __restrict__ staging, int row_bytes)
-{
-    const int b = blockIdx.x / a.Hkv, kv = blockIdx.x % a.Hkv;
-    const SlotView& V = views.v[b];
-    const int cnt = ucount[b * a.Hkv + kv];
-    const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
-    const int32_t* lst = ulist + (int64_t)(b * a.Hkv + kv) * a.ws_n;
-    const unsigned char* host = reinterpret_cast<const unsigned char*>(V.kv_host) + (int64_t)kv * V.n * row_bytes;
-    unsigned char* dst = staging + (int64_t)(b * a.Hkv + kv) * a.ws_n * row_bytes;
-    const int vec = row_bytes / 16;  // 16-byte pieces per row (32 for bf16, 64 for fp32)
-    const int stride = gridDim.y * warps;
-    // four rows in flight per warp: their zero-copy host loads overlap
-    for (int u0 = blockIdx.y * warps + (threadIdx.x >> 5); u0 < cnt; u0 += 4 * stride) {
-        int tok[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int u = u0 + k * stride;
-            tok[k] = u < cnt ? lst[u] : -1;
-        }
-        for (int v = lane; v < vec; v += 32) {
-            uint4 x[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (tok[k] >= 0) x[k] = reinterpret_cast<const uint4*>(host + (int64_t)tok[k] * row_bytes)[v];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (tok[k] >= 0) reinterpret_cast<uint4*>(dst + (int64_t)(u0 + k * stride) * row_bytes)[v] = x[k];
-        }
-    }
-}
-
 // --------------------------------------------------------------------------------------------
-// D8: weighted attention (comment closing Algorithm 2; estimator of Theorem 2).  Rows: the
-// resident H u S rows of the KV head, then its staged rows.  Per query head the weight factor is
-// the one the scoring and decision kernels wrote for each resident slot (1 on H and on L_g[:k*],
-// lambda_i / r_i on S \ L_g[:k*]) and, on a staged row, 1 if the head's exact set holds it, else 0.
-// Each block takes every gridDim.y-th chunk of 32 KB of rows (64 bf16 rows) of one KV head; chunks
-// arrive by bulk asynchronous copies (one or two per chunk: the rows are contiguous in the resident
-// cache and in the staging area) into a three-stage ring completed on mbarriers, while the block
-// computes on the previous chunk: q.k for all G query heads (a row's 128 channels split over 2G
-// threads), an online softmax per head, and p.v with two channels per thread.
+// D8 (with the D7 copy): weighted attention (comment closing Algorithm 2; estimator of Theorem 2).
+// Rows: the resident H u S rows of the KV head, then its fetched rows.  Per query head the weight
+// factor is the one the scoring and decision kernels wrote for each resident slot (1 on H and on
+// L_g[:k*], lambda_i / r_i on S \ L_g[:k*]) and, on a fetched row, 1 if the head's exact set holds
+// it, else 0.  Each block takes every gridDim.y-th chunk of 32 KB of rows (64 bf16 rows) of one KV
+// head into a three-stage shared-memory ring: a chunk of resident rows by one bulk asynchronous copy
+// completed on an mbarrier, a chunk holding fetched rows by 16-byte cp.async copies whose sources
+// for the fetched rows are the pinned host cache itself, so the host-link transfer overlaps the
+// compute of the previous chunks and the rows never round-trip through HBM.  Per chunk: q.k for
+// all G query heads (a row's 128 channels split over 2G threads), an online softmax per head, and
+// p.v with two channels per thread; the last block of the KV head merges the splits.
 // --------------------------------------------------------------------------------------------
 constexpr int kAttnChunkBytes = 32768;
 constexpr int kAttnStages = 3;
@@ -1827,6 +1777,11 @@ __device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Bounded wait for the phase with the given parity; false if it did not complete within the limit.
@@ -1859,9 +1814,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
 
 template <typename T, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
-                                                            const int32_t* __restrict__ ucount,
-                                                            const uint8_t* __restrict__ umask,
-                                                            const T* __restrict__ staging, float* __restrict__ part,
+                                                            int32_t* __restrict__ ucount, int32_t* __restrict__ ulist,
+                                                            uint8_t* __restrict__ umask, float* __restrict__ part,
                                                             int* __restrict__ done, float* __restrict__ out)
 {
     constexpr int ROWB = 2 * kHeadDim * (int)sizeof(T);   // one K/V row
@@ -1879,19 +1833,85 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     __shared__ float s_p[CR][G];
     __shared__ float s_corr[G], s_m[G], s_l[G];
     __shared__ int s_bad;
+    __shared__ int s_scan[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
     const SlotView& V = views.v[b];
     const int m_res = V.counts[kv * 4 + 3];
-    const int nu = ucount[unit];
-    const int total = m_res + nu;
-    const int nch = (total + CR - 1) / CR;
-    const int y = blockIdx.y, ny = gridDim.y;
-    const int nmine = nch > y ? (nch - y + ny - 1) / ny : 0;
-    const unsigned char* res = reinterpret_cast<const unsigned char*>(V.kvres) + V.res_off[kv] * (int64_t)ROWB;
-    const unsigned char* stg = reinterpret_cast<const unsigned char*>(staging) + (int64_t)unit * a.ws_n * ROWB;
-    const uint8_t* um = umask + (int64_t)unit * a.ws_n;
     const int row0 = row_of(b, kv * G, a.Hq);   // the G query rows of the KV head are consecutive
+    int32_t* ulw = ulist + (int64_t)unit * a.ws_n;
+    uint8_t* umw = umask + (int64_t)unit * a.ws_n;
+    // D7: the fetched rows of the KV head are the union of its G rows' L_g[:k*] \ S bitmaps, in
+    // ascending tokens.  Every block counts all the words (thread t a contiguous run); the positions
+    // of its own share below are written, with the mask of the heads holding each token, into the
+    // fetch list, which the chunk copies read back.  Block 0 writes the count.
+    int nu;
+    {
+        const int64_t stride = a.ws_n / 32 + 1;
+        const uint32_t* eb = a.ebits + (int64_t)row0 * stride;
+        const int nwords = (V.n + 31) / 32;
+        const int wpt = (nwords + kAttnThreads - 1) / kAttnThreads;
+        const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
+        int c = 0;
+        for (int wi = w0; wi < w1; ++wi) {
+            uint32_t wd = 0u;
+#pragma unroll
+            for (int g = 0; g < G; ++g) wd |= eb[g * stride + wi];
+            c += __popc(wd);
+        }
+        const int pre = block_exclusive_scan(c, s_scan, &nu);
+        const int pf_ = (nu + gridDim.y - 1) / gridDim.y;
+        const int s0 = min(nu, (int)blockIdx.y * pf_), s1 = min(nu, s0 + pf_);
+        if (c > 0 && pre < s1 && pre + c > s0) {
+            int pos = pre;
+            for (int wi = w0; wi < w1 && pos < s1; ++wi) {
+                uint32_t wg[G];
+                uint32_t wd = 0u;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    wg[g] = eb[g * stride + wi];
+                    wd |= wg[g];
+                }
+                while (wd) {
+                    const int bit = __ffs(wd) - 1;
+                    if (pos >= s0 && pos < s1) {
+                        unsigned m = 0u;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) m |= ((wg[g] >> bit) & 1u) << g;
+                        ulw[pos] = wi * 32 + bit;
+                        umw[pos] = (uint8_t)m;
+                    }
+                    ++pos;
+                    wd &= wd - 1u;
+                }
+            }
+        }
+        if (blockIdx.y == 0 && tid == 0) ucount[unit] = nu;
+        __syncthreads();   // this block's share of the list is in place
+    }
+    // this block's rows: an equal share of the fetched rows (so that every block keeps the same
+    // number of bytes on the host link) then an equal share of the resident rows; its chunks are
+    // the fetched ones first, each chunk wholly fetched or wholly resident
+    const int y = blockIdx.y, ny = gridDim.y;
+    const int pf = (nu + ny - 1) / ny, pr = (m_res + ny - 1) / ny;
+    const int f0 = min(nu, y * pf), nF = min(nu, f0 + pf) - f0;
+    const int q0 = min(m_res, y * pr), nR = min(m_res, q0 + pr) - q0;
+    const int nFc = (nF + CR - 1) / CR;
+    const int nmine = nFc + (nR + CR - 1) / CR;
+    // first row (index into resident rows, then fetched rows) and row count of chunk k
+    auto chunk = [&](int k, int& r0, int& cnt) {
+        if (k < nFc) {
+            r0 = m_res + f0 + k * CR;
+            cnt = min(CR, nF - k * CR);
+        } else {
+            r0 = q0 + (k - nFc) * CR;
+            cnt = min(CR, nR - (k - nFc) * CR);
+        }
+    };
+    const unsigned char* res = reinterpret_cast<const unsigned char*>(V.kvres) + V.res_off[kv] * (int64_t)ROWB;
+    const unsigned char* host = reinterpret_cast<const unsigned char*>(V.kv_host) + (int64_t)kv * V.n * ROWB;
+    const int32_t* ul = ulw;
+    const uint8_t* um = umw;
 
     // q slice of this thread (pre-scaled by 1/sqrt(d)), all G heads
     const int sl = tid % NSL;
@@ -1912,21 +1932,53 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     }
     __syncthreads();
 
-    auto issue = [&](int k) {
-        const int st = k % NS;
-        const int r0 = (y + k * ny) * CR, r1 = min(total, r0 + CR);
-        unsigned char* dst = sbuf + st * kAttnChunkBytes;
-        mbar_expect_tx(&full[st], (unsigned)((r1 - r0) * ROWB));
-        const int rm = min(r1, m_res);
-        if (rm > r0) bulk_g2s(dst, res + (int64_t)r0 * ROWB, (unsigned)((rm - r0) * ROWB), &full[st]);
-        const int s0 = max(r0, m_res);
-        if (r1 > s0)
-            bulk_g2s(dst + (s0 - r0) * ROWB, stg + (int64_t)(s0 - m_res) * ROWB, (unsigned)((r1 - s0) * ROWB),
-                     &full[st]);
+    // tokens of the fetched rows of chunk k: lane l < CR / 8 of warp w holds the token of row w + 8 l
+    auto load_tok = [&](int k) -> int {
+        if (k >= nFc) return 0;
+        int r0, cnt;
+        chunk(k, r0, cnt);
+        const int row = warp + 8 * lane;
+        return (lane < CR / 8 && row < cnt) ? ul[r0 + row - m_res] : 0;
+    };
+    // chunk k into stage k % NS.  A chunk of resident rows only is one bulk copy (thread 0); a chunk
+    // holding fetched rows is copied 16 bytes per lane with cp.async, one row per warp at a time, the
+    // fetched rows straight from the pinned host cache over the host link.  Every thread commits one
+    // copy group per call (empty when k is past the block's chunks) so that the group count stays in
+    // step with the chunk count; the stage's mbarrier completes one phase per chunk either way.
+    auto issue = [&](int k, int tokreg) {
+        if (k < nmine) {
+            const int st = k % NS;
+            int r0, cnt;
+            chunk(k, r0, cnt);
+            const int r1 = r0 + cnt;
+            unsigned char* dst = sbuf + st * kAttnChunkBytes;
+            if (k >= nFc) {
+                if (tid == 0) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(&full[st], (unsigned)((r1 - r0) * ROWB));
+                    bulk_g2s(dst, res + (int64_t)r0 * ROWB, (unsigned)((r1 - r0) * ROWB), &full[st]);
+                }
+            } else {
+                if (tid == 0) mbar_arrive(&full[st]);
+#pragma unroll
+                for (int u = 0; u < CR / 8; ++u) {
+                    const int row = warp + 8 * u, R = r0 + row;
+                    const int tok = __shfl_sync(0xffffffffu, tokreg, u);
+                    if (R < r1) {
+                        const unsigned char* src = R < m_res ? res + (int64_t)R * ROWB : host + (int64_t)tok * ROWB;
+#pragma unroll
+                        for (int p = lane; p < ROWB / 16; p += 32) cp_async16(dst + row * ROWB + p * 16, src + p * 16);
+                    }
+                }
+            }
+        }
+        cp_async_commit();
     };
     // weight factors of chunk k, element e = r G + g of the chunk
     auto load_om = [&](int k, float (&o)[EPT]) {
-        const int r0 = (y + k * ny) * CR, r1 = min(total, r0 + CR);
+        int r0, cnt;
+        chunk(k, r0, cnt);
+        const int r1 = r0 + cnt;
 #pragma unroll
         for (int u = 0; u < EPT; ++u) {
             const int e = tid + u * kAttnThreads;
@@ -1945,8 +1997,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
         }
     };
 
-    if (tid == 0)
-        for (int k = 0; k < min(NS, nmine); ++k) issue(k);
+    {
+        int tk[NS];
+#pragma unroll
+        for (int k = 0; k < NS; ++k) tk[k] = load_tok(k);
+#pragma unroll
+        for (int k = 0; k < NS; ++k) issue(k, tk[k]);
+    }
     float omv[EPT];
     if (nmine > 0) {
         load_om(0, omv);
@@ -1959,10 +2016,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     int k = 0;
     for (; k < nmine; ++k) {
         const int st = k % NS;
-        const int r0 = (y + k * ny) * CR, cnt = min(total, r0 + CR) - r0;
+        int r0, cnt;
+        chunk(k, r0, cnt);
         if (k + 1 < nmine) load_om(k + 1, omv);   // stored at the end of this iteration
+        const int tnext = load_tok(k + NS);         // used when chunk k + NS is issued below
         __syncthreads();
         if (!mbar_wait(&full[st], (unsigned)((k / NS) & 1), kWaitLimit)) atomicOr(&s_bad, 1);
+        cp_async_wait<NS - 1>();                    // this thread's copies of chunk k have landed
         __syncthreads();
         if (s_bad) break;
         const unsigned char* buf = sbuf + st * kAttnChunkBytes;
@@ -2053,7 +2113,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
         }
         if (k + 1 < nmine) store_om((k + 1) & 1, omv);
         __syncthreads();   // stage st and s_p are free
-        if (tid == 0 && k + NS < nmine) issue(k + NS);
+        issue(k + NS, tnext);
     }
     if (s_bad) {
         // a copy did not complete in time: report it, and before leaving wait (bounded) for the
@@ -2062,6 +2122,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
             *(volatile int*)a.err = 1;
             for (int kk = k; kk < min(nmine, k + NS); ++kk) mbar_wait(&full[kk % NS], (unsigned)((kk / NS) & 1), kWaitLimit);
         }
+        cp_async_wait<0>();
         __syncthreads();
     }
 #pragma unroll
@@ -2134,6 +2195,8 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
     if (!on_chip) {
         init_rows_kernel<<<(rowsN + 127) / 128, 128, 0, st>>>(ctx.rows, views, a, B);
         VK_LAUNCHED("init_rows");
+        // the fused decision kernel clears its row's exact-set bitmap itself; this path starts clean
+        VK_CUDA(cudaMemsetAsync(a.ebits, 0, sizeof(uint32_t) * rowsN * (a.ws_n / 32 + 1), st));
     }
     // one launch scores L (sketch tiles) and H (exact tiles past them)
     const int h_tiles = (max_nh + kTile / (8 * G) - 1) / (kTile / (8 * G));
@@ -2186,12 +2249,6 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
             views, a, ctx.rows, ctx.wl, ctx.mark);
         VK_LAUNCHED("om_sampled");
     }
-    union_kernel<G><<<B * a.Hkv, 1024, 0, st>>>(views, a, ctx.ulist, ctx.umask, ctx.ucount);
-    VK_LAUNCHED("union");
-    const int row_bytes = (int)(2 * kHeadDim * sizeof(T));
-    gather_kernel<<<dim3(B * a.Hkv, std::max(8, 1216 / (B * a.Hkv))), 256, 0, st>>>(views, a, ctx.ulist, ctx.ucount,
-                                                       (unsigned char*)ctx.staging, row_bytes);
-    VK_LAUNCHED("gather");
     static bool attn_attr = false;   // one per (T, G) instantiation
     if (!attn_attr) {
         VK_CUDA(cudaFuncSetAttribute(attn_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2199,7 +2256,7 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         attn_attr = true;
     }
     attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), kAttnThreads, kAttnStages * kAttnChunkBytes, st>>>(
-        views, q, a, ctx.ucount, ctx.umask, (const T*)ctx.staging, ctx.part, a.done, out);
+        views, q, a, ctx.ucount, ctx.ulist, ctx.umask, ctx.part, a.done, out);
     VK_LAUNCHED("attn");
     return VERKV_OK;
 }

@@ -110,7 +110,6 @@ struct Ctx {
     uint8_t* umask = nullptr;       // [max_batch][Hkv][n] query heads (bit g) whose exact set holds the row
     int32_t* adone = nullptr;       // [max_batch][Hkv] attention blocks finished (zero between calls)
     int32_t* ucount = nullptr;      // [max_batch][Hkv]
-    void* staging = nullptr;        // [max_batch][Hkv][n][2][d] fetched rows
     float* part = nullptr;          // [rows][nsplit][d + 2] attention partials
     int nsplit = 128;               // largest split of the attention over blocks per KV head
     int num_sms = 152;              // multiprocessors of the context's device
