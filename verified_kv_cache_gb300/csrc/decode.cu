@@ -1761,7 +1761,7 @@ __global__ void __launch_bounds__(256) om_sampled_kernel(Views views, DecodeArgs
 // p.v with two channels per thread; the last block of the KV head merges the splits.
 // --------------------------------------------------------------------------------------------
 constexpr int kAttnChunkBytes = 32768;
-constexpr int kAttnStages = 3;
+constexpr int kAttnStages = 2;
 constexpr int kAttnThreads = 256;
 constexpr int kMaxSplit = 128;              // attention splits per KV head (partials merged per query row)
 constexpr unsigned kWaitLimit = 1u << 22;   // try_wait polls before a wait is declared failed
@@ -2142,7 +2142,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     // the last block of the KV head to finish merges the gridDim.y partials of its G query rows
     // (log-sum-exp over the splits); the counter is left at zero for the next call
     __shared__ int s_last;
-    __shared__ float s_scl[G][kMaxSplit];
+    __shared__ float s_scl[G][kMaxSplit], s_lsp[G][kMaxSplit];
     __shared__ float s_L[G];
     __threadfence();
     __syncthreads();
@@ -2150,18 +2150,25 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    // (m, l) of every split and head in one pass, then the scale factors, then the outputs
+    for (int e = tid; e < G * ny; e += kAttnThreads) {
+        const int g = e / ny, sp = e % ny;
+        const float* pp = part + ((int64_t)(row0 + g) * a.nsplit + sp) * (kHeadDim + 2);
+        s_scl[g][sp] = pp[kHeadDim];
+        s_lsp[g][sp] = pp[kHeadDim + 1];
+    }
+    __syncthreads();
     if (warp < G) {
         const int g = warp;
-        const float* pr = part + (int64_t)(row0 + g) * a.nsplit * (kHeadDim + 2);
         float M = -INFINITY;
-        for (int sp = lane; sp < ny; sp += 32) M = fmaxf(M, pr[sp * (kHeadDim + 2) + kHeadDim]);
+        for (int sp = lane; sp < ny; sp += 32) M = fmaxf(M, s_scl[g][sp]);
         M = warp_max(M);
         float L = 0.f;
         for (int sp = lane; sp < ny; sp += 32) {
-            const float m = pr[sp * (kHeadDim + 2) + kHeadDim];
+            const float m = s_scl[g][sp];
             const float f = m == -INFINITY ? 0.f : expf(m - M);
             s_scl[g][sp] = f;
-            L += pr[sp * (kHeadDim + 2) + kHeadDim + 1] * f;
+            L += s_lsp[g][sp] * f;
         }
         for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
         if (lane == 0) s_L[g] = L;
@@ -2170,14 +2177,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     for (int e = tid; e < G * kHeadDim; e += kAttnThreads) {
         const int g = e / kHeadDim, c = e % kHeadDim;
         const float* pr = part + (int64_t)(row0 + g) * a.nsplit * (kHeadDim + 2);
-        float A0 = 0.f, A1 = 0.f;
+        float A0 = 0.f, A1 = 0.f, A2 = 0.f, A3 = 0.f;
         int sp = 0;
-        for (; sp + 2 <= ny; sp += 2) {
+        for (; sp + 4 <= ny; sp += 4) {
             A0 = fmaf(pr[sp * (kHeadDim + 2) + c], s_scl[g][sp], A0);
             A1 = fmaf(pr[(sp + 1) * (kHeadDim + 2) + c], s_scl[g][sp + 1], A1);
+            A2 = fmaf(pr[(sp + 2) * (kHeadDim + 2) + c], s_scl[g][sp + 2], A2);
+            A3 = fmaf(pr[(sp + 3) * (kHeadDim + 2) + c], s_scl[g][sp + 3], A3);
         }
-        if (sp < ny) A0 = fmaf(pr[sp * (kHeadDim + 2) + c], s_scl[g][sp], A0);
-        out[(int64_t)(row0 + g) * kHeadDim + c] = (A0 + A1) / s_L[g];
+        for (; sp < ny; ++sp) A0 = fmaf(pr[sp * (kHeadDim + 2) + c], s_scl[g][sp], A0);
+        out[(int64_t)(row0 + g) * kHeadDim + c] = ((A0 + A1) + (A2 + A3)) / s_L[g];
     }
     if (tid == 0) done[unit] = 0;
 }
