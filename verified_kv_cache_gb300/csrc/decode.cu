@@ -148,8 +148,8 @@ constexpr int kInt8TokensPerThread = G <= 4 ? 4 : 2;
 // combined over the 8 lanes), 128 / (8 G) tokens per block.  Also sets the weight factor of the
 // token's resident slot to 1 for every query head.
 template <typename T, int G>
-__device__ __forceinline__ void score_h_tile(const Views& views, const float* __restrict__ q, const DecodeArgs& a,
-                                             RowState* __restrict__ rows, float2* __restrict__ th, int tile)
+__device__ __forceinline__ void score_h_tile1(const Views& views, const float* __restrict__ q, const DecodeArgs& a,
+                                              RowState* __restrict__ rows, float2* __restrict__ th, int tile)
 {
     constexpr int TPB = kTile / (8 * G);
     const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
@@ -201,6 +201,17 @@ __device__ __forceinline__ void score_h_tile(const Views& views, const float* __
     for (int o = 8 * G; o < 32; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
     if ((threadIdx.x & 31) < 8 * G && part == 0 && mloc > -INFINITY)
         atomicMax(&rows[row].m_tag, tag_max((unsigned)a.gen, mloc));
+}
+
+// kHTilesPerBlock consecutive H tiles per block, so that the L and H blocks of a scoring launch fit in
+// one wave of resident blocks.
+constexpr int kHTilesPerBlock = 4;
+
+template <typename T, int G>
+__device__ __forceinline__ void score_h_tile(const Views& views, const float* __restrict__ q, const DecodeArgs& a,
+                                             RowState* __restrict__ rows, float2* __restrict__ th, int block)
+{
+    for (int t = 0; t < kHTilesPerBlock; ++t) score_h_tile1<T, G>(views, q, a, rows, th, block * kHTilesPerBlock + t);
 }
 
 // 2-bit sketch tile: GPB sketch groups (of kTile tokens) per block; warp w scores group w, each
@@ -984,17 +995,21 @@ __global__ void __launch_bounds__(1024) fallback_kernel(Views views, DecodeArgs 
 //   phase 1: Definition 2's fixed point by safeguarded Newton on G(beta) = beta (1 + R) - A - W,
 //            started above the root (four times the all-interior solution).
 //   phase 2: a_i, v_i, b_i; eq. (7); the no-fetch test (Algorithm 2, lines 2-5).
-//   phase 3: gain keys (eq. (9)) and k* (eq. (10)) by an MSD radix search over the 48-bit keys
-//            (gain descending, L index ascending): per 11-bit digit, a cluster-wide histogram of
-//            counts, exact fixed-point sums of a_i and v_i and the max of b_i (plain 32-bit shared
+//   phase 3: gain keys (eq. (9)) and k* (eq. (10)) by a search over the 48-bit keys (gain
+//            descending, L index ascending): per level, the remaining key range is split into at most
+//            2048 bins of a power-of-two width (the first level spans the cluster's own key range); a
+//            cluster-wide histogram
+//            of counts, exact fixed-point sums of a_i and v_i and the max of b_i (plain 32-bit shared
 //            atomics) gives the residual certificate at every bin boundary, so the bin holding the
-//            k*-th key is found without sorting; the search stops once that bin holds one key.
+//            k*-th key is found without sorting.  A bin of one key ends the search; a bin of at most
+//            64 keys is finished by one warp (the keys gathered, sorted and scanned exactly).
 //   phase 4: E = L_g[:k*] = the keys up to the k*-th, written as marks and a token list.
 // --------------------------------------------------------------------------------------------
 constexpr int kDecideThreads = 1024;
 constexpr int kDecideCap = 8192;   // L entries per CTA
 constexpr int kDecideMaxCluster = 16;  // 16 is a non-portable cluster size: used when the GPU can run it
-// k* search: keys of 31 gain bits and 17 index bits, digits of 11 bits (the last level takes 4)
+// k* search: keys of 31 gain bits and 17 index bits; each level splits the remaining key range into
+// 2^11 bins
 constexpr int kKeyBits = 48;
 constexpr int kSearchBits = 11;
 constexpr int kSearchLevels = 5;
@@ -1126,30 +1141,43 @@ __device__ __forceinline__ void block_sum_f_w0(const float (&v)[N], ff (&out)[N]
 // Thread 0 of every CTA has written slot[parity].v[0..nv) (and, for TOP2, its top-2 of b); warp 0
 // reads them, one rank per lane, and combines them with a butterfly of symmetric operations, so
 // every CTA of the cluster obtains bit-identical totals.
-template <bool TOP2>
+template <bool TOP2, bool EXT = false>
 __device__ __forceinline__ void cluster_combine(cg::cluster_group& cl, DecideSlot* slot, int parity, int nv, ff* out,
-                                                Top2* top)
+                                                Top2* top, float* ext = nullptr)
 {
     cl.sync();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         ff x[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         Top2 t = {0.f, 0.f, 0x7fffffff};
+        unsigned e[4] = {0x7f800000u, 0x7f800000u, 0u, 0u};
         if (lane < (int)cl.num_blocks()) {
             const DecideSlot* rs = cl.map_shared_rank(slot, lane) + parity;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 if (k < nv) x[k] = rs->v[k];
             if (TOP2) t = Top2{rs->f[0], rs->f[1], rs->i[0]};
+            if (EXT)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) e[k] = __float_as_uint(rs->f[k]);
         }
         for (int o = 1; o < kDecideMaxCluster; o <<= 1) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) x[k] = ff_add(x[k], shfl_xor_ff(x[k], o));
             if (TOP2) t = top2_merge(t, shfl_xor_top2(t, o));
         }
+        if (EXT) {
+            e[0] = __reduce_min_sync(0xffffffffu, e[0]);
+            e[1] = __reduce_min_sync(0xffffffffu, e[1]);
+            e[2] = __reduce_max_sync(0xffffffffu, e[2]);
+            e[3] = __reduce_max_sync(0xffffffffu, e[3]);
+        }
         if (lane == 0) {
             for (int k = 0; k < nv; ++k) out[k] = x[k];
             if (TOP2) *top = t;
+            if (EXT)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) ext[k] = __uint_as_float(e[k]);
         }
     }
     __syncthreads();
@@ -1165,13 +1193,20 @@ struct DecideScalars {
     int arg, no_fetch;
     float Df, ldf, sa_scale, sv_scale;  // fixed-point scales: a_i * sa_scale, v_i * sv_scale (totals ~2^40)
     // radix search state
-    unsigned long long prefix;          // key bits fixed so far
+    unsigned long long klo, khi;        // the key range still searched
     int rem_cnt;                        // keys below the current prefix range (removed)
     unsigned long long rest_a, rest_v;  // keys above the current prefix range (kept), fixed point
     unsigned int rest_b, rest_c;        // max b over them (ordered float bits), their count
-    int kstar, found;
+    int kstar, found, in_bin;
     unsigned long long kkey;            // the k*-th smallest key
 };
+
+// A key of the boundary bin with its exact fixed-point a, v and b (ordered bits).
+struct SmallCand {
+    unsigned long long key, a, v;
+    unsigned b, pad;
+};
+constexpr int kSmallBin = 64;   // boundary bins this small are finished by one warp
 
 // theta >= 0 is a normalised float-float (hi = RN(hi + lo)), so the smallest float >= theta is hi, or
 // the next float up when lo > 0; the largest float <= theta is hi, or the next float down when lo < 0.
@@ -1199,6 +1234,109 @@ __device__ __forceinline__ void fixed_pieces(float x, unsigned* p)
     p[0] = (unsigned)r1c;
     p[1] = (unsigned)(h1c - c2 * 0x1p14f);
     p[2] = (unsigned)(h2 + c2);
+}
+
+// Finish of the k* search when the boundary bin holds at most kSmallBin keys (run by warp 0 of every
+// CTA of the cluster, which all obtain the same answer): the keys of the bin are copied from every
+// CTA's list into `loc`, each is placed by its rank (the keys are distinct), and the residual after
+// each is the level's outside rest plus the exact suffix sums of the keys after it; k* ends at the
+// first boundary whose certificate is below eps.
+__device__ __forceinline__ void finish_small(cg::cluster_group& cl, const SmallCand* cand, const int* ncand,
+                                             SmallCand* loc, DecideScalars& sc, int C, float ldf, float Df,
+                                             float inv_fa, float inv_fv, float eps_f)
+{
+    const int lane = threadIdx.x & 31;
+    // offsets of each CTA's list
+    const int cnt = lane < C ? *cl.map_shared_rank(ncand, lane) : 0;
+    int incl = cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int ntot = __shfl_sync(0xffffffffu, incl, 31);
+    SmallCand mine[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = lane + 32 * h;
+        int rk = 0, off = 0;
+        for (int r = 0; r < C; ++r) {
+            const int ex = __shfl_sync(0xffffffffu, incl - cnt, r);   // exclusive offset of rank r
+            if (e >= ex) { rk = r; off = ex; }
+        }
+        mine[h] = SmallCand{~0ull, 0ull, 0ull, 0u, 0u};
+        if (e < ntot) mine[h] = cl.map_shared_rank(cand, rk)[e - off];
+    }
+    // rank of each key among the candidates (keys are distinct), then the sorted copy in `loc`
+    __shared__ unsigned long long keys_[kSmallBin];
+    keys_[lane] = mine[0].key;
+    keys_[lane + 32] = mine[1].key;
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (lane + 32 * h >= ntot) continue;
+        int rnk = 0;
+        for (int q = 0; q < ntot; ++q) rnk += keys_[q] < mine[h].key;
+        loc[rnk] = mine[h];
+    }
+    __syncwarp();
+    unsigned long long av[2], vv[2];
+    unsigned bb[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        av[h] = i < ntot ? loc[i].a : 0ull;
+        vv[h] = i < ntot ? loc[i].v : 0ull;
+        bb[h] = i < ntot ? loc[i].b : 0u;
+    }
+    // exclusive suffix (over larger keys) of a, v and max b
+    unsigned long long sa[2], sv[2];
+    unsigned sb_[2];
+    {
+        unsigned long long xa = av[1], xv = vv[1];
+        unsigned xb = bb[1];
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long ya = __shfl_down_sync(0xffffffffu, xa, o), yv = __shfl_down_sync(0xffffffffu, xv, o);
+            const unsigned yb = __shfl_down_sync(0xffffffffu, xb, o);
+            if (lane + o < 32) { xa += ya; xv += yv; xb = max(xb, yb); }
+        }
+        const unsigned long long ta1 = __shfl_sync(0xffffffffu, xa, 0), tv1 = __shfl_sync(0xffffffffu, xv, 0);
+        const unsigned tb1 = __shfl_sync(0xffffffffu, xb, 0);
+        sa[1] = xa - av[1];
+        sv[1] = xv - vv[1];
+        sb_[1] = __shfl_down_sync(0xffffffffu, xb, 1);
+        if (lane == 31) sb_[1] = 0u;
+        unsigned long long za = av[0], zv = vv[0];
+        unsigned zb = bb[0];
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long ya = __shfl_down_sync(0xffffffffu, za, o), yv = __shfl_down_sync(0xffffffffu, zv, o);
+            const unsigned yb = __shfl_down_sync(0xffffffffu, zb, o);
+            if (lane + o < 32) { za += ya; zv += yv; zb = max(zb, yb); }
+        }
+        unsigned nb0 = __shfl_down_sync(0xffffffffu, zb, 1);
+        if (lane == 31) nb0 = 0u;
+        sa[0] = za - av[0] + ta1;
+        sv[0] = zv - vv[0] + tv1;
+        sb_[0] = max(nb0, tb1);
+    }
+    // the first key whose residual (the keys after it, plus the rest above the bin) is accepted
+    int best = 0x7fffffff;
+#pragma unroll
+    for (int h = 1; h >= 0; --h) {
+        const int i = lane + 32 * h;
+        if (i < ntot) {
+            const unsigned long long A = sc.rest_a + sa[h], Vv = sc.rest_v + sv[h];
+            const unsigned Bm = max(sc.rest_b, sb_[h]);
+            const int after = (ntot - 1 - i) + (int)sc.rest_c;
+            if (after > 0 && cert_f((float)A * inv_fa, (float)Vv * inv_fv, __uint_as_float(Bm), ldf, Df) < eps_f) best = i;
+        }
+    }
+    best = __reduce_min_sync(0xffffffffu, best);
+    if (best == 0x7fffffff) best = ntot - 1;   // the bin's last boundary was accepted at its level
+    if (lane == 0) {
+        sc.found = 1;
+        sc.kstar = sc.rem_cnt + best + 1;
+        sc.kkey = loc[best].key;
+    }
 }
 
 __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, DecodeArgs a,
@@ -1230,6 +1368,10 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     __shared__ ff redff[32 * 4];
     __shared__ Top2 stop2[32];
     __shared__ Top2 ctop;
+    __shared__ unsigned sext[32][4];
+    __shared__ SmallCand bcand[kSmallBin], bloc[kSmallBin];
+    __shared__ int ncand;
+    __shared__ float bext[4];
     __shared__ int redi[32];
     __shared__ DecideScalars sc;
     __shared__ int wcnt[2];
@@ -1344,21 +1486,56 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         ++iters;
         const float tu = sc.th_up, td = sc.th_dn;
         float acc[3] = {0.f, 0.f, 0.f};  // A, W, R
+        // the breakpoints nearest theta: min alpha of the lambda = r class, min gamma of the interior,
+        // max alpha outside the lambda = r class, max gamma of the lambda = 1 class
+        float uA = INFINITY, uG = INFINITY, lA = 0.f, lG = 0.f;
         for (int i = tid; i < ns; i += T) {
             const float wj = sw[i];
             if (!(wj > 0.f)) continue;
             const float al = sr[i];
-            if (al >= tu) acc[0] = __fadd_rn(acc[0], al);   // theta <= alpha: lambda = r
-            else if (sg[i] > td) {                            // theta < gamma: interior
-                acc[1] = __fadd_rn(acc[1], wj);
-                acc[2] = __fadd_rn(acc[2], sp[i]);
+            if (al >= tu) {                                   // theta <= alpha: lambda = r
+                acc[0] = __fadd_rn(acc[0], al);
+                uA = fminf(uA, al);
+            } else {
+                lA = fmaxf(lA, al);
+                const float ga = sg[i];
+                if (ga > td) {                                // theta < gamma: interior
+                    acc[1] = __fadd_rn(acc[1], wj);
+                    acc[2] = __fadd_rn(acc[2], sp[i]);
+                    uG = fminf(uG, ga);
+                } else {
+                    lG = fmaxf(lG, ga);
+                }
+            }
+        }
+        {
+            const unsigned e0 = __reduce_min_sync(0xffffffffu, __float_as_uint(uA));
+            const unsigned e1 = __reduce_min_sync(0xffffffffu, __float_as_uint(uG));
+            const unsigned e2 = __reduce_max_sync(0xffffffffu, __float_as_uint(lA));
+            const unsigned e3 = __reduce_max_sync(0xffffffffu, __float_as_uint(lG));
+            if (lane == 0) {
+                sext[warp][0] = e0;
+                sext[warp][1] = e1;
+                sext[warp][2] = e2;
+                sext[warp][3] = e3;
             }
         }
         ff tot[3];
-        block_sum_f_w0<3>(acc, tot, redff);
-        if (tid == 0)
-            for (int k = 0; k < 3; ++k) slot[parity].v[k] = tot[k];
-        cluster_combine<false>(cl, slot, parity, 3, bc, nullptr);
+        block_sum_f_w0<3>(acc, tot, redff);   // its barriers also publish sext
+        if (warp == 0) {
+            const unsigned e0 = __reduce_min_sync(0xffffffffu, sext[lane][0]);
+            const unsigned e1 = __reduce_min_sync(0xffffffffu, sext[lane][1]);
+            const unsigned e2 = __reduce_max_sync(0xffffffffu, sext[lane][2]);
+            const unsigned e3 = __reduce_max_sync(0xffffffffu, sext[lane][3]);
+            if (tid == 0) {
+                for (int k = 0; k < 3; ++k) slot[parity].v[k] = tot[k];
+                slot[parity].f[0] = __uint_as_float(e0);
+                slot[parity].f[1] = __uint_as_float(e1);
+                slot[parity].f[2] = __uint_as_float(e2);
+                slot[parity].f[3] = __uint_as_float(e3);
+            }
+        }
+        cluster_combine<false, true>(cl, slot, parity, 3, bc, nullptr, bext);
         parity ^= 1;
         if (tid == 0) {
             const ff theta = sc.theta;
@@ -1366,7 +1543,16 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             const ff g = ff_sub(ff_mul(theta, oneR), AW);
             if (g.hi >= 0.f) sc.hi = ff_min(sc.hi, theta); else sc.lo = ff_max(sc.lo, theta);
             ff nt = ff_div(AW, oneR);
-            if (ff_eq(nt, theta) || iters >= 200) sc.done = 1;
+            // the classes at nt are those at theta when no breakpoint lies between them: then nt is
+            // the root (the next pass would return it again)
+            const float nu_ = nt.lo > 0.f ? __uint_as_float(__float_as_uint(nt.hi) + 1u) : nt.hi;
+            const float nd_ = nt.lo < 0.f ? __uint_as_float(__float_as_uint(nt.hi) - 1u) : nt.hi;
+            const bool up = ff_lt(theta, nt);
+            const bool same = up ? (bext[0] >= nu_ && bext[1] > nd_) : (bext[2] < nu_ && bext[3] <= nd_);
+            if (same && !ff_eq(nt, theta) && ff_lt(sc.lo, nt) && ff_lt(nt, sc.hi)) {
+                set_theta(sc, nt);
+                sc.done = 1;
+            } else if (ff_eq(nt, theta) || iters >= 200) sc.done = 1;
             else {
                 if (!(ff_lt(sc.lo, nt) && ff_lt(nt, sc.hi)))
                     nt = sc.lo.hi > 0.f ? ff_sqrt(ff_mul(sc.lo, sc.hi)) : ff_mul_f(ff_add(sc.lo, sc.hi), 0.5f);
@@ -1473,7 +1659,8 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         sc.Df = sc.D.hi;
         sc.sa_scale = SA.hi > 0.f ? __fdiv_rn(0x1p40f, SA.hi) : 0.f;
         sc.sv_scale = SV.hi > 0.f ? __fdiv_rn(0x1p40f, SV.hi) : 0.f;
-        sc.prefix = 0;
+        sc.klo = 0;
+        sc.khi = 0;
         sc.rem_cnt = 0;
         sc.rest_a = 0;
         sc.rest_v = 0;
@@ -1508,13 +1695,48 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         const GainParams gp = sc.gp;
         const int ARG = sc.arg;
         const float fa = sc.sa_scale, fv = sc.sv_scale;
+        // entries of gain exactly 0 (an underflowed weight: a = v = 0) end every order and never move
+        // k*: they stay out of the search, counted (with their max b) in every residual
+        unsigned kmin = 0xffffffffu, kmax = 0u, zc = 0u, zb = 0u;
         for (int i = tid; i < ns; i += T) {
             Coef c;
             c.a = sg[i];
             c.v = sp[i];
-            skey[i] = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
+            const unsigned k32 = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
+            skey[i] = k32;
+            if ((k32 & 0x7fffffffu) == 0x7fffffffu) {
+                ++zc;
+                zb = max(zb, fmax_bits(sb[i]));
+            } else {
+                kmin = min(kmin, k32 & 0x7fffffffu);
+                kmax = max(kmax, k32 & 0x7fffffffu);
+            }
             sa_[i] = __fmul_rn(c.a, fa);   // fixed-point-scaled a_i, v_i (exactly converted below)
             sv_[i] = __fmul_rn(c.v, fv);
+        }
+        // the cluster's range of the other keys: the first search level spreads its bins over it
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        zc = __reduce_add_sync(0xffffffffu, zc);
+        zb = __reduce_max_sync(0xffffffffu, zb);
+        if (lane == 0) {
+            sext[warp][0] = kmin;
+            sext[warp][1] = kmax;
+            sext[warp][2] = zc;
+            sext[warp][3] = zb;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            kmin = __reduce_min_sync(0xffffffffu, sext[lane][0]);
+            kmax = __reduce_max_sync(0xffffffffu, sext[lane][1]);
+            zc = __reduce_add_sync(0xffffffffu, sext[lane][2]);
+            zb = __reduce_max_sync(0xffffffffu, sext[lane][3]);
+            if (lane == 0) {
+                slot[parity].i[0] = (int)kmin;
+                slot[parity].i[1] = (int)kmax;
+                slot[parity].i[2] = (int)zc;
+                slot[parity].i[3] = (int)zb;
+            }
         }
     }
     stamp(3);
@@ -1526,18 +1748,39 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         uint4* hist4 = reinterpret_cast<uint4*>(hist);
         for (int k = tid; k < kSearchFields * kSearchBins / 4; k += T) hist4[k] = make_uint4(0u, 0u, 0u, 0u);
         cl.sync();   // every histogram of the cluster is zero before any CTA adds to a remote one
+        if (warp == 0) {
+            const DecideSlot* rs = lane < C ? cl.map_shared_rank(slot, lane) + parity : nullptr;
+            const unsigned mn = __reduce_min_sync(0xffffffffu, rs ? (unsigned)rs->i[0] : 0xffffffffu);
+            const unsigned mx = __reduce_max_sync(0xffffffffu, rs ? (unsigned)rs->i[1] : 0u);
+            const unsigned zc = __reduce_add_sync(0xffffffffu, rs ? (unsigned)rs->i[2] : 0u);
+            const unsigned zb = __reduce_max_sync(0xffffffffu, rs ? (unsigned)rs->i[3] : 0u);
+            if (lane == 0) {
+                if (mn <= mx) {
+                    sc.klo = (unsigned long long)mn << (kKeyBits - 31);
+                    sc.khi = ((unsigned long long)mx + 1ull) << (kKeyBits - 31);
+                } else {
+                    sc.klo = sc.khi = 0ull;   // no key of positive gain: the search finds no boundary
+                }
+                sc.rest_c = zc;
+                sc.rest_b = zb;
+            }
+        }
+        __syncthreads();
+        parity ^= 1;
+        // each level splits the current key range [klo, khi) into bins of 2^bs keys (K falls in bin
+        // (K - klo) >> bs, at most kSearchBins of them); a level shrinks the range by at least
+        // kSearchBins / 2, so five levels reach a single key
         for (int lev = 0; lev < kSearchLevels; ++lev) {
             ++passes;
-            const int width = lev < kSearchLevels - 1 ? kSearchBits : kKeyBits - kSearchBits * (kSearchLevels - 1);
-            const int shift = kKeyBits - kSearchBits * lev - width;
-            const int nb = 1 << width;
+            const int nb = kSearchBins;
             const int sl = nb / C;   // bins per slice: CTA r owns the cluster totals of bins [r sl, (r + 1) sl)
-            const unsigned long long hi = sc.prefix;
-            const int up = shift + width;
+            const unsigned long long klo = sc.klo, span = sc.khi - sc.klo;
+            // bins of 2^bs keys, bs the smallest shift that fits the range in nb bins (at least half used)
+            const int bs = max(0, (64 - __clzll((long long)(span - 1ull))) - kSearchBits);
             for (int i = tid; i < ns; i += T) {
                 const unsigned long long K = search_key(skey[i], j0 + i);
-                if ((K >> up) != hi) continue;
-                const unsigned d = (unsigned)(K >> shift) & (unsigned)(nb - 1);
+                if (K < klo || K - klo >= span) continue;
+                const unsigned d = (unsigned)((K - klo) >> bs);
                 unsigned pa[3], pv[3];
                 fixed_pieces(sa_[i], pa);
                 fixed_pieces(sv_[i], pv);
@@ -1648,17 +1891,44 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                         sc.rest_b = p.b;
                         sc.rest_c = p.c;
                         sc.rem_cnt = nl - (int)p.in_bin - (int)p.c;
-                        sc.prefix = (hi << width) | (unsigned long long)p.cand;
-                        if (p.in_bin == 1u || shift == 0) {
+                        const unsigned long long d_ = (unsigned long long)p.cand;
+                        sc.klo = klo + (d_ << bs);
+                        sc.khi = min(klo + span, klo + ((d_ + 1ull) << bs));
+                        sc.in_bin = (int)p.in_bin;
+                        if (p.in_bin == 1u || lev == kSearchLevels - 1) {
+                            // one key left (or, defensively, the whole bin at the last level)
                             sc.found = 1;
                             sc.kstar = sc.rem_cnt + (int)p.in_bin;
-                            sc.kkey = (sc.prefix << shift) | ((1ull << shift) - 1ull);
+                            sc.kkey = sc.khi - 1ull;
                         }
                     }
                 }
             }
             __syncthreads();
             if (sc.found) break;
+            if (sc.in_bin <= kSmallBin) {
+                // few keys left in the boundary bin: gather them, sort them and scan them directly
+                if (tid == 0) ncand = 0;
+                __syncthreads();
+                for (int i = tid; i < ns; i += T) {
+                    const unsigned long long K = search_key(skey[i], j0 + i);
+                    if (K < sc.klo || K >= sc.khi) continue;
+                    const int at = atomicAdd(&ncand, 1);
+                    unsigned pa[3], pv[3];
+                    fixed_pieces(sa_[i], pa);
+                    fixed_pieces(sv_[i], pv);
+                    bcand[at].key = K;
+                    bcand[at].a = (unsigned long long)pa[0] + ((unsigned long long)pa[1] << 14) +
+                                 ((unsigned long long)pa[2] << 28);
+                    bcand[at].v = (unsigned long long)pv[0] + ((unsigned long long)pv[1] << 14) +
+                                 ((unsigned long long)pv[2] << 28);
+                    bcand[at].b = fmax_bits(sb[i]);
+                }
+                cl.sync();
+                if (warp == 0) finish_small(cl, bcand, &ncand, bloc, sc, C, ldf, Df, inv_fa, inv_fv, a.eps_f);
+                __syncthreads();
+                break;
+            }
         }
         if (timer) R.sel_passes = passes;
     }
@@ -2208,7 +2478,7 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         VK_CUDA(cudaMemsetAsync(a.ebits, 0, sizeof(uint32_t) * rowsN * (a.ws_n / 32 + 1), st));
     }
     // one launch scores L (sketch tiles) and H (exact tiles past them)
-    const int h_tiles = (max_nh + kTile / (8 * G) - 1) / (kTile / (8 * G));
+    const int h_tiles = (max_nh + kHTilesPerBlock * (kTile / (8 * G)) - 1) / (kHTilesPerBlock * (kTile / (8 * G)));
     if (cfg.sketch == VERKV_SKETCH_INT8) {
         const int lt = (max_n + kTile * kInt8TokensPerThread<G> - 1) / (kTile * kInt8TokensPerThread<G>);
         score_int8_kernel<T, G><<<dim3(lt + h_tiles, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl, ctx.th, lt);
