@@ -46,6 +46,18 @@ def parse():
     return p.parse_args()
 
 
+def aggregate_ranks(step_ms, units_per_step, world, device):
+    """Replicas: every rank ran its own job; the slowest rank's step time counts (MAX over ranks) and
+    the value is the units of all ranks over that time.  Returns (value, step_ms)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(step_ms)], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    return world * units_per_step / (step_ms / 1e3), step_ms
+
+
 def workload(args, rank=0):
     from verified_kv_cache_gb300 import workloads
     return workloads.qwen_layer_case(seed=1 + 1000 * rank, n=args.n, steps=args.decode_steps, sketch=args.sketch)
@@ -210,12 +222,8 @@ def run_verkv(args):
     comp_ms = [a.elapsed_time(b) for k, a, b in events if k == "compress"]
     dec_ms = [a.elapsed_time(b) for k, a, b in events if k == "decode"]
     step_ms = (sum(comp_ms) + sum(dec_ms)) / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
     units_per_step = S * 1 * w.n_q * w.n        # scored tokens: every query head scores every token
-    value = world * units_per_step / (step_ms / 1e3)
+    value, step_ms = aggregate_ranks(step_ms, units_per_step, world, dev)
 
     # per-kernel shares and the dominant kernel
     agg = {}
