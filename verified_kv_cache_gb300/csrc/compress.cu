@@ -8,6 +8,8 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "async.cuh"
+#include "umma.cuh"
 
 namespace verkv {
 
@@ -111,6 +113,217 @@ __global__ void __launch_bounds__(256) tau_tile_kernel(const T* __restrict__ kv,
             tau_raw[(int64_t)h * n + t0 + tid] = best[tid];
             atomicMax(&tau_max[h], float_to_ordered(best[tid]));
         }
+    }
+}
+
+// --------------------------------------------------------------------------------------------
+// The same scores on the 5th-generation tensor cores, for bf16 keys and at most 128 observation rows
+// per KV head: the logits of a tile of 128 tokens are one 128 x 128 x 128 product, A = the head's
+// observation rows (fp32, split into three bf16 parts hi + mid + lo, which represent them to fp32
+// precision; the products with the bf16 keys are exact and accumulate in fp32) and B = the tile's
+// keys.  A stays in shared memory; key tiles arrive by cp.async into a two-stage ring in the
+// 128-byte-swizzled K-major layout; one thread issues the 24 MMAs of a tile into one of two tensor-
+// memory accumulators, so the next tile's MMAs overlap this tile's epilogue.  Epilogue: one thread
+// per observation row.  Pass 0 keeps its row's running max and sum of exp(logit - max) over the
+// block's tiles; pass 1 forms p = exp(logit - m) / Z and the max over rows of each token (a butterfly
+// transpose-reduce per warp, then over the four lane quarters).  Sixteen warps: four per lane
+// quarter of the accumulator, each on 32 of the tile's 128 columns.
+// --------------------------------------------------------------------------------------------
+constexpr int kTmmaN = 128;                       // tokens per tile
+constexpr int kTmmaTileBytes = 128 * kHeadDim * 2;  // one bf16 operand tile (32 KiB)
+constexpr int kTmmaStages = 3;                    // key tiles in flight
+constexpr size_t kTmmaSmem = (size_t)(3 + kTmmaStages) * kTmmaTileBytes + 1024;   // A x 3, B ring, alignment slack
+
+constexpr int kTmmaThreads = 512;   // 16 warps: 4 per tensor-memory lane quarter, 32 columns each
+
+template <int PASS>
+__global__ void __launch_bounds__(kTmmaThreads, 1) tau_mma_kernel(const __nv_bfloat16* __restrict__ kv, int n, int R,
+                                                                  int G, int W, const float* __restrict__ obs_q,
+                                                                  float scale, float2* __restrict__ part,
+                                                                  const float2* __restrict__ rowstat,
+                                                                  float* __restrict__ tau_raw, int* __restrict__ tau_max,
+                                                                  int* __restrict__ err)
+{
+    extern __shared__ unsigned char dsm_raw[];
+    __shared__ __align__(8) unsigned long long bar[2];
+    __shared__ unsigned tbase;
+    __shared__ float cmax[4][kTmmaN];        // pass 1: per lane quarter, max over its 32 rows of each column
+    __shared__ float2 rpart[4][128];         // pass 0: per column group, each row's (max, sum)
+    __shared__ float bred[kTmmaThreads / 32];
+    // operand tiles must start on 1024-byte boundaries of the shared window
+    unsigned char* dsm = dsm_raw + ((1024u - (umma_smem_u32(dsm_raw) & 1023u)) & 1023u);
+    unsigned char* sA = dsm;                        // three 32 KiB parts of A
+    unsigned char* sB = dsm + 3 * kTmmaTileBytes;   // kTmmaStages 32 KiB key stages
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int quarter = warp & 3, cgrp = warp >> 2;   // lane quarter (rows 32 q ..) and column group (32 cg ..)
+    const int row = 32 * quarter + lane;
+    const int h = blockIdx.y;
+    const int ntiles = (n + kTmmaN - 1) / kTmmaN;
+    const int per = (ntiles + gridDim.x - 1) / gridDim.x;
+    const int tb = min(ntiles, (int)blockIdx.x * per), nt = min(ntiles, tb + per) - tb;
+
+    // A: the observation rows of the head's query-head group, split into bf16 hi + mid + lo
+    for (int e = tid; e < 128 * kHeadDim; e += kTmmaThreads) {
+        const int r = e / kHeadDim, k = e % kHeadDim;
+        float v = 0.f;
+        if (r < R) v = obs_q[((int64_t)(h * G + r / W) * W + r % W) * kHeadDim + k];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const float r1 = __fsub_rn(v, __bfloat162float(hi));
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(r1, __bfloat162float(mid)));
+        const unsigned off = umma_sw128_offset(r, k, 128);
+        *reinterpret_cast<__nv_bfloat16*>(sA + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(sA + kTmmaTileBytes + off) = mid;
+        *reinterpret_cast<__nv_bfloat16*>(sA + 2 * kTmmaTileBytes + off) = lo;
+    }
+    // keys of local tile i into stage i % kTmmaStages (one copy group per call, possibly empty)
+    auto load_b = [&](int i) {
+        if (i < nt) {
+            const int tok0 = (tb + i) * kTmmaN;
+            unsigned char* dst = sB + (i % kTmmaStages) * kTmmaTileBytes;
+            for (int c = tid; c < kTmmaN * 16; c += kTmmaThreads) {
+                const int r = c >> 4, cc = c & 15, tok = tok0 + r;
+                const unsigned off = (unsigned)((cc >> 3) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + (((cc & 7) ^ (r & 7)) << 4));
+                if (tok < n) cp_async16(dst + off, kv + ((int64_t)h * n + tok) * 2 * kHeadDim + cc * 8);
+                else *reinterpret_cast<uint4*>(dst + off) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        cp_async_commit();
+    };
+    if (warp == 0) umma_alloc(&tbase, 256);
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int k = 0; k < kTmmaStages; ++k) load_b(k);
+    fence_proxy_async_smem();   // A (generic stores) -> tensor core
+    umma_fence_before();
+    __syncthreads();
+    umma_fence_after();
+    const unsigned tmem = tbase;
+    constexpr unsigned idesc = umma_idesc_bf16_f32(128, kTmmaN);
+    auto issue = [&](int i) {   // thread 0
+        const unsigned d = tmem + (unsigned)((i & 1) * kTmmaN);
+        const unsigned ab = umma_smem_u32(sA), bb = umma_smem_u32(sB + (i % kTmmaStages) * kTmmaTileBytes);
+#pragma unroll
+        for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                umma_bf16(d, umma_desc_sw128(ab + sp * kTmmaTileBytes + umma_kstep_offset(ks, 128)),
+                          umma_desc_sw128(bb + umma_kstep_offset(ks, kTmmaN)), idesc, sp > 0 || ks > 0);
+        umma_commit(&bar[i & 1]);
+    };
+    float m_run = -INFINITY, z_run = 0.f, best = 0.f;
+    float msub = 0.f, zinv = 1.f;
+    if (PASS == 1 && row < R) {
+        const float2 ms = rowstat[(int64_t)h * R + row];
+        msub = ms.x;
+        zinv = __fdiv_rn(1.0f, ms.y);
+    }
+    bool bad = false;
+    if (nt > 0) {
+        cp_async_wait<kTmmaStages - 1>();
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            umma_fence_after();
+            issue(0);
+        }
+    }
+    for (int i = 0; i < nt; ++i) {
+        if (i + 1 < nt) {
+            cp_async_wait<kTmmaStages - 2>();   // groups of tiles <= i + 1 are done
+            fence_proxy_async_smem();
+            umma_fence_before();
+            __syncthreads();   // tile i + 1 has landed; the epilogue of tile i - 1 is done with its accumulator
+            if (tid == 0) {
+                umma_fence_after();
+                issue(i + 1);
+            }
+        }
+        if (!mbar_wait(&bar[i & 1], (unsigned)((i >> 1) & 1), kWaitLimit)) bad = true;
+        umma_fence_after();
+        load_b(i + kTmmaStages);   // stage i % kTmmaStages is free once the MMAs of tile i are done
+        const int col0 = 32 * cgrp, tok0 = (tb + i) * kTmmaN + col0;
+        const unsigned acc = tmem + ((unsigned)(32 * quarter) << 16) + (unsigned)((i & 1) * kTmmaN + col0);
+        float v[32];
+        umma_ld16(acc, *reinterpret_cast<float(*)[16]>(v));
+        umma_ld16(acc + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+        if (PASS == 0) {
+            float cm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                v[j] = (row < R && tok0 + j < n) ? __fmul_rn(v[j], scale) : -INFINITY;
+                cm = fmaxf(cm, v[j]);
+            }
+            if (cm > -INFINITY) {
+                const float mn = fmaxf(m_run, cm);
+                float zs = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) zs += __expf(v[j] - mn);
+                z_run = z_run * __expf(m_run - mn) + zs;
+                m_run = mn;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const bool ok = row < R && tok0 + j < n;
+                v[j] = ok ? __expf(__fmul_rn(v[j], scale) - msub) * zinv : 0.f;
+            }
+            // butterfly transpose-reduce: lane l ends with the max over the warp's 32 rows of column col0 + l
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int j = 0; j < o; ++j) {
+                    const float send = upper ? v[j] : v[j + o];
+                    const float keep = upper ? v[j + o] : v[j];
+                    v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+                }
+            }
+            cmax[quarter][col0 + lane] = v[0];
+            __syncthreads();
+            if (tid < kTmmaN) {
+                const float p = fmaxf(fmaxf(cmax[0][tid], cmax[1][tid]), fmaxf(cmax[2][tid], cmax[3][tid]));
+                const int tok = (tb + i) * kTmmaN + tid;
+                if (tok < n) {
+                    tau_raw[(int64_t)h * n + tok] = p;
+                    best = fmaxf(best, p);
+                }
+            }
+            __syncthreads();   // cmax is rewritten by the next tile
+        }
+        umma_fence_before();
+    }
+    cp_async_wait<0>();
+    if (PASS == 0) {
+        rpart[cgrp][row] = make_float2(m_run, z_run);
+        __syncthreads();
+        if (tid < 128 && tid < R) {
+            // combine the four column groups of the row
+            float M = -INFINITY;
+            for (int c = 0; c < 4; ++c) M = fmaxf(M, rpart[c][tid].x);
+            float Z = 0.f;
+            if (M > -INFINITY)
+                for (int c = 0; c < 4; ++c)
+                    if (rpart[c][tid].x > -INFINITY) Z += rpart[c][tid].y * __expf(rpart[c][tid].x - M);
+            part[((int64_t)h * R + tid) * gridDim.x + blockIdx.x] = make_float2(M, Z);
+        }
+    } else {
+        best = warp_max(best);
+        if (lane == 0) bred[warp] = best;
+    }
+    if (bad) *(volatile int*)err = 1;
+    __syncthreads();
+    if (PASS == 1 && tid == 0) {
+        float b = 0.f;
+        for (int w = 0; w < kTmmaThreads / 32; ++w) b = fmaxf(b, bred[w]);
+        atomicMax(&tau_max[h], float_to_ordered(b));
+    }
+    if (warp == 0) {
+        umma_fence_after();
+        umma_dealloc(tmem, 256);
     }
 }
 
@@ -513,14 +726,36 @@ verkv_status run_scores(Ctx& ctx, Slot& s, const T* kv, int n, const float* obs_
         attr_done[sizeof(T) == 4] = true;
     }
     const float scale = (float)(1.0 / std::sqrt((double)kHeadDim));
-    dim3 gt(ntiles, Hkv);
-    tau_tile_kernel<T, 0><<<gt, 256, smem, st>>>(kv, n, R, ctx.G, W, obs_q, scale, part, nullptr, nullptr, nullptr);
-    VK_LAUNCHED("tau_tile");
     dim3 br(32, 8);
-    tau_rowstat_kernel<<<(Hkv * R + 7) / 8, br, 0, st>>>(part, ntiles, rowstat, Hkv * R);
-    VK_LAUNCHED("tau_rowstat");
-    tau_tile_kernel<T, 1><<<gt, 256, smem, st>>>(kv, n, R, ctx.G, W, obs_q, scale, nullptr, rowstat, tau_raw, tau_max);
-    VK_LAUNCHED("tau_tile");
+    if (sizeof(T) == 2 && R <= 128) {
+        // tensor cores: one block per SM, each over a run of 128-token tiles of one KV head
+        static bool mma_attr = false;
+        if (!mma_attr) {
+            VK_CUDA(cudaFuncSetAttribute(tau_mma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmmaSmem));
+            VK_CUDA(cudaFuncSetAttribute(tau_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmmaSmem));
+            mma_attr = true;
+        }
+        const int mtiles = (n + kTmmaN - 1) / kTmmaN;
+        const int cph = std::max(1, std::min(mtiles, (ctx.num_sms + Hkv - 1) / Hkv));
+        const dim3 gm(cph, Hkv);
+        const __nv_bfloat16* kvb = reinterpret_cast<const __nv_bfloat16*>(kv);
+        tau_mma_kernel<0><<<gm, kTmmaThreads, kTmmaSmem, st>>>(kvb, n, R, ctx.G, W, obs_q, scale, part, nullptr, nullptr, nullptr,
+                                                      ctx.d_err);
+        VK_LAUNCHED("tau_mma");
+        tau_rowstat_kernel<<<(Hkv * R + 7) / 8, br, 0, st>>>(part, cph, rowstat, Hkv * R);
+        VK_LAUNCHED("tau_rowstat");
+        tau_mma_kernel<1><<<gm, kTmmaThreads, kTmmaSmem, st>>>(kvb, n, R, ctx.G, W, obs_q, scale, nullptr, rowstat, tau_raw,
+                                                      tau_max, ctx.d_err);
+        VK_LAUNCHED("tau_mma");
+    } else {
+        dim3 gt(ntiles, Hkv);
+        tau_tile_kernel<T, 0><<<gt, 256, smem, st>>>(kv, n, R, ctx.G, W, obs_q, scale, part, nullptr, nullptr, nullptr);
+        VK_LAUNCHED("tau_tile");
+        tau_rowstat_kernel<<<(Hkv * R + 7) / 8, br, 0, st>>>(part, ntiles, rowstat, Hkv * R);
+        VK_LAUNCHED("tau_rowstat");
+        tau_tile_kernel<T, 1><<<gt, 256, smem, st>>>(kv, n, R, ctx.G, W, obs_q, scale, nullptr, rowstat, tau_raw, tau_max);
+        VK_LAUNCHED("tau_tile");
+    }
     tau_finish_kernel<<<g1, 256, 0, st>>>(s.tau, tau_raw, tau_max, n, cfg.n_sink, cfg.n_local);
     VK_LAUNCHED("tau_finish");
     VK_CUDA(cudaFreeAsync(part, st));
@@ -577,36 +812,50 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
     const int Hkv = cfg.n_kv_heads;
     const size_t hn = (size_t)Hkv * n;
     VK_CUDA(cudaStreamSynchronize(st));
-    free_slot(s);
+    // the per-token arrays are kept across calls while the context fits (head stride is always n)
+    if (n > s.cap_n) {
+        void* keep_res = s.kvres;
+        int64_t* keep_off = s.res_off;
+        const size_t keep_cap = s.cap_res;
+        s.kvres = nullptr;
+        s.res_off = nullptr;
+        free_slot(s);
+        s.kvres = keep_res;
+        s.res_off = keep_off;
+        s.cap_res = keep_cap;
+        const size_t hc = (size_t)Hkv * n;
+        VK_CUDA(cudaMalloc(&s.tau, sizeof(float) * hc));
+        VK_CUDA(cudaMalloc(&s.r, sizeof(float) * hc));
+        VK_CUDA(cudaMalloc(&s.flags, hc));
+        VK_CUDA(cudaMalloc(&s.lpos, sizeof(int32_t) * hc));
+        VK_CUDA(cudaMalloc(&s.ltok, sizeof(int32_t) * hc));
+        VK_CUDA(cudaMalloc(&s.rl, sizeof(float) * hc));
+        VK_CUDA(cudaMalloc(&s.lslot, sizeof(int32_t) * hc));
+        VK_CUDA(cudaMalloc(&s.lq, sizeof(float2) * hc));
+        VK_CUDA(cudaMalloc(&s.rtok, sizeof(int32_t) * hc));
+        VK_CUDA(cudaMalloc(&s.hslot, sizeof(int32_t) * hc));
+        VK_CUDA(cudaMalloc(&s.counts, sizeof(int32_t) * Hkv * 4));
+        VK_CUDA(cudaMalloc(&s.c, sizeof(double) * Hkv));
+        VK_CUDA(cudaMalloc(&s.capped, sizeof(int32_t) * (Hkv + 1)));
+        if (!s.res_off) VK_CUDA(cudaMalloc(&s.res_off, sizeof(int64_t) * (Hkv + 1)));
+        if (cfg.sketch == VERKV_SKETCH_INT8) {
+            VK_CUDA(cudaMalloc(&s.codes8, hc * kHeadDim));
+            VK_CUDA(cudaMalloc(&s.scale8, sizeof(float) * hc));
+        } else if (cfg.sketch == VERKV_SKETCH_2BIT) {
+            const size_t ng = (size_t)(n + cfg.sketch_group - 1) / cfg.sketch_group;
+            VK_CUDA(cudaMalloc(&s.codes2, sizeof(uint64_t) * hc));
+            VK_CUDA(cudaMalloc(&s.zero2, sizeof(__half) * Hkv * ng * (kHeadDim / 4)));
+            VK_CUDA(cudaMalloc(&s.scale2, sizeof(__half) * Hkv * ng * (kHeadDim / 4)));
+            VK_CUDA(cudaMalloc(&s.pairs, sizeof(int32_t) * Hkv * (kHeadDim / 8)));
+            VK_CUDA(cudaMalloc(&s.energy, sizeof(double) * Hkv * (kHeadDim / 2)));
+        } else {
+            VK_CUDA(cudaMalloc(&s.kexact, hc * kHeadDim * ctx.elt));
+        }
+        s.cap_n = n;
+    }
+    s.live = false;
     s.n = n;
     s.kv_host = kv_host;
-    VK_CUDA(cudaMalloc(&s.tau, sizeof(float) * hn));
-    VK_CUDA(cudaMalloc(&s.r, sizeof(float) * hn));
-    VK_CUDA(cudaMalloc(&s.flags, hn));
-    VK_CUDA(cudaMalloc(&s.lpos, sizeof(int32_t) * hn));
-    VK_CUDA(cudaMalloc(&s.ltok, sizeof(int32_t) * hn));
-    VK_CUDA(cudaMalloc(&s.rl, sizeof(float) * hn));
-    VK_CUDA(cudaMalloc(&s.lslot, sizeof(int32_t) * hn));
-    VK_CUDA(cudaMalloc(&s.lq, sizeof(float2) * hn));
-    VK_CUDA(cudaMalloc(&s.rtok, sizeof(int32_t) * hn));
-    VK_CUDA(cudaMalloc(&s.hslot, sizeof(int32_t) * hn));
-    VK_CUDA(cudaMalloc(&s.counts, sizeof(int32_t) * Hkv * 4));
-    VK_CUDA(cudaMalloc(&s.c, sizeof(double) * Hkv));
-    VK_CUDA(cudaMalloc(&s.capped, sizeof(int32_t) * (Hkv + 1)));
-    VK_CUDA(cudaMalloc(&s.res_off, sizeof(int64_t) * (Hkv + 1)));
-    if (cfg.sketch == VERKV_SKETCH_INT8) {
-        VK_CUDA(cudaMalloc(&s.codes8, hn * kHeadDim));
-        VK_CUDA(cudaMalloc(&s.scale8, sizeof(float) * hn));
-    } else if (cfg.sketch == VERKV_SKETCH_2BIT) {
-        const size_t ng = (size_t)(n + cfg.sketch_group - 1) / cfg.sketch_group;
-        VK_CUDA(cudaMalloc(&s.codes2, sizeof(uint64_t) * hn));
-        VK_CUDA(cudaMalloc(&s.zero2, sizeof(__half) * Hkv * ng * (kHeadDim / 4)));
-        VK_CUDA(cudaMalloc(&s.scale2, sizeof(__half) * Hkv * ng * (kHeadDim / 4)));
-        VK_CUDA(cudaMalloc(&s.pairs, sizeof(int32_t) * Hkv * (kHeadDim / 8)));
-        VK_CUDA(cudaMalloc(&s.energy, sizeof(double) * Hkv * (kHeadDim / 2)));
-    } else {
-        VK_CUDA(cudaMalloc(&s.kexact, hn * kHeadDim * ctx.elt));
-    }
     const void* kv = kv_dev ? kv_dev : kv_host;
     VK_TIMING_BEGIN();
     verkv_status rc;
@@ -648,7 +897,13 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
         max_res = std::max(max_res, hs.n_resident);
     }
     const size_t row_bytes = 2 * kHeadDim * ctx.elt;
-    VK_CUDA(cudaMalloc(&s.kvres, std::max<size_t>(1, (size_t)s.res_off_host[Hkv]) * row_bytes));
+    const size_t need_res = std::max<size_t>(1, (size_t)s.res_off_host[Hkv]);
+    if (need_res > s.cap_res) {
+        if (s.kvres) VK_CUDA(cudaFree(s.kvres));
+        s.kvres = nullptr;
+        s.cap_res = need_res + need_res / 8;   // room for the next sample of the same size
+        VK_CUDA(cudaMalloc(&s.kvres, s.cap_res * row_bytes));
+    }
     VK_CUDA(cudaMemcpyAsync(s.res_off, s.res_off_host.data(), sizeof(int64_t) * (Hkv + 1), cudaMemcpyHostToDevice, st));
     if (max_res > 0) {
         gather_resident_kernel<<<dim3((max_res + 7) / 8, Hkv), 256, 0, st>>>(

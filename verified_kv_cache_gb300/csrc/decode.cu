@@ -11,6 +11,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "async.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -42,16 +43,6 @@ struct DecodeArgs {
 __device__ __forceinline__ int row_of(int b, int hq, int Hq) { return b * Hq + hq; }
 
 // K/V row elements (bf16 or fp32) to fp32: eight channels from 16 (or 32) bytes, or a pair.
-// Asynchronous 16-byte copy global -> shared (L2 only), and its group commit / wait.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(dst)), "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
 template <typename T> struct RowCvt;
 template <> struct RowCvt<__nv_bfloat16> {
     // 8 channels from 16 bytes
@@ -2034,54 +2025,6 @@ constexpr int kAttnChunkBytes = 32768;
 constexpr int kAttnStages = 2;
 constexpr int kAttnThreads = 256;
 constexpr int kMaxSplit = 128;              // attention splits per KV head (partials merged per query row)
-constexpr unsigned kWaitLimit = 1u << 22;   // try_wait polls before a wait is declared failed
-
-__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(unsigned long long* bar, unsigned count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, unsigned bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Bounded wait for the phase with the given parity; false if it did not complete within the limit.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, unsigned limit)
-{
-    const unsigned addr = smem_u32(bar);
-    for (unsigned it = 0; it < limit; ++it) {
-        unsigned done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(addr), "r"(parity)
-            : "memory");
-        if (done) return true;
-    }
-    return false;
-}
-
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global memory into this
-// block's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 template <typename T, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
                                                             int32_t* __restrict__ ucount, int32_t* __restrict__ ulist,

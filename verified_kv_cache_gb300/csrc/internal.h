@@ -16,6 +16,8 @@ namespace verkv {
 struct Slot {
     bool live = false;
     int n = 0;
+    int cap_n = 0;              // token capacity of the per-token arrays (reused while n <= cap_n)
+    size_t cap_res = 0;         // resident rows kvres can hold
     const void* kv_host = nullptr;  // borrowed pinned [Hkv][n][2][d]
 
     float* tau = nullptr;       // [Hkv][n] importance scores after clamping / forcing
