@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
                                                            RowState* __restrict__ rows, float2* __restrict__ tl,
                                                            float2* __restrict__ th, int n_ltiles)
 {
+    pdl_trigger();   // the decision kernel may start its independent prologue
     if ((int)blockIdx.x >= n_ltiles) {
         score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
         return;
@@ -323,6 +324,7 @@ __global__ void __launch_bounds__(kTile) score_int8_kernel(Views views, const fl
                                                            RowState* __restrict__ rows, float2* __restrict__ tl,
                                                            float2* __restrict__ th, int n_ltiles)
 {
+    pdl_trigger();   // the decision kernel may start its independent prologue
     if ((int)blockIdx.x >= n_ltiles) {
         score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
         return;
@@ -434,6 +436,7 @@ __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const f
                                                             RowState* __restrict__ rows, float2* __restrict__ tl,
                                                             float2* __restrict__ th, int n_ltiles)
 {
+    pdl_trigger();   // the decision kernel may start its independent prologue
     if ((int)blockIdx.x >= n_ltiles) {
         score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
         return;
@@ -1338,6 +1341,8 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                                                                    int32_t* __restrict__ mark,
                                                                    int32_t* __restrict__ elist)
 {
+    pdl_trigger();   // the attention kernel may start its independent prologue
+    pdl_wait();      // the scoring kernel has completed (its logits, maxima and weight factors are visible)
     cg::cluster_group cl = cg::this_cluster();
     const int C = (int)cl.num_blocks();
     const int rank = (int)cl.block_rank();
@@ -1376,7 +1381,6 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const int nl = V.counts[kv * 4 + 1], nh = V.counts[kv * 4 + 0];
     const int S = (nl + C - 1) / C;
     const int j0 = min(nl, rank * S), j1 = min(nl, j0 + S), ns = j1 - j0;
-    const float m = untag_max(R.m_tag, (unsigned)a.gen);
     const float* rl = V.rl + (int64_t)kv * V.n;
     int parity = 0;
     const bool timer = rank == 0 && tid == 0;
@@ -1389,6 +1393,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         }
     };
 
+    float m;   // the row maximum of the logits
     // ---- phase 0: weights and the row totals; this row's exact-set bitmap (left by the previous
     // call for its attention) is cleared for phase 4
     {
@@ -1411,10 +1416,11 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + k * T;
-            tv[k] = i < ns ? tlr[i] : make_float2(0.f, 0.f);
             rv[k] = i < ns ? rlr[i] : 0.f;
             qv[k] = i < ns ? lqr[i] : make_float2(0.f, 0.f);
+            tv[k] = i < ns ? tlr[i] : make_float2(0.f, 0.f);
         }
+        m = untag_max(R.m_tag, (unsigned)a.gen);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + k * T;
@@ -2058,7 +2064,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     // ascending tokens.  Every block counts all the words (thread t a contiguous run); the positions
     // of its own share below are written, with the mask of the heads holding each token, into the
     // fetch list, which the chunk copies read back.  Block 0 writes the count.
+    // q slice of this thread (pre-scaled by 1/sqrt(d)), all G heads
+    const int sl = tid % NSL;
+    float qr[G][QS];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < QS; ++c) qr[g][c] = q[(int64_t)(row0 + g) * kHeadDim + sl * QS + c] * a.inv_sqrt_d_f;
+
     int nu;
+    pdl_wait();   // the decision kernel's bitmaps and weight factors are complete (the query is an input)
     {
         const int64_t stride = a.ws_n / 32 + 1;
         const uint32_t* eb = a.ebits + (int64_t)row0 * stride;
@@ -2125,14 +2140,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     const unsigned char* host = reinterpret_cast<const unsigned char*>(V.kv_host) + (int64_t)kv * V.n * ROWB;
     const int32_t* ul = ulw;
     const uint8_t* um = umw;
-
-    // q slice of this thread (pre-scaled by 1/sqrt(d)), all G heads
-    const int sl = tid % NSL;
-    float qr[G][QS];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int c = 0; c < QS; ++c) qr[g][c] = q[(int64_t)(row0 + g) * kHeadDim + sl * QS + c] * a.inv_sqrt_d_f;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
@@ -2441,13 +2448,15 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         lc.blockDim = dim3(kDecideThreads);
         lc.dynamicSmemBytes = kDecideSmem;
         lc.stream = st;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = C;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         lc.attrs = attr;
-        lc.numAttrs = 1;
+        lc.numAttrs = 2;
         VK_CUDA(cudaLaunchKernelEx(&lc, decide_kernel, views, a, ctx.rows, (const float2*)ctx.tl,
                                    (const float2*)ctx.th, ctx.wl, ctx.mark, ctx.elist));
         VK_LAUNCHED("decide");
@@ -2477,8 +2486,20 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
                                      kAttnStages * kAttnChunkBytes));
         attn_attr = true;
     }
-    attn_kernel<T, G><<<dim3(B * a.Hkv, a.nsplit), kAttnThreads, kAttnStages * kAttnChunkBytes, st>>>(
-        views, q, a, ctx.ucount, ctx.ulist, ctx.umask, ctx.part, a.done, out);
+    {
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(B * a.Hkv, a.nsplit);
+        lc.blockDim = dim3(kAttnThreads);
+        lc.dynamicSmemBytes = kAttnStages * kAttnChunkBytes;
+        lc.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        VK_CUDA(cudaLaunchKernelEx(&lc, attn_kernel<T, G>, views, q, a, ctx.ucount, ctx.ulist, ctx.umask, ctx.part,
+                                   a.done, out));
+    }
     VK_LAUNCHED("attn");
     return VERKV_OK;
 }
