@@ -3,7 +3,7 @@
 Plain double-precision CPU restatement of "Verify Before You Fetch: Reliable
 KV Cache Compression for LLM Inference" (PoissonComp: Algorithm 1, eq. (3);
 KVFetch: Algorithm 2, Definition 2 / eq. (5), Lemma 1 / eq. (7), eqs. (9)-(10);
-key sketch: Appendix A.1).  The arithmetic lives in ``verkv_oracle.c``; this
+binary shrinkage: Appendix A.2; key sketch: Appendix A.1).  The arithmetic lives in ``verkv_oracle.c``; this
 module compiles it with gcc and wraps it for numpy arrays.
 
 Only the tests, the package smoke check and the benchmark's CPU-baseline leg
@@ -78,8 +78,12 @@ def lib():
             L.vko_beta_breakpoints.restype = f64
             L.vko_kvfetch_row.argtypes = [i64, P, P, P, P, f64, f64, i32, P, P, P, P, P, P]
             L.vko_kvfetch_row.restype = i32
+            L.vko_kvfetch_row_ex.argtypes = [i64, P, P, P, P, f64, f64, i32, i32, P, P, P, P, P, P]
+            L.vko_kvfetch_row_ex.restype = i32
+            L.vko_binary_shrinkage.argtypes = [i64, P, P, P, P]
+            L.vko_binary_shrinkage.restype = f64
             L.vko_attention_row.argtypes = [i64, i32, P, P, P, P, P, P, P]
-            L.vko_kvfetch_rows.argtypes = [i64, i64, P, P, P, P, P, f64, f64, i32, P, P, i32]
+            L.vko_kvfetch_rows.argtypes = [i64, i64, P, P, P, P, P, f64, f64, i32, i32, P, P, i32]
             L.vko_kvfetch_rows.restype = i32
             L.vko_num_threads.restype = i32
         return _lib
@@ -211,8 +215,19 @@ def beta_breakpoints(w, r) -> float:
     return lib().vko_beta_breakpoints(w.shape[0], _p(w), _p(r))
 
 
-def kvfetch_row(flags, r32, t_exact, t_sketch, eps: float, delta: float, mode: int = 1):
-    """One query row of Algorithm 2.  Returns dict with cert scalars and arrays."""
+def binary_shrinkage(w, r):
+    """Appendix A.2: lambda_i in {1, r_i}.  Returns (lambda, beta, number set to r_i)."""
+    w = _c(w, np.float64)
+    r = _c(r, np.float64)
+    lam = np.zeros(w.shape[0], np.float64)
+    ns = ctypes.c_int64()
+    beta = lib().vko_binary_shrinkage(w.shape[0], _p(w), _p(r), _p(lam), ctypes.byref(ns))
+    return lam, beta, ns.value
+
+
+def kvfetch_row(flags, r32, t_exact, t_sketch, eps: float, delta: float, mode: int = 1, shrinkage: int = 0):
+    """One query row of Algorithm 2.  Returns dict with cert scalars and arrays.
+    shrinkage: 0 = the clipped coefficients of Definition 2, 1 = binary (Appendix A.2)."""
     flags = _c(flags, np.uint8)
     r32 = _c(r32, np.float32)
     te = _c(t_exact, np.float64)
@@ -225,8 +240,8 @@ def kvfetch_row(flags, r32, t_exact, t_sketch, eps: float, delta: float, mode: i
     order = np.zeros(max(n_l, 1), np.int64)
     mask = np.zeros(n, np.uint8)
     resid = np.full(n_l + 1, np.nan)
-    lib().vko_kvfetch_row(n, _p(flags), _p(r32), _p(te), _p(ts), float(eps), float(delta), int(mode),
-                          ctypes.byref(cert), _p(lam), _p(gain), _p(order), _p(mask), _p(resid))
+    lib().vko_kvfetch_row_ex(n, _p(flags), _p(r32), _p(te), _p(ts), float(eps), float(delta), int(mode),
+                             int(shrinkage), ctypes.byref(cert), _p(lam), _p(gain), _p(order), _p(mask), _p(resid))
     out = cert.as_dict()
     out.update(lam=lam, gain=gain, order=order[:n_l], exact_mask=mask.astype(bool), resid=resid)
     return out
@@ -245,7 +260,7 @@ def attention_row(flags, r32, t_exact, V, lam, exact_mask):
     return out
 
 
-def kvfetch_rows(flags, r32, kv_of, t_exact, t_sketch, eps, delta, mode=1, threads=0):
+def kvfetch_rows(flags, r32, kv_of, t_exact, t_sketch, eps, delta, mode=1, threads=0, shrinkage=0):
     """Many independent rows (OpenMP).  flags/r32: [Hkv, n]; t_*: [rows, n]."""
     flags = _c(flags, np.uint8)
     r32 = _c(r32, np.float32)
@@ -256,7 +271,7 @@ def kvfetch_rows(flags, r32, kv_of, t_exact, t_sketch, eps, delta, mode=1, threa
     certs = (Cert * rows)()
     masks = np.zeros((rows, n), np.uint8)
     lib().vko_kvfetch_rows(rows, n, _p(flags), _p(r32), _p(kv_of), _p(te), _p(ts), float(eps), float(delta),
-                           int(mode), certs, _p(masks), int(threads))
+                           int(mode), int(shrinkage), certs, _p(masks), int(threads))
     return [c.as_dict() for c in certs], masks.astype(bool)
 
 

@@ -5,7 +5,8 @@
  * "Verify Before You Fetch: Reliable KV Cache Compression for LLM Inference"
  * (PoissonComp, Algorithm 1 and Sec. 4.1, eq. (3); KVFetch, Algorithm 2 and
  * Sec. 4.2, Definition 2 / eq. (5), Theorem 1 / eq. (6), Lemma 1 / eq. (7),
- * eqs. (9)-(10), Theorem 2; key sketch, Appendix A.1).
+ * eqs. (9)-(10), Theorem 2; binary shrinkage, Appendix A.2; key sketch,
+ * Appendix A.1).
  *
  * Only the test-suite, the package smoke check and the CPU-baseline leg of
  * the benchmark may load this library.  It shares no code with the CUDA
@@ -124,7 +125,7 @@ void vko_tau(int64_t n, int d, const double* K, int rows, const double* Q,
 /* value is the stored inclusion probability and decides H = {r32 == 1}.     */
 /* Returns 0, or -1 when B' <= 0 (budget does not cover the forced set).    */
 /* ------------------------------------------------------------------------ */
-static const float* g_sort_tau;
+static _Thread_local const float* g_sort_tau;   /* per thread: rows run in parallel */
 static int cmp_tau_desc(const void* a, const void* b)
 {
     int64_t ia = *(const int64_t*)a, ib = *(const int64_t*)b;
@@ -443,6 +444,51 @@ double vko_beta_breakpoints(int64_t nl, const double* w, const double* r)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Binary shrinkage ("Verify Before You Fetch", App. A.2): every lambda_i is */
+/* one of the endpoints {1, r_i}.  Turning token i from 1 to r_i changes the */
+/* MSE of eq. (6) by w_i (1 - r_i) (2 beta - w_i (1 - r_i) / r_i), beta being */
+/* the bias already accumulated, so the tokens of L are visited by          */
+/* decreasing gamma_i = w_i (1 - r_i) / r_i (ties: lower L index first) and  */
+/* set to r_i while gamma_i > 2 beta; the others keep lambda = 1.  Writes    */
+/* lambda (length nl) and returns the final beta = sum of w_i (1 - r_i) over */
+/* the tokens set to r_i.                                                    */
+/* ------------------------------------------------------------------------ */
+static _Thread_local const double* g_sort_gam;
+static int cmp_gamma_desc(const void* a, const void* b)
+{
+    int64_t ia = *(const int64_t*)a, ib = *(const int64_t*)b;
+    double ga = g_sort_gam[ia], gb = g_sort_gam[ib];
+    if (ga > gb) return -1;
+    if (ga < gb) return 1;
+    return (ia < ib) ? -1 : (ia > ib);
+}
+
+double vko_binary_shrinkage(int64_t nl, const double* w, const double* r, double* lam, int64_t* n_shrunk)
+{
+    double* gam = (double*)malloc(sizeof(double) * (size_t)(nl + 1));
+    int64_t* ord = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nl + 1));
+    for (int64_t j = 0; j < nl; ++j) {
+        gam[j] = w[j] * (1.0 - r[j]) / r[j];
+        ord[j] = j;
+        lam[j] = 1.0;
+    }
+    g_sort_gam = gam;
+    qsort(ord, (size_t)nl, sizeof(int64_t), cmp_gamma_desc);
+    double beta = 0.0;
+    int64_t k = 0;
+    for (; k < nl; ++k) {
+        int64_t j = ord[k];
+        if (!(gam[j] > 2.0 * beta)) break;
+        lam[j] = r[j];
+        beta += w[j] * (1.0 - r[j]);
+    }
+    if (n_shrunk) *n_shrunk = k;
+    free(gam);
+    free(ord);
+    return beta;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Bernstein certificate (Lemma 1, eq. (7)) over a subset of L, with fixed  */
 /* per-token coefficients.  a_i = w_i (1 - lambda_i), v_i = lambda_i^2 w_i^2 */
 /* (1 - r_i) / r_i, b_i = lambda_i w_i / r_i * max(r_i, 1 - r_i).  Empty     */
@@ -468,8 +514,8 @@ typedef struct {
     int32_t pad;
 } vko_cert;
 
-static const double* g_sort_g;
-static const int64_t* g_sort_idx;
+static _Thread_local const double* g_sort_g;
+static _Thread_local const int64_t* g_sort_idx;
 static int cmp_gain(const void* a, const void* b)
 {
     int64_t ia = *(const int64_t*)a, ib = *(const int64_t*)b;
@@ -499,9 +545,22 @@ static int cmp_gain(const void* a, const void* b)
  *   resid[|L| + 1]        : eps^(L_g[k:]) for k = 0..|L| (from tail sums; for diagnostics).
  * Returns 0.
  */
+int vko_kvfetch_row_ex(int64_t n, const uint8_t* flags, const float* r32, const double* t_exact,
+                       const double* t_sketch, double eps, double delta, int mode, int shrinkage, vko_cert* cert,
+                       double* lambda, double* gain, int64_t* order, uint8_t* exact_mask, double* resid);
+
 int vko_kvfetch_row(int64_t n, const uint8_t* flags, const float* r32, const double* t_exact,
                     const double* t_sketch, double eps, double delta, int mode, vko_cert* cert,
                     double* lambda, double* gain, int64_t* order, uint8_t* exact_mask, double* resid)
+{
+    return vko_kvfetch_row_ex(n, flags, r32, t_exact, t_sketch, eps, delta, mode, 0, cert, lambda, gain, order,
+                              exact_mask, resid);
+}
+
+/* shrinkage: 0 = the clipped coefficients of Definition 2, 1 = binary (App. A.2). */
+int vko_kvfetch_row_ex(int64_t n, const uint8_t* flags, const float* r32, const double* t_exact,
+                       const double* t_sketch, double eps, double delta, int mode, int shrinkage, vko_cert* cert,
+                       double* lambda, double* gain, int64_t* order, uint8_t* exact_mask, double* resid)
 {
     int64_t nl = 0;
     double m = -INFINITY;
@@ -525,14 +584,21 @@ int vko_kvfetch_row(int64_t n, const uint8_t* flags, const float* r32, const dou
         }
     }
     const double ldelta = log(2.0 / delta);
-    double beta = vko_beta_breakpoints(nl, w, r);
+    double* lamb = (double*)malloc(sizeof(double) * (size_t)(nl + 1));
+    double beta;
+    if (shrinkage == 1) {
+        beta = vko_binary_shrinkage(nl, w, r, lamb, NULL);
+    } else {
+        beta = vko_beta_breakpoints(nl, w, r);
+        for (int64_t j = 0; j < nl; ++j) lamb[j] = lambda_of(beta, w[j], r[j]);
+    }
     double* a = (double*)malloc(sizeof(double) * (size_t)(nl + 1));
     double* v = (double*)malloc(sizeof(double) * (size_t)(nl + 1));
     double* bb = (double*)malloc(sizeof(double) * (size_t)(nl + 1));
     double sa = 0.0, sv = 0.0, bmax = 0.0;
     if (lambda) for (int64_t i = 0; i < n; ++i) lambda[i] = 0.0;
     for (int64_t j = 0; j < nl; ++j) {
-        double lam = lambda_of(beta, w[j], r[j]);
+        double lam = lamb[j];
         if (lambda) lambda[lidx[j]] = lam;
         a[j] = w[j] * (1.0 - lam);
         v[j] = lam * lam * w[j] * w[j] * (1.0 - r[j]) / r[j];
@@ -639,7 +705,7 @@ int vko_kvfetch_row(int64_t n, const uint8_t* flags, const float* r32, const dou
         cert->b = bmax; cert->eps_hat = eh; cert->n_l = nl; cert->kstar = kstar;
         cert->no_fetch = no_fetch; cert->pad = 0;
     }
-    free(ord); free(a); free(v); free(bb); free(lidx); free(w); free(r);
+    free(ord); free(a); free(v); free(bb); free(lidx); free(w); free(r); free(lamb);
     return 0;
 }
 
@@ -677,7 +743,7 @@ void vko_attention_row(int64_t n, int d, const uint8_t* flags, const float* r32,
 /* ------------------------------------------------------------------------ */
 int vko_kvfetch_rows(int64_t rows, int64_t n, const uint8_t* flags, const float* r32, const int32_t* kv_of,
                      const double* t_exact, const double* t_sketch, double eps, double delta, int mode,
-                     vko_cert* certs, uint8_t* exact_masks, int threads)
+                     int shrinkage, vko_cert* certs, uint8_t* exact_masks, int threads)
 {
 #ifdef _OPENMP
     if (threads > 0) omp_set_num_threads(threads);
@@ -685,8 +751,8 @@ int vko_kvfetch_rows(int64_t rows, int64_t n, const uint8_t* flags, const float*
 #endif
     for (int64_t u = 0; u < rows; ++u) {
         const int64_t kv = kv_of[u];
-        vko_kvfetch_row(n, flags + kv * n, r32 + kv * n, t_exact + u * n, t_sketch + u * n, eps, delta, mode,
-                        certs + u, NULL, NULL, NULL, exact_masks ? exact_masks + u * n : NULL, NULL);
+        vko_kvfetch_row_ex(n, flags + kv * n, r32 + kv * n, t_exact + u * n, t_sketch + u * n, eps, delta, mode,
+                           shrinkage, certs + u, NULL, NULL, NULL, exact_masks ? exact_masks + u * n : NULL, NULL);
     }
     return 0;
 }

@@ -385,6 +385,105 @@ def test_beta_breakpoints_vs_plain_bisection():
         assert math.isclose(beta, hi, rel_tol=1e-12)
 
 
+# ----------------------------------------------------------------------------- binary shrinkage (App. A.2)
+def _gamma_order(w, r):
+    """L by decreasing w (1 - r) / r, ties by lower index (the visiting order of App. A.2)."""
+    g = w * (1 - r) / r
+    return np.lexsort((np.arange(len(w)), -g))
+
+
+def test_binary_shrinkage_closed_forms():
+    """|L| = 1: the only token is shrunk (gamma > 0 = 2 beta), lambda = r, beta = w (1 - r),
+    the same as Definition 2.  m identical tokens: token k (0-based) is shrunk while
+    w (1 - r) / r > 2 k w (1 - r), i.e. 2 k r < 1, so min(m, ceil(1 / (2 r))) are shrunk."""
+    for w, r in [(1.0, 0.3), (5.0, 0.01), (1e-3, 0.9)]:
+        lam, beta, ns = oracle.binary_shrinkage([w], [r])
+        assert ns == 1 and lam[0] == r and math.isclose(beta, w * (1 - r), rel_tol=1e-15)
+    for m in [1, 2, 3, 10, 1000]:
+        for r in [0.03, 0.3, 0.7, 0.9]:
+            lam, beta, ns = oracle.binary_shrinkage(np.full(m, 2.5), np.full(m, r))
+            k0 = min(m, math.ceil(1 / (2 * r)))
+            assert ns == k0
+            assert np.array_equal(lam, np.where(np.arange(m) < k0, r, 1.0))   # ties: lower index first
+            assert math.isclose(beta, k0 * 2.5 * (1 - r), rel_tol=1e-12)
+    # a zero weight has gamma = 0, never above 2 beta >= 0
+    lam, beta, ns = oracle.binary_shrinkage([0.0, 0.0], [0.5, 0.2])
+    assert ns == 0 and beta == 0.0 and np.all(lam == 1.0)
+
+
+def test_binary_shrinkage_is_prefix_minimum_by_enumeration():
+    """App. A.2: switching token i from lambda = 1 to lambda = r_i changes the MSE by
+    w_i (1 - r_i) (2 beta - w_i (1 - r_i) / r_i), and the stop is the MSE minimum over all
+    prefixes of the order -- both checked against the MSE of every prefix computed by
+    enumerating all 2^|L| Poisson outcomes.  Theorem 1 places the continuous minimiser below it."""
+    rng = np.random.default_rng(81)
+    for trial in range(25):
+        L = int(rng.integers(1, 9))
+        w = np.exp(rng.standard_normal(L) * 2)
+        r = rng.uniform(0.02, 0.95, L)
+        if trial % 3 == 0:
+            r = rng.uniform(0.005, 0.06, L)   # small r: long prefixes
+        lam, beta, ns = oracle.binary_shrinkage(w, r)
+        order = _gamma_order(w, r)
+        mse = []
+        for k in range(L + 1):
+            lk = np.ones(L)
+            lk[order[:k]] = r[order[:k]]
+            mse.append(_mse_enumerated(w, r, lk))
+        for k in range(L):
+            i = order[k]
+            bk = (w[order[:k]] * (1 - r[order[:k]])).sum()
+            ai = w[i] * (1 - r[i])
+            assert math.isclose(mse[k + 1] - mse[k], ai * (2 * bk - ai / r[i]),
+                                rel_tol=1e-8, abs_tol=1e-10 * max(mse))
+        expect = np.ones(L)
+        expect[order[:ns]] = r[order[:ns]]
+        assert np.array_equal(lam, expect)
+        assert math.isclose(beta, (w * (1 - lam)).sum(), rel_tol=1e-12)
+        assert mse[ns] <= min(mse) * (1 + 1e-10)
+        cont = _lam(oracle.beta_breakpoints(w, r), w, r)
+        assert _mse_enumerated(w, r, cont) <= mse[ns] * (1 + 1e-10) <= mse[0] * (1 + 1e-10)
+
+
+def test_binary_shrinkage_certificate_coverage_and_fetch():
+    """Lemma 1 and Theorem 2 hold for any fixed lambda in [r, 1]: with the binary
+    coefficients, Pr(|D^ - D|/D > eps^(L)) <= delta and, after fetching L_g[:k*], the
+    (eps, delta) guarantee -- both exactly over all outcomes; brute-force and closed-form
+    gains and k* agree."""
+    rng = np.random.default_rng(82)
+    for trial in range(30):
+        L = int(rng.integers(1, 10))
+        flags, r32, t = _tiny_row(rng, L)
+        eps = float(rng.choice([0.01, 0.05, 0.2]))
+        delta = float(rng.choice([0.05, 0.1, 0.3]))
+        brute = oracle.kvfetch_row(flags, r32, t, t, eps, delta, mode=0, shrinkage=1)
+        fast = oracle.kvfetch_row(flags, r32, t, t, eps, delta, mode=1, shrinkage=1)
+        assert brute["kstar"] == fast["kstar"]
+        assert np.array_equal(brute["exact_mask"], fast["exact_mask"])
+        Lm = flags != 2
+        w = np.exp(t - fast["m"])
+        D = w.sum()
+        r = r32[Lm].astype(np.float64)
+        lam, beta, _ = oracle.binary_shrinkage(w[Lm], r)
+        assert np.array_equal(fast["lam"][Lm], lam)
+        assert math.isclose(fast["beta"], beta, rel_tol=1e-12, abs_tol=1e-300)
+        E = fast["exact_mask"]
+        idx = np.nonzero(Lm)[0]
+        fail_all = fail_fetch = 0.0
+        for z, p in _outcomes(r):
+            Z = np.zeros(len(flags))
+            Z[idx] = z
+            full = w[~Lm].sum() + (Z * fast["lam"] * w / r32)[Lm].sum()
+            if abs(full - D) / D > fast["eps_hat"]:
+                fail_all += p
+            keep = ~Lm | E
+            dhat = w[keep].sum() + (Z * fast["lam"] * w / r32)[Lm & ~E].sum()
+            if abs(dhat - D) / D > eps:
+                fail_fetch += p
+        assert fail_all <= delta + 1e-12
+        assert fail_fetch <= delta + 1e-12
+
+
 # ----------------------------------------------------------------------------- certificate / fetch (Lemma 1, Thm. 2)
 def _tiny_row(rng, L, H=2):
     n = L + H
