@@ -58,6 +58,15 @@ typedef enum {
     VERKV_SKETCH_2BIT = 2    /* Appendix A.1: d/8 rotate-half channel pairs, 2-bit, fp16 zero/scale per group */
 } verkv_sketch;
 
+/* The coefficients lambda_i of the shrinkage estimator. */
+typedef enum {
+    VERKV_SHRINK_CLIPPED = 0,  /* Definition 2: lambda_i = clip_[r_i,1](beta r_i / (w^_i (1 - r_i))) at the fixed
+                                  point beta = sum_L w^_i (1 - lambda_i), the unique MSE minimiser (Theorem 1) */
+    VERKV_SHRINK_BINARY = 1    /* Appendix A.2: lambda_i in {1, r_i}; L visited by decreasing
+                                  w^_i (1 - r_i) / r_i (ties: lower L index first), each token set to r_i while
+                                  that value exceeds twice the bias beta accumulated so far */
+} verkv_shrinkage;
+
 typedef enum {
     VERKV_DTYPE_BF16 = 0,
     VERKV_DTYPE_F32 = 1
@@ -75,7 +84,7 @@ typedef struct {
     int32_t n_local;       /* last tokens always kept (forced into H)                 */
     int32_t sketch_group;  /* 2-bit sketch: tokens per min/max group (128)            */
     int32_t topk_width;    /* per query row, gain candidates sorted on chip (4096)    */
-    int32_t pad0;
+    int32_t shrinkage;     /* verkv_shrinkage (0 = clipped, Definition 2)            */
     double eta;            /* kept fraction: expected |H u S| = eta * n (Alg. 1)      */
     uint64_t seed;         /* Philox4x32-10 key of the Poisson sample                 */
     verkv_sketch sketch;
@@ -110,12 +119,12 @@ typedef struct {
     int32_t beta_iters;    /* passes the beta solve took                                       */
     int32_t sel_passes;    /* radix-select passes of the on-chip ranking                       */
     uint32_t phase_ns[6];  /* on-chip decision: ns in weights, beta, eq. (7), gain keys, k* search, exact set */
-    int32_t pad;
+    int32_t n_shrunk;      /* VERKV_SHRINK_BINARY: tokens of L given lambda = r_i; 0 with clipped coefficients */
 } verkv_row_trace;
 
 /* Create a context for one GPU (the current device).  All slots empty.
  * EINVAL: bad sizes, n_q_heads not a multiple of n_kv_heads, eta outside
- * (0, 1]; EUNSUPPORTED: head_dim != 128 or GQA group > 8. */
+ * (0, 1], unknown shrinkage; EUNSUPPORTED: head_dim != 128 or GQA group > 8. */
 verkv_status verkv_create(const verkv_config* cfg, verkv_ctx** out);
 
 /* Free all device memory of the context.  Pending work on the streams the
@@ -166,8 +175,12 @@ verkv_status verkv_compress(verkv_ctx* ctx, int32_t layer, int32_t seq, int32_t 
  * ties by token index) and k* of eq. (10); the rows of L_g[:k*] \ S of every
  * query head of a KV head are fetched once (their union) from kv_host; the
  * output is o = N^/D^ with weight 1 on H and on L_g[:k*] and lambda_i / r_i
- * on the rest of S.  Asynchronous on `stream`: no host synchronisation.
- * EINVAL: bad eps/delta/B; ESTATE: a slot was not compressed.
+ * on the rest of S.  With cfg.shrinkage = VERKV_SHRINK_BINARY the fixed point is
+ * replaced by the binary coefficients of Appendix A.2 (beta is then their bias).
+ * Asynchronous on `stream`: no host synchronisation.
+ * EINVAL: bad eps/delta/B; ESTATE: a slot was not compressed; EUNSUPPORTED:
+ * binary shrinkage on a row whose |L| exceeds the on-chip decision (16 x 8192
+ * entries, or 8 x 8192 on a GPU without 16-block clusters).
  */
 verkv_status verkv_decode(verkv_ctx* ctx, int32_t layer, const int32_t* seq_ids, int32_t B, const float* q,
                           double eps, double delta, float* out, verkv_stream stream);

@@ -49,6 +49,7 @@ int main(void) {
   printf("verkv_row_trace %zu\n", sizeof(verkv_row_trace));
   F(verkv_config, eta) F(verkv_config, seed) F(verkv_config, sketch) F(verkv_config, kv_dtype)
   F(verkv_head_stats, n_resident) F(verkv_row_trace, eps_hat) F(verkv_row_trace, n_fetch)
+  F(verkv_config, shrinkage) F(verkv_row_trace, n_shrunk)
   return 0;
 }
 """
@@ -73,6 +74,8 @@ def test_ctypes_layouts_match_header():
     assert int(got["verkv_head_stats.n_resident"]) == binding.HeadStats.n_resident.offset
     assert int(got["verkv_row_trace.eps_hat"]) == binding.RowTrace.eps_hat.offset
     assert int(got["verkv_row_trace.n_fetch"]) == binding.RowTrace.n_fetch.offset
+    assert int(got["verkv_config.shrinkage"]) == binding.Config.shrinkage.offset
+    assert int(got["verkv_row_trace.n_shrunk"]) == binding.RowTrace.n_shrunk.offset
 
 
 def test_create_rejects_bad_configs_without_touching_the_gpu(lib):
@@ -83,4 +86,6 @@ def test_create_rejects_bad_configs_without_touching_the_gpu(lib):
     cfg = binding.Config(1, 1, 1, 8, 32, 64, 1024, 4, 64, 128, 4096, 0, 0.125, 0, 1, 0)   # head_dim 64
     assert lib.verkv_create(ctypes.byref(cfg), ctypes.byref(h)) == 5
     cfg = binding.Config(1, 1, 1, 8, 32, 128, 1024, 4, 64, 128, 4096, 0, 1.5, 0, 1, 0)    # eta > 1
+    assert lib.verkv_create(ctypes.byref(cfg), ctypes.byref(h)) == 1
+    cfg = binding.Config(1, 1, 1, 8, 32, 128, 1024, 4, 64, 128, 4096, 2, 0.125, 0, 1, 0)  # unknown shrinkage
     assert lib.verkv_create(ctypes.byref(cfg), ctypes.byref(h)) == 1

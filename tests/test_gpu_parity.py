@@ -103,14 +103,14 @@ def test_importance_scores_and_end_to_end_sample(case):
     ctx.close()
 
 
-def _decode_parity(w, gc, osl, eps, delta, steps=None, b=0, max_exempt_frac=0.05):
+def _decode_parity(w, gc, osl, eps, delta, steps=None, b=0, max_exempt_frac=0.05, shrinkage=0):
     steps = range(w.queries.shape[0]) if steps is None else steps
     ctx = gc.ctx
-    counts = {"ok": 0, "exempt-k": 0, "exempt-g": 0}
+    counts = {"ok": 0, "exempt-b": 0, "exempt-k": 0, "exempt-g": 0}
     for s in steps:
         out = gc.decode(w.queries[s], eps, delta)
         trace = ctx.decode_trace(w.batch * w.n_q)
-        rows, unions = oracle_decode(w, b, osl, w.queries[s, b], eps, delta)
+        rows, unions = oracle_decode(w, b, osl, w.queries[s, b], eps, delta, shrinkage=shrinkage)
         row_ok = []
         for hq in range(w.n_q):
             t = trace[b * w.n_q + hq]
@@ -137,6 +137,38 @@ def test_decode_parity(case):
     gc = GpuCase(w, ctx)
     tau, stats, osl = _compress_both(w, gc)
     _decode_parity(w, gc, osl, w.eps, w.delta)
+    ctx.close()
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_decode_parity_binary_shrinkage(case):
+    """Appendix A.2's binary coefficients (lambda in {1, r}): the shrunk prefix of the gamma order
+    (its length exact), beta, eps_hat, k*, the fetched set and the output against the oracle."""
+    w = CASES[case]()
+    ctx = make_lib_ctx(w, shrinkage="binary")
+    gc = GpuCase(w, ctx)
+    tau, stats, osl = _compress_both(w, gc)
+    counts = _decode_parity(w, gc, osl, w.eps, w.delta, shrinkage=1)
+    trace = ctx.decode_trace(w.batch * w.n_q)
+    assert any(t["n_shrunk"] >= 1 for t in trace), [t["n_shrunk"] for t in trace]
+    print(case, counts)
+    ctx.close()
+
+
+def test_binary_shrinkage_long_prefix_spans_search_levels():
+    """Small inclusion probabilities make the binary prefix long (about 1 / (2 r) entries of similar
+    gamma), so its end lies in a crowded bin and takes several search levels."""
+    w = small_case("int8", n=12000, steps=2, query_mode="random", eta=1 / 128)
+    w.queries *= 0.1   # flat weights
+    ctx = make_lib_ctx(w, shrinkage="binary")
+    gc = GpuCase(w, ctx)
+    tau = np.full((w.n_kv, w.n), 0.5, np.float32)
+    tau[:, ::7] = 0.45
+    tau, stats, osl = _compress_both(w, gc, tau=tau)
+    gc.decode(w.queries[0], 0.05, 0.05)
+    trace = ctx.decode_trace(w.n_q)
+    assert max(t["n_shrunk"] for t in trace) > 64, [t["n_shrunk"] for t in trace]
+    _decode_parity(w, gc, osl, 0.05, 0.05, shrinkage=1)
     ctx.close()
 
 
@@ -263,6 +295,17 @@ def test_decode_before_compress_and_bad_arguments_are_rejected():
         with pytest.raises(binding.VerkvError) as e:
             ctx.decode(0, [0], q, eps, delta, out)
         assert e.value.status == 1
+    ctx.close()
+
+
+def test_qwen_layer_full_size_binary_shrinkage():
+    """The Qwen3-4B-shaped 32K-token layer with the 2-bit sketch and binary coefficients."""
+    w = workloads.qwen_layer_case(sketch="2bit", steps=2)
+    ctx = make_lib_ctx(w, shrinkage="binary")
+    gc = GpuCase(w, ctx)
+    tau, stats, osl = _compress_both(w, gc)
+    counts = _decode_parity(w, gc, osl, w.eps, w.delta, steps=range(2), shrinkage=1)
+    print(counts)
     ctx.close()
 
 

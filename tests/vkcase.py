@@ -13,6 +13,7 @@ from verified_kv_cache_gb300 import workloads
 
 G_GAP = 1e-6      # fetched-set exemption: oracle gains closer than this (relative) at the k* boundary
 K_GAP = 1e-6      # k* exemption: residual certificate within this (relative) of eps
+B_GAP = 1e-6      # binary shrinkage: the oracle's stop test gamma > 2 beta within this (relative) of equality
 REL_SCALAR = 1e-4 # c, beta, eps_hat
 REL_OUT = 2e-3    # attention output, relative L2
 # fp32 weights w^ = exp(t - m) underflow below 2^-126 of the row maximum; scale-free scalars (eps_hat,
@@ -69,8 +70,9 @@ def oracle_sketch_logits(w, b, h, q, slot: OracleSlot):
     return oracle.logits_2bit(q, pairs, codes, zero, scale)
 
 
-def oracle_decode(w, b, slot: OracleSlot, q_bh: np.ndarray, eps, delta, mode=1):
-    """q_bh: [Hq, d] for sequence b.  Returns per row dicts and per KV head fetch unions and outputs."""
+def oracle_decode(w, b, slot: OracleSlot, q_bh: np.ndarray, eps, delta, mode=1, shrinkage=0):
+    """q_bh: [Hq, d] for sequence b.  Returns per row dicts and per KV head fetch unions and outputs.
+    shrinkage: 0 = clipped coefficients (Definition 2), 1 = binary (Appendix A.2)."""
     G = w.group
     rows = []
     for hq in range(w.n_q):
@@ -78,7 +80,12 @@ def oracle_decode(w, b, slot: OracleSlot, q_bh: np.ndarray, eps, delta, mode=1):
         q = q_bh[hq].astype(np.float64)
         te = oracle.logits_exact(q, w.K[b, h])
         ts = oracle_sketch_logits(w, b, h, q, slot)
-        res = oracle.kvfetch_row(slot.flags[h], slot.r32[h], te, ts, eps, delta, mode=mode)
+        res = oracle.kvfetch_row(slot.flags[h], slot.r32[h], te, ts, eps, delta, mode=mode, shrinkage=shrinkage)
+        if shrinkage == 1:
+            Lm = slot.flags[h] != 2
+            res["w_l"] = np.exp(ts[Lm] - res["m"])
+            res["r_l"] = slot.r32[h][Lm].astype(np.float64)
+            res["n_shrunk"] = int((res["lam"][Lm] < 1.0).sum())
         res["out"] = oracle.attention_row(slot.flags[h], slot.r32[h], te, w.V[b, h], res["lam"], res["exact_mask"])
         rows.append(res)
     unions = []
@@ -133,12 +140,12 @@ class GpuCase:
         return out.cpu().numpy()
 
 
-def make_lib_ctx(w, n_layers=1, n_seqs=None, max_batch=None, max_tokens=None):
+def make_lib_ctx(w, n_layers=1, n_seqs=None, max_batch=None, max_tokens=None, shrinkage="clipped"):
     from verified_kv_cache_gb300 import binding
     return binding.VerKV(n_kv_heads=w.n_kv, n_q_heads=w.n_q, max_tokens=max_tokens or w.n, head_dim=w.d,
                          n_layers=n_layers, n_seqs=n_seqs or w.batch, max_batch=max_batch or w.batch,
                          n_sink=w.n_sink, n_local=w.n_local, eta=w.eta, seed=w.seed, sketch=w.sketch,
-                         kv_dtype=w.kv_dtype)
+                         kv_dtype=w.kv_dtype, shrinkage=shrinkage)
 
 
 # ----------------------------------------------------------------------------- comparisons
@@ -150,8 +157,43 @@ def close(a, b, rtol=REL_SCALAR, atol=ABS_FLOOR):
     return abs(a - b) <= rtol * abs(b) + atol
 
 
+def _gamma_order(orow):
+    w, r = orow["w_l"], orow["r_l"]
+    g = w * (1 - r) / r
+    return w, r, g, np.lexsort((np.arange(len(g)), -g))
+
+
+def binary_boundary_is_near_tie(orow, k_a, k_b):
+    """Binary shrinkage: the device shrank k_a entries of the gamma order, the oracle k_b.  Exempt
+    when the oracle's own test gamma_(k) > 2 beta_k sits within B_GAP (relative) of equality at every
+    position between the two."""
+    w, r, g, order = _gamma_order(orow)
+    pre = np.concatenate([[0.0], np.cumsum((w * (1 - r))[order])])
+    for k in range(min(k_a, k_b), max(k_a, k_b) + 1):
+        if k >= len(g):
+            continue
+        gk = g[order[k]]
+        if abs(gk - 2 * pre[k]) > B_GAP * gk:
+            return False
+    return True
+
+
+def binary_boundary_underflows(orow, k_a, k_b):
+    """The entries between the two prefix ends have weights below ABS_FLOOR of D: they are zero in the
+    device's fp32 weights (which never shrinks an entry of weight 0) and move no checked quantity."""
+    w, r, g, order = _gamma_order(orow)
+    between = order[min(k_a, k_b):max(k_a, k_b)]
+    return bool(np.all(w[between] <= ABS_FLOOR * orow["D"]))
+
+
 def check_row(gpu_trace, gpu_set, orow, eps, flags_h):
-    """Compare one query row.  Returns 'ok', 'exempt-k' or 'exempt-g'; raises on a real mismatch."""
+    """Compare one query row.  Returns 'ok', 'exempt-b', 'exempt-k' or 'exempt-g'; raises on a real
+    mismatch."""
+    if "n_shrunk" in orow and gpu_trace["n_shrunk"] != orow["n_shrunk"]:
+        kg, ko = gpu_trace["n_shrunk"], orow["n_shrunk"]
+        if not binary_boundary_underflows(orow, kg, ko):
+            assert binary_boundary_is_near_tie(orow, kg, ko), ("binary shrinkage prefix differs", kg, ko)
+            return "exempt-b"
     assert close(gpu_trace["eps_hat"], orow["eps_hat"]), (gpu_trace["eps_hat"], orow["eps_hat"])
     assert close(gpu_trace["beta"] / gpu_trace["D"], orow["beta"] / orow["D"]), (gpu_trace, orow["beta"], orow["D"])
     nf_o = bool(orow["no_fetch"])

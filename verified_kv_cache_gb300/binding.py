@@ -16,6 +16,7 @@ HEADER = os.path.join(_build.ROOT, "include", "verkv.h")
 
 SKETCH = {"exact": 0, "int8": 1, "2bit": 2}
 DTYPE = {"bf16": 0, "f32": 1}
+SHRINKAGE = {"clipped": 0, "binary": 1}
 STATUS = {0: "VERKV_OK", 1: "VERKV_EINVAL", 2: "VERKV_ENOMEM", 3: "VERKV_ECUDA", 4: "VERKV_ETIMEOUT",
           5: "VERKV_EUNSUPPORTED", 6: "VERKV_ESTATE"}
 
@@ -30,7 +31,7 @@ class Config(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_seqs", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("max_tokens", ctypes.c_int32), ("n_sink", ctypes.c_int32), ("n_local", ctypes.c_int32),
-                ("sketch_group", ctypes.c_int32), ("topk_width", ctypes.c_int32), ("pad0", ctypes.c_int32),
+                ("sketch_group", ctypes.c_int32), ("topk_width", ctypes.c_int32), ("shrinkage", ctypes.c_int32),
                 ("eta", ctypes.c_double), ("seed", ctypes.c_uint64), ("sketch", ctypes.c_int),
                 ("kv_dtype", ctypes.c_int)]
 
@@ -50,10 +51,10 @@ class RowTrace(ctypes.Structure):
                 ("eps_hat", ctypes.c_double), ("n_l", ctypes.c_int32), ("kstar", ctypes.c_int32),
                 ("no_fetch", ctypes.c_int32), ("fallback", ctypes.c_int32), ("n_fetch", ctypes.c_int32),
                 ("beta_iters", ctypes.c_int32), ("sel_passes", ctypes.c_int32), ("phase_ns", ctypes.c_uint32 * 6),
-                ("pad", ctypes.c_int32)]
+                ("n_shrunk", ctypes.c_int32)]
 
     def as_dict(self):
-        d = {k: getattr(self, k) for k, _ in self._fields_ if k not in ("pad", "phase_ns")}
+        d = {k: getattr(self, k) for k, _ in self._fields_ if k != "phase_ns"}
         d["phase_ns"] = list(self.phase_ns)
         return d
 
@@ -142,9 +143,10 @@ class VerKV:
 
     def __init__(self, *, n_kv_heads, n_q_heads, max_tokens, head_dim=128, n_layers=1, n_seqs=1, max_batch=1,
                  n_sink=4, n_local=128, eta=1 / 16, seed=0, sketch="int8", kv_dtype="bf16", sketch_group=128,
-                 topk_width=4096):
+                 topk_width=4096, shrinkage="clipped"):
         self.cfg = Config(n_layers, n_seqs, max_batch, n_kv_heads, n_q_heads, head_dim, max_tokens, n_sink, n_local,
-                          sketch_group, topk_width, 0, float(eta), int(seed), SKETCH[sketch], DTYPE[kv_dtype])
+                          sketch_group, topk_width, SHRINKAGE[shrinkage], float(eta), int(seed), SKETCH[sketch],
+                          DTYPE[kv_dtype])
         self.sketch = sketch
         self.kv_dtype = kv_dtype
         h = ctypes.c_void_p()

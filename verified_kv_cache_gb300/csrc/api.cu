@@ -122,7 +122,8 @@ verkv_status verkv_create(const verkv_config* cfg, verkv_ctx** out)
     if (c.n_layers <= 0 || c.n_seqs <= 0 || c.max_batch <= 0 || c.n_kv_heads <= 0 || c.n_q_heads <= 0 ||
         c.max_tokens <= 0 || c.n_sink < 0 || c.n_local < 0 || c.n_q_heads % c.n_kv_heads != 0 ||
         !(c.eta > 0.0 && c.eta <= 1.0) || (c.kv_dtype != VERKV_DTYPE_BF16 && c.kv_dtype != VERKV_DTYPE_F32) ||
-        (c.sketch != VERKV_SKETCH_EXACT && c.sketch != VERKV_SKETCH_INT8 && c.sketch != VERKV_SKETCH_2BIT))
+        (c.sketch != VERKV_SKETCH_EXACT && c.sketch != VERKV_SKETCH_INT8 && c.sketch != VERKV_SKETCH_2BIT) ||
+        (c.shrinkage != VERKV_SHRINK_CLIPPED && c.shrinkage != VERKV_SHRINK_BINARY))
         st = fail(ctx, VERKV_EINVAL, "invalid configuration");
     else if (c.head_dim != kHeadDim)
         st = fail(ctx, VERKV_EUNSUPPORTED, "only head_dim 128 is built");
@@ -318,6 +319,7 @@ verkv_status verkv_get_decode_trace(verkv_ctx* h, verkv_row_trace* out, int32_t 
         t.beta_iters = s.beta_iters;
         t.sel_passes = s.sel_passes;
         for (int k = 0; k < 6; ++k) t.phase_ns[k] = s.phase_ns[k];
+        t.n_shrunk = s.n_shrunk;
     }
     return VERKV_OK;
 }

@@ -33,6 +33,7 @@ struct DecodeArgs {
     int* err;         // mapped host word, set when a bounded device-side wait gives up
     int* done;        // [B Hkv] attention blocks finished per KV head (the last one merges; left at 0)
     int Hkv, Hq, G, ws_n, ws_npow2, gen, nsplit;
+    int binary;       // 1: binary shrinkage coefficients (lambda in {1, r}), 0: the clipped fixed point
     float eps_f;
     double eps, ldelta;
     ff eps_ff, ld_ff;   // eps and log(2/delta) as float-float
@@ -633,6 +634,7 @@ __global__ void __launch_bounds__(1024) beta_kernel(Views views, DecodeArgs a, R
         const double eh = nl > 0 ? (SA + t + sqrt(t * t + 2.0 * SV * ld)) / R.D : 0.0;
         R.beta = beta;
         R.beta_f = bf;
+        R.n_shrunk = 0;
         R.sum_a = SA;
         R.V = SV;
         R.b1 = nl > 0 ? B1 : 0.0;
@@ -1193,7 +1195,15 @@ struct DecideScalars {
     unsigned int rest_b, rest_c;        // max b over them (ordered float bits), their count
     int kstar, found, in_bin;
     unsigned long long kkey;            // the k*-th smallest key
+    // binary shrinkage: entries whose gamma key is below bin_kb get lambda = r; alpha enters the
+    // fixed-point sums as alpha * fs1 * fs2 (below 2^40)
+    unsigned long long bin_kb;
+    int n_shrunk;
+    float fs1, fs2;
 };
+
+// Key of gamma >= 0 in the binary-shrinkage order: ~bits(gamma) without the sign bit (gamma descending).
+__device__ __forceinline__ unsigned gamma_key32(float ga) { return ~__float_as_uint(ga) & 0x7fffffffu; }
 
 // A key of the boundary bin with its exact fixed-point a, v and b (ordered bits).
 struct SmallCand {
@@ -1333,6 +1343,79 @@ __device__ __forceinline__ void finish_small(cg::cluster_group& cl, const SmallC
     }
 }
 
+// Finish of the binary-shrinkage search when the bin holding the end of the shrunk prefix has at most
+// kSmallBin entries (warp 0 of every CTA, all with the same answer): the bin's entries, gathered from
+// every CTA, are placed by rank (the keys are distinct); entry i passes when its gamma exceeds twice
+// the bias before it (the prefix up to the bin, sc.rest_a, plus the exact fixed-point sum of alpha over
+// the bin's entries before i).  The first entry of the bin passes by construction; the prefix ends at
+// the first entry that fails, or with the bin.  SmallCand carries (key, fixed-point alpha, -, gamma bits).
+__device__ __forceinline__ void finish_binary(cg::cluster_group& cl, const SmallCand* cand, const int* ncand,
+                                              SmallCand* loc, DecideScalars& sc, int C, float fs1, float fs2)
+{
+    const int lane = threadIdx.x & 31;
+    const int cnt = lane < C ? *cl.map_shared_rank(ncand, lane) : 0;
+    int incl = cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int ntot = __shfl_sync(0xffffffffu, incl, 31);
+    SmallCand mine[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = lane + 32 * h;
+        int rk = 0, off = 0;
+        for (int r = 0; r < C; ++r) {
+            const int ex = __shfl_sync(0xffffffffu, incl - cnt, r);
+            if (e >= ex) { rk = r; off = ex; }
+        }
+        mine[h] = SmallCand{~0ull, 0ull, 0ull, 0u, 0u};
+        if (e < ntot) mine[h] = cl.map_shared_rank(cand, rk)[e - off];
+    }
+    __shared__ unsigned long long bkeys_[kSmallBin];
+    bkeys_[lane] = mine[0].key;
+    bkeys_[lane + 32] = mine[1].key;
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (lane + 32 * h >= ntot) continue;
+        int rnk = 0;
+        for (int q = 0; q < ntot; ++q) rnk += bkeys_[q] < mine[h].key;
+        loc[rnk] = mine[h];
+    }
+    __syncwarp();
+    unsigned long long av[2];
+    float gv[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        av[h] = i < ntot ? loc[i].a : 0ull;
+        gv[h] = i < ntot ? __uint_as_float(loc[i].b) : 0.f;
+    }
+    // exclusive prefix of alpha over the bin's entries in key order
+    unsigned long long x0 = av[0], x1 = av[1];
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y0 = __shfl_up_sync(0xffffffffu, x0, o), y1 = __shfl_up_sync(0xffffffffu, x1, o);
+        if (lane >= o) { x0 += y0; x1 += y1; }
+    }
+    const unsigned long long tot0 = __shfl_sync(0xffffffffu, x0, 31);
+    const unsigned long long ex[2] = {sc.rest_a + x0 - av[0], sc.rest_a + tot0 + x1 - av[1]};
+    int first_fail = 0x7fffffff;
+#pragma unroll
+    for (int h = 1; h >= 0; --h) {
+        const int i = lane + 32 * h;
+        if (i < ntot && !(__fmul_rn(__fmul_rn(gv[h], fs1), fs2) > 2.0f * (float)ex[h])) first_fail = i;
+    }
+    first_fail = __reduce_min_sync(0xffffffffu, first_fail);
+    if (lane == 0) {
+        const int p = first_fail == 0x7fffffff ? ntot : first_fail;
+        sc.found = 1;
+        sc.n_shrunk = sc.rem_cnt + p;
+        sc.bin_kb = p < ntot ? loc[p].key : sc.khi;
+    }
+}
+
+template <bool BINARY>
 __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, DecodeArgs a,
                                                                    RowState* __restrict__ rows,
                                                                    const float2* __restrict__ tl,
@@ -1477,8 +1560,212 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     __syncthreads();
     stamp(0);
 
-    // ---- phase 1: beta (Newton on the classes; thread 0 does the scalar update)
     int iters = 0;
+    if (BINARY) {
+        // ---- phase 1, binary shrinkage (Appendix A.2): in the order of decreasing gamma = w^ (1 - r) / r
+        // (ties: lower L index), each entry gets lambda = r while its gamma exceeds twice the bias (sum
+        // of alpha = w^ (1 - r)) of the entries before it.  Along the order gamma falls and the bias
+        // grows, so the passing entries form a prefix.  Its end is searched like k* below, over the
+        // gamma keys: per level a cluster-wide histogram of counts, exact fixed-point sums of alpha and
+        // the largest gamma of every bin gives the test of each bin's first entry from the bias before
+        // the bin; the last bin whose first entry passes holds the end (entries of gamma 0 never pass
+        // and stay out).
+        unsigned kmin = 0xffffffffu, kmax = 0u;
+        for (int i = tid; i < ns; i += T) {
+            const float ga = sg[i];
+            if (!(ga > 0.f)) continue;
+            const unsigned k32 = gamma_key32(ga);
+            kmin = min(kmin, k32);
+            kmax = max(kmax, k32);
+        }
+        kmin = __reduce_min_sync(0xffffffffu, kmin);
+        kmax = __reduce_max_sync(0xffffffffu, kmax);
+        if (lane == 0) {
+            sext[warp][0] = kmin;
+            sext[warp][1] = kmax;
+        }
+        uint4* hist4 = reinterpret_cast<uint4*>(hist);
+        for (int k = tid; k < kSearchFields * kSearchBins / 4; k += T) hist4[k] = make_uint4(0u, 0u, 0u, 0u);
+        __syncthreads();
+        if (warp == 0) {
+            kmin = __reduce_min_sync(0xffffffffu, sext[lane][0]);
+            kmax = __reduce_max_sync(0xffffffffu, sext[lane][1]);
+            if (lane == 0) {
+                slot[parity].i[0] = (int)kmin;
+                slot[parity].i[1] = (int)kmax;
+            }
+        }
+        cl.sync();   // every CTA's key range is published and every histogram is zero
+        if (warp == 0) {
+            const DecideSlot* rs = lane < C ? cl.map_shared_rank(slot, lane) + parity : nullptr;
+            const unsigned mn = __reduce_min_sync(0xffffffffu, rs ? (unsigned)rs->i[0] : 0xffffffffu);
+            const unsigned mx = __reduce_max_sync(0xffffffffu, rs ? (unsigned)rs->i[1] : 0u);
+            if (lane == 0) {
+                sc.done = 1;
+                sc.rest_a = 0ull;
+                sc.rem_cnt = 0;
+                sc.in_bin = 0;
+                sc.n_shrunk = 0;
+                sc.bin_kb = 0ull;
+                sc.fs1 = sc.fs2 = 1.0f;
+                if (mn <= mx) {
+                    sc.found = 0;
+                    sc.klo = (unsigned long long)mn << (kKeyBits - 31);
+                    sc.khi = ((unsigned long long)mx + 1ull) << (kKeyBits - 31);
+                    // the largest gamma is below 2^E; alpha <= gamma is scaled by 2^(40 - E), split in two
+                    // powers of two that are normal floats
+                    const int E = (int)((0x7fffffffu - mn) >> 23) - 126;
+                    const int k = 40 - E, k1 = k / 2, k2 = k - k1;
+                    sc.fs1 = __int_as_float((127 + k1) << 23);
+                    sc.fs2 = __int_as_float((127 + k2) << 23);
+                } else {
+                    sc.found = 1;   // no entry of positive gamma: nothing is shrunk
+                }
+            }
+        }
+        __syncthreads();
+        parity ^= 1;
+        const float fs1 = sc.fs1, fs2 = sc.fs2;
+        const SearchAcc zero = {0ull, 0ull, 0u, 0u};
+        for (int lev = 0; lev < kSearchLevels && !sc.found; ++lev) {
+            ++iters;
+            const int nb = kSearchBins;
+            const int sl = nb / C;
+            const unsigned long long klo = sc.klo, span = sc.khi - sc.klo;
+            const int bs = max(0, (64 - __clzll((long long)(span - 1ull))) - kSearchBits);
+            for (int i = tid; i < ns; i += T) {
+                const float ga = sg[i];
+                if (!(ga > 0.f)) continue;
+                const unsigned long long K = search_key(gamma_key32(ga), j0 + i);
+                if (K < klo || K - klo >= span) continue;
+                const unsigned d = (unsigned)((K - klo) >> bs);
+                unsigned pa[3];
+                fixed_pieces(__fmul_rn(__fmul_rn(sr[i], fs1), fs2), pa);
+                atomicAdd(&hist[d], 1u);
+                atomicMax(&hist[kSearchBins + d], __float_as_uint(ga));
+#pragma unroll
+                for (int q = 0; q < 3; ++q) atomicAdd(&hist[(2 + q) * kSearchBins + d], pa[q]);
+            }
+            __syncthreads();
+            if (C > 1) {
+                for (int d = tid; d < nb; d += T) {
+                    const int ow = d / sl;
+                    const unsigned cnt = hist[d];
+                    if (ow == rank || cnt == 0u) continue;
+                    unsigned* dst = cl.map_shared_rank(hist, ow);
+                    atomicAdd(dst + d, cnt);
+                    atomicMax(dst + kSearchBins + d, hist[kSearchBins + d]);
+#pragma unroll
+                    for (int f = 2; f < 5; ++f) atomicAdd(dst + f * kSearchBins + d, hist[f * kSearchBins + d]);
+                }
+                cl.sync();
+            }
+            // the cluster totals of this CTA's slice, two bins per thread in reverse order (thread t
+            // holds bins dA = rank sl + sl - 2 - 2t and dA + 1), so the threads above t hold the bins
+            // before dA and the block's exclusive suffix is the prefix over bins
+            const int dA = rank * sl + sl - 2 - 2 * tid;
+            const bool own = 2 * tid + 2 <= sl;
+            unsigned c2[2] = {0u, 0u}, g2[2] = {0u, 0u};
+            unsigned long long a2[2] = {0ull, 0ull};
+            if (own) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int d = dA + k;
+                    c2[k] = hist[d];
+                    g2[k] = hist[kSearchBins + d];
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) a2[k] += (unsigned long long)hist[(2 + q) * kSearchBins + d] << (14 * q);
+                }
+            }
+            const SearchAcc mine = {a2[0] + a2[1], 0ull, 0u, c2[0] + c2[1]};
+            SearchAcc before = block_suffix_search(mine, sacc);
+            if (tid == 0) ssum = search_add(before, mine);
+            for (int k = tid; k < kSearchFields * kSearchBins / 4; k += T) hist4[k] = make_uint4(0u, 0u, 0u, 0u);
+            cl.sync();
+            // the slices before this one
+            if (warp == 0) {
+                SearchAcc x = (lane < rank) ? *cl.map_shared_rank(&ssum, lane) : zero;
+                for (int o = 16; o > 0; o >>= 1) {
+                    const SearchAcc y = {__shfl_xor_sync(0xffffffffu, x.a, o), __shfl_xor_sync(0xffffffffu, x.v, o),
+                                         __shfl_xor_sync(0xffffffffu, x.b, o), __shfl_xor_sync(0xffffffffu, x.c, o)};
+                    x = search_add(x, y);
+                }
+                if (lane == 0) sacc[0] = x;
+            }
+            __syncthreads();
+            before = search_add(before, sacc[0]);
+            // bias and count before the first entry of bin dA, and of bin dA + 1
+            const unsigned long long S0 = sc.rest_a + before.a, S1 = S0 + a2[0];
+            const unsigned n0 = (unsigned)sc.rem_cnt + before.c, n1 = n0 + c2[0];
+            const bool p0 = c2[0] > 0u && __fmul_rn(__fmul_rn(__uint_as_float(g2[0]), fs1), fs2) > 2.0f * (float)S0;
+            const bool p1 = c2[1] > 0u && __fmul_rn(__fmul_rn(__uint_as_float(g2[1]), fs1), fs2) > 2.0f * (float)S1;
+            int cand = own ? (p1 ? dA + 1 : (p0 ? dA : -1)) : -1;
+            cand = __reduce_max_sync(0xffffffffu, cand);
+            if (lane == 0) redi[warp] = cand;
+            __syncthreads();
+            cand = __reduce_max_sync(0xffffffffu, redi[lane]);
+            if (own && cand >= 0 && (cand == dA || cand == dA + 1)) {
+                const bool first = cand == dA;
+                sprop.a = first ? S0 : S1;
+                sprop.c = first ? n0 : n1;
+                sprop.in_bin = first ? c2[0] : c2[1];
+            }
+            if (tid == 0) sprop.cand = cand;
+            cl.sync();
+            // the last bin of the level (highest CTA with a candidate) whose first entry passes
+            if (warp == 0) {
+                const int cr = lane < C ? cl.map_shared_rank(&sprop, lane)->cand : -1;
+                const unsigned who = __ballot_sync(0xffffffffu, cr >= 0);
+                if (lane == 0) {
+                    if (who == 0u) {
+                        // the range's first entry fails (only at the top level): nothing is shrunk
+                        sc.found = 1;
+                        sc.n_shrunk = sc.rem_cnt;
+                        sc.bin_kb = klo;
+                    } else {
+                        const SearchProp p = *cl.map_shared_rank(&sprop, 31 - __clz(who));
+                        sc.rest_a = p.a;
+                        sc.rem_cnt = (int)p.c;
+                        const unsigned long long d_ = (unsigned long long)p.cand;
+                        sc.klo = klo + (d_ << bs);
+                        sc.khi = min(klo + span, klo + ((d_ + 1ull) << bs));
+                        sc.in_bin = (int)p.in_bin;
+                        if (p.in_bin == 1u || lev == kSearchLevels - 1) {
+                            sc.found = 1;
+                            sc.n_shrunk = (int)(p.c + p.in_bin);
+                            sc.bin_kb = sc.khi;
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+            if (sc.found) break;
+            if (sc.in_bin <= kSmallBin) {
+                if (tid == 0) ncand = 0;
+                __syncthreads();
+                for (int i = tid; i < ns; i += T) {
+                    const float ga = sg[i];
+                    if (!(ga > 0.f)) continue;
+                    const unsigned long long K = search_key(gamma_key32(ga), j0 + i);
+                    if (K < sc.klo || K >= sc.khi) continue;
+                    const int at = atomicAdd(&ncand, 1);
+                    unsigned pa[3];
+                    fixed_pieces(__fmul_rn(__fmul_rn(sr[i], fs1), fs2), pa);
+                    bcand[at].key = K;
+                    bcand[at].a = (unsigned long long)pa[0] + ((unsigned long long)pa[1] << 14) +
+                                  ((unsigned long long)pa[2] << 28);
+                    bcand[at].v = 0ull;
+                    bcand[at].b = __float_as_uint(ga);
+                }
+                cl.sync();
+                if (warp == 0) finish_binary(cl, bcand, &ncand, bloc, sc, C, fs1, fs2);
+                __syncthreads();
+                break;
+            }
+        }
+    }
+
+    // ---- phase 1: beta (Newton on the classes; thread 0 does the scalar update)
     while (!sc.done) {
         ++iters;
         const float tu = sc.th_up, td = sc.th_dn;
@@ -1565,6 +1852,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     }
     __syncthreads();
     const float bf = sc.bf;
+    const unsigned long long bkb = BINARY ? sc.bin_kb : 0ull;
     stamp(1);
 
     // ---- phase 2: lambda, a_i, v_i, b_i and eq. (7); the weight factor lambda_i / r_i of the
@@ -1591,15 +1879,17 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             const float w = sw[i], al = sr[i], gam = sg[i], rho = sp[i];
             Coef c = {0.f, 0.f, 0.f};
             float om_i = 1.0f;
+            // binary shrinkage: lambda = r on the passing prefix of the gamma order, 1 elsewhere
+            const bool at_r = BINARY ? (gam > 0.f && search_key(gamma_key32(gam), j0 + i) < bkb) : (bf <= al);
             if (!(w > 0.f)) {
                 om_i = __fdiv_rn(__fadd_rn(1.0f, rho), rho);   // lambda = 1: 1 / r
-            } else if (bf <= al) {
+            } else if (at_r) {
                 const float lw = __fsub_rn(w, al);
                 c.a = al;
                 c.v = __fmul_rn(lw, al);
                 c.b = fmaxf(lw, al);
             } else {
-                const float lam = fminf(__fdiv_rn(bf, gam), 1.0f);
+                const float lam = BINARY ? 1.0f : fminf(__fdiv_rn(bf, gam), 1.0f);
                 const float lw = __fmul_rn(lam, w);
                 c.a = __fsub_rn(w, lw);
                 c.v = __fmul_rn(__fmul_rn(lam, lw), gam);
@@ -1667,8 +1957,9 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         sc.kstar = nl;
         sc.kkey = ~0ull;
         if (rank == 0) {
-            R.beta = ff_to_f64(sc.theta);
-            R.beta_f = bf;
+            R.beta = BINARY ? ff_to_f64(SA) : ff_to_f64(sc.theta);   // binary: the bias of the coefficients
+            R.beta_f = BINARY ? SA.hi : bf;
+            R.n_shrunk = BINARY ? sc.n_shrunk : 0;
             R.sum_a = ff_to_f64(SA);
             R.V = ff_to_f64(SV);
             R.b1 = nl > 0 ? f32_to_f64_bits(B1) : 0.0;
@@ -2457,8 +2748,12 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         lc.attrs = attr;
         lc.numAttrs = 2;
-        VK_CUDA(cudaLaunchKernelEx(&lc, decide_kernel, views, a, ctx.rows, (const float2*)ctx.tl,
-                                   (const float2*)ctx.th, ctx.wl, ctx.mark, ctx.elist));
+        if (a.binary)
+            VK_CUDA(cudaLaunchKernelEx(&lc, decide_kernel<true>, views, a, ctx.rows, (const float2*)ctx.tl,
+                                       (const float2*)ctx.th, ctx.wl, ctx.mark, ctx.elist));
+        else
+            VK_CUDA(cudaLaunchKernelEx(&lc, decide_kernel<false>, views, a, ctx.rows, (const float2*)ctx.tl,
+                                       (const float2*)ctx.th, ctx.wl, ctx.mark, ctx.elist));
         VK_LAUNCHED("decide");
     } else {
         const int wmax = std::max(max_nl, max_nh);
@@ -2535,9 +2830,11 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     if (!g_attr_done) {
         VK_CUDA(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)(sizeof(unsigned long long) * kSelWidth)));
-        VK_CUDA(cudaFuncSetAttribute(decide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
+        VK_CUDA(cudaFuncSetAttribute(decide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
+        VK_CUDA(cudaFuncSetAttribute(decide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
         // a 16-CTA cluster (non-portable) lets rows of up to 16 x kDecideCap entries stay on chip
-        if (cudaFuncSetAttribute(decide_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        if (cudaFuncSetAttribute(decide_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+            cudaFuncSetAttribute(decide_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
             cudaLaunchConfig_t lc = {};
             lc.gridDim = dim3(kDecideMaxCluster);
             lc.blockDim = dim3(kDecideThreads);
@@ -2550,7 +2847,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
             lc.attrs = attr;
             lc.numAttrs = 1;
             int nclusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&nclusters, decide_kernel, &lc) == cudaSuccess && nclusters > 0)
+            if (cudaOccupancyMaxActiveClusters(&nclusters, decide_kernel<false>, &lc) == cudaSuccess && nclusters > 0)
                 g_decide_max_cluster = kDecideMaxCluster;
         }
         cudaGetLastError();  // a refused query leaves no error behind
@@ -2592,8 +2889,13 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         }
         ctx.last_n.push_back(s.n);
     }
+    if (cfg.shrinkage == VERKV_SHRINK_BINARY && max_nl > g_decide_max_cluster * kDecideCap) {
+        ctx.err = "binary shrinkage runs in the on-chip decision: |L| of a row is above its capacity";
+        return VERKV_EUNSUPPORTED;
+    }
     DecodeArgs a;
     a.Hkv = cfg.n_kv_heads;
+    a.binary = cfg.shrinkage == VERKV_SHRINK_BINARY ? 1 : 0;
     a.Hq = cfg.n_q_heads;
     a.G = ctx.G;
     a.ws_n = ctx.ws_n;

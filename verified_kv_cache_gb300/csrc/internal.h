@@ -69,7 +69,7 @@ struct RowState {
     double b1, b2;      // largest and second-largest b_i
     double eps_hat;
     float beta_f;       // beta in fp32 (what the attention weights use)
-    float pad;
+    int n_shrunk;       // binary shrinkage: entries given lambda = r
     int beta_iters;     // passes of the beta solve
     int sel_passes;     // radix-select passes
     unsigned int phase_ns[6];  // decide kernel: ns spent in phases 0..4 and in the ranking (rank 0)
