@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-flush", action="store_true", help="(profiling runs) skip the L2 flushes")
+    p.add_argument("--no-secondary", action="store_true",
+                   help="skip the binary-shrinkage and batch-8 stack-layer measurements")
     return p.parse_args()
 
 
@@ -104,9 +106,10 @@ class Clocks:
 
 
 # ----------------------------------------------------------------------------- roofline bookkeeping
-def algorithmic_bytes(kernel, stats, traces, w, row_bytes):
+def algorithmic_bytes(kernel, stats, traces, w, row_bytes, batch=1):
     """Bytes each kernel must move by the method's definition (per launch), from the compressed sizes
-    and the decode traces.  Intermediates a kernel writes for the next one are not counted."""
+    and the decode traces.  Intermediates a kernel writes for the next one are not counted.  `stats`
+    holds the head statistics of every sequence of the batch."""
     Hkv, Hq, n, d = w.n_kv, w.n_q, w.n, w.d
     L = sum(s["n_l"] for s in stats)
     H = sum(s["n_h"] for s in stats)
@@ -114,14 +117,32 @@ def algorithmic_bytes(kernel, stats, traces, w, row_bytes):
     sk = {"2bit": (d // 4) * 2 / 8 + (d // 4) * 4 / 128, "int8": d + 4, "exact": d * (2 if w.kv_dtype == "bf16" else 4)}
     s_sk = sk[w.sketch]
     if kernel == "score":             # sketch of every L token, the L/H position of every token,
-        return L * s_sk + Hkv * n * 4 + H * row_bytes / 2 + Hq * d * 4   # exact keys of H, the queries
+        return L * s_sk + batch * Hkv * n * 4 + H * row_bytes / 2 + batch * Hq * d * 4   # exact keys of H, q
     if kernel == "weights":           # r of L
         return L * 4 * (Hq // Hkv)
     if kernel == "attn":              # resident K/V rows from HBM, once per KV head, and the queries
-        return R * row_bytes + Hq * d * 8
+        return R * row_bytes + batch * Hq * d * 8
     if kernel == "attn_link":         # the fetched rows: over the host link, once per KV head
         return traces.get("union_rows", 0) * row_bytes
     return None
+
+
+def measured_traffic(w):
+    """DRAM bytes per launch of the decode kernels from the committed ncu summary of this workload, if
+    the kernel source is the one the counters were taken on (else {}: the kernels changed since)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"traffic_qwen3-4b-{w.n // 1024}k-{w.sketch}.txt")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        body = "".join(line for line in f if not line.startswith("#"))
+    try:
+        rec = json.loads(body)
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except (ValueError, KeyError, OSError):
+        return {}
+    return rec["dram_bytes_per_launch"] if sha == rec["source_sha256"] else {}
 
 
 # ----------------------------------------------------------------------------- the GPU arm
@@ -257,6 +278,11 @@ def run_verkv(args):
     peak_src = "measured" if hbm_peak else "fallback"
     hbm_peak = hbm_peak or 6800.0
 
+    traffic = measured_traffic(w)
+    traffic_note = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch (profiles/traffic_*.txt); rows "
+                    "fetched from pinned host memory cross NVLink-C2C and are not DRAM traffic") if traffic else \
+        "null: no ncu capture of the current kernel source"
+
     def roof(kname):
         if kname not in agg:
             return None
@@ -267,8 +293,8 @@ def run_verkv(args):
                     "unit": None, "frac": None, "traffic": None}
         ach = by / (avg_ms / 1e3) / 1e9
         return {"kernel": kname, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                "frac": ach / hbm_peak, "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
-                "algorithmic_bytes": by, "avg_us": avg_ms * 1e3}
+                "frac": ach / hbm_peak, "traffic": traffic.get(kname), "traffic_note": traffic_note,
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": by, "avg_us": avg_ms * 1e3}
 
     # host-link peak: a bulk pinned host -> device copy (the same link the fetch uses)
     link_peak = None
@@ -294,7 +320,7 @@ def run_verkv(args):
         by = algorithmic_bytes(kname + "_link", stats0, traces, w, row_bytes)
         ach = by / (avg_ms / 1e3) / 1e9
         return {"kernel": kname, "bound": "host_link", "achieved": ach, "peak": link_peak, "unit": "GB/s",
-                "frac": ach / link_peak, "traffic": None,
+                "frac": ach / link_peak, "traffic": traffic.get(kname), "traffic_note": traffic_note,
                 "peak_source": "measured in this run: pinned host -> device copy of 256 MiB",
                 "algorithmic_bytes": by, "avg_us": avg_ms * 1e3}
 
@@ -314,6 +340,9 @@ def run_verkv(args):
         d2h = out.numel() * 4
         e_ms = []
         for it in range(args.warmup + args.steps):
+            # the same L2 policy as the device-timed steps: flushed (untimed) before every call, each
+            # segment timed by its own event pair; the copies sit inside the first and last segments
+            segs = []
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(st)
@@ -321,15 +350,31 @@ def run_verkv(args):
             obs_scratch.copy_(obs_host, non_blocking=True)
             q_scratch.copy_(q_host, non_blocking=True)
             ctx.compress(0, 0, w.n, kv_host, kv_scratch, obs_scratch, W, None, st)
-            for s in range(S):
-                ctx.decode(0, [0], q_scratch[s], w.eps, w.delta, out[s], st)
-            out_host.copy_(out, non_blocking=True)
             b.record(st)
-            b.synchronize()
+            segs.append((a, b))
+            for s in range(S):
+                flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                ctx.decode(0, [0], q_scratch[s], w.eps, w.delta, out[s], st)
+                if s == S - 1:
+                    out_host.copy_(out, non_blocking=True)
+                b.record(st)
+                segs.append((a, b))
+            torch.cuda.synchronize()
             if it >= args.warmup:
-                e_ms.append(a.elapsed_time(b))
+                e_ms.append(sum(x.elapsed_time(y) for x, y in segs))
         e2e = {"value": world * units_per_step / (statistics.mean(e_ms) / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e_ms)}
+
+    secondary = {}
+    if rank == 0 and not args.no_secondary:
+        secondary["binary_shrinkage"] = binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush)
+    ctx.close()
+    if rank == 0 and not args.no_secondary:
+        del kv_dev, flush_buf
+        torch.cuda.empty_cache()
+        secondary["stack_layer_b8_int8"] = stack_run(args, dev, st, hbm_peak, peak_src)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -359,10 +404,134 @@ def run_verkv(args):
             "roofline_attn_link": roof_link_attn, "host_link_peak_gbs": link_peak,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
         }
+        line.update(secondary)
         print(json.dumps(line))
-    ctx.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- secondary measurements
+def _kernel_agg(kt):
+    agg = {}
+    for name, ms in kt:
+        a = agg.setdefault(name, [0.0, 0])
+        a[0] += ms
+        a[1] += 1
+    return agg
+
+
+def binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush):
+    """The same workload with the binary shrinkage coefficients of Appendix A.2: decode time (per-call
+    events, L2 flushed before every call), fetch statistics and the decision kernel's time."""
+    import torch
+
+    from verified_kv_cache_gb300 import binding
+    ctx = binding.VerKV(n_kv_heads=w.n_kv, n_q_heads=w.n_q, max_tokens=w.n, n_layers=1, n_seqs=1, max_batch=1,
+                        n_sink=w.n_sink, n_local=w.n_local, eta=w.eta, seed=w.seed, sketch=w.sketch,
+                        kv_dtype=w.kv_dtype, shrinkage="binary")
+    W, S = w.obs_q.shape[2], w.queries.shape[0]
+    out = torch.empty_like(q_dev)
+    ctx.compress(0, 0, w.n, kv_host, kv_dev, obs, W, None, st)
+    for s in range(S):   # warm-up
+        ctx.decode(0, [0], q_dev[s], w.eps, w.delta, out[s], st)
+    ms = []
+    for _ in range(max(1, args.steps)):
+        for s in range(S):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            ctx.decode(0, [0], q_dev[s], w.eps, w.delta, out[s], st)
+            b.record(st)
+            ms.append((a, b))
+    torch.cuda.synchronize()
+    dec_ms = [a.elapsed_time(b) for a, b in ms]
+    fetch, nof, shr, ks = [], 0, [], []
+    ctx.set_kernel_timing(True)
+    for s in range(S):
+        flush()
+        ctx.decode(0, [0], q_dev[s], w.eps, w.delta, out[s], st)
+        tr = ctx.decode_trace(w.n_q)
+        fetch += [len(ctx.fetch_set(0, h, w.n)) / w.n for h in range(w.n_kv)]
+        nof += sum(t["no_fetch"] for t in tr)
+        shr += [t["n_shrunk"] for t in tr]
+        ks += [t["kstar"] for t in tr]
+    agg = _kernel_agg(ctx.kernel_times(st))
+    ctx.set_kernel_timing(False)
+    ctx.close()
+    return {"decode_us_per_step": statistics.mean(dec_ms) * 1e3, "decode_us_p50": statistics.median(dec_ms) * 1e3,
+            "fetch_fraction_per_token": statistics.mean(fetch), "no_fetch_rate": nof / len(ks),
+            "mean_kstar": statistics.mean(ks), "mean_n_shrunk": statistics.mean(shr),
+            "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()}}
+
+
+def stack_run(args, dev, st, hbm_peak, peak_src):
+    """One layer of the 36-layer stack workload: batch 8 sequences of 32K tokens, GQA 32/8, int8
+    sketch, eta = 1/32, eps = delta = 0.1, random queries.  Per-call events (L2 flushed before every
+    call) and per-kernel events; the HBM roofline of the sketch scan and of the attention at batch 8."""
+    import torch
+
+    from verified_kv_cache_gb300 import binding, workloads
+    B, steps = 8, 16
+    w = workloads.stack_layer_case(layer=0, n=args.n, batch=B, steps=steps)
+    ctx = binding.VerKV(n_kv_heads=w.n_kv, n_q_heads=w.n_q, max_tokens=w.n, n_layers=1, n_seqs=B, max_batch=B,
+                        n_sink=w.n_sink, n_local=w.n_local, eta=w.eta, seed=w.seed, sketch=w.sketch,
+                        kv_dtype=w.kv_dtype)
+    W = w.obs_q.shape[2]
+    stats, hosts = [], []
+    for b in range(B):
+        kv_h = torch.from_numpy(w.kv_host_layout(b)).view(torch.bfloat16).pin_memory()
+        hosts.append(kv_h)
+        kv_d = kv_h.to(dev)
+        obs = torch.from_numpy(w.obs_q[b]).to(dev)
+        stats += ctx.compress(0, b, w.n, kv_h, kv_d, obs, W, None, st)
+        del kv_d
+    q = torch.from_numpy(w.queries).to(dev)             # [steps, B, Hq, d]
+    out = torch.empty_like(q)
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ids = list(range(B))
+    for s in range(3):
+        ctx.decode(0, ids, q[s], w.eps, w.delta, out[s], st)
+    ev = []
+    for s in range(steps):
+        flush_buf.fill_(1.0)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        ctx.decode(0, ids, q[s], w.eps, w.delta, out[s], st)
+        b_.record(st)
+        ev.append((a, b_))
+    torch.cuda.synchronize()
+    dec_ms = [a.elapsed_time(b_) for a, b_ in ev]
+    ctx.set_kernel_timing(True)
+    fetch = []
+    for s in range(steps):
+        flush_buf.fill_(1.0)
+        ctx.decode(0, ids, q[s], w.eps, w.delta, out[s], st)
+        for b in range(B):
+            fetch += [len(ctx.fetch_set(b, h, w.n)) / w.n for h in range(w.n_kv)]
+    agg = _kernel_agg(ctx.kernel_times(st))
+    ctx.set_kernel_timing(False)
+    row_bytes = 2 * w.d * 2
+
+    def roof(k):
+        if k not in agg:
+            return None
+        avg_ms = agg[k][0] / agg[k][1]
+        by = algorithmic_bytes(k, stats, {}, w, row_bytes, batch=B)
+        ach = by / (avg_ms / 1e3) / 1e9
+        return {"kernel": k, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                "traffic": None, "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": by,
+                "avg_us": avg_ms * 1e3}
+
+    res = {"workload": f"stack layer: batch {B} x n={w.n}, GQA {w.n_q}/{w.n_kv}, int8 sketch, eta=1/32, "
+                       f"eps=delta=0.1, {steps} decode calls, random queries",
+           "decode_us_per_call": statistics.mean(dec_ms) * 1e3,
+           "scored_tokens_per_s": B * w.n_q * w.n / (statistics.mean(dec_ms) / 1e3),
+           "fetch_fraction_per_token": statistics.mean(fetch) if fetch else None,
+           "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()},
+           "roofline_score": roof("score"), "roofline_attn": roof("attn")}
+    ctx.close()
+    del hosts, flush_buf
+    return res
 
 
 # ----------------------------------------------------------------------------- the oracle (CPU)
