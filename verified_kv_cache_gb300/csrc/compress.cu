@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kTmmaThreads, 1) tau_mma_kernel(const __nv_bfl
         for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
             for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                umma_bf16(d, umma_desc_sw128(ab + sp * kTmmaTileBytes + umma_kstep_offset(ks, 128)),
+                umma_mma(d, umma_desc_sw128(ab + sp * kTmmaTileBytes + umma_kstep_offset(ks, 128)),
                           umma_desc_sw128(bb + umma_kstep_offset(ks, kTmmaN)), idesc, sp > 0 || ks > 0);
         umma_commit(&bar[i & 1]);
     };

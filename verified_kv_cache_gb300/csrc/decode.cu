@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "async.cuh"
+#include "umma.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -92,48 +93,21 @@ __global__ void init_rows_kernel(RowState* __restrict__ rows, Views views, Decod
 }
 
 // --------------------------------------------------------------------------------------------
-// D1: sketch logits <q, k^_i>/sqrt(d) of the tokens of L, as float-float.  One thread per token
-// position, all G query heads of the KV head.  The query side is split so that the bulk of each
-// dot product is an exact fp32 sum of integer multiples of a power of two:
-//   int8:  q = h1 + h2 + l2 with h1 on the grid 2^(E-8) and h2 on 2^(E-17) (|q| < 2^E); with
-//          codes |c| <= 127 every partial sum of h1*c (and of h2*c) is an integer < 2^24 in
-//          grid units, so it is exact; only the tiny l2 part rounds.
+// D1: sketch logits <q, k^_i>/sqrt(d) of the tokens of L, as float-float.  The query side is split so
+// that the bulk of each dot product is an exact sum of integer multiples of a power of two:
+//   int8:  q = 2^(E-10) P1 + 2^(E-21) P2 + 2^(E-32) P3 + r (|q| < 2^E, |r| <= 2^(E-33)) with integer
+//          pieces |P| <= 1024, exact in fp16, as are the codes |c| <= 127; every sum over the 128
+//          channels of P c is an integer below 2^24, so the tensor core's fp32 accumulation of those
+//          products is exact.  One M = 128 tokens x N = (3 pieces x G heads, padded) x K = 128 MMA per
+//          tile of 128 tokens, accumulated in tensor memory.
 //   2-bit: kappa_j = q_j * scale_gj (exact two-product), split on the grid 2^(E-17) of the group;
 //          codes are 0..3 and 32 channels, so the grid part is exact as well.
 // --------------------------------------------------------------------------------------------
-template <int G>
-struct QSplitInt8 {
-    float h1[G][kHeadDim], h2[G][kHeadDim], l2[G][kHeadDim];
-};
-
-template <int G>
-__device__ void split_q_int8(const float* __restrict__ q, QSplitInt8<G>& s, float* red)
-{
-    // blockDim.x == kTile == kHeadDim: thread c owns channel c of every head
-    const int c = threadIdx.x;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float v = q[g * kHeadDim + c];
-        const float mx = block_max(fabsf(v), red);
-        int E;
-        frexpf(mx, &E);  // mx < 2^E
-        const float h1 = ldexpf(rintf(ldexpf(v, 8 - E)), E - 8);
-        const float l1 = __fsub_rn(v, h1);
-        const float h2 = ldexpf(rintf(ldexpf(l1, 17 - E)), E - 17);
-        s.h1[g][c] = h1;
-        s.h2[g][c] = h2;
-        s.l2[g][c] = __fsub_rn(l1, h2);
-    }
-}
-
 __device__ __forceinline__ ff combine3(float s1, float s2, float s3)
 {
     ff t = two_sum(s1, s2);
     return fast_two_sum(t.hi, __fadd_rn(t.lo, s3));
 }
-
-template <int G>
-constexpr int kInt8TokensPerThread = G <= 4 ? 4 : 2;
 
 // Exact logits of the tokens of H (resident keys), by H index, for the blocks of a scoring launch
 // past its L tiles: 8 threads per (token, query head), 16 channels each (float-float partial sums
@@ -320,98 +294,209 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
     }
 }
 
-template <typename T, int G>
-__global__ void __launch_bounds__(kTile) score_int8_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
-                                                           RowState* __restrict__ rows, float2* __restrict__ tl,
-                                                           float2* __restrict__ th, int n_ltiles)
+// Int8 sketch tiles on the tensor cores.  A CTA scores a contiguous range of 128-token tiles of one
+// (sequence, KV head): A = the tile's codes as fp16 (128 tokens x 128 channels, K-major, 128-byte
+// swizzle; two stages), B = the query pieces (N rows: piece k of head g in row 3 g + k), D = two
+// tensor-memory accumulators of N fp32 columns.  The codes of the next two tiles (and each thread's
+// L position and scale) are in flight in registers while the current tile is converted and its MMAs
+// run next to the epilogue of the previous tile; warp w holds tokens 32 w .. 32 w + 31 of a tile
+// (its tensor-memory lane quarter) and finishes one token per thread.  The grid is one wave of
+// kInt8CtasPerSm CTAs per multiprocessor; after its tiles, each CTA also takes a share of the exact
+// logits of the KV head's H tokens.
+template <int G>
+struct Int8Mma {
+    static constexpr int NP = (3 * G + 15) / 16 * 16;           // B rows, padded to the MMA's N step
+    static constexpr int COLS = 2 * NP < 32 ? 32 : 2 * NP;      // tensor-memory columns (two accumulators)
+    static constexpr int ABytes = 128 * kHeadDim * 2;           // one fp16 code tile (32 KiB)
+    static constexpr int BBytes = NP * kHeadDim * 2;
+    static constexpr size_t Smem = 2 * (size_t)ABytes + BBytes + 1024;   // + alignment slack
+};
+constexpr int kInt8CtasPerSm = 3;
+
+// Four int8 codes (one 32-bit word) to four exact fp16 values: the sign bits are flipped (c + 128),
+// each byte is placed under the fp16 exponent of 1024 (1024 + c + 128, exact) and 1152 subtracted.
+__device__ __forceinline__ uint2 codes4_to_f16(uint32_t w)
 {
-    pdl_trigger();   // the decision kernel may start its independent prologue
-    if ((int)blockIdx.x >= n_ltiles) {
-        score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
-        return;
-    }
-    constexpr int TPT = kInt8TokensPerThread<G>;   // tokens per thread: each query-split load serves them all
-    __shared__ __align__(16) QSplitInt8<G> qs;
+    const uint32_t x = w ^ 0x80808080u;
+    uint32_t lo = __byte_perm(x, 0x64646464u, 0x4140), hi = __byte_perm(x, 0x64646464u, 0x4342);
+    const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480u), __ushort_as_half((unsigned short)0x6480u));
+    __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), bias), h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+    return make_uint2(*reinterpret_cast<uint32_t*>(&l2), *reinterpret_cast<uint32_t*>(&h2));
+}
+
+template <typename T, int G>
+__device__ __forceinline__ void score_int8_ltiles(const Views& views, const float* __restrict__ q, const DecodeArgs& a,
+                                                  RowState* __restrict__ rows, float2* __restrict__ tl, int b, int kv,
+                                                  int t0, int nt)
+{
+    using P = Int8Mma<G>;
+    extern __shared__ unsigned char dsm_raw[];
+    __shared__ __align__(8) unsigned long long bar[2];
+    __shared__ unsigned tbase;
     __shared__ float red[32];
-    const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
+    __shared__ int qexp[G];
+    unsigned char* dsm = dsm_raw + ((1024u - (umma_smem_u32(dsm_raw) & 1023u)) & 1023u);
+    unsigned char* sA = dsm;
+    unsigned char* sB = dsm + 2 * P::ABytes;
     const SlotView& V = views.v[b];
     const int n = V.n;
-    const int i0 = blockIdx.x * kTile * TPT;
-    if (i0 >= n) return;  // a shorter sequence of the batch
-    split_q_int8<G>(q + ((int64_t)b * a.Hq + kv * G) * kHeadDim, qs, red);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // B: the pieces of the G query rows (thread c owns channel c), rows past 3 G zero
+    const float* qg = q + ((int64_t)b * a.Hq + kv * G) * kHeadDim;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float v = qg[g * kHeadDim + tid];
+        const float mx = block_max(fabsf(v), red);
+        int E;
+        frexpf(mx, &E);   // mx < 2^E (E = 0 for a zero query)
+        const float p1 = rintf(ldexpf(v, 10 - E));
+        const float r1 = __fsub_rn(v, ldexpf(p1, E - 10));
+        const float p2 = rintf(ldexpf(r1, 21 - E));
+        const float r2 = __fsub_rn(r1, ldexpf(p2, E - 21));
+        const float p3 = rintf(ldexpf(r2, 32 - E));
+        *reinterpret_cast<__half*>(sB + umma_sw128_offset(3 * g + 0, tid, P::NP)) = __float2half_rn(p1);
+        *reinterpret_cast<__half*>(sB + umma_sw128_offset(3 * g + 1, tid, P::NP)) = __float2half_rn(p2);
+        *reinterpret_cast<__half*>(sB + umma_sw128_offset(3 * g + 2, tid, P::NP)) = __float2half_rn(p3);
+        if (tid == 0) qexp[g] = E;
+    }
+    for (int r = 3 * G; r < P::NP; ++r) *reinterpret_cast<__half*>(sB + umma_sw128_offset(r, tid, P::NP)) = __float2half_rn(0.f);
+
+    // codes of tile i into registers: lane l of warp w reads the 16-byte chunk l % 8 of tokens
+    // 32 w + 4 j + l / 8 (j = 0..7): each load instruction of the warp covers 512 contiguous bytes.
+    // With them, the L position and scale of this thread's own token of the tile (its epilogue row).
+    const int8_t* codes = V.codes8 + (int64_t)kv * n * kHeadDim;
+    auto load = [&](int i, uint4 (&buf)[8], int& li, float& sc) {
+        const int tok0 = (t0 + i) * 128 + 32 * warp + (lane >> 3);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int tok = tok0 + 4 * j;
+            buf[j] = tok < n ? __ldg(reinterpret_cast<const uint4*>(codes + (int64_t)tok * kHeadDim) + (lane & 7))
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int tok = (t0 + i) * 128 + 32 * warp + lane;
+        li = tok < n ? __ldg(V.lpos + (int64_t)kv * n + tok) : -1;   // < 0: not in L
+        sc = tok < n ? __ldg(V.scale8 + (int64_t)kv * n + tok) : 0.f;
+    };
+    auto store = [&](int i, const uint4 (&buf)[8]) {
+        unsigned char* dst = sA + (i & 1) * P::ABytes;
+        const int k0 = 16 * (lane & 7);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int row = 32 * warp + 4 * j + (lane >> 3);
+            const uint2 c0 = codes4_to_f16(buf[j].x), c1 = codes4_to_f16(buf[j].y), c2 = codes4_to_f16(buf[j].z),
+                        c3 = codes4_to_f16(buf[j].w);
+            *reinterpret_cast<uint4*>(dst + umma_sw128_offset(row, k0, 128)) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+            *reinterpret_cast<uint4*>(dst + umma_sw128_offset(row, k0 + 8, 128)) = make_uint4(c2.x, c2.y, c3.x, c3.y);
+        }
+    };
+    // two tiles in flight: register set 0 holds even tiles, set 1 odd tiles
+    uint4 buf0[8], buf1[8];
+    int li0 = -1, li1 = -1, li_ep = -1;
+    float sc0 = 0.f, sc1 = 0.f, sc_ep = 0.f;
+    load(0, buf0, li0, sc0);
+    if (nt > 1) load(1, buf1, li1, sc1);
+    if (warp == 0) umma_alloc(&tbase, P::COLS);
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    umma_fence_before();
     __syncthreads();
-    int li[TPT];
+    umma_fence_after();
+    const unsigned tmem = tbase;
+    constexpr unsigned idesc = umma_idesc_f16_f32(128, P::NP);
+    int E[G];
 #pragma unroll
-    for (int t = 0; t < TPT; ++t) {
-        const int i = i0 + t * kTile + threadIdx.x;
-        li[t] = i < n ? V.lpos[(int64_t)kv * n + i] : -1;   // < 0: not in L
-    }
-    float s1[TPT][G], s2[TPT][G], s3[TPT][G];
-#pragma unroll
-    for (int t = 0; t < TPT; ++t)
-#pragma unroll
-        for (int g = 0; g < G; ++g) s1[t][g] = s2[t][g] = s3[t][g] = 0.f;
-#pragma unroll 1
-    for (int c16 = 0; c16 < kHeadDim / 16; ++c16) {
-        uint32_t w[TPT][4];
-#pragma unroll
-        for (int t = 0; t < TPT; ++t) {
-            uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
-            if (li[t] >= 0)
-                w4 = reinterpret_cast<const uint4*>(V.codes8 + ((int64_t)kv * n + i0 + t * kTile + threadIdx.x) * kHeadDim)[c16];
-            w[t][0] = w4.x;
-            w[t][1] = w4.y;
-            w[t][2] = w4.z;
-            w[t][3] = w4.w;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int c = c16 * 16 + k * 4;
-            float cf[TPT][4];
-#pragma unroll
-            for (int t = 0; t < TPT; ++t)
-#pragma unroll
-                for (int bte = 0; bte < 4; ++bte) cf[t][bte] = (float)(int8_t)((w[t][k] >> (8 * bte)) & 0xffu);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float4 H1 = *reinterpret_cast<const float4*>(&qs.h1[g][c]);
-                const float4 H2 = *reinterpret_cast<const float4*>(&qs.h2[g][c]);
-                const float4 L2 = *reinterpret_cast<const float4*>(&qs.l2[g][c]);
-                const float h1[4] = {H1.x, H1.y, H1.z, H1.w}, h2[4] = {H2.x, H2.y, H2.z, H2.w},
-                            l2[4] = {L2.x, L2.y, L2.z, L2.w};
-#pragma unroll
-                for (int bte = 0; bte < 4; ++bte)
-#pragma unroll
-                    for (int t = 0; t < TPT; ++t) {
-                        s1[t][g] = __fmaf_rn(h1[bte], cf[t][bte], s1[t][g]);
-                        s2[t][g] = __fmaf_rn(h2[bte], cf[t][bte], s2[t][g]);
-                        s3[t][g] = __fmaf_rn(l2[bte], cf[t][bte], s3[t][g]);
-                    }
-            }
-        }
-    }
+    for (int g = 0; g < G; ++g) E[g] = qexp[g];
     float mloc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
+    bool bad = false;
+    // step i converts tile i (from its register set, which then starts loading tile i + 2) and issues
+    // its MMAs, then finishes tile i - 1, whose MMAs ran meanwhile
+    auto step = [&](int i, uint4 (&buf)[8], int& li, float& sc) {
+        int li_t = -1;
+        float sc_t = 0.f;
+        if (i < nt) {
+            li_t = li;
+            sc_t = sc;
+            store(i, buf);   // stage i % 2: the MMAs of tile i - 2 that read it are complete (waited at i - 1)
+            if (i + 2 < nt) load(i + 2, buf, li, sc);
+            fence_proxy_async_smem();   // the fp16 tiles (generic stores) -> tensor core
+            umma_fence_before();
+            __syncthreads();   // tile i is in shared memory; accumulator i % 2 was read back at i - 1
+            if (tid == 0) {
+                umma_fence_after();
+                const unsigned d = tmem + (unsigned)((i & 1) * P::NP);
+                const unsigned ab = umma_smem_u32(sA + (i & 1) * P::ABytes), bb = umma_smem_u32(sB);
 #pragma unroll
-    for (int t = 0; t < TPT; ++t) {
-        if (li[t] < 0) continue;
-        const float sc = V.scale8[(int64_t)kv * n + i0 + t * kTile + threadIdx.x];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            ff x = combine3(s1[t][g], s2[t][g], s3[t][g]);
-            x = ff_mul(ff_mul_f(x, sc), a.inv_sqrt_d);
-            const int row = row_of(b, kv * G + g, a.Hq);
-            tl[(int64_t)row * a.ws_n + li[t]] = make_float2(x.hi, x.lo);
-            mloc[g] = fmaxf(mloc[g], x.hi);
+                for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                    umma_mma(d, umma_desc_sw128(ab + umma_kstep_offset(ks, 128)),
+                             umma_desc_sw128(bb + umma_kstep_offset(ks, P::NP)), idesc, ks > 0);
+                umma_commit(&bar[i & 1]);
+            }
         }
+        if (i >= 1 && i <= nt) {
+            const int e = i - 1;
+            if (!mbar_wait(&bar[e & 1], (unsigned)((e >> 1) & 1), kWaitLimit)) bad = true;
+            umma_fence_after();
+            float acc[P::NP];
+            const unsigned ta = tmem + ((unsigned)(32 * warp) << 16) + (unsigned)((e & 1) * P::NP);
+#pragma unroll
+            for (int c = 0; c < P::NP; c += 16) umma_ld16(ta + c, *reinterpret_cast<float(*)[16]>(acc + c));
+            umma_fence_before();
+            if (li_ep >= 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    ff x = combine3(ldexpf(acc[3 * g], E[g] - 10), ldexpf(acc[3 * g + 1], E[g] - 21),
+                                    ldexpf(acc[3 * g + 2], E[g] - 32));
+                    x = ff_mul(ff_mul_f(x, sc_ep), a.inv_sqrt_d);
+                    const int row = row_of(b, kv * G + g, a.Hq);
+                    tl[(int64_t)row * a.ws_n + li_ep] = make_float2(x.hi, x.lo);
+                    mloc[g] = fmaxf(mloc[g], x.hi);
+                }
+            }
+        }
+        li_ep = li_t;
+        sc_ep = sc_t;
+    };
+    for (int i = 0; i <= nt; i += 2) {
+        step(i, buf0, li0, sc0);
+        step(i + 1, buf1, li1, sc1);
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const float m = warp_max(mloc[g]);
-        if ((threadIdx.x & 31) == 0 && m > -INFINITY)
-            atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
+        if (lane == 0 && m > -INFINITY) atomicMax(&rows[row_of(b, kv * G + g, a.Hq)].m_tag, tag_max((unsigned)a.gen, m));
     }
+    if (bad) *(volatile int*)a.err = 1;
+    __syncthreads();
+    if (warp == 0) {
+        umma_fence_after();
+        umma_dealloc(tmem, P::COLS);
+    }
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kTile, kInt8CtasPerSm) score_int8_kernel(Views views, const float* __restrict__ q,
+                                                                            DecodeArgs a, RowState* __restrict__ rows,
+                                                                            float2* __restrict__ tl,
+                                                                            float2* __restrict__ th, int n_lchunks)
+{
+    pdl_trigger();   // the decision kernel may start its independent prologue
+    const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
+    const SlotView& V = views.v[b];
+    const int n = V.n;
+    const int ntiles = (n + 127) / 128;
+    const int per = (ntiles + n_lchunks - 1) / n_lchunks;
+    const int t0 = blockIdx.x * per, nt = min(ntiles, t0 + per) - t0;
+    if (nt > 0) score_int8_ltiles<T, G>(views, q, a, rows, tl, b, kv, t0, nt);
+    // the exact logits of the KV head's H tokens, shared out over its CTAs
+    constexpr int TPB = kTile / (8 * G);
+    const int nh_tiles = (V.counts[kv * 4 + 0] + TPB - 1) / TPB;
+    for (int ht = blockIdx.x; ht < nh_tiles; ht += gridDim.x) score_h_tile1<T, G>(views, q, a, rows, th, ht);
 }
 
 // Exact float-float dot product <q, k>/sqrt(d) of one key row (fp32 or bf16 elements).
@@ -2721,8 +2806,17 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
     // one launch scores L (sketch tiles) and H (exact tiles past them)
     const int h_tiles = (max_nh + kHTilesPerBlock * (kTile / (8 * G)) - 1) / (kHTilesPerBlock * (kTile / (8 * G)));
     if (cfg.sketch == VERKV_SKETCH_INT8) {
-        const int lt = (max_n + kTile * kInt8TokensPerThread<G> - 1) / (kTile * kInt8TokensPerThread<G>);
-        score_int8_kernel<T, G><<<dim3(lt + h_tiles, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl, ctx.th, lt);
+        static bool int8_attr = false;   // one per (T, G) instantiation
+        if (!int8_attr) {
+            VK_CUDA(cudaFuncSetAttribute(score_int8_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Int8Mma<G>::Smem));
+            int8_attr = true;
+        }
+        // CTAs per (sequence, KV head): about kInt8CtasPerSm per multiprocessor over the call
+        const int mt = (max_n + 127) / 128;
+        const int lt = std::max(1, std::min(mt, kInt8CtasPerSm * ctx.num_sms / (B * a.Hkv)));   // one wave
+        score_int8_kernel<T, G><<<dim3(lt, B * a.Hkv), kTile, Int8Mma<G>::Smem, st>>>(views, q, a, ctx.rows,
+                                                                                               ctx.tl, ctx.th, lt);
     } else if (cfg.sketch == VERKV_SKETCH_2BIT) {
         const int lt = ((max_n + kTile - 1) / kTile + kGroupsPerBlock - 1) / kGroupsPerBlock;
         score_2bit_kernel<T, G><<<dim3(lt + h_tiles, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl, ctx.th, lt);

@@ -37,6 +37,12 @@ __host__ __device__ constexpr unsigned umma_idesc_bf16_f32(int M, int N)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((unsigned)(N >> 3) << 17) | ((unsigned)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f16: fp16 A and B (K-major), fp32 D, M x N.
+__host__ __device__ constexpr unsigned umma_idesc_f16_f32(int M, int N)
+{
+    return (1u << 4) | ((unsigned)(N >> 3) << 17) | ((unsigned)(M >> 4) << 24);
+}
+
 // Start of K step ks (16 elements) of a tile laid out by umma_sw128_offset.
 __device__ __forceinline__ unsigned umma_kstep_offset(int ks, int rows)
 {
@@ -56,8 +62,9 @@ __device__ __forceinline__ void umma_dealloc(unsigned taddr, unsigned ncols)   /
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// D[tmem] (+)= A * B^T, one elected thread.
-__device__ __forceinline__ void umma_bf16(unsigned tmem_d, uint64_t adesc, uint64_t bdesc, unsigned idesc, bool acc)
+// D[tmem] (+)= A * B^T (kind::f16: the operand types are those of the instruction descriptor), one
+// elected thread.
+__device__ __forceinline__ void umma_mma(unsigned tmem_d, uint64_t adesc, uint64_t bdesc, unsigned idesc, bool acc)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
