@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--no-flush", action="store_true", help="(profiling runs) skip the L2 flushes")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the binary-shrinkage and batch-8 stack-layer measurements")
+    p.add_argument("--only-stack", action="store_true",
+                   help="(profiling runs) only the batch-8 stack-layer measurement, printed as one JSON line")
     return p.parse_args()
 
 
@@ -605,6 +607,22 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.only_stack:
+        import torch
+
+        from verified_kv_cache_gb300 import build
+        build.build()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        peaks = {}
+        pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+        if os.path.exists(pk):
+            with open(pk) as f:
+                peaks = json.load(f)
+        hbm = peaks.get("hbm_gbs")
+        print(json.dumps({"stack_layer_b8_int8": stack_run(args, dev, torch.cuda.current_stream(), hbm or 6800.0,
+                                                           "measured" if hbm else "fallback")}))
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
