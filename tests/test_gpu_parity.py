@@ -319,3 +319,90 @@ def test_qwen_layer_full_size(sketch):
     counts = _decode_parity(w, gc, osl, w.eps, w.delta, steps=range(4))
     print(sketch, counts)
     ctx.close()
+
+
+@pytest.mark.parametrize("sketch", ["int8", "2bit", "exact"])
+def test_gqa8_group(sketch):
+    """Eight query heads per KV head (the widest group built): the int8 scorer's tensor-core tile is
+    N = 32 (24 query pieces), the 2-bit and exact scorers their G = 8 variants."""
+    w = small_case(sketch, n=5000, n_kv=2, n_q=16, steps=2)
+    if sketch == "exact":
+        w.sketch = "exact"
+    ctx = make_lib_ctx(w)
+    gc = GpuCase(w, ctx)
+    tau, stats, osl = _compress_both(w, gc)
+    _decode_parity(w, gc, osl, w.eps, w.delta)
+    ctx.close()
+
+
+def test_batch_32_sequences():
+    """The largest batch built (32 sequences in one call), ragged lengths."""
+    from verified_kv_cache_gb300 import binding
+    B = 32
+    ws = [small_case("int8", n=1500 + 37 * i, seed=200 + i, steps=1, n_kv=2, n_q=8) for i in range(B)]
+    nmax = max(w.n for w in ws)
+    w0 = ws[0]
+    ctx = binding.VerKV(n_kv_heads=w0.n_kv, n_q_heads=w0.n_q, max_tokens=nmax, n_layers=1, n_seqs=B, max_batch=B,
+                        n_sink=w0.n_sink, n_local=w0.n_local, eta=w0.eta, seed=w0.seed, sketch="int8", kv_dtype="bf16")
+    slots, cases = [], []   # the cases own the pinned host K/V the library borrows until release
+    for i, w in enumerate(ws):
+        gc = GpuCase(w, ctx)
+        tau = oracle_tau(w, 0)
+        gc.compress(0, seq=i, tau=tau)
+        cases.append(gc)
+        slots.append(oracle_compress(w, 0, tau, layer=0, seq=i))
+    q = np.stack([w.queries[0, 0] for w in ws])
+    qt = torch.from_numpy(q).cuda()
+    out = torch.empty_like(qt)
+    ctx.decode(0, list(range(B)), qt, w0.eps, w0.delta, out)
+    torch.cuda.synchronize()
+    out = out.cpu().numpy()
+    trace = ctx.decode_trace(B * w0.n_q)
+    ok = 0
+    for i, w in enumerate(ws):
+        rows, unions = oracle_decode(w, 0, slots[i], w.queries[0, 0], w.eps, w.delta)
+        for hq in range(w.n_q):
+            v = check_row(trace[i * w.n_q + hq], ctx.exact_set(i, hq, w.n), rows[hq], w.eps, None)
+            if v == "ok":
+                ok += 1
+                assert rel_l2(out[i, hq].astype(np.float64), rows[hq]["out"]) <= REL_OUT
+    assert ok >= 0.95 * B * w0.n_q
+    ctx.close()
+
+
+def test_eta_one_keeps_every_token():
+    """eta = 1: every token has r = 1, L is empty, nothing is fetched and the output is the dense
+    softmax attention."""
+    w = small_case("int8", n=1000, steps=2, eta=1.0)
+    ctx = make_lib_ctx(w)
+    gc = GpuCase(w, ctx)
+    tau, stats, osl = _compress_both(w, gc)
+    assert all(s["n_l"] == 0 and s["n_h"] == w.n for s in stats)
+    for s in range(2):
+        out = gc.decode(w.queries[s], w.eps, w.delta)
+        trace = ctx.decode_trace(w.n_q)
+        for hq in range(w.n_q):
+            h = hq // w.group
+            assert trace[hq]["n_l"] == 0 and trace[hq]["kstar"] == 0 and trace[hq]["no_fetch"] == 1
+            assert trace[hq]["eps_hat"] == 0.0
+            K = torch.tensor(w.K[0, h], dtype=torch.float64)
+            V = torch.tensor(w.V[0, h], dtype=torch.float64)
+            qq = torch.tensor(w.queries[s, 0, hq], dtype=torch.float64)
+            dense = torch.nn.functional.scaled_dot_product_attention(qq[None, None, None], K[None, None],
+                                                                     V[None, None])[0, 0, 0].numpy()
+            assert rel_l2(out[0, hq].astype(np.float64), dense) <= REL_OUT
+        for h in range(w.n_kv):
+            assert len(ctx.fetch_set(0, h, w.n)) == 0
+    ctx.close()
+
+
+def test_smallest_context():
+    """n = sink + local + 3: three tokens share the budget left after the forced windows."""
+    w = workloads.qwen_layer_case(seed=13, n=4 + 64 + 3, n_kv=2, n_q=8, n_needles=0, W=8, steps=2, sketch="int8",
+                                  eta=0.98, eps=0.05, delta=0.05, n_sink=4, n_local=64, query_mode="random")
+    ctx = make_lib_ctx(w)
+    gc = GpuCase(w, ctx)
+    tau, stats, osl = _compress_both(w, gc)
+    _decode_parity(w, gc, osl, w.eps, w.delta)
+    _decode_parity(w, gc, osl, 0.0, w.delta)   # eps = 0: the whole of L is made exact
+    ctx.close()
