@@ -218,6 +218,25 @@ verkv_status verkv_get_exact_set(verkv_ctx* ctx, int32_t b, int32_t h, int32_t* 
 verkv_status verkv_get_fetch_set(verkv_ctx* ctx, int32_t b, int32_t kv_head, int32_t* tokens, int32_t cap,
                                  int32_t* count, verkv_stream stream);
 
+/* Rows of the last verkv_decode for KV head (b, kv_head): n_union = |the union of its query heads'
+ * L_g[:k*] \ S| (the rows the step needs beyond the resident ones), n_host = how many of them were read
+ * over the host link (the others came from the staging cache).  Either pointer may be NULL. */
+verkv_status verkv_get_fetch_stats(verkv_ctx* ctx, int32_t b, int32_t kv_head, int32_t* n_union, int32_t* n_host,
+                                   verkv_stream stream);
+
+/*
+ * Staging cache (the re-use of rows staged in earlier steps, Appendix A.3.2 "Fetching"): a row of
+ * L \ S that a decode reads over the host link is also written to device memory, and later decodes
+ * of the same slot read it from there.  The cache belongs to the (layer, sequence) slot and is emptied
+ * by verkv_compress and freed by verkv_release; the host cache it mirrors is unchanged while borrowed,
+ * so staged rows are exact copies.  rows_per_kv_head: -1 (default) = room for every row of L \ S of a
+ * head (512 B per row in bf16), 0 = off (every fetched row crosses the host link at every step),
+ * k > 0 = at most k rows per head, first fetched first kept, no eviction.  Takes effect at the next
+ * verkv_compress of a slot.  EINVAL: rows_per_kv_head < -1.  No counterpart in the algorithms
+ * themselves: results are identical with any setting.
+ */
+verkv_status verkv_set_stage_capacity(verkv_ctx* ctx, int64_t rows_per_kv_head);
+
 /* Sketch weights w^_i (fp32, in units of exp(-m)) of row (b, h) over L in
  * ascending token order, and those tokens. */
 verkv_status verkv_get_row_weights(verkv_ctx* ctx, int32_t b, int32_t h, float* w_hat, int32_t* tokens,

@@ -406,3 +406,33 @@ def test_smallest_context():
     _decode_parity(w, gc, osl, w.eps, w.delta)
     _decode_parity(w, gc, osl, 0.0, w.delta)   # eps = 0: the whole of L is made exact
     ctx.close()
+
+
+def test_staging_cache_reuses_fetched_rows():
+    """Rows fetched over the host link are staged in device memory and read from there by later
+    decodes of the slot: repeating a decode moves no row over the link and gives bit-identical
+    outputs; with staging off every needed row crosses the link each time; a capacity of k rows per
+    KV head keeps the first k fetched.  The outputs never depend on the setting."""
+    w = small_case("int8", n=6000, steps=2, query_mode="random")
+    outs = {}
+    for cap in [-1, 0, 10]:
+        ctx = make_lib_ctx(w)
+        ctx.set_stage_capacity(cap)
+        gc = GpuCase(w, ctx)
+        tau, stats, osl = _compress_both(w, gc)
+        first = gc.decode(w.queries[0], 0.01, 0.05)
+        s1 = [ctx.fetch_stats(0, h) for h in range(w.n_kv)]
+        assert all(nu > 0 and nh == nu for nu, nh in s1), s1
+        second = gc.decode(w.queries[0], 0.01, 0.05)
+        s2 = [ctx.fetch_stats(0, h) for h in range(w.n_kv)]
+        assert [nu for nu, _ in s2] == [nu for nu, _ in s1]
+        for (nu, nh) in s2:
+            expect = {-1: 0, 0: nu, 10: nu - min(10, nu)}[cap]
+            assert nh == expect, (cap, nu, nh)
+        assert np.array_equal(first.view(np.uint32), second.view(np.uint32))
+        outs[cap] = first
+        if cap == -1:
+            _decode_parity(w, gc, osl, 0.01, 0.05)   # both steps, the second partly from the cache
+        ctx.close()
+    assert np.array_equal(outs[-1].view(np.uint32), outs[0].view(np.uint32))
+    assert np.array_equal(outs[-1].view(np.uint32), outs[10].view(np.uint32))

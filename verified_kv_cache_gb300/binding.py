@@ -100,6 +100,10 @@ def lib():
     L.verkv_get_exact_set.restype = st
     L.verkv_get_fetch_set.argtypes = [P, i32, i32, P, i32, P, P]
     L.verkv_get_fetch_set.restype = st
+    L.verkv_get_fetch_stats.argtypes = [P, i32, i32, P, P, P]
+    L.verkv_get_fetch_stats.restype = st
+    L.verkv_set_stage_capacity.argtypes = [P, ctypes.c_int64]
+    L.verkv_set_stage_capacity.restype = st
     L.verkv_get_row_weights.argtypes = [P, i32, i32, P, P, i32, P, P]
     L.verkv_get_row_weights.restype = st
     L.verkv_last_launch_count.argtypes = [P]
@@ -245,6 +249,17 @@ class VerKV:
         cnt = ctypes.c_int32()
         self._check(lib().verkv_get_fetch_set(self.h, b, kv, out.ctypes.data, cap, ctypes.byref(cnt), _stream(stream)))
         return out[:min(cnt.value, cap)].copy()
+
+    def fetch_stats(self, b, kv, stream=None):
+        """(rows the last decode needed beyond the resident ones, rows it read over the host link) of KV
+        head (b, kv)."""
+        nu, nh = ctypes.c_int32(), ctypes.c_int32()
+        self._check(lib().verkv_get_fetch_stats(self.h, b, kv, ctypes.byref(nu), ctypes.byref(nh), _stream(stream)))
+        return nu.value, nh.value
+
+    def set_stage_capacity(self, rows_per_kv_head: int):
+        """Staging cache rows per KV head and slot: -1 = all of L minus S, 0 = off (next compress on)."""
+        self._check(lib().verkv_set_stage_capacity(self.h, int(rows_per_kv_head)))
 
     def row_weights(self, b, h, cap, stream=None):
         w = np.zeros(max(cap, 1), np.float32)

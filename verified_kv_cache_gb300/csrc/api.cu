@@ -31,7 +31,7 @@ verkv_status fail(Ctx& ctx, verkv_status s, const char* msg)
 void free_ws(Ctx& c)
 {
     void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.adone, c.ucount,
-                    c.part,
+                    c.part, c.hrows,
                     c.d_slot_n};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -67,6 +67,8 @@ verkv_status alloc_ws(Ctx& ctx)
     VK_CUDA(cudaMemset(ctx.adone, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.ucount, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMemset(ctx.ucount, 0, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMalloc(&ctx.hrows, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMemset(ctx.hrows, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.part, sizeof(float) * rows * ctx.nsplit * (kHeadDim + 2)));
     VK_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&ctx.h_err), sizeof(int), cudaHostAllocMapped));
     *ctx.h_err = 0;
@@ -366,6 +368,32 @@ verkv_status verkv_get_fetch_set(verkv_ctx* h, int32_t b, int32_t kv, int32_t* t
         VK_CUDA(cudaMemcpyAsync(tokens, ctx.ulist + (size_t)idx * ctx.ws_n, sizeof(int32_t) * m, cudaMemcpyDeviceToHost, st));
         VK_CUDA(cudaStreamSynchronize(st));
     }
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_fetch_stats(verkv_ctx* h, int32_t b, int32_t kv, int32_t* n_union, int32_t* n_host,
+                                   verkv_stream stream)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (b < 0 || b >= ctx.last_B || kv < 0 || kv >= ctx.cfg.n_kv_heads) return fail(ctx, VERKV_EINVAL, "row out of range");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int idx = b * ctx.cfg.n_kv_heads + kv;
+    int32_t v[2] = {0, 0};
+    VK_CUDA(cudaMemcpyAsync(&v[0], ctx.ucount + idx, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaMemcpyAsync(&v[1], ctx.hrows + idx, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaStreamSynchronize(st));
+    if (n_union) *n_union = v[0];
+    if (n_host) *n_host = v[1];
+    return VERKV_OK;
+}
+
+verkv_status verkv_set_stage_capacity(verkv_ctx* h, int64_t rows_per_kv_head)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (rows_per_kv_head < -1) return fail(ctx, VERKV_EINVAL, "staging capacity must be -1, 0 or positive");
+    ctx.stage_rows = rows_per_kv_head;
     return VERKV_OK;
 }
 

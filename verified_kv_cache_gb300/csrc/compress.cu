@@ -799,7 +799,8 @@ verkv_status run_sketch(Ctx& ctx, Slot& s, const T* kv, int n, cudaStream_t st)
 void free_slot(Slot& s)
 {
     void* ptrs[] = {s.tau, s.r, s.flags, s.lpos, s.ltok, s.rl, s.lslot, s.lq, s.rtok, s.hslot, s.counts, s.c, s.capped, s.kvres,
-                    s.res_off, s.codes8, s.scale8, s.codes2, s.zero2, s.scale2, s.pairs, s.energy, s.kexact};
+                    s.res_off, s.codes8, s.scale8, s.codes2, s.zero2, s.scale2, s.pairs, s.energy, s.kexact,
+                    s.stage_of, s.stage, s.stage_off, s.stage_cnt};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     s = Slot();
@@ -817,12 +818,17 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
         void* keep_res = s.kvres;
         int64_t* keep_off = s.res_off;
         const size_t keep_cap = s.cap_res;
+        void* keep_stage = s.stage;
+        const size_t keep_cap_stage = s.cap_stage;
         s.kvres = nullptr;
         s.res_off = nullptr;
+        s.stage = nullptr;
         free_slot(s);
         s.kvres = keep_res;
         s.res_off = keep_off;
         s.cap_res = keep_cap;
+        s.stage = keep_stage;
+        s.cap_stage = keep_cap_stage;
         const size_t hc = (size_t)Hkv * n;
         VK_CUDA(cudaMalloc(&s.tau, sizeof(float) * hc));
         VK_CUDA(cudaMalloc(&s.r, sizeof(float) * hc));
@@ -837,6 +843,9 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
         VK_CUDA(cudaMalloc(&s.counts, sizeof(int32_t) * Hkv * 4));
         VK_CUDA(cudaMalloc(&s.c, sizeof(double) * Hkv));
         VK_CUDA(cudaMalloc(&s.capped, sizeof(int32_t) * (Hkv + 1)));
+        VK_CUDA(cudaMalloc(&s.stage_of, sizeof(int32_t) * hc));
+        VK_CUDA(cudaMalloc(&s.stage_off, sizeof(int64_t) * (Hkv + 1)));
+        VK_CUDA(cudaMalloc(&s.stage_cnt, sizeof(int32_t) * Hkv));
         if (!s.res_off) VK_CUDA(cudaMalloc(&s.res_off, sizeof(int64_t) * (Hkv + 1)));
         if (cfg.sketch == VERKV_SKETCH_INT8) {
             VK_CUDA(cudaMalloc(&s.codes8, hc * kHeadDim));
@@ -905,6 +914,24 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
         VK_CUDA(cudaMalloc(&s.kvres, s.cap_res * row_bytes));
     }
     VK_CUDA(cudaMemcpyAsync(s.res_off, s.res_off_host.data(), sizeof(int64_t) * (Hkv + 1), cudaMemcpyHostToDevice, st));
+    // the staging cache starts empty: room for every row of L \ S of a head (or the set capacity)
+    s.stage_off_host.assign((size_t)Hkv + 1, 0);
+    for (int h = 0; h < Hkv; ++h) {
+        const int64_t fetchable = s.stats[h].n_l - s.stats[h].n_s;
+        const int64_t cap = ctx.stage_rows < 0 ? fetchable : std::min<int64_t>(ctx.stage_rows, fetchable);
+        s.stage_off_host[h + 1] = s.stage_off_host[h] + cap;
+    }
+    const size_t need_stage = (size_t)s.stage_off_host[Hkv];
+    if (need_stage > s.cap_stage) {
+        if (s.stage) VK_CUDA(cudaFree(s.stage));
+        s.stage = nullptr;
+        s.cap_stage = need_stage + need_stage / 8;
+        VK_CUDA(cudaMalloc(&s.stage, s.cap_stage * row_bytes));
+    }
+    VK_CUDA(cudaMemcpyAsync(s.stage_off, s.stage_off_host.data(), sizeof(int64_t) * (Hkv + 1), cudaMemcpyHostToDevice,
+                            st));
+    VK_CUDA(cudaMemsetAsync(s.stage_of, 0xff, sizeof(int32_t) * hn, st));
+    VK_CUDA(cudaMemsetAsync(s.stage_cnt, 0, sizeof(int32_t) * Hkv, st));
     if (max_res > 0) {
         gather_resident_kernel<<<dim3((max_res + 7) / 8, Hkv), 256, 0, st>>>(
             (const unsigned char*)kv, n, row_bytes, s.rtok, s.counts, s.res_off, (unsigned char*)s.kvres);

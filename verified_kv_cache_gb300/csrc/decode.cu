@@ -33,6 +33,7 @@ struct DecodeArgs {
     float* om;        // [B Hq][ws_n] weight factor of each resident slot (set by the scoring and decision kernels)
     int* err;         // mapped host word, set when a bounded device-side wait gives up
     int* done;        // [B Hkv] attention blocks finished per KV head (the last one merges; left at 0)
+    int32_t* hrows;   // [B Hkv] rows read over the host link (zeroed by the scoring kernel of the call)
     int Hkv, Hq, G, ws_n, ws_npow2, gen, nsplit;
     int binary;       // 1: binary shrinkage coefficients (lambda in {1, r}), 0: the clipped fixed point
     float eps_f;
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
                                                            float2* __restrict__ th, int n_ltiles)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
     if ((int)blockIdx.x >= n_ltiles) {
         score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
         return;
@@ -486,6 +488,7 @@ __global__ void __launch_bounds__(kTile, kInt8CtasPerSm) score_int8_kernel(Views
                                                                             float2* __restrict__ th, int n_lchunks)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
     const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
     const SlotView& V = views.v[b];
     const int n = V.n;
@@ -523,6 +526,7 @@ __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const f
                                                             float2* __restrict__ th, int n_ltiles)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
+    if (blockIdx.x == 0 && threadIdx.x == 0) a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
     if ((int)blockIdx.x >= n_ltiles) {
         score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
         return;
@@ -2429,6 +2433,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     __shared__ float s_corr[G], s_m[G], s_l[G];
     __shared__ int s_bad;
     __shared__ int s_scan[32];
+    __shared__ int s_sdst[NS][CR];   // staging-cache row to fill from a fetched row of the chunk (-1: none)
+    __shared__ int s_stok[NS][CR];   // its token
+    __shared__ int s_hcnt;           // rows this block read over the host link
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
     const SlotView& V = views.v[b];
@@ -2516,11 +2523,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     const unsigned char* host = reinterpret_cast<const unsigned char*>(V.kv_host) + (int64_t)kv * V.n * ROWB;
     const int32_t* ul = ulw;
     const uint8_t* um = umw;
+    // the staging cache of the KV head: token -> staged row, the rows, their capacity
+    int32_t* stg_of = V.stage_of ? V.stage_of + (int64_t)kv * V.n : nullptr;
+    unsigned char* stg = stg_of ? reinterpret_cast<unsigned char*>(V.stage) + V.stage_off[kv] * (int64_t)ROWB : nullptr;
+    const int stg_cap = stg_of ? (int)(V.stage_off[kv + 1] - V.stage_off[kv]) : 0;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_bad = 0;
+        s_hcnt = 0;
     }
     if (tid < G) {
         s_m[tid] = -INFINITY;
@@ -2528,20 +2540,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     }
     __syncthreads();
 
-    // tokens of the fetched rows of chunk k: lane l < CR / 8 of warp w holds the token of row w + 8 l
-    auto load_tok = [&](int k) -> int {
-        if (k >= nFc) return 0;
+    // tokens of the fetched rows of chunk k and their staged rows: lane l < CR / 8 of warp w holds
+    // those of row w + 8 l (staged row -1: not staged)
+    auto load_tok = [&](int k) -> int2 {
+        if (k >= nFc) return make_int2(0, -1);
         int r0, cnt;
         chunk(k, r0, cnt);
         const int row = warp + 8 * lane;
-        return (lane < CR / 8 && row < cnt) ? ul[r0 + row - m_res] : 0;
+        if (!(lane < CR / 8 && row < cnt)) return make_int2(0, -1);
+        const int tok = ul[r0 + row - m_res];
+        return make_int2(tok, stg_of ? stg_of[tok] : -1);
     };
     // chunk k into stage k % NS.  A chunk of resident rows only is one bulk copy (thread 0); a chunk
     // holding fetched rows is copied 16 bytes per lane with cp.async, one row per warp at a time, the
     // fetched rows straight from the pinned host cache over the host link.  Every thread commits one
     // copy group per call (empty when k is past the block's chunks) so that the group count stays in
     // step with the chunk count; the stage's mbarrier completes one phase per chunk either way.
-    auto issue = [&](int k, int tokreg) {
+    // A fetched row that is staged is read from the staging cache in device memory; one that is not
+    // crosses the host link and, while the cache has room, gets a staging row (filled once the chunk
+    // has landed).
+    auto issue = [&](int k, int2 tokreg) {
         if (k < nmine) {
             const int st = k % NS;
             int r0, cnt;
@@ -2556,12 +2574,28 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
                 }
             } else {
                 if (tid == 0) mbar_arrive(&full[st]);
+                const int myrow = warp + 8 * lane;
+                if (lane < CR / 8) {
+                    int sd = -1;
+                    if (myrow < cnt && tokreg.y < 0) {
+                        atomicAdd(&s_hcnt, 1);
+                        if (stg_of) {
+                            const int s_new = atomicAdd(&V.stage_cnt[kv], 1);
+                            sd = s_new < stg_cap ? s_new : -1;
+                        }
+                    }
+                    s_sdst[st][myrow] = sd;
+                    s_stok[st][myrow] = tokreg.x;
+                }
 #pragma unroll
                 for (int u = 0; u < CR / 8; ++u) {
                     const int row = warp + 8 * u, R = r0 + row;
-                    const int tok = __shfl_sync(0xffffffffu, tokreg, u);
+                    const int tok = __shfl_sync(0xffffffffu, tokreg.x, u);
+                    const int sidx = __shfl_sync(0xffffffffu, tokreg.y, u);
                     if (R < r1) {
-                        const unsigned char* src = R < m_res ? res + (int64_t)R * ROWB : host + (int64_t)tok * ROWB;
+                        const unsigned char* src = R < m_res ? res + (int64_t)R * ROWB
+                                                   : sidx >= 0 ? stg + (int64_t)sidx * ROWB
+                                                               : host + (int64_t)tok * ROWB;
 #pragma unroll
                         for (int p = lane; p < ROWB / 16; p += 32) cp_async16(dst + row * ROWB + p * 16, src + p * 16);
                     }
@@ -2594,7 +2628,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     };
 
     {
-        int tk[NS];
+        int2 tk[NS];
 #pragma unroll
         for (int k = 0; k < NS; ++k) tk[k] = load_tok(k);
 #pragma unroll
@@ -2615,13 +2649,28 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
         int r0, cnt;
         chunk(k, r0, cnt);
         if (k + 1 < nmine) load_om(k + 1, omv);   // stored at the end of this iteration
-        const int tnext = load_tok(k + NS);         // used when chunk k + NS is issued below
+        const int2 tnext = load_tok(k + NS);        // used when chunk k + NS is issued below
         __syncthreads();
         if (!mbar_wait(&full[st], (unsigned)((k / NS) & 1), kWaitLimit)) atomicOr(&s_bad, 1);
         cp_async_wait<NS - 1>();                    // this thread's copies of chunk k have landed
         __syncthreads();
         if (s_bad) break;
         const unsigned char* buf = sbuf + st * kAttnChunkBytes;
+        if (k < nFc && stg_of) {
+            // fill the staging rows given to this chunk's newly fetched rows (warp w: rows w + 8 u)
+#pragma unroll
+            for (int u = 0; u < CR / 8; ++u) {
+                const int row = warp + 8 * u;
+                const int sd = s_sdst[st][row];
+                if (row < cnt && sd >= 0) {
+                    unsigned char* drow = stg + (int64_t)sd * ROWB;
+#pragma unroll
+                    for (int p = lane; p < ROWB / 16; p += 32)
+                        *reinterpret_cast<uint4*>(drow + p * 16) = *reinterpret_cast<const uint4*>(buf + row * ROWB + p * 16);
+                    if (lane == 0) stg_of[s_stok[st][row]] = sd;
+                }
+            }
+        }
         // q.k: thread (row, slice); the 2G threads of a row are consecutive lanes
         for (int r = tid / NSL; r < CR; r += RSTEP) {
             float d[G];
@@ -2737,6 +2786,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     }
     // the last block of the KV head to finish merges the gridDim.y partials of its G query rows
     // (log-sum-exp over the splits); the counter is left at zero for the next call
+    if (tid == 0 && s_hcnt > 0) atomicAdd(&a.hrows[unit], s_hcnt);
     __shared__ int s_last;
     __shared__ float s_scl[G][kMaxSplit], s_lsp[G][kMaxSplit];
     __shared__ float s_L[G];
@@ -2976,6 +3026,11 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         v.scale2 = s.scale2;
         v.pairs = s.pairs;
         v.kexact = s.kexact;
+        const bool staged = !s.stage_off_host.empty() && s.stage_off_host.back() > 0;
+        v.stage_of = staged ? s.stage_of : nullptr;
+        v.stage = s.stage;
+        v.stage_off = s.stage_off;
+        v.stage_cnt = s.stage_cnt;
         max_n = std::max(max_n, s.n);
         for (const verkv_head_stats& hs : s.stats) {
             max_nl = std::max(max_nl, hs.n_l);
@@ -2999,6 +3054,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     a.om = ctx.om;
     a.err = ctx.d_err;
     a.done = ctx.adone;
+    a.hrows = ctx.hrows;
     // attention splits per KV head: about two blocks per SM over the whole call
     a.nsplit = std::min(std::min(ctx.nsplit, kMaxSplit), std::max(1, (2 * ctx.num_sms + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
     a.eps = eps;

@@ -46,6 +46,14 @@ struct Slot {
     double* energy = nullptr;   // [Hkv][d/2] pair energies (scratch of the 2-bit sketch)
     void* kexact = nullptr;     // [Hkv][n][d] keys for the exact sketch
 
+    // rows of L \ S fetched by earlier decodes, kept in device memory (the staging cache)
+    int32_t* stage_of = nullptr;   // [Hkv][n] token -> staged row of its head (-1: not staged)
+    void* stage = nullptr;         // [sum_h cap_h][2][d] staged K/V rows, head h from stage_off[h]
+    int64_t* stage_off = nullptr;  // device [Hkv + 1] row offsets into stage (cap_h = difference)
+    int32_t* stage_cnt = nullptr;  // [Hkv] rows staged so far
+    size_t cap_stage = 0;          // rows stage can hold
+    std::vector<int64_t> stage_off_host;
+
     std::vector<verkv_head_stats> stats;     // host copy
     std::vector<int64_t> res_off_host;       // host copy of res_off
 };
@@ -115,6 +123,8 @@ struct Ctx {
     float* part = nullptr;          // [rows][nsplit][d + 2] attention partials
     int nsplit = 128;               // largest split of the attention over blocks per KV head
     int num_sms = 152;              // multiprocessors of the context's device
+    int32_t* hrows = nullptr;       // [max_batch][Hkv] rows the last decode read over the host link
+    int64_t stage_rows = -1;        // staging capacity per KV head and slot: -1 = all of L \ S, 0 = off
     int* h_err = nullptr;           // mapped pinned host word: a device-side bounded wait gave up
     int* d_err = nullptr;           // its device address
 
@@ -152,6 +162,10 @@ struct SlotView {
     const __half* scale2;
     const int32_t* pairs;
     const void* kexact;
+    int32_t* stage_of;           // nullptr: staging off for this slot
+    void* stage;
+    const int64_t* stage_off;
+    int32_t* stage_cnt;
 };
 
 verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const void* kv_host, const void* kv_dev,
