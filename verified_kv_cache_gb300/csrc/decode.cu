@@ -1590,7 +1590,8 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             const int i = tid + k * T;
             rv[k] = i < ns ? rlr[i] : 0.f;
             qv[k] = i < ns ? lqr[i] : make_float2(0.f, 0.f);
-            tv[k] = i < ns ? tlr[i] : make_float2(0.f, 0.f);
+            // the scoring kernel's output (it may have been running when this grid started): through L2
+            tv[k] = i < ns ? __ldcg(tlr + i) : make_float2(0.f, 0.f);
         }
         m = untag_max(R.m_tag, (unsigned)a.gen);
 #pragma unroll
@@ -1614,7 +1615,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             for (int k0 = tid; k0 < nh; k0 += 4 * T) {
                 float2 hv[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) hv[u] = k0 + u * T < nh ? thr[k0 + u * T] : make_float2(-INFINITY, 0.f);
+                for (int u = 0; u < 4; ++u) hv[u] = k0 + u * T < nh ? __ldcg(thr + k0 + u * T) : make_float2(-INFINITY, 0.f);
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     if (k0 + u * T < nh) acc[1] = __fadd_rn(acc[1], weight_of(hv[u], m));
@@ -2413,6 +2414,7 @@ constexpr int kAttnThreads = 256;
 constexpr int kMaxSplit = 128;              // attention splits per KV head (partials merged per query row)
 template <typename T, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
+                                                            const RowState* rows,
                                                             int32_t* __restrict__ ucount, int32_t* __restrict__ ulist,
                                                             uint8_t* __restrict__ umask, float* __restrict__ part,
                                                             int* __restrict__ done, float* __restrict__ out)
@@ -2444,7 +2446,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     int32_t* ulw = ulist + (int64_t)unit * a.ws_n;
     uint8_t* umw = umask + (int64_t)unit * a.ws_n;
     // D7: the fetched rows of the KV head are the union of its G rows' L_g[:k*] \ S bitmaps, in
-    // ascending tokens.  Every block counts all the words (thread t a contiguous run); the positions
+    // ascending tokens (no scan when none of the G rows fetches).  Every block counts all the words (thread t a contiguous run); the positions
     // of its own share below are written, with the mask of the heads holding each token, into the
     // fetch list, which the chunk copies read back.  Block 0 writes the count.
     // q slice of this thread (pre-scaled by 1/sqrt(d)), all G heads
@@ -2455,9 +2457,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
 #pragma unroll
         for (int c = 0; c < QS; ++c) qr[g][c] = q[(int64_t)(row0 + g) * kHeadDim + sl * QS + c] * a.inv_sqrt_d_f;
 
-    int nu;
+    int nu = 0;
     pdl_wait();   // the decision kernel's bitmaps and weight factors are complete (the query is an input)
-    {
+    // the bitmaps are scanned only when a query row of the KV head fetches.  The counts come from the
+    // decision kernel, which may still have been running when this grid started (programmatic launch):
+    // they are read through L2, never through the non-coherent read-only path.
+    int any_fetch = 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g) any_fetch |= __ldcg(&rows[row0 + g].n_fetch);
+    if (!any_fetch) {
+        if (blockIdx.y == 0 && tid == 0) ucount[unit] = 0;
+    } else {
         const int64_t stride = a.ws_n / 32 + 1;
         const uint32_t* eb = a.ebits + (int64_t)row0 * stride;
         const int nwords = (V.n + 31) / 32;
@@ -2936,7 +2946,8 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         lc.attrs = attr;
         lc.numAttrs = 1;
-        VK_CUDA(cudaLaunchKernelEx(&lc, attn_kernel<T, G>, views, q, a, ctx.ucount, ctx.ulist, ctx.umask, ctx.part,
+        VK_CUDA(cudaLaunchKernelEx(&lc, attn_kernel<T, G>, views, q, a, (const RowState*)ctx.rows, ctx.ucount, ctx.ulist,
+                                   ctx.umask, ctx.part,
                                    a.done, out));
     }
     VK_LAUNCHED("attn");
