@@ -207,6 +207,10 @@ def run_verkv(args):
             events.append(("decode", a, b))
         return stats, n_launch
 
+    # the clock sampler starts before the warm-up: its start-up (driver attach) must not fall in the
+    # timed region, where it stalled one host-synchronous compress by several milliseconds
+    clocks = Clocks(dev.index or 0) if rank == 0 else None
+    time.sleep(0.5)
     # warm-up
     for _ in range(max(args.warmup, 0)):
         one_step([])
@@ -228,7 +232,6 @@ def run_verkv(args):
 
     # timed region: per-call events only (events between the kernels of a call would stop the
     # programmatic launch overlap of the decode kernels)
-    clocks = Clocks(dev.index or 0) if rank == 0 else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
