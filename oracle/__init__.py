@@ -3,7 +3,7 @@
 Plain double-precision CPU restatement of "Verify Before You Fetch: Reliable
 KV Cache Compression for LLM Inference" (PoissonComp: Algorithm 1, eq. (3);
 KVFetch: Algorithm 2, Definition 2 / eq. (5), Lemma 1 / eq. (7), eqs. (9)-(10);
-binary shrinkage: Appendix A.2; key sketch: Appendix A.1).  The arithmetic lives in ``verkv_oracle.c``; this
+binary shrinkage: Appendix A.2; key sketch and shortlist: Appendix A.1).  The arithmetic lives in ``verkv_oracle.c``; this
 module compiles it with gcc and wraps it for numpy arrays.
 
 Only the tests, the package smoke check and the benchmark's CPU-baseline leg
@@ -78,7 +78,9 @@ def lib():
             L.vko_beta_breakpoints.restype = f64
             L.vko_kvfetch_row.argtypes = [i64, P, P, P, P, f64, f64, i32, P, P, P, P, P, P]
             L.vko_kvfetch_row.restype = i32
-            L.vko_kvfetch_row_ex.argtypes = [i64, P, P, P, P, f64, f64, i32, i32, P, P, P, P, P, P]
+            L.vko_kvfetch_row_ex.argtypes = [i64, P, P, P, P, P, f64, f64, i32, i32, P, P, P, P, P, P]
+            L.vko_shortlist.argtypes = [i64, i32, P, P, i64, P]
+            L.vko_shortlist.restype = i64
             L.vko_kvfetch_row_ex.restype = i32
             L.vko_binary_shrinkage.argtypes = [i64, P, P, P, P]
             L.vko_binary_shrinkage.restype = f64
@@ -225,9 +227,22 @@ def binary_shrinkage(w, r):
     return lam, beta, ns.value
 
 
-def kvfetch_row(flags, r32, t_exact, t_sketch, eps: float, delta: float, mode: int = 1, shrinkage: int = 0):
+def shortlist(flags, t_sketch_rows, k: int):
+    """Appendix A.1 shortlist of one KV head: boolean mask of the k non-resident tokens of L with the
+    largest sketch logit over the head's query rows (t_sketch_rows: [G, n]; ties: lower index)."""
+    flags = _c(flags, np.uint8)
+    ts = _c(t_sketch_rows, np.float64)
+    G, n = ts.shape
+    mask = np.zeros(n, np.uint8)
+    lib().vko_shortlist(n, G, _p(flags), _p(ts), int(k), _p(mask))
+    return mask.astype(bool)
+
+
+def kvfetch_row(flags, r32, t_exact, t_sketch, eps: float, delta: float, mode: int = 1, shrinkage: int = 0,
+                use_exact=None):
     """One query row of Algorithm 2.  Returns dict with cert scalars and arrays.
-    shrinkage: 0 = the clipped coefficients of Definition 2, 1 = binary (Appendix A.2)."""
+    shrinkage: 0 = the clipped coefficients of Definition 2, 1 = binary (Appendix A.2).
+    use_exact: optional boolean mask of tokens of L whose exact logit replaces the sketch logit."""
     flags = _c(flags, np.uint8)
     r32 = _c(r32, np.float32)
     te = _c(t_exact, np.float64)
@@ -240,8 +255,10 @@ def kvfetch_row(flags, r32, t_exact, t_sketch, eps: float, delta: float, mode: i
     order = np.zeros(max(n_l, 1), np.int64)
     mask = np.zeros(n, np.uint8)
     resid = np.full(n_l + 1, np.nan)
-    lib().vko_kvfetch_row_ex(n, _p(flags), _p(r32), _p(te), _p(ts), float(eps), float(delta), int(mode),
-                             int(shrinkage), ctypes.byref(cert), _p(lam), _p(gain), _p(order), _p(mask), _p(resid))
+    ue = None if use_exact is None else _c(np.asarray(use_exact).astype(np.uint8), np.uint8)
+    lib().vko_kvfetch_row_ex(n, _p(flags), _p(r32), _p(te), _p(ts), None if ue is None else _p(ue), float(eps),
+                             float(delta), int(mode), int(shrinkage), ctypes.byref(cert), _p(lam), _p(gain), _p(order),
+                             _p(mask), _p(resid))
     out = cert.as_dict()
     out.update(lam=lam, gain=gain, order=order[:n_l], exact_mask=mask.astype(bool), resid=resid)
     return out

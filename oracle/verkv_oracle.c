@@ -5,8 +5,8 @@
  * "Verify Before You Fetch: Reliable KV Cache Compression for LLM Inference"
  * (PoissonComp, Algorithm 1 and Sec. 4.1, eq. (3); KVFetch, Algorithm 2 and
  * Sec. 4.2, Definition 2 / eq. (5), Theorem 1 / eq. (6), Lemma 1 / eq. (7),
- * eqs. (9)-(10), Theorem 2; binary shrinkage, Appendix A.2; key sketch,
- * Appendix A.1).
+ * eqs. (9)-(10), Theorem 2; binary shrinkage, Appendix A.2; key sketch and
+ * shortlist, Appendix A.1).
  *
  * Only the test-suite, the package smoke check and the CPU-baseline leg of
  * the benchmark may load this library.  It shares no code with the CUDA
@@ -546,27 +546,32 @@ static int cmp_gain(const void* a, const void* b)
  * Returns 0.
  */
 int vko_kvfetch_row_ex(int64_t n, const uint8_t* flags, const float* r32, const double* t_exact,
-                       const double* t_sketch, double eps, double delta, int mode, int shrinkage, vko_cert* cert,
-                       double* lambda, double* gain, int64_t* order, uint8_t* exact_mask, double* resid);
+                       const double* t_sketch, const uint8_t* use_exact, double eps, double delta, int mode,
+                       int shrinkage, vko_cert* cert, double* lambda, double* gain, int64_t* order,
+                       uint8_t* exact_mask, double* resid);
 
 int vko_kvfetch_row(int64_t n, const uint8_t* flags, const float* r32, const double* t_exact,
                     const double* t_sketch, double eps, double delta, int mode, vko_cert* cert,
                     double* lambda, double* gain, int64_t* order, uint8_t* exact_mask, double* resid)
 {
-    return vko_kvfetch_row_ex(n, flags, r32, t_exact, t_sketch, eps, delta, mode, 0, cert, lambda, gain, order,
-                              exact_mask, resid);
+    return vko_kvfetch_row_ex(n, flags, r32, t_exact, t_sketch, NULL, eps, delta, mode, 0, cert, lambda, gain,
+                              order, exact_mask, resid);
 }
 
-/* shrinkage: 0 = the clipped coefficients of Definition 2, 1 = binary (App. A.2). */
+/* shrinkage: 0 = the clipped coefficients of Definition 2, 1 = binary (App. A.2).
+ * use_exact[n] (or NULL): tokens of L whose exact logit replaces the sketch logit in every quantity of
+ * the decision (App. A.1: resident and shortlisted tokens). */
 int vko_kvfetch_row_ex(int64_t n, const uint8_t* flags, const float* r32, const double* t_exact,
-                       const double* t_sketch, double eps, double delta, int mode, int shrinkage, vko_cert* cert,
-                       double* lambda, double* gain, int64_t* order, uint8_t* exact_mask, double* resid)
+                       const double* t_sketch, const uint8_t* use_exact, double eps, double delta, int mode,
+                       int shrinkage, vko_cert* cert, double* lambda, double* gain, int64_t* order,
+                       uint8_t* exact_mask, double* resid)
 {
     int64_t nl = 0;
     double m = -INFINITY;
+#define VKO_T_OF(i) ((use_exact && use_exact[i]) ? t_exact[i] : t_sketch[i])
     for (int64_t i = 0; i < n; ++i) {
         if (flags[i] == 2) { if (t_exact[i] > m) m = t_exact[i]; }
-        else { ++nl; if (t_sketch[i] > m) m = t_sketch[i]; }
+        else { ++nl; if (VKO_T_OF(i) > m) m = VKO_T_OF(i); }
     }
     int64_t* lidx = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nl + 1));
     double* w = (double*)malloc(sizeof(double) * (size_t)(nl + 1));
@@ -577,7 +582,7 @@ int vko_kvfetch_row_ex(int64_t n, const uint8_t* flags, const float* r32, const 
         if (flags[i] == 2) D += exp(t_exact[i] - m);
         else {
             lidx[k] = i;
-            w[k] = exp(t_sketch[i] - m);
+            w[k] = exp(VKO_T_OF(i) - m);
             r[k] = (double)r32[i];
             D += w[k];
             ++k;
@@ -741,6 +746,44 @@ void vko_attention_row(int64_t n, int d, const uint8_t* flags, const float* r32,
 /* Batched driver for the CPU baseline: independent rows in parallel.       */
 /* Row u uses flags/r32 of kv row kv_of[u] and logits rows u.                */
 /* ------------------------------------------------------------------------ */
+/* ------------------------------------------------------------------------ */
+/* Shortlist ("Verify Before You Fetch", App. A.1): among the non-resident  */
+/* tokens of L (flags 0) of one KV head, the k with the largest sketch      */
+/* score over the head's G query rows (score = the largest sketch logit of  */
+/* the token over the rows; ties: lower token index).  t_sketch is [G][n].  */
+/* Sets mask[i] = 1 for them (mask is not cleared); returns how many.       */
+/* ------------------------------------------------------------------------ */
+static _Thread_local const double* g_sort_score;
+static int cmp_score_desc(const void* a, const void* b)
+{
+    int64_t ia = *(const int64_t*)a, ib = *(const int64_t*)b;
+    double sa = g_sort_score[ia], sb = g_sort_score[ib];
+    if (sa > sb) return -1;
+    if (sa < sb) return 1;
+    return (ia < ib) ? -1 : (ia > ib);
+}
+
+int64_t vko_shortlist(int64_t n, int G, const uint8_t* flags, const double* t_sketch, int64_t k, uint8_t* mask)
+{
+    double* score = (double*)malloc(sizeof(double) * (size_t)(n + 1));
+    int64_t* cand = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+    int64_t nc = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        double sc = -INFINITY;
+        for (int g = 0; g < G; ++g)
+            if (t_sketch[(int64_t)g * n + i] > sc) sc = t_sketch[(int64_t)g * n + i];
+        score[i] = sc;
+        if (flags[i] == 0) cand[nc++] = i;
+    }
+    g_sort_score = score;
+    qsort(cand, (size_t)nc, sizeof(int64_t), cmp_score_desc);
+    const int64_t take = k < nc ? k : nc;
+    for (int64_t j = 0; j < take; ++j) mask[cand[j]] = 1;
+    free(score);
+    free(cand);
+    return take;
+}
+
 int vko_kvfetch_rows(int64_t rows, int64_t n, const uint8_t* flags, const float* r32, const int32_t* kv_of,
                      const double* t_exact, const double* t_sketch, double eps, double delta, int mode,
                      int shrinkage, vko_cert* certs, uint8_t* exact_masks, int threads)
@@ -751,8 +794,9 @@ int vko_kvfetch_rows(int64_t rows, int64_t n, const uint8_t* flags, const float*
 #endif
     for (int64_t u = 0; u < rows; ++u) {
         const int64_t kv = kv_of[u];
-        vko_kvfetch_row_ex(n, flags + kv * n, r32 + kv * n, t_exact + u * n, t_sketch + u * n, eps, delta, mode,
-                           shrinkage, certs + u, NULL, NULL, NULL, exact_masks ? exact_masks + u * n : NULL, NULL);
+        vko_kvfetch_row_ex(n, flags + kv * n, r32 + kv * n, t_exact + u * n, t_sketch + u * n, NULL, eps, delta,
+                           mode, shrinkage, certs + u, NULL, NULL, NULL, exact_masks ? exact_masks + u * n : NULL,
+                           NULL);
     }
     return 0;
 }

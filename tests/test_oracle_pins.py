@@ -484,6 +484,51 @@ def test_binary_shrinkage_certificate_coverage_and_fetch():
         assert fail_fetch <= delta + 1e-12
 
 
+# ----------------------------------------------------------------------------- shortlist (App. A.1)
+def test_shortlist_is_top_k_of_the_largest_sketch_logit():
+    """The shortlist of a KV head: among tokens of L outside the sample (flags 0), the k with the
+    largest sketch logit over the head's query rows, ties by lower index -- against a plain sort."""
+    rng = np.random.default_rng(91)
+    for trial in range(20):
+        n, G, k = int(rng.integers(5, 400)), int(rng.choice([1, 2, 4, 8])), int(rng.integers(0, 150))
+        flags = rng.choice([0, 1, 2], size=n, p=[0.6, 0.2, 0.2]).astype(np.uint8)
+        ts = np.round(rng.standard_normal((G, n)) * 3, 1)   # coarse values: ties occur
+        got = oracle.shortlist(flags, ts, k)
+        score = ts.max(axis=0)
+        cand = np.nonzero(flags == 0)[0]
+        order = cand[np.lexsort((cand, -score[cand]))]
+        want = np.zeros(n, bool)
+        want[order[:k]] = True
+        assert np.array_equal(got, want)
+
+
+def test_exact_weight_mask_reductions():
+    """App. A.1's certificate weights: exact logits where the mask is set, sketch logits elsewhere.
+    With an exact sketch the mask changes nothing; a mask over all of L equals the exact sketch; and D
+    is sum_H w + sum_L of the chosen weights."""
+    rng = np.random.default_rng(92)
+    for trial in range(12):
+        L = int(rng.integers(2, 60))
+        flags, r32, t = _tiny_row(rng, L, H=3)
+        ts = t + rng.standard_normal(len(t)) * 0.4
+        mask = (rng.random(len(t)) < 0.4) & (flags != 2)
+        eps, delta = float(rng.choice([0.01, 0.05])), 0.1
+        a = oracle.kvfetch_row(flags, r32, t, t, eps, delta)
+        b = oracle.kvfetch_row(flags, r32, t, t, eps, delta, use_exact=mask)
+        for key in ["D", "beta", "eps_hat", "kstar"]:
+            assert a[key] == b[key]
+        assert np.array_equal(a["exact_mask"], b["exact_mask"])
+        c = oracle.kvfetch_row(flags, r32, t, ts, eps, delta, use_exact=flags != 2)
+        for key in ["D", "beta", "eps_hat", "kstar"]:
+            assert c[key] == a[key]
+        d = oracle.kvfetch_row(flags, r32, t, ts, eps, delta, use_exact=mask)
+        Lm = flags != 2
+        used = np.where(mask, t, ts)
+        m = max(t[~Lm].max(), used[Lm].max())
+        D = np.exp(t[~Lm] - m).sum() + np.exp(used[Lm] - m).sum()
+        assert math.isclose(d["D"], D, rel_tol=1e-12)
+
+
 # ----------------------------------------------------------------------------- certificate / fetch (Lemma 1, Thm. 2)
 def _tiny_row(rng, L, H=2):
     n = L + H
