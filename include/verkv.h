@@ -237,6 +237,21 @@ verkv_status verkv_get_fetch_stats(verkv_ctx* ctx, int32_t b, int32_t kv_head, i
  */
 verkv_status verkv_set_stage_capacity(verkv_ctx* ctx, int64_t rows_per_kv_head);
 
+/*
+ * Shortlist (Appendix A.1): at every decode, among the tokens of L outside the sample, the k of each KV
+ * head with the largest sketch logit over the head's query rows (ties: lower token index) have their
+ * keys read from the pinned host cache and scored exactly, and the decision (beta, eq. (7), gains,
+ * k*) uses exact weights for them and for the sampled (resident) tokens, sketch weights for the rest
+ * of L.  k = 0 (default) keeps sketch weights on all of L.  Takes effect at the next verkv_decode.
+ * EINVAL: k outside [0, 1024].
+ */
+verkv_status verkv_set_shortlist(verkv_ctx* ctx, int32_t k);
+
+/* The shortlist of KV head (b, kv_head) in the last verkv_decode (ascending tokens; count 0 when the
+ * shortlist is off).  At most `cap` tokens are written. */
+verkv_status verkv_get_shortlist(verkv_ctx* ctx, int32_t b, int32_t kv_head, int32_t* tokens, int32_t cap,
+                                 int32_t* count, verkv_stream stream);
+
 /* Sketch weights w^_i (fp32, in units of exp(-m)) of row (b, h) over L in
  * ascending token order, and those tokens. */
 verkv_status verkv_get_row_weights(verkv_ctx* ctx, int32_t b, int32_t h, float* w_hat, int32_t* tokens,

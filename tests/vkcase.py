@@ -70,20 +70,37 @@ def oracle_sketch_logits(w, b, h, q, slot: OracleSlot):
     return oracle.logits_2bit(q, pairs, codes, zero, scale)
 
 
-def oracle_decode(w, b, slot: OracleSlot, q_bh: np.ndarray, eps, delta, mode=1, shrinkage=0):
+def oracle_decode(w, b, slot: OracleSlot, q_bh: np.ndarray, eps, delta, mode=1, shrinkage=0, shortlist=0):
     """q_bh: [Hq, d] for sequence b.  Returns per row dicts and per KV head fetch unions and outputs.
-    shrinkage: 0 = clipped coefficients (Definition 2), 1 = binary (Appendix A.2)."""
+    shrinkage: 0 = clipped coefficients (Definition 2), 1 = binary (Appendix A.2).
+    shortlist: k > 0 uses exact weights for the sampled tokens and the Appendix A.1 shortlist of k
+    tokens per KV head (each row dict then carries the head's shortlist mask and scores)."""
     G = w.group
     rows = []
+    logits = {}
+    for hq in range(w.n_q):
+        q = q_bh[hq].astype(np.float64)
+        h = hq // G
+        logits[hq] = (oracle.logits_exact(q, w.K[b, h]), oracle_sketch_logits(w, b, h, q, slot))
+    masks = {}
+    if shortlist > 0:
+        for h in range(w.n_kv):
+            ts_rows = np.stack([logits[h * G + g][1] for g in range(G)])
+            sl = oracle.shortlist(slot.flags[h], ts_rows, shortlist)
+            masks[h] = (sl, ts_rows.max(axis=0))
     for hq in range(w.n_q):
         h = hq // G
-        q = q_bh[hq].astype(np.float64)
-        te = oracle.logits_exact(q, w.K[b, h])
-        ts = oracle_sketch_logits(w, b, h, q, slot)
-        res = oracle.kvfetch_row(slot.flags[h], slot.r32[h], te, ts, eps, delta, mode=mode, shrinkage=shrinkage)
+        te, ts = logits[hq]
+        use = None
+        if shortlist > 0:
+            use = masks[h][0] | (slot.flags[h] == 1)
+        res = oracle.kvfetch_row(slot.flags[h], slot.r32[h], te, ts, eps, delta, mode=mode, shrinkage=shrinkage,
+                                 use_exact=use)
+        if shortlist > 0:
+            res["shortlist"], res["sl_score"] = masks[h]
         if shrinkage == 1:
             Lm = slot.flags[h] != 2
-            res["w_l"] = np.exp(ts[Lm] - res["m"])
+            res["w_l"] = np.exp((ts if use is None else np.where(use, te, ts))[Lm] - res["m"])
             res["r_l"] = slot.r32[h][Lm].astype(np.float64)
             res["n_shrunk"] = int((res["lam"][Lm] < 1.0).sum())
         res["out"] = oracle.attention_row(slot.flags[h], slot.r32[h], te, w.V[b, h], res["lam"], res["exact_mask"])

@@ -102,6 +102,10 @@ def lib():
     L.verkv_get_fetch_set.restype = st
     L.verkv_get_fetch_stats.argtypes = [P, i32, i32, P, P, P]
     L.verkv_get_fetch_stats.restype = st
+    L.verkv_set_shortlist.argtypes = [P, i32]
+    L.verkv_set_shortlist.restype = st
+    L.verkv_get_shortlist.argtypes = [P, i32, i32, P, i32, P, P]
+    L.verkv_get_shortlist.restype = st
     L.verkv_set_stage_capacity.argtypes = [P, ctypes.c_int64]
     L.verkv_set_stage_capacity.restype = st
     L.verkv_get_row_weights.argtypes = [P, i32, i32, P, P, i32, P, P]
@@ -256,6 +260,16 @@ class VerKV:
         nu, nh = ctypes.c_int32(), ctypes.c_int32()
         self._check(lib().verkv_get_fetch_stats(self.h, b, kv, ctypes.byref(nu), ctypes.byref(nh), _stream(stream)))
         return nu.value, nh.value
+
+    def set_shortlist(self, k: int):
+        """Appendix A.1 shortlist of k tokens per KV head scored exactly (0: off)."""
+        self._check(lib().verkv_set_shortlist(self.h, int(k)))
+
+    def shortlist(self, b, kv, cap=1024, stream=None):
+        out = np.zeros(max(cap, 1), np.int32)
+        cnt = ctypes.c_int32()
+        self._check(lib().verkv_get_shortlist(self.h, b, kv, out.ctypes.data, cap, ctypes.byref(cnt), _stream(stream)))
+        return out[:min(cnt.value, cap)].copy()
 
     def set_stage_capacity(self, rows_per_kv_head: int):
         """Staging cache rows per KV head and slot: -1 = all of L minus S, 0 = off (next compress on)."""

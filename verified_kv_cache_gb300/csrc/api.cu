@@ -31,7 +31,7 @@ verkv_status fail(Ctx& ctx, verkv_status s, const char* msg)
 void free_ws(Ctx& c)
 {
     void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.adone, c.ucount,
-                    c.part, c.hrows,
+                    c.part, c.hrows, c.slist, c.scount,
                     c.d_slot_n};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -69,6 +69,9 @@ verkv_status alloc_ws(Ctx& ctx)
     VK_CUDA(cudaMemset(ctx.ucount, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.hrows, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMemset(ctx.hrows, 0, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMalloc(&ctx.slist, sizeof(int32_t) * kvb * kMaxShortlist));
+    VK_CUDA(cudaMalloc(&ctx.scount, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMemset(ctx.scount, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.part, sizeof(float) * rows * ctx.nsplit * (kHeadDim + 2)));
     VK_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&ctx.h_err), sizeof(int), cudaHostAllocMapped));
     *ctx.h_err = 0;
@@ -385,6 +388,46 @@ verkv_status verkv_get_fetch_stats(verkv_ctx* h, int32_t b, int32_t kv, int32_t*
     VK_CUDA(cudaStreamSynchronize(st));
     if (n_union) *n_union = v[0];
     if (n_host) *n_host = v[1];
+    return VERKV_OK;
+}
+
+verkv_status verkv_set_shortlist(verkv_ctx* h, int32_t k)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (k < 0 || k > kMaxShortlist) return fail(ctx, VERKV_EINVAL, "shortlist size must be in [0, 1024]");
+    ctx.shortlist_k = k;
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_shortlist(verkv_ctx* h, int32_t b, int32_t kv, int32_t* tokens, int32_t cap, int32_t* count,
+                                 verkv_stream stream)
+{
+    if (!h || !count) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (b < 0 || b >= ctx.last_B || kv < 0 || kv >= ctx.cfg.n_kv_heads) return fail(ctx, VERKV_EINVAL, "row out of range");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int idx = b * ctx.cfg.n_kv_heads + kv;
+    int cnt = 0;
+    if (ctx.shortlist_k > 0) {
+        VK_CUDA(cudaMemcpyAsync(&cnt, ctx.scount + idx, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+        VK_CUDA(cudaStreamSynchronize(st));
+    }
+    *count = cnt;
+    const int m = std::min(cnt, cap);
+    if (tokens && m > 0) {
+        std::vector<int32_t> li(m);
+        VK_CUDA(cudaMemcpyAsync(li.data(), ctx.slist + (size_t)idx * kMaxShortlist, sizeof(int32_t) * m,
+                                cudaMemcpyDeviceToHost, st));
+        Slot& s = ctx.slot(ctx.last_layer, ctx.last_seq[b]);
+        std::vector<int32_t> ltok((size_t)s.stats[kv].n_l);
+        if (!ltok.empty())
+            VK_CUDA(cudaMemcpyAsync(ltok.data(), s.ltok + (size_t)kv * s.n, sizeof(int32_t) * ltok.size(),
+                                    cudaMemcpyDeviceToHost, st));
+        VK_CUDA(cudaStreamSynchronize(st));
+        for (int i = 0; i < m; ++i) tokens[i] = ltok[li[i]];
+        std::sort(tokens, tokens + m);
+    }
     return VERKV_OK;
 }
 

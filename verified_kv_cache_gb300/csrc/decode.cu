@@ -519,6 +519,168 @@ __device__ __forceinline__ ff exact_logit(const float* __restrict__ q, const T* 
     return ff_mul(acc, inv_sqrt_d);
 }
 
+// --------------------------------------------------------------------------------------------
+// Shortlist and exact certificate weights (App. A.1; launched only when enabled).  Blocks y >= 1 of
+// a (sequence, KV head) replace the sketch logits of the sampled tokens (their keys are resident) by
+// exact ones.  Block 0 selects the shortlist: among the tokens of L outside the sample, the k whose
+// largest sketch logit over the head's G query rows is largest, ties by lower L index (token order).
+// The k-th key is found by a radix select over the order-preserving bits of that score (levels of
+// 12, 12 and 8 bits, histograms in shared memory); the tokens above it are taken, and of those at
+// its value the first in L order.  Their keys are then read from the pinned host cache and scored
+// exactly.  Every exact logit also raises its row's maximum.  The two kinds of blocks touch
+// disjoint entries of the logit rows.
+// --------------------------------------------------------------------------------------------
+constexpr int kSlThreads = 512;
+
+__device__ __forceinline__ unsigned score_key(float s)   // ascending key = descending score
+{
+    return ~((unsigned)float_to_ordered(s) ^ 0x80000000u);
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
+                                                              RowState* rows, float2* tl, int k_short,
+                                                              int32_t* __restrict__ slist, int32_t* __restrict__ scount)
+{
+    const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
+    const SlotView& V = views.v[b];
+    const int n = V.n;
+    const int nl = V.counts[kv * 4 + 1];
+    const int row0 = row_of(b, kv * G, a.Hq);
+    const int tid = threadIdx.x, lane = tid & 31;
+    float mloc[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
+    if (blockIdx.y > 0) {
+        // sampled tokens: resident slot rs -> token -> L index (H tokens have none)
+        const int m_res = V.counts[kv * 4 + 3];
+        const int rs = (blockIdx.y - 1) * kSlThreads + tid;
+        if (rs < m_res) {
+            const int tok = V.rtok[(int64_t)kv * n + rs];
+            const int li = V.lpos[(int64_t)kv * n + tok];
+            if (li >= 0) {
+                const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + rs) * 2 * kHeadDim;
+#pragma unroll 1
+                for (int g = 0; g < G; ++g) {
+                    const ff x = exact_logit<T>(q + (int64_t)(row0 + g) * kHeadDim, key, a.inv_sqrt_d);
+                    tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x.hi, x.lo);
+                    mloc[g] = fmaxf(mloc[g], x.hi);
+                }
+            }
+        }
+    } else {
+        __shared__ unsigned hist[4096];
+        __shared__ int s_scan[32];
+        __shared__ unsigned s_prefix;
+        __shared__ int s_need, s_count;
+        __shared__ int s_sel[kMaxShortlist];
+        const float2* tlr = tl;
+        auto cand_key = [&](int li, unsigned& key) -> bool {
+            if (V.lslot[(int64_t)kv * n + li] >= 0) return false;   // sampled: resident, not a candidate
+            float sc = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < G; ++g) sc = fmaxf(sc, tlr[(int64_t)(row0 + g) * a.ws_n + li].x);
+            key = score_key(sc);
+            return true;
+        };
+        // number of candidates, then the radix select of the k-th smallest key
+        int nc = 0;
+        for (int li = tid; li < nl; li += kSlThreads) nc += V.lslot[(int64_t)kv * n + li] < 0;
+        int ntot;
+        block_exclusive_scan(nc, s_scan, &ntot);
+        const int k = min(k_short, ntot);
+        if (tid == 0) {
+            s_prefix = 0u;
+            s_need = k;
+            s_count = 0;
+        }
+        __syncthreads();
+        const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+        for (int lev = 0; lev < 3 && k > 0 && k < ntot; ++lev) {
+            const int sh = shifts[lev], wd = widths[lev], nb = 1 << wd;
+            const unsigned prefix = s_prefix;
+            const int need = s_need;
+            for (int i = tid; i < nb; i += kSlThreads) hist[i] = 0u;
+            __syncthreads();
+            for (int li = tid; li < nl; li += kSlThreads) {
+                unsigned key;
+                if (!cand_key(li, key)) continue;
+                if (lev > 0 && (key >> (sh + wd)) != (prefix >> (sh + wd))) continue;
+                atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+            }
+            __syncthreads();
+            // the digit holding the need-th key: bins of this thread, then a block scan of their sums
+            const int per = (nb + kSlThreads - 1) / kSlThreads;
+            const int d0 = min(nb, tid * per), d1 = min(nb, d0 + per);
+            int c = 0;
+            for (int d = d0; d < d1; ++d) c += (int)hist[d];
+            int tot;
+            const int pre = block_exclusive_scan(c, s_scan, &tot);
+            if (pre < need && pre + c >= need) {
+                int acc = pre;
+                for (int d = d0; d < d1; ++d) {
+                    if (acc + (int)hist[d] >= need) {
+                        s_prefix = prefix | ((unsigned)d << sh);
+                        s_need = need - acc;
+                        break;
+                    }
+                    acc += (int)hist[d];
+                }
+            }
+            __syncthreads();
+        }
+        // selection: keys below the threshold, and the first s_need at it in L order (each thread a
+        // contiguous run of L indices, ranked by a block scan)
+        const unsigned thr = s_prefix;
+        const bool all = k >= ntot;
+        const int run = (nl + kSlThreads - 1) / kSlThreads;
+        const int l0 = min(nl, tid * run), l1 = min(nl, l0 + run);
+        int eq = 0;
+        if (!all && k > 0)
+            for (int li = l0; li < l1; ++li) {
+                unsigned key;
+                if (cand_key(li, key) && key == thr) ++eq;
+            }
+        int eqtot;
+        const int eqpre = block_exclusive_scan(eq, s_scan, &eqtot);
+        const int take_eq = s_need;
+        if (k > 0) {
+            int e = eqpre;
+            for (int li = l0; li < l1; ++li) {
+                unsigned key;
+                if (!cand_key(li, key)) continue;
+                bool sel = all || key < thr;
+                if (!all && key == thr) sel = e++ < take_eq;
+                if (sel) {
+                    const int at = atomicAdd(&s_count, 1);
+                    if (at < kMaxShortlist) s_sel[at] = li;
+                }
+            }
+        }
+        __syncthreads();
+        const int cnt = min(s_count, kMaxShortlist);
+        // exact logits of the shortlisted keys, read from the pinned host cache
+        const T* host = reinterpret_cast<const T*>(V.kv_host) + (int64_t)kv * n * 2 * kHeadDim;
+        for (int e = tid; e < cnt * G; e += kSlThreads) {
+            const int j = e / G, g = e % G;
+            const int li = s_sel[j];
+            const int tok = V.ltok[(int64_t)kv * n + li];
+            const ff x = exact_logit<T>(q + (int64_t)(row0 + g) * kHeadDim, host + (int64_t)tok * 2 * kHeadDim,
+                                        a.inv_sqrt_d);
+            tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x.hi, x.lo);
+            atomicMax(&rows[row0 + g].m_tag, tag_max((unsigned)a.gen, x.hi));
+        }
+        for (int j = tid; j < cnt; j += kSlThreads) slist[(int64_t)unit * kMaxShortlist + j] = s_sel[j];
+        if (tid == 0) scount[unit] = cnt;
+        return;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float m = warp_max(mloc[g]);
+        if (lane == 0 && m > -INFINITY) atomicMax(&rows[row0 + g].m_tag, tag_max((unsigned)a.gen, m));
+    }
+}
+
 // Exact sketch: the L logits from the keys themselves.
 template <typename T, int G>
 __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
@@ -2851,7 +3013,7 @@ int g_decide_max_cluster = 8;  // largest cluster the decide kernel is launched 
 
 template <typename T, int G>
 verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, int B, int max_n, int max_nl,
-                           int max_nh, const float* q, float* out, cudaStream_t st)
+                           int max_nh, int max_res, const float* q, float* out, cudaStream_t st)
 {
     const verkv_config& cfg = ctx.cfg;
     const int rowsN = B * a.Hq;
@@ -2885,6 +3047,12 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         score_exact_kernel<T, G><<<dim3(lt + h_tiles, B * a.Hkv), kTile, 0, st>>>(views, q, a, ctx.rows, ctx.tl, ctx.th, lt);
     }
     VK_LAUNCHED("score");
+    if (ctx.shortlist_k > 0) {
+        const int yb = 1 + (max_res + kSlThreads - 1) / kSlThreads;
+        shortlist_kernel<T, G><<<dim3(B * a.Hkv, yb), kSlThreads, 0, st>>>(views, q, a, ctx.rows, ctx.tl,
+                                                                          ctx.shortlist_k, ctx.slist, ctx.scount);
+        VK_LAUNCHED("shortlist");
+    }
     if (on_chip) {
         int C = 1;
         while (C * kDecideCap < max_nl) C <<= 1;
@@ -2956,13 +3124,13 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
 
 template <typename T>
 verkv_status dispatch_g(Ctx& ctx, const Views& views, const DecodeArgs& a, int B, int max_n, int max_nl, int max_nh,
-                        const float* q, float* out, cudaStream_t st)
+                        int max_res, const float* q, float* out, cudaStream_t st)
 {
     switch (ctx.G) {
-        case 1: return launch_decode<T, 1>(ctx, views, a, B, max_n, max_nl, max_nh, q, out, st);
-        case 2: return launch_decode<T, 2>(ctx, views, a, B, max_n, max_nl, max_nh, q, out, st);
-        case 4: return launch_decode<T, 4>(ctx, views, a, B, max_n, max_nl, max_nh, q, out, st);
-        case 8: return launch_decode<T, 8>(ctx, views, a, B, max_n, max_nl, max_nh, q, out, st);
+        case 1: return launch_decode<T, 1>(ctx, views, a, B, max_n, max_nl, max_nh, max_res, q, out, st);
+        case 2: return launch_decode<T, 2>(ctx, views, a, B, max_n, max_nl, max_nh, max_res, q, out, st);
+        case 4: return launch_decode<T, 4>(ctx, views, a, B, max_n, max_nl, max_nh, max_res, q, out, st);
+        case 8: return launch_decode<T, 8>(ctx, views, a, B, max_n, max_nl, max_nh, max_res, q, out, st);
         default: ctx.err = "GQA group must be 1, 2, 4 or 8"; return VERKV_EUNSUPPORTED;
     }
 }
@@ -3010,7 +3178,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     }
     Views views;
     memset(&views, 0, sizeof(views));
-    int max_n = 0, max_nl = 0, max_nh = 0;
+    int max_n = 0, max_nl = 0, max_nh = 0, max_res = 0;
     ctx.last_seq.assign(seq_ids, seq_ids + B);
     ctx.last_n.clear();
     for (int b = 0; b < B; ++b) {
@@ -3046,6 +3214,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         for (const verkv_head_stats& hs : s.stats) {
             max_nl = std::max(max_nl, hs.n_l);
             max_nh = std::max(max_nh, hs.n_h);
+            max_res = std::max(max_res, hs.n_resident);
         }
         ctx.last_n.push_back(s.n);
     }
@@ -3083,8 +3252,8 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     ctx.last_B = B;
     ctx.last_layer = layer;
     if (cfg.kv_dtype == VERKV_DTYPE_BF16)
-        return dispatch_g<__nv_bfloat16>(ctx, views, a, B, max_n, max_nl, max_nh, q, out, st);
-    return dispatch_g<float>(ctx, views, a, B, max_n, max_nl, max_nh, q, out, st);
+        return dispatch_g<__nv_bfloat16>(ctx, views, a, B, max_n, max_nl, max_nh, max_res, q, out, st);
+    return dispatch_g<float>(ctx, views, a, B, max_n, max_nl, max_nh, max_res, q, out, st);
 }
 
 }  // namespace verkv

@@ -83,6 +83,8 @@ struct RowState {
     unsigned int phase_ns[6];  // decide kernel: ns spent in phases 0..4 and in the ranking (rank 0)
 };
 
+constexpr int kMaxShortlist = 1024;   // largest shortlist per KV head
+
 struct Ctx {
     verkv_config cfg{};
     int device = 0;
@@ -124,6 +126,9 @@ struct Ctx {
     int nsplit = 128;               // largest split of the attention over blocks per KV head
     int num_sms = 152;              // multiprocessors of the context's device
     int32_t* hrows = nullptr;       // [max_batch][Hkv] rows the last decode read over the host link
+    int shortlist_k = 0;            // App. A.1 shortlist per KV head (0: off)
+    int32_t* slist = nullptr;       // [max_batch][Hkv][kMaxShortlist] L indices of the last shortlist
+    int32_t* scount = nullptr;      // [max_batch][Hkv] its size
     int64_t stage_rows = -1;        // staging capacity per KV head and slot: -1 = all of L \ S, 0 = off
     int* h_err = nullptr;           // mapped pinned host word: a device-side bounded wait gave up
     int* d_err = nullptr;           // its device address
