@@ -386,6 +386,8 @@ def run_verkv(args):
     secondary = {}
     if rank == 0 and not args.no_secondary:
         secondary["binary_shrinkage"] = binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush)
+        secondary["deployed_binary_shortlist128"] = binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush,
+                                                               shortlist=128)
     ctx.close()
     if rank == 0 and not args.no_secondary:
         del kv_dev, flush_buf
@@ -440,15 +442,18 @@ def _kernel_agg(kt):
     return agg
 
 
-def binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush):
-    """The same workload with the binary shrinkage coefficients of Appendix A.2: decode time (per-call
-    events, L2 flushed before every call), fetch statistics and the decision kernel's time."""
+def binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush, shortlist=0):
+    """The same workload with the binary shrinkage coefficients of Appendix A.2 (and, with shortlist >
+    0, the Appendix A.1 shortlist and exact weights for sampled and shortlisted tokens): decode time
+    (per-call events, L2 flushed before every call), fetch statistics and the kernel times."""
     import torch
 
     from verified_kv_cache_gb300 import binding
     ctx = binding.VerKV(n_kv_heads=w.n_kv, n_q_heads=w.n_q, max_tokens=w.n, n_layers=1, n_seqs=1, max_batch=1,
                         n_sink=w.n_sink, n_local=w.n_local, eta=w.eta, seed=w.seed, sketch=w.sketch,
                         kv_dtype=w.kv_dtype, shrinkage="binary")
+    if shortlist:
+        ctx.set_shortlist(shortlist)
     W, S = w.obs_q.shape[2], w.queries.shape[0]
     out = torch.empty_like(q_dev)
     ctx.compress(0, 0, w.n, kv_host, kv_dev, obs, W, None, st)

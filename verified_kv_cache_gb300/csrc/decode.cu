@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 
@@ -524,13 +525,57 @@ __device__ __forceinline__ ff exact_logit(const float* __restrict__ q, const T* 
 // a (sequence, KV head) replace the sketch logits of the sampled tokens (their keys are resident) by
 // exact ones.  Block 0 selects the shortlist: among the tokens of L outside the sample, the k whose
 // largest sketch logit over the head's G query rows is largest, ties by lower L index (token order).
-// The k-th key is found by a radix select over the order-preserving bits of that score (levels of
-// 12, 12 and 8 bits, histograms in shared memory); the tokens above it are taken, and of those at
-// its value the first in L order.  Their keys are then read from the pinned host cache and scored
+// Block 0 writes every entry's key (the order-preserving bits of that score) once into a scratch row
+// (the full-row ranking's key buffer, idle at this point of a call); the k-th key is found by a radix
+// select over the scratch (levels of 12, 12 and 8 bits, histograms in shared memory); the tokens
+// above it are taken, and of those at its value the first in L order.  Their keys are then read from the pinned host cache and scored
 // exactly.  Every exact logit also raises its row's maximum.  The two kinds of blocks touch
 // disjoint entries of the logit rows.
 // --------------------------------------------------------------------------------------------
 constexpr int kSlThreads = 512;
+
+// Exact float-float logits <q_g, k>/sqrt(d) of one key row for the G query rows q0 + g d: the key is
+// read 16 bytes at a time (once for all heads), every product is a two-product, the sums carry their
+// rounding errors.
+template <typename T, int G>
+__device__ __forceinline__ void exact_logits_row(const float* __restrict__ q0, const T* key, ff inv_sqrt_d,
+                                                 ff (&out)[G])
+{
+    float hi[G], lo[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) hi[g] = lo[g] = 0.f;
+    const unsigned char* kb = reinterpret_cast<const unsigned char*>(key);
+    // bf16 rows: all 16 words of the key in flight at once (one round trip when it is host memory)
+    constexpr bool kPre = std::is_same<T, __nv_bfloat16>::value;
+    uint4 kr[kPre ? kHeadDim / 8 : 1];
+    if constexpr (kPre) {
+#pragma unroll
+        for (int j = 0; j < kHeadDim / 8; ++j) kr[j] = reinterpret_cast<const uint4*>(kb)[j];
+    }
+#pragma unroll 4
+    for (int c8 = 0; c8 < kHeadDim; c8 += 8) {
+        float kk[8];
+        if constexpr (kPre)
+            RowCvt<T>::load8(&kr[c8 / 8], kk);
+        else
+            RowCvt<T>::load8(kb + c8 * (int)sizeof(T), kk);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float4 qa = *reinterpret_cast<const float4*>(q0 + g * kHeadDim + c8);
+            const float4 qb = *reinterpret_cast<const float4*>(q0 + g * kHeadDim + c8 + 4);
+            const float qq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const ff p = two_prod(qq[c], kk[c]);
+                const ff t = two_sum(hi[g], p.hi);
+                hi[g] = t.hi;
+                lo[g] = __fadd_rn(lo[g], __fadd_rn(t.lo, p.lo));
+            }
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) out[g] = ff_mul(fast_two_sum(hi[g], lo[g]), inv_sqrt_d);
+}
 
 __device__ __forceinline__ unsigned score_key(float s)   // ascending key = descending score
 {
@@ -540,7 +585,8 @@ __device__ __forceinline__ unsigned score_key(float s)   // ascending key = desc
 template <typename T, int G>
 __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
                                                               RowState* rows, float2* tl, int k_short,
-                                                              int32_t* __restrict__ slist, int32_t* __restrict__ scount)
+                                                              int32_t* __restrict__ slist, int32_t* __restrict__ scount,
+                                                              unsigned* __restrict__ skeys)
 {
     const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
     const SlotView& V = views.v[b];
@@ -560,11 +606,12 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, cons
             const int li = V.lpos[(int64_t)kv * n + tok];
             if (li >= 0) {
                 const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + rs) * 2 * kHeadDim;
-#pragma unroll 1
+                ff x[G];
+                exact_logits_row<T, G>(q + (int64_t)row0 * kHeadDim, key, a.inv_sqrt_d, x);
+#pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const ff x = exact_logit<T>(q + (int64_t)(row0 + g) * kHeadDim, key, a.inv_sqrt_d);
-                    tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x.hi, x.lo);
-                    mloc[g] = fmaxf(mloc[g], x.hi);
+                    tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x[g].hi, x[g].lo);
+                    mloc[g] = fmaxf(mloc[g], x[g].hi);
                 }
             }
         }
@@ -574,20 +621,39 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, cons
         __shared__ unsigned s_prefix;
         __shared__ int s_need, s_count;
         __shared__ int s_sel[kMaxShortlist];
-        const float2* tlr = tl;
-        auto cand_key = [&](int li, unsigned& key) -> bool {
-            if (V.lslot[(int64_t)kv * n + li] >= 0) return false;   // sampled: resident, not a candidate
-            float sc = -INFINITY;
-#pragma unroll
-            for (int g = 0; g < G; ++g) sc = fmaxf(sc, tlr[(int64_t)(row0 + g) * a.ws_n + li].x);
-            key = score_key(sc);
-            return true;
-        };
-        // number of candidates, then the radix select of the k-th smallest key
+        // pass 1: the key of every L entry (sampled entries are no candidates: key ~0u) into a scratch
+        // row, four entries per thread and step with all their loads issued first
+        unsigned* sk = skeys + (int64_t)unit * a.ws_npow2 * 2;
+        const int nl4 = (nl + 3) / 4;
         int nc = 0;
-        for (int li = tid; li < nl; li += kSlThreads) nc += V.lslot[(int64_t)kv * n + li] < 0;
+#pragma unroll 2
+        for (int i4 = tid; i4 < nl4; i4 += kSlThreads) {
+            int sl4[4];
+            float2 t4[4][G];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int li = 4 * i4 + u;
+                sl4[u] = li < nl ? V.lslot[(int64_t)kv * n + li] : 0;
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    t4[u][g] = li < nl ? tl[(int64_t)(row0 + g) * a.ws_n + li] : make_float2(0.f, 0.f);
+            }
+            uint4 kq;
+            unsigned kk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float sc = -INFINITY;
+#pragma unroll
+                for (int g = 0; g < G; ++g) sc = fmaxf(sc, t4[u][g].x);
+                const bool cand = 4 * i4 + u < nl && sl4[u] < 0;
+                kk[u] = cand ? score_key(sc) : ~0u;
+                nc += cand;
+            }
+            kq = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+            reinterpret_cast<uint4*>(sk)[i4] = kq;
+        }
         int ntot;
-        block_exclusive_scan(nc, s_scan, &ntot);
+        block_exclusive_scan(nc, s_scan, &ntot);   // its barriers also order the scratch writes
         const int k = min(k_short, ntot);
         if (tid == 0) {
             s_prefix = 0u;
@@ -595,18 +661,27 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, cons
             s_count = 0;
         }
         __syncthreads();
+        const uint4* sk4 = reinterpret_cast<const uint4*>(sk);
         const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+        __shared__ int s_at_thr;   // keys equal to the threshold (the last level's bin count)
+        if (tid == 0) s_at_thr = 0;
         for (int lev = 0; lev < 3 && k > 0 && k < ntot; ++lev) {
             const int sh = shifts[lev], wd = widths[lev], nb = 1 << wd;
             const unsigned prefix = s_prefix;
             const int need = s_need;
             for (int i = tid; i < nb; i += kSlThreads) hist[i] = 0u;
             __syncthreads();
-            for (int li = tid; li < nl; li += kSlThreads) {
-                unsigned key;
-                if (!cand_key(li, key)) continue;
-                if (lev > 0 && (key >> (sh + wd)) != (prefix >> (sh + wd))) continue;
-                atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+#pragma unroll 4
+            for (int i4 = tid; i4 < nl4; i4 += kSlThreads) {
+                const uint4 kq = sk4[i4];
+                const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const unsigned key = kk[u];
+                    if (key == ~0u) continue;
+                    if (lev > 0 && (key >> (sh + wd)) != (prefix >> (sh + wd))) continue;
+                    atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+                }
             }
             __syncthreads();
             // the digit holding the need-th key: bins of this thread, then a block scan of their sums
@@ -622,6 +697,7 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, cons
                     if (acc + (int)hist[d] >= need) {
                         s_prefix = prefix | ((unsigned)d << sh);
                         s_need = need - acc;
+                        s_at_thr = (int)hist[d];
                         break;
                     }
                     acc += (int)hist[d];
@@ -629,31 +705,52 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, cons
             }
             __syncthreads();
         }
-        // selection: keys below the threshold, and the first s_need at it in L order (each thread a
-        // contiguous run of L indices, ranked by a block scan)
+        // selection: keys below the threshold, and the first s_need at it in L order.  When every key
+        // at the threshold is taken (the usual case: no tie across the boundary) one strided pass
+        // takes the keys up to it; otherwise each thread takes a contiguous run of groups of four L
+        // indices, ranked by a block scan.
         const unsigned thr = s_prefix;
         const bool all = k >= ntot;
-        const int run = (nl + kSlThreads - 1) / kSlThreads;
-        const int l0 = min(nl, tid * run), l1 = min(nl, l0 + run);
+        const int take_eq = s_need;
+        const bool whole = all || take_eq == s_at_thr;
+        if (k > 0 && whole) {
+#pragma unroll 4
+            for (int i4 = tid; i4 < nl4; i4 += kSlThreads) {
+                const uint4 kq = sk4[i4];
+                const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (kk[u] == ~0u || !(all || kk[u] <= thr)) continue;
+                    const int at = atomicAdd(&s_count, 1);
+                    if (at < kMaxShortlist) s_sel[at] = 4 * i4 + u;
+                }
+            }
+        }
+        const int run = (nl4 + kSlThreads - 1) / kSlThreads;
+        const int g0 = min(nl4, tid * run), g1 = min(nl4, g0 + run);
         int eq = 0;
-        if (!all && k > 0)
-            for (int li = l0; li < l1; ++li) {
-                unsigned key;
-                if (cand_key(li, key) && key == thr) ++eq;
+        if (!whole && k > 0)
+            for (int i4 = g0; i4 < g1; ++i4) {
+                const uint4 kq = sk4[i4];
+                eq += (kq.x == thr) + (kq.y == thr) + (kq.z == thr) + (kq.w == thr);
             }
         int eqtot;
         const int eqpre = block_exclusive_scan(eq, s_scan, &eqtot);
-        const int take_eq = s_need;
-        if (k > 0) {
+        if (k > 0 && !whole) {
             int e = eqpre;
-            for (int li = l0; li < l1; ++li) {
-                unsigned key;
-                if (!cand_key(li, key)) continue;
-                bool sel = all || key < thr;
-                if (!all && key == thr) sel = e++ < take_eq;
-                if (sel) {
-                    const int at = atomicAdd(&s_count, 1);
-                    if (at < kMaxShortlist) s_sel[at] = li;
+            for (int i4 = g0; i4 < g1; ++i4) {
+                const uint4 kq = sk4[i4];
+                const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const unsigned key = kk[u];
+                    if (key == ~0u) continue;
+                    bool sel = key < thr;
+                    if (key == thr) sel = e++ < take_eq;
+                    if (sel) {
+                        const int at = atomicAdd(&s_count, 1);
+                        if (at < kMaxShortlist) s_sel[at] = 4 * i4 + u;
+                    }
                 }
             }
         }
@@ -661,14 +758,16 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, cons
         const int cnt = min(s_count, kMaxShortlist);
         // exact logits of the shortlisted keys, read from the pinned host cache
         const T* host = reinterpret_cast<const T*>(V.kv_host) + (int64_t)kv * n * 2 * kHeadDim;
-        for (int e = tid; e < cnt * G; e += kSlThreads) {
-            const int j = e / G, g = e % G;
+        for (int j = tid; j < cnt; j += kSlThreads) {
             const int li = s_sel[j];
             const int tok = V.ltok[(int64_t)kv * n + li];
-            const ff x = exact_logit<T>(q + (int64_t)(row0 + g) * kHeadDim, host + (int64_t)tok * 2 * kHeadDim,
-                                        a.inv_sqrt_d);
-            tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x.hi, x.lo);
-            atomicMax(&rows[row0 + g].m_tag, tag_max((unsigned)a.gen, x.hi));
+            ff x[G];
+            exact_logits_row<T, G>(q + (int64_t)row0 * kHeadDim, host + (int64_t)tok * 2 * kHeadDim, a.inv_sqrt_d, x);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x[g].hi, x[g].lo);
+                atomicMax(&rows[row0 + g].m_tag, tag_max((unsigned)a.gen, x[g].hi));
+            }
         }
         for (int j = tid; j < cnt; j += kSlThreads) slist[(int64_t)unit * kMaxShortlist + j] = s_sel[j];
         if (tid == 0) scount[unit] = cnt;
@@ -3050,7 +3149,8 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
     if (ctx.shortlist_k > 0) {
         const int yb = 1 + (max_res + kSlThreads - 1) / kSlThreads;
         shortlist_kernel<T, G><<<dim3(B * a.Hkv, yb), kSlThreads, 0, st>>>(views, q, a, ctx.rows, ctx.tl,
-                                                                          ctx.shortlist_k, ctx.slist, ctx.scount);
+                                                                          ctx.shortlist_k, ctx.slist, ctx.scount,
+                                                                          reinterpret_cast<unsigned*>(ctx.keys));
         VK_LAUNCHED("shortlist");
     }
     if (on_chip) {
