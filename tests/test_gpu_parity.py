@@ -450,19 +450,26 @@ def _shortlist_near_tie(orow, got_tokens):
     return bool(np.all(np.abs(sc[diff] - edge) <= 1e-6 * max(abs(edge), 1e-30)))
 
 
-@pytest.mark.parametrize("sketch,shrinkage", [("int8", "clipped"), ("2bit", "clipped"), ("2bit", "binary")])
-def test_shortlist_parity(sketch, shrinkage):
+@pytest.mark.parametrize("sketch,shrinkage,shape", [("int8", "clipped", "g4"), ("2bit", "clipped", "g4"),
+                                                    ("2bit", "binary", "g4"), ("int8", "clipped", "g8"),
+                                                    ("exact", "clipped", "tiny")])
+def test_shortlist_parity(sketch, shrinkage, shape):
     """Appendix A.1's deployed certificate weights: the shortlist of 128 tokens per KV head (exact set
     match, near-ties exempt) and exact weights for sampled and shortlisted tokens in the decision;
     beta, eps_hat, k*, the fetched set and the output against the oracle run with the same weights."""
-    w = small_case(sketch, n=6000, steps=4)
+    if shape == "tiny":      # fp32 K/V, one query head per KV head, exact sketch
+        w = workloads.tiny_oracle_case()
+    elif shape == "g8":
+        w = small_case(sketch, n=6000, n_kv=2, n_q=16, steps=4)
+    else:
+        w = small_case(sketch, n=6000, steps=4)
     ctx = make_lib_ctx(w, shrinkage=shrinkage)
     ctx.set_shortlist(128)
     sh = 1 if shrinkage == "binary" else 0
     gc = GpuCase(w, ctx)
     tau, stats, osl = _compress_both(w, gc)
     counts = {"ok": 0, "exempt": 0}
-    for s in range(4):
+    for s in range(w.queries.shape[0]):
         out = gc.decode(w.queries[s], w.eps, w.delta)
         trace = ctx.decode_trace(w.n_q)
         rows, unions = oracle_decode(w, 0, osl, w.queries[s, 0], w.eps, w.delta, shortlist=128, shrinkage=sh)
@@ -484,5 +491,5 @@ def test_shortlist_parity(sketch, shrinkage):
                 else:
                     counts["exempt"] += 1
     assert counts["ok"] >= 0.9 * sum(counts.values()), counts
-    print(sketch, shrinkage, counts)
+    print(sketch, shrinkage, shape, counts)
     ctx.close()
