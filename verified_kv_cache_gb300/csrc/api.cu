@@ -31,7 +31,7 @@ verkv_status fail(Ctx& ctx, verkv_status s, const char* msg)
 void free_ws(Ctx& c)
 {
     void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.adone, c.ucount,
-                    c.part, c.hrows, c.slist, c.scount,
+                    c.part, c.hrows, c.slist, c.scount, c.shist,
                     c.d_slot_n};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -54,7 +54,9 @@ verkv_status alloc_ws(Ctx& ctx)
     VK_CUDA(cudaMalloc(&ctx.wl, sizeof(float) * rows * n));
     VK_CUDA(cudaMalloc(&ctx.rows, sizeof(RowState) * rows));
     VK_CUDA(cudaMemset(ctx.rows, 0, sizeof(RowState) * rows));
-    VK_CUDA(cudaMalloc(&ctx.keys, sizeof(unsigned long long) * rows * (size_t)p2));
+    // at least two words a row: the shortlist reuses the buffer as rows of 2 max(p2, 2) 32-bit keys,
+    // one per KV head, written four at a time
+    VK_CUDA(cudaMalloc(&ctx.keys, sizeof(unsigned long long) * rows * (size_t)std::max(p2, 2)));
     VK_CUDA(cudaMalloc(&ctx.mark, sizeof(int32_t) * rows * n));
     VK_CUDA(cudaMemset(ctx.mark, 0, sizeof(int32_t) * rows * n));
     VK_CUDA(cudaMalloc(&ctx.elist, sizeof(int32_t) * rows * n));
@@ -72,6 +74,8 @@ verkv_status alloc_ws(Ctx& ctx)
     VK_CUDA(cudaMalloc(&ctx.slist, sizeof(int32_t) * kvb * kMaxShortlist));
     VK_CUDA(cudaMalloc(&ctx.scount, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMemset(ctx.scount, 0, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMalloc(&ctx.shist, sizeof(uint32_t) * kvb * (kShortlistBins + 1)));
+    VK_CUDA(cudaMemset(ctx.shist, 0, sizeof(uint32_t) * kvb * (kShortlistBins + 1)));
     VK_CUDA(cudaMalloc(&ctx.part, sizeof(float) * rows * ctx.nsplit * (kHeadDim + 2)));
     VK_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&ctx.h_err), sizeof(int), cudaHostAllocMapped));
     *ctx.h_err = 0;

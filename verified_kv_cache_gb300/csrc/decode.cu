@@ -521,18 +521,21 @@ __device__ __forceinline__ ff exact_logit(const float* __restrict__ q, const T* 
 }
 
 // --------------------------------------------------------------------------------------------
-// Shortlist and exact certificate weights (App. A.1; launched only when enabled).  Blocks y >= 1 of
-// a (sequence, KV head) replace the sketch logits of the sampled tokens (their keys are resident) by
-// exact ones.  Block 0 selects the shortlist: among the tokens of L outside the sample, the k whose
-// largest sketch logit over the head's G query rows is largest, ties by lower L index (token order).
-// Block 0 writes every entry's key (the order-preserving bits of that score) once into a scratch row
-// (the full-row ranking's key buffer, idle at this point of a call); the k-th key is found by a radix
-// select over the scratch (levels of 12, 12 and 8 bits, histograms in shared memory); the tokens
-// above it are taken, and of those at its value the first in L order.  Their keys are then read from the pinned host cache and scored
-// exactly.  Every exact logit also raises its row's maximum.  The two kinds of blocks touch
-// disjoint entries of the logit rows.
+// Shortlist and exact certificate weights (App. A.1; launched only when enabled), two kernels.
+// shortlist_keys_kernel: blocks y < ny_keys of a (sequence, KV head) each take a slice of L.  The key
+// of every entry -- the order-preserving bits of its largest sketch logit over the head's G query
+// rows, ascending = descending score; ~0u for sampled entries, which are no candidates -- goes into a
+// scratch row (the full-row ranking's key buffer, idle at this point of a call) and into the KV
+// head's first-level histogram (top 12 bits) in global memory.  Blocks y >= ny_keys replace the
+// sketch logits of the sampled tokens (their keys are resident) by exact ones.
+// shortlist_select_kernel: one block per (sequence, KV head) finishes the radix select of the k-th
+// key (levels of 12 and 8 more bits over the scratch), takes the tokens below it and the first at it
+// in L order (ties by lower L index, i.e. token order), reads their keys from the pinned host cache,
+// scores them exactly and clears the histogram for the next call.  Every exact logit also raises its
+// row's maximum.  The two kinds of blocks of the first kernel touch disjoint entries of the logits.
 // --------------------------------------------------------------------------------------------
 constexpr int kSlThreads = 512;
+constexpr int kSlBins = kShortlistBins;
 
 // Exact float-float logits <q_g, k>/sqrt(d) of one key row for the G query rows q0 + g d: the key is
 // read 16 bytes at a time (once for all heads), every product is a two-product, the sums carry their
@@ -577,16 +580,70 @@ __device__ __forceinline__ void exact_logits_row(const float* __restrict__ q0, c
     for (int g = 0; g < G; ++g) out[g] = ff_mul(fast_two_sum(hi[g], lo[g]), inv_sqrt_d);
 }
 
+// The same logits with one key row spread over four adjacent lanes: lane part p (0..3) sums channels
+// [32 p, 32 p + 32) and the four float-float partial sums are combined by error-free additions, so
+// every lane of the group ends with the same result.  Every lane of the warp must call it; a lane with
+// no row passes key = nullptr and reads nothing.
+template <typename T, int G>
+__device__ __forceinline__ void exact_logits_quad(const float* __restrict__ q0, const T* key, int part,
+                                                  ff inv_sqrt_d, ff (&out)[G])
+{
+    constexpr int kQ = kHeadDim / 4;   // channels of one lane
+    float hi[G], lo[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) hi[g] = lo[g] = 0.f;
+    if (key != nullptr) {
+        const unsigned char* kb = reinterpret_cast<const unsigned char*>(key + part * kQ);
+        constexpr int kWords = kQ * (int)sizeof(T) / 16;
+        uint4 kr[kWords];   // the lane's part of the row in flight at once
+#pragma unroll
+        for (int j = 0; j < kWords; ++j) kr[j] = reinterpret_cast<const uint4*>(kb)[j];
+#pragma unroll
+        for (int c8 = 0; c8 < kQ; c8 += 8) {
+            float kk[8];
+            RowCvt<T>::load8(reinterpret_cast<const unsigned char*>(kr) + c8 * (int)sizeof(T), kk);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float* qg = q0 + g * kHeadDim + part * kQ + c8;
+                const float4 qa = *reinterpret_cast<const float4*>(qg);
+                const float4 qb = *reinterpret_cast<const float4*>(qg + 4);
+                const float qq[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const ff p = two_prod(qq[c], kk[c]);
+                    const ff t = two_sum(hi[g], p.hi);
+                    hi[g] = t.hi;
+                    lo[g] = __fadd_rn(lo[g], __fadd_rn(t.lo, p.lo));
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float oh = __shfl_xor_sync(0xffffffffu, hi[g], o), ol = __shfl_xor_sync(0xffffffffu, lo[g], o);
+            const ff t = two_sum(hi[g], oh);
+            hi[g] = t.hi;
+            lo[g] = __fadd_rn(__fadd_rn(lo[g], ol), t.lo);
+        }
+#pragma unroll
+    for (int g = 0; g < G; ++g) out[g] = ff_mul(fast_two_sum(hi[g], lo[g]), inv_sqrt_d);
+}
+
+// 32-bit words of a KV head's scratch key row (a multiple of four)
+__device__ __forceinline__ int64_t shortlist_stride(const DecodeArgs& a) { return 2 * (int64_t)max(a.ws_npow2, 2); }
+
 __device__ __forceinline__ unsigned score_key(float s)   // ascending key = descending score
 {
     return ~((unsigned)float_to_ordered(s) ^ 0x80000000u);
 }
 
 template <typename T, int G>
-__global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, const float* __restrict__ q, DecodeArgs a,
-                                                              RowState* rows, float2* tl, int k_short,
-                                                              int32_t* __restrict__ slist, int32_t* __restrict__ scount,
-                                                              unsigned* __restrict__ skeys)
+__global__ void __launch_bounds__(kSlThreads) shortlist_keys_kernel(Views views, const float* __restrict__ q,
+                                                                   DecodeArgs a, RowState* rows, float2* tl,
+                                                                   unsigned* __restrict__ skeys,
+                                                                   unsigned* __restrict__ ghist, int ny_keys)
 {
     const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
     const SlotView& V = views.v[b];
@@ -594,81 +651,118 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, cons
     const int nl = V.counts[kv * 4 + 1];
     const int row0 = row_of(b, kv * G, a.Hq);
     const int tid = threadIdx.x, lane = tid & 31;
-    float mloc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
-    if (blockIdx.y > 0) {
+    if ((int)blockIdx.y >= ny_keys) {
         // sampled tokens: resident slot rs -> token -> L index (H tokens have none)
+        float mloc[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) mloc[g] = -INFINITY;
         const int m_res = V.counts[kv * 4 + 3];
-        const int rs = (blockIdx.y - 1) * kSlThreads + tid;
+        const int rs = ((int)blockIdx.y - ny_keys) * (kSlThreads / 4) + tid / 4, part = tid & 3;
+        int li = -1;
+        const T* key = nullptr;
         if (rs < m_res) {
             const int tok = V.rtok[(int64_t)kv * n + rs];
-            const int li = V.lpos[(int64_t)kv * n + tok];
-            if (li >= 0) {
-                const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + rs) * 2 * kHeadDim;
-                ff x[G];
-                exact_logits_row<T, G>(q + (int64_t)row0 * kHeadDim, key, a.inv_sqrt_d, x);
+            li = V.lpos[(int64_t)kv * n + tok];
+            if (li >= 0) key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + rs) * 2 * kHeadDim;
+        }
+        ff x[G];
+        exact_logits_quad<T, G>(q + (int64_t)row0 * kHeadDim, key, part, a.inv_sqrt_d, x);
+        if (key != nullptr) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x[g].hi, x[g].lo);
-                    mloc[g] = fmaxf(mloc[g], x[g].hi);
-                }
+            for (int g = 0; g < G; ++g) {
+                if (part == 0) tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x[g].hi, x[g].lo);
+                mloc[g] = fmaxf(mloc[g], x[g].hi);
             }
         }
-    } else {
-        __shared__ unsigned hist[4096];
-        __shared__ int s_scan[32];
-        __shared__ unsigned s_prefix;
-        __shared__ int s_need, s_count;
-        __shared__ int s_sel[kMaxShortlist];
-        // pass 1: the key of every L entry (sampled entries are no candidates: key ~0u) into a scratch
-        // row, four entries per thread and step with all their loads issued first
-        unsigned* sk = skeys + (int64_t)unit * a.ws_npow2 * 2;
-        const int nl4 = (nl + 3) / 4;
-        int nc = 0;
-#pragma unroll 2
-        for (int i4 = tid; i4 < nl4; i4 += kSlThreads) {
-            int sl4[4];
-            float2 t4[4][G];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int li = 4 * i4 + u;
-                sl4[u] = li < nl ? V.lslot[(int64_t)kv * n + li] : 0;
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    t4[u][g] = li < nl ? tl[(int64_t)(row0 + g) * a.ws_n + li] : make_float2(0.f, 0.f);
-            }
-            uint4 kq;
-            unsigned kk[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float sc = -INFINITY;
-#pragma unroll
-                for (int g = 0; g < G; ++g) sc = fmaxf(sc, t4[u][g].x);
-                const bool cand = 4 * i4 + u < nl && sl4[u] < 0;
-                kk[u] = cand ? score_key(sc) : ~0u;
-                nc += cand;
-            }
-            kq = make_uint4(kk[0], kk[1], kk[2], kk[3]);
-            reinterpret_cast<uint4*>(sk)[i4] = kq;
+        for (int g = 0; g < G; ++g) {
+            const float m = warp_max(mloc[g]);
+            if (lane == 0 && m > -INFINITY) atomicMax(&rows[row0 + g].m_tag, tag_max((unsigned)a.gen, m));
         }
-        int ntot;
-        block_exclusive_scan(nc, s_scan, &ntot);   // its barriers also order the scratch writes
-        const int k = min(k_short, ntot);
-        if (tid == 0) {
-            s_prefix = 0u;
-            s_need = k;
-            s_count = 0;
+        return;
+    }
+    __shared__ unsigned hist[kSlBins];
+    for (int i = tid; i < kSlBins; i += kSlThreads) hist[i] = 0u;
+    __syncthreads();
+    unsigned* sk = skeys + unit * shortlist_stride(a);
+    const int nl4 = (nl + 3) / 4;
+    const int per = (nl4 + ny_keys - 1) / ny_keys;
+    const int a0 = min(nl4, (int)blockIdx.y * per), a1 = min(nl4, a0 + per);
+    int nc = 0;
+    for (int i4 = a0 + tid; i4 < a1; i4 += kSlThreads) {
+        int sl4[4];
+        float2 t4[4][G];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int li = 4 * i4 + u;
+            sl4[u] = li < nl ? V.lslot[(int64_t)kv * n + li] : 0;
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                t4[u][g] = li < nl ? tl[(int64_t)(row0 + g) * a.ws_n + li] : make_float2(0.f, 0.f);
         }
-        __syncthreads();
-        const uint4* sk4 = reinterpret_cast<const uint4*>(sk);
-        const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
-        __shared__ int s_at_thr;   // keys equal to the threshold (the last level's bin count)
-        if (tid == 0) s_at_thr = 0;
-        for (int lev = 0; lev < 3 && k > 0 && k < ntot; ++lev) {
-            const int sh = shifts[lev], wd = widths[lev], nb = 1 << wd;
-            const unsigned prefix = s_prefix;
-            const int need = s_need;
+        unsigned kk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float sc = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < G; ++g) sc = fmaxf(sc, t4[u][g].x);
+            const bool cand = 4 * i4 + u < nl && sl4[u] < 0;
+            kk[u] = cand ? score_key(sc) : ~0u;
+            if (cand) {
+                ++nc;
+                atomicAdd(&hist[kk[u] >> 20], 1u);
+            }
+        }
+        reinterpret_cast<uint4*>(sk)[i4] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+    }
+    __syncthreads();
+    unsigned* gh = ghist + (int64_t)unit * (kSlBins + 1);   // bins, then the candidate count
+    for (int i = tid; i < kSlBins; i += kSlThreads)
+        if (hist[i]) atomicAdd(&gh[i], hist[i]);
+    nc = __reduce_add_sync(0xffffffffu, (unsigned)nc);
+    if (lane == 0 && nc > 0) atomicAdd(&gh[kSlBins], (unsigned)nc);
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kSlThreads) shortlist_select_kernel(Views views, const float* __restrict__ q,
+                                                                     DecodeArgs a, RowState* rows, float2* tl,
+                                                                     int k_short, int32_t* __restrict__ slist,
+                                                                     int32_t* __restrict__ scount,
+                                                                     const unsigned* __restrict__ skeys,
+                                                                     unsigned* __restrict__ ghist)
+{
+    const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
+    const SlotView& V = views.v[b];
+    const int n = V.n;
+    const int nl = V.counts[kv * 4 + 1];
+    const int row0 = row_of(b, kv * G, a.Hq);
+    const int tid = threadIdx.x;
+    __shared__ unsigned hist[kSlBins];
+    __shared__ int s_scan[32];
+    __shared__ unsigned s_prefix;
+    __shared__ int s_need, s_count, s_at_thr;
+    __shared__ int s_sel[kMaxShortlist];
+    unsigned* gh = ghist + (int64_t)unit * (kSlBins + 1);
+    const int ntot = (int)gh[kSlBins];
+    const int k = min(k_short, ntot);
+    const int nl4 = (nl + 3) / 4;
+    const uint4* sk4 = reinterpret_cast<const uint4*>(skeys + unit * shortlist_stride(a));
+    if (tid == 0) {
+        s_prefix = 0u;
+        s_need = k;
+        s_count = 0;
+        s_at_thr = 0;
+    }
+    for (int i = tid; i < kSlBins; i += kSlThreads) hist[i] = gh[i];
+    __syncthreads();
+    // the histogram is read: leave it clear for the next call
+    for (int i = tid; i <= kSlBins; i += kSlThreads) gh[i] = 0u;
+    const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+    for (int lev = 0; lev < 3 && k > 0 && k < ntot; ++lev) {
+        const int sh = shifts[lev], wd = widths[lev], nb = 1 << wd;
+        const unsigned prefix = s_prefix;
+        const int need = s_need;
+        if (lev > 0) {   // level 0 comes from the keys kernel
             for (int i = tid; i < nb; i += kSlThreads) hist[i] = 0u;
             __syncthreads();
 #pragma unroll 4
@@ -678,106 +772,101 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_kernel(Views views, cons
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const unsigned key = kk[u];
-                    if (key == ~0u) continue;
-                    if (lev > 0 && (key >> (sh + wd)) != (prefix >> (sh + wd))) continue;
+                    if (key == ~0u || (key >> (sh + wd)) != (prefix >> (sh + wd))) continue;
                     atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
                 }
             }
             __syncthreads();
-            // the digit holding the need-th key: bins of this thread, then a block scan of their sums
-            const int per = (nb + kSlThreads - 1) / kSlThreads;
-            const int d0 = min(nb, tid * per), d1 = min(nb, d0 + per);
-            int c = 0;
-            for (int d = d0; d < d1; ++d) c += (int)hist[d];
-            int tot;
-            const int pre = block_exclusive_scan(c, s_scan, &tot);
-            if (pre < need && pre + c >= need) {
-                int acc = pre;
-                for (int d = d0; d < d1; ++d) {
-                    if (acc + (int)hist[d] >= need) {
-                        s_prefix = prefix | ((unsigned)d << sh);
-                        s_need = need - acc;
-                        s_at_thr = (int)hist[d];
-                        break;
-                    }
-                    acc += (int)hist[d];
-                }
-            }
-            __syncthreads();
         }
-        // selection: keys below the threshold, and the first s_need at it in L order.  When every key
-        // at the threshold is taken (the usual case: no tie across the boundary) one strided pass
-        // takes the keys up to it; otherwise each thread takes a contiguous run of groups of four L
-        // indices, ranked by a block scan.
-        const unsigned thr = s_prefix;
-        const bool all = k >= ntot;
-        const int take_eq = s_need;
-        const bool whole = all || take_eq == s_at_thr;
-        if (k > 0 && whole) {
+        // the digit holding the need-th key: bins of this thread, then a block scan of their sums
+        const int per = (nb + kSlThreads - 1) / kSlThreads;
+        const int d0 = min(nb, tid * per), d1 = min(nb, d0 + per);
+        int c = 0;
+        for (int d = d0; d < d1; ++d) c += (int)hist[d];
+        int tot;
+        const int pre = block_exclusive_scan(c, s_scan, &tot);
+        if (pre < need && pre + c >= need) {
+            int acc = pre;
+            for (int d = d0; d < d1; ++d) {
+                if (acc + (int)hist[d] >= need) {
+                    s_prefix = prefix | ((unsigned)d << sh);
+                    s_need = need - acc;
+                    s_at_thr = (int)hist[d];
+                    break;
+                }
+                acc += (int)hist[d];
+            }
+        }
+        __syncthreads();
+    }
+    // selection: keys below the threshold, and the first s_need at it in L order.  When every key
+    // at the threshold is taken (the usual case: no tie across the boundary) one strided pass
+    // takes the keys up to it; otherwise each thread takes a contiguous run of groups of four L
+    // indices, ranked by a block scan.
+    const unsigned thr = s_prefix;
+    const bool all = k >= ntot;
+    const int take_eq = s_need;
+    const bool whole = all || take_eq == s_at_thr;
+    if (k > 0 && whole) {
 #pragma unroll 4
-            for (int i4 = tid; i4 < nl4; i4 += kSlThreads) {
-                const uint4 kq = sk4[i4];
-                const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
+        for (int i4 = tid; i4 < nl4; i4 += kSlThreads) {
+            const uint4 kq = sk4[i4];
+            const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (kk[u] == ~0u || !(all || kk[u] <= thr)) continue;
+            for (int u = 0; u < 4; ++u) {
+                if (kk[u] == ~0u || !(all || kk[u] <= thr)) continue;
+                const int at = atomicAdd(&s_count, 1);
+                if (at < kMaxShortlist) s_sel[at] = 4 * i4 + u;
+            }
+        }
+    }
+    const int run = (nl4 + kSlThreads - 1) / kSlThreads;
+    const int g0 = min(nl4, tid * run), g1 = min(nl4, g0 + run);
+    int eq = 0;
+    if (!whole && k > 0)
+        for (int i4 = g0; i4 < g1; ++i4) {
+            const uint4 kq = sk4[i4];
+            eq += (kq.x == thr) + (kq.y == thr) + (kq.z == thr) + (kq.w == thr);
+        }
+    int eqtot;
+    const int eqpre = block_exclusive_scan(eq, s_scan, &eqtot);
+    if (k > 0 && !whole) {
+        int e = eqpre;
+        for (int i4 = g0; i4 < g1; ++i4) {
+            const uint4 kq = sk4[i4];
+            const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const unsigned key = kk[u];
+                if (key == ~0u) continue;
+                bool sel = key < thr;
+                if (key == thr) sel = e++ < take_eq;
+                if (sel) {
                     const int at = atomicAdd(&s_count, 1);
                     if (at < kMaxShortlist) s_sel[at] = 4 * i4 + u;
                 }
             }
         }
-        const int run = (nl4 + kSlThreads - 1) / kSlThreads;
-        const int g0 = min(nl4, tid * run), g1 = min(nl4, g0 + run);
-        int eq = 0;
-        if (!whole && k > 0)
-            for (int i4 = g0; i4 < g1; ++i4) {
-                const uint4 kq = sk4[i4];
-                eq += (kq.x == thr) + (kq.y == thr) + (kq.z == thr) + (kq.w == thr);
-            }
-        int eqtot;
-        const int eqpre = block_exclusive_scan(eq, s_scan, &eqtot);
-        if (k > 0 && !whole) {
-            int e = eqpre;
-            for (int i4 = g0; i4 < g1; ++i4) {
-                const uint4 kq = sk4[i4];
-                const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const unsigned key = kk[u];
-                    if (key == ~0u) continue;
-                    bool sel = key < thr;
-                    if (key == thr) sel = e++ < take_eq;
-                    if (sel) {
-                        const int at = atomicAdd(&s_count, 1);
-                        if (at < kMaxShortlist) s_sel[at] = 4 * i4 + u;
-                    }
-                }
-            }
-        }
-        __syncthreads();
-        const int cnt = min(s_count, kMaxShortlist);
-        // exact logits of the shortlisted keys, read from the pinned host cache
-        const T* host = reinterpret_cast<const T*>(V.kv_host) + (int64_t)kv * n * 2 * kHeadDim;
-        for (int j = tid; j < cnt; j += kSlThreads) {
-            const int li = s_sel[j];
-            const int tok = V.ltok[(int64_t)kv * n + li];
-            ff x[G];
-            exact_logits_row<T, G>(q + (int64_t)row0 * kHeadDim, host + (int64_t)tok * 2 * kHeadDim, a.inv_sqrt_d, x);
+    }
+    __syncthreads();
+    const int cnt = min(s_count, kMaxShortlist);
+    // exact logits of the shortlisted keys, read from the pinned host cache, four lanes per key
+    const T* host = reinterpret_cast<const T*>(V.kv_host) + (int64_t)kv * n * 2 * kHeadDim;
+    for (int j0 = 0; j0 < cnt; j0 += kSlThreads / 4) {
+        const int j = j0 + tid / 4;
+        const int li = j < cnt ? s_sel[j] : -1;
+        const T* key = li >= 0 ? host + (int64_t)V.ltok[(int64_t)kv * n + li] * 2 * kHeadDim : nullptr;
+        ff x[G];
+        exact_logits_quad<T, G>(q + (int64_t)row0 * kHeadDim, key, tid & 3, a.inv_sqrt_d, x);
+        if (key != nullptr && (tid & 3) == 0)
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 tl[(int64_t)(row0 + g) * a.ws_n + li] = make_float2(x[g].hi, x[g].lo);
                 atomicMax(&rows[row0 + g].m_tag, tag_max((unsigned)a.gen, x[g].hi));
             }
-        }
-        for (int j = tid; j < cnt; j += kSlThreads) slist[(int64_t)unit * kMaxShortlist + j] = s_sel[j];
-        if (tid == 0) scount[unit] = cnt;
-        return;
     }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float m = warp_max(mloc[g]);
-        if (lane == 0 && m > -INFINITY) atomicMax(&rows[row0 + g].m_tag, tag_max((unsigned)a.gen, m));
-    }
+    for (int j = tid; j < cnt; j += kSlThreads) slist[(int64_t)unit * kMaxShortlist + j] = s_sel[j];
+    if (tid == 0) scount[unit] = cnt;
 }
 
 // Exact sketch: the L logits from the keys themselves.
@@ -3147,10 +3236,18 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
     }
     VK_LAUNCHED("score");
     if (ctx.shortlist_k > 0) {
-        const int yb = 1 + (max_res + kSlThreads - 1) / kSlThreads;
-        shortlist_kernel<T, G><<<dim3(B * a.Hkv, yb), kSlThreads, 0, st>>>(views, q, a, ctx.rows, ctx.tl,
-                                                                          ctx.shortlist_k, ctx.slist, ctx.scount,
-                                                                          reinterpret_cast<unsigned*>(ctx.keys));
+        // keys: about two blocks per multiprocessor over the call, at least 2048 entries a block
+        const int units = B * a.Hkv;
+        const int ny = std::max(1, std::min((max_nl + 4 * kSlThreads - 1) / (4 * kSlThreads),
+                                            2 * ctx.num_sms / units));
+        const int yb = ny + (max_res + kSlThreads / 4 - 1) / (kSlThreads / 4);   // four lanes per sampled key
+        shortlist_keys_kernel<T, G><<<dim3(units, yb), kSlThreads, 0, st>>>(
+            views, q, a, ctx.rows, ctx.tl, reinterpret_cast<unsigned*>(ctx.keys), ctx.shist, ny);
+        VK_LAUNCHED("shortlist_keys");
+        shortlist_select_kernel<T, G><<<units, kSlThreads, 0, st>>>(views, q, a, ctx.rows, ctx.tl, ctx.shortlist_k,
+                                                                    ctx.slist, ctx.scount,
+                                                                    reinterpret_cast<const unsigned*>(ctx.keys),
+                                                                    ctx.shist);
         VK_LAUNCHED("shortlist");
     }
     if (on_chip) {

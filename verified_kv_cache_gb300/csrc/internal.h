@@ -83,7 +83,8 @@ struct RowState {
     unsigned int phase_ns[6];  // decide kernel: ns spent in phases 0..4 and in the ranking (rank 0)
 };
 
-constexpr int kMaxShortlist = 1024;   // largest shortlist per KV head
+constexpr int kMaxShortlist = 1024;    // largest shortlist per KV head
+constexpr int kShortlistBins = 4096;   // shortlist radix select: first-level bins (top 12 key bits)
 
 struct Ctx {
     verkv_config cfg{};
@@ -129,6 +130,8 @@ struct Ctx {
     int shortlist_k = 0;            // App. A.1 shortlist per KV head (0: off)
     int32_t* slist = nullptr;       // [max_batch][Hkv][kMaxShortlist] L indices of the last shortlist
     int32_t* scount = nullptr;      // [max_batch][Hkv] its size
+    uint32_t* shist = nullptr;      // [max_batch][Hkv][kShortlistBins + 1] shortlist first-level histogram + count
+                                    // (zero between calls)
     int64_t stage_rows = -1;        // staging capacity per KV head and slot: -1 = all of L \ S, 0 = off
     int* h_err = nullptr;           // mapped pinned host word: a device-side bounded wait gave up
     int* d_err = nullptr;           // its device address
