@@ -450,6 +450,37 @@ def _shortlist_near_tie(orow, got_tokens):
     return bool(np.all(np.abs(sc[diff] - edge) <= 1e-6 * max(abs(edge), 1e-30)))
 
 
+@pytest.mark.parametrize("pool,n", [(1, 6000), (2, 6000), (24, 6000), (0, 180)])
+def test_shortlist_ties_and_short_rows(pool, n):
+    """Appendix A.1's shortlist where sketch scores tie exactly: every key is a copy of one of `pool`
+    rows, so equal scores are bit-equal on both sides and the k-th largest is broken by token order
+    (exact set match, no exemption).  pool 1 and 2 put thousands of keys at the boundary value, pool 24
+    a few hundred; pool 0 keeps the keys and makes L minus S shorter than the shortlist (all taken)."""
+    w = small_case("int8", n=n, steps=2, eta=1 / 16 if pool else 0.5)
+    if pool:
+        rng = np.random.default_rng(5)
+        for b in range(w.batch):
+            for h in range(w.n_kv):
+                rows = rng.standard_normal((pool, w.d)).astype(np.float32)
+                w.K[b, h] = rows[np.arange(w.n) % pool]
+    ctx = make_lib_ctx(w)
+    ctx.set_shortlist(128)
+    gc = GpuCase(w, ctx)
+    tau, stats, osl = _compress_both(w, gc)
+    for s in range(w.queries.shape[0]):
+        gc.decode(w.queries[s], w.eps, w.delta)
+        rows, _ = oracle_decode(w, 0, osl, w.queries[s, 0], w.eps, w.delta, shortlist=128)
+        for h in range(w.n_kv):
+            got = ctx.shortlist(0, h)
+            want = np.nonzero(rows[h * w.group]["shortlist"])[0]
+            n_cand = int((osl.flags[h] == 0).sum())
+            assert len(want) == min(128, n_cand)
+            if pool == 0:
+                assert n_cand <= 128
+            assert np.array_equal(got, want), (pool, s, h, np.setxor1d(got, want)[:8])
+    ctx.close()
+
+
 @pytest.mark.parametrize("sketch,shrinkage,shape", [("int8", "clipped", "g4"), ("2bit", "clipped", "g4"),
                                                     ("2bit", "binary", "g4"), ("int8", "clipped", "g8"),
                                                     ("exact", "clipped", "tiny")])

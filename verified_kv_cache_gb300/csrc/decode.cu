@@ -723,6 +723,31 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_keys_kernel(Views views,
     if (lane == 0 && nc > 0) atomicAdd(&gh[kSlBins], (unsigned)nc);
 }
 
+// Calls f(key, L index) for every scratch key of a row, eight 16-byte words per thread in flight.
+template <typename F>
+__device__ __forceinline__ void for_each_key(const uint4* __restrict__ sk4, int nl4, int tid, F&& f)
+{
+    constexpr int kB = 8;
+    for (int base = 0; base < nl4; base += kB * kSlThreads) {
+        uint4 kq[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int i4 = base + j * kSlThreads + tid;
+            kq[j] = i4 < nl4 ? sk4[i4] : make_uint4(~0u, ~0u, ~0u, ~0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int li = 4 * (base + j * kSlThreads + tid);
+            f(kq[j].x, li);
+            f(kq[j].y, li + 1);
+            f(kq[j].z, li + 2);
+            f(kq[j].w, li + 3);
+        }
+    }
+}
+
+constexpr int kSlCand = 2048;   // keys of the threshold's first-level bin ranked in shared memory
+
 template <typename T, int G>
 __global__ void __launch_bounds__(kSlThreads) shortlist_select_kernel(Views views, const float* __restrict__ q,
                                                                      DecodeArgs a, RowState* rows, float2* tl,
@@ -740,10 +765,19 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_select_kernel(Views view
     __shared__ unsigned hist[kSlBins];
     __shared__ int s_scan[32];
     __shared__ unsigned s_prefix;
-    __shared__ int s_need, s_count, s_at_thr;
+    __shared__ int s_need, s_count, s_at_thr, s_ncand;
     __shared__ int s_sel[kMaxShortlist];
+    __shared__ uint2 s_cand[kSlCand];
     unsigned* gh = ghist + (int64_t)unit * (kSlBins + 1);
-    const int ntot = (int)gh[kSlBins];
+    // the first-level histogram, every word in flight at once
+    {
+        unsigned hv[kSlBins / kSlThreads];
+#pragma unroll
+        for (int j = 0; j < kSlBins / kSlThreads; ++j) hv[j] = __ldcg(gh + tid + j * kSlThreads);
+#pragma unroll
+        for (int j = 0; j < kSlBins / kSlThreads; ++j) hist[tid + j * kSlThreads] = hv[j];
+    }
+    const int ntot = (int)__ldcg(gh + kSlBins);
     const int k = min(k_short, ntot);
     const int nl4 = (nl + 3) / 4;
     const uint4* sk4 = reinterpret_cast<const uint4*>(skeys + unit * shortlist_stride(a));
@@ -752,30 +786,28 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_select_kernel(Views view
         s_need = k;
         s_count = 0;
         s_at_thr = 0;
+        s_ncand = 0;
     }
-    for (int i = tid; i < kSlBins; i += kSlThreads) hist[i] = gh[i];
     __syncthreads();
     // the histogram is read: leave it clear for the next call
-    for (int i = tid; i <= kSlBins; i += kSlThreads) gh[i] = 0u;
-    const int shifts[3] = {20, 8, 0}, widths[3] = {12, 12, 8};
+#pragma unroll
+    for (int j = 0; j < kSlBins / kSlThreads; ++j) gh[tid + j * kSlThreads] = 0u;
+    if (tid == 0) gh[kSlBins] = 0u;
+    // radix select of the k-th key.  A level stops the search once every key of the digit it found
+    // is taken; after the first level, a bin of at most kSlCand keys is ranked in shared memory.
+    unsigned lowmask = 0u;
+    bool cand = false;
     for (int lev = 0; lev < 3 && k > 0 && k < ntot; ++lev) {
-        const int sh = shifts[lev], wd = widths[lev], nb = 1 << wd;
+        const int sh = lev == 0 ? 20 : lev == 1 ? 8 : 0, wd = lev < 2 ? 12 : 8, nb = 1 << wd;   // 12, 12, 8 bits
         const unsigned prefix = s_prefix;
         const int need = s_need;
         if (lev > 0) {   // level 0 comes from the keys kernel
             for (int i = tid; i < nb; i += kSlThreads) hist[i] = 0u;
             __syncthreads();
-#pragma unroll 4
-            for (int i4 = tid; i4 < nl4; i4 += kSlThreads) {
-                const uint4 kq = sk4[i4];
-                const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const unsigned key = kk[u];
-                    if (key == ~0u || (key >> (sh + wd)) != (prefix >> (sh + wd))) continue;
+            for_each_key(sk4, nl4, tid, [&](unsigned key, int) {
+                if (key != ~0u && (key >> (sh + wd)) == (prefix >> (sh + wd)))
                     atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
-                }
-            }
+            });
             __syncthreads();
         }
         // the digit holding the need-th key: bins of this thread, then a block scan of their sums
@@ -798,39 +830,67 @@ __global__ void __launch_bounds__(kSlThreads) shortlist_select_kernel(Views view
             }
         }
         __syncthreads();
+        if (s_need == s_at_thr) {   // every key of the digit is taken
+            lowmask = (1u << sh) - 1u;
+            break;
+        }
+        if (lev == 0 && s_at_thr <= kSlCand) {
+            cand = true;
+            break;
+        }
     }
-    // selection: keys below the threshold, and the first s_need at it in L order.  When every key
-    // at the threshold is taken (the usual case: no tie across the boundary) one strided pass
-    // takes the keys up to it; otherwise each thread takes a contiguous run of groups of four L
-    // indices, ranked by a block scan.
-    const unsigned thr = s_prefix;
+    // selection.  Candidate path: keys of a first-level bin below the threshold's are taken, those of
+    // its bin are ranked by (key, L index) and the first s_need taken.  Otherwise, when every key at
+    // the threshold is taken (the usual case) one strided pass takes the keys up to it; else each
+    // thread takes a contiguous run of groups of four L indices, ranked by a block scan.
+    const unsigned thr = s_prefix | lowmask;
     const bool all = k >= ntot;
     const int take_eq = s_need;
-    const bool whole = all || take_eq == s_at_thr;
-    if (k > 0 && whole) {
-#pragma unroll 4
-        for (int i4 = tid; i4 < nl4; i4 += kSlThreads) {
-            const uint4 kq = sk4[i4];
-            const unsigned kk[4] = {kq.x, kq.y, kq.z, kq.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (kk[u] == ~0u || !(all || kk[u] <= thr)) continue;
+    const bool whole = !cand && (all || take_eq == s_at_thr);
+    if (cand) {
+        const unsigned b0 = thr >> 20;
+        for_each_key(sk4, nl4, tid, [&](unsigned key, int li) {
+            if (key == ~0u) return;
+            if ((key >> 20) < b0) {
                 const int at = atomicAdd(&s_count, 1);
-                if (at < kMaxShortlist) s_sel[at] = 4 * i4 + u;
+                if (at < kMaxShortlist) s_sel[at] = li;
+            } else if ((key >> 20) == b0) {
+                const int c = atomicAdd(&s_ncand, 1);
+                if (c < kSlCand) s_cand[c] = make_uint2(key, (unsigned)li);
+            }
+        });
+        __syncthreads();
+        const int nc = min(s_ncand, kSlCand);
+        for (int c = tid; c < nc; c += kSlThreads) {
+            const uint2 me = s_cand[c];
+            int r = 0;
+            for (int o = 0; o < nc; ++o) {
+                const uint2 ot = s_cand[o];
+                r += (ot.x < me.x) || (ot.x == me.x && ot.y < me.y);
+            }
+            if (r < take_eq) {
+                const int at = atomicAdd(&s_count, 1);
+                if (at < kMaxShortlist) s_sel[at] = (int)me.y;
             }
         }
     }
+    if (k > 0 && whole)
+        for_each_key(sk4, nl4, tid, [&](unsigned key, int li) {
+            if (key == ~0u || !(all || key <= thr)) return;
+            const int at = atomicAdd(&s_count, 1);
+            if (at < kMaxShortlist) s_sel[at] = li;
+        });
     const int run = (nl4 + kSlThreads - 1) / kSlThreads;
     const int g0 = min(nl4, tid * run), g1 = min(nl4, g0 + run);
     int eq = 0;
-    if (!whole && k > 0)
+    if (!whole && !cand && k > 0)
         for (int i4 = g0; i4 < g1; ++i4) {
             const uint4 kq = sk4[i4];
             eq += (kq.x == thr) + (kq.y == thr) + (kq.z == thr) + (kq.w == thr);
         }
     int eqtot;
     const int eqpre = block_exclusive_scan(eq, s_scan, &eqtot);
-    if (k > 0 && !whole) {
+    if (k > 0 && !whole && !cand) {
         int e = eqpre;
         for (int i4 = g0; i4 < g1; ++i4) {
             const uint4 kq = sk4[i4];
