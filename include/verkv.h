@@ -247,6 +247,28 @@ verkv_status verkv_set_stage_capacity(verkv_ctx* ctx, int64_t rows_per_kv_head);
  */
 verkv_status verkv_set_shortlist(verkv_ctx* ctx, int32_t k);
 
+/*
+ * Decode-time growth (Appendix A.3.1: the per-(layer, head) list of resident positions is extended
+ * as tokens are generated).  verkv_set_append_capacity reserves, at every later verkv_compress, room
+ * for rows_per_kv_head appended tokens per KV head of a slot (512 B per row in bf16, capped at
+ * max_tokens - n).  Default 0.  EINVAL: rows_per_kv_head < 0.
+ *
+ * verkv_append adds n_new generated tokens to the (layer, seq) slot: token ids n + n_appended ...,
+ * the same tokens for every KV head.  They join H (r = 1): resident, scored with exact keys, in the
+ * certificate's denominator and attended with weight 1 by every later verkv_decode; the prefix's
+ * L, S, r and sketch stay as verkv_compress left them.  kv_new: [Hkv][n_new][2][d] rows (K then V)
+ * in the storage dtype, device or pinned host memory, read on `stream` (caller-owned; free to reuse
+ * once the stream has passed the call).  The appended rows live in the slot's device memory until
+ * its next verkv_compress or verkv_release.  n_new = 0 is a no-op.
+ * EINVAL: n_new < 0, kv_new NULL with n_new > 0, or more rows than the reserved room;
+ * ESTATE: the slot holds no compressed context.
+ */
+verkv_status verkv_set_append_capacity(verkv_ctx* ctx, int32_t rows_per_kv_head);
+verkv_status verkv_append(verkv_ctx* ctx, int32_t layer, int32_t seq, int32_t n_new, const void* kv_new,
+                          verkv_stream stream);
+/* Tokens appended to the slot since its last verkv_compress. */
+verkv_status verkv_get_appended(verkv_ctx* ctx, int32_t layer, int32_t seq, int32_t* n_appended);
+
 /* The shortlist of KV head (b, kv_head) in the last verkv_decode (ascending tokens; count 0 when the
  * shortlist is off).  At most `cap` tokens are written. */
 verkv_status verkv_get_shortlist(verkv_ctx* ctx, int32_t b, int32_t kv_head, int32_t* tokens, int32_t cap,

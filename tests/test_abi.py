@@ -38,6 +38,15 @@ def test_status_strings(lib):
     assert lib.verkv_last_error(None) == b"null context"
 
 
+def test_null_context_is_rejected_without_touching_the_gpu(lib):
+    einval = 1
+    assert lib.verkv_set_append_capacity(None, 16) == einval
+    assert lib.verkv_append(None, 0, 0, 1, None, None) == einval
+    assert lib.verkv_get_appended(None, 0, 0, None) == einval
+    assert lib.verkv_set_stage_capacity(None, 0) == einval
+    assert lib.verkv_set_shortlist(None, 8) == einval
+
+
 PROBE = r"""
 #include <stdio.h>
 #include <stddef.h>

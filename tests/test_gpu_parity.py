@@ -5,6 +5,7 @@ sketch codes; c, beta/D and eps_hat within 1e-4 relative; the fetched set exact 
 oracle's gains at the k* boundary are within 1e-6 relative (or the residual certificate is within
 1e-6 of eps); attention output within 2e-3 relative L2.
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -406,6 +407,63 @@ def test_smallest_context():
     _decode_parity(w, gc, osl, w.eps, w.delta)
     _decode_parity(w, gc, osl, 0.0, w.delta)   # eps = 0: the whole of L is made exact
     ctx.close()
+
+
+@pytest.mark.parametrize("sketch", ["int8", "2bit", "exact"])
+def test_appended_tokens_join_h(sketch):
+    """Decode-time growth (App. A.3.1: the resident list grows as tokens are generated): tokens
+    appended after compress are H -- exact logits, in D_cert, attended with weight 1 -- while the
+    prefix's L, S, r and sketch stay as compressed.  Appends of 1, 1 and 298 tokens, a decode after
+    each; the last step's queries point at an appended token.  Against the oracle run on the prefix's
+    compress state with the appended tokens flagged H."""
+    n0, t = 4000, 300
+    full = small_case(sketch, n=n0 + t, steps=3)
+    w0 = dataclasses.replace(full, n=n0, K=full.K[:, :, :n0].copy(), V=full.V[:, :, :n0].copy())
+    rng = np.random.default_rng(23)
+    qs = full.queries.copy()
+    for hq in range(full.n_q):   # step 2: every query row near appended token n0 + 100 of its KV head
+        qs[2, 0, hq] = 3.0 * full.K[0, hq // full.group, n0 + 100] + rng.standard_normal(full.d)
+    ctx = make_lib_ctx(w0, max_tokens=n0 + t)
+    ctx.set_append_capacity(t)
+    gc = GpuCase(w0, ctx)
+    tau, stats, osl = _compress_both(w0, gc)
+    tail = full.kv_host_layout(0)[:, n0:]
+    counts = {"ok": 0, "exempt": 0}
+    done = 0
+    for s, m in enumerate([1, 1, t - 2]):
+        piece = torch.from_numpy(np.ascontiguousarray(tail[:, done:done + m]))
+        if full.kv_dtype == "bf16":
+            piece = piece.view(torch.bfloat16)
+        piece = piece.to("cuda")
+        ctx.append(0, 0, m, piece)
+        done += m
+        assert ctx.appended(0, 0) == done
+        cur = dataclasses.replace(full, n=n0 + done, K=full.K[:, :, :n0 + done], V=full.V[:, :, :n0 + done])
+        out = gc.decode(qs[s], full.eps, full.delta)
+        trace = ctx.decode_trace(full.n_q)
+        rows, _ = oracle_decode(cur, 0, osl, qs[s, 0], full.eps, full.delta)
+        for hq in range(full.n_q):
+            v = check_row(trace[hq], ctx.exact_set(0, hq, cur.n), rows[hq], full.eps, None)
+            if v == "ok":
+                counts["ok"] += 1
+                assert rel_l2(out[0, hq].astype(np.float64), rows[hq]["out"]) <= REL_OUT, (s, hq)
+            else:
+                counts["exempt"] += 1
+    assert counts["ok"] >= 0.9 * sum(counts.values()), counts
+    # the step aimed at an appended token attends mostly to it: the output is near its value row
+    for hq in range(full.n_q):
+        assert rel_l2(out[0, hq].astype(np.float64), full.V[0, hq // full.group, n0 + 100]) < 0.1, hq
+    with pytest.raises(binding_error()):
+        ctx.append(0, 0, 1, piece)   # beyond the room reserved at compress
+    gc.compress(0, tau=tau)          # a new compress drops the appended tokens
+    assert ctx.appended(0, 0) == 0
+    print(sketch, counts)
+    ctx.close()
+
+
+def binding_error():
+    from verified_kv_cache_gb300 import binding
+    return binding.VerkvError
 
 
 def test_staging_cache_reuses_fetched_rows():

@@ -74,42 +74,50 @@ def oracle_decode(w, b, slot: OracleSlot, q_bh: np.ndarray, eps, delta, mode=1, 
     """q_bh: [Hq, d] for sequence b.  Returns per row dicts and per KV head fetch unions and outputs.
     shrinkage: 0 = clipped coefficients (Definition 2), 1 = binary (Appendix A.2).
     shortlist: k > 0 uses exact weights for the sampled tokens and the Appendix A.1 shortlist of k
-    tokens per KV head (each row dict then carries the head's shortlist mask and scores)."""
+    tokens per KV head (each row dict then carries the head's shortlist mask and scores).
+    When w holds more tokens than the slot (w.n > len(slot.flags[h])), the extra tokens are ones
+    appended at decode time: they join H (r = 1) and have no sketch."""
     G = w.group
+    n0 = slot.flags.shape[1]
+    tail = w.n - n0
+    flags = np.concatenate([slot.flags, np.full((w.n_kv, tail), 2, np.uint8)], axis=1)
+    r32 = np.concatenate([slot.r32, np.ones((w.n_kv, tail), np.float32)], axis=1)
     rows = []
     logits = {}
     for hq in range(w.n_q):
         q = q_bh[hq].astype(np.float64)
         h = hq // G
-        logits[hq] = (oracle.logits_exact(q, w.K[b, h]), oracle_sketch_logits(w, b, h, q, slot))
+        ts = oracle_sketch_logits(w, b, h, q, slot)
+        ts = np.concatenate([ts[:n0], np.zeros(tail)])
+        logits[hq] = (oracle.logits_exact(q, w.K[b, h]), ts)
     masks = {}
     if shortlist > 0:
         for h in range(w.n_kv):
             ts_rows = np.stack([logits[h * G + g][1] for g in range(G)])
-            sl = oracle.shortlist(slot.flags[h], ts_rows, shortlist)
+            sl = oracle.shortlist(flags[h], ts_rows, shortlist)
             masks[h] = (sl, ts_rows.max(axis=0))
     for hq in range(w.n_q):
         h = hq // G
         te, ts = logits[hq]
         use = None
         if shortlist > 0:
-            use = masks[h][0] | (slot.flags[h] == 1)
-        res = oracle.kvfetch_row(slot.flags[h], slot.r32[h], te, ts, eps, delta, mode=mode, shrinkage=shrinkage,
+            use = masks[h][0] | (flags[h] == 1)
+        res = oracle.kvfetch_row(flags[h], r32[h], te, ts, eps, delta, mode=mode, shrinkage=shrinkage,
                                  use_exact=use)
         if shortlist > 0:
             res["shortlist"], res["sl_score"] = masks[h]
         if shrinkage == 1:
-            Lm = slot.flags[h] != 2
+            Lm = flags[h] != 2
             res["w_l"] = np.exp((ts if use is None else np.where(use, te, ts))[Lm] - res["m"])
-            res["r_l"] = slot.r32[h][Lm].astype(np.float64)
+            res["r_l"] = r32[h][Lm].astype(np.float64)
             res["n_shrunk"] = int((res["lam"][Lm] < 1.0).sum())
-        res["out"] = oracle.attention_row(slot.flags[h], slot.r32[h], te, w.V[b, h], res["lam"], res["exact_mask"])
+        res["out"] = oracle.attention_row(flags[h], r32[h], te, w.V[b, h], res["lam"], res["exact_mask"])
         rows.append(res)
     unions = []
     for h in range(w.n_kv):
         u = np.zeros(w.n, bool)
         for g in range(G):
-            u |= rows[h * G + g]["exact_mask"] & (slot.flags[h] == 0)
+            u |= rows[h * G + g]["exact_mask"] & (flags[h] == 0)
         unions.append(np.nonzero(u)[0])
     return rows, unions
 

@@ -108,6 +108,12 @@ def lib():
     L.verkv_get_shortlist.restype = st
     L.verkv_set_stage_capacity.argtypes = [P, ctypes.c_int64]
     L.verkv_set_stage_capacity.restype = st
+    L.verkv_set_append_capacity.argtypes = [P, i32]
+    L.verkv_set_append_capacity.restype = st
+    L.verkv_append.argtypes = [P, i32, i32, i32, P, P]
+    L.verkv_append.restype = st
+    L.verkv_get_appended.argtypes = [P, i32, i32, P]
+    L.verkv_get_appended.restype = st
     L.verkv_get_row_weights.argtypes = [P, i32, i32, P, P, i32, P, P]
     L.verkv_get_row_weights.restype = st
     L.verkv_last_launch_count.argtypes = [P]
@@ -274,6 +280,20 @@ class VerKV:
     def set_stage_capacity(self, rows_per_kv_head: int):
         """Staging cache rows per KV head and slot: -1 = all of L minus S, 0 = off (next compress on)."""
         self._check(lib().verkv_set_stage_capacity(self.h, int(rows_per_kv_head)))
+
+    def set_append_capacity(self, rows_per_kv_head: int):
+        """Room reserved per KV head and slot for tokens appended at decode time (next compress on)."""
+        self._check(lib().verkv_set_append_capacity(self.h, int(rows_per_kv_head)))
+
+    def append(self, layer, seq, n_new, kv_new, stream=None):
+        """Append n_new generated tokens to H of the slot: kv_new holds [Hkv][n_new][2][d] rows in the
+        storage dtype, in device or pinned host memory."""
+        self._check(lib().verkv_append(self.h, layer, seq, int(n_new), _ptr(kv_new), _stream(stream)))
+
+    def appended(self, layer, seq) -> int:
+        n = ctypes.c_int32()
+        self._check(lib().verkv_get_appended(self.h, layer, seq, ctypes.byref(n)))
+        return n.value
 
     def row_weights(self, b, h, cap, stream=None):
         w = np.zeros(max(cap, 1), np.float32)

@@ -444,6 +444,51 @@ verkv_status verkv_set_stage_capacity(verkv_ctx* h, int64_t rows_per_kv_head)
     return VERKV_OK;
 }
 
+verkv_status verkv_set_append_capacity(verkv_ctx* h, int32_t rows_per_kv_head)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (rows_per_kv_head < 0) return fail(ctx, VERKV_EINVAL, "append capacity must be >= 0");
+    ctx.append_rows = rows_per_kv_head;
+    return VERKV_OK;
+}
+
+verkv_status verkv_append(verkv_ctx* h, int32_t layer, int32_t seq, int32_t n_new, const void* kv_new,
+                          verkv_stream stream)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (!slot_ok(ctx, layer, seq)) return fail(ctx, VERKV_EINVAL, "layer/seq slot out of range");
+    if (n_new < 0 || (n_new > 0 && !kv_new)) return fail(ctx, VERKV_EINVAL, "bad appended rows");
+    Slot& s = ctx.slot(layer, seq);
+    if (!s.live) return fail(ctx, VERKV_ESTATE, "slot was not compressed");
+    if (n_new == 0) return VERKV_OK;
+    if ((int64_t)s.n_tail + n_new > s.cap_tail)
+        return fail(ctx, VERKV_EINVAL, "appended tokens exceed the room reserved at compress");
+    // one copy per KV head: its n_new rows go after its resident rows and earlier appended rows
+    const size_t row_bytes = 2 * kHeadDim * ctx.elt;
+    cudaStream_t st = (cudaStream_t)stream;
+    for (int kv = 0; kv < ctx.cfg.n_kv_heads; ++kv) {
+        const int64_t row = s.res_off_host[kv] + s.stats[kv].n_resident + s.n_tail;
+        VK_CUDA(cudaMemcpyAsync(static_cast<unsigned char*>(s.kvres) + row * row_bytes,
+                                static_cast<const unsigned char*>(kv_new) + (size_t)kv * n_new * row_bytes,
+                                (size_t)n_new * row_bytes, cudaMemcpyDefault, st));
+    }
+    s.n_tail += n_new;
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_appended(verkv_ctx* h, int32_t layer, int32_t seq, int32_t* n_appended)
+{
+    if (!h || !n_appended) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (!slot_ok(ctx, layer, seq)) return fail(ctx, VERKV_EINVAL, "layer/seq slot out of range");
+    Slot& s = ctx.slot(layer, seq);
+    if (!s.live) return fail(ctx, VERKV_ESTATE, "slot was not compressed");
+    *n_appended = s.n_tail;
+    return VERKV_OK;
+}
+
 verkv_status verkv_get_row_weights(verkv_ctx* h, int32_t b, int32_t hq, float* w_hat, int32_t* tokens, int32_t cap,
                                    int32_t* count, verkv_stream stream)
 {

@@ -893,6 +893,9 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
     VK_CUDA(cudaStreamSynchronize(st));
     s.res_off_host.assign((size_t)Hkv + 1, 0);
     s.stats.assign((size_t)Hkv, verkv_head_stats{});
+    // room for tokens appended at decode time after each head's resident rows (empty until then)
+    s.n_tail = 0;
+    s.cap_tail = std::max(0, std::min(ctx.append_rows, ctx.cfg.max_tokens - n));
     int max_res = 0;
     for (int h = 0; h < Hkv; ++h) {
         verkv_head_stats& hs = s.stats[h];
@@ -902,7 +905,7 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
         hs.n_l = counts[h * 4 + 1];
         hs.n_s = counts[h * 4 + 2];
         hs.n_resident = counts[h * 4 + 3];
-        s.res_off_host[h + 1] = s.res_off_host[h] + hs.n_resident;
+        s.res_off_host[h + 1] = s.res_off_host[h] + hs.n_resident + s.cap_tail;
         max_res = std::max(max_res, hs.n_resident);
     }
     const size_t row_bytes = 2 * kHeadDim * ctx.elt;

@@ -88,7 +88,7 @@ __global__ void init_rows_kernel(RowState* __restrict__ rows, Views views, Decod
     RowState s;
     memset(&s, 0, sizeof(s));
     s.m_tag = 0;
-    s.n_h = views.v[b].counts[kv * 4 + 0];
+    s.n_h = views.v[b].counts[kv * 4 + 0] + views.v[b].n_tail;   // appended tokens are H
     s.n_l = views.v[b].counts[kv * 4 + 1];
     s.b_arg = -1;
     rows[row] = s;
@@ -123,7 +123,7 @@ __device__ __forceinline__ void score_h_tile1(const Views& views, const float* _
     const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
     const SlotView& V = views.v[b];
     const int n = V.n;
-    const int nh = V.counts[kv * 4 + 0];
+    const int nh0 = V.counts[kv * 4 + 0], nh = nh0 + V.n_tail;   // H of the compress, then appended tokens
     const int t = threadIdx.x;
     const int part = t & 7, g = (t >> 3) % G, tk = t / (8 * G);
     const int hk = tile * TPB + tk;
@@ -132,7 +132,7 @@ __device__ __forceinline__ void score_h_tile1(const Views& views, const float* _
     ff s = {0.f, 0.f};
     int slot = 0;
     if (live) {
-        slot = V.hslot[(int64_t)kv * n + hk];
+        slot = hk < nh0 ? V.hslot[(int64_t)kv * n + hk] : V.counts[kv * 4 + 3] + (hk - nh0);
         const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + slot) * 2 * kHeadDim + part * 16;
         const float* qr = q + (int64_t)row * kHeadDim + part * 16;
         float kk[16], qq[16];
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kTile, kInt8CtasPerSm) score_int8_kernel(Views
     if (nt > 0) score_int8_ltiles<T, G>(views, q, a, rows, tl, b, kv, t0, nt);
     // the exact logits of the KV head's H tokens, shared out over its CTAs
     constexpr int TPB = kTile / (8 * G);
-    const int nh_tiles = (V.counts[kv * 4 + 0] + TPB - 1) / TPB;
+    const int nh_tiles = (V.counts[kv * 4 + 0] + V.n_tail + TPB - 1) / TPB;
     for (int ht = blockIdx.x; ht < nh_tiles; ht += gridDim.x) score_h_tile1<T, G>(views, q, a, rows, th, ht);
 }
 
@@ -1960,7 +1960,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const int b = row / a.Hq, kv = (row % a.Hq) / a.G;
     const SlotView& V = views.v[b];
     RowState& R = rows[row];
-    const int nl = V.counts[kv * 4 + 1], nh = V.counts[kv * 4 + 0];
+    const int nl = V.counts[kv * 4 + 1], nh = V.counts[kv * 4 + 0] + V.n_tail;
     const int S = (nl + C - 1) / C;
     const int j0 = min(nl, rank * S), j1 = min(nl, j0 + S), ns = j1 - j0;
     const float* rl = V.rl + (int64_t)kv * V.n;
@@ -2851,7 +2851,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
     const SlotView& V = views.v[b];
-    const int m_res = V.counts[kv * 4 + 3];
+    // resident rows: H u S of the compress (weights from om), then the appended tokens (weight 1)
+    const int m_cmp = V.counts[kv * 4 + 3];
+    const int m_res = m_cmp + V.n_tail;
     const int row0 = row_of(b, kv * G, a.Hq);   // the G query rows of the KV head are consecutive
     int32_t* ulw = ulist + (int64_t)unit * a.ws_n;
     uint8_t* umw = umask + (int64_t)unit * a.ws_n;
@@ -3035,7 +3037,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
             const int r = e / G, g = e % G, R = r0 + r;
             float w = 0.f;
             if (e < CR * G && R < r1)
-                w = R < m_res ? a.om[(int64_t)(row0 + g) * a.ws_n + R] : (float)((um[R - m_res] >> g) & 1u);
+                w = R < m_cmp   ? a.om[(int64_t)(row0 + g) * a.ws_n + R]
+                    : R < m_res ? 1.f
+                                : (float)((um[R - m_res] >> g) & 1u);
             o[u] = w;
         }
     };
@@ -3442,6 +3446,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         Slot& s = ctx.slot(layer, seq_ids[b]);
         SlotView& v = views.v[b];
         v.n = s.n;
+        v.n_tail = s.n_tail;
         v.r = s.r;
         v.flags = s.flags;
         v.lpos = s.lpos;
@@ -3470,7 +3475,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         max_n = std::max(max_n, s.n);
         for (const verkv_head_stats& hs : s.stats) {
             max_nl = std::max(max_nl, hs.n_l);
-            max_nh = std::max(max_nh, hs.n_h);
+            max_nh = std::max(max_nh, hs.n_h + s.n_tail);
             max_res = std::max(max_res, hs.n_resident);
         }
         ctx.last_n.push_back(s.n);

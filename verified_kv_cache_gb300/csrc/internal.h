@@ -18,6 +18,8 @@ struct Slot {
     int n = 0;
     int cap_n = 0;              // token capacity of the per-token arrays (reused while n <= cap_n)
     size_t cap_res = 0;         // resident rows kvres can hold
+    int n_tail = 0;             // tokens appended since compress (ids n ..): H, rows after each head's H u S
+    int cap_tail = 0;           // room for appended rows per KV head, reserved in kvres
     const void* kv_host = nullptr;  // borrowed pinned [Hkv][n][2][d]
 
     float* tau = nullptr;       // [Hkv][n] importance scores after clamping / forcing
@@ -33,7 +35,8 @@ struct Slot {
     int32_t* counts = nullptr;  // [Hkv][4] |H|, |L|, |S|, |H|+|S|
     double* c = nullptr;        // [Hkv] water-filling constant
     int32_t* capped = nullptr;  // [Hkv] tokens outside sink/local with r = 1
-    void* kvres = nullptr;      // [sum_h m_h][2][d] resident K/V rows, head h from res_off[h]
+    void* kvres = nullptr;      // [sum_h (m_h + cap_tail)][2][d] resident K/V rows, head h from res_off[h]:
+                                // its m_h rows of H u S, then the appended rows
     int64_t* res_off = nullptr; // device [Hkv + 1] row offsets into kvres
 
     // sketches
@@ -133,6 +136,7 @@ struct Ctx {
     uint32_t* shist = nullptr;      // [max_batch][Hkv][kShortlistBins + 1] shortlist first-level histogram + count
                                     // (zero between calls)
     int64_t stage_rows = -1;        // staging capacity per KV head and slot: -1 = all of L \ S, 0 = off
+    int append_rows = 0;            // room reserved per KV head and slot for decode-time appended tokens
     int* h_err = nullptr;           // mapped pinned host word: a device-side bounded wait gave up
     int* d_err = nullptr;           // its device address
 
@@ -149,7 +153,7 @@ struct Ctx {
 // Slot pointers for the decode kernels (device-side copy, one entry per b).
 struct SlotView {
     int n;
-    int pad;
+    int n_tail;                  // appended tokens (H), rows m_h .. m_h + n_tail - 1 of the head in kvres
     const float* r;
     const uint8_t* flags;
     const int32_t* lpos;
