@@ -388,6 +388,7 @@ def run_verkv(args):
         secondary["binary_shrinkage"] = binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush)
         secondary["deployed_binary_shortlist128"] = binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush,
                                                                shortlist=128)
+        secondary["growth_append1"] = growth_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush)
     ctx.close()
     if rank == 0 and not args.no_secondary:
         del kv_dev, flush_buf
@@ -487,6 +488,43 @@ def binary_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush, shortlist=0):
             "fetch_fraction_per_token": statistics.mean(fetch), "no_fetch_rate": nof / len(ks),
             "mean_kstar": statistics.mean(ks), "mean_n_shrunk": statistics.mean(shr),
             "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()}}
+
+
+def growth_run(args, w, kv_host, kv_dev, obs, q_dev, st, flush):
+    """A serving loop on the same workload (decode-time growth, App. A.3.1): before each of the 64
+    decode calls one generated token (random bf16 K/V rows, one per KV head, already on the device)
+    is appended to H with verkv_append.  Time per step = append + decode (per-step events, L2 flushed
+    before every step); the context grows from n to n + 64 over the job."""
+    import torch
+
+    from verified_kv_cache_gb300 import binding
+    W, S = w.obs_q.shape[2], w.queries.shape[0]
+    ctx = binding.VerKV(n_kv_heads=w.n_kv, n_q_heads=w.n_q, max_tokens=w.n + S, n_layers=1, n_seqs=1, max_batch=1,
+                        n_sink=w.n_sink, n_local=w.n_local, eta=w.eta, seed=w.seed, sketch=w.sketch,
+                        kv_dtype=w.kv_dtype)
+    ctx.set_append_capacity(S)
+    g = torch.Generator(device=q_dev.device).manual_seed(31)
+    new_kv = torch.randn((S, w.n_kv, 1, 2, w.d), generator=g, device=q_dev.device).to(torch.bfloat16)
+    out = torch.empty_like(q_dev)
+    ms = []
+    for rep in range(1 + max(1, args.steps)):   # the first job is a warm-up
+        ctx.compress(0, 0, w.n, kv_host, kv_dev, obs, W, None, st)
+        for s in range(S):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            ctx.append(0, 0, 1, new_kv[s], st)
+            ctx.decode(0, [0], q_dev[s], w.eps, w.delta, out[s], st)
+            b.record(st)
+            if rep > 0:
+                ms.append((a, b))
+    torch.cuda.synchronize()
+    assert ctx.appended(0, 0) == S
+    step_ms = [a.elapsed_time(b) for a, b in ms]
+    ctx.close()
+    return {"workload": "the bench layer with one token appended to H before every decode call",
+            "us_per_step": statistics.mean(step_ms) * 1e3, "us_p50": statistics.median(step_ms) * 1e3,
+            "tokens_appended_per_job": S}
 
 
 def stack_run(args, dev, st, hbm_peak, peak_src):
