@@ -257,10 +257,11 @@ verkv_status verkv_set_shortlist(verkv_ctx* ctx, int32_t k);
  * the same tokens for every KV head.  They join H (r = 1): resident, scored with exact keys, in the
  * certificate's denominator and attended with weight 1 by every later verkv_decode; the prefix's
  * L, S, r and sketch stay as verkv_compress left them.  kv_new: [Hkv][n_new][2][d] rows (K then V)
- * in the storage dtype, device or pinned host memory, read on `stream` (caller-owned; free to reuse
- * once the stream has passed the call).  The appended rows live in the slot's device memory until
- * its next verkv_compress or verkv_release.  n_new = 0 is a no-op.
- * EINVAL: n_new < 0, kv_new NULL with n_new > 0, or more rows than the reserved room;
+ * in the storage dtype, 16-byte aligned, in device or pinned host memory, read by one kernel on
+ * `stream` (caller-owned; free to reuse once the stream has passed the call).  The appended rows live
+ * in the slot's device memory until its next verkv_compress or verkv_release.  n_new = 0 is a no-op.
+ * EINVAL: n_new < 0, kv_new NULL with n_new > 0, misaligned or in pageable host memory, or more rows
+ * than the reserved room;
  * ESTATE: the slot holds no compressed context.
  */
 verkv_status verkv_set_append_capacity(verkv_ctx* ctx, int32_t rows_per_kv_head);

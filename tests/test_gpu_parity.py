@@ -413,8 +413,8 @@ def test_smallest_context():
 def test_appended_tokens_join_h(sketch):
     """Decode-time growth (App. A.3.1: the resident list grows as tokens are generated): tokens
     appended after compress are H -- exact logits, in D_cert, attended with weight 1 -- while the
-    prefix's L, S, r and sketch stay as compressed.  Appends of 1, 1 and 298 tokens, a decode after
-    each; the last step's queries point at an appended token.  Against the oracle run on the prefix's
+    prefix's L, S, r and sketch stay as compressed.  Appends of 1 (from pinned host memory), 1 and 298
+    tokens (device memory), a decode after each; the last step's queries point at an appended token.  Against the oracle run on the prefix's
     compress state with the appended tokens flagged H."""
     n0, t = 4000, 300
     full = small_case(sketch, n=n0 + t, steps=3)
@@ -434,7 +434,7 @@ def test_appended_tokens_join_h(sketch):
         piece = torch.from_numpy(np.ascontiguousarray(tail[:, done:done + m]))
         if full.kv_dtype == "bf16":
             piece = piece.view(torch.bfloat16)
-        piece = piece.to("cuda")
+        piece = piece.pin_memory() if s == 0 else piece.to("cuda")   # pinned host rows, then device rows
         ctx.append(0, 0, m, piece)
         done += m
         assert ctx.appended(0, 0) == done

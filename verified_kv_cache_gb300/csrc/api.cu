@@ -465,17 +465,12 @@ verkv_status verkv_append(verkv_ctx* h, int32_t layer, int32_t seq, int32_t n_ne
     if (n_new == 0) return VERKV_OK;
     if ((int64_t)s.n_tail + n_new > s.cap_tail)
         return fail(ctx, VERKV_EINVAL, "appended tokens exceed the room reserved at compress");
-    // one copy per KV head: its n_new rows go after its resident rows and earlier appended rows
-    const size_t row_bytes = 2 * kHeadDim * ctx.elt;
-    cudaStream_t st = (cudaStream_t)stream;
-    for (int kv = 0; kv < ctx.cfg.n_kv_heads; ++kv) {
-        const int64_t row = s.res_off_host[kv] + s.stats[kv].n_resident + s.n_tail;
-        VK_CUDA(cudaMemcpyAsync(static_cast<unsigned char*>(s.kvres) + row * row_bytes,
-                                static_cast<const unsigned char*>(kv_new) + (size_t)kv * n_new * row_bytes,
-                                (size_t)n_new * row_bytes, cudaMemcpyDefault, st));
-    }
-    s.n_tail += n_new;
-    return VERKV_OK;
+    if (reinterpret_cast<uintptr_t>(kv_new) % 16 != 0) return fail(ctx, VERKV_EINVAL, "appended rows must be 16-byte aligned");
+    cudaPointerAttributes pa;
+    VK_CUDA(cudaPointerGetAttributes(&pa, kv_new));
+    if (pa.type == cudaMemoryTypeUnregistered)   // read by a kernel: device or page-locked host memory only
+        return fail(ctx, VERKV_EINVAL, "appended rows must be in device or pinned host memory");
+    return append_rows(ctx, s, n_new, kv_new, (cudaStream_t)stream);
 }
 
 verkv_status verkv_get_appended(verkv_ctx* h, int32_t layer, int32_t seq, int32_t* n_appended)

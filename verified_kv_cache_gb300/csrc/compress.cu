@@ -806,6 +806,30 @@ void free_slot(Slot& s)
     s = Slot();
 }
 
+// Decode-time growth: n_new rows per KV head (src [Hkv][n_new][row], 16-byte words) go after the head's
+// resident rows and the rows appended before them.
+__global__ void append_rows_kernel(const uint4* __restrict__ src, int n_new, int words, const int64_t* __restrict__ res_off,
+                                   const int32_t* __restrict__ counts, int n_tail, uint4* __restrict__ kvres)
+{
+    const int kv = blockIdx.y;
+    const int64_t row0 = res_off[kv] + counts[kv * 4 + 3] + n_tail;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n_new * words; e += gridDim.x * blockDim.x) {
+        const int j = e / words, w = e % words;
+        kvres[(row0 + j) * words + w] = src[((int64_t)kv * n_new + j) * words + w];
+    }
+}
+
+verkv_status append_rows(Ctx& ctx, Slot& s, int n_new, const void* src, cudaStream_t st)
+{
+    const int words = (int)(2 * kHeadDim * ctx.elt / 16);
+    const int blocks = std::max(1, std::min(64, (n_new * words + 255) / 256));
+    append_rows_kernel<<<dim3(blocks, ctx.cfg.n_kv_heads), 256, 0, st>>>(
+        static_cast<const uint4*>(src), n_new, words, s.res_off, s.counts, s.n_tail, static_cast<uint4*>(s.kvres));
+    VK_CUDA(cudaGetLastError());
+    s.n_tail += n_new;
+    return VERKV_OK;
+}
+
 verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const void* kv_host, const void* kv_dev,
                            const float* obs_q, int W, const float* tau, cudaStream_t st)
 {

@@ -185,6 +185,7 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
 verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, const float* q, double eps,
                          double delta, float* out, cudaStream_t st);
 void free_slot(Slot& s);
+verkv_status append_rows(Ctx& ctx, Slot& s, int n_new, const void* src, cudaStream_t st);
 
 }  // namespace verkv
 
