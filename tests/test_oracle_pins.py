@@ -658,6 +658,38 @@ def test_eps_zero_fetches_everything_and_equals_dense_attention():
     assert np.allclose(out, sdpa, rtol=1e-10, atol=1e-12)
 
 
+@pytest.mark.parametrize("sketch", ["int8", "2bit"])
+def test_appended_tokens_at_eps_zero_equal_dense_attention(sketch):
+    """Decode-time growth (App. A.3.1): tokens appended after compress are H.  At eps = 0 every token of
+    L is fetched, so the decision over the compressed prefix plus the appended tokens must return plain
+    softmax attention over all of them (closed form), whatever the prefix's sample; and the certificate
+    denominator must count the appended tokens (D = sum of every exact weight when the sketch is exact
+    on H, checked here through the output).  Pins the test harness's extension of a compressed slot."""
+    import dataclasses
+
+    from vkcase import oracle_compress, oracle_decode, oracle_tau
+    from verified_kv_cache_gb300 import workloads
+    n0, t = 700, 40
+    full = workloads.qwen_layer_case(seed=5, n=n0 + t, n_kv=1, n_q=2, n_needles=2, W=4, steps=2, sketch=sketch,
+                                     eta=0.25, eps=0.0, delta=0.05, n_sink=4, n_local=64)
+    w0 = dataclasses.replace(full, n=n0, K=full.K[:, :, :n0], V=full.V[:, :, :n0])
+    osl = oracle_compress(w0, 0, oracle_tau(w0, 0))
+    for s in range(2):
+        rows, unions = oracle_decode(full, 0, osl, full.queries[s, 0], 0.0, 0.05)
+        assert len(unions[0]) == int((osl.flags[0] == 0).sum())   # all of L minus S, nothing appended
+        for hq in range(full.n_q):
+            q = full.queries[s, 0, hq].astype(np.float64)
+            K, V = full.K[0, 0].astype(np.float64), full.V[0, 0].astype(np.float64)
+            lg = K @ q / math.sqrt(full.d)
+            p = np.exp(lg - lg.max())
+            dense = (p[:, None] * V).sum(0) / p.sum()
+            assert np.allclose(rows[hq]["out"], dense, rtol=1e-10, atol=1e-12), (s, hq)
+            if s == 1:   # a random query spreads its weight: the appended tokens carry a visible share
+                p0 = p[:n0]
+                prefix_only = (p0[:, None] * V[:n0]).sum(0) / p0.sum()
+                assert not np.allclose(prefix_only, dense, rtol=1e-6, atol=1e-8)
+
+
 def test_no_fetch_estimator_is_horvitz_thompson_when_lambda_is_one():
     """With lambda = 1 the estimator (5) is unbiased (Horvitz-Thompson): the
     exact expectation over all outcomes equals D.  The oracle's attention with
