@@ -280,6 +280,14 @@ verkv_status verkv_get_shortlist(verkv_ctx* ctx, int32_t b, int32_t kv_head, int
 verkv_status verkv_get_row_weights(verkv_ctx* ctx, int32_t b, int32_t h, float* w_hat, int32_t* tokens,
                                    int32_t cap, int32_t* count, verkv_stream stream);
 
+/* Failure-path self test (no counterpart in the paper).  Every device-side wait of the decode and
+ * compress kernels (mbarrier waits for asynchronous copies) is bounded: when it gives up, the kernel
+ * raises the context's mapped error word, leaves its in-flight copies to land and returns, and the
+ * next call reports VERKV_ETIMEOUT.  This call takes that path on purpose: it launches one block whose
+ * bounded wait is given a barrier that nothing completes, synchronises `stream`, and returns
+ * VERKV_ETIMEOUT (VERKV_OK would mean the wait did not give up).  The context stays usable. */
+verkv_status verkv_selftest_wait_timeout(verkv_ctx* ctx, verkv_stream stream);
+
 /* Number of kernels the last verkv_decode / verkv_compress enqueued. */
 int32_t verkv_last_launch_count(const verkv_ctx* ctx);
 

@@ -45,6 +45,7 @@ def test_null_context_is_rejected_without_touching_the_gpu(lib):
     assert lib.verkv_get_appended(None, 0, 0, None) == einval
     assert lib.verkv_set_stage_capacity(None, 0) == einval
     assert lib.verkv_set_shortlist(None, 8) == einval
+    assert lib.verkv_selftest_wait_timeout(None, None) == einval
 
 
 PROBE = r"""

@@ -466,6 +466,22 @@ def binding_error():
     return binding.VerkvError
 
 
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """Failure detection without a GPU fault: a kernel whose bounded mbarrier wait is given nothing to
+    wait for gives up, raises the context's error word, and the call reports VERKV_ETIMEOUT; the next
+    decode of the same context runs and returns the same output as before."""
+    w = small_case("int8", n=3000, steps=2)
+    ctx = make_lib_ctx(w)
+    gc = GpuCase(w, ctx)
+    _compress_both(w, gc)
+    before = gc.decode(w.queries[1], w.eps, w.delta)
+    assert ctx.selftest_wait_timeout() == 4   # VERKV_ETIMEOUT
+    assert ctx.selftest_wait_timeout() == 4   # the word was cleared by the report and raised again
+    after = gc.decode(w.queries[1], w.eps, w.delta)
+    assert np.array_equal(before, after)
+    ctx.close()
+
+
 def test_staging_cache_reuses_fetched_rows():
     """Rows fetched over the host link are staged in device memory and read from there by later
     decodes of the slot: repeating a decode moves no row over the link and gives bit-identical

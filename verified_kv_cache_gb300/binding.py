@@ -108,6 +108,8 @@ def lib():
     L.verkv_get_shortlist.restype = st
     L.verkv_set_stage_capacity.argtypes = [P, ctypes.c_int64]
     L.verkv_set_stage_capacity.restype = st
+    L.verkv_selftest_wait_timeout.argtypes = [P, P]
+    L.verkv_selftest_wait_timeout.restype = st
     L.verkv_set_append_capacity.argtypes = [P, i32]
     L.verkv_set_append_capacity.restype = st
     L.verkv_append.argtypes = [P, i32, i32, i32, P, P]
@@ -280,6 +282,11 @@ class VerKV:
     def set_stage_capacity(self, rows_per_kv_head: int):
         """Staging cache rows per KV head and slot: -1 = all of L minus S, 0 = off (next compress on)."""
         self._check(lib().verkv_set_stage_capacity(self.h, int(rows_per_kv_head)))
+
+    def selftest_wait_timeout(self, stream=None) -> int:
+        """Run the failure-path self test; returns its status (VERKV_ETIMEOUT = 4 when the bounded wait
+        gave up as intended)."""
+        return int(lib().verkv_selftest_wait_timeout(self.h, _stream(stream)))
 
     def set_append_capacity(self, rows_per_kv_head: int):
         """Room reserved per KV head and slot for tokens appended at decode time (next compress on)."""

@@ -6,6 +6,7 @@
 #include <new>
 #include <vector>
 
+#include "async.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -94,6 +95,18 @@ bool take_device_timeout(Ctx& ctx)
 bool slot_ok(const Ctx& c, int layer, int seq)
 {
     return layer >= 0 && layer < c.cfg.n_layers && seq >= 0 && seq < c.cfg.n_seqs;
+}
+
+// One block waits on an mbarrier that nothing arrives at, with the bounded wait every kernel uses
+// (a shorter limit), and raises the error word when it gives up.
+__global__ void wait_timeout_kernel(int* err)
+{
+    __shared__ unsigned long long bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait(&bar, 0u, 1u << 14)) *(volatile int*)err = 1;
+    }
 }
 
 }  // namespace
@@ -441,6 +454,20 @@ verkv_status verkv_set_stage_capacity(verkv_ctx* h, int64_t rows_per_kv_head)
     Ctx& ctx = h->c;
     if (rows_per_kv_head < -1) return fail(ctx, VERKV_EINVAL, "staging capacity must be -1, 0 or positive");
     ctx.stage_rows = rows_per_kv_head;
+    return VERKV_OK;
+}
+
+verkv_status verkv_selftest_wait_timeout(verkv_ctx* h, verkv_stream stream)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    cudaStream_t st = (cudaStream_t)stream;
+    VK_CUDA(cudaStreamSynchronize(st));
+    if (take_device_timeout(ctx)) return fail(ctx, VERKV_ETIMEOUT, "a bounded device-side wait gave up in an earlier call");
+    wait_timeout_kernel<<<1, 32, 0, st>>>(ctx.d_err);
+    VK_CUDA(cudaGetLastError());
+    VK_CUDA(cudaStreamSynchronize(st));
+    if (take_device_timeout(ctx)) return fail(ctx, VERKV_ETIMEOUT, "the self-test wait gave up, as intended");
     return VERKV_OK;
 }
 
