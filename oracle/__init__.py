@@ -85,6 +85,8 @@ def lib():
             L.vko_binary_shrinkage.argtypes = [i64, P, P, P, P]
             L.vko_binary_shrinkage.restype = f64
             L.vko_attention_row.argtypes = [i64, i32, P, P, P, P, P, P, P]
+            L.vko_estimate_row.argtypes = [i64, i32, P, P, P, P, P, P, f64, P]
+            L.vko_estimate_row.restype = f64
             L.vko_kvfetch_rows.argtypes = [i64, i64, P, P, P, P, P, f64, f64, i32, i32, P, P, i32]
             L.vko_kvfetch_rows.restype = i32
             L.vko_num_threads.restype = i32
@@ -275,6 +277,25 @@ def attention_row(flags, r32, t_exact, V, lam, exact_mask):
     lib().vko_attention_row(flags.shape[0], V.shape[1], _p(flags), _p(r32), _p(te), _p(V), _p(lam), _p(mask),
                             _p(out))
     return out
+
+
+def estimate_row(flags, r32, t_exact, lam, exact_mask, m: float = 0.0, V=None):
+    """Definition 2 / eq. (5) after the fetch: (D^, N^) with weights exp(t_exact - m); flags carry the
+    sample outcome (1 = sampled).  N^ is None when V is None."""
+    flags = _c(flags, np.uint8)
+    r32 = _c(r32, np.float32)
+    te = _c(t_exact, np.float64)
+    lam = _c(lam, np.float64)
+    mask = _c(exact_mask, np.uint8)
+    if V is None:
+        den = lib().vko_estimate_row(flags.shape[0], 0, _p(flags), _p(r32), _p(te), None, _p(lam), _p(mask),
+                                     float(m), None)
+        return den, None
+    V = _c(V, np.float64)
+    num = np.zeros(V.shape[1], np.float64)
+    den = lib().vko_estimate_row(flags.shape[0], V.shape[1], _p(flags), _p(r32), _p(te), _p(V), _p(lam), _p(mask),
+                                 float(m), _p(num))
+    return den, num
 
 
 def kvfetch_rows(flags, r32, kv_of, t_exact, t_sketch, eps, delta, mode=1, threads=0, shrinkage=0):

@@ -715,10 +715,35 @@ int vko_kvfetch_row_ex(int64_t n, const uint8_t* flags, const float* r32, const 
 }
 
 /* ------------------------------------------------------------------------ */
-/* Final attention (comment after Algorithm 2; estimator of Theorem 2):     */
-/* o = sum_i omega_i w_i V_i / sum_i omega_i w_i over exact logits, with    */
-/* omega = 1 on H and on the tokens made exact, lambda_i / r_i on the rest  */
-/* of the sample S, and 0 on unsampled tokens of L that were not fetched.   */
+/* The estimator of Definition 2 / eq. (5) after the fetch (Theorem 2):     */
+/*   D^ = sum_H w_i + sum_{L_g[:k*]} w_i + sum_{S \ L_g[:k*]} lambda_i w_i / r_i */
+/* and the numerator N^ with the same weights on the value rows, where w_i  */
+/* = exp(t_i - m) is the EXACT weight (the keys of the sample are resident, */
+/* those of L_g[:k*] are fetched).  Tokens of L outside the sample and not  */
+/* fetched contribute nothing (their Z_i = 0).  flags encode the sample     */
+/* outcome (1 = Z_i = 1).  Writes num[d] and returns D^ (units exp(-m)).     */
+/* ------------------------------------------------------------------------ */
+double vko_estimate_row(int64_t n, int d, const uint8_t* flags, const float* r32, const double* t_exact,
+                        const double* V, const double* lambda, const uint8_t* exact_mask, double m, double* num)
+{
+    double den = 0.0;
+    if (num) for (int c = 0; c < d; ++c) num[c] = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double om;
+        if (flags[i] == 2 || (exact_mask && exact_mask[i])) om = 1.0;
+        else if (flags[i] == 1) om = lambda[i] / (double)r32[i];
+        else continue;
+        double wt = om * exp(t_exact[i] - m);
+        den += wt;
+        if (num) for (int c = 0; c < d; ++c) num[c] += wt * V[(size_t)i * d + c];
+    }
+    return den;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Final attention (comment after Algorithm 2): o = N^ / D^ of the estimator */
+/* above, the shift m taken as the largest logit of a token with nonzero     */
+/* weight (any m gives the same ratio).                                      */
 /* ------------------------------------------------------------------------ */
 void vko_attention_row(int64_t n, int d, const uint8_t* flags, const float* r32, const double* t_exact,
                        const double* V, const double* lambda, const uint8_t* exact_mask, double* out)
@@ -728,17 +753,7 @@ void vko_attention_row(int64_t n, int d, const uint8_t* flags, const float* r32,
         int live = flags[i] == 2 || flags[i] == 1 || (exact_mask && exact_mask[i]);
         if (live && t_exact[i] > m) m = t_exact[i];
     }
-    double den = 0.0;
-    for (int c = 0; c < d; ++c) out[c] = 0.0;
-    for (int64_t i = 0; i < n; ++i) {
-        double om;
-        if (flags[i] == 2 || (exact_mask && exact_mask[i])) om = 1.0;
-        else if (flags[i] == 1) om = lambda[i] / (double)r32[i];
-        else continue;
-        double wt = om * exp(t_exact[i] - m);
-        den += wt;
-        for (int c = 0; c < d; ++c) out[c] += wt * V[(size_t)i * d + c];
-    }
+    double den = vko_estimate_row(n, d, flags, r32, t_exact, V, lambda, exact_mask, m, out);
     for (int c = 0; c < d; ++c) out[c] /= den;
 }
 

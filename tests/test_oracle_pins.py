@@ -546,9 +546,16 @@ def _outcomes(r):
         yield z, float(np.prod(np.where(z == 1, r, 1 - r)))
 
 
+def _outcome_flags(flags, z):
+    """The row's flags with the sample set to the Poisson outcome z over L (1 = sampled)."""
+    f = flags.copy()
+    f[flags != 2] = z.astype(np.uint8)
+    return f
+
+
 def test_lemma1_coverage_exact_enumeration():
-    """Lemma 1: Pr(|D^ - D|/D > eps^(L)) <= delta, computed exactly over all
-    Poisson outcomes (exact sketch: sketch logits = exact logits)."""
+    """Lemma 1: Pr(|D^ - D|/D > eps^(L)) <= delta, computed exactly over all Poisson outcomes (exact
+    sketch: sketch logits = exact logits), with D^ read from the oracle's estimator for every outcome."""
     rng = np.random.default_rng(10)
     for trial in range(40):
         L = int(rng.integers(1, 11))
@@ -557,13 +564,12 @@ def test_lemma1_coverage_exact_enumeration():
         res = oracle.kvfetch_row(flags, r32, t, t, eps=1e9, delta=delta)
         w = np.exp(t - res["m"])
         assert math.isclose(res["D"], w.sum(), rel_tol=1e-12)
+        assert not res["exact_mask"].any()
         Lm = flags != 2
-        r = r32[Lm].astype(np.float64)
-        lam = res["lam"][Lm]
         fail = 0.0
-        for z, p in _outcomes(r):
-            dhat = w[~Lm].sum() + (z * lam * w[Lm] / r).sum()
-            if abs(dhat - w.sum()) / w.sum() > res["eps_hat"]:
+        for z, p in _outcomes(r32[Lm].astype(np.float64)):
+            dhat, _ = oracle.estimate_row(_outcome_flags(flags, z), r32, t, res["lam"], res["exact_mask"], res["m"])
+            if abs(dhat - res["D"]) / res["D"] > res["eps_hat"]:
                 fail += p
         assert fail <= delta + 1e-12
     empty = oracle.kvfetch_row(np.full(5, 2, np.uint8), np.ones(5, np.float32), np.zeros(5), np.zeros(5), 0.1, 0.1)
@@ -606,15 +612,11 @@ def test_theorem2_coverage_and_monotone_residual_certificate():
             e = (a[rest].sum() + bb * ld / 3 + math.sqrt((bb * ld / 3) ** 2 + 2 * v[rest].sum() * ld)) / D
             assert e <= prev * (1 + 1e-12)
             prev = e
-        # exact coverage of the returned estimator
+        # exact coverage of the returned estimator, D^ read from the oracle for every outcome
         E = fast["exact_mask"]
-        idx = np.nonzero(Lm)[0]
         fail = 0.0
         for z, p in _outcomes(r32[Lm].astype(np.float64)):
-            Z = np.zeros(len(flags))
-            Z[idx] = z
-            keep = ~Lm | E
-            dhat = w[keep].sum() + (Z * lam * w / r32)[Lm & ~E].sum()
+            dhat, _ = oracle.estimate_row(_outcome_flags(flags, z), r32, t, lam, E, fast["m"])
             if abs(dhat - D) / D > eps:
                 fail += p
         assert fail <= delta + 1e-12
@@ -690,17 +692,66 @@ def test_appended_tokens_at_eps_zero_equal_dense_attention(sketch):
                 assert not np.allclose(prefix_only, dense, rtol=1e-6, atol=1e-8)
 
 
-def test_no_fetch_estimator_is_horvitz_thompson_when_lambda_is_one():
-    """With lambda = 1 the estimator (5) is unbiased (Horvitz-Thompson): the
-    exact expectation over all outcomes equals D.  The oracle's attention with
-    eps large (no fetch) uses weights lambda/r on the sample; with r close to
-    1 the shrinkage is inactive and the output mean matches."""
-    rng = np.random.default_rng(14)
-    L = 8
-    w = np.exp(rng.standard_normal(L))
-    r = rng.uniform(0.1, 0.9, L)
-    mean = sum(p * (z * w / r).sum() for z, p in _outcomes(r))
-    assert math.isclose(mean, w.sum(), rel_tol=1e-12)
+@pytest.mark.parametrize("sketch_noise", [0.0, 0.4])
+@pytest.mark.parametrize("eps", [1e9, 0.02])
+def test_attention_weights_follow_eq5_by_one_hot_values(sketch_noise, eps):
+    """The oracle's output weights, pinned by enumeration: with one-hot value rows (V_i = e_i, d = n)
+    the attention returns each token's share of the estimator itself, o_i = omega_i w_i / D^.  Eq. (5)
+    after the fetch gives omega_i = 1 on H and on L_g[:k*], lambda_i / r_i on the rest of the sample
+    and 0 on unsampled, unfetched tokens, with the EXACT weight w_i (the keys of S are resident and
+    those of L_g[:k*] fetched), while lambda and the order come from the sketch weights.  Checked for
+    every Poisson outcome of tiny rows, with no fetch (eps huge) and with part of L made exact."""
+    rng = np.random.default_rng(15)
+    checked_exact = 0
+    for trial in range(12):
+        L = int(rng.integers(2, 9))
+        flags, r32, t = _tiny_row(rng, L)
+        ts = t + sketch_noise * rng.standard_normal(len(t))
+        res = oracle.kvfetch_row(flags, r32, t, ts, eps, 0.1)
+        lam, E = res["lam"], res["exact_mask"]
+        checked_exact += int(E.sum())
+        n = len(flags)
+        V = np.eye(n)
+        w = np.exp(t - t.max())
+        for z, _ in _outcomes(r32[flags != 2].astype(np.float64)):
+            f = _outcome_flags(flags, z)
+            out = oracle.attention_row(f, r32, t, V, lam, E)
+            term = np.where((f == 2) | E, w, np.where(f == 1, lam * w / r32.astype(np.float64), 0.0))
+            assert np.allclose(out, term / term.sum(), rtol=1e-12, atol=1e-15), (trial, z)
+            # lambda_i / r_i, not lambda_i: a sampled, unfetched token of L is weighted above its lambda
+            s_only = (f == 1) & ~E
+            if s_only.any():
+                i = int(np.nonzero(s_only)[0][0])
+                assert out[i] / out[f == 2][0] == pytest.approx(lam[i] / r32[i] * w[i] / w[f == 2][0], rel=1e-12)
+    if eps < 1:
+        assert checked_exact > 0, "no row made part of L exact"
+
+
+def test_estimator_moments_match_bias_and_eq6():
+    """Theorem 1's objects, read from two different oracle functions: over all Poisson outcomes the
+    oracle's D^ (no fetch) has mean D - beta(L) (the bias sum_L w_i (1 - lambda_i), i.e. sum_a of the
+    certificate) and mean squared error beta(L)^2 + V(L) (eq. (6) at the returned lambda), both from
+    kvfetch_row.  A weight lambda_i instead of lambda_i / r_i, or a nonzero weight on unsampled tokens,
+    moves both moments."""
+    rng = np.random.default_rng(16)
+    for trial in range(30):
+        L = int(rng.integers(1, 11))
+        flags, r32, t = _tiny_row(rng, L)
+        res = oracle.kvfetch_row(flags, r32, t, t, 1e9, 0.1)
+        D = res["D"]
+        m1 = m2 = 0.0
+        for z, p in _outcomes(r32[flags != 2].astype(np.float64)):
+            dhat, _ = oracle.estimate_row(_outcome_flags(flags, z), r32, t, res["lam"], res["exact_mask"], res["m"])
+            m1 += p * dhat
+            m2 += p * (dhat - D) ** 2
+        assert math.isclose(m1, D - res["sum_a"], rel_tol=1e-12), (m1, D, res["sum_a"])
+        assert math.isclose(m2, res["sum_a"] ** 2 + res["V"], rel_tol=1e-10), (m2, res["sum_a"], res["V"])
+    # lambda forced to one: the Horvitz-Thompson estimator, read from the oracle, is unbiased
+    flags, r32, t = _tiny_row(rng, 8)
+    ones = np.where(flags != 2, 1.0, 0.0)
+    m1 = sum(p * oracle.estimate_row(_outcome_flags(flags, z), r32, t, ones, np.zeros(len(flags), bool), 0.0)[0]
+             for z, p in _outcomes(r32[flags != 2].astype(np.float64)))
+    assert math.isclose(m1, np.exp(t).sum(), rel_tol=1e-12)
 
 
 @pytest.mark.slow
@@ -729,8 +780,7 @@ def test_empirical_coverage_over_philox_seeds_tiny_case():
         lam = res["lam"]
         for seed in range(seeds):
             f = oracle.poisson_sample(r32, seed, 0, 0, 0)
-            Z = f == 1
-            dhat = ww[~Lm | E].sum() + (ww * lam / r32)[Lm & ~E & Z].sum()
+            dhat, _ = oracle.estimate_row(f, r32, tl, lam, E, res["m"])
             fails += abs(dhat - D) / D > w.eps
             total += 1
     assert fails / total <= w.delta
