@@ -83,7 +83,6 @@ typedef struct {
     int32_t n_sink;        /* first tokens always kept (forced into H)                */
     int32_t n_local;       /* last tokens always kept (forced into H)                 */
     int32_t sketch_group;  /* 2-bit sketch: tokens per min/max group (128)            */
-    int32_t topk_width;    /* per query row, gain candidates sorted on chip (4096)    */
     int32_t shrinkage;     /* verkv_shrinkage (0 = clipped, Definition 2)            */
     double eta;            /* kept fraction: expected |H u S| = eta * n (Alg. 1)      */
     uint64_t seed;         /* Philox4x32-10 key of the Poisson sample                 */
@@ -303,22 +302,30 @@ verkv_status verkv_get_kernel_times(verkv_ctx* ctx, const char** names, float* m
                                     verkv_stream stream);
 
 /*
- * Allocation-free certificate for one query row (no counterpart in the paper: it is the decision
- * of verkv_decode for a single row -- the beta fixed point, eq. (7), the gains, the full ranking and
- * k* -- packaged for callers that cannot allocate device memory, e.g. code inside a stream capture
- * whose graph must not own allocations, or under a fixed external memory budget).
- *   w_hat   device [n_l] fp32 sketch weights of the row's L tokens (any common scale),
- *   r       device [n_l] fp32 inclusion probabilities of those tokens (0 < r < 1),
+ * Allocation-free decision for one query row.  This entry point has no counterpart in the paper.  It
+ * runs the same per-row decision as verkv_decode -- the shrinkage fixed point beta, the error
+ * certificate eps_hat, the per-token gains, their full ranking and the number k* of tokens to make
+ * exact -- without a context and without allocating any device memory.  It is for callers that
+ * cannot call cudaMalloc: code whose memory is fixed up front (an engine with its own arena, a
+ * real-time loop that must not allocate), or code running while a CUDA stream is being captured
+ * into a graph, where an allocation would either fail or become part of the graph.
+ *   w_hat   device [n_l] fp32 sketch weights of the row's L tokens (any common scale), >= 0 and finite,
+ *   r       device [n_l] fp32 inclusion probabilities of those tokens, 0 < r < 1,
  *   D       the certificate denominator in the same scale (sum_H w + sum_L w_hat), > 0,
- *   scalars device [4] output: beta, eps_hat, beta(L), V(L),
- *   kstar   device [1] output: k* (0 when eps_hat < eps),
- *   exact   device [n_l] output: the first k* entries are the indices (into w_hat) of L_g[:k*].
- * Creates no context and calls no allocator.  Scratch is a library-wide static device array of
- * VERKV_STATIC_MAX_L 64-bit keys (512 KiB, held by every GPU that loads the library until exit):
- * n_l > VERKV_STATIC_MAX_L returns VERKV_EINVAL.  All calls share that array, so calls whose kernels
- * overlap on a GPU (different streams, or several host threads) race and must be serialised by the
- * caller.  The first call on each device looks up the array's device address (with that device
- * current) and should be made before any stream capture.  Asynchronous on `stream`. */
+ *   scalars device [4] output: beta, eps_hat, sum_L w_hat (1 - lambda), the variance term V,
+ *   kstar   device [1] output: k* (0 when eps_hat < eps or n_l = 0),
+ *   exact   device [n_l] output: the first k* entries are the indices (into w_hat) of the tokens to
+ *           make exact, best gain first; nothing is written when k* = 0 (exact may be NULL when n_l = 0).
+ * An entry of r outside (0, 1), or of w_hat negative or not finite, is reported on the device:
+ * kstar = -1 and NaN scalars (the host cannot see the values without a copy).
+ * Scratch is a library-wide static device array of VERKV_STATIC_MAX_L 64-bit keys (512 KiB, held by
+ * every GPU that loads the library until the process exits): n_l > VERKV_STATIC_MAX_L returns
+ * VERKV_EINVAL.  All calls share that array and it keeps the last call's contents (every call
+ * rewrites the part it reads), so calls whose kernels overlap on a GPU (different streams, or several
+ * host threads) race and must be serialised by the caller.  The first call on each device looks up
+ * the array's device address (with that device current) and keeps it for the life of the process:
+ * make that first call before any stream capture, and do not use this entry point on a device after
+ * cudaDeviceReset (the kept address would be stale).  Asynchronous on `stream`. */
 #define VERKV_STATIC_MAX_L 65536
 verkv_status verkv_certify_row_static(const float* w_hat, const float* r, int32_t n_l, double D, double eps,
                                       double delta, double* scalars, int32_t* kstar, int32_t* exact,

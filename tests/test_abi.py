@@ -90,12 +90,12 @@ def test_ctypes_layouts_match_header():
 
 def test_create_rejects_bad_configs_without_touching_the_gpu(lib):
     # argument checks run before any CUDA call
-    cfg = binding.Config(1, 1, 1, 8, 30, 128, 1024, 4, 64, 128, 4096, 0, 0.125, 0, 1, 0)  # 30 % 8 != 0
+    cfg = binding.Config(1, 1, 1, 8, 30, 128, 1024, 4, 64, 128, 0, 0.125, 0, 1, 0)  # 30 % 8 != 0
     h = ctypes.c_void_p()
     assert lib.verkv_create(ctypes.byref(cfg), ctypes.byref(h)) == 1
-    cfg = binding.Config(1, 1, 1, 8, 32, 64, 1024, 4, 64, 128, 4096, 0, 0.125, 0, 1, 0)   # head_dim 64
+    cfg = binding.Config(1, 1, 1, 8, 32, 64, 1024, 4, 64, 128, 0, 0.125, 0, 1, 0)   # head_dim 64
     assert lib.verkv_create(ctypes.byref(cfg), ctypes.byref(h)) == 5
-    cfg = binding.Config(1, 1, 1, 8, 32, 128, 1024, 4, 64, 128, 4096, 0, 1.5, 0, 1, 0)    # eta > 1
+    cfg = binding.Config(1, 1, 1, 8, 32, 128, 1024, 4, 64, 128, 0, 1.5, 0, 1, 0)    # eta > 1
     assert lib.verkv_create(ctypes.byref(cfg), ctypes.byref(h)) == 1
-    cfg = binding.Config(1, 1, 1, 8, 32, 128, 1024, 4, 64, 128, 4096, 2, 0.125, 0, 1, 0)  # unknown shrinkage
+    cfg = binding.Config(1, 1, 1, 8, 32, 128, 1024, 4, 64, 128, 2, 0.125, 0, 1, 0)  # unknown shrinkage
     assert lib.verkv_create(ctypes.byref(cfg), ctypes.byref(h)) == 1

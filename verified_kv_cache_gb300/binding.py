@@ -31,7 +31,7 @@ class Config(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_seqs", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("max_tokens", ctypes.c_int32), ("n_sink", ctypes.c_int32), ("n_local", ctypes.c_int32),
-                ("sketch_group", ctypes.c_int32), ("topk_width", ctypes.c_int32), ("shrinkage", ctypes.c_int32),
+                ("sketch_group", ctypes.c_int32), ("shrinkage", ctypes.c_int32),
                 ("eta", ctypes.c_double), ("seed", ctypes.c_uint64), ("sketch", ctypes.c_int),
                 ("kv_dtype", ctypes.c_int)]
 
@@ -159,9 +159,9 @@ class VerKV:
 
     def __init__(self, *, n_kv_heads, n_q_heads, max_tokens, head_dim=128, n_layers=1, n_seqs=1, max_batch=1,
                  n_sink=4, n_local=128, eta=1 / 16, seed=0, sketch="int8", kv_dtype="bf16", sketch_group=128,
-                 topk_width=4096, shrinkage="clipped"):
+                 shrinkage="clipped"):
         self.cfg = Config(n_layers, n_seqs, max_batch, n_kv_heads, n_q_heads, head_dim, max_tokens, n_sink, n_local,
-                          sketch_group, topk_width, SHRINKAGE[shrinkage], float(eta), int(seed), SKETCH[sketch],
+                          sketch_group, SHRINKAGE[shrinkage], float(eta), int(seed), SKETCH[sketch],
                           DTYPE[kv_dtype])
         self.sketch = sketch
         self.kv_dtype = kv_dtype

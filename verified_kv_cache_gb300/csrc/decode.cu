@@ -3521,8 +3521,8 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
 }  // namespace verkv
 
 // ================================================================================================
-// Allocation-free variant of the per-row decision (the beta solve, eq. (7), the gains, the full-row
-// ranking and k* of the full-row path above) for callers that cannot allocate device memory: code
+// Allocation-free variant of the per-row decision (the beta solve, the certificate, the gains, the
+// full-row ranking and k* of the full-row path above) for callers that cannot allocate device memory: code
 // running where cudaMalloc is unavailable or forbidden (inside a stream capture whose graph must not
 // own allocations, under an external memory pool or budget, in a real-time loop).  Its only scratch
 // is the file-scope array below, which every GPU that loads the library holds until the process
@@ -3549,6 +3549,27 @@ __global__ void __launch_bounds__(1024) certify_static_kernel(const float* __res
     __shared__ ScanVal shs[32];
     __shared__ ScanVal chunk_total;
     __shared__ int found;
+    // inputs outside the documented domain (r not in (0, 1), w negative or not finite) give k* = -1
+    // and NaN scalars instead of a silent inf / NaN from the divisions below
+    int bad = 0;
+    for (int j = threadIdx.x; j < nl; j += blockDim.x) {
+        const float wj = w[j], rj = rr[j];
+        bad |= !(rj > 0.f && rj < 1.f) || !(wj >= 0.f && wj <= 3.4028234663852886e38f);
+    }
+    if (__syncthreads_or(bad)) {
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < 4; ++i) out_scalars[i] = __longlong_as_double(0x7ff8000000000000ll);
+            *out_kstar = -1;
+        }
+        return;
+    }
+    if (nl == 0) {   // empty L: nothing to estimate, eps_hat = 0, and nothing to fetch whatever eps is
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < 4; ++i) out_scalars[i] = 0.0;
+            *out_kstar = 0;
+        }
+        return;
+    }
     // top of the beta bracket: sum_L w (1 - r)
     ff al = {0.f, 0.f};
     for (int j = threadIdx.x; j < nl; j += blockDim.x) al = ff_add(al, two_prod(w[j], __fsub_rn(1.0f, rr[j])));
@@ -3679,7 +3700,7 @@ __global__ void __launch_bounds__(1024) certify_static_kernel(const float* __res
         carry = scan_combine(carry, chunk_total);
         __syncthreads();
     }
-    if (kstar < 1) kstar = 1;
+    kstar = min(max(kstar, 1), nl);   // eps_hat(L) >= eps here, so k* >= 1; k = |L| is always accepted
     for (int p = threadIdx.x; p < kstar; p += blockDim.x) out_exact[p] = (int32_t)(key[p] & 0xffffffffu);
     if (threadIdx.x == 0) *out_kstar = kstar;
 }
