@@ -228,12 +228,21 @@ verkv_status verkv_get_fetch_stats(verkv_ctx* ctx, int32_t b, int32_t kv_head, i
  * L \ S that a decode reads over the host link is also written to device memory, and later decodes
  * of the same slot read it from there.  The cache belongs to the (layer, sequence) slot and is emptied
  * by verkv_compress and freed by verkv_release; the host cache it mirrors is unchanged while borrowed,
- * so staged rows are exact copies.  rows_per_kv_head: -1 (default) = room for every row of L \ S of a
- * head (512 B per row in bf16), 0 = off (every fetched row crosses the host link at every step),
- * k > 0 = at most k rows per head, first fetched first kept, no eviction.  Takes effect at the next
- * verkv_compress of a slot.  EINVAL: rows_per_kv_head < -1.  No counterpart in the algorithms
- * themselves: results are identical with any setting.
+ * so staged rows are exact copies.  rows_per_kv_head:
+ *   VERKV_STAGE_ETA_N (-2, the default): ceil(eta n) rows per KV head, the size of the resident sample
+ *                    again, so that resident and staged rows together hold at most about 2 eta of the
+ *                    cache (12.5 % at eta = 1/16; 512 B per row in bf16);
+ *   VERKV_STAGE_ALL (-1): room for every row of L \ S of a head (the whole offloaded cache);
+ *   0: off (every fetched row crosses the host link at every step);
+ *   k > 0: at most k rows per head.
+ * A full cache keeps what it holds: rows are staged in the order they are first fetched and never
+ * evicted before the next verkv_compress of the slot (an eviction could overwrite a row that another
+ * block of the same decode is still reading).  Takes effect at the next verkv_compress of a slot.
+ * EINVAL: rows_per_kv_head < -2.  No counterpart in the algorithms themselves: results are identical
+ * with any setting.
  */
+#define VERKV_STAGE_ETA_N (-2)
+#define VERKV_STAGE_ALL (-1)
 verkv_status verkv_set_stage_capacity(verkv_ctx* ctx, int64_t rows_per_kv_head);
 
 /*

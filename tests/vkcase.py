@@ -112,6 +112,8 @@ def oracle_decode(w, b, slot: OracleSlot, q_bh: np.ndarray, eps, delta, mode=1, 
             res["r_l"] = r32[h][Lm].astype(np.float64)
             res["n_shrunk"] = int((res["lam"][Lm] < 1.0).sum())
         res["out"] = oracle.attention_row(flags[h], r32[h], te, w.V[b, h], res["lam"], res["exact_mask"])
+        # what the output check of an exempted row needs: the row's state, logits and values
+        res["_flags"], res["_r32"], res["_te"], res["_ts"], res["_V"] = flags[h], r32[h], te, ts, w.V[b, h]
         rows.append(res)
     unions = []
     for h in range(w.n_kv):
@@ -251,3 +253,31 @@ def check_row(gpu_trace, gpu_set, orow, eps, flags_h):
 
 def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def output_with_device_decision(orow, gpu_set, n_shrunk=None):
+    """The oracle's output for a row whose decision took an exemption: the oracle's coefficients and
+    the DEVICE's exact set (and, for binary shrinkage, the device's shrunk prefix of the oracle's gamma
+    order), so that the attention of every row is checked even where the decision legitimately differs."""
+    flags, r32, te, V = orow["_flags"], orow["_r32"], orow["_te"], orow["_V"]
+    lam = orow["lam"]
+    if n_shrunk is not None and "w_l" in orow and n_shrunk != orow["n_shrunk"]:
+        _, r, _, order = _gamma_order(orow)
+        Lm = flags != 2
+        lam_l = np.ones(int(Lm.sum()))
+        lam_l[order[:n_shrunk]] = r[order[:n_shrunk]]
+        lam = np.zeros(len(flags))
+        lam[Lm] = lam_l
+    mask = np.zeros(len(flags), bool)
+    mask[np.asarray(gpu_set, np.int64)] = True
+    return oracle.attention_row(flags, r32, te, V, lam, mask)
+
+
+def check_row_output(gpu_trace, gpu_set, orow, eps, out_row, ctx_msg=None):
+    """check_row, then the attention output of the row within REL_OUT: against the oracle's own output
+    when the decision matched, else against the oracle's output over the device's decision."""
+    verdict = check_row(gpu_trace, gpu_set, orow, eps, None)
+    ref = orow["out"] if verdict == "ok" else output_with_device_decision(orow, gpu_set, gpu_trace.get("n_shrunk"))
+    err = rel_l2(np.asarray(out_row, np.float64), ref)
+    assert err <= REL_OUT, (ctx_msg, verdict, err)
+    return verdict

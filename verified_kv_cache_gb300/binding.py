@@ -27,6 +27,10 @@ class VerkvError(RuntimeError):
         self.status = status
 
 
+STAGE_ETA_N = -2   # default staging capacity: ceil(eta n) rows per KV head
+STAGE_ALL = -1     # room for every row of L minus S
+
+
 class Config(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_seqs", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
@@ -280,7 +284,8 @@ class VerKV:
         return out[:min(cnt.value, cap)].copy()
 
     def set_stage_capacity(self, rows_per_kv_head: int):
-        """Staging cache rows per KV head and slot: -1 = all of L minus S, 0 = off (next compress on)."""
+        """Staging cache rows per KV head and slot (from the next compress on): STAGE_ETA_N (-2, default) =
+        ceil(eta n), STAGE_ALL (-1) = all of L minus S, 0 = off, k > 0 = k rows."""
         self._check(lib().verkv_set_stage_capacity(self.h, int(rows_per_kv_head)))
 
     def selftest_wait_timeout(self, stream=None) -> int:

@@ -452,7 +452,8 @@ verkv_status verkv_set_stage_capacity(verkv_ctx* h, int64_t rows_per_kv_head)
 {
     if (!h) return VERKV_EINVAL;
     Ctx& ctx = h->c;
-    if (rows_per_kv_head < -1) return fail(ctx, VERKV_EINVAL, "staging capacity must be -1, 0 or positive");
+    if (rows_per_kv_head < VERKV_STAGE_ETA_N)
+        return fail(ctx, VERKV_EINVAL, "staging capacity must be VERKV_STAGE_ETA_N, VERKV_STAGE_ALL, 0 or positive");
     ctx.stage_rows = rows_per_kv_head;
     return VERKV_OK;
 }

@@ -941,11 +941,15 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
         VK_CUDA(cudaMalloc(&s.kvres, s.cap_res * row_bytes));
     }
     VK_CUDA(cudaMemcpyAsync(s.res_off, s.res_off_host.data(), sizeof(int64_t) * (Hkv + 1), cudaMemcpyHostToDevice, st));
-    // the staging cache starts empty: room for every row of L \ S of a head (or the set capacity)
+    // the staging cache starts empty: room for ceil(eta n) rows of L \ S per head by default (the size of
+    // the resident sample again), every row of L \ S, or the set capacity
     s.stage_off_host.assign((size_t)Hkv + 1, 0);
+    const int64_t eta_n = (int64_t)std::ceil(cfg.eta * (double)n);
     for (int h = 0; h < Hkv; ++h) {
         const int64_t fetchable = s.stats[h].n_l - s.stats[h].n_s;
-        const int64_t cap = ctx.stage_rows < 0 ? fetchable : std::min<int64_t>(ctx.stage_rows, fetchable);
+        const int64_t want = ctx.stage_rows == VERKV_STAGE_ALL ? fetchable
+                             : ctx.stage_rows == VERKV_STAGE_ETA_N ? eta_n : ctx.stage_rows;
+        const int64_t cap = std::min<int64_t>(want, fetchable);
         s.stage_off_host[h + 1] = s.stage_off_host[h] + cap;
     }
     const size_t need_stage = (size_t)s.stage_off_host[Hkv];

@@ -135,7 +135,7 @@ struct Ctx {
     int32_t* scount = nullptr;      // [max_batch][Hkv] its size
     uint32_t* shist = nullptr;      // [max_batch][Hkv][kShortlistBins + 1] shortlist first-level histogram + count
                                     // (zero between calls)
-    int64_t stage_rows = -1;        // staging capacity per KV head and slot: -1 = all of L \ S, 0 = off
+    int64_t stage_rows = VERKV_STAGE_ETA_N;   // staging capacity per KV head and slot (verkv_set_stage_capacity)
     int append_rows = 0;            // room reserved per KV head and slot for decode-time appended tokens
     int* h_err = nullptr;           // mapped pinned host word: a device-side bounded wait gave up
     int* d_err = nullptr;           // its device address
