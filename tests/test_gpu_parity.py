@@ -246,20 +246,68 @@ def test_large_kstar_on_the_cluster_path():
 
 
 def test_full_row_path_for_long_rows():
-    """|L| above the on-chip capacity of the cluster kernel (131072 per row with 16-CTA clusters) uses
-    the multi-kernel path: on-chip ranking of 4096 candidates and, when k* lies beyond them, the
-    full-row sort."""
-    w = small_case("int8", n=150000, steps=1, query_mode="random", eta=1 / 16, n_kv=2, n_q=4)
+    """|L| above the fused decision's limit (262144 entries per row) uses the multi-kernel path: on-chip
+    ranking of 4096 candidates and, when k* lies beyond them, the full-row sort."""
+    w = small_case("int8", n=280000, steps=1, query_mode="random", eta=1 / 16, n_kv=2, n_q=4)
     w.queries *= 0.3
     ctx = make_lib_ctx(w)
     gc = GpuCase(w, ctx)
     tau, stats, osl = _compress_both(w, gc, tau=workloads.synthetic_scores(w.n_kv, w.n, seed=9))
-    assert max(s["n_l"] for s in stats) > 131072
+    assert max(s["n_l"] for s in stats) > 262144
     eps = 0.005
     gc.decode(w.queries[0], eps, 0.05)
     trace = ctx.decode_trace(w.n_q)
     assert any(t["fallback"] for t in trace), [t["kstar"] for t in trace]
     _decode_parity(w, gc, osl, eps, 0.05, steps=[0])
+    ctx.close()
+
+
+@pytest.mark.parametrize("shrinkage", ["clipped", "binary"])
+def test_streaming_decision_on_rows_beyond_shared_memory(shrinkage):
+    """Rows longer than the on-chip decision holds (16 x 8192 entries): the streaming variant of the
+    fused decision (entries re-read from L2 in every pass), with both coefficient rules.  n = 250000
+    gives |L| of about 234000 per row; binary shrinkage runs there too."""
+    w = small_case("int8", n=250000, steps=2, query_mode="needle_half", eta=1 / 16, n_kv=2, n_q=4)
+    ctx = make_lib_ctx(w, shrinkage=shrinkage)
+    gc = GpuCase(w, ctx)
+    tau, stats, osl = _compress_both(w, gc, tau=workloads.synthetic_scores(w.n_kv, w.n, seed=19))
+    assert max(s["n_l"] for s in stats) > 131072
+    for eps in (0.05, 0.01):
+        counts = _decode_parity(w, gc, osl, eps, 0.05, shrinkage=1 if shrinkage == "binary" else 0)
+        trace = ctx.decode_trace(w.n_q)
+        assert not any(t["fallback"] for t in trace)
+        print(shrinkage, eps, counts)
+    ctx.close()
+
+
+def test_streaming_and_on_chip_decisions_agree():
+    """The same sequence decoded alone (one wave: the on-chip decision) and as eight copies in one call
+    (256 query rows: the streaming decision).  Both must meet the oracle's bars on every row; k* and
+    the sets agree except at near-ties, which the oracle comparison exempts row by row."""
+    base = small_case("int8", n=6000, steps=2, query_mode="needle_half", n_kv=8, n_q=32)
+    w8 = dataclasses.replace(base, batch=8, K=np.repeat(base.K, 8, axis=0), V=np.repeat(base.V, 8, axis=0),
+                             obs_q=np.repeat(base.obs_q, 8, axis=0), queries=np.repeat(base.queries, 8, axis=1))
+    ctx = make_lib_ctx(w8)
+    gc = GpuCase(w8, ctx)
+    tau = oracle_tau(base, 0)
+    slots = []
+    for b in range(8):
+        gc.compress(b, seq=b, tau=tau)
+        slots.append(oracle_compress(w8, b, tau, layer=0, seq=b))
+    for s in range(2):
+        single = gc.decode(w8.queries[s, :1], w8.eps, w8.delta, seq_ids=[0])     # on-chip
+        tr1 = ctx.decode_trace(w8.n_q)
+        sets1 = [ctx.exact_set(0, hq, w8.n) for hq in range(w8.n_q)]
+        full = gc.decode(w8.queries[s], w8.eps, w8.delta)                         # streaming
+        tr8 = ctx.decode_trace(8 * w8.n_q)
+        for b in range(8):
+            rows, _ = oracle_decode(w8, b, slots[b], w8.queries[s, b], w8.eps, w8.delta)
+            for hq in range(w8.n_q):
+                check_row_output(tr8[b * w8.n_q + hq], ctx.exact_set(b, hq, w8.n), rows[hq], w8.eps, full[b, hq],
+                                 (s, b, hq))
+        rows0, _ = oracle_decode(w8, 0, slots[0], w8.queries[s, 0], w8.eps, w8.delta)
+        for hq in range(w8.n_q):
+            check_row_output(tr1[hq], sets1[hq], rows0[hq], w8.eps, single[0, hq], (s, "single", hq))
     ctx.close()
 
 

@@ -1501,17 +1501,21 @@ __global__ void __launch_bounds__(1024) fallback_kernel(Views views, DecodeArgs 
 //   phase 4: E = L_g[:k*] = the keys up to the k*-th, written as marks and a token list.
 // --------------------------------------------------------------------------------------------
 constexpr int kDecideThreads = 1024;
+constexpr int kDecideStreamThreads = 512;   // streaming variant: two CTAs per multiprocessor
 constexpr int kDecideCap = 8192;   // L entries per CTA
 constexpr int kDecideMaxCluster = 16;  // 16 is a non-portable cluster size: used when the GPU can run it
-// k* search: keys of 31 gain bits and 17 index bits; each level splits the remaining key range into
+constexpr int kDecideStreamMaxCluster = 8;
+// k* search: keys of 31 gain bits and 18 index bits; each level splits the remaining key range into
 // 2^11 bins
-constexpr int kKeyBits = 48;
+constexpr int kKeyBits = 49;
+constexpr int kDecideMaxL = 1 << (kKeyBits - 31);   // the longest L a row may have on the fused decision
 constexpr int kSearchBits = 11;
 constexpr int kSearchLevels = 5;
 constexpr int kSearchBins = 1 << kSearchBits;
 // histogram fields per bin: count, max b, three 14-bit pieces of sum a, three of sum v
 constexpr int kSearchFields = 8;
-constexpr size_t kDecideSmem = (size_t)kDecideCap * 16 + (size_t)kSearchFields * kSearchBins * 4;
+constexpr size_t kDecideHistSmem = (size_t)kSearchFields * kSearchBins * 4;
+constexpr size_t kDecideSmem = (size_t)kDecideCap * 16 + kDecideHistSmem;
 static_assert(kDecideCap * kDecideMaxCluster <= (1 << (kKeyBits - 31)), "L index must fit the key's low bits");
 
 struct DecideSlot {
@@ -1914,14 +1918,16 @@ __device__ __forceinline__ void finish_binary(cg::cluster_group& cl, const Small
     }
 }
 
-template <bool BINARY>
-__global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, DecodeArgs a,
+template <bool BINARY, bool STREAM>
+__global__ void __launch_bounds__(STREAM ? kDecideStreamThreads : kDecideThreads, STREAM ? 2 : 1)
+decide_kernel(Views views, DecodeArgs a,
                                                                    RowState* __restrict__ rows,
                                                                    const float2* __restrict__ tl,
                                                                    const float2* __restrict__ th,
                                                                    float* __restrict__ wl,
                                                                    int32_t* __restrict__ mark,
-                                                                   int32_t* __restrict__ elist)
+                                                                   int32_t* __restrict__ elist,
+                                                                   unsigned long long* scratch)
 {
     pdl_trigger();   // the attention kernel may start its independent prologue
     pdl_wait();      // the scoring kernel has completed (its logits, maxima and weight factors are visible)
@@ -1940,7 +1946,8 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     float* sb = sw;
     float* sa_ = sg;
     float* sv_ = sp;
-    unsigned* hist = reinterpret_cast<unsigned*>(sp + kDecideCap);  // [kSearchFields][kSearchBins]
+    // [kSearchFields][kSearchBins]; the streaming variant keeps no entries in shared memory
+    unsigned* hist = STREAM ? reinterpret_cast<unsigned*>(dsm) : reinterpret_cast<unsigned*>(sp + kDecideCap);
     __shared__ DecideSlot slot[2];
     __shared__ ff bc[8];
     __shared__ ff redff[32 * 4];
@@ -1956,7 +1963,8 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     __shared__ SearchAcc sacc[64];
     __shared__ SearchAcc ssum;   // this CTA's slice total at the current search level
     __shared__ SearchProp sprop;
-    const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = T >> 5;
+    constexpr int BPT = STREAM ? 4 : 2;   // histogram bins per thread when a CTA reads its slice of bins
     const int b = row / a.Hq, kv = (row % a.Hq) / a.G;
     const SlotView& V = views.v[b];
     RowState& R = rows[row];
@@ -1964,6 +1972,48 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const int S = (nl + C - 1) / C;
     const int j0 = min(nl, rank * S), j1 = min(nl, j0 + S), ns = j1 - j0;
     const float* rl = V.rl + (int64_t)kv * V.n;
+    // The streaming variant keeps an entry's state in global memory (L2) instead of shared memory and
+    // reads it back in every pass, four entries per thread in flight.  Up to phase 2 that state is w^
+    // (the row of wl) and the KV head's r and ratios ((1 - r) / r, r / (1 - r)), shared by the query
+    // rows of the head, from which alpha = w (1 - r), gamma = w (1 - r) / r and rho = r / (1 - r) are
+    // formed with the operations phase 0 of the on-chip variant uses.  From phase 2 on it is held in
+    // two scratch rows -- the row's logits in tl (dead once phase 0 has read them; float2 per entry) and
+    // the row of the full-row key buffer (idle on this path; two float planes of ws_npow2 entries):
+    //   phase 2:  tl = (a_i, v_i), plane B = b_i
+    //   phase 3:  tl = the fixed-point-scaled (a_i, v_i), plane A = gain key, plane B = bits of b_i
+    // An entry is written and read back only by the thread that owns it (entry i on thread i mod T,
+    // in every pass), so program order makes the values visible.
+    float* const wl_row = wl + (int64_t)row * a.ws_n + j0;
+    const float* const rl_row = rl + j0;
+    const float2* const lq_row = V.lq + (int64_t)kv * V.n + j0;
+    float2* const st_row = const_cast<float2*>(tl) + (int64_t)row * a.ws_n + j0;
+    float* const pa_row = reinterpret_cast<float*>(scratch + (int64_t)row * a.ws_npow2) + j0;
+    float* const pb_row = reinterpret_cast<float*>(scratch + (int64_t)row * a.ws_npow2) + a.ws_npow2 + j0;
+    constexpr int U = 4;
+    // body(i, w^, alpha, gamma, rho) for every entry of the slice (rho only where NEED_RHO)
+    auto pass = [&](auto&& body) {
+        if (STREAM) {
+            for (int g0 = 0; g0 < ns; g0 += U * T) {
+                float wv[U], rv[U];
+                float2 qv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    wv[u] = i < ns ? wl_row[i] : 0.f;
+                    rv[u] = i < ns ? __ldg(rl_row + i) : 0.5f;
+                    qv[u] = i < ns ? __ldg(lq_row + i) : make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    if (i < ns)
+                        body(i, wv[u], __fmul_rn(wv[u], __fsub_rn(1.0f, rv[u])), __fmul_rn(wv[u], qv[u].x), qv[u].y);
+                }
+            }
+        } else {
+            for (int i = tid; i < ns; i += T) body(i, sw[i], sr[i], sg[i], sp[i]);
+        }
+    };
     int parity = 0;
     const bool timer = rank == 0 && tid == 0;
     unsigned long long t_prev = timer ? global_ns() : 0ull;
@@ -1976,6 +2026,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     };
 
     float m;   // the row maximum of the logits
+    float acc_lo[4] = {0.f, 0.f, 0.f, 0.f};   // streaming variant: low parts of the phase-0 partials
     // ---- phase 0: weights and the row totals; this row's exact-set bitmap (left by the previous
     // call for its attention) is cleared for phase 4
     {
@@ -1985,13 +2036,47 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             const int per = (int)((stride + C - 1) / C);
             for (int wi = rank * per + tid; wi < min((int)stride, (rank + 1) * per); wi += T) eb[wi] = 0u;
         }
-        // per-thread partial sums in fp32 (at most eight terms), combined across the block and the
-        // cluster in float-float: sum_L w^, sum_H w, sum alpha, sum rho
+        // per-thread partial sums in fp32, combined across the block and the cluster in float-float:
+        // sum_L w^, sum_H w, sum alpha, sum rho
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         const float2* tlr = tl + (int64_t)row * a.ws_n + j0;
         const float* rlr = rl + j0;
         const float2* lqr = V.lq + (int64_t)kv * V.n + j0;
         float* wlr = wl + (int64_t)row * a.ws_n + j0;
+        if (STREAM) {
+            // any number of entries per thread: float-float partials (a thread may hold hundreds)
+            m = untag_max(R.m_tag, (unsigned)a.gen);
+            ff pw = {0.f, 0.f}, pa = {0.f, 0.f}, pr = {0.f, 0.f};
+            for (int g0 = 0; g0 < ns; g0 += U * T) {
+                float2 tv[U], qv[U];
+                float rv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    tv[u] = i < ns ? __ldcg(tlr + i) : make_float2(0.f, 0.f);
+                    rv[u] = i < ns ? __ldg(rlr + i) : 0.5f;
+                    qv[u] = i < ns ? __ldg(lqr + i) : make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    if (i >= ns) break;
+                    const float w = weight_of(tv[u], m);
+                    const float al = __fmul_rn(w, __fsub_rn(1.0f, rv[u]));   // alpha = w (1 - r)
+                    wlr[i] = w;
+                    pw = ff_add_f(pw, w);
+                    pa = ff_add_f(pa, al);
+                    pr = ff_add_f(pr, qv[u].y);
+                }
+            }
+            acc[0] = pw.hi;
+            acc[2] = pa.hi;
+            acc[3] = pr.hi;
+            // the low parts join the compensated block sum as a second set of terms below
+            acc_lo[0] = pw.lo;
+            acc_lo[2] = pa.lo;
+            acc_lo[3] = pr.lo;
+        } else {
         // all loads of a thread issued before any is used
         float2 tv[8], qv[8];
         float rv[8];
@@ -2020,6 +2105,7 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             acc[2] = __fadd_rn(acc[2], al);
             acc[3] = __fadd_rn(acc[3], qv[k].y);
         }
+        }
         if (rank == 0) {
             const float2* thr = th + (int64_t)row * a.ws_n;
             for (int k0 = tid; k0 < nh; k0 += 4 * T) {
@@ -2033,6 +2119,13 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         }
         ff tot[4];
         block_sum_f_w0<4>(acc, tot, redff);
+        if (STREAM) {
+            ff tlo[4];
+            block_sum_f_w0<4>(acc_lo, tlo, redff);
+            if (warp == 0)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tot[k] = ff_add(tot[k], tlo[k]);
+        }
         if (tid == 0) {
             for (int k = 0; k < 4; ++k) slot[parity].v[k] = tot[k];
             if (rank == 0) { wcnt[0] = 0; wcnt[1] = 0; }   // exact-list position and fetch count (phase 4)
@@ -2071,13 +2164,12 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         // the bin; the last bin whose first entry passes holds the end (entries of gamma 0 never pass
         // and stay out).
         unsigned kmin = 0xffffffffu, kmax = 0u;
-        for (int i = tid; i < ns; i += T) {
-            const float ga = sg[i];
-            if (!(ga > 0.f)) continue;
+        pass([&](int i, float, float, float ga, float) {
+            if (!(ga > 0.f)) return;
             const unsigned k32 = gamma_key32(ga);
             kmin = min(kmin, k32);
             kmax = max(kmax, k32);
-        }
+        });
         kmin = __reduce_min_sync(0xffffffffu, kmin);
         kmax = __reduce_max_sync(0xffffffffu, kmax);
         if (lane == 0) {
@@ -2088,8 +2180,8 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         for (int k = tid; k < kSearchFields * kSearchBins / 4; k += T) hist4[k] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
         if (warp == 0) {
-            kmin = __reduce_min_sync(0xffffffffu, sext[lane][0]);
-            kmax = __reduce_max_sync(0xffffffffu, sext[lane][1]);
+            kmin = __reduce_min_sync(0xffffffffu, lane < nw ? sext[lane][0] : 0xffffffffu);
+            kmax = __reduce_max_sync(0xffffffffu, lane < nw ? sext[lane][1] : 0u);
             if (lane == 0) {
                 slot[parity].i[0] = (int)kmin;
                 slot[parity].i[1] = (int)kmax;
@@ -2133,19 +2225,18 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             const int sl = nb / C;
             const unsigned long long klo = sc.klo, span = sc.khi - sc.klo;
             const int bs = max(0, (64 - __clzll((long long)(span - 1ull))) - kSearchBits);
-            for (int i = tid; i < ns; i += T) {
-                const float ga = sg[i];
-                if (!(ga > 0.f)) continue;
+            pass([&](int i, float, float al, float ga, float) {
+                if (!(ga > 0.f)) return;
                 const unsigned long long K = search_key(gamma_key32(ga), j0 + i);
-                if (K < klo || K - klo >= span) continue;
+                if (K < klo || K - klo >= span) return;
                 const unsigned d = (unsigned)((K - klo) >> bs);
                 unsigned pa[3];
-                fixed_pieces(__fmul_rn(__fmul_rn(sr[i], fs1), fs2), pa);
+                fixed_pieces(__fmul_rn(__fmul_rn(al, fs1), fs2), pa);
                 atomicAdd(&hist[d], 1u);
                 atomicMax(&hist[kSearchBins + d], __float_as_uint(ga));
 #pragma unroll
                 for (int q = 0; q < 3; ++q) atomicAdd(&hist[(2 + q) * kSearchBins + d], pa[q]);
-            }
+            });
             __syncthreads();
             if (C > 1) {
                 for (int d = tid; d < nb; d += T) {
@@ -2160,24 +2251,28 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                 }
                 cl.sync();
             }
-            // the cluster totals of this CTA's slice, two bins per thread in reverse order (thread t
-            // holds bins dA = rank sl + sl - 2 - 2t and dA + 1), so the threads above t hold the bins
-            // before dA and the block's exclusive suffix is the prefix over bins
-            const int dA = rank * sl + sl - 2 - 2 * tid;
-            const bool own = 2 * tid + 2 <= sl;
-            unsigned c2[2] = {0u, 0u}, g2[2] = {0u, 0u};
-            unsigned long long a2[2] = {0ull, 0ull};
-            if (own) {
+            // the cluster totals of this CTA's slice, BPT bins per thread in reverse order (thread t
+            // holds bins dA = rank sl + sl - BPT (t + 1) .. dA + BPT - 1), so the threads above t hold
+            // the bins before dA and the block's exclusive suffix is the prefix over bins
+            const int dA = rank * sl + sl - BPT * (tid + 1);
+            const bool own = BPT * (tid + 1) <= sl;
+            unsigned c2[BPT], g2[BPT];
+            unsigned long long a2[BPT];
+            SearchAcc mine = zero;
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < BPT; ++k) {
+                c2[k] = g2[k] = 0u;
+                a2[k] = 0ull;
+                if (own) {
                     const int d = dA + k;
                     c2[k] = hist[d];
                     g2[k] = hist[kSearchBins + d];
 #pragma unroll
                     for (int q = 0; q < 3; ++q) a2[k] += (unsigned long long)hist[(2 + q) * kSearchBins + d] << (14 * q);
                 }
+                mine.a += a2[k];
+                mine.c += c2[k];
             }
-            const SearchAcc mine = {a2[0] + a2[1], 0ull, 0u, c2[0] + c2[1]};
             SearchAcc before = block_suffix_search(mine, sacc);
             if (tid == 0) ssum = search_add(before, mine);
             for (int k = tid; k < kSearchFields * kSearchBins / 4; k += T) hist4[k] = make_uint4(0u, 0u, 0u, 0u);
@@ -2194,21 +2289,31 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             }
             __syncthreads();
             before = search_add(before, sacc[0]);
-            // bias and count before the first entry of bin dA, and of bin dA + 1
-            const unsigned long long S0 = sc.rest_a + before.a, S1 = S0 + a2[0];
-            const unsigned n0 = (unsigned)sc.rem_cnt + before.c, n1 = n0 + c2[0];
-            const bool p0 = c2[0] > 0u && __fmul_rn(__fmul_rn(__uint_as_float(g2[0]), fs1), fs2) > 2.0f * (float)S0;
-            const bool p1 = c2[1] > 0u && __fmul_rn(__fmul_rn(__uint_as_float(g2[1]), fs1), fs2) > 2.0f * (float)S1;
-            int cand = own ? (p1 ? dA + 1 : (p0 ? dA : -1)) : -1;
-            cand = __reduce_max_sync(0xffffffffu, cand);
+            // bias and count before the first entry of each of the thread's bins; the last bin whose
+            // first entry passes
+            unsigned long long Sk[BPT];
+            unsigned nk[BPT];
+            int mycand = -1;
+#pragma unroll
+            for (int k = 0; k < BPT; ++k) {
+                Sk[k] = k == 0 ? sc.rest_a + before.a : Sk[k - 1] + a2[k - 1];
+                nk[k] = k == 0 ? (unsigned)sc.rem_cnt + before.c : nk[k - 1] + c2[k - 1];
+                const bool pk = c2[k] > 0u &&
+                                __fmul_rn(__fmul_rn(__uint_as_float(g2[k]), fs1), fs2) > 2.0f * (float)Sk[k];
+                if (own && pk) mycand = dA + k;
+            }
+            int cand = __reduce_max_sync(0xffffffffu, mycand);
             if (lane == 0) redi[warp] = cand;
             __syncthreads();
-            cand = __reduce_max_sync(0xffffffffu, redi[lane]);
-            if (own && cand >= 0 && (cand == dA || cand == dA + 1)) {
-                const bool first = cand == dA;
-                sprop.a = first ? S0 : S1;
-                sprop.c = first ? n0 : n1;
-                sprop.in_bin = first ? c2[0] : c2[1];
+            cand = __reduce_max_sync(0xffffffffu, lane < nw ? redi[lane] : -1);
+            if (own && cand >= dA && cand < dA + BPT) {
+#pragma unroll
+                for (int k = 0; k < BPT; ++k)
+                    if (cand == dA + k) {
+                        sprop.a = Sk[k];
+                        sprop.c = nk[k];
+                        sprop.in_bin = c2[k];
+                    }
             }
             if (tid == 0) sprop.cand = cand;
             cl.sync();
@@ -2243,20 +2348,19 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             if (sc.in_bin <= kSmallBin) {
                 if (tid == 0) ncand = 0;
                 __syncthreads();
-                for (int i = tid; i < ns; i += T) {
-                    const float ga = sg[i];
-                    if (!(ga > 0.f)) continue;
+                pass([&](int i, float, float al, float ga, float) {
+                    if (!(ga > 0.f)) return;
                     const unsigned long long K = search_key(gamma_key32(ga), j0 + i);
-                    if (K < sc.klo || K >= sc.khi) continue;
+                    if (K < sc.klo || K >= sc.khi) return;
                     const int at = atomicAdd(&ncand, 1);
                     unsigned pa[3];
-                    fixed_pieces(__fmul_rn(__fmul_rn(sr[i], fs1), fs2), pa);
+                    fixed_pieces(__fmul_rn(__fmul_rn(al, fs1), fs2), pa);
                     bcand[at].key = K;
                     bcand[at].a = (unsigned long long)pa[0] + ((unsigned long long)pa[1] << 14) +
                                   ((unsigned long long)pa[2] << 28);
                     bcand[at].v = 0ull;
                     bcand[at].b = __float_as_uint(ga);
-                }
+                });
                 cl.sync();
                 if (warp == 0) finish_binary(cl, bcand, &ncand, bloc, sc, C, fs1, fs2);
                 __syncthreads();
@@ -2273,25 +2377,28 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         // the breakpoints nearest theta: min alpha of the lambda = r class, min gamma of the interior,
         // max alpha outside the lambda = r class, max gamma of the lambda = 1 class
         float uA = INFINITY, uG = INFINITY, lA = 0.f, lG = 0.f;
-        for (int i = tid; i < ns; i += T) {
-            const float wj = sw[i];
-            if (!(wj > 0.f)) continue;
-            const float al = sr[i];
+        ff accs[3] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};   // streaming variant: float-float partials
+        pass([&](int i, float wj, float al, float ga, float rho) {
+            if (!(wj > 0.f)) return;
             if (al >= tu) {                                   // theta <= alpha: lambda = r
-                acc[0] = __fadd_rn(acc[0], al);
+                if (STREAM) accs[0] = ff_add_f(accs[0], al); else acc[0] = __fadd_rn(acc[0], al);
                 uA = fminf(uA, al);
             } else {
                 lA = fmaxf(lA, al);
-                const float ga = sg[i];
                 if (ga > td) {                                // theta < gamma: interior
-                    acc[1] = __fadd_rn(acc[1], wj);
-                    acc[2] = __fadd_rn(acc[2], sp[i]);
+                    if (STREAM) {
+                        accs[1] = ff_add_f(accs[1], wj);
+                        accs[2] = ff_add_f(accs[2], rho);
+                    } else {
+                        acc[1] = __fadd_rn(acc[1], wj);
+                        acc[2] = __fadd_rn(acc[2], rho);
+                    }
                     uG = fminf(uG, ga);
                 } else {
                     lG = fmaxf(lG, ga);
                 }
             }
-        }
+        });
         {
             const unsigned e0 = __reduce_min_sync(0xffffffffu, __float_as_uint(uA));
             const unsigned e1 = __reduce_min_sync(0xffffffffu, __float_as_uint(uG));
@@ -2305,12 +2412,22 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             }
         }
         ff tot[3];
-        block_sum_f_w0<3>(acc, tot, redff);   // its barriers also publish sext
+        if (STREAM) {
+            float hi3[3] = {accs[0].hi, accs[1].hi, accs[2].hi}, lo3[3] = {accs[0].lo, accs[1].lo, accs[2].lo};
+            ff tlo[3];
+            block_sum_f_w0<3>(hi3, tot, redff);   // its barriers also publish sext
+            block_sum_f_w0<3>(lo3, tlo, redff);
+            if (warp == 0)
+#pragma unroll
+                for (int k = 0; k < 3; ++k) tot[k] = ff_add(tot[k], tlo[k]);
+        } else {
+            block_sum_f_w0<3>(acc, tot, redff);   // its barriers also publish sext
+        }
         if (warp == 0) {
-            const unsigned e0 = __reduce_min_sync(0xffffffffu, sext[lane][0]);
-            const unsigned e1 = __reduce_min_sync(0xffffffffu, sext[lane][1]);
-            const unsigned e2 = __reduce_max_sync(0xffffffffu, sext[lane][2]);
-            const unsigned e3 = __reduce_max_sync(0xffffffffu, sext[lane][3]);
+            const unsigned e0 = __reduce_min_sync(0xffffffffu, lane < nw ? sext[lane][0] : 0x7f800000u);
+            const unsigned e1 = __reduce_min_sync(0xffffffffu, lane < nw ? sext[lane][1] : 0x7f800000u);
+            const unsigned e2 = __reduce_max_sync(0xffffffffu, lane < nw ? sext[lane][2] : 0u);
+            const unsigned e3 = __reduce_max_sync(0xffffffffu, lane < nw ? sext[lane][3] : 0u);
             if (tid == 0) {
                 for (int k = 0; k < 3; ++k) slot[parity].v[k] = tot[k];
                 slot[parity].f[0] = __uint_as_float(e0);
@@ -2354,64 +2471,114 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     const float bf = sc.bf;
     const unsigned long long bkb = BINARY ? sc.bin_kb : 0ull;
     stamp(1);
+    // lambda, a_i, v_i, b_i of entry i and, for a sampled entry, its weight factor.  With alpha =
+    // w (1 - r), gamma = alpha / r, rho = r / (1 - r):
+    //   beta <= alpha: lambda = r, a = alpha, lambda w = w - alpha, v = lambda w alpha,
+    //                  b = max(lambda w, alpha), weight factor 1;
+    //   otherwise:     lambda = min(beta / gamma, 1), a = w - lambda w, v = lambda (lambda w) gamma,
+    //                  b = max(lambda w, lambda gamma), weight factor lambda (1 + rho) / rho
+    // (binary shrinkage: lambda = r on the passing prefix of the gamma order, 1 elsewhere)
+    auto coef_entry = [&](int i, float w, float al, float gam, float rho, bool sampled, float& om_i) -> Coef {
+        Coef c = {0.f, 0.f, 0.f};
+        om_i = 1.0f;
+        const bool at_r = BINARY ? (gam > 0.f && search_key(gamma_key32(gam), j0 + i) < bkb) : (bf <= al);
+        if (!(w > 0.f)) {
+            if (sampled) om_i = __fdiv_rn(__fadd_rn(1.0f, rho), rho);   // lambda = 1: 1 / r
+        } else if (at_r) {
+            const float lw = __fsub_rn(w, al);
+            c.a = al;
+            c.v = __fmul_rn(lw, al);
+            c.b = fmaxf(lw, al);
+        } else {
+            const float lam = BINARY ? 1.0f : fminf(__fdiv_rn(bf, gam), 1.0f);
+            const float lw = __fmul_rn(lam, w);
+            c.a = __fsub_rn(w, lw);
+            c.v = __fmul_rn(__fmul_rn(lam, lw), gam);
+            c.b = fmaxf(lw, __fmul_rn(lam, gam));
+            if (sampled) om_i = __fdiv_rn(__fmul_rn(lam, __fadd_rn(1.0f, rho)), rho);
+        }
+        return c;
+    };
 
     // ---- phase 2: lambda, a_i, v_i, b_i and eq. (7); the weight factor lambda_i / r_i of the
     // sampled entries.  a, v, b replace gamma, rho, w^ in shared memory.
     {
         float acc[2] = {0.f, 0.f};
         Top2 t2 = {0.f, 0.f, 0x7fffffff};
+        float* omr = a.om + (int64_t)row * a.ws_n;
+        auto top2_add = [&](float bv, int j) {
+            if (bv > t2.b1 || (bv == t2.b1 && j < t2.arg)) { t2.b2 = t2.b1; t2.b1 = bv; t2.arg = j; }
+            else if (bv > t2.b2) t2.b2 = bv;
+        };
+        ff acc2[2] = {{0.f, 0.f}, {0.f, 0.f}};
+        if (STREAM) {
+            const int32_t* ls_row = V.lslot + (int64_t)kv * V.n + j0;
+            for (int g0 = 0; g0 < ns; g0 += U * T) {
+                float wv[U], rv[U];
+                float2 qv[U];
+                int sv_[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    wv[u] = i < ns ? wl_row[i] : 0.f;
+                    rv[u] = i < ns ? __ldg(rl_row + i) : 0.5f;
+                    qv[u] = i < ns ? __ldg(lq_row + i) : make_float2(0.f, 0.f);
+                    sv_[u] = i < ns ? __ldg(ls_row + i) : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    if (i >= ns) break;
+                    float om_i;
+                    const Coef c = coef_entry(i, wv[u], __fmul_rn(wv[u], __fsub_rn(1.0f, rv[u])),
+                                              __fmul_rn(wv[u], qv[u].x), qv[u].y, sv_[u] >= 0, om_i);
+                    if (sv_[u] >= 0) omr[sv_[u]] = om_i;
+                    st_row[i] = make_float2(c.a, c.v);
+                    pb_row[i] = c.b;
+                    acc2[0] = ff_add_f(acc2[0], c.a);
+                    acc2[1] = ff_add_f(acc2[1], c.v);
+                    top2_add(c.b, j0 + i);
+                }
+            }
+            acc[0] = acc2[0].hi;
+            acc[1] = acc2[1].hi;
+        } else {
         int slv[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + k * T;
             slv[k] = i < ns ? V.lslot[(int64_t)kv * V.n + j0 + i] : -1;
         }
-        float* omr = a.om + (int64_t)row * a.ws_n;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int i = tid + k * T;
             if (i >= ns) break;
-            // with alpha = w (1 - r), gamma = alpha / r, rho = r / (1 - r):
-            //   beta <= alpha: lambda = r, a = alpha, lambda w = w - alpha, v = lambda w alpha,
-            //                  b = max(lambda w, alpha), weight factor 1;
-            //   otherwise:     lambda = min(beta / gamma, 1), a = w - lambda w, v = lambda (lambda w) gamma,
-            //                  b = max(lambda w, lambda gamma), weight factor lambda (1 + rho) / rho
-            const float w = sw[i], al = sr[i], gam = sg[i], rho = sp[i];
-            Coef c = {0.f, 0.f, 0.f};
-            float om_i = 1.0f;
-            // binary shrinkage: lambda = r on the passing prefix of the gamma order, 1 elsewhere
-            const bool at_r = BINARY ? (gam > 0.f && search_key(gamma_key32(gam), j0 + i) < bkb) : (bf <= al);
-            if (!(w > 0.f)) {
-                om_i = __fdiv_rn(__fadd_rn(1.0f, rho), rho);   // lambda = 1: 1 / r
-            } else if (at_r) {
-                const float lw = __fsub_rn(w, al);
-                c.a = al;
-                c.v = __fmul_rn(lw, al);
-                c.b = fmaxf(lw, al);
-            } else {
-                const float lam = BINARY ? 1.0f : fminf(__fdiv_rn(bf, gam), 1.0f);
-                const float lw = __fmul_rn(lam, w);
-                c.a = __fsub_rn(w, lw);
-                c.v = __fmul_rn(__fmul_rn(lam, lw), gam);
-                c.b = fmaxf(lw, __fmul_rn(lam, gam));
-                if (slv[k] >= 0) om_i = __fdiv_rn(__fmul_rn(lam, __fadd_rn(1.0f, rho)), rho);
-            }
+            float om_i;
+            const Coef c = coef_entry(i, sw[i], sr[i], sg[i], sp[i], slv[k] >= 0, om_i);
             if (slv[k] >= 0) omr[slv[k]] = om_i;
             sg[i] = c.a;
             sp[i] = c.v;
             sw[i] = c.b;
             acc[0] = __fadd_rn(acc[0], c.a);
             acc[1] = __fadd_rn(acc[1], c.v);
-            const int j = j0 + i;
-            if (c.b > t2.b1 || (c.b == t2.b1 && j < t2.arg)) { t2.b2 = t2.b1; t2.b1 = c.b; t2.arg = j; }
-            else if (c.b > t2.b2) t2.b2 = c.b;
+            top2_add(c.b, j0 + i);
+        }
         }
         for (int o = 16; o > 0; o >>= 1) t2 = top2_merge(t2, shfl_xor_top2(t2, o));
         if (lane == 0) stop2[warp] = t2;
         ff tot[2];
         block_sum_f_w0<2>(acc, tot, redff);   // its barriers also publish stop2
+        if (STREAM) {
+            float lo2[2] = {acc2[0].lo, acc2[1].lo};
+            ff tlo[2];
+            block_sum_f_w0<2>(lo2, tlo, redff);
+            if (warp == 0) {
+                tot[0] = ff_add(tot[0], tlo[0]);
+                tot[1] = ff_add(tot[1], tlo[1]);
+            }
+        }
         if (warp == 0) {
-            Top2 x = stop2[lane];
+            Top2 x = lane < nw ? stop2[lane] : Top2{0.f, 0.f, 0x7fffffff};
             for (int o = 16; o > 0; o >>= 1) x = top2_merge(x, shfl_xor_top2(x, o));
             if (tid == 0) {
                 slot[parity].v[0] = tot[0];
@@ -2477,30 +2644,85 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     __syncthreads();
     stamp(2);
     if (!sc.no_fetch) {
+    const GainParams gp = sc.gp;
+    const int ARG = sc.arg;
+    const float fa = sc.sa_scale, fv = sc.sv_scale;
+    // f(i, k32, sa, sv, bb) for every entry of the slice: its 32-bit gain key (~bits of D g_i), its
+    // fixed-point-scaled a_i and v_i and the ordered bits of b_i (read from shared memory after the key
+    // pass, recomputed from w^, r and beta by the streaming variant)
+    auto search_pass = [&](auto&& f) {
+        if (STREAM) {
+            for (int g0 = 0; g0 < ns; g0 += U * T) {
+                float2 av[U];
+                unsigned kv_[U], bv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    av[u] = i < ns ? st_row[i] : make_float2(0.f, 0.f);
+                    kv_[u] = i < ns ? __float_as_uint(pa_row[i]) : 0u;
+                    bv[u] = i < ns ? __float_as_uint(pb_row[i]) : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    if (i < ns) f(i, kv_[u], av[u].x, av[u].y, bv[u]);
+                }
+            }
+        } else {
+            for (int i = tid; i < ns; i += T) f(i, skey[i], sa_[i], sv_[i], fmax_bits(sb[i]));
+        }
+    };
 
     // ---- phase 3: gain keys, then k* by the radix search
     {
-        const GainParams gp = sc.gp;
-        const int ARG = sc.arg;
-        const float fa = sc.sa_scale, fv = sc.sv_scale;
         // entries of gain exactly 0 (an underflowed weight: a = v = 0) end every order and never move
         // k*: they stay out of the search, counted (with their max b) in every residual
         unsigned kmin = 0xffffffffu, kmax = 0u, zc = 0u, zb = 0u;
-        for (int i = tid; i < ns; i += T) {
-            Coef c;
-            c.a = sg[i];
-            c.v = sp[i];
-            const unsigned k32 = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
-            skey[i] = k32;
+        auto range = [&](unsigned k32, unsigned bb) {
             if ((k32 & 0x7fffffffu) == 0x7fffffffu) {
                 ++zc;
-                zb = max(zb, fmax_bits(sb[i]));
+                zb = max(zb, bb);
             } else {
                 kmin = min(kmin, k32 & 0x7fffffffu);
                 kmax = max(kmax, k32 & 0x7fffffffu);
             }
-            sa_[i] = __fmul_rn(c.a, fa);   // fixed-point-scaled a_i, v_i (exactly converted below)
-            sv_[i] = __fmul_rn(c.v, fv);
+        };
+        if (STREAM) {
+            for (int g0 = 0; g0 < ns; g0 += U * T) {
+                float2 av[U];
+                float bv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    av[u] = i < ns ? st_row[i] : make_float2(0.f, 0.f);
+                    bv[u] = i < ns ? pb_row[i] : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    if (i >= ns) break;
+                    Coef c;
+                    c.a = av[u].x;
+                    c.v = av[u].y;
+                    const unsigned k32 = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
+                    const unsigned bb = fmax_bits(bv[u]);
+                    st_row[i] = make_float2(__fmul_rn(c.a, fa), __fmul_rn(c.v, fv));
+                    pa_row[i] = __uint_as_float(k32);
+                    pb_row[i] = __uint_as_float(bb);
+                    range(k32, bb);
+                }
+            }
+        } else {
+            for (int i = tid; i < ns; i += T) {
+                Coef c;
+                c.a = sg[i];
+                c.v = sp[i];
+                const unsigned k32 = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
+                skey[i] = k32;
+                sa_[i] = __fmul_rn(c.a, fa);   // fixed-point-scaled a_i, v_i (exactly converted below)
+                sv_[i] = __fmul_rn(c.v, fv);
+                range(k32, fmax_bits(sb[i]));
+            }
         }
         // the cluster's range of the other keys: the first search level spreads its bins over it
         kmin = __reduce_min_sync(0xffffffffu, kmin);
@@ -2515,10 +2737,10 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
         }
         __syncthreads();
         if (warp == 0) {
-            kmin = __reduce_min_sync(0xffffffffu, sext[lane][0]);
-            kmax = __reduce_max_sync(0xffffffffu, sext[lane][1]);
-            zc = __reduce_add_sync(0xffffffffu, sext[lane][2]);
-            zb = __reduce_max_sync(0xffffffffu, sext[lane][3]);
+            kmin = __reduce_min_sync(0xffffffffu, lane < nw ? sext[lane][0] : 0xffffffffu);
+            kmax = __reduce_max_sync(0xffffffffu, lane < nw ? sext[lane][1] : 0u);
+            zc = __reduce_add_sync(0xffffffffu, lane < nw ? sext[lane][2] : 0u);
+            zb = __reduce_max_sync(0xffffffffu, lane < nw ? sext[lane][3] : 0u);
             if (lane == 0) {
                 slot[parity].i[0] = (int)kmin;
                 slot[parity].i[1] = (int)kmax;
@@ -2565,21 +2787,21 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             const unsigned long long klo = sc.klo, span = sc.khi - sc.klo;
             // bins of 2^bs keys, bs the smallest shift that fits the range in nb bins (at least half used)
             const int bs = max(0, (64 - __clzll((long long)(span - 1ull))) - kSearchBits);
-            for (int i = tid; i < ns; i += T) {
-                const unsigned long long K = search_key(skey[i], j0 + i);
-                if (K < klo || K - klo >= span) continue;
+            search_pass([&](int i, unsigned k32, float sa, float sv, unsigned bb) {
+                const unsigned long long K = search_key(k32, j0 + i);
+                if (K < klo || K - klo >= span) return;
                 const unsigned d = (unsigned)((K - klo) >> bs);
                 unsigned pa[3], pv[3];
-                fixed_pieces(sa_[i], pa);
-                fixed_pieces(sv_[i], pv);
+                fixed_pieces(sa, pa);
+                fixed_pieces(sv, pv);
                 atomicAdd(&hist[d], 1u);
-                atomicMax(&hist[kSearchBins + d], fmax_bits(sb[i]));
+                atomicMax(&hist[kSearchBins + d], bb);
 #pragma unroll
                 for (int q = 0; q < 3; ++q) {
                     atomicAdd(&hist[(2 + q) * kSearchBins + d], pa[q]);
                     atomicAdd(&hist[(5 + q) * kSearchBins + d], pv[q]);
                 }
-            }
+            });
             __syncthreads();
             if (C > 1) {
                 // add the non-empty bins of the other slices into their owners' histograms
@@ -2595,24 +2817,28 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                 }
                 cl.sync();
             }
-            // cluster totals of this CTA's bins d0 = rank sl + 2 tid and d0 + 1
-            const int d0 = rank * sl + 2 * tid;
-            unsigned c2[2] = {0u, 0u}, b2[2] = {0u, 0u};
-            unsigned long long a2[2] = {0ull, 0ull}, v2[2] = {0ull, 0ull};
+            // cluster totals of this CTA's bins d0 = rank sl + BPT tid .. d0 + BPT - 1
+            const int d0 = rank * sl + BPT * tid;
+            unsigned c2[BPT], b2[BPT];
+            unsigned long long a2[BPT], v2[BPT];
+            SearchAcc mine = zero;
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                if (2 * tid + k >= sl) break;   // a slice of one bin (16 CTAs at the last level)
-                const int d = d0 + k;
-                c2[k] = hist[d];
-                b2[k] = hist[kSearchBins + d];
+            for (int k = 0; k < BPT; ++k) {
+                c2[k] = b2[k] = 0u;
+                a2[k] = v2[k] = 0ull;
+                if (BPT * tid + k < sl) {
+                    const int d = d0 + k;
+                    c2[k] = hist[d];
+                    b2[k] = hist[kSearchBins + d];
 #pragma unroll
-                for (int q = 0; q < 3; ++q) {
-                    a2[k] += (unsigned long long)hist[(2 + q) * kSearchBins + d] << (14 * q);
-                    v2[k] += (unsigned long long)hist[(5 + q) * kSearchBins + d] << (14 * q);
+                    for (int q = 0; q < 3; ++q) {
+                        a2[k] += (unsigned long long)hist[(2 + q) * kSearchBins + d] << (14 * q);
+                        v2[k] += (unsigned long long)hist[(5 + q) * kSearchBins + d] << (14 * q);
+                    }
                 }
+                mine = search_add(mine, SearchAcc{a2[k], v2[k], b2[k], c2[k]});
             }
             // exclusive suffix within the slice (higher bins = smaller gains); the slice total goes out
-            const SearchAcc mine = {a2[0] + a2[1], v2[0] + v2[1], max(b2[0], b2[1]), c2[0] + c2[1]};
             SearchAcc above = block_suffix_search(mine, sacc);
             if (tid == 0) ssum = search_add(above, mine);
             // the histogram is consumed: clear it for the next level
@@ -2634,13 +2860,14 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             above.v += sc.rest_v;
             above.b = max(above.b, sc.rest_b);
             above.c += sc.rest_c;
-            // residual after bin d0 + 1 = above; after bin d0 = above + bin d0 + 1
-            SearchAcc after[2];
-            after[1] = above;
-            after[0] = {above.a + a2[1], above.v + v2[1], max(above.b, b2[1]), above.c + c2[1]};
+            // residual after bin d0 + BPT - 1 = above; after bin d0 + k = after bin d0 + k + 1 plus that bin
+            SearchAcc after[BPT];
+            after[BPT - 1] = above;
+#pragma unroll
+            for (int k = BPT - 2; k >= 0; --k) after[k] = search_add(after[k + 1], SearchAcc{a2[k + 1], v2[k + 1], b2[k + 1], c2[k + 1]});
             int cand = 0x7fffffff;
 #pragma unroll
-            for (int k = 1; k >= 0; --k) {
+            for (int k = BPT - 1; k >= 0; --k) {
                 if (c2[k] > 0 && after[k].c > 0) {
                     const float A_ = (float)after[k].a * inv_fa, V_ = (float)after[k].v * inv_fv;
                     if (cert_f(A_, V_, __uint_as_float(after[k].b), ldf, Df) < a.eps_f) cand = d0 + k;
@@ -2649,15 +2876,17 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             cand = __reduce_min_sync(0xffffffffu, cand);
             if (lane == 0) redi[warp] = cand;
             __syncthreads();
-            cand = __reduce_min_sync(0xffffffffu, redi[lane]);
-            if (cand != 0x7fffffff && (cand - rank * sl) >> 1 == tid) {
-                const bool first = cand == d0;
-                const SearchAcc rest = first ? after[0] : after[1];
-                sprop.a = rest.a;
-                sprop.v = rest.v;
-                sprop.b = rest.b;
-                sprop.c = rest.c;
-                sprop.in_bin = first ? c2[0] : c2[1];
+            cand = __reduce_min_sync(0xffffffffu, lane < nw ? redi[lane] : 0x7fffffff);
+            if (cand != 0x7fffffff && (cand - rank * sl) / BPT == tid) {
+#pragma unroll
+                for (int k = 0; k < BPT; ++k)
+                    if (cand == d0 + k) {
+                        sprop.a = after[k].a;
+                        sprop.v = after[k].v;
+                        sprop.b = after[k].b;
+                        sprop.c = after[k].c;
+                        sprop.in_bin = c2[k];
+                    }
             }
             if (tid == 0) sprop.cand = cand;
             cl.sync();
@@ -2698,20 +2927,20 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
                 // few keys left in the boundary bin: gather them, sort them and scan them directly
                 if (tid == 0) ncand = 0;
                 __syncthreads();
-                for (int i = tid; i < ns; i += T) {
-                    const unsigned long long K = search_key(skey[i], j0 + i);
-                    if (K < sc.klo || K >= sc.khi) continue;
+                search_pass([&](int i, unsigned k32, float sa, float sv, unsigned bb) {
+                    const unsigned long long K = search_key(k32, j0 + i);
+                    if (K < sc.klo || K >= sc.khi) return;
                     const int at = atomicAdd(&ncand, 1);
                     unsigned pa[3], pv[3];
-                    fixed_pieces(sa_[i], pa);
-                    fixed_pieces(sv_[i], pv);
+                    fixed_pieces(sa, pa);
+                    fixed_pieces(sv, pv);
                     bcand[at].key = K;
                     bcand[at].a = (unsigned long long)pa[0] + ((unsigned long long)pa[1] << 14) +
                                  ((unsigned long long)pa[2] << 28);
                     bcand[at].v = (unsigned long long)pv[0] + ((unsigned long long)pv[1] << 14) +
                                  ((unsigned long long)pv[2] << 28);
-                    bcand[at].b = fmax_bits(sb[i]);
-                }
+                    bcand[at].b = bb;
+                });
                 cl.sync();
                 if (warp == 0) finish_small(cl, bcand, &ncand, bloc, sc, C, ldf, Df, inv_fa, inv_fv, a.eps_f);
                 __syncthreads();
@@ -2727,6 +2956,47 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
     {
         const unsigned long long kk = sc.kkey;
         static_assert(kDecideCap == 8 * kDecideThreads, "emit assumes eight entries per thread");
+        int* pos0 = cl.map_shared_rank(&wcnt[0], 0);
+        int nf = 0;
+        int32_t* el = elist + (int64_t)row * a.ws_n;
+        uint32_t* eb = a.ebits + (int64_t)row * (a.ws_n / 32 + 1);
+        float* omr = a.om + (int64_t)row * a.ws_n;
+        // one selected entry: its list position (claimed per warp), weight factor 1 if sampled, else a
+        // bit of the fetch bitmap
+        auto emit = [&](bool sel, int tok, int slt) {
+            const unsigned m8 = __ballot_sync(0xffffffffu, sel);
+            if (m8 == 0u) return;
+            int base = 0;
+            if (lane == __ffs(m8) - 1) base = atomicAdd(pos0, __popc(m8));
+            base = __shfl_sync(0xffffffffu, base, __ffs(m8) - 1);
+            if (sel) {
+                el[base + __popc(m8 & ((1u << lane) - 1u))] = tok;
+                if (slt >= 0) {
+                    omr[slt] = 1.0f;   // sampled and made exact: weight factor 1
+                } else {
+                    ++nf;
+                    atomicOr(&eb[tok >> 5], 1u << (tok & 31));
+                }
+            }
+        };
+        if (STREAM) {
+            // a warp-uniform trip count: the ballots of emit need every lane
+            for (int g0 = 0; g0 < ns; g0 += U * T) {
+                unsigned kv_[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    kv_[u] = i < ns ? __float_as_uint(pa_row[i]) : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int i = g0 + u * T + tid;
+                    const bool sel = i < ns && search_key(kv_[u], j0 + i) <= kk;
+                    const int64_t e = (int64_t)kv * V.n + j0 + i;
+                    emit(sel, sel ? V.ltok[e] : 0, sel ? V.lslot[e] : -1);
+                }
+            }
+        } else {
         bool sel[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -2741,27 +3011,8 @@ __global__ void __launch_bounds__(kDecideThreads, 1) decide_kernel(Views views, 
             tok[k] = sel[k] ? V.ltok[e] : 0;
             sl8[k] = sel[k] ? V.lslot[e] : -1;
         }
-        int* pos0 = cl.map_shared_rank(&wcnt[0], 0);
-        int nf = 0;
-        int32_t* el = elist + (int64_t)row * a.ws_n;
-        uint32_t* eb = a.ebits + (int64_t)row * (a.ws_n / 32 + 1);
-        float* omr = a.om + (int64_t)row * a.ws_n;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const unsigned m8 = __ballot_sync(0xffffffffu, sel[k]);
-            if (m8 == 0u) continue;
-            int base = 0;
-            if (lane == __ffs(m8) - 1) base = atomicAdd(pos0, __popc(m8));
-            base = __shfl_sync(0xffffffffu, base, __ffs(m8) - 1);
-            if (sel[k]) {
-                el[base + __popc(m8 & ((1u << lane) - 1u))] = tok[k];
-                if (sl8[k] >= 0) {
-                    omr[sl8[k]] = 1.0f;   // sampled and made exact: weight factor 1
-                } else {
-                    ++nf;
-                    atomicOr(&eb[tok[k] >> 5], 1u << (tok[k] & 31));
-                }
-            }
+        for (int k = 0; k < 8; ++k) emit(sel[k], tok[k], sl8[k]);
         }
         nf = __reduce_add_sync(0xffffffffu, (unsigned)nf);
         if (lane == 0 && nf > 0) atomicAdd(cl.map_shared_rank(&wcnt[1], 0), nf);
@@ -3270,7 +3521,16 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
     const verkv_config& cfg = ctx.cfg;
     const int rowsN = B * a.Hq;
     VK_TIMING_BEGIN();
-    const bool on_chip = max_nl <= g_decide_max_cluster * kDecideCap;
+    // The fused decision takes rows of up to kDecideMaxL entries.  It keeps the entries in shared
+    // memory (clusters of C CTAs of kDecideCap entries, one CTA per multiprocessor) when every row of
+    // the call fits one wave; otherwise the streaming variant re-reads them from L2 in every pass, with
+    // two CTAs per multiprocessor and clusters of Cs CTAs sized so the call's rows fill about one wave.
+    int C = 1;
+    while (C * kDecideCap < max_nl) C <<= 1;
+    const bool on_chip = max_nl <= kDecideMaxL;
+    const bool stream = on_chip && !(max_nl <= g_decide_max_cluster * kDecideCap && rowsN * C <= ctx.num_sms);
+    int Cs = 1;
+    while (Cs * 2 <= kDecideStreamMaxCluster && rowsN * Cs * 2 <= 2 * ctx.num_sms) Cs <<= 1;
     if (!on_chip) {
         init_rows_kernel<<<(rowsN + 127) / 128, 128, 0, st>>>(ctx.rows, views, a, B);
         VK_LAUNCHED("init_rows");
@@ -3315,28 +3575,25 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         VK_LAUNCHED("shortlist");
     }
     if (on_chip) {
-        int C = 1;
-        while (C * kDecideCap < max_nl) C <<= 1;
+        const int CC = stream ? Cs : C;
         cudaLaunchConfig_t lc = {};
-        lc.gridDim = dim3(rowsN * C);
-        lc.blockDim = dim3(kDecideThreads);
-        lc.dynamicSmemBytes = kDecideSmem;
+        lc.gridDim = dim3(rowsN * CC);
+        lc.blockDim = dim3(stream ? kDecideStreamThreads : kDecideThreads);
+        lc.dynamicSmemBytes = stream ? kDecideHistSmem : kDecideSmem;
         lc.stream = st;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.x = CC;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         lc.attrs = attr;
         lc.numAttrs = 2;
-        if (a.binary)
-            VK_CUDA(cudaLaunchKernelEx(&lc, decide_kernel<true>, views, a, ctx.rows, (const float2*)ctx.tl,
-                                       (const float2*)ctx.th, ctx.wl, ctx.mark, ctx.elist));
-        else
-            VK_CUDA(cudaLaunchKernelEx(&lc, decide_kernel<false>, views, a, ctx.rows, (const float2*)ctx.tl,
-                                       (const float2*)ctx.th, ctx.wl, ctx.mark, ctx.elist));
+        auto kern = a.binary ? (stream ? decide_kernel<true, true> : decide_kernel<true, false>)
+                             : (stream ? decide_kernel<false, true> : decide_kernel<false, false>);
+        VK_CUDA(cudaLaunchKernelEx(&lc, kern, views, a, ctx.rows, (const float2*)ctx.tl, (const float2*)ctx.th,
+                                   ctx.wl, ctx.mark, ctx.elist, ctx.keys));
         VK_LAUNCHED("decide");
     } else {
         const int wmax = std::max(max_nl, max_nh);
@@ -3349,7 +3606,7 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         select_kernel<<<rowsN, 1024, sel_smem, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
         VK_LAUNCHED("select");
     }
-    if (max_nl > g_decide_max_cluster * kDecideCap) {
+    if (!on_chip) {
         fallback_kernel<<<rowsN, 1024, 0, st>>>(views, a, ctx.rows, ctx.wl, ctx.keys, ctx.mark, ctx.elist);
         VK_LAUNCHED("fallback");
     }
@@ -3414,11 +3671,15 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     if (!g_attr_done) {
         VK_CUDA(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)(sizeof(unsigned long long) * kSelWidth)));
-        VK_CUDA(cudaFuncSetAttribute(decide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
-        VK_CUDA(cudaFuncSetAttribute(decide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
+        VK_CUDA(cudaFuncSetAttribute(decide_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
+        VK_CUDA(cudaFuncSetAttribute(decide_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem));
+        VK_CUDA(cudaFuncSetAttribute(decide_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kDecideHistSmem));
+        VK_CUDA(cudaFuncSetAttribute(decide_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kDecideHistSmem));
         // a 16-CTA cluster (non-portable) lets rows of up to 16 x kDecideCap entries stay on chip
-        if (cudaFuncSetAttribute(decide_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-            cudaFuncSetAttribute(decide_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        if (cudaFuncSetAttribute(decide_kernel<false, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+            cudaFuncSetAttribute(decide_kernel<true, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
             cudaLaunchConfig_t lc = {};
             lc.gridDim = dim3(kDecideMaxCluster);
             lc.blockDim = dim3(kDecideThreads);
@@ -3431,7 +3692,7 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
             lc.attrs = attr;
             lc.numAttrs = 1;
             int nclusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&nclusters, decide_kernel<false>, &lc) == cudaSuccess && nclusters > 0)
+            if (cudaOccupancyMaxActiveClusters(&nclusters, decide_kernel<false, false>, &lc) == cudaSuccess && nclusters > 0)
                 g_decide_max_cluster = kDecideMaxCluster;
         }
         cudaGetLastError();  // a refused query leaves no error behind
@@ -3480,8 +3741,8 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
         }
         ctx.last_n.push_back(s.n);
     }
-    if (cfg.shrinkage == VERKV_SHRINK_BINARY && max_nl > g_decide_max_cluster * kDecideCap) {
-        ctx.err = "binary shrinkage runs in the on-chip decision: |L| of a row is above its capacity";
+    if (cfg.shrinkage == VERKV_SHRINK_BINARY && max_nl > kDecideMaxL) {
+        ctx.err = "binary shrinkage runs in the fused decision: |L| of a row is above 262144";
         return VERKV_EUNSUPPORTED;
     }
     DecodeArgs a;
