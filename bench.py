@@ -178,9 +178,9 @@ def algorithmic_bytes(kernel, stats, traces, w, row_bytes, batch=1):
     return None
 
 
-def measured_traffic(w):
-    """DRAM bytes per launch of the decode kernels from the committed ncu summary of this workload, if
-    the kernel source is the one the counters were taken on (else {}: the kernels changed since)."""
+def measured_counters(w):
+    """The committed ncu record of this workload's decode kernels (DRAM bytes and warp instructions per
+    launch), if the kernel source is the one the counters were taken on (else {}: changed since)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", f"traffic_qwen3-4b-{w.n // 1024}k-{w.sketch}.txt")
     if not os.path.exists(path):
@@ -193,7 +193,12 @@ def measured_traffic(w):
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
     except (ValueError, KeyError, OSError):
         return {}
-    return rec["dram_bytes_per_launch"] if sha == rec["source_sha256"] else {}
+    return rec if sha == rec["source_sha256"] else {}
+
+
+def measured_traffic(w):
+    """DRAM bytes per launch of the decode kernels from the committed ncu summary (see measured_counters)."""
+    return measured_counters(w).get("dram_bytes_per_launch", {})
 
 
 def roof_entry(kernel, avg_ms, by, peak, unit, bound, peak_source, traffic=None, note=None):
@@ -395,8 +400,20 @@ def run_verkv(args):
         t_hbm = algorithmic_bytes("attn", stats0, traces, w, ROW_BYTES) / hbm_peak
         if t_link > t_hbm:
             roofline = roof_link("attn")
-    roof_score = roof_hbm("score", "2-bit scan: issue-bound (float-float logits on CUDA cores)"
-                          if w.sketch == "2bit" else None)
+    roof_score = roof_hbm("score")
+    # the 2-bit scan is bound by instruction issue (exact float-float sketch logits on the CUDA cores):
+    # its issue roofline is the warp instructions of a launch (committed ncu counter) over its time,
+    # against 4 instructions per cycle on each of the SMs at the sampled SM clock
+    roof_issue = None
+    inst = measured_counters(w).get("warp_instructions_per_launch", {}).get("score")
+    if inst and "score" in agg and clk and clk.get("sm_mhz"):
+        import torch as _t
+        sms = _t.cuda.get_device_properties(dev).multi_processor_count
+        avg_s = agg["score"][0] / agg["score"][1] / 1e3
+        peak = sms * 4 * clk["sm_mhz"] * 1e6
+        roof_issue = {"kernel": "score", "bound": "issue", "achieved": inst / avg_s, "peak": peak,
+                      "unit": "warp instructions/s", "frac": inst / avg_s / peak, "warp_instructions": inst,
+                      "avg_us": avg_s * 1e6, "peak_source": f"{sms} SMs x 4 issue slots x sampled {clk['sm_mhz']} MHz"}
     roof_decide = ({"kernel": "decide", "bound": "latency", "avg_us": agg["decide"][0] / agg["decide"][1] * 1e3,
                     "achieved": None, "peak": None, "frac": None,
                     "note": "cluster barriers and block reductions over on-chip rows; reported as time only"}
@@ -492,7 +509,8 @@ def run_verkv(args):
             "mean_kstar": statistics.mean(kstars) if kstars else None,
             "kernel_share": {k: round(v[0] / total_ms, 4) for k, v in sorted(agg.items(), key=lambda kv: -kv[1][0])},
             "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()},
-            "roofline": roofline, "roofline_score": roof_score, "roofline_attn": roof_hbm("attn"),
+            "roofline": roofline, "roofline_score": roof_score, "roofline_score_issue": roof_issue,
+            "roofline_attn": roof_hbm("attn"),
             "roofline_attn_link": roof_link("attn"), "roofline_decide": roof_decide,
             "host_link_peak_gbs": link_peak,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,

@@ -1973,16 +1973,16 @@ decide_kernel(Views views, DecodeArgs a,
     const int j0 = min(nl, rank * S), j1 = min(nl, j0 + S), ns = j1 - j0;
     const float* rl = V.rl + (int64_t)kv * V.n;
     // The streaming variant keeps an entry's state in global memory (L2) instead of shared memory and
-    // reads it back in every pass, four entries per thread in flight.  Up to phase 2 that state is w^
+    // reads it back in every pass, four entries per thread in flight.  Through phase 2 that state is w^
     // (the row of wl) and the KV head's r and ratios ((1 - r) / r, r / (1 - r)), shared by the query
     // rows of the head, from which alpha = w (1 - r), gamma = w (1 - r) / r and rho = r / (1 - r) are
-    // formed with the operations phase 0 of the on-chip variant uses.  From phase 2 on it is held in
-    // two scratch rows -- the row's logits in tl (dead once phase 0 has read them; float2 per entry) and
-    // the row of the full-row key buffer (idle on this path; two float planes of ws_npow2 entries):
-    //   phase 2:  tl = (a_i, v_i), plane B = b_i
-    //   phase 3:  tl = the fixed-point-scaled (a_i, v_i), plane A = gain key, plane B = bits of b_i
-    // An entry is written and read back only by the thread that owns it (entry i on thread i mod T,
-    // in every pass), so program order makes the values visible.
+    // formed with the operations phase 0 of the on-chip variant uses.  For the k* search (rows that
+    // fetch) the key pass writes each entry's search state into two scratch rows -- the row's logits
+    // in tl (dead once phase 0 has read them; float2 per entry) and the row of the full-row key buffer
+    // (idle on this path; two float planes of ws_npow2 entries): tl = the fixed-point-scaled
+    // (a_i, v_i), plane A = gain key, plane B = bits of b_i.  An entry is written and read back only by
+    // the thread that owns it (entry i on thread i mod T, in every pass), so program order makes the
+    // values visible.
     float* const wl_row = wl + (int64_t)row * a.ws_n + j0;
     const float* const rl_row = rl + j0;
     const float2* const lq_row = V.lq + (int64_t)kv * V.n + j0;
@@ -2533,8 +2533,6 @@ decide_kernel(Views views, DecodeArgs a,
                     const Coef c = coef_entry(i, wv[u], __fmul_rn(wv[u], __fsub_rn(1.0f, rv[u])),
                                               __fmul_rn(wv[u], qv[u].x), qv[u].y, sv_[u] >= 0, om_i);
                     if (sv_[u] >= 0) omr[sv_[u]] = om_i;
-                    st_row[i] = make_float2(c.a, c.v);
-                    pb_row[i] = c.b;
                     acc2[0] = ff_add_f(acc2[0], c.a);
                     acc2[1] = ff_add_f(acc2[1], c.v);
                     top2_add(c.b, j0 + i);
@@ -2688,30 +2686,17 @@ decide_kernel(Views views, DecodeArgs a,
             }
         };
         if (STREAM) {
-            for (int g0 = 0; g0 < ns; g0 += U * T) {
-                float2 av[U];
-                float bv[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int i = g0 + u * T + tid;
-                    av[u] = i < ns ? st_row[i] : make_float2(0.f, 0.f);
-                    bv[u] = i < ns ? pb_row[i] : 0.f;
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int i = g0 + u * T + tid;
-                    if (i >= ns) break;
-                    Coef c;
-                    c.a = av[u].x;
-                    c.v = av[u].y;
-                    const unsigned k32 = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
-                    const unsigned bb = fmax_bits(bv[u]);
-                    st_row[i] = make_float2(__fmul_rn(c.a, fa), __fmul_rn(c.v, fv));
-                    pa_row[i] = __uint_as_float(k32);
-                    pb_row[i] = __uint_as_float(bb);
-                    range(k32, bb);
-                }
-            }
+            // a_i, v_i, b_i recomputed from w^, r and beta (rows that fetch nothing never get here)
+            pass([&](int i, float w, float al, float gam, float rho) {
+                float om_;
+                const Coef c = coef_entry(i, w, al, gam, rho, false, om_);
+                const unsigned k32 = ~__float_as_uint(gain_num(c, j0 + i, ARG, gp));
+                const unsigned bb = fmax_bits(c.b);
+                st_row[i] = make_float2(__fmul_rn(c.a, fa), __fmul_rn(c.v, fv));
+                pa_row[i] = __uint_as_float(k32);
+                pb_row[i] = __uint_as_float(bb);
+                range(k32, bb);
+            });
         } else {
             for (int i = tid; i < ns; i += T) {
                 Coef c;
