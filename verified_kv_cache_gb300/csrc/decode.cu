@@ -111,13 +111,14 @@ __device__ __forceinline__ ff combine3(float s1, float s2, float s3)
     return fast_two_sum(t.hi, __fadd_rn(t.lo, s3));
 }
 
-// Exact logits of the tokens of H (resident keys), by H index, for the blocks of a scoring launch
-// past its L tiles: 8 threads per (token, query head), 16 channels each (float-float partial sums
-// combined over the 8 lanes), 128 / (8 G) tokens per block.  Also sets the weight factor of the
-// token's resident slot to 1 for every query head.
-template <typename T, int G>
-__device__ __forceinline__ void score_h_tile1(const Views& views, const float* __restrict__ q, const DecodeArgs& a,
-                                              RowState* __restrict__ rows, float2* __restrict__ th, int tile)
+// Exact logits of the tokens of H (resident keys), by H index: U tiles of kTile / (8 G) tokens each,
+// tiles t0, t0 + stride, ..., 8 threads per (token, query head), 16 channels each (float-float
+// partial sums combined over the 8 lanes).  The resident slots and key rows of all U tiles are loaded
+// before any is used.  Also sets the weight factor of each token's resident slot to 1 for every query
+// head.
+template <typename T, int G, int U>
+__device__ __forceinline__ void score_h_tiles(const Views& views, const float* __restrict__ q, const DecodeArgs& a,
+                                              RowState* __restrict__ rows, float2* __restrict__ th, int t0, int stride)
 {
     constexpr int TPB = kTile / (8 * G);
     const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
@@ -126,18 +127,25 @@ __device__ __forceinline__ void score_h_tile1(const Views& views, const float* _
     const int nh0 = V.counts[kv * 4 + 0], nh = nh0 + V.n_tail;   // H of the compress, then appended tokens
     const int t = threadIdx.x;
     const int part = t & 7, g = (t >> 3) % G, tk = t / (8 * G);
-    const int hk = tile * TPB + tk;
-    const bool live = hk < nh;
     const int row = row_of(b, kv * G + g, a.Hq);
-    ff s = {0.f, 0.f};
-    int slot = 0;
-    if (live) {
-        slot = hk < nh0 ? V.hslot[(int64_t)kv * n + hk] : V.counts[kv * 4 + 3] + (hk - nh0);
-        const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + slot) * 2 * kHeadDim + part * 16;
+    int hk[U], slot[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        hk[u] = (t0 + u * stride) * TPB + tk;
+        slot[u] = hk[u] < nh0 ? V.hslot[(int64_t)kv * n + hk[u]] : V.counts[kv * 4 + 3] + (hk[u] - nh0);
+    }
+    float kk[U][16];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (hk[u] < nh) {
+            const T* key = reinterpret_cast<const T*>(V.kvres) + (V.res_off[kv] + slot[u]) * 2 * kHeadDim + part * 16;
+            RowCvt<T>::load8(key, kk[u]);
+            RowCvt<T>::load8(key + 8, kk[u] + 8);
+        }
+    }
+    float qq[16];
+    {
         const float* qr = q + (int64_t)row * kHeadDim + part * 16;
-        float kk[16], qq[16];
-        RowCvt<T>::load8(key, kk);
-        RowCvt<T>::load8(key + 8, kk + 8);
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
             const float4 x = reinterpret_cast<const float4*>(qr)[c4];
@@ -146,24 +154,31 @@ __device__ __forceinline__ void score_h_tile1(const Views& views, const float* _
             qq[4 * c4 + 2] = x.z;
             qq[4 * c4 + 3] = x.w;
         }
-        float hi = 0.f, lo = 0.f;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const ff p = two_prod(qq[c], kk[c]);
-            const ff u = two_sum(hi, p.hi);
-            hi = u.hi;
-            lo = __fadd_rn(lo, __fadd_rn(u.lo, p.lo));
-        }
-        s = fast_two_sum(hi, lo);
     }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) s = ff_add(s, shfl_xor_ff(s, o));
     float mloc = -INFINITY;
-    if (live && part == 0) {
-        const ff x = ff_mul(s, a.inv_sqrt_d);
-        th[(int64_t)row * a.ws_n + hk] = make_float2(x.hi, x.lo);
-        a.om[(int64_t)row * a.ws_n + slot] = 1.0f;   // H: weight factor 1
-        mloc = x.hi;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const bool live = hk[u] < nh;
+        ff s = {0.f, 0.f};
+        if (live) {
+            float hi = 0.f, lo = 0.f;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const ff p = two_prod(qq[c], kk[u][c]);
+                const ff w = two_sum(hi, p.hi);
+                hi = w.hi;
+                lo = __fadd_rn(lo, __fadd_rn(w.lo, p.lo));
+            }
+            s = fast_two_sum(hi, lo);
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) s = ff_add(s, shfl_xor_ff(s, o));
+        if (live && part == 0) {
+            const ff x = ff_mul(s, a.inv_sqrt_d);
+            th[(int64_t)row * a.ws_n + hk[u]] = make_float2(x.hi, x.lo);
+            a.om[(int64_t)row * a.ws_n + slot[u]] = 1.0f;   // H: weight factor 1
+            mloc = fmaxf(mloc, x.hi);
+        }
     }
     // max per query head: lanes of head g are the 8-lane groups with the same g in the warp
     for (int o = 8 * G; o < 32; o <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
@@ -179,7 +194,9 @@ template <typename T, int G>
 __device__ __forceinline__ void score_h_tile(const Views& views, const float* __restrict__ q, const DecodeArgs& a,
                                              RowState* __restrict__ rows, float2* __restrict__ th, int block)
 {
-    for (int t = 0; t < kHTilesPerBlock; ++t) score_h_tile1<T, G>(views, q, a, rows, th, block * kHTilesPerBlock + t);
+    // two tiles at a time: the blocks of this path share the register budget of the L-tile blocks
+    for (int t = 0; t < kHTilesPerBlock; t += 2)
+        score_h_tiles<T, G, 2>(views, q, a, rows, th, block * kHTilesPerBlock + t, 1);
 }
 
 // 2-bit sketch tile: GPB sketch groups (of kTile tokens) per block; warp w scores group w, each
@@ -500,7 +517,8 @@ __global__ void __launch_bounds__(kTile, kInt8CtasPerSm) score_int8_kernel(Views
     // the exact logits of the KV head's H tokens, shared out over its CTAs
     constexpr int TPB = kTile / (8 * G);
     const int nh_tiles = (V.counts[kv * 4 + 0] + V.n_tail + TPB - 1) / TPB;
-    for (int ht = blockIdx.x; ht < nh_tiles; ht += gridDim.x) score_h_tile1<T, G>(views, q, a, rows, th, ht);
+    for (int ht = blockIdx.x; ht < nh_tiles; ht += kHTilesPerBlock * gridDim.x)
+        score_h_tiles<T, G, kHTilesPerBlock>(views, q, a, rows, th, ht, gridDim.x);
 }
 
 // Exact float-float dot product <q, k>/sqrt(d) of one key row (fp32 or bf16 elements).
