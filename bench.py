@@ -325,14 +325,17 @@ def run_verkv(args):
     torch.cuda.synchronize()
     # fetch statistics of the workload (one untimed job with traces)
     ctx.compress(0, 0, w.n, kv_host, kv_dev, obs, W, None, st)
-    fetch_frac, no_fetch, union_rows, host_rows, kstars = [], 0, [], [], []
+    fetch_frac, no_fetch, union_rows, host_rows, kstars, pf_copied, pf_used = [], 0, [], [], [], [], []
     for s in range(S):
         ctx.decode(0, [0], q_dev[s], w.eps, w.delta, out[s], st)
         tr = ctx.decode_trace(w.n_q)
         for h in range(w.n_kv):
             u, hr = ctx.fetch_stats(0, h)
+            pc, pu = ctx.prefetch_stats(0, h)
             union_rows.append(u)
             host_rows.append(hr)
+            pf_copied.append(pc)
+            pf_used.append(pu)
             fetch_frac.append(u / w.n)
         no_fetch += sum(t["no_fetch"] for t in tr)
         kstars += [t["kstar"] for t in tr]
@@ -355,12 +358,21 @@ def run_verkv(args):
         dist.barrier()
     clk = clocks.stop() if clocks else None
     # the same K steps again with an event pair around every kernel: per-kernel durations for the
-    # rooflines and the kernel shares
+    # rooflines and the kernel shares, with the rows the attention itself read over the host link in
+    # those calls (the events stop the overlap of the kernels, so the prefetch, which runs beside the
+    # decision, finds it decided and copies next to nothing there)
     ctx.set_kernel_timing(True)
     kt = []
+    kt_host = []
     for _ in range(args.steps):
         one_step([])
         kt += ctx.kernel_times(st)   # drains the per-kernel records (one sync between steps)
+    ctx.compress(0, 0, w.n, kv_host, kv_dev, obs, W, None, st)
+    for s in range(S):
+        flush()
+        ctx.decode(0, [0], q_dev[s], w.eps, w.delta, out[s], st)
+        kt_host.append(sum(ctx.fetch_stats(0, h)[1] for h in range(w.n_kv)))
+    ctx.kernel_times(st)
     torch.cuda.synchronize()
     ctx.set_kernel_timing(False)
     comp_ms = [a.elapsed_time(b) for k, a, b in events if k == "compress"]
@@ -371,10 +383,18 @@ def run_verkv(args):
 
     agg = kernel_agg(kt)
     total_ms = sum(v[0] for v in agg.values())
+    # the attention's rows in the per-kernel timing pass (what its timed launches moved) for its rooflines
     traces = {"union_rows": statistics.mean(union_rows) * w.n_kv if union_rows else 0,
-              "host_rows": statistics.mean(host_rows) * w.n_kv if host_rows else 0}
+              "host_rows": statistics.mean(kt_host) if kt_host else 0}
+    # the whole decode job as it runs: every byte over the host link (the prefetch's copies and the
+    # attention's own reads) against the decode time
+    link_bytes = (statistics.mean(host_rows) + statistics.mean(pf_copied)) * w.n_kv * ROW_BYTES if host_rows else 0
+    job_link = {"bytes_per_call": link_bytes, "decode_us_per_call": statistics.mean(dec_ms) * 1e3,
+                "achieved_gbs": link_bytes / (statistics.mean(dec_ms) / 1e3) / 1e9}
     traffic = measured_traffic(w)
     link_peak = measure_link_peak(dev, st) if rank == 0 else None
+    if link_peak:
+        job_link["frac_of_link_peak"] = job_link["achieved_gbs"] / link_peak
 
     def roof_hbm(kname, note=None):
         if kname not in agg:
@@ -503,7 +523,12 @@ def run_verkv(args):
             "compress_us_steps": [round(x * 1e3, 1) for x in comp_ms],
             "wall_ms_per_step": t_wall / args.steps * 1e3,
             "fetch_fraction_per_token": statistics.mean(fetch_frac) if fetch_frac else None,
-            "host_rows_per_call": traces["host_rows"], "union_rows_per_call": traces["union_rows"],
+            "host_rows_per_call": statistics.mean(host_rows) * w.n_kv,
+            "union_rows_per_call": traces["union_rows"],
+            "prefetch": {"rows_copied_per_call": statistics.mean(pf_copied) * w.n_kv,
+                         "rows_used_per_call": statistics.mean(pf_used) * w.n_kv,
+                         "precision": sum(pf_used) / max(1, sum(pf_copied))},
+            "link_over_decode_job": job_link,
             "device_footprint": footprint(stats0, w, -2),
             "no_fetch_rate": no_fetch / max(1, len(kstars)),
             "mean_kstar": statistics.mean(kstars) if kstars else None,

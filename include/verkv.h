@@ -218,8 +218,9 @@ verkv_status verkv_get_fetch_set(verkv_ctx* ctx, int32_t b, int32_t kv_head, int
                                  int32_t* count, verkv_stream stream);
 
 /* Rows of the last verkv_decode for KV head (b, kv_head): n_union = |the union of its query heads'
- * L_g[:k*] \ S| (the rows the step needs beyond the resident ones), n_host = how many of them were read
- * over the host link (the others came from the staging cache).  Either pointer may be NULL. */
+ * L_g[:k*] \ S| (the rows the step needs beyond the resident ones), n_host = how many of them the
+ * attention read over the host link (the others came from the staging cache or the prefetch buffer).
+ * Either pointer may be NULL. */
 verkv_status verkv_get_fetch_stats(verkv_ctx* ctx, int32_t b, int32_t kv_head, int32_t* n_union, int32_t* n_host,
                                    verkv_stream stream);
 
@@ -244,6 +245,27 @@ verkv_status verkv_get_fetch_stats(verkv_ctx* ctx, int32_t b, int32_t kv_head, i
 #define VERKV_STAGE_ETA_N (-2)
 #define VERKV_STAGE_ALL (-1)
 verkv_status verkv_set_stage_capacity(verkv_ctx* ctx, int64_t rows_per_kv_head);
+
+/*
+ * Speculative prefetch (no counterpart in the algorithms: results are identical with it on or off).
+ * The host link idles while the decision runs, and the rows a decode fetches are mostly the tokens of
+ * L \ S with the largest sketch weights.  Beside the decision, up to rows_per_kv_head such tokens of
+ * each (sequence, KV head) -- neither sampled nor staged, ranked by their largest sketch weight over
+ * the head's query rows relative to each row's maximum (within 16 in log weight) -- have their K/V rows
+ * copied from the pinned host cache into a per-context device buffer; the copying stops once every
+ * query row of the call is decided.  It runs on calls of at most 64 query rows that leave
+ * multiprocessors free beside the decision (at larger batches the decision is bound by L2 / HBM and
+ * the prefetch slowed it).  The attention reads each row it needs from that buffer when the
+ * buffer holds it, and over the host link otherwise.  Default 4096 (a buffer of max_batch x n_kv_heads
+ * x 4096 rows, 512 B each in bf16, allocated at the next verkv_decode); 0 = off.  Takes effect at the
+ * next verkv_decode.  EINVAL: rows_per_kv_head outside [0, 65536].
+ * verkv_get_prefetch_stats: for KV head (b, kv_head) of the last verkv_decode, n_copied = rows the
+ * prefetch copied, n_used = of the rows the step needed beyond the resident and staged ones, how
+ * many came from the prefetch buffer (the others crossed the host link during the attention).
+ */
+verkv_status verkv_set_prefetch(verkv_ctx* ctx, int32_t rows_per_kv_head);
+verkv_status verkv_get_prefetch_stats(verkv_ctx* ctx, int32_t b, int32_t kv_head, int32_t* n_copied, int32_t* n_used,
+                                      verkv_stream stream);
 
 /*
  * Shortlist (Appendix A.1): at every decode, among the tokens of L outside the sample, the k of each KV

@@ -587,6 +587,7 @@ def test_staging_cache_reuses_fetched_rows():
     for cap in [-1, 0, 10, -2]:
         ctx = make_lib_ctx(w)
         ctx.set_stage_capacity(cap)
+        ctx.set_prefetch(0)   # every needed row not staged crosses the host link (the prefetch has its own test)
         gc = GpuCase(w, ctx)
         tau, stats, osl = _compress_both(w, gc)
         first = gc.decode(w.queries[0], 0.01, 0.05)
@@ -606,6 +607,40 @@ def test_staging_cache_reuses_fetched_rows():
     assert np.array_equal(outs[-1].view(np.uint32), outs[0].view(np.uint32))
     assert np.array_equal(outs[-1].view(np.uint32), outs[10].view(np.uint32))
     assert np.array_equal(outs[-1].view(np.uint32), outs[-2].view(np.uint32))
+
+
+def test_prefetch_copies_ahead_and_changes_no_result():
+    """The speculative prefetch copies rows of likely-fetched tokens while the decision runs; the
+    attention reads the needed ones from its buffer.  Outputs and exact sets are bit-identical with it
+    on and off; with staging off, every needed row comes either from the buffer or over the host link
+    (n_host + n_used = n_union), the buffer serves only rows it holds (n_used <= n_copied <= cap), and
+    on random queries it serves some.  Parity against the oracle with the prefetch on runs in every
+    other test (it is on by default)."""
+    w = small_case("int8", n=8000, steps=4, query_mode="needle_half")
+    res = {}
+    for pf in (0, 512):
+        ctx = make_lib_ctx(w)
+        ctx.set_stage_capacity(0)
+        ctx.set_prefetch(pf)
+        gc = GpuCase(w, ctx)
+        tau, stats, osl = _compress_both(w, gc)
+        outs, sets, st_ = [], [], []
+        for s in range(4):
+            outs.append(gc.decode(w.queries[s], 0.01, 0.05))
+            sets.append([ctx.exact_set(0, hq, w.n) for hq in range(w.n_q)])
+            st_.append([(ctx.fetch_stats(0, h), ctx.prefetch_stats(0, h)) for h in range(w.n_kv)])
+        if pf:
+            _decode_parity(w, gc, osl, 0.01, 0.05)
+        res[pf] = (outs, sets, st_)
+        ctx.close()
+    for s in range(4):
+        assert np.array_equal(res[0][0][s].view(np.uint32), res[512][0][s].view(np.uint32)), s
+        assert all(np.array_equal(x, y) for x, y in zip(res[0][1][s], res[512][1][s]))
+        for ((nu0, nh0), (nc0, nd0)), ((nu, nh), (nc, nd)) in zip(res[0][2][s], res[512][2][s]):
+            assert nc0 == 0 and nd0 == 0 and nh0 == nu0
+            assert nu == nu0 and nh + nd == nu and nd <= nc <= 512, (s, nu, nh, nc, nd)
+    used = sum(nd for s in (1, 3) for (_, (nc, nd)) in res[512][2][s])
+    assert used > 0, res[512][2]
 
 
 def _shortlist_near_tie(orow, got_tokens):

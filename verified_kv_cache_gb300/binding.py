@@ -112,6 +112,10 @@ def lib():
     L.verkv_get_shortlist.restype = st
     L.verkv_set_stage_capacity.argtypes = [P, ctypes.c_int64]
     L.verkv_set_stage_capacity.restype = st
+    L.verkv_set_prefetch.argtypes = [P, i32]
+    L.verkv_set_prefetch.restype = st
+    L.verkv_get_prefetch_stats.argtypes = [P, i32, i32, P, P, P]
+    L.verkv_get_prefetch_stats.restype = st
     L.verkv_selftest_wait_timeout.argtypes = [P, P]
     L.verkv_selftest_wait_timeout.restype = st
     L.verkv_set_append_capacity.argtypes = [P, i32]
@@ -282,6 +286,16 @@ class VerKV:
         cnt = ctypes.c_int32()
         self._check(lib().verkv_get_shortlist(self.h, b, kv, out.ctypes.data, cap, ctypes.byref(cnt), _stream(stream)))
         return out[:min(cnt.value, cap)].copy()
+
+    def set_prefetch(self, rows_per_kv_head: int):
+        """Rows per (sequence, KV head) the speculative prefetch may copy ahead (0 = off; default 4096)."""
+        self._check(lib().verkv_set_prefetch(self.h, int(rows_per_kv_head)))
+
+    def prefetch_stats(self, b, kv, stream=None):
+        """(rows the prefetch copied, rows the attention read from them) for KV head (b, kv), last decode."""
+        nc, nu = ctypes.c_int32(), ctypes.c_int32()
+        self._check(lib().verkv_get_prefetch_stats(self.h, b, kv, ctypes.byref(nc), ctypes.byref(nu), _stream(stream)))
+        return nc.value, nu.value
 
     def set_stage_capacity(self, rows_per_kv_head: int):
         """Staging cache rows per KV head and slot (from the next compress on): STAGE_ETA_N (-2, default) =

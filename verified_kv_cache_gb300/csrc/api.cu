@@ -33,7 +33,7 @@ void free_ws(Ctx& c)
 {
     void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.adone, c.ucount,
                     c.part, c.hrows, c.slist, c.scount, c.shist,
-                    c.d_slot_n};
+                    c.d_slot_n, c.pf_buf, c.pf_of, c.pf_tok, c.pf_cnt, c.pf_used, c.dprog};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     if (c.h_err) cudaFreeHost(c.h_err);
@@ -72,6 +72,12 @@ verkv_status alloc_ws(Ctx& ctx)
     VK_CUDA(cudaMemset(ctx.ucount, 0, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMalloc(&ctx.hrows, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMemset(ctx.hrows, 0, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMalloc(&ctx.pf_cnt, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMemset(ctx.pf_cnt, 0, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMalloc(&ctx.pf_used, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMemset(ctx.pf_used, 0, sizeof(int32_t) * kvb));
+    VK_CUDA(cudaMalloc(&ctx.dprog, sizeof(unsigned long long)));
+    VK_CUDA(cudaMemset(ctx.dprog, 0, sizeof(unsigned long long)));
     VK_CUDA(cudaMalloc(&ctx.slist, sizeof(int32_t) * kvb * kMaxShortlist));
     VK_CUDA(cudaMalloc(&ctx.scount, sizeof(int32_t) * kvb));
     VK_CUDA(cudaMemset(ctx.scount, 0, sizeof(int32_t) * kvb));
@@ -405,6 +411,33 @@ verkv_status verkv_get_fetch_stats(verkv_ctx* h, int32_t b, int32_t kv, int32_t*
     VK_CUDA(cudaStreamSynchronize(st));
     if (n_union) *n_union = v[0];
     if (n_host) *n_host = v[1];
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_prefetch_stats(verkv_ctx* h, int32_t b, int32_t kv, int32_t* n_copied, int32_t* n_used,
+                                      verkv_stream stream)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (b < 0 || b >= ctx.last_B || kv < 0 || kv >= ctx.cfg.n_kv_heads) return fail(ctx, VERKV_EINVAL, "row out of range");
+    cudaStream_t st = (cudaStream_t)stream;
+    const int idx = b * ctx.cfg.n_kv_heads + kv;
+    int32_t v[2] = {0, 0};
+    VK_CUDA(cudaMemcpyAsync(&v[0], ctx.pf_cnt + idx, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaMemcpyAsync(&v[1], ctx.pf_used + idx, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaStreamSynchronize(st));
+    if (n_copied) *n_copied = ctx.last_pf_cap > 0 ? std::min(v[0], ctx.last_pf_cap) : 0;
+    if (n_used) *n_used = v[1];
+    return VERKV_OK;
+}
+
+verkv_status verkv_set_prefetch(verkv_ctx* h, int32_t rows_per_kv_head)
+{
+    if (!h) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    if (rows_per_kv_head < 0 || rows_per_kv_head > 65536)
+        return fail(ctx, VERKV_EINVAL, "prefetch rows per KV head must be in [0, 65536]");
+    ctx.prefetch_rows = rows_per_kv_head;
     return VERKV_OK;
 }
 

@@ -35,6 +35,14 @@ struct DecodeArgs {
     int* err;         // mapped host word, set when a bounded device-side wait gives up
     int* done;        // [B Hkv] attention blocks finished per KV head (the last one merges; left at 0)
     int32_t* hrows;   // [B Hkv] rows read over the host link (zeroed by the scoring kernel of the call)
+    // speculative prefetch (see prefetch_kernel): rows copied ahead, their maps and counters
+    unsigned char* pf_buf;
+    int32_t* pf_of;
+    int32_t* pf_tok;
+    int32_t* pf_cnt;
+    int32_t* pf_used;
+    unsigned long long* dprog;
+    int pf_cap;       // rows per (sequence, KV head); 0: the prefetch is off for this call
     int Hkv, Hq, G, ws_n, ws_npow2, gen, nsplit;
     int binary;       // 1: binary shrinkage coefficients (lambda in {1, r}), 0: the clipped fixed point
     float eps_f;
@@ -210,7 +218,12 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
                                                            float2* __restrict__ th, int n_ltiles)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
-    if (blockIdx.x == 0 && threadIdx.x == 0) a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
+        a.pf_cnt[blockIdx.y] = 0;   // rows the prefetch claims, and of them the attention reads
+        a.pf_used[blockIdx.y] = 0;
+        if (blockIdx.y == 0) *a.dprog = (unsigned long long)(unsigned)a.gen << 32;   // no row decided yet
+    }
     if ((int)blockIdx.x >= n_ltiles) {
         score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
         return;
@@ -506,7 +519,12 @@ __global__ void __launch_bounds__(kTile, kInt8CtasPerSm) score_int8_kernel(Views
                                                                             float2* __restrict__ th, int n_lchunks)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
-    if (blockIdx.x == 0 && threadIdx.x == 0) a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
+        a.pf_cnt[blockIdx.y] = 0;   // rows the prefetch claims, and of them the attention reads
+        a.pf_used[blockIdx.y] = 0;
+        if (blockIdx.y == 0) *a.dprog = (unsigned long long)(unsigned)a.gen << 32;   // no row decided yet
+    }
     const int b = blockIdx.y / a.Hkv, kv = blockIdx.y % a.Hkv;
     const SlotView& V = views.v[b];
     const int n = V.n;
@@ -954,7 +972,12 @@ __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const f
                                                             float2* __restrict__ th, int n_ltiles)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
-    if (blockIdx.x == 0 && threadIdx.x == 0) a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
+        a.pf_cnt[blockIdx.y] = 0;   // rows the prefetch claims, and of them the attention reads
+        a.pf_used[blockIdx.y] = 0;
+        if (blockIdx.y == 0) *a.dprog = (unsigned long long)(unsigned)a.gen << 32;   // no row decided yet
+    }
     if ((int)blockIdx.x >= n_ltiles) {
         score_h_tile<T, G>(views, q, a, rows, th, blockIdx.x - n_ltiles);
         return;
@@ -1947,8 +1970,8 @@ decide_kernel(Views views, DecodeArgs a,
                                                                    int32_t* __restrict__ elist,
                                                                    unsigned long long* scratch)
 {
-    pdl_trigger();   // the attention kernel may start its independent prologue
     pdl_wait();      // the scoring kernel has completed (its logits, maxima and weight factors are visible)
+    pdl_trigger();   // the next kernel (prefetch or attention) may start: the scoring kernel's results are complete
     cg::cluster_group cl = cg::this_cluster();
     const int C = (int)cl.num_blocks();
     const int rank = (int)cl.block_rank();
@@ -3029,6 +3052,7 @@ decide_kernel(Views views, DecodeArgs a,
     stamp(5);
 
     cl.sync();   // no CTA leaves while its shared memory may still be read
+    if (rank == 0 && tid == 0) atomicAdd(a.dprog, 1ull);   // this row is decided (read by the prefetch)
 }
 
 // --------------------------------------------------------------------------------------------
@@ -3057,6 +3081,194 @@ __global__ void __launch_bounds__(256) om_sampled_kernel(Views views, DecodeArgs
         }
         a.om[(int64_t)row * a.ws_n + sl] = w;
     }
+}
+
+// --------------------------------------------------------------------------------------------
+// Speculative prefetch (no counterpart in the algorithms; results are identical with it on or off).
+// The host link idles while the decision runs, and the rows a decode ends up fetching are mostly the
+// tokens of L \ S with the largest sketch weights.  This kernel runs beside the decision (launched
+// after it with programmatic dependent launch): per (sequence, KV head) it takes the tokens of
+// L \ S that are neither sampled nor staged, keyed by their largest sketch weight over the head's
+// query rows relative to each row's maximum, log(w^ / w^_max) = max_g (t^_g - m_g); each of its blocks
+// bins its share of them in steps of 1/16 over (-16, 0], keeps the top pf_cap / gridDim.y by those
+// bins and copies their K/V rows from pinned host memory into the call's prefetch buffer (a warp per
+// row, 16 bytes a lane), recording token -> row.  It stops claiming rows once every query row of the
+// call is decided (the decision counts its rows), and before exiting it waits for the decision to
+// complete, so that the attention, launched after it, sees both.  The attention reads a needed row
+// from this buffer instead of the host when the buffer holds it.
+// --------------------------------------------------------------------------------------------
+constexpr int kPfThreads = 256;
+constexpr int kPfBins = 256;
+constexpr int kPfListCap = 2048;   // candidates a prefetch block keeps
+constexpr int kPfMaxRows = 64;     // query rows of a call up to which the prefetch runs
+
+template <typename T, int G>
+__global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, DecodeArgs a, const RowState* rows,
+                                                              const float2* tl, int rows_in_call)
+{
+    constexpr int ROWB = 2 * kHeadDim * (int)sizeof(T);
+    constexpr int CHUNKS = ROWB / 16;
+    constexpr int U = 4;   // entries per thread in flight
+    constexpr int NW = kPfThreads / 32;
+    __shared__ unsigned hist[kPfBins], off[kPfBins];
+    __shared__ int lst[kPfListCap];                 // candidates (L indices), then their tokens in bin order
+    __shared__ unsigned char lbin[kPfListCap];
+    __shared__ int s_n, s_thr, s_base, s_stop;
+    pdl_trigger();   // the attention may launch and wait at its own dependency point
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
+    const SlotView& V = views.v[b];
+    const int nl = V.counts[kv * 4 + 1];
+    const int row0 = row_of(b, kv * G, a.Hq);
+    const int per = (nl + gridDim.y - 1) / gridDim.y;
+    const int j0 = min(nl, (int)blockIdx.y * per), j1 = min(nl, j0 + per);
+    const int cap_blk = min(kPfListCap, a.pf_cap / (int)gridDim.y);
+    const int64_t kvn = (int64_t)kv * V.n;
+    const int32_t* stg_of = V.stage_of ? V.stage_of + kvn : nullptr;
+    float m[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) m[g] = untag_max(__ldcg(&rows[row0 + g].m_tag), (unsigned)a.gen);
+    // bins of U entries j = base + u T + tid (-1: sampled, so resident, or below the range); every load
+    // of the group is issued before any is used
+    auto bins = [&](int base, int (&bn)[U]) {
+        int sl[U];
+        float k[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = base + u * kPfThreads + tid;
+            sl[u] = j < j1 ? __ldg(V.lslot + kvn + j) : 0;
+            k[u] = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+                if (j < j1) k[u] = fmaxf(k[u], __ldcg(tl + (int64_t)(row0 + g) * a.ws_n + j).x - m[g]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            bn[u] = (sl[u] < 0 && k[u] > -16.0f) ? min(kPfBins - 1, (int)(-k[u] * 16.0f)) : -1;
+    };
+    for (int i = tid; i < kPfBins; i += kPfThreads) hist[i] = 0u;
+    if (tid == 0) {
+        s_n = 0;
+        s_stop = 0;
+    }
+    __syncthreads();
+    // pass 1: the histogram of the block's share
+    for (int base = j0; base < j1; base += U * kPfThreads) {
+        int bn[U];
+        bins(base, bn);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (bn[u] >= 0) atomicAdd(&hist[bn[u]], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // the bins holding the block's top cap_blk (staged tokens are counted here and dropped below)
+        int thr = -1;
+        unsigned cum = 0u;
+        for (int i = 0; i < kPfBins && cum < (unsigned)cap_blk; ++i) {
+            cum += hist[i];
+            thr = i;
+        }
+        s_thr = thr;
+    }
+    __syncthreads();
+    const int thr = s_thr;
+    if (thr >= 0) {
+        // pass 2: the candidates (at most cap_blk), then ordered by bin (a counting sort)
+        for (int base = j0; base < j1; base += U * kPfThreads) {
+            int bn[U];
+            bins(base, bn);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (bn[u] >= 0 && bn[u] <= thr) {
+                    const int at = atomicAdd(&s_n, 1);
+                    if (at < cap_blk) {
+                        lst[at] = base + u * kPfThreads + tid;
+                        lbin[at] = (unsigned char)bn[u];
+                    }
+                }
+        }
+        __syncthreads();
+        const int n0 = min(s_n, cap_blk);
+        // their tokens; staged ones are dropped (-1): they are read from the staging cache anyway
+        for (int i = tid; i < n0; i += kPfThreads) {
+            const int tok = __ldg(V.ltok + kvn + lst[i]);
+            lst[i] = (stg_of && __ldcg(stg_of + tok) >= 0) ? -1 : tok;
+        }
+        for (int i = tid; i < kPfBins; i += kPfThreads) hist[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n0; i += kPfThreads)
+            if (lst[i] >= 0) atomicAdd(&hist[lbin[i]], 1u);
+        __syncthreads();
+        if (tid == 0) {
+            unsigned c = 0u;
+            for (int i = 0; i < kPfBins; ++i) {
+                off[i] = c;
+                c += hist[i];
+            }
+            s_n = (int)c;   // the kept candidates
+        }
+        __syncthreads();
+        // the kept tokens in bin order (a counting sort through registers)
+        int tk[kPfListCap / kPfThreads], ps[kPfListCap / kPfThreads];
+#pragma unroll
+        for (int u = 0; u < kPfListCap / kPfThreads; ++u) {
+            const int i = u * kPfThreads + tid;
+            tk[u] = i < n0 ? lst[i] : -1;
+            ps[u] = tk[u] >= 0 ? (int)atomicAdd(&off[lbin[i]], 1u) : 0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kPfListCap / kPfThreads; ++u)
+            if (tk[u] >= 0) lst[ps[u]] = tk[u];
+        __syncthreads();
+        const int n1 = s_n;
+        if (tid == 0) s_base = atomicAdd(&a.pf_cnt[unit], n1);   // prefetch rows s_base .. of this block
+        __syncthreads();
+        const int base_row = s_base;
+        unsigned char* buf = a.pf_buf + (int64_t)unit * a.pf_cap * ROWB;
+        const unsigned char* host = reinterpret_cast<const unsigned char*>(V.kv_host) + kvn * ROWB;
+        int32_t* pf_tok = a.pf_tok + (int64_t)unit * a.pf_cap;
+        int32_t* pf_of = a.pf_of + (int64_t)unit * a.ws_n;
+        // copies in bin order, a warp per row and four rows in flight (lane l moves bytes 16 l .. 16 l +
+        // 15, and the next 512 when rows are fp32); once every query row of the call is decided the
+        // remaining claimed rows are released (token -1), so the fetch no longer waits for them
+        bool stop = false;
+        for (int q0 = warp * 4; q0 < n1; q0 += 4 * NW) {
+            if (!stop && lane == 0) {
+                const unsigned long long p = *reinterpret_cast<volatile unsigned long long*>(a.dprog);
+                stop = (unsigned)(p >> 32) == (unsigned)a.gen && (int)(p & 0xffffffffu) >= rows_in_call;
+            }
+            stop = __shfl_sync(0xffffffffu, stop, 0);
+            uint4 v[4][CHUNKS / 32];
+            int tok4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int qi = q0 + u;
+                tok4[u] = qi < n1 && base_row + qi < a.pf_cap ? lst[qi] : -1;
+                if (tok4[u] >= 0 && !stop) {
+                    const uint4* src = reinterpret_cast<const uint4*>(host + (int64_t)tok4[u] * ROWB);
+#pragma unroll
+                    for (int c = 0; c < CHUNKS / 32; ++c) v[u][c] = src[lane + 32 * c];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (tok4[u] < 0) continue;
+                const int sr = base_row + q0 + u;
+                if (!stop) {
+                    uint4* dst = reinterpret_cast<uint4*>(buf + (int64_t)sr * ROWB);
+#pragma unroll
+                    for (int c = 0; c < CHUNKS / 32; ++c) dst[lane + 32 * c] = v[u][c];
+                }
+                if (lane == 0) {
+                    pf_tok[sr] = stop ? -1 : tok4[u];
+                    if (!stop) pf_of[tok4[u]] = sr;
+                }
+            }
+        }
+    }
+    pdl_wait();   // the decision has completed: the attention, launched after this grid, may read its results
 }
 
 // --------------------------------------------------------------------------------------------
@@ -3102,6 +3314,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     __shared__ int s_sdst[NS][CR];   // staging-cache row to fill from a fetched row of the chunk (-1: none)
     __shared__ int s_stok[NS][CR];   // its token
     __shared__ int s_hcnt;           // rows this block read over the host link
+    __shared__ int s_pcnt;           // rows this block read from the call's prefetch buffer
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
     const SlotView& V = views.v[b];
@@ -3203,12 +3416,18 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     int32_t* stg_of = V.stage_of ? V.stage_of + (int64_t)kv * V.n : nullptr;
     unsigned char* stg = stg_of ? reinterpret_cast<unsigned char*>(V.stage) + V.stage_off[kv] * (int64_t)ROWB : nullptr;
     const int stg_cap = stg_of ? (int)(V.stage_off[kv + 1] - V.stage_off[kv]) : 0;
+    // the rows this call's prefetch copied ahead (written by the previous grid: read through L2)
+    const int pf_n = a.pf_cap > 0 ? min(a.pf_cap, __ldcg(&a.pf_cnt[unit])) : 0;
+    const int32_t* pf_of = a.pf_of + (int64_t)unit * a.ws_n;
+    const int32_t* pf_tok = a.pf_tok + (int64_t)unit * a.pf_cap;
+    const unsigned char* pfb = a.pf_buf + (int64_t)unit * a.pf_cap * ROWB;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_bad = 0;
         s_hcnt = 0;
+        s_pcnt = 0;
     }
     if (tid < G) {
         s_m[tid] = -INFINITY;
@@ -3225,7 +3444,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
         const int row = warp + 8 * lane;
         if (!(lane < CR / 8 && row < cnt)) return make_int2(0, -1);
         const int tok = ul[r0 + row - m_res];
-        return make_int2(tok, stg_of ? stg_of[tok] : -1);
+        int src = stg_of ? stg_of[tok] : -1;   // >= 0: staged row
+        if (src < 0 && pf_n > 0) {
+            // copied ahead by this call's prefetch: the row records it when its token agrees
+            const int s = __ldcg(pf_of + tok);
+            if (s >= 0 && s < pf_n && __ldcg(pf_tok + s) == tok) src = -2 - s;
+        }
+        return make_int2(tok, src);   // -1: read over the host link
     };
     // chunk k into stage k % NS.  A chunk of resident rows only is one bulk copy (thread 0); a chunk
     // holding fetched rows is copied 16 bytes per lane with cp.async, one row per warp at a time, the
@@ -3254,7 +3479,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
                 if (lane < CR / 8) {
                     int sd = -1;
                     if (myrow < cnt && tokreg.y < 0) {
-                        atomicAdd(&s_hcnt, 1);
+                        atomicAdd(tokreg.y == -1 ? &s_hcnt : &s_pcnt, 1);
                         if (stg_of) {
                             const int s_new = atomicAdd(&V.stage_cnt[kv], 1);
                             sd = s_new < stg_cap ? s_new : -1;
@@ -3269,9 +3494,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
                     const int tok = __shfl_sync(0xffffffffu, tokreg.x, u);
                     const int sidx = __shfl_sync(0xffffffffu, tokreg.y, u);
                     if (R < r1) {
-                        const unsigned char* src = R < m_res ? res + (int64_t)R * ROWB
-                                                   : sidx >= 0 ? stg + (int64_t)sidx * ROWB
-                                                               : host + (int64_t)tok * ROWB;
+                        const unsigned char* src = R < m_res   ? res + (int64_t)R * ROWB
+                                                   : sidx >= 0  ? stg + (int64_t)sidx * ROWB
+                                                   : sidx <= -2 ? pfb + (int64_t)(-2 - sidx) * ROWB
+                                                                : host + (int64_t)tok * ROWB;
 #pragma unroll
                         for (int p = lane; p < ROWB / 16; p += 32) cp_async16(dst + row * ROWB + p * 16, src + p * 16);
                     }
@@ -3465,6 +3691,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
     // the last block of the KV head to finish merges the gridDim.y partials of its G query rows
     // (log-sum-exp over the splits); the counter is left at zero for the next call
     if (tid == 0 && s_hcnt > 0) atomicAdd(&a.hrows[unit], s_hcnt);
+    if (tid == 0 && s_pcnt > 0) atomicAdd(&a.pf_used[unit], s_pcnt);
     __shared__ int s_last;
     __shared__ float s_scl[G][kMaxSplit], s_lsp[G][kMaxSplit];
     __shared__ float s_L[G];
@@ -3618,6 +3845,29 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
             views, a, ctx.rows, ctx.wl, ctx.mark);
         VK_LAUNCHED("om_sampled");
     }
+    // beside the decision: on the multiprocessors its CTAs leave free (one CTA per SM on chip, two
+    // streaming), four prefetch blocks each, shared out over the call's (sequence, KV head) units.
+    // Calls of many rows (a streaming decision bound by L2 / HBM, few free SMs) run without it: there
+    // its reads and writes slowed the decision more than the rows it moved saved (measured at batch 8).
+    const int dec_ctas = rowsN * (stream ? Cs : C);
+    const int free_sms = std::max(0, ctx.num_sms - (stream ? (dec_ctas + 1) / 2 : dec_ctas));
+    const bool prefetch = on_chip && a.pf_cap > 0 && rowsN <= kPfMaxRows && free_sms >= 8;
+    ctx.last_pf_cap = prefetch ? a.pf_cap : 0;
+    if (prefetch) {
+        const int nb = std::max(1, std::min(16, 4 * free_sms / (B * a.Hkv)));
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(B * a.Hkv, nb);
+        lc.blockDim = dim3(kPfThreads);
+        lc.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        VK_CUDA(cudaLaunchKernelEx(&lc, prefetch_kernel<T, G>, views, a, (const RowState*)ctx.rows,
+                                   (const float2*)ctx.tl, rowsN));
+        VK_LAUNCHED("prefetch");
+    }
     static bool attn_attr = false;   // one per (T, G) instantiation
     if (!attn_attr) {
         VK_CUDA(cudaFuncSetAttribute(attn_kernel<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -3761,6 +4011,29 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     a.err = ctx.d_err;
     a.done = ctx.adone;
     a.hrows = ctx.hrows;
+    if (ctx.prefetch_rows > 0 && ctx.pf_cap != ctx.prefetch_rows) {
+        // the prefetch buffers, sized at the first decode after a change of the setting
+        if (ctx.pf_buf) VK_CUDA(cudaFree(ctx.pf_buf));
+        if (ctx.pf_tok) VK_CUDA(cudaFree(ctx.pf_tok));
+        ctx.pf_buf = nullptr;
+        ctx.pf_tok = nullptr;
+        ctx.pf_cap = 0;
+        const size_t kvb = (size_t)cfg.max_batch * cfg.n_kv_heads;
+        VK_CUDA(cudaMalloc(&ctx.pf_buf, kvb * (size_t)ctx.prefetch_rows * 2 * kHeadDim * ctx.elt));
+        VK_CUDA(cudaMalloc(&ctx.pf_tok, sizeof(int32_t) * kvb * (size_t)ctx.prefetch_rows));
+        if (!ctx.pf_of) {
+            VK_CUDA(cudaMalloc(&ctx.pf_of, sizeof(int32_t) * kvb * (size_t)ctx.ws_n));
+            VK_CUDA(cudaMemsetAsync(ctx.pf_of, 0xff, sizeof(int32_t) * kvb * (size_t)ctx.ws_n, st));
+        }
+        ctx.pf_cap = ctx.prefetch_rows;
+    }
+    a.pf_cap = ctx.prefetch_rows > 0 ? ctx.pf_cap : 0;
+    a.pf_buf = reinterpret_cast<unsigned char*>(ctx.pf_buf);
+    a.pf_of = ctx.pf_of;
+    a.pf_tok = ctx.pf_tok;
+    a.pf_cnt = ctx.pf_cnt;
+    a.pf_used = ctx.pf_used;
+    a.dprog = ctx.dprog;
     // attention splits per KV head: about two blocks per SM over the whole call
     a.nsplit = std::min(std::min(ctx.nsplit, kMaxSplit), std::max(1, (2 * ctx.num_sms + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
     a.eps = eps;

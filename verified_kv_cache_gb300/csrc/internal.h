@@ -136,6 +136,18 @@ struct Ctx {
     uint32_t* shist = nullptr;      // [max_batch][Hkv][kShortlistBins + 1] shortlist first-level histogram + count
                                     // (zero between calls)
     int64_t stage_rows = VERKV_STAGE_ETA_N;   // staging capacity per KV head and slot (verkv_set_stage_capacity)
+    // speculative prefetch (verkv_set_prefetch): while the decision runs, rows of L \ S with the
+    // largest sketch weights are copied from pinned host memory into a per-call device buffer, and
+    // the attention reads the ones it needs from there
+    int prefetch_rows = 4096;       // rows per (sequence, KV head) a decode may copy ahead (0: off)
+    int pf_cap = 0;                 // rows per (sequence, KV head) the buffers below hold
+    void* pf_buf = nullptr;         // [max_batch][Hkv][pf_cap][2][d] rows copied ahead
+    int32_t* pf_of = nullptr;       // [max_batch][Hkv][max_tokens] token -> prefetch row (valid when pf_tok agrees)
+    int32_t* pf_tok = nullptr;      // [max_batch][Hkv][pf_cap] prefetch row -> token, this call
+    int32_t* pf_cnt = nullptr;      // [max_batch][Hkv] rows claimed this call (reset by the scoring kernel)
+    int32_t* pf_used = nullptr;     // [max_batch][Hkv] prefetched rows the attention read (reset likewise)
+    unsigned long long* dprog = nullptr;  // (decode generation << 32) | query rows decided so far
+    int last_pf_cap = 0;            // pf_cap of the last decode (0: the prefetch did not run)
     int append_rows = 0;            // room reserved per KV head and slot for decode-time appended tokens
     int* h_err = nullptr;           // mapped pinned host word: a device-side bounded wait gave up
     int* d_err = nullptr;           // its device address
