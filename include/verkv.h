@@ -112,7 +112,7 @@ typedef struct {
     double eps_hat;        /* eq. (7) on the whole of L                                       */
     int32_t n_l;           /* |L|                                                             */
     int32_t kstar;         /* eq. (10); 0 when no fetch is needed                              */
-    int32_t no_fetch;      /* eps_hat < eps (Algorithm 2, line 3)                              */
+    int32_t no_fetch;      /* eps_hat < eps (Algorithm 2, the no-fetch test)                   */
     int32_t fallback;      /* k* was beyond the on-chip candidate width: full-row path used   */
     int32_t n_fetch;       /* |L_g[:k*] \ S|, tokens of this row read from the host            */
     int32_t beta_iters;    /* passes the beta solve took                                       */
@@ -139,7 +139,7 @@ verkv_status verkv_destroy(verkv_ctx* ctx);
  *   kv_dev    optional device copy with the same layout (what prefill leaves
  *             on the GPU).  NULL: compression reads kv_host over the host link.
  *   obs_q     device [n_q_heads][W][head_dim] fp32 observation queries for the
- *             synthetic importance score (Algorithm 1, line 1: per token, the
+ *             synthetic importance score (Algorithm 1, scoring step: per token, the
  *             largest softmax weight any observation query of the KV head's
  *             group gives it, divided by its maximum over tokens); or NULL.
  *   tau       device [n_kv_heads][n] fp32 importance scores supplied by the

@@ -20,7 +20,7 @@
  *   flags: 2 = H (kept with probability one), 1 = S (in L and sampled),
  *          0 = in L and not sampled.
  *   Importance scores tau are fp32 data.  Tokens of the sink/local windows
- *   are forced to tau = 1 (Algorithm 1, line 1) and lie outside the
+ *   are forced to tau = 1 (Algorithm 1, scoring step) and lie outside the
  *   water-filling; every other score is floored at 2^-38 so that every token
  *   is in H or L (the paper defines L by 0 < r_i < 1).
  */
@@ -72,7 +72,7 @@ float vko_uniform(uint64_t seed, uint32_t token, uint32_t kv_head, uint32_t laye
 }
 
 /* ------------------------------------------------------------------------ */
-/* Importance scores (Algorithm 1, line 1).  The scorer C of the paper is a  */
+/* Importance scores (Algorithm 1, scoring step).  The scorer C of the paper is a  */
 /* trained model; the synthetic stand-in is: for every observation query row */
 /* j, p_j = softmax over tokens of <Q_j, K_i>/sqrt(d); tau_i = max_j p_j(i), */
 /* divided by its maximum over i; tau = 1 on the sink and local windows.     */
@@ -113,7 +113,7 @@ void vko_tau(int64_t n, int d, const double* K, int rows, const double* Q,
 }
 
 /* ------------------------------------------------------------------------ */
-/* Water-filling (Algorithm 1, lines 2-3; eq. (3)).                          */
+/* Water-filling (Algorithm 1, water-filling step; eq. (3)).                 */
 /* I = sink/local tokens (always in H).  U = the rest, B' = budget - |I|.    */
 /* Find c with sum_{i in U} min(1, c tau_i) = B' exactly as the paper's c:   */
 /* sort U by tau descending; with the top t capped, c_t = (B' - t) / S_t,    */
@@ -207,7 +207,7 @@ int vko_waterfill(int64_t n, const float* tau_in, int n_sink, int n_local, doubl
 }
 
 /* ------------------------------------------------------------------------ */
-/* H/L split and Poisson sample (Algorithm 1, lines 3-4).                    */
+/* H/L split and Poisson sample (Algorithm 1, split and sampling steps).     */
 /* ------------------------------------------------------------------------ */
 void vko_poisson_sample(int64_t n, const float* r32, uint64_t seed, uint32_t kv_head,
                         uint32_t layer, uint32_t seq, uint8_t* flags)

@@ -100,7 +100,7 @@ def _random_tau(rng, n, kind):
 @pytest.mark.parametrize("kind", ["uniform", "heavy", "lognormal"])
 @pytest.mark.parametrize("n,eta", [(1024, 1 / 8), (4099, 1 / 16), (20000, 1 / 32), (777, 0.5)])
 def test_waterfill_inclusion_identity_and_bisection(kind, n, eta):
-    """Algorithm 1 line 2: sum_i min(1, c tau_i) = eta n (to 1e-12), and c agrees
+    """Algorithm 1, water-filling step: sum_i min(1, c tau_i) = eta n (to 1e-12), and c agrees
     with an independent plain bisection on c."""
     rng = np.random.default_rng(n)
     tau = _random_tau(rng, n, kind)
@@ -175,7 +175,7 @@ def test_u128_to_double_is_correctly_rounded():
 
 # ----------------------------------------------------------------------------- Poisson sample
 def test_poisson_sample_frequencies_match_r():
-    """Z_i ~ Bernoulli(r_i) independently (Algorithm 1 line 4): over many seeds
+    """Z_i ~ Bernoulli(r_i) independently (Algorithm 1, sampling step): over many seeds
     the empirical inclusion frequency of each token matches r_i."""
     rng = np.random.default_rng(1)
     n = 200

@@ -20,7 +20,7 @@ constexpr int kTauRows = 64;  // observation rows per chunk
 constexpr int kTauLd = kHeadDim + 1;
 
 // --------------------------------------------------------------------------------------------
-// Importance scores (Algorithm 1, line 1), synthetic scorer: for the observation rows of the KV
+// Importance scores (Algorithm 1, its scoring step), synthetic scorer: for the observation rows of the KV
 // head's query-head group, p_j(i) = softmax_i(<Q_j, K_i>/sqrt(d)); tau_i = max_j p_j(i) / max.
 // Pass 0 computes per (row, tile) the max logit and the sum of exp(logit - max); pass 1 turns the
 // per-row totals into p and keeps the max over rows for each token.
@@ -356,7 +356,7 @@ __global__ void tau_finish_kernel(float* __restrict__ tau, const float* __restri
 }
 
 // --------------------------------------------------------------------------------------------
-// Water-filling (Algorithm 1, lines 2-3; eq. (3)).  With U the tokens outside the sink/local
+// Water-filling (Algorithm 1, its water-filling step; eq. (3)).  With U the tokens outside the sink/local
 // windows and B' = eta n - |I|, the constant is c = (B' - t) / S where t tokens of U are capped
 // (c tau >= 1) and S is the exact sum of the other scores.  For a threshold theta let
 // psi(theta) = (B' - #{tau > theta}) theta - sum_{tau <= theta} tau; the capped set is
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(1024) waterfill_kernel(const float* __restrict
 }
 
 // --------------------------------------------------------------------------------------------
-// r_i = min(1, c tau_i) rounded to fp32 (H = {r = 1}); Z_i = [u_i < r_i] (Algorithm 1, lines 3-4).
+// r_i = min(1, c tau_i) rounded to fp32 (H = {r = 1}); Z_i = [u_i < r_i] (Algorithm 1, its split and sampling steps).
 // --------------------------------------------------------------------------------------------
 __global__ void sample_kernel(const float* __restrict__ tau, const double* __restrict__ c, int n, int n_sink,
                               int n_local, uint64_t seed, int layer, int seq, float* __restrict__ r_out,

@@ -1064,7 +1064,7 @@ __global__ void __launch_bounds__(256) weights_kernel(Views views, DecodeArgs a,
 // beta = sum_L w (1 - lambda(beta)) is G(beta) = beta (1 + R) - A - W = 0 with A, W, R sums over
 // those classes; Newton's step on this piecewise-linear, increasing G is beta' = (A + W)/(1 + R)
 // (exact once the classes are right), safeguarded by bisection on the bracket [lo, hi].
-// Then lambda, a_i, v_i, b_i, eq. (7) and the no-fetch test (Algorithm 2, lines 2-5).
+// Then lambda, a_i, v_i, b_i, eq. (7) and the no-fetch test (Algorithm 2, its certificate and no-fetch steps).
 // --------------------------------------------------------------------------------------------
 struct Coef {
     float a, v, b;
@@ -1530,7 +1530,7 @@ __global__ void __launch_bounds__(1024) fallback_kernel(Views views, DecodeArgs 
 //            rho = r/(1-r); D, sum w^, sum w^(1-r), sum rho.
 //   phase 1: Definition 2's fixed point by safeguarded Newton on G(beta) = beta (1 + R) - A - W,
 //            started above the root (four times the all-interior solution).
-//   phase 2: a_i, v_i, b_i; eq. (7); the no-fetch test (Algorithm 2, lines 2-5).
+//   phase 2: a_i, v_i, b_i; eq. (7); the no-fetch test (Algorithm 2, its certificate and no-fetch steps).
 //   phase 3: gain keys (eq. (9)) and k* (eq. (10)) by a search over the 48-bit keys (gain
 //            descending, L index ascending): per level, the remaining key range is split into at most
 //            2048 bins of a power-of-two width (the first level spans the cluster's own key range); a
