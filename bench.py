@@ -844,6 +844,20 @@ def stack36_run(args, dev, st, hbm_peak, peak_src, link_peak):
                     fetch.append(u / n)
                     host.append(hr)
     ctx.set_kernel_timing(False)
+    # the prefetch's rows (copied beside the decision, read by the attention) over two more steps,
+    # without per-kernel events (they would serialise the prefetch behind the decision)
+    pf_c, pf_u = [], []
+    for s in range(4, 6):
+        for l in range(layers):
+            ctx.decode(l, ids, qs[l][s], eps, delta, out, st)
+            c_, u_ = 0, 0
+            for bb in range(B):
+                for h in range(Hkv):
+                    pc, pu = ctx.prefetch_stats(bb, h)
+                    c_ += pc
+                    u_ += pu
+            pf_c.append(c_)
+            pf_u.append(u_)
     agg = kernel_agg(kt)
     calls = steps * layers
     traces = {"union_rows": statistics.mean(fetch) * n * B * Hkv, "host_rows": statistics.mean(host) * B * Hkv}
@@ -857,6 +871,8 @@ def stack36_run(args, dev, st, hbm_peak, peak_src, link_peak):
            "us_per_token_step_all_layers": job_ms / steps * 1e3,
            "scored_tokens_per_s": B * Hq * n * calls / (job_ms / 1e3),
            "fetch_fraction_per_token": statistics.mean(fetch), "host_rows_per_call": traces["host_rows"],
+           "prefetch": {"rows_copied_per_call": statistics.mean(pf_c), "rows_used_per_call": statistics.mean(pf_u),
+                        "precision": statistics.mean(pf_u) / max(1e-9, statistics.mean(pf_c))},
            "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()},
            "l2": "not flushed: per-layer working set above L2, layers called in turn"}
     res.update(layer_rooflines(agg, layer_stats, wl, traces, hbm_peak, peak_src, link_peak, B))

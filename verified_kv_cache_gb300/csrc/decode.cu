@@ -3090,17 +3090,28 @@ __global__ void __launch_bounds__(256) om_sampled_kernel(Views views, DecodeArgs
 // after it with programmatic dependent launch): per (sequence, KV head) it takes the tokens of
 // L \ S that are neither sampled nor staged, keyed by their largest sketch weight over the head's
 // query rows relative to each row's maximum, log(w^ / w^_max) = max_g (t^_g - m_g); each of its blocks
-// bins its share of them in steps of 1/16 over (-16, 0], keeps the top pf_cap / gridDim.y by those
-// bins and copies their K/V rows from pinned host memory into the call's prefetch buffer (a warp per
-// row, 16 bytes a lane), recording token -> row.  It stops claiming rows once every query row of the
-// call is decided (the decision counts its rows), and before exiting it waits for the decision to
-// complete, so that the attention, launched after it, sees both.  The attention reads a needed row
-// from this buffer instead of the host when the buffer holds it.
+// bins its share of them in steps of 1/16 over (-255/16, 0] (one read of the logits; the bins are kept
+// in shared memory when the share fits), keeps the top pf_cap / gridDim.y by those bins and copies
+// their K/V rows from pinned host memory into the call's prefetch buffer (a warp per row, 16 bytes a
+// lane), recording token -> row.  Once every query row of the call is decided (the decision counts
+// its rows) it stops: in the binning pass, before claiming rows and between the copies.  Before
+// exiting it waits for the decision to complete, so that the attention, launched after it, sees
+// both.  The attention reads a needed row from this buffer instead of the host when the buffer holds
+// it.
 // --------------------------------------------------------------------------------------------
 constexpr int kPfThreads = 256;
-constexpr int kPfBins = 256;
-constexpr int kPfListCap = 2048;   // candidates a prefetch block keeps
-constexpr int kPfMaxRows = 64;     // query rows of a call up to which the prefetch runs
+constexpr int kPfBins = 255;         // bin 255 marks an entry that is not a candidate
+constexpr int kPfListCap = 2048;     // candidates a prefetch block keeps
+constexpr int kPfMaxRows = 4096;     // query rows of a call up to which the prefetch runs
+constexpr int kPfShareCap = 32768;   // entries per block whose bins are kept in shared memory
+
+// every query row of the call decided (the decision adds one per row to the counter, tagged with
+// the call's generation)
+__device__ __forceinline__ bool decision_done(const DecodeArgs& a, int rows_in_call)
+{
+    const unsigned long long p = *reinterpret_cast<volatile unsigned long long*>(a.dprog);
+    return (unsigned)(p >> 32) == (unsigned)a.gen && (int)(p & 0xffffffffu) >= rows_in_call;
+}
 
 template <typename T, int G>
 __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, DecodeArgs a, const RowState* rows,
@@ -3110,10 +3121,14 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
     constexpr int CHUNKS = ROWB / 16;
     constexpr int U = 4;   // entries per thread in flight
     constexpr int NW = kPfThreads / 32;
+    // host rows a warp reads at a time: two keep the link busy; more outstanding host reads slowed a
+    // concurrent streaming decision by a quarter (batch 8 x 32K: 435 -> 540 us; with two, 445 us)
+    constexpr int RF = 2;
     __shared__ unsigned hist[kPfBins], off[kPfBins];
     __shared__ int lst[kPfListCap];                 // candidates (L indices), then their tokens in bin order
     __shared__ unsigned char lbin[kPfListCap];
     __shared__ int s_n, s_thr, s_base, s_stop;
+    extern __shared__ unsigned char sbin[];         // the share's bins (when it fits kPfShareCap)
     pdl_trigger();   // the attention may launch and wait at its own dependency point
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
@@ -3144,23 +3159,44 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
         }
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            bn[u] = (sl[u] < 0 && k[u] > -16.0f) ? min(kPfBins - 1, (int)(-k[u] * 16.0f)) : -1;
+            bn[u] = (sl[u] < 0 && k[u] > -(float)kPfBins / 16.0f) ? min(kPfBins - 1, (int)(-k[u] * 16.0f)) : -1;
     };
+    unsigned dyn_bytes;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+    const bool keep = j1 - j0 <= (int)dyn_bytes;   // the launch sized sbin for the largest share, or 0
     for (int i = tid; i < kPfBins; i += kPfThreads) hist[i] = 0u;
     if (tid == 0) {
         s_n = 0;
         s_stop = 0;
     }
     __syncthreads();
-    // pass 1: the histogram of the block's share
-    for (int base = j0; base < j1; base += U * kPfThreads) {
-        int bn[U];
-        bins(base, bn);
+    // pass 1: the histogram of the block's share (a warp leaves it once the decision is complete)
+    {
+        int it = 0;
+        for (int base = j0; base < j1; base += U * kPfThreads, ++it) {
+            if ((it & 3) == 3) {
+                bool dn = lane == 0 && decision_done(a, rows_in_call);
+                dn = __shfl_sync(0xffffffffu, dn, 0);
+                if (dn) {
+                    if (lane == 0) s_stop = 1;
+                    break;
+                }
+            }
+            int bn[U];
+            bins(base, bn);
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (bn[u] >= 0) atomicAdd(&hist[bn[u]], 1u);
+            for (int u = 0; u < U; ++u) {
+                if (bn[u] >= 0) atomicAdd(&hist[bn[u]], 1u);
+                const int j = base + u * kPfThreads + tid;
+                if (keep && j < j1) sbin[j - j0] = (unsigned char)(bn[u] >= 0 ? bn[u] : kPfBins);
+            }
+        }
     }
     __syncthreads();
+    if (s_stop) {
+        pdl_wait();
+        return;
+    }
     if (tid == 0) {
         // the bins holding the block's top cap_blk (staged tokens are counted here and dropped below)
         int thr = -1;
@@ -3175,18 +3211,25 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
     const int thr = s_thr;
     if (thr >= 0) {
         // pass 2: the candidates (at most cap_blk), then ordered by bin (a counting sort)
-        for (int base = j0; base < j1; base += U * kPfThreads) {
-            int bn[U];
-            bins(base, bn);
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (bn[u] >= 0 && bn[u] <= thr) {
-                    const int at = atomicAdd(&s_n, 1);
-                    if (at < cap_blk) {
-                        lst[at] = base + u * kPfThreads + tid;
-                        lbin[at] = (unsigned char)bn[u];
-                    }
+        auto take = [&](int j, int bn) {
+            if (bn <= thr) {
+                const int at = atomicAdd(&s_n, 1);
+                if (at < cap_blk) {
+                    lst[at] = j;
+                    lbin[at] = (unsigned char)bn;
                 }
+            }
+        };
+        if (keep) {
+            for (int i = tid; i < j1 - j0; i += kPfThreads) take(j0 + i, sbin[i]);
+        } else {
+            for (int base = j0; base < j1; base += U * kPfThreads) {
+                int bn[U];
+                bins(base, bn);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (bn[u] >= 0) take(base + u * kPfThreads + tid, bn[u]);
+            }
         }
         __syncthreads();
         const int n0 = min(s_n, cap_blk);
@@ -3230,36 +3273,33 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
         const unsigned char* host = reinterpret_cast<const unsigned char*>(V.kv_host) + kvn * ROWB;
         int32_t* pf_tok = a.pf_tok + (int64_t)unit * a.pf_cap;
         int32_t* pf_of = a.pf_of + (int64_t)unit * a.ws_n;
-        // copies in bin order, a warp per row and four rows in flight (lane l moves bytes 16 l .. 16 l +
+        // copies in bin order, a warp per row and two rows in flight (lane l moves bytes 16 l .. 16 l +
         // 15, and the next 512 when rows are fp32); once every query row of the call is decided the
         // remaining claimed rows are released (token -1), so the fetch no longer waits for them
         bool stop = false;
-        for (int q0 = warp * 4; q0 < n1; q0 += 4 * NW) {
-            if (!stop && lane == 0) {
-                const unsigned long long p = *reinterpret_cast<volatile unsigned long long*>(a.dprog);
-                stop = (unsigned)(p >> 32) == (unsigned)a.gen && (int)(p & 0xffffffffu) >= rows_in_call;
-            }
+        for (int q0 = warp * RF; q0 < n1; q0 += RF * NW) {
+            if (!stop && lane == 0) stop = decision_done(a, rows_in_call);
             stop = __shfl_sync(0xffffffffu, stop, 0);
-            uint4 v[4][CHUNKS / 32];
-            int tok4[4];
+            uint4 v[RF][CHUNKS / 32];
+            int tok4[RF];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < RF; ++u) {
                 const int qi = q0 + u;
                 tok4[u] = qi < n1 && base_row + qi < a.pf_cap ? lst[qi] : -1;
                 if (tok4[u] >= 0 && !stop) {
                     const uint4* src = reinterpret_cast<const uint4*>(host + (int64_t)tok4[u] * ROWB);
 #pragma unroll
-                    for (int c = 0; c < CHUNKS / 32; ++c) v[u][c] = src[lane + 32 * c];
+                    for (int c = 0; c < CHUNKS / 32; ++c) v[u][c] = __ldcs(src + lane + 32 * c);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < RF; ++u) {
                 if (tok4[u] < 0) continue;
                 const int sr = base_row + q0 + u;
                 if (!stop) {
                     uint4* dst = reinterpret_cast<uint4*>(buf + (int64_t)sr * ROWB);
 #pragma unroll
-                    for (int c = 0; c < CHUNKS / 32; ++c) dst[lane + 32 * c] = v[u][c];
+                    for (int c = 0; c < CHUNKS / 32; ++c) __stcs(dst + lane + 32 * c, v[u][c]);
                 }
                 if (lane == 0) {
                     pf_tok[sr] = stop ? -1 : tok4[u];
@@ -3846,18 +3886,20 @@ verkv_status launch_decode(Ctx& ctx, const Views& views, const DecodeArgs& a, in
         VK_LAUNCHED("om_sampled");
     }
     // beside the decision: on the multiprocessors its CTAs leave free (one CTA per SM on chip, two
-    // streaming), four prefetch blocks each, shared out over the call's (sequence, KV head) units.
-    // Calls of many rows (a streaming decision bound by L2 / HBM, few free SMs) run without it: there
-    // its reads and writes slowed the decision more than the rows it moved saved (measured at batch 8).
+    // streaming), four prefetch blocks each, shared out over the call's (sequence, KV head) units (at
+    // least one per unit).  Calls whose decision leaves fewer than eight multiprocessors free run
+    // without it.
     const int dec_ctas = rowsN * (stream ? Cs : C);
     const int free_sms = std::max(0, ctx.num_sms - (stream ? (dec_ctas + 1) / 2 : dec_ctas));
     const bool prefetch = on_chip && a.pf_cap > 0 && rowsN <= kPfMaxRows && free_sms >= 8;
     ctx.last_pf_cap = prefetch ? a.pf_cap : 0;
     if (prefetch) {
         const int nb = std::max(1, std::min(16, 4 * free_sms / (B * a.Hkv)));
+        const int share = (max_nl + nb - 1) / nb;
         cudaLaunchConfig_t lc = {};
         lc.gridDim = dim3(B * a.Hkv, nb);
         lc.blockDim = dim3(kPfThreads);
+        lc.dynamicSmemBytes = share <= kPfShareCap ? (size_t)((share + 15) & ~15) : 0;
         lc.stream = st;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
