@@ -3086,10 +3086,10 @@ __global__ void __launch_bounds__(256) om_sampled_kernel(Views views, DecodeArgs
 // --------------------------------------------------------------------------------------------
 // Speculative prefetch (no counterpart in the algorithms; results are identical with it on or off).
 // The host link idles while the decision runs, and the rows a decode ends up fetching are mostly the
-// tokens of L \ S with the largest sketch weights.  This kernel runs beside the decision (launched
+// tokens of L \ S with the largest alpha = w^ (1 - r).  This kernel runs beside the decision (launched
 // after it with programmatic dependent launch): per (sequence, KV head) it takes the tokens of
-// L \ S that are neither sampled nor staged, keyed by their largest sketch weight over the head's
-// query rows relative to each row's maximum, log(w^ / w^_max) = max_g (t^_g - m_g); each of its blocks
+// L \ S that are neither sampled nor staged, keyed by their largest alpha over the head's query rows
+// relative to each row's largest weight, log(alpha / w^_max) = max_g (t^_g - m_g) + log(1 - r); each of its blocks
 // bins its share of them in steps of 1/16 over (-255/16, 0] (one read of the logits; the bins are kept
 // in shared memory when the share fits), keeps the top pf_cap / gridDim.y by those bins and copies
 // their K/V rows from pinned host memory into the call's prefetch buffer (a warp per row, 16 bytes a
@@ -3147,19 +3147,22 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
     // of the group is issued before any is used
     auto bins = [&](int base, int (&bn)[U]) {
         int sl[U];
-        float k[U];
+        float k[U], r[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int j = base + u * kPfThreads + tid;
             sl[u] = j < j1 ? __ldg(V.lslot + kvn + j) : 0;
+            r[u] = j < j1 ? __ldg(V.rl + kvn + j) : 0.f;
             k[u] = -INFINITY;
 #pragma unroll
             for (int g = 0; g < G; ++g)
                 if (j < j1) k[u] = fmaxf(k[u], __ldcg(tl + (int64_t)(row0 + g) * a.ws_n + j).x - m[g]);
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            bn[u] = (sl[u] < 0 && k[u] > -(float)kPfBins / 16.0f) ? min(kPfBins - 1, (int)(-k[u] * 16.0f)) : -1;
+        for (int u = 0; u < U; ++u) {
+            const float kk = k[u] + __logf(1.0f - r[u]);   // log of alpha = w^ (1 - r) over the row's largest w^
+            bn[u] = (sl[u] < 0 && kk > -(float)kPfBins / 16.0f) ? min(kPfBins - 1, (int)(-kk * 16.0f)) : -1;
+        }
     };
     unsigned dyn_bytes;
     asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
@@ -3197,15 +3200,32 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
         pdl_wait();
         return;
     }
-    if (tid == 0) {
-        // the bins holding the block's top cap_blk (staged tokens are counted here and dropped below)
-        int thr = -1;
-        unsigned cum = 0u;
-        for (int i = 0; i < kPfBins && cum < (unsigned)cap_blk; ++i) {
-            cum += hist[i];
-            thr = i;
+    if (warp == 0) {
+        // the bins holding the block's top cap_blk (staged tokens are counted here and dropped below):
+        // up to the first bin at which the running count reaches cap_blk, else all of them
+        unsigned c[8], tot = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = 8 * lane + j < kPfBins ? hist[8 * lane + j] : 0u;
+            tot += c[j];
         }
-        s_thr = thr;
+        unsigned inc = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        int thr = -1;
+        if (inc >= (unsigned)cap_blk && inc - tot < (unsigned)cap_blk) {
+            unsigned cum = inc - tot;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                cum += c[j];
+                if (thr < 0 && cum >= (unsigned)cap_blk) thr = 8 * lane + j;
+            }
+        }
+        thr = __reduce_max_sync(0xffffffffu, thr);
+        if (lane == 0) s_thr = thr >= 0 ? thr : kPfBins - 1;
     }
     __syncthreads();
     const int thr = s_thr;
@@ -3243,13 +3263,27 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
         for (int i = tid; i < n0; i += kPfThreads)
             if (lst[i] >= 0) atomicAdd(&hist[lbin[i]], 1u);
         __syncthreads();
-        if (tid == 0) {
-            unsigned c = 0u;
-            for (int i = 0; i < kPfBins; ++i) {
-                off[i] = c;
-                c += hist[i];
+        if (warp == 0) {
+            // exclusive prefix of the kept counts over the bins (lane l: bins 8 l .. 8 l + 7)
+            unsigned c[8], tot = 0u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = 8 * lane + j < kPfBins ? hist[8 * lane + j] : 0u;
+                tot += c[j];
             }
-            s_n = (int)c;   // the kept candidates
+            unsigned inc = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            unsigned run = inc - tot;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (8 * lane + j < kPfBins) off[8 * lane + j] = run;
+                run += c[j];
+            }
+            if (lane == 31) s_n = (int)inc;   // the kept candidates
         }
         __syncthreads();
         // the kept tokens in bin order (a counting sort through registers)
