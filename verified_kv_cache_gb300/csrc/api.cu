@@ -33,7 +33,7 @@ void free_ws(Ctx& c)
 {
     void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.adone, c.ucount,
                     c.part, c.hrows, c.slist, c.scount, c.shist,
-                    c.d_slot_n, c.pf_buf, c.pf_of, c.pf_tok, c.pf_cnt, c.pf_used, c.dprog};
+                    c.d_slot_n, c.pf_buf, c.pf_of, c.pf_tok, c.pf_cnt, c.pf_used, c.dprog, c.tau_ws};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     if (c.h_err) cudaFreeHost(c.h_err);

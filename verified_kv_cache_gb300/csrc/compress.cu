@@ -382,18 +382,25 @@ struct WfPass {
 
 __device__ WfPass wf_pass(const float* __restrict__ t, int n, int n_sink, int n_local, uint32_t u, void* sm_raw)
 {
+    // the warps' partials, then the block's totals (sm_raw: 32 x 24 bytes + 24)
+    struct Part {
+        unsigned long long lo, hi;
+        int cnt;
+        unsigned int mx;
+    };
     struct Sm {
         unsigned long long lo, hi;
         int cnt;
         unsigned int max_le, min_gt;
     };
-    Sm* sm = reinterpret_cast<Sm*>(sm_raw);
-    __syncthreads();
-    if (threadIdx.x == 0) { sm->lo = 0; sm->hi = 0; sm->cnt = 0; sm->max_le = 0; sm->min_gt = 0xffffffffu; }
-    __syncthreads();
+    Part* wp = reinterpret_cast<Part*>(sm_raw);
+    unsigned int* wmn = reinterpret_cast<unsigned int*>(wp + 32);
+    Sm* sm = reinterpret_cast<Sm*>(wmn + 32);
+    __syncthreads();   // the previous pass has read its totals
     unsigned long long lo = 0, hi = 0;
     int cnt = 0;
     uint32_t mx = 0, mn = 0xffffffffu;
+#pragma unroll 8
     for (int i = n_sink + threadIdx.x; i < n - n_local; i += blockDim.x) {
         const uint32_t b = __float_as_uint(t[i]);
         if (b > u) { ++cnt; mn = min(mn, b); }
@@ -411,12 +418,31 @@ __device__ WfPass wf_pass(const float* __restrict__ t, int n, int n_sink, int n_
         mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     }
-    if ((threadIdx.x & 31) == 0) {
-        atomicAdd(&sm->lo, lo);
-        atomicAdd(&sm->hi, hi);
-        atomicAdd(&sm->cnt, cnt);
-        atomicMax(&sm->max_le, mx);
-        atomicMin(&sm->min_gt, mn);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (lane == 0) {
+        wp[warp] = Part{lo, hi, cnt, mx};
+        wmn[warp] = mn;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // integer sums and extremes: the same totals in any order
+        unsigned long long l2 = lane < nw ? wp[lane].lo : 0ull, h2 = lane < nw ? wp[lane].hi : 0ull;
+        int c2 = lane < nw ? wp[lane].cnt : 0;
+        unsigned int x2 = lane < nw ? wp[lane].mx : 0u, n2 = lane < nw ? wmn[lane] : 0xffffffffu;
+        l2 = warp_sum(l2);
+        h2 = warp_sum(h2);
+        c2 = warp_sum(c2);
+        for (int o = 16; o > 0; o >>= 1) {
+            x2 = max(x2, __shfl_xor_sync(0xffffffffu, x2, o));
+            n2 = min(n2, __shfl_xor_sync(0xffffffffu, n2, o));
+        }
+        if (lane == 0) {
+            sm->lo = l2;
+            sm->hi = h2;
+            sm->cnt = c2;
+            sm->max_le = x2;
+            sm->min_gt = n2;
+        }
     }
     __syncthreads();
     WfPass r;
@@ -431,13 +457,24 @@ __device__ WfPass wf_pass(const float* __restrict__ t, int n, int n_sink, int n_
     return r;
 }
 
+constexpr int kWaterfillSmem = 200 * 1024;   // scores of a head kept on chip up to 51200 tokens
+
 __global__ void __launch_bounds__(1024) waterfill_kernel(const float* __restrict__ tau, int n, int n_sink,
                                                          int n_local, double budget, double* __restrict__ c_out,
                                                          int* __restrict__ capped_out, int* __restrict__ neartie)
 {
-    __shared__ __align__(16) unsigned char sm[64];
+    __shared__ __align__(16) unsigned char sm[32 * 24 + 32 * 4 + 32];
+    extern __shared__ __align__(16) float wf_tau[];   // the head's scores, when the launch gave room for them
     const int h = blockIdx.x;
     const float* t = tau + (int64_t)h * n;
+    unsigned dyn_bytes;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+    if ((size_t)n * sizeof(float) <= dyn_bytes) {
+        // every bisection step reads all the scores: read them from HBM once
+        for (int i = threadIdx.x; i < n; i += blockDim.x) wf_tau[i] = t[i];
+        __syncthreads();
+        t = wf_tau;
+    }
     const int nf = n_sink + n_local;
     const double bprime = budget - (double)nf;
     const int nu = n - nf;
@@ -603,19 +640,24 @@ __global__ void sketch_int8_kernel(const T* __restrict__ kv, int n, int n_kv, in
     if (lane == 0) scale[tok] = s;
 }
 
-// 2-bit sketch, step 1: energy of each rotate-half pair (p, p + d/2), summed in double.
+// 2-bit sketch, step 1: energy of each rotate-half pair (p, p + d/2), summed in float-float per
+// block of tokens and in double across the blocks.
 template <typename T>
 __global__ void pair_energy_kernel(const T* __restrict__ kv, int n, int tokens_per_block, double* __restrict__ energy)
 {
     const int h = blockIdx.y, c = threadIdx.x;  // blockDim.x == kHeadDim
     const int i0 = blockIdx.x * tokens_per_block;
     const int i1 = min(n, i0 + tokens_per_block);
-    double e = 0.0;
+    // float-float accumulation (fp64 arithmetic is slow on this part): x^2 is rounded to fp32 once
+    // (exact for bf16 keys) and the running sum carries its rounding error, about 2^-44 relative
+    ff e = {0.f, 0.f};
+#pragma unroll 8
     for (int i = i0; i < i1; ++i) {
-        const double x = (double)Elt<T>::load(kv, ((int64_t)h * n + i) * 2 * kHeadDim + c);
-        e += x * x;
+        const float x = Elt<T>::load(kv, ((int64_t)h * n + i) * 2 * kHeadDim + c);
+        const ff t = two_sum(e.hi, __fmul_rn(x, x));
+        e = fast_two_sum(t.hi, __fadd_rn(e.lo, t.lo));
     }
-    atomicAdd(&energy[h * (kHeadDim / 2) + (c % (kHeadDim / 2))], e);
+    atomicAdd(&energy[h * (kHeadDim / 2) + (c % (kHeadDim / 2))], (double)e.hi + (double)e.lo);
 }
 
 // Step 2: the d/8 pairs of largest energy (ties: lower pair index), ascending.
@@ -650,28 +692,48 @@ __device__ __forceinline__ uint64_t spread_bits(uint32_t x)
 }
 
 // Step 3: per (group of `group` tokens, kept channel) zero = fp16(min), scale = fp16((max-min)/3),
-// code = rint((k - zero) / scale) clamped to [0, 3].  One warp per group, lane = kept channel.
+// code = rint((k - zero) / scale) clamped to [0, 3].  One block of kSk2Warps warps per group: warp w
+// takes every kSk2Warps-th token of the group, lane = kept channel; the warps' minima and maxima are
+// combined in shared memory (min and max are exact, so every warp obtains the same zero and scale).
+constexpr int kSk2Warps = 4;
 template <typename T>
-__global__ void sketch_2bit_kernel(const T* __restrict__ kv, int n, int group, const int32_t* __restrict__ pairs,
-                                   uint64_t* __restrict__ codes, __half* __restrict__ zero, __half* __restrict__ scl)
+__global__ void __launch_bounds__(32 * kSk2Warps) sketch_2bit_kernel(const T* __restrict__ kv, int n, int group,
+                                                                     const int32_t* __restrict__ pairs,
+                                                                     uint64_t* __restrict__ codes,
+                                                                     __half* __restrict__ zero,
+                                                                     __half* __restrict__ scl)
 {
     constexpr int NP = kHeadDim / 8, KEPT = kHeadDim / 4;
-    const int h = blockIdx.y, g = blockIdx.x, lane = threadIdx.x;  // blockDim.x == 32 == KEPT
+    static_assert(KEPT == 32, "a lane per kept channel");
+    __shared__ float smn[kSk2Warps][KEPT], smx[kSk2Warps][KEPT];
+    const int h = blockIdx.y, g = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ch = lane < NP ? pairs[h * NP + lane] : pairs[h * NP + lane - NP] + kHeadDim / 2;
     const int i0 = g * group, i1 = min(n, i0 + group);
     float mn = INFINITY, mx = -INFINITY;
-    for (int i = i0; i < i1; ++i) {
+#pragma unroll 8
+    for (int i = i0 + warp; i < i1; i += kSk2Warps) {
         const float v = Elt<T>::load(kv, ((int64_t)h * n + i) * 2 * kHeadDim + ch);
         mn = fminf(mn, v);
         mx = fmaxf(mx, v);
     }
+    smn[warp][lane] = mn;
+    smx[warp][lane] = mx;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kSk2Warps; ++w) {
+        mn = fminf(mn, smn[w][lane]);
+        mx = fmaxf(mx, smx[w][lane]);
+    }
     const __half zh = __float2half_rn(mn);
     const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
     const int ngroups = (n + group - 1) / group;
-    zero[((int64_t)h * ngroups + g) * KEPT + lane] = zh;
-    scl[((int64_t)h * ngroups + g) * KEPT + lane] = sh;
+    if (warp == 0) {
+        zero[((int64_t)h * ngroups + g) * KEPT + lane] = zh;
+        scl[((int64_t)h * ngroups + g) * KEPT + lane] = sh;
+    }
     const float zf = __half2float(zh), sf = __half2float(sh);
-    for (int i = i0; i < i1; ++i) {
+#pragma unroll 8
+    for (int i = i0 + warp; i < i1; i += kSk2Warps) {
         const float v = Elt<T>::load(kv, ((int64_t)h * n + i) * 2 * kHeadDim + ch);
         int code = 0;
         if (sf > 0.f) {
@@ -709,13 +771,24 @@ verkv_status run_scores(Ctx& ctx, Slot& s, const T* kv, int n, const float* obs_
     }
     const int R = ctx.G * W;
     const int ntiles = (n + kTauTok - 1) / kTauTok;
-    float2 *part = nullptr, *rowstat = nullptr;
-    float* tau_raw = nullptr;
-    int* tau_max = nullptr;
-    VK_CUDA(cudaMallocAsync(&part, sizeof(float2) * (size_t)Hkv * R * ntiles, st));
-    VK_CUDA(cudaMallocAsync(&rowstat, sizeof(float2) * (size_t)Hkv * R, st));
-    VK_CUDA(cudaMallocAsync(&tau_raw, sizeof(float) * (size_t)Hkv * n, st));
-    VK_CUDA(cudaMallocAsync(&tau_max, sizeof(int) * Hkv, st));
+    // scratch kept by the context (grown when a call needs more; the stream is idle here, the compress
+    // having synchronised it on entry): per-tile partials, row statistics, raw scores, head maxima
+    auto up = [](size_t b) { return (b + 255) & ~(size_t)255; };
+    const size_t b_part = up(sizeof(float2) * (size_t)Hkv * R * ntiles), b_row = up(sizeof(float2) * (size_t)Hkv * R),
+                 b_raw = up(sizeof(float) * (size_t)Hkv * n), b_max = up(sizeof(int) * Hkv);
+    const size_t need = b_part + b_row + b_raw + b_max;
+    if (need > ctx.tau_ws_cap) {
+        if (ctx.tau_ws) VK_CUDA(cudaFree(ctx.tau_ws));
+        ctx.tau_ws = nullptr;
+        ctx.tau_ws_cap = 0;
+        VK_CUDA(cudaMalloc(&ctx.tau_ws, need));
+        ctx.tau_ws_cap = need;
+    }
+    unsigned char* ws = static_cast<unsigned char*>(ctx.tau_ws);
+    float2* part = reinterpret_cast<float2*>(ws);
+    float2* rowstat = reinterpret_cast<float2*>(ws + b_part);
+    float* tau_raw = reinterpret_cast<float*>(ws + b_part + b_row);
+    int* tau_max = reinterpret_cast<int*>(ws + b_part + b_row + b_raw);
     VK_CUDA(cudaMemsetAsync(tau_max, 0x80, sizeof(int) * Hkv, st));  // ordered(-huge)
     const size_t smem = sizeof(float) * ((size_t)kTauTok * kTauLd + (size_t)kTauRows * kTauLd +
                                          (size_t)kTauRows * (kTauTok + 1) + kTauTok);
@@ -758,10 +831,6 @@ verkv_status run_scores(Ctx& ctx, Slot& s, const T* kv, int n, const float* obs_
     }
     tau_finish_kernel<<<g1, 256, 0, st>>>(s.tau, tau_raw, tau_max, n, cfg.n_sink, cfg.n_local);
     VK_LAUNCHED("tau_finish");
-    VK_CUDA(cudaFreeAsync(part, st));
-    VK_CUDA(cudaFreeAsync(rowstat, st));
-    VK_CUDA(cudaFreeAsync(tau_raw, st));
-    VK_CUDA(cudaFreeAsync(tau_max, st));
     return VERKV_OK;
 }
 
@@ -782,8 +851,8 @@ verkv_status run_sketch(Ctx& ctx, Slot& s, const T* kv, int n, cudaStream_t st)
         select_pairs_kernel<<<Hkv, kHeadDim / 2, 0, st>>>(s.energy, s.pairs);
         VK_LAUNCHED("select_pairs");
         const int ngroups = (n + cfg.sketch_group - 1) / cfg.sketch_group;
-        sketch_2bit_kernel<T><<<dim3(ngroups, Hkv), 32, 0, st>>>(kv, n, cfg.sketch_group, s.pairs, s.codes2, s.zero2,
-                                                                s.scale2);
+        sketch_2bit_kernel<T><<<dim3(ngroups, Hkv), 32 * kSk2Warps, 0, st>>>(kv, n, cfg.sketch_group, s.pairs,
+                                                                             s.codes2, s.zero2, s.scale2);
         VK_LAUNCHED("sketch_2bit");
     } else {
         const int64_t rows = (int64_t)Hkv * n;
@@ -899,8 +968,14 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
     if (rc != VERKV_OK) return rc;
 
     VK_CUDA(cudaMemsetAsync(s.capped + Hkv, 0, sizeof(int32_t), st));
-    waterfill_kernel<<<Hkv, 1024, 0, st>>>(s.tau, n, cfg.n_sink, cfg.n_local, cfg.eta * (double)n, s.c, s.capped,
-                                          s.capped + Hkv);
+    static bool wf_attr = false;
+    if (!wf_attr) {
+        VK_CUDA(cudaFuncSetAttribute(waterfill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWaterfillSmem));
+        wf_attr = true;
+    }
+    const size_t wf_smem = (size_t)n * sizeof(float) <= (size_t)kWaterfillSmem ? (size_t)n * sizeof(float) : 0;
+    waterfill_kernel<<<Hkv, 1024, wf_smem, st>>>(s.tau, n, cfg.n_sink, cfg.n_local, cfg.eta * (double)n, s.c,
+                                                 s.capped, s.capped + Hkv);
     VK_LAUNCHED("waterfill");
     sample_kernel<<<dim3((n + 255) / 256, Hkv), 256, 0, st>>>(s.tau, s.c, n, cfg.n_sink, cfg.n_local, cfg.seed, layer,
                                                             seq, s.r, s.flags);

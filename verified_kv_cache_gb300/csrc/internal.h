@@ -141,6 +141,8 @@ struct Ctx {
     // the attention reads the ones it needs from there
     int prefetch_rows = 4096;       // rows per (sequence, KV head) a decode may copy ahead (0: off)
     int pf_cap = 0;                 // rows per (sequence, KV head) the buffers below hold
+    void* tau_ws = nullptr;         // compress: importance-score scratch (partials, row stats, raw scores)
+    size_t tau_ws_cap = 0;
     void* pf_buf = nullptr;         // [max_batch][Hkv][pf_cap][2][d] rows copied ahead
     int32_t* pf_of = nullptr;       // [max_batch][Hkv][max_tokens] token -> prefetch row (valid when pf_tok agrees)
     int32_t* pf_tok = nullptr;      // [max_batch][Hkv][pf_cap] prefetch row -> token, this call
