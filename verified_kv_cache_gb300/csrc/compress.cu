@@ -6,10 +6,14 @@
 #include <cmath>
 #include <cstring>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "async.cuh"
 #include "umma.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace verkv {
 
@@ -378,30 +382,27 @@ struct WfPass {
     double s_le;
     uint32_t max_le;  // largest bit pattern <= u (0 if none)
     uint32_t min_gt;  // smallest bit pattern > u (0xffffffff if none)
+    bool below;       // psi(u) < 0: (B' - cnt_gt) u < s_le
 };
 
-__device__ WfPass wf_pass(const float* __restrict__ t, int n, int n_sink, int n_local, uint32_t u, void* sm_raw)
+// One bisection step, evaluated by the C CTAs of a head's cluster over their slices [i0, i1) of U:
+// per CTA the warps' partials and the CTA's totals (in `tot[par]`, double-buffered by step parity),
+// then every CTA combines all C totals through distributed shared memory.  The sums and extremes are
+// integers, so every CTA obtains the same totals and takes the same bisection branch.
+struct WfTot {
+    unsigned long long lo, hi;
+    int cnt;
+    unsigned int max_le, min_gt, pad;
+};
+
+__device__ WfPass wf_pass(cg::cluster_group& cl, const float* __restrict__ t, int i0, int i1, uint32_t u,
+                          double bprime, WfTot* wp, WfTot* tot, int par, WfPass* res)
 {
-    // the warps' partials, then the block's totals (sm_raw: 32 x 24 bytes + 24)
-    struct Part {
-        unsigned long long lo, hi;
-        int cnt;
-        unsigned int mx;
-    };
-    struct Sm {
-        unsigned long long lo, hi;
-        int cnt;
-        unsigned int max_le, min_gt;
-    };
-    Part* wp = reinterpret_cast<Part*>(sm_raw);
-    unsigned int* wmn = reinterpret_cast<unsigned int*>(wp + 32);
-    Sm* sm = reinterpret_cast<Sm*>(wmn + 32);
-    __syncthreads();   // the previous pass has read its totals
     unsigned long long lo = 0, hi = 0;
     int cnt = 0;
     uint32_t mx = 0, mn = 0xffffffffu;
 #pragma unroll 8
-    for (int i = n_sink + threadIdx.x; i < n - n_local; i += blockDim.x) {
+    for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
         const uint32_t b = __float_as_uint(t[i]);
         if (b > u) { ++cnt; mn = min(mn, b); }
         else {
@@ -419,16 +420,12 @@ __device__ WfPass wf_pass(const float* __restrict__ t, int n, int n_sink, int n_
         mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if (lane == 0) {
-        wp[warp] = Part{lo, hi, cnt, mx};
-        wmn[warp] = mn;
-    }
+    if (lane == 0) wp[warp] = WfTot{lo, hi, cnt, mx, mn, 0u};
     __syncthreads();
     if (warp == 0) {
-        // integer sums and extremes: the same totals in any order
         unsigned long long l2 = lane < nw ? wp[lane].lo : 0ull, h2 = lane < nw ? wp[lane].hi : 0ull;
         int c2 = lane < nw ? wp[lane].cnt : 0;
-        unsigned int x2 = lane < nw ? wp[lane].mx : 0u, n2 = lane < nw ? wmn[lane] : 0xffffffffu;
+        unsigned int x2 = lane < nw ? wp[lane].max_le : 0u, n2 = lane < nw ? wp[lane].min_gt : 0xffffffffu;
         l2 = warp_sum(l2);
         h2 = warp_sum(h2);
         c2 = warp_sum(c2);
@@ -436,56 +433,79 @@ __device__ WfPass wf_pass(const float* __restrict__ t, int n, int n_sink, int n_
             x2 = max(x2, __shfl_xor_sync(0xffffffffu, x2, o));
             n2 = min(n2, __shfl_xor_sync(0xffffffffu, n2, o));
         }
-        if (lane == 0) {
-            sm->lo = l2;
-            sm->hi = h2;
-            sm->cnt = c2;
-            sm->max_le = x2;
-            sm->min_gt = n2;
+        if (lane == 0) tot[par] = WfTot{l2, h2, c2, x2, n2, 0u};
+    }
+    cl.sync();   // every CTA's totals of this step are in place (and the previous step's were read)
+    // one thread combines them and does the double-precision part (fp64 is slow on this part), the
+    // block reads the result
+    if (threadIdx.x == 0) {
+        unsigned long long L = 0, Hh = 0;
+        int C = 0;
+        uint32_t MX = 0, MN = 0xffffffffu;
+        for (int q = 0; q < (int)cl.num_blocks(); ++q) {
+            const WfTot x = cl.map_shared_rank(tot, q)[par];
+            L += x.lo;
+            Hh += x.hi;
+            C += x.cnt;
+            MX = max(MX, x.max_le);
+            MN = min(MN, x.min_gt);
         }
+        WfPass r;
+        r.cnt_gt = C;
+        const uint64_t low64 = (Hh << 32) + L;
+        const uint64_t carry = low64 < L ? 1 : 0;
+        const uint64_t high64 = (Hh >> 32) + carry;
+        r.s_le = ldexp(u128_to_double_rn(high64, low64), -61);
+        r.max_le = MX;
+        r.min_gt = MN;
+        r.below = (bprime - (double)C) * (double)__uint_as_float(u) < r.s_le;
+        *res = r;
     }
     __syncthreads();
-    WfPass r;
-    r.cnt_gt = sm->cnt;
-    const unsigned long long L = sm->lo, Hh = sm->hi;
-    const uint64_t low64 = (Hh << 32) + L;
-    const uint64_t carry = low64 < L ? 1 : 0;
-    const uint64_t high64 = (Hh >> 32) + carry;
-    r.s_le = ldexp(u128_to_double_rn(high64, low64), -61);
-    r.max_le = sm->max_le;
-    r.min_gt = sm->min_gt;
-    return r;
+    return *res;
 }
 
-constexpr int kWaterfillSmem = 200 * 1024;   // scores of a head kept on chip up to 51200 tokens
+constexpr int kWfCluster = 8;                 // CTAs per head
+constexpr int kWaterfillSmem = 200 * 1024;    // a CTA's slice of the scores kept on chip up to 51200 tokens
 
 __global__ void __launch_bounds__(1024) waterfill_kernel(const float* __restrict__ tau, int n, int n_sink,
                                                          int n_local, double budget, double* __restrict__ c_out,
                                                          int* __restrict__ capped_out, int* __restrict__ neartie)
 {
-    __shared__ __align__(16) unsigned char sm[32 * 24 + 32 * 4 + 32];
-    extern __shared__ __align__(16) float wf_tau[];   // the head's scores, when the launch gave room for them
-    const int h = blockIdx.x;
+    __shared__ WfTot wp[32], tot[2];
+    __shared__ WfPass res;
+    extern __shared__ __align__(16) float wf_tau[];   // this CTA's slice of the scores, when the launch gave room
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank(), C = (int)cl.num_blocks();
+    const int h = blockIdx.y;
     const float* t = tau + (int64_t)h * n;
-    unsigned dyn_bytes;
-    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
-    if ((size_t)n * sizeof(float) <= dyn_bytes) {
-        // every bisection step reads all the scores: read them from HBM once
-        for (int i = threadIdx.x; i < n; i += blockDim.x) wf_tau[i] = t[i];
-        __syncthreads();
-        t = wf_tau;
-    }
     const int nf = n_sink + n_local;
     const double bprime = budget - (double)nf;
     const int nu = n - nf;
-    if (bprime >= (double)nu) {
-        if (threadIdx.x == 0) { c_out[h] = INFINITY; capped_out[h] = nu; }
+    if (bprime >= (double)nu) {   // the same in every CTA of the cluster: none of them synchronises
+        if (rank == 0 && threadIdx.x == 0) { c_out[h] = INFINITY; capped_out[h] = nu; }
         return;
     }
-    auto pred = [&](uint32_t u) -> bool {
-        WfPass p = wf_pass(t, n, n_sink, n_local, u, sm);
-        return (bprime - (double)p.cnt_gt) * (double)__uint_as_float(u) < p.s_le;
+    // this CTA's slice of U
+    const int per = (nu + C - 1) / C;
+    int i0 = n_sink + min(nu, rank * per), i1 = n_sink + min(nu, (rank + 1) * per);
+    unsigned dyn_bytes;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+    if ((size_t)(i1 - i0) * sizeof(float) <= dyn_bytes) {
+        // every bisection step reads the whole slice: read it from HBM once
+        for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) wf_tau[i - i0] = t[i];
+        __syncthreads();
+        t = wf_tau;
+        i1 -= i0;
+        i0 = 0;
+    }
+    int par = 0;
+    auto pass = [&](uint32_t u) {
+        const WfPass p = wf_pass(cl, t, i0, i1, u, bprime, wp, tot, par, &res);
+        par ^= 1;
+        return p;
     };
+    auto pred = [&](uint32_t u) -> bool { return pass(u).below; };
     uint32_t lo = 1u, hi = 0x3f800000u;
     uint32_t ustar;
     if (pred(hi)) ustar = hi;
@@ -496,17 +516,16 @@ __global__ void __launch_bounds__(1024) waterfill_kernel(const float* __restrict
         }
         ustar = lo;
     }
-    WfPass p = wf_pass(t, n, n_sink, n_local, ustar, sm);
-    const double c = (bprime - (double)p.cnt_gt) / p.s_le;
+    const WfPass p = pass(ustar);
     // The same decision at the data values themselves (the form of the rule that walks the
     // sorted scores): the capped/uncapped boundary must be accepted at max_le and rejected at min_gt.
-    int tie = 0;
-    if (p.max_le != 0 && !((bprime - (double)p.cnt_gt) * (double)__uint_as_float(p.max_le) < p.s_le)) tie = 1;
-    if (p.min_gt != 0xffffffffu) {
-        WfPass q = wf_pass(t, n, n_sink, n_local, p.min_gt, sm);
-        if ((bprime - (double)q.cnt_gt) * (double)__uint_as_float(p.min_gt) < q.s_le) tie = 1;
-    }
-    if (threadIdx.x == 0) {
+    bool tie_hi = false;
+    if (p.min_gt != 0xffffffffu) tie_hi = pass(p.min_gt).below;
+    cl.sync();   // no CTA leaves while another may still read its totals
+    if (rank == 0 && threadIdx.x == 0) {
+        const double c = (bprime - (double)p.cnt_gt) / p.s_le;
+        int tie = tie_hi ? 1 : 0;
+        if (p.max_le != 0 && !((bprime - (double)p.cnt_gt) * (double)__uint_as_float(p.max_le) < p.s_le)) tie = 1;
         c_out[h] = c;
         capped_out[h] = p.cnt_gt;
         if (tie) atomicAdd(neartie, 1);
@@ -973,9 +992,24 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
         VK_CUDA(cudaFuncSetAttribute(waterfill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWaterfillSmem));
         wf_attr = true;
     }
-    const size_t wf_smem = (size_t)n * sizeof(float) <= (size_t)kWaterfillSmem ? (size_t)n * sizeof(float) : 0;
-    waterfill_kernel<<<Hkv, 1024, wf_smem, st>>>(s.tau, n, cfg.n_sink, cfg.n_local, cfg.eta * (double)n, s.c,
-                                                 s.capped, s.capped + Hkv);
+    {
+        // one cluster of kWfCluster CTAs per KV head, each over a slice of the scores
+        const size_t slice = (size_t)((n + kWfCluster - 1) / kWfCluster) * sizeof(float);
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(kWfCluster, Hkv);
+        lc.blockDim = dim3(1024);
+        lc.dynamicSmemBytes = slice <= (size_t)kWaterfillSmem ? slice : 0;
+        lc.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kWfCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        VK_CUDA(cudaLaunchKernelEx(&lc, waterfill_kernel, (const float*)s.tau, n, cfg.n_sink, cfg.n_local,
+                                   cfg.eta * (double)n, s.c, s.capped, s.capped + Hkv));
+    }
     VK_LAUNCHED("waterfill");
     sample_kernel<<<dim3((n + 255) / 256, Hkv), 256, 0, st>>>(s.tau, s.c, n, cfg.n_sink, cfg.n_local, cfg.seed, layer,
                                                             seq, s.r, s.flags);
