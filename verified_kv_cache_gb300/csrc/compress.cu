@@ -557,7 +557,11 @@ __global__ void sample_kernel(const float* __restrict__ tau, const double* __res
 }
 
 // Ordered compaction of one KV head: L list (with r in L order), resident list (H u S), H list.
-// lpos[token] is the L index for tokens of L and -(H index) - 1 for tokens of H.
+// lpos[token] is the L index for tokens of L and -(H index) - 1 for tokens of H.  A cluster of
+// kCompactCluster CTAs per head: each counts the four classes over its run of tokens, takes the
+// counts of the runs before it from the other CTAs' shared memory as its starting offsets, and then
+// compacts its run in order.
+constexpr int kCompactCluster = 8;
 __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ flags, const float* __restrict__ r,
                                                        int n, int32_t* __restrict__ lpos, int32_t* __restrict__ ltok,
                                                        float* __restrict__ rl, int32_t* __restrict__ lslot,
@@ -566,18 +570,62 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict
                                                        int32_t* __restrict__ hslot, int32_t* __restrict__ counts)
 {
     __shared__ int scratch[32];
-    const int h = blockIdx.x;
+    __shared__ int cnt4[4];   // this CTA's run: |L|, |H u S|, |H|, |S|
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank(), C = (int)cl.num_blocks();
+    const int h = blockIdx.y;
     const int64_t base = (int64_t)h * n;
+    // this CTA's run of tokens, in whole blocks of blockDim.x
+    const int per = (((n + C - 1) / C) + (int)blockDim.x - 1) / (int)blockDim.x * (int)blockDim.x;
+    const int j0 = min(n, rank * per), j1 = min(n, j0 + per);
+    {
+        int cL = 0, cR = 0, cH = 0, cS = 0;
+        for (int i = j0 + threadIdx.x; i < j1; i += blockDim.x) {
+            const int f = flags[base + i];
+            cL += (f == 0 || f == 1);
+            cR += (f == 1 || f == 2);
+            cH += (f == 2);
+            cS += (f == 1);
+        }
+        cL = warp_sum(cL);
+        cR = warp_sum(cR);
+        cH = warp_sum(cH);
+        cS = warp_sum(cS);
+        if (threadIdx.x < 4) cnt4[threadIdx.x] = 0;
+        __syncthreads();
+        if ((threadIdx.x & 31) == 0) {
+            atomicAdd(&cnt4[0], cL);
+            atomicAdd(&cnt4[1], cR);
+            atomicAdd(&cnt4[2], cH);
+            atomicAdd(&cnt4[3], cS);
+        }
+    }
+    cl.sync();   // every run's counts are in place
     int offL = 0, offR = 0, offH = 0, offS = 0;
-    for (int t0 = 0; t0 < n; t0 += blockDim.x) {
+    for (int q = 0; q < rank; ++q) {
+        const int* c4 = cl.map_shared_rank(cnt4, q);
+        offL += c4[0];
+        offR += c4[1];
+        offH += c4[2];
+        offS += c4[3];
+    }
+    int totL = offL, totR = offR, totH = offH, totS = offS;
+    if (rank == C - 1 && threadIdx.x == 0) {
+        totL += cnt4[0];
+        totR += cnt4[1];
+        totH += cnt4[2];
+        totS += cnt4[3];
+    }
+    cl.sync();   // every CTA has read the counts it needs (none is read after this)
+    for (int t0 = j0; t0 < j1; t0 += blockDim.x) {
         const int i = t0 + threadIdx.x;
-        const int f = i < n ? flags[base + i] : -1;
+        const int f = i < j1 ? flags[base + i] : -1;
         const int isL = (f == 0 || f == 1), isR = (f == 1 || f == 2), isH = (f == 2), isS = (f == 1);
         int tot1, tot2;
         const int ex1 = block_exclusive_scan(isL | (isR << 16), scratch, &tot1);
         const int ex2 = block_exclusive_scan(isH | (isS << 16), scratch, &tot2);
         const int pL = ex1 & 0xffff, pR = ex1 >> 16, pH = ex2 & 0xffff;
-        if (i < n) {
+        if (i < j1) {
             if (isL) {
                 ltok[base + offL + pL] = i;
                 rl[base + offL + pL] = r[base + i];
@@ -599,11 +647,11 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict
         offS += tot2 >> 16;
         __syncthreads();
     }
-    if (threadIdx.x == 0) {
-        counts[h * 4 + 0] = offH;
-        counts[h * 4 + 1] = offL;
-        counts[h * 4 + 2] = offS;
-        counts[h * 4 + 3] = offR;
+    if (rank == C - 1 && threadIdx.x == 0) {
+        counts[h * 4 + 0] = totH;
+        counts[h * 4 + 1] = totL;
+        counts[h * 4 + 2] = totS;
+        counts[h * 4 + 3] = totR;
     }
 }
 
@@ -1014,8 +1062,21 @@ verkv_status compress_slot(Ctx& ctx, Slot& s, int layer, int seq, int n, const v
     sample_kernel<<<dim3((n + 255) / 256, Hkv), 256, 0, st>>>(s.tau, s.c, n, cfg.n_sink, cfg.n_local, cfg.seed, layer,
                                                             seq, s.r, s.flags);
     VK_LAUNCHED("sample");
-    compact_kernel<<<Hkv, 1024, 0, st>>>(s.flags, s.r, n, s.lpos, s.ltok, s.rl, s.lslot, s.lq, s.rtok,
-                                          s.hslot, s.counts);
+    {
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(kCompactCluster, Hkv);
+        lc.blockDim = dim3(1024);
+        lc.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kCompactCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        VK_CUDA(cudaLaunchKernelEx(&lc, compact_kernel, (const uint8_t*)s.flags, (const float*)s.r, n, s.lpos, s.ltok,
+                                   s.rl, s.lslot, s.lq, s.rtok, s.hslot, s.counts));
+    }
     VK_LAUNCHED("compact");
 
     std::vector<int32_t> counts((size_t)Hkv * 4), capped((size_t)Hkv + 1);
