@@ -326,8 +326,12 @@ def run_verkv(args):
     # fetch statistics of the workload (one untimed job with traces)
     ctx.compress(0, 0, w.n, kv_host, kv_dev, obs, W, None, st)
     fetch_frac, no_fetch, union_rows, host_rows, kstars, pf_copied, pf_used = [], 0, [], [], [], [], []
+    tlines = {"needle": [], "random": []}   # device timeline of each call (even steps aim at needles)
+    ctx.set_timeline(True)
     for s in range(S):
+        flush()
         ctx.decode(0, [0], q_dev[s], w.eps, w.delta, out[s], st)
+        tlines["needle" if s % 2 == 0 else "random"].append(ctx.timeline(st))
         tr = ctx.decode_trace(w.n_q)
         for h in range(w.n_kv):
             u, hr = ctx.fetch_stats(0, h)
@@ -339,6 +343,10 @@ def run_verkv(args):
             fetch_frac.append(u / w.n)
         no_fetch += sum(t["no_fetch"] for t in tr)
         kstars += [t["kstar"] for t in tr]
+    ctx.set_timeline(False)
+    timeline = {kind: {k: round(statistics.median(t[k] for t in ts), 1) for k in ts[0]
+                       if all(math.isfinite(t[k]) for t in ts)}
+                for kind, ts in tlines.items() if ts}
     stats0 = ctx.compress(0, 0, w.n, kv_host, kv_dev, obs, W, None, st)
 
     # timed region: per-call events only (events between the kernels of a call would stop the
@@ -529,6 +537,9 @@ def run_verkv(args):
                          "rows_used_per_call": statistics.mean(pf_used) * w.n_kv,
                          "precision": sum(pf_used) / max(1, sum(pf_copied))},
             "link_over_decode_job": job_link,
+            "timeline_us": dict(timeline, note="median device times of the untimed statistics job's calls, us after "
+                                               "the scoring kernel started (L2 flushed before each call; the "
+                                               "decision starts once the scoring completes)"),
             "device_footprint": footprint(stats0, w, -2),
             "no_fetch_rate": no_fetch / max(1, len(kstars)),
             "mean_kstar": statistics.mean(kstars) if kstars else None,

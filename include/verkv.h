@@ -249,16 +249,15 @@ verkv_status verkv_set_stage_capacity(verkv_ctx* ctx, int64_t rows_per_kv_head);
 /*
  * Speculative prefetch (no counterpart in the algorithms: results are identical with it on or off).
  * The host link idles while the decision runs, and the rows a decode fetches are mostly the tokens of
- * L \ S with the largest sketch weights.  Beside the decision, up to rows_per_kv_head such tokens of
- * each (sequence, KV head) -- neither sampled nor staged, ranked by their largest sketch weight over
- * the head's query rows relative to each row's maximum (within 16 in log weight) -- have their K/V rows
- * copied from the pinned host cache into a per-context device buffer; the copying stops once every
- * query row of the call is decided.  It runs on calls of at most 64 query rows that leave
- * multiprocessors free beside the decision (at larger batches the decision is bound by L2 / HBM and
- * the prefetch slowed it).  The attention reads each row it needs from that buffer when the
- * buffer holds it, and over the host link otherwise.  Default 4096 (a buffer of max_batch x n_kv_heads
- * x 4096 rows, 512 B each in bf16, allocated at the next verkv_decode); 0 = off.  Takes effect at the
- * next verkv_decode.  EINVAL: rows_per_kv_head outside [0, 65536].
+ * L \ S with the largest alpha = w^ (1 - r).  Beside the decision, up to rows_per_kv_head such tokens
+ * of each (sequence, KV head) -- neither sampled nor staged, ranked by their largest alpha over the
+ * head's query rows relative to each row's largest sketch weight (within 255/16 in log) -- have their
+ * K/V rows copied from the pinned host cache into a per-context device buffer; the copying stops once
+ * every query row of the call is decided.  It runs on calls whose decision leaves at least eight
+ * multiprocessors free.  The attention reads each row it needs from that buffer when the buffer holds
+ * it, and over the host link otherwise.  Default 4096 (a buffer of max_batch x n_kv_heads x 4096
+ * rows, 512 B each in bf16, allocated at the next verkv_decode); 0 = off.  Takes effect at the next
+ * verkv_decode.  EINVAL: rows_per_kv_head outside [0, 65536].
  * verkv_get_prefetch_stats: for KV head (b, kv_head) of the last verkv_decode, n_copied = rows the
  * prefetch copied, n_used = of the rows the step needed beyond the resident and staged ones, how
  * many came from the prefetch buffer (the others crossed the host link during the attention).
@@ -266,6 +265,24 @@ verkv_status verkv_set_stage_capacity(verkv_ctx* ctx, int64_t rows_per_kv_head);
 verkv_status verkv_set_prefetch(verkv_ctx* ctx, int32_t rows_per_kv_head);
 verkv_status verkv_get_prefetch_stats(verkv_ctx* ctx, int32_t b, int32_t kv_head, int32_t* n_copied, int32_t* n_used,
                                       verkv_stream stream);
+
+/*
+ * Call timeline (tracing; no counterpart in the paper).  verkv_set_timeline(ctx, 1) makes every
+ * following verkv_decode record device times (the GPU's global timer, read by the first CTA to reach
+ * a point and by the last to leave it) at two extra small copies per call; 0 turns it off (default).
+ * verkv_get_timeline synchronises `stream` and writes VERKV_TIMELINE_N values for the last
+ * verkv_decode, in microseconds after the scoring kernel's first CTA started:
+ *   [0] decision started (its dependency on the scoring kernel resolved, so the scoring complete),
+ *   [1] decision complete (last query row decided), [2] prefetch started, [3] prefetch binning done,
+ *   [4] prefetch complete, [5] attention started (after its dependency wait), [6] attention complete
+ *   (last KV head merged).
+ * NaN where that kernel did not run in the call (the prefetch off or skipped; the multi-kernel
+ * decision of rows beyond 262144 L entries records neither [0] nor [1]).  EINVAL when the last
+ * verkv_decode recorded no timeline.
+ */
+#define VERKV_TIMELINE_N 7
+verkv_status verkv_set_timeline(verkv_ctx* ctx, int32_t on);
+verkv_status verkv_get_timeline(verkv_ctx* ctx, double* out_us, verkv_stream stream);
 
 /*
  * Shortlist (Appendix A.1): at every decode, among the tokens of L outside the sample, the k of each KV

@@ -643,6 +643,36 @@ def test_prefetch_copies_ahead_and_changes_no_result():
     assert used > 0, res[512][2]
 
 
+def test_call_timeline_orders_the_kernels_and_changes_no_result():
+    """verkv_set_timeline records, per decode call, when the decision, the prefetch and the attention
+    started and ended (device times after the scoring kernel started).  The entries follow the launch
+    order (the decision waits for the scoring, the attention for the decision and the prefetch), every
+    time lies within the call, and the outputs are bit-identical with recording on and off."""
+    from verified_kv_cache_gb300 import binding
+    w = small_case("int8", n=8000, steps=4, query_mode="needle_half")
+    outs = {}
+    for on in (False, True):
+        ctx = make_lib_ctx(w)
+        ctx.set_timeline(on)
+        gc = GpuCase(w, ctx)
+        _compress_both(w, gc)
+        outs[on] = []
+        for s in range(4):
+            outs[on].append(gc.decode(w.queries[s], 0.01, 0.05))
+            if on:
+                t = ctx.timeline()
+                assert all(np.isfinite(t[k]) for k in ("decide_start", "decide_end", "attn_start", "attn_end")), t
+                assert 0.0 <= t["decide_start"] <= t["decide_end"] <= t["attn_start"] <= t["attn_end"] < 1e6, t
+                if np.isfinite(t["prefetch_start"]):
+                    assert t["prefetch_start"] <= t["prefetch_binned"] <= t["prefetch_end"] <= t["attn_start"], t
+            else:
+                with pytest.raises(binding.VerkvError):
+                    ctx.timeline()
+        ctx.close()
+    for s in range(4):
+        assert np.array_equal(outs[False][s].view(np.uint32), outs[True][s].view(np.uint32)), s
+
+
 def _shortlist_near_tie(orow, got_tokens):
     """The device shortlist may differ from the oracle's only where the oracle's scores of the
     differing tokens lie within 1e-6 (relative) of the score at the shortlist boundary."""

@@ -116,6 +116,10 @@ def lib():
     L.verkv_set_prefetch.restype = st
     L.verkv_get_prefetch_stats.argtypes = [P, i32, i32, P, P, P]
     L.verkv_get_prefetch_stats.restype = st
+    L.verkv_set_timeline.argtypes = [P, i32]
+    L.verkv_set_timeline.restype = st
+    L.verkv_get_timeline.argtypes = [P, P, P]
+    L.verkv_get_timeline.restype = st
     L.verkv_selftest_wait_timeout.argtypes = [P, P]
     L.verkv_selftest_wait_timeout.restype = st
     L.verkv_set_append_capacity.argtypes = [P, i32]
@@ -290,6 +294,20 @@ class VerKV:
     def set_prefetch(self, rows_per_kv_head: int):
         """Rows per (sequence, KV head) the speculative prefetch may copy ahead (0 = off; default 4096)."""
         self._check(lib().verkv_set_prefetch(self.h, int(rows_per_kv_head)))
+
+    TIMELINE_KEYS = ("decide_start", "decide_end", "prefetch_start", "prefetch_binned", "prefetch_end",
+                     "attn_start", "attn_end")
+
+    def set_timeline(self, on: bool):
+        """Record the device timeline of every following decode (verkv_set_timeline)."""
+        self._check(lib().verkv_set_timeline(self.h, 1 if on else 0))
+
+    def timeline(self, stream=None):
+        """Timeline of the last decode: microseconds after its scoring kernel started, per TIMELINE_KEYS
+        (NaN where that kernel did not run)."""
+        v = (ctypes.c_double * len(self.TIMELINE_KEYS))()
+        self._check(lib().verkv_get_timeline(self.h, v, _stream(stream)))
+        return dict(zip(self.TIMELINE_KEYS, list(v)))
 
     def prefetch_stats(self, b, kv, stream=None):
         """(rows the prefetch copied, rows the attention read from them) for KV head (b, kv), last decode."""

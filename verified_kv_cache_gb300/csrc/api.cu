@@ -33,7 +33,7 @@ void free_ws(Ctx& c)
 {
     void* ptrs[] = {c.tl, c.th, c.wl, c.rows, c.keys, c.mark, c.elist, c.ebits, c.om, c.ulist, c.umask, c.adone, c.ucount,
                     c.part, c.hrows, c.slist, c.scount, c.shist,
-                    c.d_slot_n, c.pf_buf, c.pf_of, c.pf_tok, c.pf_cnt, c.pf_used, c.dprog, c.tau_ws};
+                    c.d_slot_n, c.pf_buf, c.pf_of, c.pf_tok, c.pf_cnt, c.pf_used, c.dprog, c.tau_ws, c.tline};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     if (c.h_err) cudaFreeHost(c.h_err);
@@ -438,6 +438,36 @@ verkv_status verkv_set_prefetch(verkv_ctx* h, int32_t rows_per_kv_head)
     if (rows_per_kv_head < 0 || rows_per_kv_head > 65536)
         return fail(ctx, VERKV_EINVAL, "prefetch rows per KV head must be in [0, 65536]");
     ctx.prefetch_rows = rows_per_kv_head;
+    return VERKV_OK;
+}
+
+verkv_status verkv_set_timeline(verkv_ctx* h, int32_t on)
+{
+    if (!h) return VERKV_EINVAL;
+    h->c.timeline = on ? 1 : 0;
+    return VERKV_OK;
+}
+
+verkv_status verkv_get_timeline(verkv_ctx* h, double* out_us, verkv_stream stream)
+{
+    if (!h || !out_us) return VERKV_EINVAL;
+    Ctx& ctx = h->c;
+    for (int k = 0; k < VERKV_TIMELINE_N; ++k) out_us[k] = NAN;
+    if (!ctx.last_tline || !ctx.tline) return fail(ctx, VERKV_EINVAL, "the last decode recorded no timeline");
+    cudaStream_t st = (cudaStream_t)stream;
+    unsigned long long t[16];
+    VK_CUDA(cudaMemcpyAsync(t, ctx.tline, sizeof(t), cudaMemcpyDeviceToHost, st));
+    VK_CUDA(cudaStreamSynchronize(st));
+    const unsigned long long t0 = t[0];
+    if (t0 == ~0ull) return fail(ctx, VERKV_EINVAL, "the last decode recorded no timeline");
+    // starts (min slots 1..3, unset = ~0) and ends (max slots 8..11, unset = 0), in microseconds after
+    // the scoring kernel's first CTA started
+    const int slot[VERKV_TIMELINE_N] = {1, 8, 2, 9, 10, 3, 11};
+    for (int k = 0; k < VERKV_TIMELINE_N; ++k) {
+        const unsigned long long v = t[slot[k]];
+        const bool unset = slot[k] < 8 ? v == ~0ull : v == 0ull;
+        out_us[k] = unset ? NAN : (double)(long long)(v - t0) * 1e-3;
+    }
     return VERKV_OK;
 }
 

@@ -42,6 +42,10 @@ struct DecodeArgs {
     int32_t* pf_cnt;
     int32_t* pf_used;
     unsigned long long* dprog;
+    // call timeline (null: off): device times of the first CTA start ([0] scoring, [1] decision after
+    // its dependency wait, [2] prefetch, [3] attention after its wait) and of the last CTA end ([8]
+    // decision, [9] prefetch binning, [10] prefetch, [11] attention), in globaltimer nanoseconds
+    unsigned long long* tline;
     int pf_cap;       // rows per (sequence, KV head); 0: the prefetch is off for this call
     int Hkv, Hq, G, ws_n, ws_npow2, gen, nsplit;
     int binary;       // 1: binary shrinkage coefficients (lambda in {1, r}), 0: the clipped fixed point
@@ -53,6 +57,16 @@ struct DecodeArgs {
 };
 
 __device__ __forceinline__ int row_of(int b, int hq, int Hq) { return b * Hq + hq; }
+
+// Call timeline entry k: the earliest (first) or the latest (!first) time any CTA reached it.
+__device__ __forceinline__ void tline_stamp(unsigned long long* t, int k, bool first)
+{
+    if (t) {
+        const unsigned long long v = global_ns();
+        if (first) atomicMin(t + k, v);
+        else atomicMax(t + k, v);
+    }
+}
 
 // K/V row elements (bf16 or fp32) to fp32: eight channels from 16 (or 32) bytes, or a pair.
 template <typename T> struct RowCvt;
@@ -218,6 +232,7 @@ __global__ void __launch_bounds__(kTile) score_2bit_kernel(Views views, const fl
                                                            float2* __restrict__ th, int n_ltiles)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
+    if (threadIdx.x == 0) tline_stamp(a.tline, 0, true);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
         a.pf_cnt[blockIdx.y] = 0;   // rows the prefetch claims, and of them the attention reads
@@ -519,6 +534,7 @@ __global__ void __launch_bounds__(kTile, kInt8CtasPerSm) score_int8_kernel(Views
                                                                             float2* __restrict__ th, int n_lchunks)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
+    if (threadIdx.x == 0) tline_stamp(a.tline, 0, true);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
         a.pf_cnt[blockIdx.y] = 0;   // rows the prefetch claims, and of them the attention reads
@@ -972,6 +988,7 @@ __global__ void __launch_bounds__(kTile) score_exact_kernel(Views views, const f
                                                             float2* __restrict__ th, int n_ltiles)
 {
     pdl_trigger();   // the decision kernel may start its independent prologue
+    if (threadIdx.x == 0) tline_stamp(a.tline, 0, true);
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         a.hrows[blockIdx.y] = 0;   // host rows of this call (attention)
         a.pf_cnt[blockIdx.y] = 0;   // rows the prefetch claims, and of them the attention reads
@@ -1972,6 +1989,7 @@ decide_kernel(Views views, DecodeArgs a,
 {
     pdl_wait();      // the scoring kernel has completed (its logits, maxima and weight factors are visible)
     pdl_trigger();   // the next kernel (prefetch or attention) may start: the scoring kernel's results are complete
+    if (threadIdx.x == 0) tline_stamp(a.tline, 1, true);
     cg::cluster_group cl = cg::this_cluster();
     const int C = (int)cl.num_blocks();
     const int rank = (int)cl.block_rank();
@@ -3052,7 +3070,10 @@ decide_kernel(Views views, DecodeArgs a,
     stamp(5);
 
     cl.sync();   // no CTA leaves while its shared memory may still be read
-    if (rank == 0 && tid == 0) atomicAdd(a.dprog, 1ull);   // this row is decided (read by the prefetch)
+    if (rank == 0 && tid == 0) {
+        atomicAdd(a.dprog, 1ull);
+        tline_stamp(a.tline, 8, false);
+    }   // this row is decided (read by the prefetch)
 }
 
 // --------------------------------------------------------------------------------------------
@@ -3130,6 +3151,7 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
     __shared__ int s_n, s_thr, s_base, s_stop;
     extern __shared__ unsigned char sbin[];         // the share's bins (when it fits kPfShareCap)
     pdl_trigger();   // the attention may launch and wait at its own dependency point
+    if (threadIdx.x == 0) tline_stamp(a.tline, 2, true);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int unit = blockIdx.x, b = unit / a.Hkv, kv = unit % a.Hkv;
     const SlotView& V = views.v[b];
@@ -3196,7 +3218,9 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
         }
     }
     __syncthreads();
+    if (tid == 0) tline_stamp(a.tline, 9, false);
     if (s_stop) {
+        if (tid == 0) tline_stamp(a.tline, 10, false);
         pdl_wait();
         return;
     }
@@ -3342,6 +3366,7 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
             }
         }
     }
+    if (tid == 0) tline_stamp(a.tline, 10, false);
     pdl_wait();   // the decision has completed: the attention, launched after this grid, may read its results
 }
 
@@ -3412,6 +3437,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
 
     int nu = 0;
     pdl_wait();   // the decision kernel's bitmaps and weight factors are complete (the query is an input)
+    if (tid == 0) tline_stamp(a.tline, 3, true);
     // the bitmaps are scanned only when a query row of the KV head fetches.  The counts come from the
     // decision kernel, which may still have been running when this grid started (programmatic launch):
     // they are read through L2, never through the non-coherent read-only path.
@@ -3813,7 +3839,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(Views views, cons
         for (; sp < ny; ++sp) A0 = fmaf(pr[sp * (kHeadDim + 2) + c], s_scl[g][sp], A0);
         out[(int64_t)(row0 + g) * kHeadDim + c] = ((A0 + A1) + (A2 + A3)) / s_L[g];
     }
-    if (tid == 0) done[unit] = 0;
+    if (tid == 0) {
+        done[unit] = 0;
+        tline_stamp(a.tline, 11, false);
+    }
 }
 
 int g_decide_max_cluster = 8;  // largest cluster the decide kernel is launched with (set once)
@@ -4110,6 +4139,14 @@ verkv_status decode_rows(Ctx& ctx, int layer, const int32_t* seq_ids, int B, con
     a.pf_cnt = ctx.pf_cnt;
     a.pf_used = ctx.pf_used;
     a.dprog = ctx.dprog;
+    a.tline = nullptr;
+    if (ctx.timeline) {
+        if (!ctx.tline) VK_CUDA(cudaMalloc(&ctx.tline, sizeof(unsigned long long) * 16));
+        VK_CUDA(cudaMemsetAsync(ctx.tline, 0xff, sizeof(unsigned long long) * 8, st));
+        VK_CUDA(cudaMemsetAsync(ctx.tline + 8, 0, sizeof(unsigned long long) * 8, st));
+        a.tline = ctx.tline;
+    }
+    ctx.last_tline = ctx.timeline;
     // attention splits per KV head: about two blocks per SM over the whole call
     a.nsplit = std::min(std::min(ctx.nsplit, kMaxSplit), std::max(1, (2 * ctx.num_sms + B * cfg.n_kv_heads - 1) / (B * cfg.n_kv_heads)));
     a.eps = eps;

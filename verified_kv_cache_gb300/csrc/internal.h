@@ -141,6 +141,9 @@ struct Ctx {
     // the attention reads the ones it needs from there
     int prefetch_rows = 4096;       // rows per (sequence, KV head) a decode may copy ahead (0: off)
     int pf_cap = 0;                 // rows per (sequence, KV head) the buffers below hold
+    unsigned long long* tline = nullptr;   // decode call timeline (16 device times), when enabled
+    int timeline = 0;               // verkv_set_timeline
+    int last_tline = 0;             // the last decode recorded one
     void* tau_ws = nullptr;         // compress: importance-score scratch (partials, row stats, raw scores)
     size_t tau_ws_cap = 0;
     void* pf_buf = nullptr;         // [max_batch][Hkv][pf_cap][2][d] rows copied ahead
