@@ -3376,7 +3376,7 @@ __global__ void __launch_bounds__(kPfThreads) prefetch_kernel(Views views, Decod
 // factor is the one the scoring and decision kernels wrote for each resident slot (1 on H and on
 // L_g[:k*], lambda_i / r_i on S \ L_g[:k*]) and, on a fetched row, 1 if the head's exact set holds
 // it, else 0.  Each block takes every gridDim.y-th chunk of 32 KB of rows (64 bf16 rows) of one KV
-// head into a three-stage shared-memory ring: a chunk of resident rows by one bulk asynchronous copy
+// head into a two-stage shared-memory ring: a chunk of resident rows by one bulk asynchronous copy
 // completed on an mbarrier, a chunk holding fetched rows by 16-byte cp.async copies whose sources
 // for the fetched rows are the pinned host cache itself, so the host-link transfer overlaps the
 // compute of the previous chunks and the rows never round-trip through HBM.  Per chunk: q.k for
