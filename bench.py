@@ -508,7 +508,8 @@ def run_verkv(args):
             secondary["long_context_128k_int8"] = long_context_run(args, dev, st, hbm_peak, peak_src, link_peak)
             torch.cuda.empty_cache()
         if only in (None, "sweep"):
-            secondary["sweep"] = sweep_run(args, dev, st, hbm_peak, peak_src, link_peak)
+            secondary["sweep"] = sweep_run(args, dev, st, hbm_peak, peak_src, link_peak,
+                                           clk.get("sm_mhz") if clk else None)
             torch.cuda.empty_cache()
 
     cpu = None
@@ -955,13 +956,14 @@ def long_context_run(args, dev, st, hbm_peak, peak_src, link_peak):
     return res
 
 
-def sweep_run(args, dev, st, hbm_peak, peak_src, link_peak):
+def sweep_run(args, dev, st, hbm_peak, peak_src, link_peak, sm_mhz=None):
     """The sweep over 8 KV heads, d = 128, bf16: verkv_compress at n in {32K, 64K, 128K, 256K} (the
     whole compress: importance scores from 32 observation queries per query head, water-filling,
     Philox sample, compaction, int8 sketch; and with caller-supplied scores), and verkv_decode at
     n = 32K over eta in {1/8, 1/16, 1/32} x eps in {0.02, 0.05, 0.1}, delta = 0.05, batch in
     {1, 8, 32}, int8 sketch, the Qwen3-4B-shaped query mix (half aimed at needles): per point the
-    decode time, scored tokens/s, fetch fraction and the score / attention rooflines."""
+    decode time, scored tokens/s, fetch fraction and the score / attention rooflines; and one batch-8
+    point (eta = 1/16, eps = 0.05) with the paper's 2-bit sketch."""
     import torch
 
     from verified_kv_cache_gb300 import binding
@@ -969,7 +971,7 @@ def sweep_run(args, dev, st, hbm_peak, peak_src, link_peak):
 
     def flush():
         flush_buf.fill_(1.0)
-    res = {"compress": [], "decode": []}
+    res = {"compress": [], "decode": [], "decode_2bit": []}
     ns = [32768, 65536] if args.quick else [32768, 65536, 131072, 262144]
     for n in ns:
         kv, obs, _ = gpu_layer_inputs(700 + n // 1024, 1, n, dev, n_needles=16, W=32, steps=1)
@@ -991,49 +993,65 @@ def sweep_run(args, dev, st, hbm_peak, peak_src, link_peak):
     etas = [1 / 16] if args.quick else [1 / 8, 1 / 16, 1 / 32]
     epss = [0.05] if args.quick else [0.02, 0.05, 0.1]
     steps = 8
+
+    def point(ctx, B, eta, eps, sketch, q, ids, out, stats):
+        """One decode point: event-timed calls, then per-kernel times, fetch statistics, rooflines."""
+        for s in range(2):
+            ctx.decode(0, ids, q[s], eps, 0.05, out, st)
+        ms = timed_calls([lambda s=s: ctx.decode(0, ids, q[s], eps, 0.05, out, st) for s in range(steps)], flush, st)
+        ctx.set_kernel_timing(True)
+        fetch, host, kt = [], [], []
+        for s in range(steps):
+            flush()
+            ctx.decode(0, ids, q[s], eps, 0.05, out, st)
+            kt += ctx.kernel_times(st)
+            for b in range(B):
+                for hh in range(8):
+                    u, hr = ctx.fetch_stats(b, hh)
+                    fetch.append(u / n)
+                    host.append(hr)
+        ctx.set_kernel_timing(False)
+        agg = kernel_agg(kt)
+        traces = {"union_rows": statistics.mean(fetch) * n * B * 8, "host_rows": statistics.mean(host) * B * 8}
+        pt = {"batch": B, "eta": f"1/{round(1 / eta)}", "eps": eps, "delta": 0.05, "sketch": sketch,
+              "decode_us_per_call": statistics.mean(ms) * 1e3,
+              "scored_tokens_per_s": B * 32 * n / (statistics.mean(ms) / 1e3),
+              "fetch_fraction_per_token": statistics.mean(fetch),
+              "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()}}
+        rl = layer_rooflines(agg, stats, _W(n, eta, sketch), traces, hbm_peak, peak_src, link_peak, B)
+        pt.update({k: round(v["frac"], 4) for k, v in rl.items()})
+        # the 2-bit scan is bound by instruction issue: the committed ncu count of the batch-1 launch of
+        # the bench layer, times the batch (the same work per KV head), over the launch's time, against
+        # SMs x 4 issue slots x the SM clock sampled during the headline's timed region
+        inst1 = measured_counters(_W(n, 1 / 16, "2bit")).get("warp_instructions_per_launch", {}).get("score")
+        if sketch == "2bit" and inst1 and sm_mhz and "score" in agg:
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            avg_s = agg["score"][0] / agg["score"][1] / 1e3
+            pt["roofline_score_issue"] = round(inst1 * B / avg_s / (sms * 4 * sm_mhz * 1e6), 4)
+        return pt
+
     for B in batches:
         kv, obs, q = gpu_layer_inputs(800 + B, B, n, dev, n_needles=16, W=32, steps=steps)
         hosts = [pinned_copy(kv[b]) for b in range(B)]
         out = torch.empty((B, 32, 128), device=dev)
         ids = list(range(B))
-        for eta in etas:
-            ctx = binding.VerKV(n_kv_heads=8, n_q_heads=32, max_tokens=n, n_layers=1, n_seqs=B, max_batch=B,
-                                n_sink=4, n_local=128, eta=eta, seed=0, sketch="int8", kv_dtype="bf16")
-            stats = []
-            for b in range(B):
-                stats += ctx.compress(0, b, n, hosts[b], kv[b], obs[b], 32, None, st)
-            for eps in epss:
-                for s in range(2):
-                    ctx.decode(0, ids, q[s], eps, 0.05, out, st)
-                ms = timed_calls([lambda s=s: ctx.decode(0, ids, q[s], eps, 0.05, out, st) for s in range(steps)],
-                                 flush, st)
-                ctx.set_kernel_timing(True)
-                fetch, host, kt = [], [], []
-                for s in range(steps):
-                    flush()
-                    ctx.decode(0, ids, q[s], eps, 0.05, out, st)
-                    kt += ctx.kernel_times(st)
-                    for b in range(B):
-                        for hh in range(8):
-                            u, hr = ctx.fetch_stats(b, hh)
-                            fetch.append(u / n)
-                            host.append(hr)
-                ctx.set_kernel_timing(False)
-                agg = kernel_agg(kt)
-                traces = {"union_rows": statistics.mean(fetch) * n * B * 8, "host_rows": statistics.mean(host) * B * 8}
-                pt = {"batch": B, "eta": f"1/{round(1 / eta)}", "eps": eps, "delta": 0.05,
-                      "decode_us_per_call": statistics.mean(ms) * 1e3,
-                      "scored_tokens_per_s": B * 32 * n / (statistics.mean(ms) / 1e3),
-                      "fetch_fraction_per_token": statistics.mean(fetch),
-                      "kernel_avg_us": {k: round(v[0] / v[1] * 1e3, 2) for k, v in agg.items()}}
-                rl = layer_rooflines(agg, stats, _W(n, eta, "int8"), traces, hbm_peak, peak_src, link_peak, B)
-                pt.update({k: round(v["frac"], 4) for k, v in rl.items()})
-                res["decode"].append(pt)
-            ctx.close()
+        sketches = ["int8", "2bit"] if B == 8 else ["int8"]
+        for sketch in sketches:
+            for eta in (etas if sketch == "int8" else [1 / 16]):
+                ctx = binding.VerKV(n_kv_heads=8, n_q_heads=32, max_tokens=n, n_layers=1, n_seqs=B, max_batch=B,
+                                    n_sink=4, n_local=128, eta=eta, seed=0, sketch=sketch, kv_dtype="bf16")
+                stats = []
+                for b in range(B):
+                    stats += ctx.compress(0, b, n, hosts[b], kv[b], obs[b], 32, None, st)
+                for eps in (epss if sketch == "int8" else [0.05]):
+                    pt = point(ctx, B, eta, eps, sketch, q, ids, out, stats)
+                    res["decode" if sketch == "int8" else "decode_2bit"].append(pt)
+                ctx.close()
         del kv, obs, q, hosts
         torch.cuda.empty_cache()
     res["note"] = ("roofline_* per point are fractions: score and attn of the measured HBM copy peak, attn_link of "
-                   "the measured host-link peak; int8 sketch throughout (the configs' sketch)")
+                   "the measured host-link peak; int8 sketch (the configs' sketch) in `decode`, one batch-8 point "
+                   "with the paper's 2-bit sketch in `decode_2bit`")
     return res
 
 
