@@ -137,7 +137,7 @@ struct Ctx {
                                     // (zero between calls)
     int64_t stage_rows = VERKV_STAGE_ETA_N;   // staging capacity per KV head and slot (verkv_set_stage_capacity)
     // speculative prefetch (verkv_set_prefetch): while the decision runs, rows of L \ S with the
-    // largest sketch weights are copied from pinned host memory into a per-call device buffer, and
+    // largest alpha = w^ (1 - r) are copied from pinned host memory into a per-call device buffer, and
     // the attention reads the ones it needs from there
     int prefetch_rows = 4096;       // rows per (sequence, KV head) a decode may copy ahead (0: off)
     int pf_cap = 0;                 // rows per (sequence, KV head) the buffers below hold
